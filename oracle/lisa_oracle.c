@@ -1,0 +1,428 @@
+/*
+ * lisa_oracle.c -- plain double-precision CPU oracle of the LiSA forward layer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file: only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg use it.  It shares no code, header, table or helper with
+ * the CUDA library; it is written straight from the method's definition.
+ *
+ * Source: "LiSA: Linear Stochastic Attention for Long-Range Visual Modeling"
+ * (reading note of arXiv 2611.04216v2, cc.laoqi.cc), cited below as [note].
+ *   [note §2.1]  token set, projections, ReLU feature map (paper Table 8)
+ *   [note §2.2]  row-stochastic transition S = Q~ K^T, geometric truncated
+ *                walk weights (paper Sec. 3.2, Eq. 4)
+ *   [note §2.3]  low-rank evaluation S^k V = Q~ (K^T Q~)^(k-1) K^T V
+ *                (paper Eq. 8, Algorithm 1)
+ *   [note §2.4]  adaptive per-token, per-head step weights from a 2-layer
+ *                MLP + softmax (paper Eq. 10, Supp. Sec. 8); the 3x3 local
+ *                branch and the alpha mix (paper Sec. 3.2, Fig. 2)
+ *
+ * The display equations were lost when the note was extracted, so a few
+ * details are readings, stated where they are used:
+ *   - Q~_i = Q_i / (Q_i . sum_j K_j + eps), the sum running over every token.
+ *   - walk index k = 0..T-1 with k = 0 the identity (T = 1 keeps only S^0 = I).
+ *   - MLP input is concat(q_i, k_i) of the feature-mapped (post-ReLU) query
+ *     and key; hidden layer has a bias and the exact erf GELU; the output
+ *     layer has a bias; softmax over the T logits with the max subtracted.
+ *   - local branch: scores q_i . k_j / sqrt(d_h) over the token itself and its
+ *     in-grid 8-neighbours (neighbours outside the grid are left out, not
+ *     zero-padded), softmax over those, applied to V.
+ *   - alpha is used as given, one value per head.
+ *
+ * Two evaluation modes give the same global branch by different routes:
+ *   EXPLICIT: rows of S are formed one at a time and Y_k = S Y_(k-1) is
+ *             iterated over n x n products (O(T n^2 d)); S is never stored.
+ *   LOWRANK:  s, M = K^T Q~, U_1 = K^T V, U_k = M U_(k-1), Y_k = Q~ U_k.
+ *
+ * Every array is row-major, double precision, contiguous:
+ *   Q, K  [B][heads][n][d_h]      V, O, G, L  [B][heads][n][d_v]
+ * with n = H*W and token index i = r*W + c on the H x W grid.
+ */
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_EXPLICIT 0
+#define ORACLE_LOWRANK 1
+
+#define ORACLE_W_GEOMETRIC 0
+#define ORACLE_W_FIXED 1
+#define ORACLE_W_MLP 2
+
+/* ---------------------------------------------------------------------- */
+/* Walk weights, [note §2.2] (paper Eq. 4): a walk continues with          */
+/* probability beta; the weight of length k is (1-beta) beta^k, and the     */
+/* first T weights are renormalised by their sum 1 - beta^T.                */
+/* ---------------------------------------------------------------------- */
+int lisa_oracle_geometric_weights(double beta, int T, double *w)
+{
+    if (T < 1 || !(beta >= 0.0) || !(beta < 1.0)) return 1;
+    double norm = 1.0 - pow(beta, (double)T);
+    for (int k = 0; k < T; ++k)
+        w[k] = (1.0 - beta) * pow(beta, (double)k) / norm;
+    return 0;
+}
+
+/* Feature map [note §2.1]: Q = ReLU(Xq), K = ReLU(Xk), or a plain copy when
+ * the caller has already applied it. */
+static void feature_map(const double *X, double *out, long count, int relu)
+{
+    for (long t = 0; t < count; ++t) {
+        double x = X[t];
+        out[t] = (relu && x < 0.0) ? 0.0 : x;
+    }
+}
+
+/* s = sum over every token j of K_j  [note §2.2]. */
+static void key_sum(const double *K, int n, int dh, double *s)
+{
+    for (int a = 0; a < dh; ++a) s[a] = 0.0;
+    for (int j = 0; j < n; ++j)
+        for (int a = 0; a < dh; ++a) s[a] += K[(long)j * dh + a];
+}
+
+/* Q~_i = Q_i / (Q_i . s + eps)  [note §2.2]. */
+static void normalised_queries(const double *Q, const double *s, int n, int dh,
+                               double eps, double *Qt)
+{
+    for (int i = 0; i < n; ++i) {
+        const double *q = Q + (long)i * dh;
+        double den = eps;
+        for (int a = 0; a < dh; ++a) den += q[a] * s[a];
+        for (int a = 0; a < dh; ++a) Qt[(long)i * dh + a] = q[a] / den;
+    }
+}
+
+/* ---------------------------------------------------------------------- */
+/* Global branch, EXPLICIT mode: Y_0 = V, Y_k = S Y_(k-1) with             */
+/* S_ij = Q~_i . K_j formed on the fly.  Writes Y_0..Y_(T-1) into          */
+/* Y[T][n][dv].                                                             */
+/* ---------------------------------------------------------------------- */
+static void walk_terms_explicit(const double *Qt, const double *K,
+                                const double *V, int n, int dh, int dv, int T,
+                                double *Y, double *Srow)
+{
+    memcpy(Y, V, sizeof(double) * (size_t)n * dv);
+    for (int k = 1; k < T; ++k) {
+        const double *prev = Y + (size_t)(k - 1) * n * dv;
+        double *cur = Y + (size_t)k * n * dv;
+        for (int i = 0; i < n; ++i) {
+            for (int j = 0; j < n; ++j) {
+                double sij = 0.0;
+                for (int a = 0; a < dh; ++a)
+                    sij += Qt[(long)i * dh + a] * K[(long)j * dh + a];
+                Srow[j] = sij;
+            }
+            for (int e = 0; e < dv; ++e) {
+                double acc = 0.0;
+                for (int j = 0; j < n; ++j) acc += Srow[j] * prev[(long)j * dv + e];
+                cur[(long)i * dv + e] = acc;
+            }
+        }
+    }
+}
+
+/* ---------------------------------------------------------------------- */
+/* Global branch, LOWRANK mode [note §2.3] (paper Eq. 8, Algorithm 1):      */
+/* for k >= 1, S^k V = Q~ (K^T Q~)^(k-1) (K^T V).                           */
+/*   M   = K^T Q~            (dh x dh)                                      */
+/*   U_1 = K^T V             (dh x dv)                                      */
+/*   U_k = M U_(k-1)                                                        */
+/*   Y_k = Q~ U_k            (n x dv),  Y_0 = V                             */
+/* ---------------------------------------------------------------------- */
+static void walk_terms_lowrank(const double *Qt, const double *K,
+                               const double *V, int n, int dh, int dv, int T,
+                               double *Y, double *M, double *U, double *Unext)
+{
+    memcpy(Y, V, sizeof(double) * (size_t)n * dv);
+    if (T < 2) return;
+    for (int a = 0; a < dh; ++a)
+        for (int b = 0; b < dh; ++b) {
+            double acc = 0.0;
+            for (int j = 0; j < n; ++j) acc += K[(long)j * dh + a] * Qt[(long)j * dh + b];
+            M[a * dh + b] = acc;
+        }
+    for (int a = 0; a < dh; ++a)
+        for (int e = 0; e < dv; ++e) {
+            double acc = 0.0;
+            for (int j = 0; j < n; ++j) acc += K[(long)j * dh + a] * V[(long)j * dv + e];
+            U[a * dv + e] = acc;
+        }
+    for (int k = 1; k < T; ++k) {
+        if (k > 1) {
+            for (int a = 0; a < dh; ++a)
+                for (int e = 0; e < dv; ++e) {
+                    double acc = 0.0;
+                    for (int b = 0; b < dh; ++b) acc += M[a * dh + b] * U[b * dv + e];
+                    Unext[a * dv + e] = acc;
+                }
+            memcpy(U, Unext, sizeof(double) * (size_t)dh * dv);
+        }
+        double *cur = Y + (size_t)k * n * dv;
+        for (int i = 0; i < n; ++i)
+            for (int e = 0; e < dv; ++e) {
+                double acc = 0.0;
+                for (int a = 0; a < dh; ++a) acc += Qt[(long)i * dh + a] * U[a * dv + e];
+                cur[(long)i * dv + e] = acc;
+            }
+    }
+}
+
+/* ---------------------------------------------------------------------- */
+/* Adaptive step weights [note §2.4] (paper Eq. 10, Supp. Sec. 8):          */
+/* x = concat(q_i, k_i);  h = GELU(W1 x + b1);  z = W2 h + b2;              */
+/* w(i) = softmax(z) over the T walk lengths.  W1 is [hidden][2*dh] and     */
+/* W2 is [T][hidden] (output-major, like a torch Linear weight).           */
+/* ---------------------------------------------------------------------- */
+static double gelu_erf(double x) { return 0.5 * x * (1.0 + erf(x / sqrt(2.0))); }
+
+static void mlp_step_weights(const double *q, const double *k, int dh, int T,
+                             const double *W1, const double *b1,
+                             const double *W2, const double *b2, int hidden,
+                             double *h, double *w)
+{
+    for (int m = 0; m < hidden; ++m) {
+        const double *row = W1 + (long)m * 2 * dh;
+        double acc = b1[m];
+        for (int a = 0; a < dh; ++a) acc += row[a] * q[a];
+        for (int a = 0; a < dh; ++a) acc += row[dh + a] * k[a];
+        h[m] = gelu_erf(acc);
+    }
+    double zmax = -INFINITY;
+    for (int t = 0; t < T; ++t) {
+        double acc = b2[t];
+        for (int m = 0; m < hidden; ++m) acc += W2[(long)t * hidden + m] * h[m];
+        w[t] = acc;
+        if (acc > zmax) zmax = acc;
+    }
+    double sum = 0.0;
+    for (int t = 0; t < T; ++t) {
+        w[t] = exp(w[t] - zmax);
+        sum += w[t];
+    }
+    for (int t = 0; t < T; ++t) w[t] /= sum;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Local 3x3 branch [note §2.4] (paper Sec. 3.2): for token i at (r, c) the  */
+/* window is every in-grid (r+dr, c+dc), dr, dc in {-1, 0, 1}: the token     */
+/* itself plus at most 8 neighbours.  e_ij = q_i . k_j / sqrt(dh); the       */
+/* weights are exp(e_ij - max_j e_ij) normalised over the window.           */
+/* ---------------------------------------------------------------------- */
+static void local_branch(const double *Qf, const double *Kf, const double *V,
+                         int H, int W, int dh, int dv, double *L)
+{
+    const double scale = 1.0 / sqrt((double)dh);
+    for (int r = 0; r < H; ++r)
+        for (int c = 0; c < W; ++c) {
+            int i = r * W + c;
+            int nb[9], cnt = 0;
+            double e[9];
+            for (int dr = -1; dr <= 1; ++dr)
+                for (int dc = -1; dc <= 1; ++dc) {
+                    int rr = r + dr, cc = c + dc;
+                    if (rr < 0 || rr >= H || cc < 0 || cc >= W) continue;
+                    nb[cnt++] = rr * W + cc;
+                }
+            double emax = -INFINITY;
+            for (int t = 0; t < cnt; ++t) {
+                double acc = 0.0;
+                for (int a = 0; a < dh; ++a)
+                    acc += Qf[(long)i * dh + a] * Kf[(long)nb[t] * dh + a];
+                e[t] = acc * scale;
+                if (e[t] > emax) emax = e[t];
+            }
+            double den = 0.0;
+            for (int t = 0; t < cnt; ++t) {
+                e[t] = exp(e[t] - emax);
+                den += e[t];
+            }
+            for (int x = 0; x < dv; ++x) {
+                double acc = 0.0;
+                for (int t = 0; t < cnt; ++t) acc += e[t] * V[(long)nb[t] * dv + x];
+                L[(long)i * dv + x] = acc / den;
+            }
+        }
+}
+
+/* ---------------------------------------------------------------------- */
+/* One (batch, head) slice: feature map, global walk, weights, local branch, */
+/* alpha mix  o = alpha * g + (1 - alpha) * l  [note §2.4] (paper Fig. 2).   */
+/* ---------------------------------------------------------------------- */
+typedef struct {
+    int H, W, dh, dv, T, wmode, hidden, mode, relu;
+    double eps;
+    const double *w, *W1, *b1, *W2, *b2;
+} slice_args;
+
+static int forward_slice(const slice_args *A, const double *Xq, const double *Xk,
+                         const double *V, double alpha, double *O, double *G,
+                         double *L)
+{
+    const int n = A->H * A->W, dh = A->dh, dv = A->dv, T = A->T;
+    double *Qf = malloc(sizeof(double) * (size_t)n * dh);
+    double *Kf = malloc(sizeof(double) * (size_t)n * dh);
+    double *Qt = malloc(sizeof(double) * (size_t)n * dh);
+    double *Y = malloc(sizeof(double) * (size_t)T * n * dv);
+    double *g = malloc(sizeof(double) * (size_t)n * dv);
+    double *l = malloc(sizeof(double) * (size_t)n * dv);
+    double *Srow = malloc(sizeof(double) * (size_t)n);
+    double *M = malloc(sizeof(double) * (size_t)dh * dh);
+    double *U = malloc(sizeof(double) * (size_t)dh * dv);
+    double *Un = malloc(sizeof(double) * (size_t)dh * dv);
+    double *wk = malloc(sizeof(double) * (size_t)T);
+    double *h = malloc(sizeof(double) * (size_t)(A->hidden > 0 ? A->hidden : 1));
+    double s[256];
+    int err = 0;
+    if (!Qf || !Kf || !Qt || !Y || !g || !l || !Srow || !M || !U || !Un || !wk || !h) {
+        err = 2;
+        goto done;
+    }
+    feature_map(Xq, Qf, (long)n * dh, A->relu);
+    feature_map(Xk, Kf, (long)n * dh, A->relu);
+    key_sum(Kf, n, dh, s);
+    normalised_queries(Qf, s, n, dh, A->eps, Qt);
+    if (A->mode == ORACLE_EXPLICIT)
+        walk_terms_explicit(Qt, Kf, V, n, dh, dv, T, Y, Srow);
+    else
+        walk_terms_lowrank(Qt, Kf, V, n, dh, dv, T, Y, M, U, Un);
+
+    for (int i = 0; i < n; ++i) {
+        if (A->wmode == ORACLE_W_MLP)
+            mlp_step_weights(Qf + (long)i * dh, Kf + (long)i * dh, dh, T, A->W1,
+                             A->b1, A->W2, A->b2, A->hidden, h, wk);
+        else
+            for (int k = 0; k < T; ++k) wk[k] = A->w[k];
+        for (int x = 0; x < dv; ++x) {
+            double acc = 0.0;
+            for (int k = 0; k < T; ++k) acc += wk[k] * Y[(size_t)k * n * dv + (long)i * dv + x];
+            g[(long)i * dv + x] = acc;
+        }
+    }
+    local_branch(Qf, Kf, V, A->H, A->W, dh, dv, l);
+    for (long t = 0; t < (long)n * dv; ++t) {
+        if (O) O[t] = alpha * g[t] + (1.0 - alpha) * l[t];
+        if (G) G[t] = g[t];
+        if (L) L[t] = l[t];
+    }
+done:
+    free(Qf); free(Kf); free(Qt); free(Y); free(g); free(l); free(Srow);
+    free(M); free(U); free(Un); free(wk); free(h);
+    return err;
+}
+
+/*
+ * Full layer over B x heads independent slices.
+ *   wmode   0 geometric (beta), 1 fixed (w[T]), 2 MLP (W1,b1,W2,b2,hidden)
+ *   alpha   [heads]
+ *   mode    0 EXPLICIT, 1 LOWRANK
+ *   O, G, L may each be NULL; G and L receive the global and local branches.
+ *   nthreads <= 0 uses the OpenMP default.
+ * Returns 0 on success, 1 on a bad argument, 2 on allocation failure.
+ */
+int lisa_oracle_forward(const double *Xq, const double *Xk, const double *V,
+                        double *O, double *G, double *L, int B, int heads,
+                        int H, int W, int dh, int dv, int T, int wmode,
+                        double beta, const double *w, const double *W1,
+                        const double *b1, const double *W2, const double *b2,
+                        int hidden, const double *alpha, double eps,
+                        int relu_inputs, int mode, int nthreads)
+{
+    if (B < 0 || heads < 0 || H < 1 || W < 1 || dh < 1 || dh > 256 || dv < 1 || T < 1)
+        return 1;
+    if (eps < 0.0 || !alpha) return 1;
+    double *wts = malloc(sizeof(double) * (size_t)T);
+    if (!wts) return 2;
+    if (wmode == ORACLE_W_GEOMETRIC) {
+        if (lisa_oracle_geometric_weights(beta, T, wts)) { free(wts); return 1; }
+    } else if (wmode == ORACLE_W_FIXED) {
+        if (!w) { free(wts); return 1; }
+        memcpy(wts, w, sizeof(double) * (size_t)T);
+    } else if (wmode == ORACLE_W_MLP) {
+        if (!W1 || !b1 || !W2 || !b2 || hidden < 1) { free(wts); return 1; }
+    } else {
+        free(wts);
+        return 1;
+    }
+    slice_args A = {H, W, dh, dv, T, wmode, hidden, mode, relu_inputs, eps,
+                    wts, W1, b1, W2, b2};
+    const long n = (long)H * W;
+    const long slices = (long)B * heads;
+    int err = 0;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+#endif
+    for (long sl = 0; sl < slices; ++sl) {
+        long hq = sl * n * dh, hv = sl * n * dv;
+        err |= forward_slice(&A, Xq + hq, Xk + hq, V + hv, alpha[sl % heads],
+                             O ? O + hv : NULL, G ? G + hv : NULL, L ? L + hv : NULL);
+    }
+    free(wts);
+    return err;
+}
+
+/*
+ * Dense transition matrix of one slice, S_ij = Q~_i . K_j  [note §2.2], for
+ * small n only (n x n doubles).  Used by the tests that check that S is
+ * non-negative, row-stochastic up to eps and of rank at most dh.
+ */
+int lisa_oracle_transition(const double *Xq, const double *Xk, int n, int dh,
+                           double eps, int relu_inputs, double *S)
+{
+    if (n < 1 || dh < 1 || dh > 256 || eps < 0.0) return 1;
+    double *Qf = malloc(sizeof(double) * (size_t)n * dh);
+    double *Kf = malloc(sizeof(double) * (size_t)n * dh);
+    double *Qt = malloc(sizeof(double) * (size_t)n * dh);
+    double s[256];
+    if (!Qf || !Kf || !Qt) { free(Qf); free(Kf); free(Qt); return 2; }
+    feature_map(Xq, Qf, (long)n * dh, relu_inputs);
+    feature_map(Xk, Kf, (long)n * dh, relu_inputs);
+    key_sum(Kf, n, dh, s);
+    normalised_queries(Qf, s, n, dh, eps, Qt);
+    for (int i = 0; i < n; ++i)
+        for (int j = 0; j < n; ++j) {
+            double acc = 0.0;
+            for (int a = 0; a < dh; ++a) acc += Qt[(long)i * dh + a] * Kf[(long)j * dh + a];
+            S[(long)i * n + j] = acc;
+        }
+    free(Qf); free(Kf); free(Qt);
+    return 0;
+}
+
+/*
+ * Adaptive step weights of every token of one slice [note §2.4]:
+ * out[n][T].  Xq, Xk are [n][dh]; the feature map is applied when
+ * relu_inputs is set.
+ */
+int lisa_oracle_step_weights(const double *Xq, const double *Xk, int n, int dh,
+                             int T, const double *W1, const double *b1,
+                             const double *W2, const double *b2, int hidden,
+                             int relu_inputs, double *out)
+{
+    if (n < 1 || dh < 1 || T < 1 || hidden < 1) return 1;
+    double *q = malloc(sizeof(double) * (size_t)dh);
+    double *k = malloc(sizeof(double) * (size_t)dh);
+    double *h = malloc(sizeof(double) * (size_t)hidden);
+    if (!q || !k || !h) { free(q); free(k); free(h); return 2; }
+    for (int i = 0; i < n; ++i) {
+        feature_map(Xq + (long)i * dh, q, dh, relu_inputs);
+        feature_map(Xk + (long)i * dh, k, dh, relu_inputs);
+        mlp_step_weights(q, k, dh, T, W1, b1, W2, b2, hidden, h, out + (long)i * T);
+    }
+    free(q); free(k); free(h);
+    return 0;
+}
+
+/* Number of OpenMP threads a parallel region would use (1 without OpenMP). */
+int lisa_oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
