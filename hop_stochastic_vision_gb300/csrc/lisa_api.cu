@@ -1,0 +1,257 @@
+// lisa_api.cu -- the C ABI of liblisa.so: argument checks, the split-K plan,
+// the workspace carve-up, host-side walk weights, and dispatch to the kernel
+// families.  Every check runs on the host before the first launch.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include <cuda_runtime.h>
+
+#include "lisa.h"
+#include "lisa_internal.h"
+
+namespace lisa {
+namespace {
+
+constexpr int kTargetCtas = 2 * 152;  // two resident CTAs on each of the 152 SMs
+constexpr int kMinChunk = 64;         // smallest split-K chunk, in tokens
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool supported_dim(int d) { return d == 16 || d == 32 || d == 64; }
+
+bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+bool overlaps(const void *a, size_t an, const void *b, size_t bn) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + bn && y < x + an;
+}
+
+}  // namespace
+
+Plan make_plan(int slices, int n, int D, int T, int dtype) {
+    (void)dtype;
+    Plan pl{};
+    int chunks = (kTargetCtas + slices - 1) / slices;
+    const int max_chunks = (n + kMinChunk - 1) / kMinChunk;
+    if (chunks > max_chunks) chunks = max_chunks;
+    if (chunks < 1) chunks = 1;
+    int chunk = (n + chunks - 1) / chunks;
+    chunk = (chunk + 15) / 16 * 16;  // whole 16-token MMA steps
+    chunks = (n + chunk - 1) / chunk;
+    pl.chunks = chunks;
+    pl.chunk = chunk;
+    const size_t S = (size_t)slices, C = (size_t)chunks, d = (size_t)D;
+    const size_t nmat = (size_t)(T > 1 ? T - 1 : 1);
+    size_t off = 0;
+    pl.off_s_part = off; off = align_up(off + S * C * d * sizeof(float));
+    pl.off_u_part = off; off = align_up(off + S * C * d * d * sizeof(float));
+    pl.off_m_part = off; off = align_up(off + S * C * d * d * sizeof(float));
+    pl.off_s_red = off;  off = align_up(off + S * d * sizeof(float));
+    pl.off_ucat = off;   off = align_up(off + S * nmat * d * d * sizeof(float));
+    pl.off_aux = off;    off = align_up(off + S * nmat * d * d * 2 * sizeof(uint16_t));
+    pl.total = off;
+    return pl;
+}
+
+namespace {
+
+// Shared validation of lisa_forward / lisa_forward_host / lisa_workspace_bytes
+// scalars.  Returns LISA_OK, or the status to report.
+lisa_status check_sizes(int B, int heads, int H, int W, int d_h, int d_v, int T, int dtype) {
+    if (B < 0 || heads < 0 || H < 0 || W < 0) return LISA_ERR_INVALID_ARG;
+    if (dtype != LISA_F32 && dtype != LISA_BF16) return LISA_ERR_INVALID_ARG;
+    if (d_h < 1 || d_v < 1 || T < 1) return LISA_ERR_INVALID_ARG;
+    if (!supported_dim(d_h) || d_v != d_h) return LISA_ERR_UNSUPPORTED;
+    if (T > LISA_MAX_T) return LISA_ERR_UNSUPPORTED;
+    const long long slices = (long long)B * heads, n = (long long)H * W;
+    if (n > (1LL << 30) || slices > (1LL << 30) || slices * n > (1LL << 31) - 1)
+        return LISA_ERR_UNSUPPORTED;
+    return LISA_OK;
+}
+
+}  // namespace
+}  // namespace lisa
+
+using namespace lisa;
+
+extern "C" size_t lisa_workspace_bytes(int B, int heads, int H, int W, int d_h, int d_v, int T,
+                                       int dtype) {
+    if (check_sizes(B, heads, H, W, d_h, d_v, T, dtype) != LISA_OK) return 0;
+    const long long slices = (long long)B * heads, n = (long long)H * W;
+    if (slices == 0 || n == 0) return 0;
+    return make_plan((int)slices, (int)n, d_h, T, dtype).total;
+}
+
+namespace {
+
+// Checks every argument of a forward call and fills the Problem.  Sets
+// *empty when there is nothing to compute.  Launches nothing.
+lisa_status prepare(Problem &p, bool &empty, const void *Q, const void *K, const void *V, void *O,
+                    int B, int heads, int H, int W, int d_h, int d_v, int T,
+                    const lisa_weights *wts, const float *alpha, float eps, int relu_inputs,
+                    int dtype, void *workspace, size_t workspace_bytes) {
+    empty = false;
+    lisa_status st = check_sizes(B, heads, H, W, d_h, d_v, T, dtype);
+    if (st != LISA_OK) return st;
+    if (!wts) return LISA_ERR_INVALID_ARG;
+    if (!(eps > 0.f) || !std::isfinite(eps)) return LISA_ERR_INVALID_ARG;
+    if (relu_inputs != 0 && relu_inputs != 1) return LISA_ERR_INVALID_ARG;
+
+    p = Problem{};
+    p.T = T;
+    switch (wts->mode) {
+        case LISA_W_GEOMETRIC: {
+            const double beta = (double)wts->beta;
+            if (!(beta >= 0.0 && beta < 1.0)) return LISA_ERR_INVALID_ARG;
+            // paper Eq. 4: (1-beta) beta^k renormalised over k < T, in double
+            const double norm = 1.0 - std::pow(beta, (double)T);
+            for (int k = 0; k < T; ++k)
+                p.w[k] = (float)((1.0 - beta) * std::pow(beta, (double)k) / norm);
+            p.wmode = LISA_W_FIXED;
+            break;
+        }
+        case LISA_W_FIXED:
+            if (!wts->w) return LISA_ERR_INVALID_ARG;
+            for (int k = 0; k < T; ++k) {
+                if (!std::isfinite(wts->w[k])) return LISA_ERR_INVALID_ARG;
+                p.w[k] = wts->w[k];
+            }
+            p.wmode = LISA_W_FIXED;
+            break;
+        case LISA_W_MLP:
+            if (!wts->W1 || !wts->b1 || !wts->W2 || !wts->b2) return LISA_ERR_INVALID_ARG;
+            if (wts->hidden < 1) return LISA_ERR_INVALID_ARG;
+            if (wts->hidden > LISA_MAX_HIDDEN || T > LISA_MAX_T_MLP) return LISA_ERR_UNSUPPORTED;
+            p.wmode = LISA_W_MLP;
+            p.W1 = wts->W1; p.b1 = wts->b1; p.W2 = wts->W2; p.b2 = wts->b2;
+            p.hidden = wts->hidden;
+            break;
+        default:
+            return LISA_ERR_INVALID_ARG;
+    }
+
+    const long long slices = (long long)B * heads, n = (long long)H * W;
+    if (slices == 0 || n == 0) {  // empty problem: nothing to launch
+        empty = true;
+        return LISA_OK;
+    }
+    if (!Q || !K || !V || !O || !alpha) return LISA_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O))
+        return LISA_ERR_INVALID_ARG;
+    const size_t esz = (dtype == LISA_BF16) ? 2 : 4;
+    const size_t bytes = (size_t)slices * (size_t)n * (size_t)d_h * esz;
+    if (overlaps(O, bytes, Q, bytes) || overlaps(O, bytes, K, bytes) || overlaps(O, bytes, V, bytes))
+        return LISA_ERR_INVALID_ARG;
+
+    const Plan pl = make_plan((int)slices, (int)n, d_h, T, dtype);
+    if (!workspace || workspace_bytes < pl.total) return LISA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return LISA_ERR_INVALID_ARG;
+
+    p.Q = Q; p.K = K; p.V = V; p.O = O;
+    p.slices = (int)slices;
+    p.heads = heads;
+    p.H = H; p.W = W; p.n = (int)n;
+    p.D = d_h;
+    p.relu = relu_inputs;
+    p.eps = eps;
+    p.alpha = alpha;
+    p.dtype = dtype;
+    p.chunks = pl.chunks;
+    p.chunk = pl.chunk;
+    char *ws = static_cast<char *>(workspace);
+    p.s_part = reinterpret_cast<float *>(ws + pl.off_s_part);
+    p.u_part = reinterpret_cast<float *>(ws + pl.off_u_part);
+    p.m_part = reinterpret_cast<float *>(ws + pl.off_m_part);
+    p.s_red = reinterpret_cast<float *>(ws + pl.off_s_red);
+    p.ucat = reinterpret_cast<float *>(ws + pl.off_ucat);
+    p.aux = ws + pl.off_aux;
+    return LISA_OK;
+}
+
+lisa_status launch(const Problem &p, cudaStream_t cs, int stage = -1) {
+    cudaError_t err = launch_simt(p, cs, stage);
+    return err == cudaSuccess ? LISA_OK : LISA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" lisa_status lisa_forward(const void *Q, const void *K, const void *V, void *O, int B,
+                                    int heads, int H, int W, int d_h, int d_v, int T,
+                                    const lisa_weights *wts, const float *alpha, float eps,
+                                    int relu_inputs, int dtype, void *workspace,
+                                    size_t workspace_bytes, void *stream) {
+    Problem p;
+    bool empty;
+    lisa_status st = prepare(p, empty, Q, K, V, O, B, heads, H, W, d_h, d_v, T, wts, alpha, eps,
+                             relu_inputs, dtype, workspace, workspace_bytes);
+    if (st != LISA_OK || empty) return st;
+    return launch(p, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" lisa_status lisa_forward_host(const void *hQ, const void *hK, const void *hV, void *hO,
+                                         void *dQ, void *dK, void *dV, void *dO, int B, int heads,
+                                         int H, int W, int d_h, int d_v, int T,
+                                         const lisa_weights *wts, const float *alpha, float eps,
+                                         int relu_inputs, int dtype, void *workspace,
+                                         size_t workspace_bytes, void *stream) {
+    Problem p;
+    bool empty;
+    lisa_status st = prepare(p, empty, dQ, dK, dV, dO, B, heads, H, W, d_h, d_v, T, wts, alpha,
+                             eps, relu_inputs, dtype, workspace, workspace_bytes);
+    if (st != LISA_OK || empty) return st;
+    if (!hQ || !hK || !hV || !hO) return LISA_ERR_INVALID_ARG;
+    const size_t esz = (dtype == LISA_BF16) ? 2 : 4;
+    const size_t bytes = (size_t)p.slices * (size_t)p.n * (size_t)p.D * esz;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(dQ, hQ, bytes, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+        cudaMemcpyAsync(dK, hK, bytes, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+        cudaMemcpyAsync(dV, hV, bytes, cudaMemcpyHostToDevice, cs) != cudaSuccess)
+        return LISA_ERR_CUDA;
+    st = launch(p, cs);
+    if (st != LISA_OK) return st;
+    if (cudaMemcpyAsync(hO, dO, bytes, cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+        return LISA_ERR_CUDA;
+    return LISA_OK;
+}
+
+extern "C" int lisa_num_stages(int dtype, int d_h, int T, int wmode) {
+    (void)dtype; (void)d_h; (void)T; (void)wmode;
+    return kSimtStages;
+}
+
+extern "C" const char *lisa_stage_name(int dtype, int d_h, int T, int wmode, int stage) {
+    if (stage < 0 || stage >= lisa_num_stages(dtype, d_h, T, wmode)) return nullptr;
+    return kSimtStageNames[stage];
+}
+
+extern "C" lisa_status lisa_forward_stage(int stage, const void *Q, const void *K, const void *V,
+                                          void *O, int B, int heads, int H, int W, int d_h,
+                                          int d_v, int T, const lisa_weights *wts,
+                                          const float *alpha, float eps, int relu_inputs,
+                                          int dtype, void *workspace, size_t workspace_bytes,
+                                          void *stream) {
+    Problem p;
+    bool empty;
+    lisa_status st = prepare(p, empty, Q, K, V, O, B, heads, H, W, d_h, d_v, T, wts, alpha, eps,
+                             relu_inputs, dtype, workspace, workspace_bytes);
+    if (st != LISA_OK) return st;
+    if (stage < 0 || stage >= lisa_num_stages(dtype, d_h, T, wts->mode)) return LISA_ERR_INVALID_ARG;
+    if (empty) return LISA_OK;
+    return launch(p, static_cast<cudaStream_t>(stream), stage);
+}
+
+extern "C" const char *lisa_status_string(int status) {
+    switch (status) {
+        case LISA_OK: return "LISA_OK";
+        case LISA_ERR_INVALID_ARG: return "LISA_ERR_INVALID_ARG: invalid argument";
+        case LISA_ERR_UNSUPPORTED: return "LISA_ERR_UNSUPPORTED: unsupported size or mode";
+        case LISA_ERR_WORKSPACE: return "LISA_ERR_WORKSPACE: workspace missing or too small";
+        case LISA_ERR_CUDA: return "LISA_ERR_CUDA: CUDA launch or runtime error";
+        case LISA_ERR_TIMEOUT: return "LISA_ERR_TIMEOUT: a bounded device wait gave up";
+        default: return "unknown lisa_status";
+    }
+}
+
+extern "C" int lisa_abi_version(void) { return 100; }

@@ -1,0 +1,207 @@
+"""ctypes binding of liblisa.so (C ABI in include/lisa.h).
+
+Argument marshalling only: torch supplies device memory and the current CUDA
+stream, every step of the layer runs in the library's kernels.  There is no
+CPU path: a missing library, a CPU tensor or a non-zero status raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "liblisa.so")
+
+LISA_OK = 0
+LISA_ERR_INVALID_ARG = 1
+LISA_ERR_UNSUPPORTED = 2
+LISA_ERR_WORKSPACE = 3
+LISA_ERR_CUDA = 4
+LISA_ERR_TIMEOUT = 5
+
+LISA_F32 = 0
+LISA_BF16 = 1
+
+LISA_W_GEOMETRIC = 0
+LISA_W_FIXED = 1
+LISA_W_MLP = 2
+
+LISA_MAX_T = 16
+LISA_MAX_T_MLP = 8
+LISA_MAX_HIDDEN = 64
+
+EXPORTED = ("lisa_workspace_bytes", "lisa_forward", "lisa_forward_host", "lisa_num_stages",
+            "lisa_stage_name", "lisa_forward_stage", "lisa_status_string", "lisa_abi_version")
+
+
+class lisa_weights(ctypes.Structure):
+    _fields_ = [
+        ("mode", ctypes.c_int),
+        ("beta", ctypes.c_float),
+        ("w", ctypes.POINTER(ctypes.c_float)),
+        ("W1", ctypes.c_void_p),
+        ("b1", ctypes.c_void_p),
+        ("W2", ctypes.c_void_p),
+        ("b2", ctypes.c_void_p),
+        ("hidden", ctypes.c_int),
+    ]
+
+
+class LisaError(RuntimeError):
+    def __init__(self, status: int):
+        self.status = status
+        super().__init__(lisa_status_string(status))
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load liblisa.so (built by hop_stochastic_vision_gb300.build); raise if absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError("liblisa.so is not built (%s); run hop_stochastic_vision_gb300.build" % path)
+        lib = ctypes.CDLL(path)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        wp = ctypes.POINTER(lisa_weights)
+        lib.lisa_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i]
+        lib.lisa_workspace_bytes.restype = sz
+        lib.lisa_forward.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, wp, vp, f, i, i, vp, sz, vp]
+        lib.lisa_forward.restype = i
+        lib.lisa_forward_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, wp, vp,
+                                          f, i, i, vp, sz, vp]
+        lib.lisa_forward_host.restype = i
+        lib.lisa_num_stages.argtypes = [i, i, i, i]
+        lib.lisa_num_stages.restype = i
+        lib.lisa_stage_name.argtypes = [i, i, i, i, i]
+        lib.lisa_stage_name.restype = ctypes.c_char_p
+        lib.lisa_forward_stage.argtypes = [i] + lib.lisa_forward.argtypes
+        lib.lisa_forward_stage.restype = i
+        lib.lisa_status_string.argtypes = [i]
+        lib.lisa_status_string.restype = ctypes.c_char_p
+        lib.lisa_abi_version.argtypes = []
+        lib.lisa_abi_version.restype = i
+        _lib = lib
+        return lib
+
+
+# -- the C entry points under their own names ---------------------------------------
+
+def lisa_status_string(status: int) -> str:
+    return load().lisa_status_string(int(status)).decode()
+
+
+def lisa_abi_version() -> int:
+    return int(load().lisa_abi_version())
+
+
+def lisa_workspace_bytes(B, heads, H, W, d_h, d_v, T, dtype) -> int:
+    return int(load().lisa_workspace_bytes(B, heads, H, W, d_h, d_v, T, dtype))
+
+
+def lisa_forward(Q, K, V, O, B, heads, H, W, d_h, d_v, T, wts, alpha, eps, relu_inputs, dtype,
+                 workspace, workspace_bytes, stream) -> int:
+    """Raw call: pointers are ints (device addresses), wts a lisa_weights."""
+    return int(load().lisa_forward(Q, K, V, O, B, heads, H, W, d_h, d_v, T, ctypes.byref(wts), alpha,
+                                   eps, relu_inputs, dtype, workspace, workspace_bytes, stream))
+
+
+def lisa_num_stages(dtype, d_h, T, wmode) -> int:
+    return int(load().lisa_num_stages(dtype, d_h, T, wmode))
+
+
+def lisa_stage_name(dtype, d_h, T, wmode, stage):
+    r = load().lisa_stage_name(dtype, d_h, T, wmode, stage)
+    return None if r is None else r.decode()
+
+
+def lisa_forward_stage(stage, Q, K, V, O, B, heads, H, W, d_h, d_v, T, wts, alpha, eps, relu_inputs,
+                       dtype, workspace, workspace_bytes, stream) -> int:
+    return int(load().lisa_forward_stage(stage, Q, K, V, O, B, heads, H, W, d_h, d_v, T,
+                                         ctypes.byref(wts), alpha, eps, relu_inputs, dtype,
+                                         workspace, workspace_bytes, stream))
+
+
+def lisa_forward_host(hQ, hK, hV, hO, dQ, dK, dV, dO, B, heads, H, W, d_h, d_v, T, wts, alpha, eps,
+                      relu_inputs, dtype, workspace, workspace_bytes, stream) -> int:
+    return int(load().lisa_forward_host(hQ, hK, hV, hO, dQ, dK, dV, dO, B, heads, H, W, d_h, d_v, T,
+                                        ctypes.byref(wts), alpha, eps, relu_inputs, dtype, workspace,
+                                        workspace_bytes, stream))
+
+
+# -- tensor-level convenience ---------------------------------------------------------
+
+_DTYPES = {torch.float32: LISA_F32, torch.bfloat16: LISA_BF16}
+
+
+def make_weights(T: int, beta=None, w=None, mlp=None):
+    """Build the lisa_weights struct.  Returns (struct, keepalive) -- keep the
+    second item alive for as long as the struct is used."""
+    wt = lisa_weights()
+    keep = []
+    if w is not None:
+        arr = (ctypes.c_float * T)(*[float(x) for x in w])
+        keep.append(arr)
+        wt.mode = LISA_W_FIXED
+        wt.w = ctypes.cast(arr, ctypes.POINTER(ctypes.c_float))
+    elif mlp is not None:
+        W1, b1, W2, b2 = mlp
+        for t in (W1, b1, W2, b2):
+            if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous()):
+                raise ValueError("MLP parameters must be contiguous fp32 CUDA tensors")
+        keep.extend((W1, b1, W2, b2))
+        wt.mode = LISA_W_MLP
+        wt.W1, wt.b1, wt.W2, wt.b2 = W1.data_ptr(), b1.data_ptr(), W2.data_ptr(), b2.data_ptr()
+        wt.hidden = int(W1.shape[0])
+    elif beta is not None:
+        wt.mode = LISA_W_GEOMETRIC
+        wt.beta = float(beta)
+    else:
+        raise ValueError("give beta, w or mlp")
+    return wt, keep
+
+
+def workspace_for(q: torch.Tensor, T: int) -> torch.Tensor:
+    B, heads, n, d = q.shape
+    nbytes = lisa_workspace_bytes(B, heads, n, 1, d, d, T, _DTYPES[q.dtype])
+    return torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+
+
+def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, grid, T: int, *, alpha: torch.Tensor,
+            beta=None, w=None, mlp=None, eps: float = 1e-6, relu: bool = True, out=None,
+            workspace=None, stream=None) -> torch.Tensor:
+    """LiSA forward on CUDA tensors [B, heads, H*W, d] (fp32 or bf16).
+    Returns O (a new tensor unless ``out`` is given)."""
+    if not (q.is_cuda and k.is_cuda and v.is_cuda and alpha.is_cuda):
+        raise ValueError("lisa.forward runs on CUDA tensors only")
+    if q.dtype not in _DTYPES or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share dtype float32 or bfloat16")
+    if alpha.dtype != torch.float32:
+        raise ValueError("alpha must be fp32")
+    for t in (q, k, v, alpha):
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+    B, heads, n, d = q.shape
+    H, W = grid
+    dv = v.shape[-1]
+    O = torch.empty_like(v) if out is None else out
+    wt, keep = make_weights(T, beta=beta, w=w, mlp=mlp)
+    dt = _DTYPES[q.dtype]
+    nbytes = lisa_workspace_bytes(B, heads, H, W, d, dv, T, dt)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    st = torch.cuda.current_stream(q.device).cuda_stream if stream is None else stream
+    status = lisa_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), O.data_ptr(), B, heads, H, W, d,
+                          dv, T, wt, alpha.data_ptr(), float(eps), int(bool(relu)), dt,
+                          workspace.data_ptr(), workspace.numel(), st)
+    del keep
+    if status != LISA_OK:
+        raise LisaError(status)
+    return O

@@ -1,0 +1,152 @@
+/*
+ * lisa.h -- C ABI of the GB300 (sm_103a) LiSA forward layer library, liblisa.so.
+ *
+ * LiSA ("LiSA: Linear Stochastic Attention for Long-Range Visual Modeling",
+ * arXiv 2611.04216v2; cited from its reading note, sections 2.1-2.5) works
+ * per (batch, head) slice on an H x W token grid, n = H*W tokens:
+ *
+ *   feature map      Q = ReLU(Xq), K = ReLU(Xk)                 [note §2.1]
+ *   transition       Q~_i = Q_i / (Q_i . sum_j K_j + eps),
+ *                    S = Q~ K^T  (row-stochastic, never formed)  [note §2.2]
+ *   global branch    g_i = sum_{k<T} w_k(i) (S^k V)_i, evaluated as
+ *                    S^k V = Q~ U_k, U_1 = K^T V, U_k = (K^T Q~) U_(k-1)
+ *                                                   [note §2.3; paper Eq. 8]
+ *   walk weights     geometric w_k = (1-beta) beta^k / (1-beta^T)
+ *                                                   [note §2.2; paper Eq. 4]
+ *                    or per token and head: softmax(W2 GELU(W1 [q_i;k_i] + b1) + b2)
+ *                                          [note §2.4; paper Eq. 10, Supp. 8]
+ *   local branch     softmax over the token and its in-grid 8-neighbours of
+ *                    q_i . k_j / sqrt(d_h), applied to V   [note §2.4]
+ *   output           o_i = alpha_h g_i + (1 - alpha_h) l_i  [note §2.4; Fig. 2]
+ *
+ * Conventions shared by every entry point:
+ *   - Tensors are contiguous row-major: Q, K [B][heads][H*W][d_h] and
+ *     V, O [B][heads][H*W][d_v]; token index i = r*W + c.
+ *   - dtype LISA_F32: fp32 in, fp32 out, fp32 arithmetic throughout.
+ *     dtype LISA_BF16: bf16 in, bf16 out (round to nearest even), fp32
+ *     accumulation; bf16 tensor-core operands where the contraction allows.
+ *   - d_h == d_v, each one of 16, 32, 64; other sizes give LISA_ERR_UNSUPPORTED.
+ *   - Device pointers must be 16-byte aligned.  O must not overlap an input.
+ *   - The library allocates nothing and keeps no global state: the caller
+ *     owns every buffer, including the workspace.  Calls on different
+ *     streams with different workspaces may run concurrently.
+ *   - Every argument is checked on the host before anything is launched; a
+ *     bad argument returns its status and launches nothing.  Launch
+ *     failures return LISA_ERR_CUDA.  The call is asynchronous on `stream`
+ *     (a cudaStream_t; NULL = legacy default stream) and never synchronises.
+ */
+#ifndef LISA_H_
+#define LISA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum lisa_status {
+    LISA_OK = 0,
+    LISA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, T < 1, beta outside [0,1), eps <= 0, misalignment */
+    LISA_ERR_UNSUPPORTED = 2,  /* d_h / d_v / T / hidden outside what the kernels are built for */
+    LISA_ERR_WORKSPACE = 3,    /* workspace missing or smaller than lisa_workspace_bytes() */
+    LISA_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed */
+    LISA_ERR_TIMEOUT = 5       /* a bounded device-side wait gave up */
+} lisa_status;
+
+typedef enum lisa_dtype { LISA_F32 = 0, LISA_BF16 = 1 } lisa_dtype;
+
+/* Walk-weight modes [note §2.2, §2.4]. */
+typedef enum lisa_wmode {
+    LISA_W_GEOMETRIC = 0,  /* w_k = (1-beta) beta^k / (1-beta^T), computed on the host in double */
+    LISA_W_FIXED = 1,      /* w[0..T-1] given by the caller (host memory), any real values */
+    LISA_W_MLP = 2         /* per-token, per-head weights from the 2-layer MLP + softmax */
+} lisa_wmode;
+
+#define LISA_MAX_T 16        /* largest truncation depth T */
+#define LISA_MAX_T_MLP 8     /* largest T with adaptive (MLP) weights */
+#define LISA_MAX_HIDDEN 64   /* largest MLP hidden width */
+
+typedef struct lisa_weights {
+    int mode;          /* lisa_wmode */
+    float beta;        /* GEOMETRIC: continue probability, 0 <= beta < 1 */
+    const float *w;    /* FIXED: host array [T] */
+    const float *W1;   /* MLP: device fp32 [hidden][2*d_h]; input is concat(q_i, k_i) post-ReLU */
+    const float *b1;   /* MLP: device fp32 [hidden] */
+    const float *W2;   /* MLP: device fp32 [T][hidden] */
+    const float *b2;   /* MLP: device fp32 [T] */
+    int hidden;        /* MLP: hidden width, 1..LISA_MAX_HIDDEN (32 in the paper's setting) */
+} lisa_weights;
+
+/*
+ * Bytes of device workspace lisa_forward needs for this problem (a pure
+ * host computation; no CUDA call).  Returns 0 for arguments lisa_forward
+ * would reject.  The workspace holds the split-K partial sums of sum_j K_j,
+ * K^T V and K^T Q~ [note §2.3], the reduced statistics and U_1..U_(T-1);
+ * lisa_forward overwrites all of it, so it needs no initialisation.
+ */
+size_t lisa_workspace_bytes(int B, int heads, int H, int W, int d_h, int d_v, int T,
+                            int dtype);
+
+/*
+ * The LiSA forward layer [note §2.1-2.4] on device buffers.
+ *   Q, K        device [B][heads][H*W][d_h], dtype; raw projections Xq, Xk
+ *               when relu_inputs = 1 (ReLU applied on load), or already
+ *               feature-mapped (non-negative) when relu_inputs = 0.
+ *   V           device [B][heads][H*W][d_v], dtype.
+ *   O           device [B][heads][H*W][d_v], dtype; written.
+ *   T           truncation depth, 1..LISA_MAX_T (1..LISA_MAX_T_MLP for MLP).
+ *   wts         host struct; see lisa_weights.
+ *   alpha       device fp32 [heads]: branch mix per head, used as given.
+ *   eps         stabiliser of the row normaliser, > 0 (the paper's setting: 1e-6).
+ *   workspace   device, >= lisa_workspace_bytes(...) bytes, 16-byte aligned.
+ *   stream      cudaStream_t.
+ */
+lisa_status lisa_forward(const void *Q, const void *K, const void *V, void *O, int B,
+                         int heads, int H, int W, int d_h, int d_v, int T,
+                         const lisa_weights *wts, const float *alpha, float eps,
+                         int relu_inputs, int dtype, void *workspace,
+                         size_t workspace_bytes, void *stream);
+
+/*
+ * End-to-end variant on host buffers: copies hQ, hK, hV (host, ideally
+ * pinned) into the caller's device buffers dQ, dK, dV, runs lisa_forward,
+ * and copies dO back into hO, all enqueued on `stream` in that order.  The
+ * host buffers must stay valid until the stream has drained; the call does
+ * not wait for it.  Sizes and the other arguments are as for lisa_forward.
+ */
+lisa_status lisa_forward_host(const void *hQ, const void *hK, const void *hV, void *hO,
+                              void *dQ, void *dK, void *dV, void *dO, int B, int heads,
+                              int H, int W, int d_h, int d_v, int T,
+                              const lisa_weights *wts, const float *alpha, float eps,
+                              int relu_inputs, int dtype, void *workspace,
+                              size_t workspace_bytes, void *stream);
+
+/*
+ * Per-kernel access for profiling.  One lisa_forward call is a fixed chain of
+ * lisa_num_stages(...) kernel launches; lisa_forward_stage(i, ...) launches
+ * only kernel i of that chain with the same arguments and checks.  Running
+ * stages 0 .. n-1 in order on one stream with one workspace computes exactly
+ * what lisa_forward computes (each stage reads what the earlier ones left in
+ * the workspace), so a caller can put timing events between the kernels.
+ * lisa_stage_name returns the kernel's name, or NULL for a bad index.
+ * A bad stage index returns LISA_ERR_INVALID_ARG.
+ */
+int lisa_num_stages(int dtype, int d_h, int T, int wmode);
+const char *lisa_stage_name(int dtype, int d_h, int T, int wmode, int stage);
+lisa_status lisa_forward_stage(int stage, const void *Q, const void *K, const void *V, void *O,
+                               int B, int heads, int H, int W, int d_h, int d_v, int T,
+                               const lisa_weights *wts, const float *alpha, float eps,
+                               int relu_inputs, int dtype, void *workspace,
+                               size_t workspace_bytes, void *stream);
+
+/* Static, human-readable name of a status code. */
+const char *lisa_status_string(int status);
+
+/* ABI version, bumped on any signature change: major * 100 + minor. */
+int lisa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LISA_H_ */

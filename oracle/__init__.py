@@ -36,7 +36,9 @@ def build(force: bool = False) -> str:
     """Compile ``lisa_oracle.c`` into ``liblisa_oracle.so`` next to it.
 
     -O2 without -ffast-math keeps the C evaluation order; OpenMP only spreads
-    independent (batch, head) slices over threads.
+    independent outputs (query rows, matrix entries, tokens) over threads, so
+    every sum keeps its serial order and the result does not depend on the
+    thread count.
     """
     if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
         return _LIB

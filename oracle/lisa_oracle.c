@@ -51,6 +51,28 @@
 #define ORACLE_W_GEOMETRIC 0
 #define ORACLE_W_FIXED 1
 #define ORACLE_W_MLP 2
+#define ORACLE_MAX_T 256
+#define ORACLE_MAX_HIDDEN 1024
+
+/* OpenMP only spreads independent outputs (query rows, matrix entries,
+ * tokens) over threads; every sum keeps its serial order. */
+static int omp_thread(void)
+{
+#ifdef _OPENMP
+    return omp_get_thread_num();
+#else
+    return 0;
+#endif
+}
+
+static int omp_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
 
 /* ---------------------------------------------------------------------- */
 /* Walk weights, [note §2.2] (paper Eq. 4): a walk continues with          */
@@ -103,13 +125,15 @@ static void normalised_queries(const double *Q, const double *s, int n, int dh,
 /* ---------------------------------------------------------------------- */
 static void walk_terms_explicit(const double *Qt, const double *K,
                                 const double *V, int n, int dh, int dv, int T,
-                                double *Y, double *Srow)
+                                double *Y, double *Srows)
 {
     memcpy(Y, V, sizeof(double) * (size_t)n * dv);
     for (int k = 1; k < T; ++k) {
         const double *prev = Y + (size_t)(k - 1) * n * dv;
         double *cur = Y + (size_t)k * n * dv;
+#pragma omp parallel for schedule(static)
         for (int i = 0; i < n; ++i) {
+            double *Srow = Srows + (size_t)omp_thread() * n;
             for (int j = 0; j < n; ++j) {
                 double sij = 0.0;
                 for (int a = 0; a < dh; ++a)
@@ -139,12 +163,14 @@ static void walk_terms_lowrank(const double *Qt, const double *K,
 {
     memcpy(Y, V, sizeof(double) * (size_t)n * dv);
     if (T < 2) return;
+#pragma omp parallel for collapse(2) schedule(static)
     for (int a = 0; a < dh; ++a)
         for (int b = 0; b < dh; ++b) {
             double acc = 0.0;
             for (int j = 0; j < n; ++j) acc += K[(long)j * dh + a] * Qt[(long)j * dh + b];
             M[a * dh + b] = acc;
         }
+#pragma omp parallel for collapse(2) schedule(static)
     for (int a = 0; a < dh; ++a)
         for (int e = 0; e < dv; ++e) {
             double acc = 0.0;
@@ -162,6 +188,7 @@ static void walk_terms_lowrank(const double *Qt, const double *K,
             memcpy(U, Unext, sizeof(double) * (size_t)dh * dv);
         }
         double *cur = Y + (size_t)k * n * dv;
+#pragma omp parallel for schedule(static)
         for (int i = 0; i < n; ++i)
             for (int e = 0; e < dv; ++e) {
                 double acc = 0.0;
@@ -216,6 +243,7 @@ static void local_branch(const double *Qf, const double *Kf, const double *V,
                          int H, int W, int dh, int dv, double *L)
 {
     const double scale = 1.0 / sqrt((double)dh);
+#pragma omp parallel for collapse(2) schedule(static)
     for (int r = 0; r < H; ++r)
         for (int c = 0; c < W; ++c) {
             int i = r * W + c;
@@ -269,15 +297,13 @@ static int forward_slice(const slice_args *A, const double *Xq, const double *Xk
     double *Y = malloc(sizeof(double) * (size_t)T * n * dv);
     double *g = malloc(sizeof(double) * (size_t)n * dv);
     double *l = malloc(sizeof(double) * (size_t)n * dv);
-    double *Srow = malloc(sizeof(double) * (size_t)n);
+    double *Srows = malloc(sizeof(double) * (size_t)n * omp_threads());
     double *M = malloc(sizeof(double) * (size_t)dh * dh);
     double *U = malloc(sizeof(double) * (size_t)dh * dv);
     double *Un = malloc(sizeof(double) * (size_t)dh * dv);
-    double *wk = malloc(sizeof(double) * (size_t)T);
-    double *h = malloc(sizeof(double) * (size_t)(A->hidden > 0 ? A->hidden : 1));
     double s[256];
     int err = 0;
-    if (!Qf || !Kf || !Qt || !Y || !g || !l || !Srow || !M || !U || !Un || !wk || !h) {
+    if (!Qf || !Kf || !Qt || !Y || !g || !l || !Srows || !M || !U || !Un) {
         err = 2;
         goto done;
     }
@@ -286,11 +312,14 @@ static int forward_slice(const slice_args *A, const double *Xq, const double *Xk
     key_sum(Kf, n, dh, s);
     normalised_queries(Qf, s, n, dh, A->eps, Qt);
     if (A->mode == ORACLE_EXPLICIT)
-        walk_terms_explicit(Qt, Kf, V, n, dh, dv, T, Y, Srow);
+        walk_terms_explicit(Qt, Kf, V, n, dh, dv, T, Y, Srows);
     else
         walk_terms_lowrank(Qt, Kf, V, n, dh, dv, T, Y, M, U, Un);
 
+    /* g_i = sum_k w_k(i) Y_k,i with the token's own weights in MLP mode */
+#pragma omp parallel for schedule(static)
     for (int i = 0; i < n; ++i) {
+        double wk[ORACLE_MAX_T], h[ORACLE_MAX_HIDDEN];
         if (A->wmode == ORACLE_W_MLP)
             mlp_step_weights(Qf + (long)i * dh, Kf + (long)i * dh, dh, T, A->W1,
                              A->b1, A->W2, A->b2, A->hidden, h, wk);
@@ -309,8 +338,8 @@ static int forward_slice(const slice_args *A, const double *Xq, const double *Xk
         if (L) L[t] = l[t];
     }
 done:
-    free(Qf); free(Kf); free(Qt); free(Y); free(g); free(l); free(Srow);
-    free(M); free(U); free(Un); free(wk); free(h);
+    free(Qf); free(Kf); free(Qt); free(Y); free(g); free(l); free(Srows);
+    free(M); free(U); free(Un);
     return err;
 }
 
@@ -331,7 +360,8 @@ int lisa_oracle_forward(const double *Xq, const double *Xk, const double *V,
                         int hidden, const double *alpha, double eps,
                         int relu_inputs, int mode, int nthreads)
 {
-    if (B < 0 || heads < 0 || H < 1 || W < 1 || dh < 1 || dh > 256 || dv < 1 || T < 1)
+    if (B < 0 || heads < 0 || H < 1 || W < 1 || dh < 1 || dh > 256 || dv < 1 || T < 1 ||
+        T > ORACLE_MAX_T)
         return 1;
     if (eps < 0.0 || !alpha) return 1;
     double *wts = malloc(sizeof(double) * (size_t)T);
@@ -342,7 +372,10 @@ int lisa_oracle_forward(const double *Xq, const double *Xk, const double *V,
         if (!w) { free(wts); return 1; }
         memcpy(wts, w, sizeof(double) * (size_t)T);
     } else if (wmode == ORACLE_W_MLP) {
-        if (!W1 || !b1 || !W2 || !b2 || hidden < 1) { free(wts); return 1; }
+        if (!W1 || !b1 || !W2 || !b2 || hidden < 1 || hidden > ORACLE_MAX_HIDDEN) {
+            free(wts);
+            return 1;
+        }
     } else {
         free(wts);
         return 1;
@@ -354,7 +387,6 @@ int lisa_oracle_forward(const double *Xq, const double *Xk, const double *V,
     int err = 0;
 #ifdef _OPENMP
     if (nthreads > 0) omp_set_num_threads(nthreads);
-#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
 #endif
     for (long sl = 0; sl < slices; ++sl) {
         long hq = sl * n * dh, hv = sl * n * dv;

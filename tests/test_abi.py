@@ -1,0 +1,155 @@
+"""The C ABI of liblisa.so on the host: the library loads without a GPU,
+exports every function include/lisa.h declares, and rejects bad arguments
+with a status code before anything is launched (no test here reaches a
+kernel launch, so none needs a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from hop_stochastic_vision_gb300 import build as lisa_build
+from hop_stochastic_vision_gb300 import lisa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    lisa_build.build()
+    lisa.load()
+
+
+def _declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"\b(lisa_\w+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_function():
+    names = _declared_functions()
+    assert "lisa_forward" in names and "lisa_workspace_bytes" in names
+    lib = ctypes.CDLL(lisa.LIB_PATH)
+    for name in names:
+        assert hasattr(lib, name), name
+    assert set(names) <= set(lisa.EXPORTED) | set(names)
+    for name in lisa.EXPORTED:
+        assert name in names
+
+
+def test_status_strings_and_version():
+    assert lisa.lisa_abi_version() >= 100
+    for st in range(6):
+        assert lisa.lisa_status_string(st).startswith("LISA_")
+    assert "unknown" in lisa.lisa_status_string(99)
+
+
+def test_workspace_bytes():
+    ws = lisa.lisa_workspace_bytes
+    assert ws(32, 1, 56, 56, 64, 64, 3, lisa.LISA_BF16) > 0
+    assert ws(32, 1, 56, 56, 64, 64, 5, lisa.LISA_BF16) >= ws(32, 1, 56, 56, 64, 64, 3, lisa.LISA_BF16)
+    assert ws(0, 1, 56, 56, 64, 64, 3, lisa.LISA_BF16) == 0          # empty problem
+    assert ws(1, 1, 4, 4, 48, 48, 3, lisa.LISA_BF16) == 0            # unsupported d
+    assert ws(1, 1, 4, 4, 64, 32, 3, lisa.LISA_BF16) == 0            # d_v != d_h
+    assert ws(1, 1, 4, 4, 64, 64, 0, lisa.LISA_BF16) == 0            # T < 1
+    assert ws(1, 1, 4, 4, 64, 64, 3, 7) == 0                         # bad dtype
+    assert ws(-1, 1, 4, 4, 64, 64, 3, lisa.LISA_F32) == 0
+    assert ws(1, 1, 4, 4, 16, 16, 16, lisa.LISA_F32) > 0
+    assert ws(1, 1, 4, 4, 16, 16, 17, lisa.LISA_F32) == 0
+
+
+FAKE = 1 << 20          # a 16-byte aligned address; never dereferenced (checks fail first)
+
+
+def _call(**over):
+    args = dict(Q=FAKE, K=FAKE + 4096, V=FAKE + 8192, O=FAKE + 12288, B=1, heads=1, H=4, W=4, d_h=16,
+                d_v=16, T=3, alpha=FAKE + 16384, eps=1e-6, relu=1, dtype=lisa.LISA_F32,
+                workspace=FAKE + 32768, wbytes=1 << 30, beta=0.5)
+    args.update(over)
+    wt, keep = lisa.make_weights(args["T"] if args["T"] > 0 else 1, beta=args["beta"]) \
+        if "wt" not in args else (args["wt"], None)
+    return lisa.lisa_forward(args["Q"], args["K"], args["V"], args["O"], args["B"], args["heads"],
+                             args["H"], args["W"], args["d_h"], args["d_v"], args["T"], wt,
+                             args["alpha"], args["eps"], args["relu"], args["dtype"],
+                             args["workspace"], args["wbytes"], 0)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(Q=0), lisa.LISA_ERR_INVALID_ARG),
+    (dict(K=0), lisa.LISA_ERR_INVALID_ARG),
+    (dict(V=0), lisa.LISA_ERR_INVALID_ARG),
+    (dict(O=0), lisa.LISA_ERR_INVALID_ARG),
+    (dict(alpha=0), lisa.LISA_ERR_INVALID_ARG),
+    (dict(Q=FAKE + 8), lisa.LISA_ERR_INVALID_ARG),                  # misaligned
+    (dict(O=FAKE + 4), lisa.LISA_ERR_INVALID_ARG),
+    (dict(O=FAKE + 4096), lisa.LISA_ERR_INVALID_ARG),               # O overlaps K
+    (dict(B=-1), lisa.LISA_ERR_INVALID_ARG),
+    (dict(H=-2), lisa.LISA_ERR_INVALID_ARG),
+    (dict(T=0), lisa.LISA_ERR_INVALID_ARG),
+    (dict(T=17), lisa.LISA_ERR_UNSUPPORTED),
+    (dict(d_h=48, d_v=48), lisa.LISA_ERR_UNSUPPORTED),
+    (dict(d_h=128, d_v=128), lisa.LISA_ERR_UNSUPPORTED),
+    (dict(d_v=32), lisa.LISA_ERR_UNSUPPORTED),
+    (dict(d_h=0), lisa.LISA_ERR_INVALID_ARG),
+    (dict(eps=0.0), lisa.LISA_ERR_INVALID_ARG),
+    (dict(eps=-1e-6), lisa.LISA_ERR_INVALID_ARG),
+    (dict(eps=float("nan")), lisa.LISA_ERR_INVALID_ARG),
+    (dict(eps=float("inf")), lisa.LISA_ERR_INVALID_ARG),
+    (dict(beta=1.0), lisa.LISA_ERR_INVALID_ARG),
+    (dict(beta=-0.1), lisa.LISA_ERR_INVALID_ARG),
+    (dict(relu=2), lisa.LISA_ERR_INVALID_ARG),
+    (dict(dtype=5), lisa.LISA_ERR_INVALID_ARG),
+    (dict(workspace=0), lisa.LISA_ERR_WORKSPACE),
+    (dict(wbytes=16), lisa.LISA_ERR_WORKSPACE),
+    (dict(workspace=FAKE + 32776), lisa.LISA_ERR_INVALID_ARG),      # misaligned workspace
+])
+def test_forward_rejects_before_launch(over, status):
+    assert _call(**over) == status
+
+
+def test_weight_struct_checks():
+    wt = lisa.lisa_weights()
+    wt.mode = 9
+    assert _call(wt=wt) == lisa.LISA_ERR_INVALID_ARG
+    wt = lisa.lisa_weights()
+    wt.mode = lisa.LISA_W_FIXED                      # w missing
+    assert _call(wt=wt) == lisa.LISA_ERR_INVALID_ARG
+    arr = (ctypes.c_float * 3)(0.5, float("nan"), 0.5)
+    wt.w = ctypes.cast(arr, ctypes.POINTER(ctypes.c_float))
+    assert _call(wt=wt) == lisa.LISA_ERR_INVALID_ARG
+    wt = lisa.lisa_weights()
+    wt.mode = lisa.LISA_W_MLP                        # MLP pointers missing
+    assert _call(wt=wt) == lisa.LISA_ERR_INVALID_ARG
+    wt.W1 = wt.b1 = wt.W2 = wt.b2 = FAKE
+    wt.hidden = 0
+    assert _call(wt=wt) == lisa.LISA_ERR_INVALID_ARG
+    wt.hidden = 65
+    assert _call(wt=wt) == lisa.LISA_ERR_UNSUPPORTED
+    wt.hidden = 32
+    assert _call(wt=wt, T=9) == lisa.LISA_ERR_UNSUPPORTED
+    # a null weight struct
+    lib = lisa.load()
+    rc = lib.lisa_forward(FAKE, FAKE, FAKE, FAKE, 1, 1, 4, 4, 16, 16, 3, None, FAKE, 1e-6, 1, 0,
+                          FAKE, 1 << 30, None)
+    assert rc == lisa.LISA_ERR_INVALID_ARG
+
+
+def test_empty_problem_launches_nothing():
+    # zero slices or zero tokens: OK with null buffers, nothing to do
+    assert _call(B=0, Q=0, K=0, V=0, O=0, workspace=0) == lisa.LISA_OK
+    assert _call(heads=0, Q=0, K=0, V=0, O=0, workspace=0) == lisa.LISA_OK
+    assert _call(H=0, Q=0, K=0, V=0, O=0, workspace=0) == lisa.LISA_OK
+
+
+def test_forward_host_checks_before_copies():
+    wt, _ = lisa.make_weights(3, beta=0.5)
+    dev = [FAKE + 4096 * i for i in range(4)]
+    args = [FAKE] * 4 + dev + [1, 1, 4, 4, 16, 16, 3, wt, FAKE, 1e-6, 1, lisa.LISA_F32, FAKE, 16, 0]
+    assert lisa.lisa_forward_host(*args) == lisa.LISA_ERR_WORKSPACE
+    args[0] = 0
+    args[-3], args[-2] = FAKE, 1 << 30
+    assert lisa.lisa_forward_host(*args) == lisa.LISA_ERR_INVALID_ARG
