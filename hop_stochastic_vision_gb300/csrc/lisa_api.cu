@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include <cuda_runtime.h>
 
@@ -255,3 +256,60 @@ extern "C" const char *lisa_status_string(int status) {
 }
 
 extern "C" int lisa_abi_version(void) { return 100; }
+
+// ---------------------------------------------------------------------------
+// lisa_forward_noalloc -- the layer for callers that may not allocate device
+// memory.  Some hosts of this code cannot call cudaMalloc when they run it:
+// a stream being captured into a CUDA graph in global capture mode (an
+// allocation there invalidates the capture), an operator plugged into an
+// inference engine or framework that owns all device memory through its own
+// pool and plans it before execution, or a serving loop that cannot afford
+// the device-wide synchronisation cudaFree implies.  This entry point needs
+// no workspace from them: it runs in a scratch array compiled into the
+// library (LISA_NOALLOC_SCRATCH_BYTES on every device that loads the
+// library, held until the process exits).
+// ---------------------------------------------------------------------------
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[LISA_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kMaxDevices];  // device address of g_noalloc_scratch, per device
+
+// In host code g_noalloc_scratch names a host-side shadow, not device memory;
+// its device address comes from the runtime, looked up once per device with
+// that device current.
+lisa_status noalloc_scratch(void **out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return LISA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return LISA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return LISA_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return LISA_OK;
+}
+
+}  // namespace
+
+extern "C" lisa_status lisa_forward_noalloc(const void *Q, const void *K, const void *V, void *O,
+                                            int B, int heads, int H, int W, int d_h, int d_v,
+                                            int T, const lisa_weights *wts, const float *alpha,
+                                            float eps, int relu_inputs, int dtype, void *stream) {
+    lisa_status st = check_sizes(B, heads, H, W, d_h, d_v, T, dtype);
+    if (st != LISA_OK) return st;
+    const long long slices = (long long)B * heads, n = (long long)H * W;
+    const size_t need = (slices == 0 || n == 0) ? 0 : make_plan((int)slices, (int)n, d_h, T, dtype).total;
+    if (need > (size_t)LISA_NOALLOC_SCRATCH_BYTES) return LISA_ERR_WORKSPACE;
+    void *scratch = nullptr;
+    if (need > 0) {
+        st = noalloc_scratch(&scratch);
+        if (st != LISA_OK) return st;
+    }
+    return lisa_forward(Q, K, V, O, B, heads, H, W, d_h, d_v, T, wts, alpha, eps, relu_inputs, dtype,
+                        scratch, (size_t)LISA_NOALLOC_SCRATCH_BYTES, stream);
+}

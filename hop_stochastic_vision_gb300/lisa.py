@@ -34,7 +34,10 @@ LISA_MAX_T_MLP = 8
 LISA_MAX_HIDDEN = 64
 
 EXPORTED = ("lisa_workspace_bytes", "lisa_forward", "lisa_forward_host", "lisa_num_stages",
-            "lisa_stage_name", "lisa_forward_stage", "lisa_status_string", "lisa_abi_version")
+            "lisa_stage_name", "lisa_forward_stage", "lisa_forward_noalloc", "lisa_status_string",
+            "lisa_abi_version")
+
+LISA_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class lisa_weights(ctypes.Structure):
@@ -84,6 +87,8 @@ def load(path: str = LIB_PATH):
         lib.lisa_stage_name.restype = ctypes.c_char_p
         lib.lisa_forward_stage.argtypes = [i] + lib.lisa_forward.argtypes
         lib.lisa_forward_stage.restype = i
+        lib.lisa_forward_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, wp, vp, f, i, i, vp]
+        lib.lisa_forward_noalloc.restype = i
         lib.lisa_status_string.argtypes = [i]
         lib.lisa_status_string.restype = ctypes.c_char_p
         lib.lisa_abi_version.argtypes = []
@@ -127,6 +132,14 @@ def lisa_forward_stage(stage, Q, K, V, O, B, heads, H, W, d_h, d_v, T, wts, alph
     return int(load().lisa_forward_stage(stage, Q, K, V, O, B, heads, H, W, d_h, d_v, T,
                                          ctypes.byref(wts), alpha, eps, relu_inputs, dtype,
                                          workspace, workspace_bytes, stream))
+
+
+def lisa_forward_noalloc(Q, K, V, O, B, heads, H, W, d_h, d_v, T, wts, alpha, eps, relu_inputs, dtype,
+                         stream) -> int:
+    """lisa_forward for callers that cannot allocate device memory: the
+    library's own fixed scratch array replaces the workspace (see lisa.h)."""
+    return int(load().lisa_forward_noalloc(Q, K, V, O, B, heads, H, W, d_h, d_v, T, ctypes.byref(wts),
+                                           alpha, eps, relu_inputs, dtype, stream))
 
 
 def lisa_forward_host(hQ, hK, hV, hO, dQ, dK, dV, dO, B, heads, H, W, d_h, d_v, T, wts, alpha, eps,

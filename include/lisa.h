@@ -139,6 +139,40 @@ lisa_status lisa_forward_stage(int stage, const void *Q, const void *K, const vo
                                int relu_inputs, int dtype, void *workspace,
                                size_t workspace_bytes, void *stream);
 
+/*
+ * lisa_forward without a workspace argument, for callers that cannot
+ * allocate device memory when they run the layer: work captured into a CUDA
+ * graph in global capture mode (an allocation there breaks the capture), an
+ * operator inside an engine or framework that owns all device memory through
+ * its own planned pool, or a latency-bound loop that cannot take the
+ * device-wide synchronisation of cudaFree.  The paper has no counterpart;
+ * this is a property of the library, not of the method.
+ *
+ * Instead of a caller workspace it uses one scratch array compiled into the
+ * library: LISA_NOALLOC_SCRATCH_BYTES of device memory on every GPU that
+ * loads liblisa.so, held until the process exits.  It calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *   - A problem whose lisa_workspace_bytes(...) exceeds
+ *     LISA_NOALLOC_SCRATCH_BYTES is rejected with LISA_ERR_WORKSPACE before
+ *     anything is launched; use lisa_forward with your own workspace there.
+ *   - The first call on a device looks up the scratch array's device address
+ *     (cudaGetSymbolAddress, with that device current).  Make that first call
+ *     before capturing any stream; later calls do no runtime lookups.  Call
+ *     with the device of `stream` current.
+ *   - Every call on a device shares the one array, and it keeps whatever the
+ *     last call left there.  Nothing in it has to start at zero: each call
+ *     writes every scratch entry it reads.  Calls whose kernels overlap on the
+ *     GPU (different streams, no ordering between them) race on the array and
+ *     give wrong results; order them on one stream, or give each its own
+ *     workspace through lisa_forward.
+ * Other arguments, checks and statuses are those of lisa_forward.
+ */
+#define LISA_NOALLOC_SCRATCH_BYTES (32u << 20)
+lisa_status lisa_forward_noalloc(const void *Q, const void *K, const void *V, void *O, int B,
+                                 int heads, int H, int W, int d_h, int d_v, int T,
+                                 const lisa_weights *wts, const float *alpha, float eps,
+                                 int relu_inputs, int dtype, void *stream);
+
 /* Static, human-readable name of a status code. */
 const char *lisa_status_string(int status);
 
