@@ -252,10 +252,14 @@ STAGE_BYTES_PER_TOKEN = {
     # algorithmic bytes each kernel must move per token*head (bf16, d = 64):
     # what it has to read of Q, K, V and write of O.  Workspace traffic of the
     # split-K partials is per chunk, not per token, and is left out.
-    "stats_kv": 2 * 64 * 2,
-    "stats_kq": 2 * 64 * 2,
+    "stats_kv": 2 * 64 * 2,       # SIMT chain: K, V
+    "stats_kq": 2 * 64 * 2,       # SIMT chain: Q, K
     "recur": 0,
-    "epilogue": 4 * 64 * 2,
+    "epilogue": 4 * 64 * 2,       # Q, K, V in, O out
+    "tc_keysum": 64 * 2,          # tensor-core chain: K
+    "tc_stats": 3 * 64 * 2,       # V, Q, K
+    "tc_recur": 0,
+    "tc_epilogue": 4 * 64 * 2,    # Q, K, V in (halo rows counted once), O out
 }
 
 
@@ -312,7 +316,7 @@ def ours_arm(args, shape):
         if rc != 0:
             raise RuntimeError("lisa_forward: " + lisa.lisa_status_string(rc))
 
-    nstages = lisa.lisa_num_stages(dt, D, T, wmode)
+    nstages = lisa.lisa_num_stages(dt, D, T, wt)
     # warm-up (also loads the kernels before graph capture)
     with torch.cuda.stream(stream):
         for i in range(max(args.warmup, 1)):
@@ -385,7 +389,7 @@ def ours_arm(args, shape):
                     raise RuntimeError("lisa_forward_stage: " + lisa.lisa_status_string(rc))
             evs[i][nstages].record(stream)
     torch.cuda.synchronize(dev)
-    names = [lisa.lisa_stage_name(dt, D, T, wmode, s) for s in range(nstages)]
+    names = [lisa.lisa_stage_name(dt, D, T, wt, s) for s in range(nstages)]
     stage_us = [1e3 * sum(evs[i][s].elapsed_time(evs[i][s + 1]) for i in range(Ks)) / Ks
                 for s in range(nstages)]
     dom = max(range(nstages), key=lambda s: stage_us[s])

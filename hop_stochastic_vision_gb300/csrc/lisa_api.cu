@@ -15,6 +15,7 @@ namespace lisa {
 namespace {
 
 constexpr int kTargetCtas = 2 * 152;  // two resident CTAs on each of the 152 SMs
+constexpr int kTcTargetCtas = 228;     // about 1.5 waves of the 152 SMs
 constexpr int kMinChunk = 64;         // smallest split-K chunk, in tokens
 constexpr size_t kAlign = 256;
 
@@ -31,27 +32,64 @@ bool overlaps(const void *a, size_t an, const void *b, size_t bn) {
 
 }  // namespace
 
-Plan make_plan(int slices, int n, int D, int T, int dtype) {
-    (void)dtype;
+int choose_family(int dtype, int D, int T, int wmode, int hidden) {
+    if (dtype != LISA_BF16 || D != 64) return kFamilySimt;
+    if (wmode == LISA_W_MLP) {
+        // TMEM holds Q [U_1..U_(T-1) | s] (64 (T-1) + 16 columns) and the MLP
+        // hidden layer (hidden rounded up to 16) side by side: 512 columns.
+        const int cols = 64 * (T - 1) + 16 + (hidden + 15) / 16 * 16;
+        if (T < 2 || cols > 512) return kFamilySimt;
+    }
+    return kFamilyTc;
+}
+
+Plan make_plan(int slices, int n, int D, int T, int dtype, int wmode, int hidden) {
     Plan pl{};
-    int chunks = (kTargetCtas + slices - 1) / slices;
-    const int max_chunks = (n + kMinChunk - 1) / kMinChunk;
-    if (chunks > max_chunks) chunks = max_chunks;
-    if (chunks < 1) chunks = 1;
-    int chunk = (n + chunks - 1) / chunks;
-    chunk = (chunk + 15) / 16 * 16;  // whole 16-token MMA steps
-    chunks = (n + chunk - 1) / chunk;
+    pl.family = choose_family(dtype, D, T, wmode, hidden);
+    int chunks, chunk;
+    if (pl.family == kFamilyTc) {
+        // chunks of whole 64-token pipeline stages, about 1.5 waves of CTAs,
+        // and a chunk count a cluster of at most 8 CTAs divides evenly
+        chunks = (kTcTargetCtas + slices - 1) / slices;
+        const int max_chunks = (n + 63) / 64;
+        if (chunks > max_chunks) chunks = max_chunks;
+        if (chunks < 1) chunks = 1;
+        if (chunks > 8) chunks = (chunks + 7) / 8 * 8;
+        chunk = ((n + chunks - 1) / chunks + 63) / 64 * 64;
+        chunks = (n + chunk - 1) / chunk;
+        int cl = 1;
+        for (int d = 8; d >= 1; --d)
+            if (chunks % d == 0) { cl = d; break; }
+        pl.cluster = cl;
+    } else {
+        chunks = (kTargetCtas + slices - 1) / slices;
+        const int max_chunks = (n + kMinChunk - 1) / kMinChunk;
+        if (chunks > max_chunks) chunks = max_chunks;
+        if (chunks < 1) chunks = 1;
+        chunk = (n + chunks - 1) / chunks;
+        chunk = (chunk + 15) / 16 * 16;
+        chunks = (n + chunk - 1) / chunk;
+        pl.cluster = 1;
+    }
     pl.chunks = chunks;
     pl.chunk = chunk;
     const size_t S = (size_t)slices, C = (size_t)chunks, d = (size_t)D;
-    const size_t nmat = (size_t)(T > 1 ? T - 1 : 1);
     size_t off = 0;
+    pl.off_err = off;    off = align_up(off + sizeof(int));
     pl.off_s_part = off; off = align_up(off + S * C * d * sizeof(float));
-    pl.off_u_part = off; off = align_up(off + S * C * d * d * sizeof(float));
-    pl.off_m_part = off; off = align_up(off + S * C * d * d * sizeof(float));
-    pl.off_s_red = off;  off = align_up(off + S * d * sizeof(float));
-    pl.off_ucat = off;   off = align_up(off + S * nmat * d * d * sizeof(float));
-    pl.off_aux = off;    off = align_up(off + S * nmat * d * d * 2 * sizeof(uint16_t));
+    if (pl.family == kFamilySimt) {
+        const size_t nmat = (size_t)(T > 1 ? T - 1 : 1);
+        pl.off_u_part = off; off = align_up(off + S * C * d * d * sizeof(float));
+        pl.off_m_part = off; off = align_up(off + S * C * d * d * sizeof(float));
+        pl.off_s_red = off;  off = align_up(off + S * d * sizeof(float));
+        pl.off_ucat = off;   off = align_up(off + S * nmat * d * d * sizeof(float));
+    } else {
+        const size_t parts = C / (size_t)pl.cluster;
+        const size_t n_umat = (wmode == LISA_W_MLP) ? (size_t)(T - 1) : 1;
+        pl.off_tc_part = off;  off = align_up(off + S * parts * 128 * 64 * sizeof(float));
+        pl.off_tc_bepi = off;  off = align_up(off + S * (64 * n_umat + 16) * 128);
+        pl.off_tc_w1img = off; off = align_up(off + 2 * 64 * 128);
+    }
     pl.total = off;
     return pl;
 }
@@ -82,7 +120,13 @@ extern "C" size_t lisa_workspace_bytes(int B, int heads, int H, int W, int d_h, 
     if (check_sizes(B, heads, H, W, d_h, d_v, T, dtype) != LISA_OK) return 0;
     const long long slices = (long long)B * heads, n = (long long)H * W;
     if (slices == 0 || n == 0) return 0;
-    return make_plan((int)slices, (int)n, d_h, T, dtype).total;
+    // the weight mode is not known here: size for whichever needs more
+    size_t need = make_plan((int)slices, (int)n, d_h, T, dtype, LISA_W_FIXED, 0).total;
+    for (int hidden : {16, LISA_MAX_HIDDEN}) {
+        const size_t m = make_plan((int)slices, (int)n, d_h, T, dtype, LISA_W_MLP, hidden).total;
+        if (m > need) need = m;
+    }
+    return need;
 }
 
 namespace {
@@ -146,7 +190,7 @@ lisa_status prepare(Problem &p, bool &empty, const void *Q, const void *K, const
     if (overlaps(O, bytes, Q, bytes) || overlaps(O, bytes, K, bytes) || overlaps(O, bytes, V, bytes))
         return LISA_ERR_INVALID_ARG;
 
-    const Plan pl = make_plan((int)slices, (int)n, d_h, T, dtype);
+    const Plan pl = make_plan((int)slices, (int)n, d_h, T, dtype, p.wmode, p.hidden);
     if (!workspace || workspace_bytes < pl.total) return LISA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return LISA_ERR_INVALID_ARG;
 
@@ -161,19 +205,32 @@ lisa_status prepare(Problem &p, bool &empty, const void *Q, const void *K, const
     p.dtype = dtype;
     p.chunks = pl.chunks;
     p.chunk = pl.chunk;
+    p.family = pl.family;
+    p.tc_cluster = pl.cluster;
     char *ws = static_cast<char *>(workspace);
+    p.err = reinterpret_cast<int *>(ws + pl.off_err);
     p.s_part = reinterpret_cast<float *>(ws + pl.off_s_part);
-    p.u_part = reinterpret_cast<float *>(ws + pl.off_u_part);
-    p.m_part = reinterpret_cast<float *>(ws + pl.off_m_part);
-    p.s_red = reinterpret_cast<float *>(ws + pl.off_s_red);
-    p.ucat = reinterpret_cast<float *>(ws + pl.off_ucat);
-    p.aux = ws + pl.off_aux;
+    if (pl.family == kFamilySimt) {
+        p.u_part = reinterpret_cast<float *>(ws + pl.off_u_part);
+        p.m_part = reinterpret_cast<float *>(ws + pl.off_m_part);
+        p.s_red = reinterpret_cast<float *>(ws + pl.off_s_red);
+        p.ucat = reinterpret_cast<float *>(ws + pl.off_ucat);
+    } else {
+        p.tc_part = reinterpret_cast<float *>(ws + pl.off_tc_part);
+        p.tc_bepi = reinterpret_cast<uint8_t *>(ws + pl.off_tc_bepi);
+        p.tc_w1img = reinterpret_cast<uint8_t *>(ws + pl.off_tc_w1img);
+    }
     return LISA_OK;
 }
 
 lisa_status launch(const Problem &p, cudaStream_t cs, int stage = -1) {
-    cudaError_t err = launch_simt(p, cs, stage);
+    cudaError_t err = (p.family == kFamilyTc) ? launch_tc(p, cs, stage) : launch_simt(p, cs, stage);
     return err == cudaSuccess ? LISA_OK : LISA_ERR_CUDA;
+}
+
+int weights_mode(const lisa_weights *wts) {
+    if (!wts) return -1;
+    return wts->mode == LISA_W_MLP ? LISA_W_MLP : LISA_W_FIXED;
 }
 
 }  // namespace
@@ -217,14 +274,17 @@ extern "C" lisa_status lisa_forward_host(const void *hQ, const void *hK, const v
     return LISA_OK;
 }
 
-extern "C" int lisa_num_stages(int dtype, int d_h, int T, int wmode) {
-    (void)dtype; (void)d_h; (void)T; (void)wmode;
-    return kSimtStages;
+extern "C" int lisa_num_stages(int dtype, int d_h, int T, const lisa_weights *wts) {
+    if (!wts) return 0;
+    const int fam = choose_family(dtype, d_h, T, weights_mode(wts), wts->hidden);
+    return fam == kFamilyTc ? kTcStages : kSimtStages;
 }
 
-extern "C" const char *lisa_stage_name(int dtype, int d_h, int T, int wmode, int stage) {
-    if (stage < 0 || stage >= lisa_num_stages(dtype, d_h, T, wmode)) return nullptr;
-    return kSimtStageNames[stage];
+extern "C" const char *lisa_stage_name(int dtype, int d_h, int T, const lisa_weights *wts,
+                                       int stage) {
+    if (stage < 0 || stage >= lisa_num_stages(dtype, d_h, T, wts)) return nullptr;
+    const int fam = choose_family(dtype, d_h, T, weights_mode(wts), wts->hidden);
+    return fam == kFamilyTc ? kTcStageNames[stage] : kSimtStageNames[stage];
 }
 
 extern "C" lisa_status lisa_forward_stage(int stage, const void *Q, const void *K, const void *V,
@@ -238,7 +298,7 @@ extern "C" lisa_status lisa_forward_stage(int stage, const void *Q, const void *
     lisa_status st = prepare(p, empty, Q, K, V, O, B, heads, H, W, d_h, d_v, T, wts, alpha, eps,
                              relu_inputs, dtype, workspace, workspace_bytes);
     if (st != LISA_OK) return st;
-    if (stage < 0 || stage >= lisa_num_stages(dtype, d_h, T, wts->mode)) return LISA_ERR_INVALID_ARG;
+    if (stage < 0 || stage >= lisa_num_stages(dtype, d_h, T, wts)) return LISA_ERR_INVALID_ARG;
     if (empty) return LISA_OK;
     return launch(p, static_cast<cudaStream_t>(stream), stage);
 }
@@ -303,7 +363,11 @@ extern "C" lisa_status lisa_forward_noalloc(const void *Q, const void *K, const 
     lisa_status st = check_sizes(B, heads, H, W, d_h, d_v, T, dtype);
     if (st != LISA_OK) return st;
     const long long slices = (long long)B * heads, n = (long long)H * W;
-    const size_t need = (slices == 0 || n == 0) ? 0 : make_plan((int)slices, (int)n, d_h, T, dtype).total;
+    const size_t need = (slices == 0 || n == 0 || !wts)
+                            ? 0
+                            : make_plan((int)slices, (int)n, d_h, T, dtype, weights_mode(wts),
+                                        wts->hidden)
+                                  .total;
     if (need > (size_t)LISA_NOALLOC_SCRATCH_BYTES) return LISA_ERR_WORKSPACE;
     void *scratch = nullptr;
     if (need > 0) {

@@ -34,24 +34,41 @@ struct Problem {
     int chunks;          // C: chunks per slice
     int chunk;           // tokens per chunk (last one may be shorter)
 
-    // workspace views (fp32)
+    int family;          // kFamilySimt / kFamilyTc
+
+    // workspace views
+    int *err;        // error word (bounded device waits that gave up)
     float *s_part;   // [slices][C][D]        partial sum_j K_j
+    // SIMT family
     float *u_part;   // [slices][C][D][D]     partial K^T V
     float *m_part;   // [slices][C][D][D]     partial K^T Q~
     float *s_red;    // [slices][D]           sum_j K_j
     float *ucat;     // [slices][max(T-1,1)][D][D]  U_1..U_(T-1), or [slices][D][D] folded
-    void *aux;       // [slices][...] kernel-family specific (bf16 operand copies)
+    // tensor-core family
+    int tc_cluster;        // CTAs per cluster in the stats kernel (divides chunks)
+    float *tc_part;        // [slices][chunks / cluster][128][64] cluster-reduced [U_1^T ; M^T]
+    uint8_t *tc_bepi;      // [slices][64 * n_umat + 16][128 B] bf16 epilogue operand
+    uint8_t *tc_w1img;     // [2][64][128 B] bf16 MLP first-layer weights
 };
 
+constexpr int kFamilySimt = 0;
+constexpr int kFamilyTc = 1;
+
 struct Plan {
-    int chunks, chunk;
-    size_t off_s_part, off_u_part, off_m_part, off_s_red, off_ucat, off_aux;
+    int family;
+    int chunks, chunk, cluster;
+    size_t off_err, off_s_part, off_u_part, off_m_part, off_s_red, off_ucat;
+    size_t off_tc_part, off_tc_bepi, off_tc_w1img;
     size_t total;
 };
 
+// Which kernel family serves a problem: the tensor-core chain for bf16 with
+// d = 64 (when its TMEM budget holds), the SIMT chain otherwise.
+int choose_family(int dtype, int D, int T, int wmode, int hidden);
+
 // Deterministic split-K plan and workspace carve-up; the same function serves
 // lisa_workspace_bytes and lisa_forward, so the two always agree.
-Plan make_plan(int slices, int n, int D, int T, int dtype);
+Plan make_plan(int slices, int n, int D, int T, int dtype, int wmode, int hidden);
 
 // Kernel families.  Each launches its kernels in order on `stream`; with
 // stage >= 0 it launches only that one (for per-kernel timing).  Returns
@@ -59,5 +76,9 @@ Plan make_plan(int slices, int n, int D, int T, int dtype);
 constexpr int kSimtStages = 4;
 extern const char *const kSimtStageNames[kSimtStages];
 cudaError_t launch_simt(const Problem &p, cudaStream_t stream, int stage);
+
+constexpr int kTcStages = 4;
+extern const char *const kTcStageNames[kTcStages];
+cudaError_t launch_tc(const Problem &p, cudaStream_t stream, int stage);
 
 }  // namespace lisa
