@@ -260,6 +260,7 @@ STAGE_BYTES_PER_TOKEN = {
     "tc_stats": 3 * 64 * 2,       # V, Q, K
     "tc_recur": 0,
     "tc_epilogue": 4 * 64 * 2,    # Q, K, V in (halo rows counted once), O out
+    "tc_stats_fused": 3 * 64 * 2, # V, Q, K (K once: it stays resident)
 }
 
 
@@ -316,7 +317,7 @@ def ours_arm(args, shape):
         if rc != 0:
             raise RuntimeError("lisa_forward: " + lisa.lisa_status_string(rc))
 
-    nstages = lisa.lisa_num_stages(dt, D, T, wt)
+    nstages = lisa.lisa_num_stages(B, heads, shape.H, shape.W, D, T, dt, wt)
     # warm-up (also loads the kernels before graph capture)
     with torch.cuda.stream(stream):
         for i in range(max(args.warmup, 1)):
@@ -389,7 +390,7 @@ def ours_arm(args, shape):
                     raise RuntimeError("lisa_forward_stage: " + lisa.lisa_status_string(rc))
             evs[i][nstages].record(stream)
     torch.cuda.synchronize(dev)
-    names = [lisa.lisa_stage_name(dt, D, T, wt, s) for s in range(nstages)]
+    names = [lisa.lisa_stage_name(B, heads, shape.H, shape.W, D, T, dt, wt, s) for s in range(nstages)]
     stage_us = [1e3 * sum(evs[i][s].elapsed_time(evs[i][s + 1]) for i in range(Ks)) / Ks
                 for s in range(nstages)]
     dom = max(range(nstages), key=lambda s: stage_us[s])

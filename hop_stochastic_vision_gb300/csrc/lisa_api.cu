@@ -274,17 +274,37 @@ extern "C" lisa_status lisa_forward_host(const void *hQ, const void *hK, const v
     return LISA_OK;
 }
 
-extern "C" int lisa_num_stages(int dtype, int d_h, int T, const lisa_weights *wts) {
-    if (!wts) return 0;
-    const int fam = choose_family(dtype, d_h, T, weights_mode(wts), wts->hidden);
-    return fam == kFamilyTc ? kTcStages : kSimtStages;
+namespace {
+
+// Number of kernels and their names for one problem; 0 / NULL for sizes or
+// weights lisa_forward would reject.
+int stage_info(int B, int heads, int H, int W, int d_h, int T, int dtype, const lisa_weights *wts,
+               int stage, const char **name) {
+    if (name) *name = nullptr;
+    if (!wts || check_sizes(B, heads, H, W, d_h, d_h, T, dtype) != LISA_OK) return 0;
+    const long long slices = (long long)B * heads, n = (long long)H * W;
+    if (slices == 0 || n == 0) return 0;
+    const Plan pl = make_plan((int)slices, (int)n, d_h, T, dtype, weights_mode(wts), wts->hidden);
+    if (pl.family == kFamilyTc) {
+        if (name) *name = tc_stage_name(pl.chunks, pl.cluster, pl.chunk, stage);
+        return tc_num_stages(pl.chunks, pl.cluster, pl.chunk);
+    }
+    if (name && stage >= 0 && stage < kSimtStages) *name = kSimtStageNames[stage];
+    return kSimtStages;
 }
 
-extern "C" const char *lisa_stage_name(int dtype, int d_h, int T, const lisa_weights *wts,
-                                       int stage) {
-    if (stage < 0 || stage >= lisa_num_stages(dtype, d_h, T, wts)) return nullptr;
-    const int fam = choose_family(dtype, d_h, T, weights_mode(wts), wts->hidden);
-    return fam == kFamilyTc ? kTcStageNames[stage] : kSimtStageNames[stage];
+}  // namespace
+
+extern "C" int lisa_num_stages(int B, int heads, int H, int W, int d_h, int T, int dtype,
+                               const lisa_weights *wts) {
+    return stage_info(B, heads, H, W, d_h, T, dtype, wts, -1, nullptr);
+}
+
+extern "C" const char *lisa_stage_name(int B, int heads, int H, int W, int d_h, int T, int dtype,
+                                       const lisa_weights *wts, int stage) {
+    const char *name = nullptr;
+    stage_info(B, heads, H, W, d_h, T, dtype, wts, stage, &name);
+    return name;
 }
 
 extern "C" lisa_status lisa_forward_stage(int stage, const void *Q, const void *K, const void *V,
@@ -298,7 +318,8 @@ extern "C" lisa_status lisa_forward_stage(int stage, const void *Q, const void *
     lisa_status st = prepare(p, empty, Q, K, V, O, B, heads, H, W, d_h, d_v, T, wts, alpha, eps,
                              relu_inputs, dtype, workspace, workspace_bytes);
     if (st != LISA_OK) return st;
-    if (stage < 0 || stage >= lisa_num_stages(dtype, d_h, T, wts)) return LISA_ERR_INVALID_ARG;
+    if (stage < 0 || stage >= lisa_num_stages(B, heads, H, W, d_h, T, dtype, wts))
+        return LISA_ERR_INVALID_ARG;
     if (empty) return LISA_OK;
     return launch(p, static_cast<cudaStream_t>(stream), stage);
 }

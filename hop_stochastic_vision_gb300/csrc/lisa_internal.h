@@ -77,8 +77,10 @@ constexpr int kSimtStages = 4;
 extern const char *const kSimtStageNames[kSimtStages];
 cudaError_t launch_simt(const Problem &p, cudaStream_t stream, int stage);
 
-constexpr int kTcStages = 4;
-extern const char *const kTcStageNames[kTcStages];
 cudaError_t launch_tc(const Problem &p, cudaStream_t stream, int stage);
+// The tensor-core chain is 2 kernels when a slice's chunks fit one cluster
+// (fused statistics), else 4.
+int tc_num_stages(int chunks, int cluster, int chunk);
+const char *tc_stage_name(int chunks, int cluster, int chunk, int stage);
 
 }  // namespace lisa

@@ -2,29 +2,39 @@
 // layers with d_h = d_v = 64 on sm_103a.
 //
 // "note" below is the reading note of "LiSA: Linear Stochastic Attention for
-// Long-Range Visual Modeling" (arXiv 2611.04216v2).  Four launches, chained
-// with programmatic dependent launch so each kernel's prologue (TMEM
-// allocation, barrier set-up, TMA prefetch of its own inputs) overlaps the
-// previous kernel's tail:
+// Long-Range Visual Modeling" (arXiv 2611.04216v2).  Per (batch, head)
+// slice the layer needs the key sum s [note §2.2], the statistics
+// U_1 = K^T V and M = K^T Q~ [note §2.3, paper Eq. 8], the recurrence
+// U_k = M U_(k-1), and a per-token epilogue [note §2.4].  Two chains:
 //
-//   1. keysum   s = sum_j K_j, split over token chunks           [note §2.2]
-//   2. stats    per chunk, one tcgen05 MMA chain over the tokens:
-//                 [V | Q~]^T K = [U_1^T ; M^T]   (128 x 64, fp32 in TMEM)
-//               with Q~_j = Q_j / (Q_j . s + eps) formed in shared memory;
-//               the chunks of a thread-block cluster sum their results in
-//               distributed shared memory (fixed order)        [note §2.3]
-//   3. recur    per slice: U_k^T = U_(k-1)^T M^T, fold sum_k w_k U_k^T
-//               (or keep U_1..U_(T-1) for per-token weights), and emit the
-//               epilogue's B operand [U^T rows | s_hi | s_lo] in bf16  [Eq. 8]
-//   4. epilogue per 128-token tile of the grid:
-//               tcgen05: Q [U | s] -> Q U and Q . s (so Q~ U = (Q U)/(Q.s+eps))
-//               and, with adaptive weights, [Q | K] W1^T for the MLP;
-//               mma.sync: the 3x3 local branch on 4x4-token blocks (scores
-//               against the 6x6 key window, masked softmax, weights times V);
-//               then alpha mix and a TMA store                    [note §2.4]
+//  fused (a slice's chunks fit one thread-block cluster, <= 8 CTAs):
+//   1. stats   each CTA streams its token chunk with TMA: its K rows stay
+//              resident in shared memory; the cluster all-reduces s in
+//              distributed shared memory; Q~_j = Q_j / (Q_j.s + eps) is formed
+//              in shared memory and one tcgen05 MMA chain per CTA computes
+//              [V | Q~]^T K = [U_1^T ; M^T] (128 x 64 fp32 in TMEM); the
+//              cluster sums the chunk results (fixed order) and runs the
+//              recurrence U_k^T = U_(k-1)^T M^T on its rows, writing the
+//              epilogue's B operand [sum_k w_k U_k^T | s_hi | s_lo] in bf16.
+//   2. epilogue (below).
 //
-// Shared-memory operands use the 128-byte swizzle that TMA writes: one token
-// row of 64 bf16 is 128 bytes, 8 rows form a 1024-byte atom.
+//  split (longer slices, more chunks than a cluster holds):
+//   1. keysum  s partials;  2. stats  cluster partials of [U_1^T ; M^T];
+//   3. recur   reduction, recurrence and B operand;  4. epilogue.
+//
+//  epilogue: persistent CTAs walk 128-token tiles of the grid (2 x 8-token
+//   blocks), double-buffering the TMA loads of the next tile.  tcgen05 forms
+//   Q [U | s] (and [Q | K] W1^T for per-token weights) in TMEM; each warp runs
+//   the 3x3 local branch of one 2 x 8 block on the legacy mma.sync path
+//   (scores against the 4 x 10 key window, masked softmax, weights times V)
+//   and reads the block's TMEM rows straight into the same fragment layout
+//   (tcgen05.ld 16x256b), so the alpha mix happens in registers; TMA stores
+//   the tile.
+//
+// Kernels are chained with programmatic dependent launch: each one's
+// prologue and input prefetch overlap the previous kernel's tail.  Shared-
+// memory operands use the 128-byte swizzle TMA writes (a 64-bf16 token row is
+// 128 bytes; 8 rows form a 1024-byte atom).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -40,16 +50,16 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kD = 64;             // head width of this family
-constexpr int kRow = 128;          // bytes of one token row (64 bf16)
-constexpr int kSub = 64;           // tokens per stats pipeline stage
-constexpr int kStages = 3;         // stats pipeline depth
-constexpr int kStageBytes = 3 * kSub * kRow;   // V | Q~ | K
-constexpr int kRecurRowBlocks = 4; // recur CTAs per slice (16 rows of U^T each)
-constexpr int kRedStride = 68;     // fp32 row stride of the cluster-reduction buffer
-constexpr int kXStride = 68;       // fp32 row stride of the epilogue exchange buffer
+constexpr int kD = 64;                         // head width of this family
+constexpr int kRow = 128;                      // bytes of one token row (64 bf16)
+constexpr int kSub = 64;                       // tokens per stats pipeline stage
+constexpr int kSubBytes = kSub * kRow;         // 8 KB
+constexpr int kStages = 3;                     // stats pipeline depth
+constexpr int kRecurRowBlocks = 4;             // split recur: CTAs per slice
+constexpr int kRedStride = 68;                 // fp32 row stride of reduction buffers
+constexpr int kFusedMaxSub = 7;                // fused stats: resident K chunk <= 448 tokens
+constexpr int kFusedWork = 72 * 1024;          // fused stats: minimum work area
 
-// error word bits
 constexpr int kErrTimeoutLoad = 1;
 constexpr int kErrTimeoutMma = 2;
 
@@ -60,11 +70,13 @@ struct TcParams {
     float w[LISA_MAX_T];
     const float *W1, *b1, *W2, *b2;
     const void *K;
-    int chunks, chunk, cl, parts;    // split-K plan; cluster size; partials per slice
-    int th, tw, tiles_r, tiles_c;    // epilogue tile (th x tw = 128 tokens)
-    int n_umat, epi_rows, n_mlp;     // epilogue B operand: U blocks, rows, MLP width (x16)
-    float *s_part;                   // [S][C][64]
-    float *part;                     // [S][P][128][64]
+    int chunks, chunk, cl, parts;    // split-K plan; cluster size; cluster partials per slice
+    int BR, BC;                      // epilogue tile = BR x BC blocks of 2 x 8 tokens
+    int tiles_r, tiles_c, tiles;     // tiles per slice (rows, cols), total tiles
+    int epi_stages;                  // epilogue input buffers (1 or 2)
+    int n_umat, epi_rows, n_mlp;     // B operand: U blocks, rows, MLP width (multiple of 16)
+    float *s_part;                   // [S][C][64] (split chain)
+    float *part;                     // [S][P][128][64] (split chain)
     uint8_t *bepi;                   // [S][epi_rows][128] bf16, 128-B swizzled rows
     uint8_t *w1img;                  // [2][n_mlp][128] bf16 (W1 q-part | k-part), swizzled
     int *err;
@@ -74,8 +86,7 @@ __device__ __forceinline__ void record_error(int *err, int bits) { atomicOr(err,
 
 __device__ __forceinline__ uint32_t relu2(uint32_t v) {
     __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162 *>(&v);
-    __nv_bfloat162 z = __float2bfloat162_rn(0.f);
-    x = __hmax2(x, z);
+    x = __hmax2(x, __float2bfloat162_rn(0.f));
     return *reinterpret_cast<uint32_t *>(&x);
 }
 __device__ __forceinline__ uint4 relu4(uint4 v) {
@@ -87,8 +98,415 @@ __device__ __forceinline__ void relu_smem(uint8_t *p, int bytes, int tid, int nt
     for (int i = tid; i < bytes / 16; i += nthreads) v[i] = relu4(v[i]);
 }
 
+// Writes one 64-element fp32 row as bf16 into a 128-B-swizzled row image.
+__device__ __forceinline__ void put_row_bf16(uint8_t *img, int row, const float *v, int chunk) {
+    uint4 o;
+    o.x = pack_bf16(v[0], v[1]);
+    o.y = pack_bf16(v[2], v[3]);
+    o.z = pack_bf16(v[4], v[5]);
+    o.w = pack_bf16(v[6], v[7]);
+    *reinterpret_cast<uint4 *>(img + (size_t)row * kRow + ((chunk ^ (row & 7)) << 4)) = o;
+}
+
+// ------------------------------------------------------------------ clusters
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t map_rank(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+// Remote shared-memory loads.  Volatile keeps them after the cluster barrier
+// that precedes them; no memory clobber, so a run of them can be in flight
+// together.
+__device__ __forceinline__ float4 ld_dsmem4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ float ld_dsmem(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
+}
+
+// Sum of one float4 over the CL <= 8 CTAs of the cluster, rank order 0..CL-1;
+// all remote loads are issued before the first add.
+__device__ __forceinline__ float4 cluster_sum4(uint32_t local_addr, int CL) {
+    float4 v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        if (q < CL) v[q] = ld_dsmem4(map_rank(local_addr, (uint32_t)q));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        if (q < CL) {
+            acc.x += v[q].x; acc.y += v[q].y; acc.z += v[q].z; acc.w += v[q].w;
+        }
+    return acc;
+}
+
+// U_next[i][a] = sum_b U[i][b] Mt[b][a] for `rows` rows (fp32, row stride 64),
+// four outputs of one row per work item.
+__device__ __forceinline__ void rows_times_mt(const float *U, const float *Mt, float *Un, int rows,
+                                              int tid, int nthreads) {
+    for (int item = tid; item < rows * 16; item += nthreads) {
+        const int i = item >> 4, a0 = item & 15;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+        for (int b = 0; b < 64; ++b) {
+            const float u = U[i * 64 + b];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) acc[k] = fmaf(u, Mt[b * 64 + a0 + 16 * k], acc[k]);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) Un[i * 64 + a0 + 16 * k] = acc[k];
+    }
+}
+
+// ------------------------------------------------------- shared stats steps
+// Q~_j = Q_j / (Q_j . s + eps) in place for the 64 tokens of a stage (128
+// threads, two per token, 32 features each); ReLU on load when asked.
+__device__ __forceinline__ void form_qtilde(uint8_t *Qb, const float *s, float eps, int relu,
+                                            int tid) {
+    const int j = tid >> 1, h = tid & 1;
+    uint4 q[4];
+    float dot = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int chunk = 4 * h + k;
+        q[k] = *reinterpret_cast<uint4 *>(Qb + sw128_offset(j, chunk));
+        if (relu) q[k] = relu4(q[k]);
+        const uint32_t w4[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            dot = fmaf(bf16_lo(w4[e]), s[chunk * 8 + 2 * e], dot);
+            dot = fmaf(bf16_hi(w4[e]), s[chunk * 8 + 2 * e + 1], dot);
+        }
+    }
+    dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+    const float r = 1.f / (dot + eps);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t w4[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
+        uint4 o;
+        o.x = pack_bf16(bf16_lo(w4[0]) * r, bf16_hi(w4[0]) * r);
+        o.y = pack_bf16(bf16_lo(w4[1]) * r, bf16_hi(w4[1]) * r);
+        o.z = pack_bf16(bf16_lo(w4[2]) * r, bf16_hi(w4[2]) * r);
+        o.w = pack_bf16(bf16_lo(w4[3]) * r, bf16_hi(w4[3]) * r);
+        *reinterpret_cast<uint4 *>(Qb + sw128_offset(j, 4 * h + k)) = o;
+    }
+}
+
+// TMEM [128 x 64] fp32 -> shared rows of kRedStride floats (thread = row).
+__device__ __forceinline__ void tmem_rows_to_smem(uint32_t tmem, float *red, int warp, int lane) {
+    const int row = 32 * warp + lane;
+#pragma unroll
+    for (int cb = 0; cb < 64; cb += 16) {
+        uint32_t r[16];
+        tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + cb, r);
+        tc_wait_ld();
+        float4 *dst = reinterpret_cast<float4 *>(red + row * kRedStride + cb);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            dst[k] = make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
+                                 __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
+    }
+}
+
+// B-operand rows of the s term: n_umat*64 + {0: s_hi, 1: s_lo, 2..15: 0}.
+__device__ __forceinline__ void put_s_rows(uint8_t *img, int row0, const float *s, int tid) {
+    if (tid < 128) {
+        const int r16 = tid >> 3, chunk = tid & 7;
+        float v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float x = s[chunk * 8 + e];
+            const float hi = __bfloat162float(__float2bfloat16_rn(x));
+            v[e] = r16 == 0 ? hi : (r16 == 1 ? x - hi : 0.f);
+        }
+        put_row_bf16(img, row0 + r16, v, chunk);
+    }
+}
+
+// W1 [hidden][128] -> two K-major bf16 images [n_mlp rows][64]: q-part, k-part.
+__device__ __forceinline__ void put_w1_image(const TcParams &p, int tid, int nthreads) {
+    for (int idx = tid; idx < 2 * p.n_mlp * 8; idx += nthreads) {
+        const int half = idx / (p.n_mlp * 8), rem = idx % (p.n_mlp * 8);
+        const int m = rem >> 3, chunk = rem & 7;
+        float v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            v[e] = m < p.hidden ? p.W1[(size_t)m * 2 * kD + half * kD + chunk * 8 + e] : 0.f;
+        put_row_bf16(p.w1img + (size_t)half * p.n_mlp * kRow, m, v, chunk);
+    }
+}
+
 // ===========================================================================
-// 1. keysum: partial s over a chunk of tokens (ReLU applied), fp32.
+// fused stats: s, [U_1^T ; M^T] and the recurrence for one slice per cluster
+// ===========================================================================
+__device__ __forceinline__ void named_sync_compute() {
+    asm volatile("bar.sync 1, 128;" ::: "memory");   // the four compute warps only
+}
+// Barrier of the four compute warps that also ANDs a flag over them, so every
+// thread takes the same branch after it.
+__device__ __forceinline__ bool named_sync_and(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.and.pred q, 1, 128, p;\nselp.u32 %0, 1, 0, q;\n}"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
+
+// Threads: warps 0-3 compute (prep, MMA issue, reductions), warp 4 produces
+// the TMA loads and refills each ring stage as soon as its MMA completed.
+constexpr int kStatsThreads = 160;
+
+__global__ void __launch_bounds__(kStatsThreads) tc_stats_fused_kernel(const __grid_constant__ CUtensorMap mQ,
+                                                                       const __grid_constant__ CUtensorMap mK,
+                                                                       const __grid_constant__ CUtensorMap mV,
+                                                                       TcParams p, int kres_bytes) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ __align__(8) uint64_t kbar, full_bar[kStages], empty_bar[kStages], done_bar;
+    __shared__ uint32_t tmem_slot;
+    __shared__ float s_loc[kD];
+    __shared__ float s_sh[kD];
+    __shared__ float s_red[16][kD + 1];
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int sl = blockIdx.x / p.chunks, c = blockIdx.x % p.chunks;
+    const uint32_t rank = cluster_rank();
+    const int CL = p.cl;
+    const int t0 = c * p.chunk;
+    const int ntok = max(0, min(p.n, t0 + p.chunk) - t0);
+    const int nsub = (ntok + kSub - 1) / kSub;
+    const uint32_t base = smem_u32(sm);
+    uint8_t *kres = sm;                                  // resident K rows of the chunk
+    uint8_t *ring = sm + kres_bytes;                     // V | Q stages
+    const uint32_t ring_addr = base + kres_bytes;
+    constexpr int kStage = 2 * kSubBytes;
+
+    if (tid == 0) {
+        mbar_init(smem_u32(&kbar), 1);
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(smem_u32(&full_bar[i]), 1);
+            mbar_init(smem_u32(&empty_bar[i]), 1);
+        }
+        mbar_init(smem_u32(&done_bar), 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(smem_u32(&tmem_slot), 64);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    if (blockIdx.x == 0 && tid == 0) *p.err = 0;
+    pdl_launch_dependents();
+    bool ok = true;
+
+    if (warp == 4) {
+        // ---------------- producer
+        if (lane == 0) {
+            mbar_arrive_expect_tx(smem_u32(&kbar), nsub * kSubBytes);
+            for (int i = 0; i < nsub; ++i)
+                tma_load_3d(base + i * kSubBytes, &mK, 0, t0 + i * kSub, sl, smem_u32(&kbar));
+            for (int i = 0; i < kStages && i < nsub; ++i) {
+                const uint32_t fb = smem_u32(&full_bar[i]);
+                mbar_arrive_expect_tx(fb, kStage);
+                tma_load_3d(ring_addr + i * kStage, &mV, 0, t0 + i * kSub, sl, fb);
+                tma_load_3d(ring_addr + i * kStage + kSubBytes, &mQ, 0, t0 + i * kSub, sl, fb);
+            }
+        }
+        __syncwarp();
+        cluster_sync();                                  // (A) s exchange
+        if (lane == 0) {
+            for (int i = kStages; i < nsub; ++i) {
+                const int st = i % kStages;
+                // the MMA of sub-chunk i - kStages must have read the stage
+                if (!mbar_wait(smem_u32(&empty_bar[st]), ((i - kStages) / kStages) & 1)) {
+                    record_error(p.err, kErrTimeoutMma);
+                    break;
+                }
+                const uint32_t fb = smem_u32(&full_bar[st]);
+                mbar_arrive_expect_tx(fb, kStage);
+                tma_load_3d(ring_addr + st * kStage, &mV, 0, t0 + i * kSub, sl, fb);
+                tma_load_3d(ring_addr + st * kStage + kSubBytes, &mQ, 0, t0 + i * kSub, sl, fb);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------- key sum (ReLU in place), then cluster all-reduce
+        if (!mbar_wait(smem_u32(&kbar), 0)) {
+            record_error(p.err, kErrTimeoutLoad);
+            ok = false;
+        }
+        {
+            const int cg = tid & 7, jl = tid >> 3;   // 16 token lanes x 8 feature chunks
+            float acc[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+            for (int j = jl; j < nsub * kSub; j += 16) {
+                uint4 *ptr = reinterpret_cast<uint4 *>(kres + sw128_offset(j, cg));
+                uint4 v = *ptr;
+                if (p.relu) {
+                    v = relu4(v);
+                    *ptr = v;
+                }
+                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    acc[2 * e] += bf16_lo(w4[e]);
+                    acc[2 * e + 1] += bf16_hi(w4[e]);
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) s_red[jl][cg * 8 + e] = acc[e];
+        }
+        named_sync_compute();
+        if (tid < kD) {
+            float s = 0.f;
+            for (int r = 0; r < 16; ++r) s += s_red[r][tid];
+            s_loc[tid] = s;
+        }
+        fence_proxy_async();      // K's ReLU (generic proxy) before the MMAs read it
+        cluster_sync();           // (A)
+        if (tid < kD) {
+            const uint32_t a = smem_u32(&s_loc[tid]);
+            float v[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (q < CL) v[q] = ld_dsmem(map_rank(a, (uint32_t)q));
+            float s = 0.f;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (q < CL) s += v[q];
+            s_sh[tid] = s;
+        }
+        named_sync_compute();
+
+        // ---------------- [V | Q~]^T K over the chunk on tcgen05
+        constexpr uint32_t idesc = make_idesc_bf16(128, 64, true, true);
+        ok = named_sync_and(ok);
+        for (int i = 0; i < nsub && ok; ++i) {
+            const int st = i % kStages;
+            if (!mbar_wait(smem_u32(&full_bar[st]), (i / kStages) & 1)) {
+                record_error(p.err, kErrTimeoutLoad);
+                ok = false;
+            }
+            if (!named_sync_and(ok)) break;
+            form_qtilde(ring + st * kStage + kSubBytes, s_sh, p.eps, p.relu, tid);
+            fence_proxy_async();
+            named_sync_compute();
+            if (tid == 0) {
+                tc_fence_after();
+                const uint32_t vaddr = ring_addr + st * kStage;
+                const uint32_t kaddr = base + i * kSubBytes;
+#pragma unroll
+                for (int ks = 0; ks < kSub / 16; ++ks) {
+                    const uint64_t ad = make_desc_sw128(vaddr + ks * 2048, kSubBytes, 1024);
+                    const uint64_t bd = make_desc_sw128(kaddr + ks * 2048, 1024, 1024);
+                    tc_mma(tmem, ad, bd, idesc, (i | ks) != 0);
+                }
+                tc_commit(smem_u32(&empty_bar[st]));
+            }
+        }
+        if (tid == 0) tc_commit(smem_u32(&done_bar));
+        if (!mbar_wait(smem_u32(&done_bar), 0)) record_error(p.err, kErrTimeoutMma);
+        tc_fence_after();
+    }
+
+    // ---- cluster reduction: rank q sums rows q, q + CL, ... (fixed order)
+    float *red = reinterpret_cast<float *>(sm);                    // [128][68]
+    float *redsum = reinterpret_cast<float *>(sm + 36 * 1024);     // [128][64] own rows
+    if (warp < 4) tmem_rows_to_smem(tmem, red, warp, lane);
+    tc_fence_before();
+    cluster_sync();                                                // (B)
+    const uint32_t red_addr = smem_u32(red);
+    const int my_rows = (128 - (int)rank + CL - 1) / CL;
+    for (int item = tid; item < my_rows * 16; item += kStatsThreads) {
+        const int rr = (int)rank + CL * (item >> 4);
+        const int f = item & 15;
+        const uint32_t off = (uint32_t)(rr * kRedStride + 4 * f) * 4u;
+        reinterpret_cast<float4 *>(redsum + rr * kD)[f] = cluster_sum4(red_addr + off, CL);
+    }
+    cluster_sync();                                                // (C)
+
+    // ---- M^T (rows 64..127) gathered from their owners; own U_1^T rows
+    float *Mt = reinterpret_cast<float *>(sm);                     // [64][64]
+    float *Ucur = reinterpret_cast<float *>(sm + 16 * 1024);       // [my_u][64]
+    const int my_u = (64 - (int)rank + CL - 1) / CL;               // own rows e < 64
+    const uint32_t redsum_addr = smem_u32(redsum);
+    if (tid < 128) {
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {          // 1024 float4 of M^T, 8 per thread
+            const int item = tid + 128 * u;
+            const int rr = 64 + (item >> 4);
+            const uint32_t off = (uint32_t)(rr * kD + 4 * (item & 15)) * 4u;
+            v[u] = ld_dsmem4(map_rank(redsum_addr + off, (uint32_t)(rr % CL)));
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int item = tid + 128 * u;
+            reinterpret_cast<float4 *>(Mt + (item >> 4) * kD)[item & 15] = v[u];
+        }
+    }
+    for (int item = tid; item < my_u * 16; item += kStatsThreads) {
+        const int i = item >> 4, f = item & 15;
+        const int e = (int)rank + CL * i;
+        reinterpret_cast<float4 *>(Ucur + i * kD)[f] = reinterpret_cast<const float4 *>(redsum + e * kD)[f];
+    }
+    cluster_sync();   // (D) every CTA is done reading the others' redsum
+
+    // ---- U_k^T = U_(k-1)^T M^T on the own rows; B operand rows
+    float *Unext = reinterpret_cast<float *>(sm + 36 * 1024);
+    float *Fold = reinterpret_cast<float *>(sm + 52 * 1024);
+    const bool folded = (p.wmode != LISA_W_MLP);
+    uint8_t *img = p.bepi + (size_t)sl * p.epi_rows * kRow;
+    for (int idx = tid; idx < my_u * kD; idx += kStatsThreads) Fold[idx] = 0.f;
+    __syncthreads();
+    for (int k = 1; k < p.T; ++k) {
+        if (k > 1) {
+            rows_times_mt(Ucur, Mt, Unext, my_u, tid, kStatsThreads);
+            __syncthreads();
+            for (int idx = tid; idx < my_u * kD; idx += kStatsThreads) Ucur[idx] = Unext[idx];
+            __syncthreads();
+        }
+        if (folded) {
+            for (int idx = tid; idx < my_u * kD; idx += kStatsThreads) Fold[idx] = fmaf(p.w[k], Ucur[idx], Fold[idx]);
+        } else {
+            for (int item = tid; item < my_u * 8; item += kStatsThreads) {
+                const int i = item >> 3, chunk = item & 7;
+                put_row_bf16(img, (k - 1) * kD + (int)rank + CL * i, Ucur + i * kD + chunk * 8, chunk);
+            }
+        }
+        __syncthreads();
+    }
+    if (folded)
+        for (int item = tid; item < my_u * 8; item += kStatsThreads) {
+            const int i = item >> 3, chunk = item & 7;
+            put_row_bf16(img, (int)rank + CL * i, Fold + i * kD + chunk * 8, chunk);
+        }
+    if (rank == 0) put_s_rows(img, p.n_umat * kD, s_sh, tid);
+    if (!folded && sl == 0 && rank == 0) put_w1_image(p, tid, kStatsThreads);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 64);
+}
+
+// ===========================================================================
+// split chain: keysum, stats (cluster partials), recur
 // ===========================================================================
 __global__ void __launch_bounds__(256) tc_keysum_kernel(TcParams p) {
     __shared__ float red[32][kD + 1];
@@ -102,12 +520,12 @@ __global__ void __launch_bounds__(256) tc_keysum_kernel(TcParams p) {
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = 0.f;
     int j = t0 + j0;
-    for (; j + 96 < t1; j += 128) {
-        uint4 v[4];
+    for (; j + 224 < t1; j += 256) {
+        uint4 v[8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) v[u] = __ldg(K + (size_t)(j + 32 * u) * 8 + cg);
+        for (int u = 0; u < 8; ++u) v[u] = __ldg(K + (size_t)(j + 32 * u) * 8 + cg);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < 8; ++u) {
             const uint4 x = p.relu ? relu4(v[u]) : v[u];
             const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
@@ -137,49 +555,25 @@ __global__ void __launch_bounds__(256) tc_keysum_kernel(TcParams p) {
     }
 }
 
-// ===========================================================================
-// 2. stats: [U_1^T ; M^T] of a chunk on tcgen05, cluster-reduced.
-// ===========================================================================
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ uint32_t map_rank(uint32_t saddr, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-    return r;
-}
-__device__ __forceinline__ float4 ld_dsmem4(uint32_t addr) {
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(addr)
-                 : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void stats_issue_loads(const CUtensorMap *mQ, const CUtensorMap *mK,
+__device__ __forceinline__ void split_issue_loads(const CUtensorMap *mQ, const CUtensorMap *mK,
                                                   const CUtensorMap *mV, uint32_t stage_base,
                                                   uint32_t bar, int tok, int sl) {
-    mbar_arrive_expect_tx(bar, kStageBytes);
+    mbar_arrive_expect_tx(bar, 3 * kSubBytes);
     tma_load_3d(stage_base, mV, 0, tok, sl, bar);
-    tma_load_3d(stage_base + kSub * kRow, mQ, 0, tok, sl, bar);
-    tma_load_3d(stage_base + 2 * kSub * kRow, mK, 0, tok, sl, bar);
+    tma_load_3d(stage_base + kSubBytes, mQ, 0, tok, sl, bar);
+    tma_load_3d(stage_base + 2 * kSubBytes, mK, 0, tok, sl, bar);
 }
 
-__global__ void __launch_bounds__(128) tc_stats_kernel(const __grid_constant__ CUtensorMap mQ,
-                                                       const __grid_constant__ CUtensorMap mK,
-                                                       const __grid_constant__ CUtensorMap mV,
-                                                       TcParams p) {
+__global__ void __launch_bounds__(kStatsThreads) tc_stats_split_kernel(const __grid_constant__ CUtensorMap mQ,
+                                                                       const __grid_constant__ CUtensorMap mK,
+                                                                       const __grid_constant__ CUtensorMap mV,
+                                                                       TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], done_bar;
     __shared__ uint32_t tmem_slot;
     __shared__ float s_sh[kD];
+    constexpr int kStage = 3 * kSubBytes;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int sl = blockIdx.x / p.chunks, c = blockIdx.x % p.chunks;
@@ -203,179 +597,126 @@ __global__ void __launch_bounds__(128) tc_stats_kernel(const __grid_constant__ C
     const uint32_t tmem = tmem_slot;
     pdl_launch_dependents();
 
-    // Inputs do not depend on the previous kernel: start streaming them now.
-    if (tid == 0)
-        for (int i = 0; i < kStages && i < nsub; ++i)
-            stats_issue_loads(&mQ, &mK, &mV, base + i * kStageBytes, smem_u32(&full_bar[i]),
-                              t0 + i * kSub, sl);
-    pdl_wait();  // s partials are complete
+    if (warp == 4) {
+        // ---------------- producer: inputs do not depend on the earlier kernels
+        if (lane == 0) {
+            for (int i = 0; i < nsub; ++i) {
+                const int st = i % kStages;
+                if (i >= kStages && !mbar_wait(smem_u32(&empty_bar[st]), ((i - kStages) / kStages) & 1)) {
+                    record_error(p.err, kErrTimeoutMma);
+                    break;
+                }
+                split_issue_loads(&mQ, &mK, &mV, base + st * kStage, smem_u32(&full_bar[st]), t0 + i * kSub, sl);
+            }
+        }
+        __syncwarp();
+    } else {
+        pdl_wait();  // s partials are complete
+        if (tid < kD) {
+            float s = 0.f;
+            for (int cc = 0; cc < p.chunks; ++cc) s += p.s_part[((size_t)sl * p.chunks + cc) * kD + tid];
+            s_sh[tid] = s;
+        }
+        named_sync_compute();
+        constexpr uint32_t idesc = make_idesc_bf16(128, 64, true, true);
+        bool ok = true;
+        for (int i = 0; i < nsub; ++i) {
+            const int st = i % kStages;
+            if (!mbar_wait(smem_u32(&full_bar[st]), (i / kStages) & 1)) {
+                record_error(p.err, kErrTimeoutLoad);
+                ok = false;
+            }
+            if (!named_sync_and(ok)) break;
+            uint8_t *Vb = sm + st * kStage;
+            if (p.relu) relu_smem(Vb + 2 * kSubBytes, kSubBytes, tid, 128);
+            form_qtilde(Vb + kSubBytes, s_sh, p.eps, p.relu, tid);
+            fence_proxy_async();
+            named_sync_compute();
+            if (tid == 0) {
+                tc_fence_after();
+                const uint32_t vaddr = base + st * kStage;
+                const uint32_t kaddr = vaddr + 2 * kSubBytes;
+#pragma unroll
+                for (int ks = 0; ks < kSub / 16; ++ks) {
+                    const uint64_t ad = make_desc_sw128(vaddr + ks * 2048, kSubBytes, 1024);
+                    const uint64_t bd = make_desc_sw128(kaddr + ks * 2048, 1024, 1024);
+                    tc_mma(tmem, ad, bd, idesc, (i | ks) != 0);
+                }
+                tc_commit(smem_u32(&empty_bar[st]));
+            }
+        }
+        if (tid == 0) tc_commit(smem_u32(&done_bar));
+        if (!mbar_wait(smem_u32(&done_bar), 0)) record_error(p.err, kErrTimeoutMma);
+        tc_fence_after();
+    }
+
+    float *red = reinterpret_cast<float *>(sm);
+    if (warp < 4) tmem_rows_to_smem(tmem, red, warp, lane);
+    tc_fence_before();
+    cluster_sync();
+    const uint32_t rank = cluster_rank();
+    const int CL = p.cl;
+    float *out = p.part + ((size_t)sl * p.parts + c / CL) * 128 * kD;
+    const int my_rows = (128 - (int)rank + CL - 1) / CL;
+    const uint32_t red_addr = smem_u32(red);
+    for (int item = tid; item < my_rows * 16; item += kStatsThreads) {
+        const int rr = (int)rank + CL * (item >> 4);
+        const int f = item & 15;
+        const uint32_t off = (uint32_t)(rr * kRedStride + 4 * f) * 4u;
+        reinterpret_cast<float4 *>(out + rr * kD)[f] = cluster_sum4(red_addr + off, CL);
+    }
+    cluster_sync();
+    if (warp == 0) tmem_dealloc(tmem, 64);
+}
+
+__global__ void __launch_bounds__(256) tc_recur_kernel(TcParams p) {
+    __shared__ __align__(16) float Mt[kD][kD];     // M^T [b][a]
+    __shared__ __align__(16) float Ut[16][kD];     // this CTA's 16 rows of U_k^T
+    __shared__ __align__(16) float Un[16][kD];
+    __shared__ __align__(16) float Fold[16][kD];
+    __shared__ float s_sh[kD];
+    const int tid = threadIdx.x;
+    const int sl = blockIdx.x / kRecurRowBlocks, rb = blockIdx.x % kRecurRowBlocks;
+    pdl_launch_dependents();
+    pdl_wait();
+    const float4 *part = reinterpret_cast<const float4 *>(p.part + (size_t)sl * p.parts * 128 * kD);
+    // M^T: 1024 float4, 4 per thread; each partial's loads issued before the sums
+    {
+        float4 acc[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q = 0; q < p.parts; ++q) {
+            float4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v[u] = part[((size_t)q * 128 + kD) * 16 + tid + 256 * u];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                acc[u].x += v[u].x; acc[u].y += v[u].y; acc[u].z += v[u].z; acc[u].w += v[u].w;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) reinterpret_cast<float4 *>(&Mt[0][0])[tid + 256 * u] = acc[u];
+    }
+    {   // own 16 rows of U_1^T: 256 float4, one per thread
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q = 0; q < p.parts; ++q) {
+            const float4 v = part[((size_t)q * 128 + 16 * rb) * 16 + tid];
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+        reinterpret_cast<float4 *>(&Ut[0][0])[tid] = acc;
+        reinterpret_cast<float4 *>(&Fold[0][0])[tid] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     if (tid < kD) {
         float s = 0.f;
         for (int cc = 0; cc < p.chunks; ++cc) s += p.s_part[((size_t)sl * p.chunks + cc) * kD + tid];
         s_sh[tid] = s;
     }
     __syncthreads();
-
-    constexpr uint32_t idesc = make_idesc_bf16(128, 64, true, true);
-    bool ok = true;
-    for (int i = 0; i < nsub; ++i) {
-        const int st = i % kStages;
-        const uint32_t ph = (i / kStages) & 1;
-        if (!mbar_wait(smem_u32(&full_bar[st]), ph)) {
-            record_error(p.err, kErrTimeoutLoad);
-            ok = false;
-        }
-        if (!__syncthreads_and(ok)) break;
-        uint8_t *Vb = sm + st * kStageBytes;
-        uint8_t *Qb = Vb + kSub * kRow;
-        uint8_t *Kb = Qb + kSub * kRow;
-        if (p.relu) relu_smem(Kb, kSub * kRow, tid, 128);
-        {   // Q~_j = Q_j / (Q_j . s + eps): two threads per token, 32 features each
-            const int j = tid >> 1, h = tid & 1;
-            uint4 q[4];
-            float dot = 0.f;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int chunk = 4 * h + k;
-                q[k] = *reinterpret_cast<uint4 *>(Qb + sw128_offset(j, chunk));
-                if (p.relu) q[k] = relu4(q[k]);
-                const uint32_t w4[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    dot = fmaf(bf16_lo(w4[e]), s_sh[chunk * 8 + 2 * e], dot);
-                    dot = fmaf(bf16_hi(w4[e]), s_sh[chunk * 8 + 2 * e + 1], dot);
-                }
-            }
-            dot += __shfl_xor_sync(0xffffffffu, dot, 1);
-            const float r = 1.f / (dot + p.eps);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint32_t w4[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
-                uint4 o;
-                o.x = pack_bf16(bf16_lo(w4[0]) * r, bf16_hi(w4[0]) * r);
-                o.y = pack_bf16(bf16_lo(w4[1]) * r, bf16_hi(w4[1]) * r);
-                o.z = pack_bf16(bf16_lo(w4[2]) * r, bf16_hi(w4[2]) * r);
-                o.w = pack_bf16(bf16_lo(w4[3]) * r, bf16_hi(w4[3]) * r);
-                *reinterpret_cast<uint4 *>(Qb + sw128_offset(j, 4 * h + k)) = o;
-            }
-        }
-        fence_proxy_async();
-        __syncthreads();
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t vaddr = base + st * kStageBytes;
-            const uint32_t kaddr = vaddr + 2 * kSub * kRow;
-#pragma unroll
-            for (int ks = 0; ks < kSub / 16; ++ks) {
-                const uint64_t ad = make_desc_sw128(vaddr + ks * 2048, kSub * kRow, 1024);
-                const uint64_t bd = make_desc_sw128(kaddr + ks * 2048, 1024, 1024);
-                tc_mma(tmem, ad, bd, idesc, (i | ks) != 0);
-            }
-            tc_commit(smem_u32(&empty_bar[st]));
-            // refill the stage the previous sub-chunk used
-            const int prev = i - 1, nxt = prev + kStages;
-            if (prev >= 0 && nxt < nsub) {
-                const int pst = prev % kStages;
-                if (!mbar_wait(smem_u32(&empty_bar[pst]), (prev / kStages) & 1)) {
-                    record_error(p.err, kErrTimeoutMma);
-                } else {
-                    stats_issue_loads(&mQ, &mK, &mV, base + pst * kStageBytes,
-                                      smem_u32(&full_bar[pst]), t0 + nxt * kSub, sl);
-                }
-            }
-        }
-    }
-    if (tid == 0) tc_commit(smem_u32(&done_bar));
-    if (!mbar_wait(smem_u32(&done_bar), 0)) record_error(p.err, kErrTimeoutMma);
-    tc_fence_after();
-
-    // TMEM -> shared: thread owns row 32*warp + lane of the 128 x 64 result
-    float *red = reinterpret_cast<float *>(sm);
-    const int row = 32 * warp + lane;
-#pragma unroll
-    for (int cb = 0; cb < 64; cb += 16) {
-        uint32_t r[16];
-        tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + cb, r);
-        tc_wait_ld();
-        float4 *dst = reinterpret_cast<float4 *>(red + row * kRedStride + cb);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-            dst[k] = make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
-                                 __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
-    }
-    tc_fence_before();
-    cluster_sync();
-
-    // rank q of the cluster sums rows q, q + CL, ... over the cluster's CTAs
-    const uint32_t rank = cluster_rank();
-    const int CL = p.cl;
-    const int pidx = c / CL;
-    float *out = p.part + ((size_t)sl * p.parts + pidx) * 128 * kD;
-    const int my_rows = (128 - (int)rank + CL - 1) / CL;
-    const uint32_t red_base = smem_u32(red);
-    for (int item = tid; item < my_rows * 16; item += 128) {
-        const int rr = (int)rank + CL * (item >> 4);
-        const int f = item & 15;
-        const uint32_t off = (uint32_t)(rr * kRedStride + 4 * f) * 4u;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int qq = 0; qq < CL; ++qq) {
-            const float4 v = ld_dsmem4(map_rank(red_base + off, (uint32_t)qq));
-            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-        }
-        reinterpret_cast<float4 *>(out + rr * kD)[f] = acc;
-    }
-    cluster_sync();
-    if (warp == 0) tmem_dealloc(tmem, 64);
-}
-
-// ===========================================================================
-// 3. recur: partial reduction, U_k^T = U_(k-1)^T M^T, epilogue operand.
-// ===========================================================================
-// Writes one 64-element fp32 row as bf16 into a 128-B-swizzled row image.
-__device__ __forceinline__ void put_row_bf16(uint8_t *img, int row, const float *v, int chunk) {
-    uint4 o;
-    o.x = pack_bf16(v[0], v[1]);
-    o.y = pack_bf16(v[2], v[3]);
-    o.z = pack_bf16(v[4], v[5]);
-    o.w = pack_bf16(v[6], v[7]);
-    *reinterpret_cast<uint4 *>(img + (size_t)row * kRow + ((chunk ^ (row & 7)) << 4)) = o;
-}
-
-__global__ void __launch_bounds__(256) tc_recur_kernel(TcParams p) {
-    __shared__ float Mt[kD][kD + 1];     // M^T [b][a]
-    __shared__ float Ut[16][kD + 1];     // this CTA's 16 rows of U_k^T
-    __shared__ float Un[16][kD + 1];
-    __shared__ float Fold[16][kD + 1];
-    const int tid = threadIdx.x;
-    const int sl = blockIdx.x / kRecurRowBlocks, rb = blockIdx.x % kRecurRowBlocks;
-    pdl_launch_dependents();
-    pdl_wait();
-    const float *part = p.part + (size_t)sl * p.parts * 128 * kD;
-    for (int idx = tid; idx < kD * kD; idx += 256) {
-        const int b = idx / kD, a = idx % kD;
-        float m = 0.f;
-        for (int q = 0; q < p.parts; ++q) m += part[((size_t)q * 128 + kD + b) * kD + a];
-        Mt[b][a] = m;
-    }
-    for (int idx = tid; idx < 16 * kD; idx += 256) {
-        const int e = idx / kD, a = idx % kD;
-        float u = 0.f;
-        for (int q = 0; q < p.parts; ++q) u += part[((size_t)q * 128 + 16 * rb + e) * kD + a];
-        Ut[e][a] = u;
-        Fold[e][a] = 0.f;
-    }
-    __syncthreads();
     const bool folded = (p.wmode != LISA_W_MLP);
     uint8_t *img = p.bepi + (size_t)sl * p.epi_rows * kRow;
     for (int k = 1; k < p.T; ++k) {
         if (k > 1) {
-            for (int idx = tid; idx < 16 * kD; idx += 256) {
-                const int e = idx / kD, a = idx % kD;
-                float acc = 0.f;
-#pragma unroll 8
-                for (int b = 0; b < kD; ++b) acc = fmaf(Ut[e][b], Mt[b][a], acc);
-                Un[e][a] = acc;
-            }
+            rows_times_mt(&Ut[0][0], &Mt[0][0], &Un[0][0], 16, tid, 256);
             __syncthreads();
             for (int idx = tid; idx < 16 * kD; idx += 256) Ut[idx / kD][idx % kD] = Un[idx / kD][idx % kD];
             __syncthreads();
@@ -393,56 +734,33 @@ __global__ void __launch_bounds__(256) tc_recur_kernel(TcParams p) {
         const int e = tid >> 3, chunk = tid & 7;
         put_row_bf16(img, 16 * rb + e, &Fold[e][chunk * 8], chunk);
     }
-    if (rb == 0 && tid < 128) {
-        // rows n_umat*64 + {0: s_hi, 1: s_lo, 2..15: 0}
-        __shared__ float srow[2][kD];
-        if (tid < kD) {
-            float s = 0.f;
-            for (int cc = 0; cc < p.chunks; ++cc) s += p.s_part[((size_t)sl * p.chunks + cc) * kD + tid];
-            const float hi = __bfloat162float(__float2bfloat16_rn(s));
-            srow[0][tid] = hi;
-            srow[1][tid] = s - hi;
-        }
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        const int r16 = tid >> 3, chunk = tid & 7;
-        float zero[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        const float *src = r16 < 2 ? &srow[r16][chunk * 8] : zero;
-        put_row_bf16(img, p.n_umat * kD + r16, src, chunk);
-    }
-    if (!folded && sl == 0 && rb == 0) {
-        // W1 [hidden][2*64] -> two K-major images [n_mlp rows][64]: q-part, k-part
-        for (int idx = tid; idx < 2 * p.n_mlp * 8; idx += 256) {
-            const int half = idx / (p.n_mlp * 8), rem = idx % (p.n_mlp * 8);
-            const int m = rem >> 3, chunk = rem & 7;
-            float v[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                v[e] = m < p.hidden ? p.W1[(size_t)m * 2 * kD + half * kD + chunk * 8 + e] : 0.f;
-            put_row_bf16(p.w1img + (size_t)half * p.n_mlp * kRow, m, v, chunk);
-        }
-    }
+    if (rb == 0) put_s_rows(img, p.n_umat * kD, s_sh, tid);
+    if (!folded && sl == 0 && rb == 0) put_w1_image(p, tid, 256);
 }
 
 // ===========================================================================
-// 4. epilogue
+// epilogue
 // ===========================================================================
 struct EpiLayout {
-    uint32_t q, kh, vh, bepi, kt, w1, x, total;
+    uint32_t q, kh, vh, bepi, kt, stage, w1, out, total;
 };
 
 __host__ __device__ inline uint32_t align1k(uint32_t x) { return (x + 1023u) & ~1023u; }
 
-__host__ __device__ inline EpiLayout epi_layout(int th, int tw, int epi_rows, int n_mlp, bool mlp) {
+__host__ __device__ inline EpiLayout epi_layout(int BR, int BC, int epi_rows, int n_mlp, bool mlp,
+                                                int stages) {
     EpiLayout L;
-    const uint32_t halo = align1k((uint32_t)(th + 2) * (tw + 2) * kRow);
+    const uint32_t halo = align1k((uint32_t)(2 * BR + 2) * (8 * BC + 2) * kRow);
     uint32_t off = 0;
     L.q = off; off += 128 * kRow;
     L.kh = off; off += halo;
     L.vh = off; off += halo;
     L.bepi = off; off += align1k((uint32_t)epi_rows * kRow);
     L.kt = off; if (mlp) off += 128 * kRow;
+    L.stage = off;                     // bytes per input stage
+    off *= (uint32_t)stages;
     L.w1 = off; if (mlp) off += align1k(2u * n_mlp * kRow);
-    L.x = off; off += 128u * kXStride * 4u;
+    L.out = off; off += 128 * kRow;
     L.total = off;
     return L;
 }
@@ -451,30 +769,101 @@ __device__ __forceinline__ float gelu_erf(float x) {
     return 0.5f * x * (1.f + erff(x * 0.70710678118654752f));
 }
 
-__global__ void __launch_bounds__(256) tc_epilogue_kernel(const __grid_constant__ CUtensorMap mQ,
-                                                          const __grid_constant__ CUtensorMap mKh,
-                                                          const __grid_constant__ CUtensorMap mVh,
-                                                          const __grid_constant__ CUtensorMap mKt,
-                                                          const __grid_constant__ CUtensorMap mO,
-                                                          TcParams p, uint32_t tmem_cols) {
+// 16 TMEM lanes x 8 consecutive fp32 columns in mma.sync C-fragment layout:
+// f0,f1 = (row g, cols 2q, 2q+1), f2,f3 = (row g+8, same cols).
+__device__ __forceinline__ void tmem_ld_frag(uint32_t taddr, float (&f)[4]) {
+    uint32_t r0, r1, r2, r3;
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(taddr)
+                 : "memory");
+    tc_wait_ld();
+    f[0] = __uint_as_float(r0); f[1] = __uint_as_float(r1);
+    f[2] = __uint_as_float(r2); f[3] = __uint_as_float(r3);
+}
+
+// Same layout, no wait: 8 repetitions cover 64 columns (32 registers).
+__device__ __forceinline__ void tmem_ld_frag8_nowait(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld_frag_nowait(uint32_t taddr, uint32_t (&r)[4]) {
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr)
+                 : "memory");
+}
+
+struct TileCoord {
+    int sl, r0, c0;
+};
+__device__ __forceinline__ TileCoord tile_coord(const TcParams &p, int t) {
+    const int per = p.tiles_r * p.tiles_c;
+    TileCoord tc;
+    tc.sl = t / per;
+    const int rem = t % per;
+    tc.r0 = (rem / p.tiles_c) * (2 * p.BR);
+    tc.c0 = (rem % p.tiles_c) * (8 * p.BC);
+    return tc;
+}
+
+// TMA loads of one tile into the stage at `sbase`: Q (and K) as BC boxes of
+// 8 columns x 2 BR rows (block-major rows), the K and V halos, and the slice's
+// B operand when the stage does not hold it yet.
+__device__ __forceinline__ void epi_issue_loads(const TcParams &p, const EpiLayout &L, uint32_t sbase,
+                                                uint32_t bar, TileCoord tc, bool load_bepi, bool mlp,
+                                                const CUtensorMap *mQ, const CUtensorMap *mKh,
+                                                const CUtensorMap *mVh, const CUtensorMap *mKt) {
+    const uint32_t halo_rows = (uint32_t)(2 * p.BR + 2) * (8 * p.BC + 2);
+    uint32_t bytes = (128u + 2u * halo_rows + (mlp ? 128u : 0u)) * kRow;
+    if (load_bepi) bytes += (uint32_t)p.epi_rows * kRow;
+    mbar_arrive_expect_tx(bar, bytes);
+    for (int bj = 0; bj < p.BC; ++bj) {
+        tma_load_4d(sbase + L.q + bj * 16 * p.BR * kRow, mQ, 0, tc.c0 + 8 * bj, tc.r0, tc.sl, bar);
+        if (mlp) tma_load_4d(sbase + L.kt + bj * 16 * p.BR * kRow, mKt, 0, tc.c0 + 8 * bj, tc.r0, tc.sl, bar);
+    }
+    tma_load_4d(sbase + L.kh, mKh, 0, tc.c0 - 1, tc.r0 - 1, tc.sl, bar);
+    tma_load_4d(sbase + L.vh, mVh, 0, tc.c0 - 1, tc.r0 - 1, tc.sl, bar);
+    if (load_bepi)
+        bulk_load(sbase + L.bepi, p.bepi + (size_t)tc.sl * p.epi_rows * kRow, (uint32_t)p.epi_rows * kRow, bar);
+}
+
+template <bool kMlp>
+__global__ void __launch_bounds__(256, kMlp ? 1 : 2) tc_epilogue_kernel(const __grid_constant__ CUtensorMap mQ,
+                                                             const __grid_constant__ CUtensorMap mKh,
+                                                             const __grid_constant__ CUtensorMap mVh,
+                                                             const __grid_constant__ CUtensorMap mKt,
+                                                             const __grid_constant__ CUtensorMap mO,
+                                                             TcParams p, uint32_t tmem_cols) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ __align__(8) uint64_t load_bar, bepi_bar, mma_bar;
+    __shared__ __align__(8) uint64_t load_bar[2], w1_bar, mma_bar;
     __shared__ uint32_t tmem_slot;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const bool mlp = (p.wmode == LISA_W_MLP);
-    const int th = p.th, tw = p.tw, hw = tw + 2;
-    const EpiLayout L = epi_layout(th, tw, p.epi_rows, p.n_mlp, mlp);
-    const int tiles = p.tiles_r * p.tiles_c;
-    const int sl = blockIdx.x / tiles, tix = blockIdx.x % tiles;
-    const int r0 = (tix / p.tiles_c) * th, c0 = (tix % p.tiles_c) * tw;
+    constexpr bool mlp = kMlp;
+    const int BR = p.BR, BC = p.BC, hw = 8 * BC + 2;
+    const EpiLayout L = epi_layout(BR, BC, p.epi_rows, p.n_mlp, mlp, p.epi_stages);
     const uint32_t base = smem_u32(sm);
-    const uint32_t halo_rows = (uint32_t)(th + 2) * hw;
+    const int g = lane >> 2, q4 = lane & 3;
+
+    // this warp's 2 x 8 block: TMEM lanes 16 blk .. 16 blk + 15 (inside its quadrant)
+    const int blk = 2 * (warp & 3) + (warp >> 2);
+    const int bi = blk % BR, bj = blk / BR;
+    const uint32_t lane_base = (uint32_t)(16 * blk) << 16;
 
     if (tid == 0) {
-        mbar_init(smem_u32(&load_bar), 1);
-        mbar_init(smem_u32(&bepi_bar), 1);
+        mbar_init(smem_u32(&load_bar[0]), 1);
+        mbar_init(smem_u32(&load_bar[1]), 1);
+        mbar_init(smem_u32(&w1_bar), 1);
         mbar_init(smem_u32(&mma_bar), 1);
         fence_mbar_init();
     }
@@ -485,260 +874,321 @@ __global__ void __launch_bounds__(256) tc_epilogue_kernel(const __grid_constant_
     const uint32_t tmem = tmem_slot;
     pdl_launch_dependents();
 
-    if (tid == 0) {  // this tile's inputs: independent of the earlier kernels
-        const uint32_t bytes = (128u + 2u * halo_rows + (mlp ? 128u : 0u)) * kRow;
-        const uint32_t lb = smem_u32(&load_bar);
-        mbar_arrive_expect_tx(lb, bytes);
-        tma_load_4d(base + L.q, &mQ, 0, c0, r0, sl, lb);
-        tma_load_4d(base + L.kh, &mKh, 0, c0 - 1, r0 - 1, sl, lb);
-        tma_load_4d(base + L.vh, &mVh, 0, c0 - 1, r0 - 1, sl, lb);
-        if (mlp) tma_load_4d(base + L.kt, &mKt, 0, c0, r0, sl, lb);
-    }
-    pdl_wait();  // the B operand of this slice is ready
-    if (tid == 0) {
-        const uint32_t bb = smem_u32(&bepi_bar);
-        const uint32_t bbytes = (uint32_t)p.epi_rows * kRow;
-        const uint32_t wbytes = mlp ? 2u * p.n_mlp * kRow : 0u;
-        mbar_arrive_expect_tx(bb, bbytes + wbytes);
-        bulk_load(base + L.bepi, p.bepi + (size_t)sl * p.epi_rows * kRow, bbytes, bb);
-        if (mlp) bulk_load(base + L.w1, p.w1img, wbytes, bb);
-    }
-    bool ok = mbar_wait(smem_u32(&load_bar), 0);
-    if (!ok) record_error(p.err, kErrTimeoutLoad);
-    if (p.relu) {
-        relu_smem(sm + L.q, 128 * kRow, tid, 256);
-        relu_smem(sm + L.kh, (int)halo_rows * kRow, tid, 256);
-        if (mlp) relu_smem(sm + L.kt, 128 * kRow, tid, 256);
-    }
-    fence_proxy_async();
-    __syncthreads();
-
-    // ---- tensor-core products (one thread issues, completion on mma_bar)
-    if (tid == 0) {
-        if (!mbar_wait(smem_u32(&bepi_bar), 0)) record_error(p.err, kErrTimeoutLoad);
-        tc_fence_after();
-        for (int r = 0; r < p.epi_rows; r += 256) {
-            const int N = min(256, p.epi_rows - r);
-            const uint32_t idesc = make_idesc_bf16(128, N, false, false);
+    // Per-lane constants of the local branch.  Window key kappa indexes the
+    // 4 x 10 key window of the block: ka = kappa / 10, kb = kappa % 10.
+    uint32_t win_mask = 0;            // bit j*4+e: key of score element (j, e) is in the query's 3x3 window
+    uint32_t kab[5][2];               // (ka, kb) of the two keys of n-tile j
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t ad = make_desc_sw128(base + L.q + ks * 32, 16, 1024);
-                const uint64_t bd = make_desc_sw128(base + L.bepi + r * kRow + ks * 32, 16, 1024);
-                tc_mma(tmem + r, ad, bd, idesc, ks > 0);
+    for (int j = 0; j < 5; ++j)
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            const int kappa = 8 * j + 2 * q4 + b;
+            const int ka = kappa / 10, kb = kappa % 10;
+            kab[j][b] = (uint32_t)(ka | (kb << 8));
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int du = ka - h, dv = kb - g;
+                if (du >= 0 && du <= 2 && dv >= 0 && dv <= 2) win_mask |= 1u << (j * 4 + 2 * h + b);
             }
         }
+    // halo rows of the ldmatrix loads (static per warp)
+    uint32_t koff[3], voff[3];
+#pragma unroll
+    for (int pr = 0; pr < 3; ++pr) {
+        const int kk = 8 * (2 * pr + (lane >> 4)) + (lane & 7);          // scores: n-tile pairs
+        const int kv = 16 * pr + (lane & 7) + 8 * ((lane >> 3) & 1);      // values: k-steps
+        const int kk2 = kk < 40 ? kk : 0, kv2 = kv < 40 ? kv : 0;
+        koff[pr] = (uint32_t)((2 * bi + kk2 / 10) * hw + 8 * bj + kk2 % 10);
+        voff[pr] = (uint32_t)((2 * bi + kv2 / 10) * hw + 8 * bj + kv2 % 10);
+    }
+    const int qrow = 16 * blk + (lane & 7) + 8 * ((lane >> 3) & 1);      // A-fragment row
+    // the block's own tokens in the halo (V_i of the w_0 V_i term): rows g, g+8
+    const uint32_t vi_row[2] = {(uint32_t)((2 * bi + 1) * hw + 8 * bj + g + 1),
+                                (uint32_t)((2 * bi + 2) * hw + 8 * bj + g + 1)};
+
+    const int first = blockIdx.x;
+    const int step = gridDim.x;
+    int last_slice[2] = {-1, -1};
+    if (tid == 0 && first < p.tiles) {
+        // Q, K, V of the first tile do not depend on the earlier kernels
+        const TileCoord tc = tile_coord(p, first);
+        const uint32_t bar = smem_u32(&load_bar[0]);
+        const uint32_t halo_rows = (uint32_t)(2 * BR + 2) * hw;
+        mbar_arrive_expect_tx(bar, (128u + 2u * halo_rows + (mlp ? 128u : 0u) + (uint32_t)p.epi_rows) * kRow);
+        for (int b2 = 0; b2 < BC; ++b2) {
+            tma_load_4d(base + L.q + b2 * 16 * BR * kRow, &mQ, 0, tc.c0 + 8 * b2, tc.r0, tc.sl, bar);
+            if (mlp) tma_load_4d(base + L.kt + b2 * 16 * BR * kRow, &mKt, 0, tc.c0 + 8 * b2, tc.r0, tc.sl, bar);
+        }
+        tma_load_4d(base + L.kh, &mKh, 0, tc.c0 - 1, tc.r0 - 1, tc.sl, bar);
+        tma_load_4d(base + L.vh, &mVh, 0, tc.c0 - 1, tc.r0 - 1, tc.sl, bar);
+    }
+    pdl_wait();  // B operands of every slice are ready
+    if (tid == 0 && first < p.tiles) {
+        const TileCoord tc = tile_coord(p, first);
+        bulk_load(base + L.bepi, p.bepi + (size_t)tc.sl * p.epi_rows * kRow, (uint32_t)p.epi_rows * kRow,
+                  smem_u32(&load_bar[0]));
         if (mlp) {
-            const uint32_t idesc = make_idesc_bf16(128, p.n_mlp, false, false);
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t abase = (ks < 4 ? L.q : L.kt) + (ks & 3) * 32;
-                const uint32_t bbase = L.w1 + (ks < 4 ? 0u : (uint32_t)p.n_mlp * kRow) + (ks & 3) * 32;
-                tc_mma(tmem + p.epi_rows, make_desc_sw128(base + abase, 16, 1024),
-                       make_desc_sw128(base + bbase, 16, 1024), idesc, ks > 0);
-            }
-        }
-        tc_commit(smem_u32(&mma_bar));
-    }
-
-    // ---- 3x3 local branch on the legacy tensor path: warp w owns 4x4 block w
-    const int g = lane >> 2, q4 = lane & 3;
-    const int bpr = tw >> 2;
-    const int bi = warp / bpr, bj = warp % bpr;
-    float lacc[8][4];
-    {
-        // A fragments: the block's 16 query rows, 4 k-steps of 16 channels
-        uint32_t a[4][4];
-        {
-            const int ml = (lane & 7) + ((lane >> 3) & 1) * 8;
-            const int trow = (4 * bi + (ml >> 2)) * tw + 4 * bj + (ml & 3);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                ldsm_x4(base + L.q + sw128_offset(trow, 2 * ks + (lane >> 4)), a[ks][0], a[ks][1],
-                        a[ks][2], a[ks][3]);
-        }
-        // window key kappa (0..35) -> halo row; padding keys point at key 0
-        auto halo_row = [&](int kappa) -> uint32_t {
-            if (kappa >= 36) kappa = 0;
-            return (uint32_t)((4 * bi + kappa / 6) * hw + 4 * bj + kappa % 6);
-        };
-        float sc[5][4];
-#pragma unroll
-        for (int j = 0; j < 5; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-#pragma unroll
-            for (int pr = 0; pr < 3; ++pr) {
-                const int kappa = 8 * (2 * pr + (lane >> 4)) + (lane & 7);
-                const int chunk = 2 * ks + ((lane >> 3) & 1);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(base + L.kh + sw128_offset(halo_row(kappa), chunk), b0, b1, b2, b3);
-                mma_bf16_16816(sc[2 * pr], a[ks][0], a[ks][1], a[ks][2], a[ks][3], b0, b1);
-                if (pr < 2) mma_bf16_16816(sc[2 * pr + 1], a[ks][0], a[ks][1], a[ks][2], a[ks][3], b2, b3);
-            }
-        }
-        // mask: key in the 3x3 window of the query and inside the grid
-        const float c2 = 1.4426950408889634f * 0.125f;   // log2(e) / sqrt(64)
-        float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-        for (int j = 0; j < 5; ++j)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int m = g + 8 * (e >> 1);
-                const int kappa = 8 * j + 2 * q4 + (e & 1);
-                const int ka = kappa / 6, kb = kappa % 6;
-                const int du = ka - (m >> 2), dv = kb - (m & 3);
-                const int gr = r0 + 4 * bi + ka - 1, gc = c0 + 4 * bj + kb - 1;
-                const bool valid = kappa < 36 && du >= 0 && du <= 2 && dv >= 0 && dv <= 2 &&
-                                   gr >= 0 && gr < p.H && gc >= 0 && gc < p.W;
-                sc[j][e] = valid ? sc[j][e] * c2 : -INFINITY;
-                mx[e >> 1] = fmaxf(mx[e >> 1], sc[j][e]);
-            }
-        float sum[2] = {0.f, 0.f};
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
-            mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
-            if (mx[h] == -INFINITY) mx[h] = 0.f;
-        }
-#pragma unroll
-        for (int j = 0; j < 5; ++j)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                sc[j][e] = exp2f(sc[j][e] - mx[e >> 1]);
-                sum[e >> 1] += sc[j][e];
-            }
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            sum[h] += __shfl_xor_sync(0xffffffffu, sum[h], 1);
-            sum[h] += __shfl_xor_sync(0xffffffffu, sum[h], 2);
-        }
-        const float inv[2] = {sum[0] > 0.f ? 1.f / sum[0] : 0.f, sum[1] > 0.f ? 1.f / sum[1] : 0.f};
-        // weights as A fragments (keys are the k dimension), times V window
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt) lacc[nt][0] = lacc[nt][1] = lacc[nt][2] = lacc[nt][3] = 0.f;
-#pragma unroll
-        for (int ks = 0; ks < 3; ++ks) {
-            const int j0 = 2 * ks, j1 = 2 * ks + 1;
-            const uint32_t pa0 = pack_bf16(sc[j0][0], sc[j0][1]);
-            const uint32_t pa1 = pack_bf16(sc[j0][2], sc[j0][3]);
-            const uint32_t pa2 = j1 < 5 ? pack_bf16(sc[j1][0], sc[j1][1]) : 0u;
-            const uint32_t pa3 = j1 < 5 ? pack_bf16(sc[j1][2], sc[j1][3]) : 0u;
-            const int kappa = 16 * ks + (lane & 7) + 8 * ((lane >> 3) & 1);
-            const uint32_t hrow = halo_row(kappa);
-#pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(base + L.vh + sw128_offset(hrow, 2 * np + (lane >> 4)), b0, b1, b2, b3);
-                mma_bf16_16816(lacc[2 * np], pa0, pa1, pa2, pa3, b0, b1);
-                mma_bf16_16816(lacc[2 * np + 1], pa0, pa1, pa2, pa3, b2, b3);
-            }
-        }
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-            lacc[nt][0] *= inv[0]; lacc[nt][1] *= inv[0];
-            lacc[nt][2] *= inv[1]; lacc[nt][3] *= inv[1];
+            mbar_arrive_expect_tx(smem_u32(&w1_bar), 2u * p.n_mlp * kRow);
+            bulk_load(base + L.w1, p.w1img, 2u * p.n_mlp * kRow, smem_u32(&w1_bar));
         }
     }
+    if (first < p.tiles) last_slice[0] = tile_coord(p, first).sl;
+    if (mlp && first < p.tiles && !mbar_wait(smem_u32(&w1_bar), 0)) record_error(p.err, kErrTimeoutLoad);
 
-    // ---- global branch from TMEM: thread = tile row, half the channels
-    const float alpha = p.alpha[sl % p.heads];
-    float *X = reinterpret_cast<float *>(sm + L.x);
-    if (!mbar_wait(smem_u32(&mma_bar), 0)) record_error(p.err, kErrTimeoutMma);
-    tc_fence_after();
-    {
-        const int quad = warp & 3, half = warp >> 2;
-        const int row = 32 * quad + lane;
-        const uint32_t tl = tmem + ((uint32_t)(32 * quad) << 16);
-        uint32_t r[16];
-        tmem_ld16(tl + p.n_umat * kD, r);   // Q.s_hi, Q.s_lo
-        tc_wait_ld();
-        const float rq = 1.f / (__uint_as_float(r[0]) + __uint_as_float(r[1]) + p.eps);
-        float wk[LISA_MAX_T];
-        if (mlp) {
-            float z[LISA_MAX_T_MLP];
-            for (int t = 0; t < p.T; ++t) z[t] = p.b2[t];
-            for (int cb = 0; cb < p.n_mlp; cb += 16) {
-                tmem_ld16(tl + p.epi_rows + cb, r);
-                tc_wait_ld();
+    const float c2 = 1.4426950408889634f * 0.125f;   // log2(e) / sqrt(64)
+    int it = 0;
+    for (int t = first; t < p.tiles; t += step, ++it) {
+        const int st = (p.epi_stages == 2) ? (it & 1) : 0;
+        const uint32_t sb = base + st * L.stage;
+        uint8_t *sp = sm + st * L.stage;
+        const TileCoord tc = tile_coord(p, t);
+        const int tn = t + step;
+        // prefetch the next tile into the other buffer (free since the last tile)
+        if (p.epi_stages == 2 && tid == 0 && tn < p.tiles) {
+            const int sn = st ^ 1;
+            const TileCoord tcn = tile_coord(p, tn);
+            epi_issue_loads(p, L, base + sn * L.stage, smem_u32(&load_bar[sn]), tcn, last_slice[sn] != tcn.sl, mlp,
+                            &mQ, &mKh, &mVh, &mKt);
+            last_slice[sn] = tcn.sl;
+        }
+        const uint32_t ph = (p.epi_stages == 2) ? ((it >> 1) & 1) : (it & 1);
+        if (!mbar_wait(smem_u32(&load_bar[st]), ph)) record_error(p.err, kErrTimeoutLoad);
+        if (tid == 0) bulk_wait_read0();   // the previous tile's store has read the output buffer
+        if (p.relu) {
+            relu_smem(sp + L.q, 128 * kRow, tid, 256);
+            if (mlp) relu_smem(sp + L.kt, 128 * kRow, tid, 256);
+        }
+        fence_proxy_async();
+        __syncthreads();
+
+        // ---- tensor-core products into TMEM
+        if (tid == 0) {
+            tc_fence_after();
+            for (int r = 0; r < p.epi_rows; r += 256) {
+                const int N = min(256, p.epi_rows - r);
+                const uint32_t idesc = make_idesc_bf16(128, N, false, false);
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const int m = cb + k;
-                    if (m < p.hidden) {
-                        const float hv = gelu_erf(__uint_as_float(r[k]) + p.b1[m]);
-                        for (int t = 0; t < p.T; ++t) z[t] = fmaf(p.W2[t * p.hidden + m], hv, z[t]);
-                    }
+                for (int ks = 0; ks < 4; ++ks)
+                    tc_mma(tmem + r, make_desc_sw128(sb + L.q + ks * 32, 16, 1024),
+                           make_desc_sw128(sb + L.bepi + r * kRow + ks * 32, 16, 1024), idesc, ks > 0);
+            }
+            if (mlp) {
+                const uint32_t idesc = make_idesc_bf16(128, p.n_mlp, false, false);
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t a = sb + (ks < 4 ? L.q : L.kt) + (ks & 3) * 32;
+                    const uint32_t b = base + L.w1 + (ks < 4 ? 0u : (uint32_t)p.n_mlp * kRow) + (ks & 3) * 32;
+                    tc_mma(tmem + p.epi_rows, make_desc_sw128(a, 16, 1024), make_desc_sw128(b, 16, 1024), idesc,
+                           ks > 0);
                 }
             }
-            float zmax = z[0];
-            for (int t = 1; t < p.T; ++t) zmax = fmaxf(zmax, z[t]);
-            float zs = 0.f;
-            for (int t = 0; t < p.T; ++t) {
-                z[t] = expf(z[t] - zmax);
-                zs += z[t];
-            }
-            for (int t = 0; t < p.T; ++t) wk[t] = z[t] / zs;
-        } else {
-            wk[0] = p.w[0];
+            tc_commit(smem_u32(&mma_bar));
         }
-        float acc[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) acc[k] = 0.f;
-        for (int u = 0; u < p.n_umat; ++u) {
-            const float wu = mlp ? wk[u + 1] : 1.f;
-#pragma unroll
-            for (int cb = 0; cb < 32; cb += 16) {
-                tmem_ld16(tl + u * kD + 32 * half + cb, r);
-                tc_wait_ld();
-#pragma unroll
-                for (int k = 0; k < 16; ++k) acc[cb + k] = fmaf(wu, __uint_as_float(r[k]), acc[cb + k]);
-            }
-        }
-        // V_i (row `row` of the tile) from the halo buffer
-        const int tr = row / tw, tcl = row % tw;
-        const int hrow = (tr + 1) * hw + tcl + 1;
-        float *xr = X + row * kXStride + 32 * half;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int chunk = 4 * half + k;
-            const uint4 v = *reinterpret_cast<const uint4 *>(sm + L.vh + sw128_offset(hrow, chunk));
-            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-            float o[8];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                o[2 * e] = alpha * (wk[0] * bf16_lo(w4[e]) + rq * acc[8 * k + 2 * e]);
-                o[2 * e + 1] = alpha * (wk[0] * bf16_hi(w4[e]) + rq * acc[8 * k + 2 * e + 1]);
-            }
-            reinterpret_cast<float4 *>(xr + 8 * k)[0] = make_float4(o[0], o[1], o[2], o[3]);
-            reinterpret_cast<float4 *>(xr + 8 * k)[1] = make_float4(o[4], o[5], o[6], o[7]);
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
 
-    // ---- mix and store: warp w writes its 4x4 block into the output tile
-    {
-        const float beta_l = 1.f - alpha;
+        // ---- local branch of this warp's block (mma.sync)
+        float lacc[8][4];
+        {
+            uint32_t a[4][4];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int m = g + 8 * h;
-            const int trow = (4 * bi + (m >> 2)) * tw + 4 * bj + (m & 3);
-            const float *xr = X + trow * kXStride;
+            for (int ks = 0; ks < 4; ++ks)
+                ldsm_x4(sb + L.q + sw128_offset(qrow, 2 * ks + (lane >> 4)), a[ks][0], a[ks][1], a[ks][2], a[ks][3]);
+            float sc[5][4];
+#pragma unroll
+            for (int j = 0; j < 5; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+#pragma unroll
+                for (int pr = 0; pr < 3; ++pr) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(sb + L.kh + sw128_offset(koff[pr], 2 * ks + ((lane >> 3) & 1)), b0, b1, b2, b3);
+                    if (p.relu) {
+                        b0 = relu2(b0); b1 = relu2(b1); b2 = relu2(b2); b3 = relu2(b3);
+                    }
+                    mma_bf16_16816(sc[2 * pr], a[ks][0], a[ks][1], a[ks][2], a[ks][3], b0, b1);
+                    if (pr < 2) mma_bf16_16816(sc[2 * pr + 1], a[ks][0], a[ks][1], a[ks][2], a[ks][3], b2, b3);
+                }
+            }
+            // mask: the query's 3x3 window, keys inside the grid
+            uint32_t mask = win_mask;
+            const int gr0 = tc.r0 + 2 * bi - 1, gc0 = tc.c0 + 8 * bj - 1;   // grid position of window (0, 0)
+            if (gr0 < 0 || gr0 + 3 >= p.H || gc0 < 0 || gc0 + 9 >= p.W) {
+#pragma unroll
+                for (int j = 0; j < 5; ++j)
+#pragma unroll
+                    for (int b = 0; b < 2; ++b) {
+                        const int gr = gr0 + (int)(kab[j][b] & 0xff), gc = gc0 + (int)(kab[j][b] >> 8);
+                        if (gr < 0 || gr >= p.H || gc < 0 || gc >= p.W) mask &= ~(0x5u << (j * 4 + b));
+                    }
+            }
+            float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+            for (int j = 0; j < 5; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const bool valid = (mask >> (j * 4 + e)) & 1u;
+                    sc[j][e] = valid ? sc[j][e] * c2 : -INFINITY;
+                    mx[e >> 1] = fmaxf(mx[e >> 1], sc[j][e]);
+                }
+            float sum[2] = {0.f, 0.f};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+                mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+                if (mx[h] == -INFINITY) mx[h] = 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < 5; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    sc[j][e] = exp2f(sc[j][e] - mx[e >> 1]);
+                    sum[e >> 1] += sc[j][e];
+                }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                sum[h] += __shfl_xor_sync(0xffffffffu, sum[h], 1);
+                sum[h] += __shfl_xor_sync(0xffffffffu, sum[h], 2);
+            }
+            const float inv[2] = {sum[0] > 0.f ? 1.f / sum[0] : 0.f, sum[1] > 0.f ? 1.f / sum[1] : 0.f};
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) lacc[nt][0] = lacc[nt][1] = lacc[nt][2] = lacc[nt][3] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < 3; ++ks) {
+                const int j0 = 2 * ks, j1 = 2 * ks + 1;
+                const uint32_t pa0 = pack_bf16(sc[j0][0], sc[j0][1]);
+                const uint32_t pa1 = pack_bf16(sc[j0][2], sc[j0][3]);
+                const uint32_t pa2 = j1 < 5 ? pack_bf16(sc[j1][0], sc[j1][1]) : 0u;
+                const uint32_t pa3 = j1 < 5 ? pack_bf16(sc[j1][2], sc[j1][3]) : 0u;
+#pragma unroll
+                for (int np = 0; np < 4; ++np) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(sb + L.vh + sw128_offset(voff[ks], 2 * np + (lane >> 4)), b0, b1, b2, b3);
+                    mma_bf16_16816(lacc[2 * np], pa0, pa1, pa2, pa3, b0, b1);
+                    mma_bf16_16816(lacc[2 * np + 1], pa0, pa1, pa2, pa3, b2, b3);
+                }
+            }
 #pragma unroll
             for (int nt = 0; nt < 8; ++nt) {
-                const int ch = 8 * nt + 2 * q4;
-                const float2 xv = *reinterpret_cast<const float2 *>(xr + ch);
-                const uint32_t o = pack_bf16(xv.x + beta_l * lacc[nt][2 * h], xv.y + beta_l * lacc[nt][2 * h + 1]);
-                *reinterpret_cast<uint32_t *>(sm + L.q + sw128_offset(trow, nt) + 4 * q4) = o;
+                lacc[nt][0] *= inv[0]; lacc[nt][1] *= inv[0];
+                lacc[nt][2] *= inv[1]; lacc[nt][3] *= inv[1];
+            }
+        }
+
+        // ---- global branch from TMEM in fragment layout, mix, output tile
+        if (!mbar_wait(smem_u32(&mma_bar), it & 1)) record_error(p.err, kErrTimeoutMma);
+        tc_fence_after();
+        {
+            const float alpha = p.alpha[tc.sl % p.heads];
+            const uint32_t tl = tmem + lane_base;
+            uint32_t rs[4];
+            tmem_ld_frag_nowait(tl + p.n_umat * kD, rs);     // Q.s_hi, Q.s_lo: columns held by lane q4 = 0
+            uint32_t hr[8][4];
+            if (mlp) {
+#pragma unroll
+                for (int f8 = 0; f8 < 8; ++f8)
+                    if (8 * f8 < p.n_mlp) tmem_ld_frag_nowait(tl + p.epi_rows + 8 * f8, hr[f8]);
+            }
+            uint32_t ru[32];
+            tmem_ld_frag8_nowait(tl, ru);
+            tc_wait_ld();
+            const int src = lane & ~3;
+            const float d0 = __shfl_sync(0xffffffffu, __uint_as_float(rs[0]) + __uint_as_float(rs[1]), src);
+            const float d1 = __shfl_sync(0xffffffffu, __uint_as_float(rs[2]) + __uint_as_float(rs[3]), src);
+            const float rq[2] = {1.f / (d0 + p.eps), 1.f / (d1 + p.eps)};
+            float w0[2], wk[2][LISA_MAX_T_MLP];
+            float acc[32];
+            if (mlp) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int t2 = 0; t2 < LISA_MAX_T_MLP; ++t2) wk[h][t2] = 0.f;
+#pragma unroll
+                for (int f8 = 0; f8 < 8; ++f8) {
+                    if (8 * f8 >= p.n_mlp) break;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int m = 8 * f8 + 2 * q4 + (e & 1);
+                        if (m < p.hidden) {
+                            const float hv = gelu_erf(__uint_as_float(hr[f8][e]) + p.b1[m]);
+#pragma unroll
+                            for (int t2 = 0; t2 < LISA_MAX_T_MLP; ++t2)
+                                if (t2 < p.T) wk[e >> 1][t2] = fmaf(p.W2[t2 * p.hidden + m], hv, wk[e >> 1][t2]);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    float zmax = -INFINITY;
+#pragma unroll
+                    for (int t2 = 0; t2 < LISA_MAX_T_MLP; ++t2) {
+                        if (t2 >= p.T) break;
+                        float z = wk[h][t2];
+                        z += __shfl_xor_sync(0xffffffffu, z, 1);
+                        z += __shfl_xor_sync(0xffffffffu, z, 2);
+                        z += p.b2[t2];
+                        wk[h][t2] = z;
+                        zmax = fmaxf(zmax, z);
+                    }
+                    float zs = 0.f;
+#pragma unroll
+                    for (int t2 = 0; t2 < LISA_MAX_T_MLP; ++t2) {
+                        if (t2 >= p.T) break;
+                        wk[h][t2] = expf(wk[h][t2] - zmax);
+                        zs += wk[h][t2];
+                    }
+                    const float zi = 1.f / zs;
+#pragma unroll
+                    for (int t2 = 0; t2 < LISA_MAX_T_MLP; ++t2) wk[h][t2] *= zi;
+                    w0[h] = wk[h][0];
+                }
+                // sum_k w_k(i) (Q U_k)_i: first block already loaded
+#pragma unroll
+                for (int k = 0; k < 32; ++k) acc[k] = wk[(k >> 1) & 1][1] * __uint_as_float(ru[k]);
+                for (int u = 1; u < p.n_umat; ++u) {
+                    tmem_ld_frag8_nowait(tl + u * kD, ru);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) acc[k] = fmaf(wk[(k >> 1) & 1][u + 1], __uint_as_float(ru[k]), acc[k]);
+                }
+            } else {
+                w0[0] = w0[1] = p.w[0];
+#pragma unroll
+                for (int k = 0; k < 32; ++k) acc[k] = __uint_as_float(ru[k]);
+            }
+            const float bl = 1.f - alpha;
+            const uint8_t *vh = sp + L.vh;
+            uint8_t *out = sm + L.out;
+            const int orow[2] = {16 * blk + g, 16 * blk + g + 8};
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t vv = *reinterpret_cast<const uint32_t *>(vh + sw128_offset(vi_row[h], nt) + 4 * q4);
+                    const float o0 = alpha * (w0[h] * bf16_lo(vv) + rq[h] * acc[4 * nt + 2 * h]) + bl * lacc[nt][2 * h];
+                    const float o1 =
+                        alpha * (w0[h] * bf16_hi(vv) + rq[h] * acc[4 * nt + 2 * h + 1]) + bl * lacc[nt][2 * h + 1];
+                    *reinterpret_cast<uint32_t *>(out + sw128_offset(orow[h], nt) + 4 * q4) = pack_bf16(o0, o1);
+                }
+            }
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            for (int b2 = 0; b2 < BC; ++b2)
+                tma_store_4d(&mO, base + L.out + b2 * 16 * BR * kRow, 0, tc.c0 + 8 * b2, tc.r0, tc.sl);
+            bulk_commit();
+            // single buffer: the inputs are consumed, load the next tile now
+            if (p.epi_stages == 1 && tn < p.tiles) {
+                const TileCoord tcn = tile_coord(p, tn);
+                epi_issue_loads(p, L, base, smem_u32(&load_bar[0]), tcn, last_slice[0] != tcn.sl, mlp, &mQ, &mKh,
+                                &mVh, &mKt);
+                last_slice[0] = tcn.sl;
             }
         }
     }
-    fence_proxy_async();
+    if (tid == 0) bulk_wait0();
+    tc_fence_before();
     __syncthreads();
-    if (tid == 0) {
-        tma_store_4d(&mO, base + L.q, 0, c0, r0, sl);
-        bulk_commit();
-        bulk_wait_read0();
-    }
-    __syncthreads();
+    tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem, tmem_cols);
 }
 
@@ -794,7 +1244,7 @@ bool make_map_grid(CUtensorMap *m, const void *ptr, int S, int H, int W, int bh,
 template <typename Kern>
 cudaError_t set_smem(Kern k, int slot, int bytes) {
     static std::mutex mu;
-    static int done[4][64];
+    static int done[8][64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -812,21 +1262,33 @@ uint32_t pow2_cols(int cols) {
     return c;
 }
 
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 152;
+    return n;
+}
+
 }  // namespace
 
-// Tile shape of the epilogue: th x tw = 128 tokens, both multiples of 4;
-// fewest tiles, ties to the squarer shape.
-void tc_tile_shape(int H, int W, int *th, int *tw) {
-    static const int shapes[4][2] = {{8, 16}, {16, 8}, {4, 32}, {32, 4}};
+// Epilogue tile: BR x BC blocks of 2 x 8 tokens (BR * BC = 8); fewest tiles.
+void tc_tile_shape(int H, int W, int *BR, int *BC) {
+    static const int shapes[3][2] = {{4, 2}, {8, 1}, {2, 4}};
     long best = -1;
     for (auto &s : shapes) {
-        const long t = (long)((H + s[0] - 1) / s[0]) * ((W + s[1] - 1) / s[1]);
+        const long t = (long)((H + 2 * s[0] - 1) / (2 * s[0])) * ((W + 8 * s[1] - 1) / (8 * s[1]));
         if (best < 0 || t < best) {
             best = t;
-            *th = s[0];
-            *tw = s[1];
+            *BR = s[0];
+            *BC = s[1];
         }
     }
+}
+
+// The fused stats kernel needs all of a slice's chunks in one cluster and the
+// chunk's K rows resident in shared memory.
+bool tc_fused(int chunks, int cluster, int chunk) {
+    return chunks == cluster && (chunk + kSub - 1) / kSub <= kFusedMaxSub;
 }
 
 cudaError_t launch_tc(const Problem &p, cudaStream_t st, int stage) {
@@ -836,83 +1298,132 @@ cudaError_t launch_tc(const Problem &p, cudaStream_t st, int stage) {
     for (int k = 0; k < LISA_MAX_T; ++k) t.w[k] = p.w[k];
     t.W1 = p.W1; t.b1 = p.b1; t.W2 = p.W2; t.b2 = p.b2; t.K = p.K;
     t.chunks = p.chunks; t.chunk = p.chunk; t.cl = p.tc_cluster; t.parts = p.chunks / p.tc_cluster;
-    tc_tile_shape(p.H, p.W, &t.th, &t.tw);
-    t.tiles_r = (p.H + t.th - 1) / t.th;
-    t.tiles_c = (p.W + t.tw - 1) / t.tw;
+    tc_tile_shape(p.H, p.W, &t.BR, &t.BC);
+    t.tiles_r = (p.H + 2 * t.BR - 1) / (2 * t.BR);
+    t.tiles_c = (p.W + 8 * t.BC - 1) / (8 * t.BC);
+    t.tiles = p.slices * t.tiles_r * t.tiles_c;
     const bool mlp = p.wmode == LISA_W_MLP;
     t.n_umat = mlp ? p.T - 1 : 1;
     t.epi_rows = 64 * t.n_umat + 16;
     t.n_mlp = mlp ? (p.hidden + 15) / 16 * 16 : 0;
     t.s_part = p.s_part; t.part = p.tc_part; t.bepi = p.tc_bepi; t.w1img = p.tc_w1img; t.err = p.err;
+    const bool fused = tc_fused(p.chunks, p.tc_cluster, p.chunk);
+    // stage index of each kernel in this chain (-1: not part of it)
+    const int s_keysum = fused ? -1 : 0, s_stats = fused ? 0 : 1, s_recur = fused ? -1 : 2,
+              s_epi = fused ? 1 : 3;
+    auto run = [&](int s) { return s >= 0 && (stage < 0 || stage == s); };
 
     cudaLaunchAttribute attrs[2];
+    attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[0].val.programmaticStreamSerializationAllowed = 1;
+    attrs[1].id = cudaLaunchAttributeClusterDimension;
+    attrs[1].val.clusterDim.x = (unsigned)t.cl;
+    attrs[1].val.clusterDim.y = 1;
+    attrs[1].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg{};
     cfg.stream = st;
-    cfg.attrs = attrs;
     cudaError_t err = cudaSuccess;
 
-    // 1. keysum
-    if (stage < 0 || stage == 0) {
+    if (run(s_keysum)) {   // first kernel of the split chain: plain stream order
         cfg.gridDim = dim3((unsigned)(p.slices * p.chunks));
         cfg.blockDim = dim3(256);
         cfg.dynamicSmemBytes = 0;
+        cfg.attrs = nullptr;
         cfg.numAttrs = 0;
-        err = cudaLaunchKernelEx(&cfg, tc_keysum_kernel, t);
-        if (err != cudaSuccess) return err;
+        if ((err = cudaLaunchKernelEx(&cfg, tc_keysum_kernel, t)) != cudaSuccess) return err;
     }
-    attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attrs[0].val.programmaticStreamSerializationAllowed = 1;
-    // 2. stats
-    if (stage < 0 || stage == 1) {
+    if (run(s_stats)) {
         CUtensorMap mq, mk, mv;
         if (!make_map_tokens(&mq, p.Q, p.slices, p.n) || !make_map_tokens(&mk, p.K, p.slices, p.n) ||
             !make_map_tokens(&mv, p.V, p.slices, p.n))
             return cudaErrorInvalidValue;
-        const int smem = kStages * kStageBytes + 1024;
-        if ((err = set_smem(tc_stats_kernel, 0, smem)) != cudaSuccess) return err;
         cfg.gridDim = dim3((unsigned)(p.slices * p.chunks));
         cfg.blockDim = dim3(128);
-        cfg.dynamicSmemBytes = smem;
-        attrs[1].id = cudaLaunchAttributeClusterDimension;
-        attrs[1].val.clusterDim.x = (unsigned)t.cl;
-        attrs[1].val.clusterDim.y = 1;
-        attrs[1].val.clusterDim.z = 1;
-        cfg.numAttrs = 2;
-        err = cudaLaunchKernelEx(&cfg, tc_stats_kernel, mq, mk, mv, t);
-        if (err != cudaSuccess) return err;
+        if (fused) {
+            const int nsub = (p.chunk + kSub - 1) / kSub;
+            int kres = nsub * kSubBytes;
+            const int ring = kStages * 2 * kSubBytes;
+            if (kres + ring < kFusedWork) kres = kFusedWork - ring;
+            const int smem = kres + ring + 1024;
+            if ((err = set_smem(tc_stats_fused_kernel, 0, smem)) != cudaSuccess) return err;
+            cfg.dynamicSmemBytes = smem;
+            cfg.blockDim = dim3(kStatsThreads);
+            cfg.attrs = attrs + 1;    // first kernel of the fused chain: cluster only
+            cfg.numAttrs = 1;
+            if ((err = cudaLaunchKernelEx(&cfg, tc_stats_fused_kernel, mq, mk, mv, t, kres)) != cudaSuccess)
+                return err;
+        } else {
+            const int smem = kStages * 3 * kSubBytes + 1024;
+            if ((err = set_smem(tc_stats_split_kernel, 1, smem)) != cudaSuccess) return err;
+            cfg.dynamicSmemBytes = smem;
+            cfg.blockDim = dim3(kStatsThreads);
+            cfg.attrs = attrs;
+            cfg.numAttrs = 2;
+            if ((err = cudaLaunchKernelEx(&cfg, tc_stats_split_kernel, mq, mk, mv, t)) != cudaSuccess) return err;
+        }
     }
-    // 3. recur
-    if (stage < 0 || stage == 2) {
+    if (run(s_recur)) {
         cfg.gridDim = dim3((unsigned)(p.slices * kRecurRowBlocks));
         cfg.blockDim = dim3(256);
         cfg.dynamicSmemBytes = 0;
+        cfg.attrs = attrs;
         cfg.numAttrs = 1;
-        err = cudaLaunchKernelEx(&cfg, tc_recur_kernel, t);
-        if (err != cudaSuccess) return err;
+        if ((err = cudaLaunchKernelEx(&cfg, tc_recur_kernel, t)) != cudaSuccess) return err;
     }
-    // 4. epilogue
-    if (stage < 0 || stage == 3) {
+    if (run(s_epi)) {
         CUtensorMap mq, mkh, mvh, mkt, mo;
-        if (!make_map_grid(&mq, p.Q, p.slices, p.H, p.W, t.th, t.tw) ||
-            !make_map_grid(&mkh, p.K, p.slices, p.H, p.W, t.th + 2, t.tw + 2) ||
-            !make_map_grid(&mvh, p.V, p.slices, p.H, p.W, t.th + 2, t.tw + 2) ||
-            !make_map_grid(&mkt, p.K, p.slices, p.H, p.W, t.th, t.tw) ||
-            !make_map_grid(&mo, p.O, p.slices, p.H, p.W, t.th, t.tw))
+        const int th = 2 * t.BR, tw = 8 * t.BC;
+        if (!make_map_grid(&mq, p.Q, p.slices, p.H, p.W, th, 8) ||
+            !make_map_grid(&mkh, p.K, p.slices, p.H, p.W, th + 2, tw + 2) ||
+            !make_map_grid(&mvh, p.V, p.slices, p.H, p.W, th + 2, tw + 2) ||
+            !make_map_grid(&mkt, p.K, p.slices, p.H, p.W, th, 8) ||
+            !make_map_grid(&mo, p.O, p.slices, p.H, p.W, th, 8))
             return cudaErrorInvalidValue;
-        const EpiLayout L = epi_layout(t.th, t.tw, t.epi_rows, t.n_mlp, mlp);
+        // fixed weights: two CTAs per SM, one input buffer each (one CTA's
+        // loads overlap the other's compute); adaptive weights: one CTA per SM
+        // with two input buffers when they fit
+        EpiLayout L;
+        int per_sm;
+        if (!mlp) {
+            L = epi_layout(t.BR, t.BC, t.epi_rows, t.n_mlp, mlp, 1);
+            t.epi_stages = 1;
+            per_sm = 2;
+        } else {
+            L = epi_layout(t.BR, t.BC, t.epi_rows, t.n_mlp, mlp, 2);
+            t.epi_stages = 2;
+            if (L.total + 1024 > 227 * 1024) {
+                L = epi_layout(t.BR, t.BC, t.epi_rows, t.n_mlp, mlp, 1);
+                t.epi_stages = 1;
+            }
+            per_sm = 1;
+        }
         const int smem = (int)L.total + 1024;
-        if ((err = set_smem(tc_epilogue_kernel, 1, smem)) != cudaSuccess) return err;
         const uint32_t cols = pow2_cols(t.epi_rows + t.n_mlp);
-        cfg.gridDim = dim3((unsigned)(p.slices * t.tiles_r * t.tiles_c));
+        const int nctas = per_sm * sm_count();
+        cfg.gridDim = dim3((unsigned)(t.tiles < nctas ? t.tiles : nctas));
         cfg.blockDim = dim3(256);
         cfg.dynamicSmemBytes = smem;
+        cfg.attrs = attrs;
         cfg.numAttrs = 1;
-        err = cudaLaunchKernelEx(&cfg, tc_epilogue_kernel, mq, mkh, mvh, mkt, mo, t, cols);
+        if (mlp) {
+            if ((err = set_smem(tc_epilogue_kernel<true>, 2, smem)) != cudaSuccess) return err;
+            err = cudaLaunchKernelEx(&cfg, tc_epilogue_kernel<true>, mq, mkh, mvh, mkt, mo, t, cols);
+        } else {
+            if ((err = set_smem(tc_epilogue_kernel<false>, 3, smem)) != cudaSuccess) return err;
+            err = cudaLaunchKernelEx(&cfg, tc_epilogue_kernel<false>, mq, mkh, mvh, mkt, mo, t, cols);
+        }
         if (err != cudaSuccess) return err;
     }
     return cudaGetLastError();
 }
 
-const char *const kTcStageNames[kTcStages] = {"tc_keysum", "tc_stats", "tc_recur", "tc_epilogue"};
+int tc_num_stages(int chunks, int cluster, int chunk) { return tc_fused(chunks, cluster, chunk) ? 2 : 4; }
+
+const char *tc_stage_name(int chunks, int cluster, int chunk, int stage) {
+    static const char *const split[4] = {"tc_keysum", "tc_stats", "tc_recur", "tc_epilogue"};
+    static const char *const fused[2] = {"tc_stats_fused", "tc_epilogue"};
+    if (tc_fused(chunks, cluster, chunk)) return (stage >= 0 && stage < 2) ? fused[stage] : nullptr;
+    return (stage >= 0 && stage < 4) ? split[stage] : nullptr;
+}
 
 }  // namespace lisa

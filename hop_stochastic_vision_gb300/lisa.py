@@ -81,9 +81,9 @@ def load(path: str = LIB_PATH):
         lib.lisa_forward_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, wp, vp,
                                           f, i, i, vp, sz, vp]
         lib.lisa_forward_host.restype = i
-        lib.lisa_num_stages.argtypes = [i, i, i, wp]
+        lib.lisa_num_stages.argtypes = [i, i, i, i, i, i, i, wp]
         lib.lisa_num_stages.restype = i
-        lib.lisa_stage_name.argtypes = [i, i, i, wp, i]
+        lib.lisa_stage_name.argtypes = [i, i, i, i, i, i, i, wp, i]
         lib.lisa_stage_name.restype = ctypes.c_char_p
         lib.lisa_forward_stage.argtypes = [i] + lib.lisa_forward.argtypes
         lib.lisa_forward_stage.restype = i
@@ -118,12 +118,12 @@ def lisa_forward(Q, K, V, O, B, heads, H, W, d_h, d_v, T, wts, alpha, eps, relu_
                                    eps, relu_inputs, dtype, workspace, workspace_bytes, stream))
 
 
-def lisa_num_stages(dtype, d_h, T, wts) -> int:
-    return int(load().lisa_num_stages(dtype, d_h, T, ctypes.byref(wts)))
+def lisa_num_stages(B, heads, H, W, d_h, T, dtype, wts) -> int:
+    return int(load().lisa_num_stages(B, heads, H, W, d_h, T, dtype, ctypes.byref(wts)))
 
 
-def lisa_stage_name(dtype, d_h, T, wts, stage):
-    r = load().lisa_stage_name(dtype, d_h, T, ctypes.byref(wts), stage)
+def lisa_stage_name(B, heads, H, W, d_h, T, dtype, wts, stage):
+    r = load().lisa_stage_name(B, heads, H, W, d_h, T, dtype, ctypes.byref(wts), stage)
     return None if r is None else r.decode()
 
 

@@ -128,13 +128,16 @@ lisa_status lisa_forward_host(const void *hQ, const void *hK, const void *hV, vo
  * stages 0 .. n-1 in order on one stream with one workspace computes exactly
  * what lisa_forward computes (each stage reads what the earlier ones left in
  * the workspace), so a caller can put timing events between the kernels.
- * The chain depends on dtype, d_h, T and the weights (mode, MLP width);
- * lisa_num_stages returns 0 for a NULL weight struct.  lisa_stage_name
- * returns the kernel's name, or NULL for a bad index.
+ * The chain depends on the problem's sizes, dtype and weights (mode, MLP
+ * width); lisa_num_stages returns 0 for arguments lisa_forward would reject
+ * or for an empty problem.  lisa_stage_name returns the kernel's name, or
+ * NULL for a bad index.
  * A bad stage index returns LISA_ERR_INVALID_ARG.
  */
-int lisa_num_stages(int dtype, int d_h, int T, const lisa_weights *wts);
-const char *lisa_stage_name(int dtype, int d_h, int T, const lisa_weights *wts, int stage);
+int lisa_num_stages(int B, int heads, int H, int W, int d_h, int T, int dtype,
+                    const lisa_weights *wts);
+const char *lisa_stage_name(int B, int heads, int H, int W, int d_h, int T, int dtype,
+                            const lisa_weights *wts, int stage);
 lisa_status lisa_forward_stage(int stage, const void *Q, const void *K, const void *V, void *O,
                                int B, int heads, int H, int W, int d_h, int d_v, int T,
                                const lisa_weights *wts, const float *alpha, float eps,
