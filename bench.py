@@ -68,6 +68,24 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The slowest rank's value (a collective over the default process group
+    when world > 1; identity otherwise)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_throughput(world: int, units_per_rank: int, steps: int, ms_max: float) -> float:
+    """Whole-job units per second: every rank processed its own batch of
+    `units_per_rank` per step; the job took the slowest rank's time."""
+    return world * units_per_rank * steps / (ms_max / 1e3)
+
+
 def host_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -366,12 +384,8 @@ def ours_arm(args, shape):
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
-    ms = start.elapsed_time(end)
-    t = torch.tensor([ms], device=dev, dtype=torch.float64)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
-    value = world * units * args.steps / (ms_max / 1e3)
+    ms_max = max_over_ranks(start.elapsed_time(end), world, dev)
+    value = weak_throughput(world, units, args.steps, ms_max)
 
     # per-kernel pass: events between the kernels of each step; the stream is
     # held by a short bounded sleep while the host enqueues, so the kernels
@@ -425,10 +439,7 @@ def ours_arm(args, shape):
                 raise RuntimeError("lisa_forward_host: " + lisa.lisa_status_string(rc))
         e1.record(stream)
     torch.cuda.synchronize(dev)
-    te = torch.tensor([e0.elapsed_time(e1)], device=dev, dtype=torch.float64)
-    if world > 1:
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-    e2e_value = world * units * Ke / (float(te.item()) / 1e3)
+    e2e_value = weak_throughput(world, units, Ke, max_over_ranks(e0.elapsed_time(e1), world, dev))
     io_bytes = inp["xq"].numel() * inp["xq"].element_size()
 
     cpu = None
