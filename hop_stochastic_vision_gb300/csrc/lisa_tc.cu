@@ -132,6 +132,11 @@ __device__ __forceinline__ float4 ld_dsmem4(uint32_t addr) {
                  : "r"(addr));
     return v;
 }
+__device__ __forceinline__ void st_dsmem4(uint32_t addr, float4 v) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
+                 "f"(v.w)
+                 : "memory");
+}
 __device__ __forceinline__ float ld_dsmem(uint32_t addr) {
     float v;
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
@@ -179,7 +184,7 @@ __device__ __forceinline__ void form_qtilde(uint8_t *Qb, const float *s, float e
                                             int tid) {
     const int j = tid >> 1, h = tid & 1;
     uint4 q[4];
-    float dot = 0.f;
+    float part[4] = {0.f, 0.f, 0.f, 0.f};   // one partial sum per 16-byte chunk
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         const int chunk = 4 * h + k;
@@ -188,10 +193,11 @@ __device__ __forceinline__ void form_qtilde(uint8_t *Qb, const float *s, float e
         const uint32_t w4[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            dot = fmaf(bf16_lo(w4[e]), s[chunk * 8 + 2 * e], dot);
-            dot = fmaf(bf16_hi(w4[e]), s[chunk * 8 + 2 * e + 1], dot);
+            part[k] = fmaf(bf16_lo(w4[e]), s[chunk * 8 + 2 * e], part[k]);
+            part[k] = fmaf(bf16_hi(w4[e]), s[chunk * 8 + 2 * e + 1], part[k]);
         }
     }
+    float dot = (part[0] + part[1]) + (part[2] + part[3]);
     dot += __shfl_xor_sync(0xffffffffu, dot, 1);
     const float r = 1.f / (dot + eps);
 #pragma unroll
@@ -321,6 +327,8 @@ __global__ void __launch_bounds__(kStatsThreads) tc_stats_fused_kernel(const __g
             mbar_arrive_expect_tx(smem_u32(&kbar), nsub * kSubBytes);
             for (int i = 0; i < nsub; ++i)
                 tma_load_3d(base + i * kSubBytes, &mK, 0, t0 + i * kSub, sl, smem_u32(&kbar));
+            // K gates the key sum and the cluster exchange: let it land first
+            if (!mbar_wait(smem_u32(&kbar), 0)) record_error(p.err, kErrTimeoutLoad);
             for (int i = 0; i < kStages && i < nsub; ++i) {
                 const uint32_t fb = smem_u32(&full_bar[i]);
                 mbar_arrive_expect_tx(fb, kStage);
@@ -426,52 +434,39 @@ __global__ void __launch_bounds__(kStatsThreads) tc_stats_fused_kernel(const __g
         tc_fence_after();
     }
 
-    // ---- cluster reduction: rank q sums rows q, q + CL, ... (fixed order)
+    // ---- cluster reduction (fixed rank order): rank q sums rows q, q + CL, ...
+    // and pushes each reduced M^T row into every CTA's copy of M^T; its own
+    // U_1^T rows stay local.
     float *red = reinterpret_cast<float *>(sm);                    // [128][68]
-    float *redsum = reinterpret_cast<float *>(sm + 36 * 1024);     // [128][64] own rows
+    float *Mt = reinterpret_cast<float *>(sm + 36 * 1024);         // [64][64], filled by the owners
+    float *Ucur = reinterpret_cast<float *>(sm + 52 * 1024);       // [my_u][64]
+    const int my_u = (64 - (int)rank + CL - 1) / CL;               // own rows e < 64
     if (warp < 4) tmem_rows_to_smem(tmem, red, warp, lane);
     tc_fence_before();
     cluster_sync();                                                // (B)
-    const uint32_t red_addr = smem_u32(red);
-    const int my_rows = (128 - (int)rank + CL - 1) / CL;
-    for (int item = tid; item < my_rows * 16; item += kStatsThreads) {
-        const int rr = (int)rank + CL * (item >> 4);
-        const int f = item & 15;
-        const uint32_t off = (uint32_t)(rr * kRedStride + 4 * f) * 4u;
-        reinterpret_cast<float4 *>(redsum + rr * kD)[f] = cluster_sum4(red_addr + off, CL);
-    }
-    cluster_sync();                                                // (C)
-
-    // ---- M^T (rows 64..127) gathered from their owners; own U_1^T rows
-    float *Mt = reinterpret_cast<float *>(sm);                     // [64][64]
-    float *Ucur = reinterpret_cast<float *>(sm + 16 * 1024);       // [my_u][64]
-    const int my_u = (64 - (int)rank + CL - 1) / CL;               // own rows e < 64
-    const uint32_t redsum_addr = smem_u32(redsum);
-    if (tid < 128) {
-        float4 v[8];
+    {
+        const uint32_t red_addr = smem_u32(red);
+        const uint32_t mt_addr = smem_u32(Mt);
+        const int my_rows = (128 - (int)rank + CL - 1) / CL;
+        for (int item = tid; item < my_rows * 16; item += kStatsThreads) {
+            const int k = item >> 4, f = item & 15;
+            const int rr = (int)rank + CL * k;
+            const float4 v = cluster_sum4(red_addr + (uint32_t)(rr * kRedStride + 4 * f) * 4u, CL);
+            if (rr < 64) {
+                reinterpret_cast<float4 *>(Ucur + k * kD)[f] = v;
+            } else {
+                const uint32_t dst = mt_addr + (uint32_t)((rr - 64) * kD + 4 * f) * 4u;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {          // 1024 float4 of M^T, 8 per thread
-            const int item = tid + 128 * u;
-            const int rr = 64 + (item >> 4);
-            const uint32_t off = (uint32_t)(rr * kD + 4 * (item & 15)) * 4u;
-            v[u] = ld_dsmem4(map_rank(redsum_addr + off, (uint32_t)(rr % CL)));
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int item = tid + 128 * u;
-            reinterpret_cast<float4 *>(Mt + (item >> 4) * kD)[item & 15] = v[u];
+                for (int q = 0; q < 8; ++q)
+                    if (q < CL) st_dsmem4(map_rank(dst, (uint32_t)q), v);
+            }
         }
     }
-    for (int item = tid; item < my_u * 16; item += kStatsThreads) {
-        const int i = item >> 4, f = item & 15;
-        const int e = (int)rank + CL * i;
-        reinterpret_cast<float4 *>(Ucur + i * kD)[f] = reinterpret_cast<const float4 *>(redsum + e * kD)[f];
-    }
-    cluster_sync();   // (D) every CTA is done reading the others' redsum
+    cluster_sync();                                                // (C) M^T complete everywhere
 
     // ---- U_k^T = U_(k-1)^T M^T on the own rows; B operand rows
-    float *Unext = reinterpret_cast<float *>(sm + 36 * 1024);
-    float *Fold = reinterpret_cast<float *>(sm + 52 * 1024);
+    float *Unext = reinterpret_cast<float *>(sm);
+    float *Fold = reinterpret_cast<float *>(sm + 16 * 1024);
     const bool folded = (p.wmode != LISA_W_MLP);
     uint8_t *img = p.bepi + (size_t)sl * p.epi_rows * kRow;
     for (int idx = tid; idx < my_u * kD; idx += kStatsThreads) Fold[idx] = 0.f;
@@ -742,13 +737,12 @@ __global__ void __launch_bounds__(256) tc_recur_kernel(TcParams p) {
 // epilogue
 // ===========================================================================
 struct EpiLayout {
-    uint32_t q, kh, vh, bepi, kt, stage, w1, out, total;
+    uint32_t q, kh, vh, bepi, kt, w1, out, total;
 };
 
 __host__ __device__ inline uint32_t align1k(uint32_t x) { return (x + 1023u) & ~1023u; }
 
-__host__ __device__ inline EpiLayout epi_layout(int BR, int BC, int epi_rows, int n_mlp, bool mlp,
-                                                int stages) {
+__host__ __device__ inline EpiLayout epi_layout(int BR, int BC, int epi_rows, int n_mlp, bool mlp) {
     EpiLayout L;
     const uint32_t halo = align1k((uint32_t)(2 * BR + 2) * (8 * BC + 2) * kRow);
     uint32_t off = 0;
@@ -757,8 +751,6 @@ __host__ __device__ inline EpiLayout epi_layout(int BR, int BC, int epi_rows, in
     L.vh = off; off += halo;
     L.bepi = off; off += align1k((uint32_t)epi_rows * kRow);
     L.kt = off; if (mlp) off += 128 * kRow;
-    L.stage = off;                     // bytes per input stage
-    off *= (uint32_t)stages;
     L.w1 = off; if (mlp) off += align1k(2u * n_mlp * kRow);
     L.out = off; off += 128 * kRow;
     L.total = off;
@@ -769,20 +761,8 @@ __device__ __forceinline__ float gelu_erf(float x) {
     return 0.5f * x * (1.f + erff(x * 0.70710678118654752f));
 }
 
-// 16 TMEM lanes x 8 consecutive fp32 columns in mma.sync C-fragment layout:
-// f0,f1 = (row g, cols 2q, 2q+1), f2,f3 = (row g+8, same cols).
-__device__ __forceinline__ void tmem_ld_frag(uint32_t taddr, float (&f)[4]) {
-    uint32_t r0, r1, r2, r3;
-    asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(taddr)
-                 : "memory");
-    tc_wait_ld();
-    f[0] = __uint_as_float(r0); f[1] = __uint_as_float(r1);
-    f[2] = __uint_as_float(r2); f[3] = __uint_as_float(r3);
-}
-
-// Same layout, no wait: 8 repetitions cover 64 columns (32 registers).
+// 16 TMEM lanes x 8 consecutive fp32 columns per repetition, in mma.sync
+// C-fragment layout: regs 4r+0,1 = (row g, cols 8r+2q, +1), 4r+2,3 = (row g+8, same).
 __device__ __forceinline__ void tmem_ld_frag8_nowait(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
@@ -815,43 +795,49 @@ __device__ __forceinline__ TileCoord tile_coord(const TcParams &p, int t) {
     return tc;
 }
 
-// TMA loads of one tile into the stage at `sbase`: Q (and K) as BC boxes of
-// 8 columns x 2 BR rows (block-major rows), the K and V halos, and the slice's
-// B operand when the stage does not hold it yet.
-__device__ __forceinline__ void epi_issue_loads(const TcParams &p, const EpiLayout &L, uint32_t sbase,
-                                                uint32_t bar, TileCoord tc, bool load_bepi, bool mlp,
-                                                const CUtensorMap *mQ, const CUtensorMap *mKh,
-                                                const CUtensorMap *mVh, const CUtensorMap *mKt) {
+// Tile inputs are refilled piecewise, each as soon as the current tile no
+// longer reads it: Q (and K rows) + K halo after the scores, the B operand
+// after the tensor-core products, the V halo after the values.
+__device__ __forceinline__ void epi_load_qk(const TcParams &p, const EpiLayout &L, uint32_t base, uint32_t bar,
+                                            TileCoord tc, bool mlp, const CUtensorMap *mQ, const CUtensorMap *mKh,
+                                            const CUtensorMap *mKt) {
     const uint32_t halo_rows = (uint32_t)(2 * p.BR + 2) * (8 * p.BC + 2);
-    uint32_t bytes = (128u + 2u * halo_rows + (mlp ? 128u : 0u)) * kRow;
-    if (load_bepi) bytes += (uint32_t)p.epi_rows * kRow;
-    mbar_arrive_expect_tx(bar, bytes);
+    mbar_arrive_expect_tx(bar, (128u + halo_rows + (mlp ? 128u : 0u)) * kRow);
     for (int bj = 0; bj < p.BC; ++bj) {
-        tma_load_4d(sbase + L.q + bj * 16 * p.BR * kRow, mQ, 0, tc.c0 + 8 * bj, tc.r0, tc.sl, bar);
-        if (mlp) tma_load_4d(sbase + L.kt + bj * 16 * p.BR * kRow, mKt, 0, tc.c0 + 8 * bj, tc.r0, tc.sl, bar);
+        tma_load_4d(base + L.q + bj * 16 * p.BR * kRow, mQ, 0, tc.c0 + 8 * bj, tc.r0, tc.sl, bar);
+        if (mlp) tma_load_4d(base + L.kt + bj * 16 * p.BR * kRow, mKt, 0, tc.c0 + 8 * bj, tc.r0, tc.sl, bar);
     }
-    tma_load_4d(sbase + L.kh, mKh, 0, tc.c0 - 1, tc.r0 - 1, tc.sl, bar);
-    tma_load_4d(sbase + L.vh, mVh, 0, tc.c0 - 1, tc.r0 - 1, tc.sl, bar);
-    if (load_bepi)
-        bulk_load(sbase + L.bepi, p.bepi + (size_t)tc.sl * p.epi_rows * kRow, (uint32_t)p.epi_rows * kRow, bar);
+    tma_load_4d(base + L.kh, mKh, 0, tc.c0 - 1, tc.r0 - 1, tc.sl, bar);
+}
+__device__ __forceinline__ void epi_load_v(const TcParams &p, const EpiLayout &L, uint32_t base, uint32_t bar,
+                                           TileCoord tc, const CUtensorMap *mVh) {
+    const uint32_t halo_rows = (uint32_t)(2 * p.BR + 2) * (8 * p.BC + 2);
+    mbar_arrive_expect_tx(bar, halo_rows * kRow);
+    tma_load_4d(base + L.vh, mVh, 0, tc.c0 - 1, tc.r0 - 1, tc.sl, bar);
+}
+__device__ __forceinline__ void epi_load_bepi(const TcParams &p, const EpiLayout &L, uint32_t base, uint32_t bar,
+                                              int sl) {
+    mbar_arrive_expect_tx(bar, (uint32_t)p.epi_rows * kRow);
+    bulk_load(base + L.bepi, p.bepi + (size_t)sl * p.epi_rows * kRow, (uint32_t)p.epi_rows * kRow, bar);
 }
 
 template <bool kMlp>
 __global__ void __launch_bounds__(256, kMlp ? 1 : 2) tc_epilogue_kernel(const __grid_constant__ CUtensorMap mQ,
-                                                             const __grid_constant__ CUtensorMap mKh,
-                                                             const __grid_constant__ CUtensorMap mVh,
-                                                             const __grid_constant__ CUtensorMap mKt,
-                                                             const __grid_constant__ CUtensorMap mO,
-                                                             TcParams p, uint32_t tmem_cols) {
+                                                                        const __grid_constant__ CUtensorMap mKh,
+                                                                        const __grid_constant__ CUtensorMap mVh,
+                                                                        const __grid_constant__ CUtensorMap mKt,
+                                                                        const __grid_constant__ CUtensorMap mO,
+                                                                        TcParams p, uint32_t tmem_cols) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ __align__(8) uint64_t load_bar[2], w1_bar, mma_bar;
+    __shared__ __align__(8) uint64_t qk_bar, v_bar, b_bar, w1_bar, mma_bar;
     __shared__ uint32_t tmem_slot;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     constexpr bool mlp = kMlp;
     const int BR = p.BR, BC = p.BC, hw = 8 * BC + 2;
-    const EpiLayout L = epi_layout(BR, BC, p.epi_rows, p.n_mlp, mlp, p.epi_stages);
+    const uint32_t halo_bytes = (uint32_t)(2 * BR + 2) * hw * kRow;
+    const EpiLayout L = epi_layout(BR, BC, p.epi_rows, p.n_mlp, mlp);
     const uint32_t base = smem_u32(sm);
     const int g = lane >> 2, q4 = lane & 3;
 
@@ -860,9 +846,15 @@ __global__ void __launch_bounds__(256, kMlp ? 1 : 2) tc_epilogue_kernel(const __
     const int bi = blk % BR, bj = blk / BR;
     const uint32_t lane_base = (uint32_t)(16 * blk) << 16;
 
+    // contiguous run of tiles (consecutive tiles mostly share a slice)
+    const int per_cta = (p.tiles + gridDim.x - 1) / gridDim.x;
+    const int t_begin = blockIdx.x * per_cta;
+    const int t_end = min(p.tiles, t_begin + per_cta);
+
     if (tid == 0) {
-        mbar_init(smem_u32(&load_bar[0]), 1);
-        mbar_init(smem_u32(&load_bar[1]), 1);
+        mbar_init(smem_u32(&qk_bar), 1);
+        mbar_init(smem_u32(&v_bar), 1);
+        mbar_init(smem_u32(&b_bar), 1);
         mbar_init(smem_u32(&w1_bar), 1);
         mbar_init(smem_u32(&mma_bar), 1);
         fence_mbar_init();
@@ -876,23 +868,23 @@ __global__ void __launch_bounds__(256, kMlp ? 1 : 2) tc_epilogue_kernel(const __
 
     // Per-lane constants of the local branch.  Window key kappa indexes the
     // 4 x 10 key window of the block: ka = kappa / 10, kb = kappa % 10.
-    uint32_t win_mask = 0;            // bit j*4+e: key of score element (j, e) is in the query's 3x3 window
-    uint32_t kab[5][2];               // (ka, kb) of the two keys of n-tile j
+    // Score element (j, e) of this lane: row g + 8 (e >> 1), key 8 j + 2 q + (e & 1).
+    uint32_t win_mask = 0;            // bit j*4+e: key in the query's 3x3 window
+    uint32_t ctr_mask = 0;            // bit j*4+e: key is the query token itself
 #pragma unroll
     for (int j = 0; j < 5; ++j)
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
             const int kappa = 8 * j + 2 * q4 + b;
             const int ka = kappa / 10, kb = kappa % 10;
-            kab[j][b] = (uint32_t)(ka | (kb << 8));
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int du = ka - h, dv = kb - g;
                 if (du >= 0 && du <= 2 && dv >= 0 && dv <= 2) win_mask |= 1u << (j * 4 + 2 * h + b);
+                if (du == 1 && dv == 1) ctr_mask |= 1u << (j * 4 + 2 * h + b);
             }
         }
-    // halo rows of the ldmatrix loads (static per warp)
-    uint32_t koff[3], voff[3];
+    uint32_t koff[3], voff[3];        // halo rows of the ldmatrix loads (static per warp)
 #pragma unroll
     for (int pr = 0; pr < 3; ++pr) {
         const int kk = 8 * (2 * pr + (lane >> 4)) + (lane & 7);          // scores: n-tile pairs
@@ -902,96 +894,73 @@ __global__ void __launch_bounds__(256, kMlp ? 1 : 2) tc_epilogue_kernel(const __
         voff[pr] = (uint32_t)((2 * bi + kv2 / 10) * hw + 8 * bj + kv2 % 10);
     }
     const int qrow = 16 * blk + (lane & 7) + 8 * ((lane >> 3) & 1);      // A-fragment row
-    // the block's own tokens in the halo (V_i of the w_0 V_i term): rows g, g+8
-    const uint32_t vi_row[2] = {(uint32_t)((2 * bi + 1) * hw + 8 * bj + g + 1),
-                                (uint32_t)((2 * bi + 2) * hw + 8 * bj + g + 1)};
+    const uint32_t orow[2] = {(uint32_t)(16 * blk + g), (uint32_t)(16 * blk + g + 8)};
+    const uint32_t obase[2] = {orow[0] * kRow + 4 * q4, orow[1] * kRow + 4 * q4};
 
-    const int first = blockIdx.x;
-    const int step = gridDim.x;
-    int last_slice[2] = {-1, -1};
-    if (tid == 0 && first < p.tiles) {
-        // Q, K, V of the first tile do not depend on the earlier kernels
-        const TileCoord tc = tile_coord(p, first);
-        const uint32_t bar = smem_u32(&load_bar[0]);
-        const uint32_t halo_rows = (uint32_t)(2 * BR + 2) * hw;
-        mbar_arrive_expect_tx(bar, (128u + 2u * halo_rows + (mlp ? 128u : 0u) + (uint32_t)p.epi_rows) * kRow);
-        for (int b2 = 0; b2 < BC; ++b2) {
-            tma_load_4d(base + L.q + b2 * 16 * BR * kRow, &mQ, 0, tc.c0 + 8 * b2, tc.r0, tc.sl, bar);
-            if (mlp) tma_load_4d(base + L.kt + b2 * 16 * BR * kRow, &mKt, 0, tc.c0 + 8 * b2, tc.r0, tc.sl, bar);
-        }
-        tma_load_4d(base + L.kh, &mKh, 0, tc.c0 - 1, tc.r0 - 1, tc.sl, bar);
-        tma_load_4d(base + L.vh, &mVh, 0, tc.c0 - 1, tc.r0 - 1, tc.sl, bar);
+    // ---- prologue: the first tile's Q, K, V do not depend on the earlier kernels
+    if (tid == 0 && t_begin < t_end) {
+        const TileCoord tc = tile_coord(p, t_begin);
+        epi_load_qk(p, L, base, smem_u32(&qk_bar), tc, mlp, &mQ, &mKh, &mKt);
+        epi_load_v(p, L, base, smem_u32(&v_bar), tc, &mVh);
     }
-    pdl_wait();  // B operands of every slice are ready
-    if (tid == 0 && first < p.tiles) {
-        const TileCoord tc = tile_coord(p, first);
-        bulk_load(base + L.bepi, p.bepi + (size_t)tc.sl * p.epi_rows * kRow, (uint32_t)p.epi_rows * kRow,
-                  smem_u32(&load_bar[0]));
-        if (mlp) {
-            mbar_arrive_expect_tx(smem_u32(&w1_bar), 2u * p.n_mlp * kRow);
-            bulk_load(base + L.w1, p.w1img, 2u * p.n_mlp * kRow, smem_u32(&w1_bar));
-        }
-    }
-    if (first < p.tiles) last_slice[0] = tile_coord(p, first).sl;
-    if (mlp && first < p.tiles && !mbar_wait(smem_u32(&w1_bar), 0)) record_error(p.err, kErrTimeoutLoad);
+    // The B operands come from the previous kernel: the first tile computes
+    // its local-branch scores before waiting for them (see the tile loop).
 
     const float c2 = 1.4426950408889634f * 0.125f;   // log2(e) / sqrt(64)
-    int it = 0;
-    for (int t = first; t < p.tiles; t += step, ++it) {
-        const int st = (p.epi_stages == 2) ? (it & 1) : 0;
-        const uint32_t sb = base + st * L.stage;
-        uint8_t *sp = sm + st * L.stage;
+    int b_loads = 1;                                  // B operands loaded so far (phase of b_bar)
+    int prev_sl = -1;
+    for (int t = t_begin, it = 0; t < t_end; ++t, ++it) {
         const TileCoord tc = tile_coord(p, t);
-        const int tn = t + step;
-        // prefetch the next tile into the other buffer (free since the last tile)
-        if (p.epi_stages == 2 && tid == 0 && tn < p.tiles) {
-            const int sn = st ^ 1;
-            const TileCoord tcn = tile_coord(p, tn);
-            epi_issue_loads(p, L, base + sn * L.stage, smem_u32(&load_bar[sn]), tcn, last_slice[sn] != tcn.sl, mlp,
-                            &mQ, &mKh, &mVh, &mKt);
-            last_slice[sn] = tcn.sl;
-        }
-        const uint32_t ph = (p.epi_stages == 2) ? ((it >> 1) & 1) : (it & 1);
-        if (!mbar_wait(smem_u32(&load_bar[st]), ph)) record_error(p.err, kErrTimeoutLoad);
-        if (tid == 0) bulk_wait_read0();   // the previous tile's store has read the output buffer
+        const bool has_next = t + 1 < t_end;
+        const TileCoord tn = tile_coord(p, has_next ? t + 1 : t);
+        const bool new_b = tc.sl != prev_sl;
+        prev_sl = tc.sl;
+
+        // ---- inputs of this tile
+        if (!mbar_wait(smem_u32(&qk_bar), it & 1)) record_error(p.err, kErrTimeoutLoad);
+        if (it > 0 && new_b && !mbar_wait(smem_u32(&b_bar), (b_loads - 1) & 1)) record_error(p.err, kErrTimeoutLoad);
         if (p.relu) {
-            relu_smem(sp + L.q, 128 * kRow, tid, 256);
-            if (mlp) relu_smem(sp + L.kt, 128 * kRow, tid, 256);
+            relu_smem(sm + L.q, 128 * kRow, tid, 256);
+            relu_smem(sm + L.kh, (int)halo_bytes, tid, 256);
+            if (mlp) relu_smem(sm + L.kt, 128 * kRow, tid, 256);
         }
         fence_proxy_async();
         __syncthreads();
 
-        // ---- tensor-core products into TMEM
-        if (tid == 0) {
+        // ---- tensor-core products into TMEM (one thread issues)
+        auto issue_mma = [&]() {
             tc_fence_after();
             for (int r = 0; r < p.epi_rows; r += 256) {
                 const int N = min(256, p.epi_rows - r);
                 const uint32_t idesc = make_idesc_bf16(128, N, false, false);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    tc_mma(tmem + r, make_desc_sw128(sb + L.q + ks * 32, 16, 1024),
-                           make_desc_sw128(sb + L.bepi + r * kRow + ks * 32, 16, 1024), idesc, ks > 0);
+                    tc_mma(tmem + r, make_desc_sw128(base + L.q + ks * 32, 16, 1024),
+                           make_desc_sw128(base + L.bepi + r * kRow + ks * 32, 16, 1024), idesc, ks > 0);
             }
             if (mlp) {
                 const uint32_t idesc = make_idesc_bf16(128, p.n_mlp, false, false);
                 for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t a = sb + (ks < 4 ? L.q : L.kt) + (ks & 3) * 32;
+                    const uint32_t a = base + (ks < 4 ? L.q : L.kt) + (ks & 3) * 32;
                     const uint32_t b = base + L.w1 + (ks < 4 ? 0u : (uint32_t)p.n_mlp * kRow) + (ks & 3) * 32;
                     tc_mma(tmem + p.epi_rows, make_desc_sw128(a, 16, 1024), make_desc_sw128(b, 16, 1024), idesc,
                            ks > 0);
                 }
             }
             tc_commit(smem_u32(&mma_bar));
+        };
+        if (tid == 0) {
+            if (it > 0) issue_mma();
+            bulk_wait_read0();   // the previous tile's store has read the output buffer
         }
 
-        // ---- local branch of this warp's block (mma.sync)
-        float lacc[8][4];
+        // ---- local branch scores: Q block (16 x 64) against its 4 x 10 key window
+        float sc[5][4];
         {
             uint32_t a[4][4];
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-                ldsm_x4(sb + L.q + sw128_offset(qrow, 2 * ks + (lane >> 4)), a[ks][0], a[ks][1], a[ks][2], a[ks][3]);
-            float sc[5][4];
+                ldsm_x4(base + L.q + sw128_offset(qrow, 2 * ks + (lane >> 4)), a[ks][0], a[ks][1], a[ks][2], a[ks][3]);
 #pragma unroll
             for (int j = 0; j < 5; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
 #pragma unroll
@@ -999,15 +968,100 @@ __global__ void __launch_bounds__(256, kMlp ? 1 : 2) tc_epilogue_kernel(const __
 #pragma unroll
                 for (int pr = 0; pr < 3; ++pr) {
                     uint32_t b0, b1, b2, b3;
-                    ldsm_x4(sb + L.kh + sw128_offset(koff[pr], 2 * ks + ((lane >> 3) & 1)), b0, b1, b2, b3);
-                    if (p.relu) {
-                        b0 = relu2(b0); b1 = relu2(b1); b2 = relu2(b2); b3 = relu2(b3);
-                    }
+                    ldsm_x4(base + L.kh + sw128_offset(koff[pr], 2 * ks + ((lane >> 3) & 1)), b0, b1, b2, b3);
                     mma_bf16_16816(sc[2 * pr], a[ks][0], a[ks][1], a[ks][2], a[ks][3], b0, b1);
                     if (pr < 2) mma_bf16_16816(sc[2 * pr + 1], a[ks][0], a[ks][1], a[ks][2], a[ks][3], b2, b3);
                 }
             }
-            // mask: the query's 3x3 window, keys inside the grid
+        }
+        __syncthreads();   // Q, K halo and (after the wait below) the B operand are free
+        if (it == 0) {
+            pdl_wait();    // the B operands (and the MLP image) of the previous kernel are ready
+            if (tid == 0) {
+                epi_load_bepi(p, L, base, smem_u32(&b_bar), tc.sl);
+                if (mlp) {
+                    mbar_arrive_expect_tx(smem_u32(&w1_bar), 2u * p.n_mlp * kRow);
+                    bulk_load(base + L.w1, p.w1img, 2u * p.n_mlp * kRow, smem_u32(&w1_bar));
+                }
+                if (!mbar_wait(smem_u32(&b_bar), 0)) record_error(p.err, kErrTimeoutLoad);
+                if (mlp && !mbar_wait(smem_u32(&w1_bar), 0)) record_error(p.err, kErrTimeoutLoad);
+                issue_mma();
+            }
+        }
+        if (tid == 0) {
+            if (!mbar_wait(smem_u32(&mma_bar), it & 1)) record_error(p.err, kErrTimeoutMma);
+            if (has_next) {
+                epi_load_qk(p, L, base, smem_u32(&qk_bar), tn, mlp, &mQ, &mKh, &mKt);
+                if (tn.sl != tc.sl) {
+                    epi_load_bepi(p, L, base, smem_u32(&b_bar), tn.sl);
+                }
+            }
+        }
+        if (has_next && tn.sl != tc.sl) ++b_loads;
+
+        const float alpha = p.alpha[tc.sl % p.heads];
+        const uint32_t tl = tmem + lane_base;
+        float w0[2], wk[2][LISA_MAX_T_MLP];
+        if (mlp) {
+            // adaptive step weights of rows g, g+8 from the MLP hidden layer in TMEM
+            if (!mbar_wait(smem_u32(&mma_bar), it & 1)) record_error(p.err, kErrTimeoutMma);
+            tc_fence_after();
+            uint32_t hr[8][4];
+#pragma unroll
+            for (int f8 = 0; f8 < 8; ++f8)
+                if (8 * f8 < p.n_mlp) tmem_ld_frag_nowait(tl + p.epi_rows + 8 * f8, hr[f8]);
+            tc_wait_ld();
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int t2 = 0; t2 < LISA_MAX_T_MLP; ++t2) wk[h][t2] = 0.f;
+#pragma unroll
+            for (int f8 = 0; f8 < 8; ++f8) {
+                if (8 * f8 >= p.n_mlp) break;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int m = 8 * f8 + 2 * q4 + (e & 1);
+                    if (m < p.hidden) {
+                        const float hv = gelu_erf(__uint_as_float(hr[f8][e]) + p.b1[m]);
+#pragma unroll
+                        for (int t2 = 0; t2 < LISA_MAX_T_MLP; ++t2)
+                            if (t2 < p.T) wk[e >> 1][t2] = fmaf(p.W2[t2 * p.hidden + m], hv, wk[e >> 1][t2]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                float zmax = -INFINITY;
+#pragma unroll
+                for (int t2 = 0; t2 < LISA_MAX_T_MLP; ++t2) {
+                    if (t2 >= p.T) break;
+                    float z = wk[h][t2];
+                    z += __shfl_xor_sync(0xffffffffu, z, 1);
+                    z += __shfl_xor_sync(0xffffffffu, z, 2);
+                    z += p.b2[t2];
+                    wk[h][t2] = z;
+                    zmax = fmaxf(zmax, z);
+                }
+                float zs = 0.f;
+#pragma unroll
+                for (int t2 = 0; t2 < LISA_MAX_T_MLP; ++t2) {
+                    if (t2 >= p.T) break;
+                    wk[h][t2] = expf(wk[h][t2] - zmax);
+                    zs += wk[h][t2];
+                }
+                const float zi = 1.f / zs;
+#pragma unroll
+                for (int t2 = 0; t2 < LISA_MAX_T_MLP; ++t2) wk[h][t2] *= zi;
+                w0[h] = wk[h][0];
+            }
+        } else {
+            w0[0] = w0[1] = p.w[0];
+        }
+
+        // ---- masked softmax over the window; the weight matrix also carries
+        // alpha w_0 on the token itself, so P' V = (1 - alpha) l_i + alpha w_0 V_i
+        float lacc[8][4];
+        {
             uint32_t mask = win_mask;
             const int gr0 = tc.r0 + 2 * bi - 1, gc0 = tc.c0 + 8 * bj - 1;   // grid position of window (0, 0)
             if (gr0 < 0 || gr0 + 3 >= p.H || gc0 < 0 || gc0 + 9 >= p.W) {
@@ -1015,7 +1069,8 @@ __global__ void __launch_bounds__(256, kMlp ? 1 : 2) tc_epilogue_kernel(const __
                 for (int j = 0; j < 5; ++j)
 #pragma unroll
                     for (int b = 0; b < 2; ++b) {
-                        const int gr = gr0 + (int)(kab[j][b] & 0xff), gc = gc0 + (int)(kab[j][b] >> 8);
+                        const int kappa = 8 * j + 2 * q4 + b;
+                        const int gr = gr0 + kappa / 10, gc = gc0 + kappa % 10;
                         if (gr < 0 || gr >= p.H || gc < 0 || gc >= p.W) mask &= ~(0x5u << (j * 4 + b));
                     }
             }
@@ -1024,8 +1079,7 @@ __global__ void __launch_bounds__(256, kMlp ? 1 : 2) tc_epilogue_kernel(const __
             for (int j = 0; j < 5; ++j)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const bool valid = (mask >> (j * 4 + e)) & 1u;
-                    sc[j][e] = valid ? sc[j][e] * c2 : -INFINITY;
+                    sc[j][e] = ((mask >> (j * 4 + e)) & 1u) ? sc[j][e] * c2 : -INFINITY;
                     mx[e >> 1] = fmaxf(mx[e >> 1], sc[j][e]);
                 }
             float sum[2] = {0.f, 0.f};
@@ -1042,12 +1096,21 @@ __global__ void __launch_bounds__(256, kMlp ? 1 : 2) tc_epilogue_kernel(const __
                     sc[j][e] = exp2f(sc[j][e] - mx[e >> 1]);
                     sum[e >> 1] += sc[j][e];
                 }
+            float scale[2], self[2];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 sum[h] += __shfl_xor_sync(0xffffffffu, sum[h], 1);
                 sum[h] += __shfl_xor_sync(0xffffffffu, sum[h], 2);
+                scale[h] = sum[h] > 0.f ? (1.f - alpha) / sum[h] : 0.f;
+                self[h] = alpha * w0[h];
             }
-            const float inv[2] = {sum[0] > 0.f ? 1.f / sum[0] : 0.f, sum[1] > 0.f ? 1.f / sum[1] : 0.f};
+#pragma unroll
+            for (int j = 0; j < 5; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    sc[j][e] = fmaf(sc[j][e], scale[e >> 1], ((ctr_mask >> (j * 4 + e)) & 1u) ? self[e >> 1] : 0.f);
+
+            if (!mbar_wait(smem_u32(&v_bar), it & 1)) record_error(p.err, kErrTimeoutLoad);
 #pragma unroll
             for (int nt = 0; nt < 8; ++nt) lacc[nt][0] = lacc[nt][1] = lacc[nt][2] = lacc[nt][3] = 0.f;
 #pragma unroll
@@ -1060,86 +1123,28 @@ __global__ void __launch_bounds__(256, kMlp ? 1 : 2) tc_epilogue_kernel(const __
 #pragma unroll
                 for (int np = 0; np < 4; ++np) {
                     uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(sb + L.vh + sw128_offset(voff[ks], 2 * np + (lane >> 4)), b0, b1, b2, b3);
+                    ldsm_x4_t(base + L.vh + sw128_offset(voff[ks], 2 * np + (lane >> 4)), b0, b1, b2, b3);
                     mma_bf16_16816(lacc[2 * np], pa0, pa1, pa2, pa3, b0, b1);
                     mma_bf16_16816(lacc[2 * np + 1], pa0, pa1, pa2, pa3, b2, b3);
                 }
             }
-#pragma unroll
-            for (int nt = 0; nt < 8; ++nt) {
-                lacc[nt][0] *= inv[0]; lacc[nt][1] *= inv[0];
-                lacc[nt][2] *= inv[1]; lacc[nt][3] *= inv[1];
-            }
         }
 
-        // ---- global branch from TMEM in fragment layout, mix, output tile
-        if (!mbar_wait(smem_u32(&mma_bar), it & 1)) record_error(p.err, kErrTimeoutMma);
+        // ---- global branch from TMEM (fragment layout) and output tile
+        if (!mlp && !mbar_wait(smem_u32(&mma_bar), it & 1)) record_error(p.err, kErrTimeoutMma);
         tc_fence_after();
         {
-            const float alpha = p.alpha[tc.sl % p.heads];
-            const uint32_t tl = tmem + lane_base;
-            uint32_t rs[4];
+            uint32_t rs[4], ru[32];
             tmem_ld_frag_nowait(tl + p.n_umat * kD, rs);     // Q.s_hi, Q.s_lo: columns held by lane q4 = 0
-            uint32_t hr[8][4];
-            if (mlp) {
-#pragma unroll
-                for (int f8 = 0; f8 < 8; ++f8)
-                    if (8 * f8 < p.n_mlp) tmem_ld_frag_nowait(tl + p.epi_rows + 8 * f8, hr[f8]);
-            }
-            uint32_t ru[32];
             tmem_ld_frag8_nowait(tl, ru);
             tc_wait_ld();
             const int src = lane & ~3;
             const float d0 = __shfl_sync(0xffffffffu, __uint_as_float(rs[0]) + __uint_as_float(rs[1]), src);
             const float d1 = __shfl_sync(0xffffffffu, __uint_as_float(rs[2]) + __uint_as_float(rs[3]), src);
-            const float rq[2] = {1.f / (d0 + p.eps), 1.f / (d1 + p.eps)};
-            float w0[2], wk[2][LISA_MAX_T_MLP];
+            // alpha / (Q_i . s + eps): the global term is alpha Q~_i U = alpha (Q_i U) / (Q_i . s + eps)
+            float arq[2] = {alpha / (d0 + p.eps), alpha / (d1 + p.eps)};
             float acc[32];
             if (mlp) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
-#pragma unroll
-                    for (int t2 = 0; t2 < LISA_MAX_T_MLP; ++t2) wk[h][t2] = 0.f;
-#pragma unroll
-                for (int f8 = 0; f8 < 8; ++f8) {
-                    if (8 * f8 >= p.n_mlp) break;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int m = 8 * f8 + 2 * q4 + (e & 1);
-                        if (m < p.hidden) {
-                            const float hv = gelu_erf(__uint_as_float(hr[f8][e]) + p.b1[m]);
-#pragma unroll
-                            for (int t2 = 0; t2 < LISA_MAX_T_MLP; ++t2)
-                                if (t2 < p.T) wk[e >> 1][t2] = fmaf(p.W2[t2 * p.hidden + m], hv, wk[e >> 1][t2]);
-                        }
-                    }
-                }
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    float zmax = -INFINITY;
-#pragma unroll
-                    for (int t2 = 0; t2 < LISA_MAX_T_MLP; ++t2) {
-                        if (t2 >= p.T) break;
-                        float z = wk[h][t2];
-                        z += __shfl_xor_sync(0xffffffffu, z, 1);
-                        z += __shfl_xor_sync(0xffffffffu, z, 2);
-                        z += p.b2[t2];
-                        wk[h][t2] = z;
-                        zmax = fmaxf(zmax, z);
-                    }
-                    float zs = 0.f;
-#pragma unroll
-                    for (int t2 = 0; t2 < LISA_MAX_T_MLP; ++t2) {
-                        if (t2 >= p.T) break;
-                        wk[h][t2] = expf(wk[h][t2] - zmax);
-                        zs += wk[h][t2];
-                    }
-                    const float zi = 1.f / zs;
-#pragma unroll
-                    for (int t2 = 0; t2 < LISA_MAX_T_MLP; ++t2) wk[h][t2] *= zi;
-                    w0[h] = wk[h][0];
-                }
-                // sum_k w_k(i) (Q U_k)_i: first block already loaded
 #pragma unroll
                 for (int k = 0; k < 32; ++k) acc[k] = wk[(k >> 1) & 1][1] * __uint_as_float(ru[k]);
                 for (int u = 1; u < p.n_umat; ++u) {
@@ -1149,40 +1154,27 @@ __global__ void __launch_bounds__(256, kMlp ? 1 : 2) tc_epilogue_kernel(const __
                     for (int k = 0; k < 32; ++k) acc[k] = fmaf(wk[(k >> 1) & 1][u + 1], __uint_as_float(ru[k]), acc[k]);
                 }
             } else {
-                w0[0] = w0[1] = p.w[0];
 #pragma unroll
                 for (int k = 0; k < 32; ++k) acc[k] = __uint_as_float(ru[k]);
             }
-            const float bl = 1.f - alpha;
-            const uint8_t *vh = sp + L.vh;
             uint8_t *out = sm + L.out;
-            const int orow[2] = {16 * blk + g, 16 * blk + g + 8};
 #pragma unroll
-            for (int nt = 0; nt < 8; ++nt) {
+            for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const uint32_t vv = *reinterpret_cast<const uint32_t *>(vh + sw128_offset(vi_row[h], nt) + 4 * q4);
-                    const float o0 = alpha * (w0[h] * bf16_lo(vv) + rq[h] * acc[4 * nt + 2 * h]) + bl * lacc[nt][2 * h];
-                    const float o1 =
-                        alpha * (w0[h] * bf16_hi(vv) + rq[h] * acc[4 * nt + 2 * h + 1]) + bl * lacc[nt][2 * h + 1];
-                    *reinterpret_cast<uint32_t *>(out + sw128_offset(orow[h], nt) + 4 * q4) = pack_bf16(o0, o1);
+                    const float o0 = fmaf(arq[h], acc[4 * nt + 2 * h], lacc[nt][2 * h]);
+                    const float o1 = fmaf(arq[h], acc[4 * nt + 2 * h + 1], lacc[nt][2 * h + 1]);
+                    *reinterpret_cast<uint32_t *>(out + obase[h] + ((nt ^ (orow[h] & 7u)) << 4)) = pack_bf16(o0, o1);
                 }
-            }
         }
         fence_proxy_async();
         tc_fence_before();
-        __syncthreads();
+        __syncthreads();   // output written; V halo and TMEM are free
         if (tid == 0) {
             for (int b2 = 0; b2 < BC; ++b2)
                 tma_store_4d(&mO, base + L.out + b2 * 16 * BR * kRow, 0, tc.c0 + 8 * b2, tc.r0, tc.sl);
             bulk_commit();
-            // single buffer: the inputs are consumed, load the next tile now
-            if (p.epi_stages == 1 && tn < p.tiles) {
-                const TileCoord tcn = tile_coord(p, tn);
-                epi_issue_loads(p, L, base, smem_u32(&load_bar[0]), tcn, last_slice[0] != tcn.sl, mlp, &mQ, &mKh,
-                                &mVh, &mKt);
-                last_slice[0] = tcn.sl;
-            }
+            if (has_next) epi_load_v(p, L, base, smem_u32(&v_bar), tn, &mVh);
         }
     }
     if (tid == 0) bulk_wait0();
@@ -1379,24 +1371,11 @@ cudaError_t launch_tc(const Problem &p, cudaStream_t st, int stage) {
             !make_map_grid(&mkt, p.K, p.slices, p.H, p.W, th, 8) ||
             !make_map_grid(&mo, p.O, p.slices, p.H, p.W, th, 8))
             return cudaErrorInvalidValue;
-        // fixed weights: two CTAs per SM, one input buffer each (one CTA's
-        // loads overlap the other's compute); adaptive weights: one CTA per SM
-        // with two input buffers when they fit
-        EpiLayout L;
-        int per_sm;
-        if (!mlp) {
-            L = epi_layout(t.BR, t.BC, t.epi_rows, t.n_mlp, mlp, 1);
-            t.epi_stages = 1;
-            per_sm = 2;
-        } else {
-            L = epi_layout(t.BR, t.BC, t.epi_rows, t.n_mlp, mlp, 2);
-            t.epi_stages = 2;
-            if (L.total + 1024 > 227 * 1024) {
-                L = epi_layout(t.BR, t.BC, t.epi_rows, t.n_mlp, mlp, 1);
-                t.epi_stages = 1;
-            }
-            per_sm = 1;
-        }
+        // fixed weights: two CTAs per SM (the warps of both hide each other's
+        // latencies); adaptive weights: one CTA per SM (registers)
+        const EpiLayout L = epi_layout(t.BR, t.BC, t.epi_rows, t.n_mlp, mlp);
+        t.epi_stages = 1;
+        const int per_sm = mlp ? 1 : 2;
         const int smem = (int)L.total + 1024;
         const uint32_t cols = pow2_cols(t.epi_rows + t.n_mlp);
         const int nctas = per_sm * sm_count();
