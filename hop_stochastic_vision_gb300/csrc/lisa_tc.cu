@@ -73,7 +73,8 @@ struct TcParams {
     int chunks, chunk, cl, parts;    // split-K plan; cluster size; cluster partials per slice
     int BR, BC;                      // epilogue tile = BR x BC blocks of 2 x 8 tokens
     int tiles_r, tiles_c, tiles;     // tiles per slice (rows, cols), total tiles
-    int epi_stages;                  // epilogue input buffers (1 or 2)
+    int epi_nbepi;                   // epilogue B-operand buffers (1 or 2)
+    int slot_cols;                   // TMEM columns per epilogue slot
     int n_umat, epi_rows, n_mlp;     // B operand: U blocks, rows, MLP width (multiple of 16)
     float *s_part;                   // [S][C][64] (split chain)
     float *part;                     // [S][P][128][64] (split chain)
@@ -514,13 +515,16 @@ __global__ void __launch_bounds__(256) tc_keysum_kernel(TcParams p) {
     float acc[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-    int j = t0 + j0;
-    for (; j + 224 < t1; j += 256) {
-        uint4 v[8];
+    // every thread keeps the loads of a 512-token batch in flight together
+    for (int jb = t0 + j0; jb < t1; jb += 512) {
+        uint4 v[16];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = __ldg(K + (size_t)(j + 32 * u) * 8 + cg);
+        for (int u = 0; u < 16; ++u) {
+            const int j = jb + 32 * u;
+            v[u] = j < t1 ? __ldg(K + (size_t)j * 8 + cg) : make_uint4(0u, 0u, 0u, 0u);
+        }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < 16; ++u) {
             const uint4 x = p.relu ? relu4(v[u]) : v[u];
             const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
@@ -528,16 +532,6 @@ __global__ void __launch_bounds__(256) tc_keysum_kernel(TcParams p) {
                 acc[2 * e] += bf16_lo(w4[e]);
                 acc[2 * e + 1] += bf16_hi(w4[e]);
             }
-        }
-    }
-    for (; j < t1; j += 32) {
-        uint4 x = __ldg(K + (size_t)j * 8 + cg);
-        if (p.relu) x = relu4(x);
-        const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            acc[2 * e] += bf16_lo(w4[e]);
-            acc[2 * e + 1] += bf16_hi(w4[e]);
         }
     }
 #pragma unroll
@@ -736,23 +730,53 @@ __global__ void __launch_bounds__(256) tc_recur_kernel(TcParams p) {
 // ===========================================================================
 // epilogue
 // ===========================================================================
+// Threads: eight compute warps, each owning one 2 x 8 token block of the
+// 128-token tile, and one control warp whose lane 0 issues every TMA load and
+// tensor-core MMA.  Tiles move through kSlots input slots; mbarriers carry
+// every hand-off, so no block-wide barrier sits inside the tile loop:
+//   qk_full, v_full    a slot's Q + K halo (+ the tile's K rows) / V halo landed
+//   qrelu              the compute warps wrote the ReLU'd Q (and K rows) back
+//   mma_full           the tile's products are in its TMEM slot
+//   qk_empty, v_empty  the compute warps no longer read the slot's Q/K, V
+//   tmem_empty         the compute warps have read their rows of the TMEM slot
+//   b_full, b_free     a B-operand buffer landed / its last MMA completed
+// Each compute warp stages its 2 x 8 output block in its own two buffers and
+// stores it with TMA itself.
+constexpr int kEpiWarps = 8;
+constexpr int kEpiThreads = 32 * (kEpiWarps + 1);
+constexpr uint32_t kOutBuf = 16 * kRow;   // one warp's 2 x 8 output block
+
 struct EpiLayout {
-    uint32_t q, kh, vh, bepi, kt, w1, out, total;
+    uint32_t q[2], kh[2], vh[2], kt[2], bepi[2], w1, out, total;
 };
 
 __host__ __device__ inline uint32_t align1k(uint32_t x) { return (x + 1023u) & ~1023u; }
 
-__host__ __device__ inline EpiLayout epi_layout(int BR, int BC, int epi_rows, int n_mlp, bool mlp) {
-    EpiLayout L;
+__host__ __device__ inline EpiLayout epi_layout(int BR, int BC, int epi_rows, int n_mlp, bool mlp, int slots,
+                                                int nbepi) {
+    EpiLayout L{};
     const uint32_t halo = align1k((uint32_t)(2 * BR + 2) * (8 * BC + 2) * kRow);
     uint32_t off = 0;
-    L.q = off; off += 128 * kRow;
-    L.kh = off; off += halo;
-    L.vh = off; off += halo;
-    L.bepi = off; off += align1k((uint32_t)epi_rows * kRow);
-    L.kt = off; if (mlp) off += 128 * kRow;
+    for (int s = 0; s < 2; ++s) {
+        if (s < slots) {
+            L.q[s] = off; off += 128 * kRow;
+            L.kh[s] = off; off += halo;
+            L.vh[s] = off; off += halo;
+            L.kt[s] = off; if (mlp) off += 128 * kRow;
+        } else {
+            L.q[s] = L.q[0]; L.kh[s] = L.kh[0]; L.vh[s] = L.vh[0]; L.kt[s] = L.kt[0];
+        }
+    }
+    for (int b = 0; b < 2; ++b) {
+        if (b < nbepi) {
+            L.bepi[b] = off;
+            off += align1k((uint32_t)epi_rows * kRow);
+        } else {
+            L.bepi[b] = L.bepi[0];
+        }
+    }
     L.w1 = off; if (mlp) off += align1k(2u * n_mlp * kRow);
-    L.out = off; off += 128 * kRow;
+    L.out = off; off += kEpiWarps * 2 * kOutBuf;
     L.total = off;
     return L;
 }
@@ -795,68 +819,45 @@ __device__ __forceinline__ TileCoord tile_coord(const TcParams &p, int t) {
     return tc;
 }
 
-// Tile inputs are refilled piecewise, each as soon as the current tile no
-// longer reads it: Q (and K rows) + K halo after the scores, the B operand
-// after the tensor-core products, the V halo after the values.
-__device__ __forceinline__ void epi_load_qk(const TcParams &p, const EpiLayout &L, uint32_t base, uint32_t bar,
-                                            TileCoord tc, bool mlp, const CUtensorMap *mQ, const CUtensorMap *mKh,
-                                            const CUtensorMap *mKt) {
-    const uint32_t halo_rows = (uint32_t)(2 * p.BR + 2) * (8 * p.BC + 2);
-    mbar_arrive_expect_tx(bar, (128u + halo_rows + (mlp ? 128u : 0u)) * kRow);
-    for (int bj = 0; bj < p.BC; ++bj) {
-        tma_load_4d(base + L.q + bj * 16 * p.BR * kRow, mQ, 0, tc.c0 + 8 * bj, tc.r0, tc.sl, bar);
-        if (mlp) tma_load_4d(base + L.kt + bj * 16 * p.BR * kRow, mKt, 0, tc.c0 + 8 * bj, tc.r0, tc.sl, bar);
-    }
-    tma_load_4d(base + L.kh, mKh, 0, tc.c0 - 1, tc.r0 - 1, tc.sl, bar);
-}
-__device__ __forceinline__ void epi_load_v(const TcParams &p, const EpiLayout &L, uint32_t base, uint32_t bar,
-                                           TileCoord tc, const CUtensorMap *mVh) {
-    const uint32_t halo_rows = (uint32_t)(2 * p.BR + 2) * (8 * p.BC + 2);
-    mbar_arrive_expect_tx(bar, halo_rows * kRow);
-    tma_load_4d(base + L.vh, mVh, 0, tc.c0 - 1, tc.r0 - 1, tc.sl, bar);
-}
-__device__ __forceinline__ void epi_load_bepi(const TcParams &p, const EpiLayout &L, uint32_t base, uint32_t bar,
-                                              int sl) {
-    mbar_arrive_expect_tx(bar, (uint32_t)p.epi_rows * kRow);
-    bulk_load(base + L.bepi, p.bepi + (size_t)sl * p.epi_rows * kRow, (uint32_t)p.epi_rows * kRow, bar);
-}
+struct EpiBars {
+    uint64_t qk_full[2], v_full[2], qrelu[2], mma_full[2], qk_empty[2], v_empty[2], tmem_empty[2];
+    uint64_t b_full[2], b_free[2], w1;
+};
 
-template <bool kMlp>
-__global__ void __launch_bounds__(256, kMlp ? 1 : 2) tc_epilogue_kernel(const __grid_constant__ CUtensorMap mQ,
-                                                                        const __grid_constant__ CUtensorMap mKh,
-                                                                        const __grid_constant__ CUtensorMap mVh,
-                                                                        const __grid_constant__ CUtensorMap mKt,
-                                                                        const __grid_constant__ CUtensorMap mO,
-                                                                        TcParams p, uint32_t tmem_cols) {
+template <bool kMlp, int kSlots, int kMinBlocks>
+__global__ void __launch_bounds__(kEpiThreads, kMinBlocks)
+    tc_epilogue_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mKh,
+                       const __grid_constant__ CUtensorMap mVh, const __grid_constant__ CUtensorMap mKt,
+                       const __grid_constant__ CUtensorMap mO, TcParams p, uint32_t tmem_cols) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ __align__(8) uint64_t qk_bar, v_bar, b_bar, w1_bar, mma_bar;
+    __shared__ __align__(8) EpiBars bar;
     __shared__ uint32_t tmem_slot;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     constexpr bool mlp = kMlp;
     const int BR = p.BR, BC = p.BC, hw = 8 * BC + 2;
-    const uint32_t halo_bytes = (uint32_t)(2 * BR + 2) * hw * kRow;
-    const EpiLayout L = epi_layout(BR, BC, p.epi_rows, p.n_mlp, mlp);
+    const EpiLayout L = epi_layout(BR, BC, p.epi_rows, p.n_mlp, mlp, kSlots, p.epi_nbepi);
     const uint32_t base = smem_u32(sm);
-    const int g = lane >> 2, q4 = lane & 3;
 
-    // this warp's 2 x 8 block: TMEM lanes 16 blk .. 16 blk + 15 (inside its quadrant)
-    const int blk = 2 * (warp & 3) + (warp >> 2);
-    const int bi = blk % BR, bj = blk / BR;
-    const uint32_t lane_base = (uint32_t)(16 * blk) << 16;
-
-    // contiguous run of tiles (consecutive tiles mostly share a slice)
-    const int per_cta = (p.tiles + gridDim.x - 1) / gridDim.x;
-    const int t_begin = blockIdx.x * per_cta;
-    const int t_end = min(p.tiles, t_begin + per_cta);
+    // contiguous run of tiles (consecutive tiles mostly share a slice); runs
+    // differ in length by at most one tile
+    const int t_begin = (int)((long long)blockIdx.x * p.tiles / gridDim.x);
+    const int t_end = (int)((long long)(blockIdx.x + 1) * p.tiles / gridDim.x);
 
     if (tid == 0) {
-        mbar_init(smem_u32(&qk_bar), 1);
-        mbar_init(smem_u32(&v_bar), 1);
-        mbar_init(smem_u32(&b_bar), 1);
-        mbar_init(smem_u32(&w1_bar), 1);
-        mbar_init(smem_u32(&mma_bar), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(smem_u32(&bar.qk_full[s]), 1);
+            mbar_init(smem_u32(&bar.v_full[s]), 1);
+            mbar_init(smem_u32(&bar.mma_full[s]), 1);
+            mbar_init(smem_u32(&bar.qrelu[s]), kEpiWarps);
+            mbar_init(smem_u32(&bar.qk_empty[s]), kEpiWarps);
+            mbar_init(smem_u32(&bar.v_empty[s]), kEpiWarps);
+            mbar_init(smem_u32(&bar.tmem_empty[s]), kEpiWarps);
+            mbar_init(smem_u32(&bar.b_full[s]), 1);
+            mbar_init(smem_u32(&bar.b_free[s]), 1);
+        }
+        mbar_init(smem_u32(&bar.w1), 1);
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(smem_u32(&tmem_slot), tmem_cols);
@@ -866,318 +867,397 @@ __global__ void __launch_bounds__(256, kMlp ? 1 : 2) tc_epilogue_kernel(const __
     const uint32_t tmem = tmem_slot;
     pdl_launch_dependents();
 
-    // Per-lane constants of the local branch.  Window key kappa indexes the
-    // 4 x 10 key window of the block: ka = kappa / 10, kb = kappa % 10.
-    // Score element (j, e) of this lane: row g + 8 (e >> 1), key 8 j + 2 q + (e & 1).
-    uint32_t win_mask = 0;            // bit j*4+e: key in the query's 3x3 window
-    uint32_t ctr_mask = 0;            // bit j*4+e: key is the query token itself
-#pragma unroll
-    for (int j = 0; j < 5; ++j)
-#pragma unroll
-        for (int b = 0; b < 2; ++b) {
-            const int kappa = 8 * j + 2 * q4 + b;
-            const int ka = kappa / 10, kb = kappa % 10;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int du = ka - h, dv = kb - g;
-                if (du >= 0 && du <= 2 && dv >= 0 && dv <= 2) win_mask |= 1u << (j * 4 + 2 * h + b);
-                if (du == 1 && dv == 1) ctr_mask |= 1u << (j * 4 + 2 * h + b);
+    if (warp == kEpiWarps) {
+        // ===================== control: TMA loads and tensor-core products
+        if (lane == 0 && t_begin < t_end) {
+            const uint32_t halo_tx = (uint32_t)(2 * BR + 2) * hw * kRow;
+            auto load_qk = [&](int t, int s) {
+                const TileCoord tc = tile_coord(p, t);
+                const uint32_t b = smem_u32(&bar.qk_full[s]);
+                mbar_arrive_expect_tx(b, (mlp ? 256u : 128u) * kRow + halo_tx);
+                for (int bj = 0; bj < BC; ++bj) {
+                    tma_load_4d(base + L.q[s] + bj * 16 * BR * kRow, &mQ, 0, tc.c0 + 8 * bj, tc.r0, tc.sl, b);
+                    if (mlp)
+                        tma_load_4d(base + L.kt[s] + bj * 16 * BR * kRow, &mKt, 0, tc.c0 + 8 * bj, tc.r0, tc.sl, b);
+                }
+                tma_load_4d(base + L.kh[s], &mKh, 0, tc.c0 - 1, tc.r0 - 1, tc.sl, b);
+            };
+            auto load_v = [&](int t, int s) {
+                const TileCoord tc = tile_coord(p, t);
+                const uint32_t b = smem_u32(&bar.v_full[s]);
+                mbar_arrive_expect_tx(b, halo_tx);
+                tma_load_4d(base + L.vh[s], &mVh, 0, tc.c0 - 1, tc.r0 - 1, tc.sl, b);
+            };
+            // the tiles' Q, K, V do not depend on the previous kernel
+            for (int u = 0; u < kSlots && t_begin + u < t_end; ++u) {
+                load_qk(t_begin + u, u);
+                load_v(t_begin + u, u);
             }
-        }
-    uint32_t koff[3], voff[3];        // halo rows of the ldmatrix loads (static per warp)
-#pragma unroll
-    for (int pr = 0; pr < 3; ++pr) {
-        const int kk = 8 * (2 * pr + (lane >> 4)) + (lane & 7);          // scores: n-tile pairs
-        const int kv = 16 * pr + (lane & 7) + 8 * ((lane >> 3) & 1);      // values: k-steps
-        const int kk2 = kk < 40 ? kk : 0, kv2 = kv < 40 ? kv : 0;
-        koff[pr] = (uint32_t)((2 * bi + kk2 / 10) * hw + 8 * bj + kk2 % 10);
-        voff[pr] = (uint32_t)((2 * bi + kv2 / 10) * hw + 8 * bj + kv2 % 10);
-    }
-    const int qrow = 16 * blk + (lane & 7) + 8 * ((lane >> 3) & 1);      // A-fragment row
-    const uint32_t orow[2] = {(uint32_t)(16 * blk + g), (uint32_t)(16 * blk + g + 8)};
-    const uint32_t obase[2] = {orow[0] * kRow + 4 * q4, orow[1] * kRow + 4 * q4};
-
-    // ---- prologue: the first tile's Q, K, V do not depend on the earlier kernels
-    if (tid == 0 && t_begin < t_end) {
-        const TileCoord tc = tile_coord(p, t_begin);
-        epi_load_qk(p, L, base, smem_u32(&qk_bar), tc, mlp, &mQ, &mKh, &mKt);
-        epi_load_v(p, L, base, smem_u32(&v_bar), tc, &mVh);
-    }
-    // The B operands come from the previous kernel: the first tile computes
-    // its local-branch scores before waiting for them (see the tile loop).
-
-    const float c2 = 1.4426950408889634f * 0.125f;   // log2(e) / sqrt(64)
-    int b_loads = 1;                                  // B operands loaded so far (phase of b_bar)
-    int prev_sl = -1;
-    for (int t = t_begin, it = 0; t < t_end; ++t, ++it) {
-        const TileCoord tc = tile_coord(p, t);
-        const bool has_next = t + 1 < t_end;
-        const TileCoord tn = tile_coord(p, has_next ? t + 1 : t);
-        const bool new_b = tc.sl != prev_sl;
-        prev_sl = tc.sl;
-
-        // ---- inputs of this tile
-        if (!mbar_wait(smem_u32(&qk_bar), it & 1)) record_error(p.err, kErrTimeoutLoad);
-        if (it > 0 && new_b && !mbar_wait(smem_u32(&b_bar), (b_loads - 1) & 1)) record_error(p.err, kErrTimeoutLoad);
-        if (p.relu) {
-            relu_smem(sm + L.q, 128 * kRow, tid, 256);
-            relu_smem(sm + L.kh, (int)halo_bytes, tid, 256);
-            if (mlp) relu_smem(sm + L.kt, 128 * kRow, tid, 256);
-        }
-        fence_proxy_async();
-        __syncthreads();
-
-        // ---- tensor-core products into TMEM (one thread issues)
-        auto issue_mma = [&]() {
-            tc_fence_after();
-            for (int r = 0; r < p.epi_rows; r += 256) {
-                const int N = min(256, p.epi_rows - r);
-                const uint32_t idesc = make_idesc_bf16(128, N, false, false);
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    tc_mma(tmem + r, make_desc_sw128(base + L.q + ks * 32, 16, 1024),
-                           make_desc_sw128(base + L.bepi + r * kRow + ks * 32, 16, 1024), idesc, ks > 0);
-            }
+            pdl_wait();   // the B operands (and the W1 image) come from the previous kernel
             if (mlp) {
-                const uint32_t idesc = make_idesc_bf16(128, p.n_mlp, false, false);
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t a = base + (ks < 4 ? L.q : L.kt) + (ks & 3) * 32;
-                    const uint32_t b = base + L.w1 + (ks < 4 ? 0u : (uint32_t)p.n_mlp * kRow) + (ks & 3) * 32;
-                    tc_mma(tmem + p.epi_rows, make_desc_sw128(a, 16, 1024), make_desc_sw128(b, 16, 1024), idesc,
-                           ks > 0);
+                mbar_arrive_expect_tx(smem_u32(&bar.w1), 2u * p.n_mlp * kRow);
+                bulk_load(base + L.w1, p.w1img, 2u * p.n_mlp * kRow, smem_u32(&bar.w1));
+                if (!mbar_wait(smem_u32(&bar.w1), 0)) record_error(p.err, kErrTimeoutLoad);
+            }
+            const int nb = p.epi_nbepi;
+            const uint32_t brow_bytes = (uint32_t)p.epi_rows * kRow;
+            int cur_sl = -1, cur_b = 0, n_loads = 0;
+            int commits[2] = {0, 0}, waited[2] = {0, 0};
+            for (int t = t_begin, it = 0; t < t_end; ++t, ++it) {
+                const int s = it % kSlots;
+                const uint32_t ph = (uint32_t)(it / kSlots) & 1u;
+                const int sl = tile_coord(p, t).sl;
+                if (sl != cur_sl) {
+                    // B operand of a new slice; its buffer's previous slice must be done
+                    cur_b = n_loads % nb;
+                    const int use = n_loads / nb;
+                    if (use > 0) {
+                        if (!mbar_wait(smem_u32(&bar.b_free[cur_b]), (uint32_t)(use - 1) & 1u))
+                            record_error(p.err, kErrTimeoutMma);
+                        waited[cur_b] = use;
+                    }
+                    const uint32_t b = smem_u32(&bar.b_full[cur_b]);
+                    mbar_arrive_expect_tx(b, brow_bytes);
+                    bulk_load(base + L.bepi[cur_b], p.bepi + (size_t)sl * brow_bytes, brow_bytes, b);
+                    if (!mbar_wait(b, (uint32_t)use & 1u)) record_error(p.err, kErrTimeoutLoad);
+                    ++n_loads;
+                    cur_sl = sl;
+                }
+                if (!mbar_wait(smem_u32(&bar.qrelu[s]), ph)) record_error(p.err, kErrTimeoutLoad);
+                if (it >= kSlots && !mbar_wait(smem_u32(&bar.tmem_empty[s]), ph ^ 1u))
+                    record_error(p.err, kErrTimeoutMma);
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(s * p.slot_cols);
+                const uint32_t qa = base + L.q[s], ba = base + L.bepi[cur_b];
+                for (int r = 0; r < p.epi_rows; r += 256) {
+                    const int N = min(256, p.epi_rows - r);
+                    const uint32_t idesc = make_idesc_bf16(128, N, false, false);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        tc_mma(d + r, make_desc_sw128(qa + ks * 32, 16, 1024),
+                               make_desc_sw128(ba + r * kRow + ks * 32, 16, 1024), idesc, ks > 0);
+                }
+                if (mlp) {
+                    // hidden pre-activations [Q | K] W1^T next to the global products
+                    const uint32_t idesc = make_idesc_bf16(128, p.n_mlp, false, false);
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t a = base + (ks < 4 ? L.q[s] : L.kt[s]) + (ks & 3) * 32;
+                        const uint32_t b = base + L.w1 + (ks < 4 ? 0u : (uint32_t)p.n_mlp * kRow) + (ks & 3) * 32;
+                        tc_mma(d + p.epi_rows, make_desc_sw128(a, 16, 1024), make_desc_sw128(b, 16, 1024), idesc,
+                               ks > 0);
+                    }
+                }
+                tc_commit(smem_u32(&bar.mma_full[s]));
+                if (t + 1 < t_end && tile_coord(p, t + 1).sl != sl) {
+                    tc_commit(smem_u32(&bar.b_free[cur_b]));
+                    ++commits[cur_b];
+                }
+                // refill this slot with tile it + kSlots as soon as the warps and the MMA let go of it
+                if (t + kSlots < t_end) {
+                    if (!mbar_wait(smem_u32(&bar.qk_empty[s]), ph)) record_error(p.err, kErrTimeoutLoad);
+                    if (!mbar_wait(smem_u32(&bar.mma_full[s]), ph)) record_error(p.err, kErrTimeoutMma);
+                    load_qk(t + kSlots, s);
+                    if (!mbar_wait(smem_u32(&bar.v_empty[s]), ph)) record_error(p.err, kErrTimeoutLoad);
+                    load_v(t + kSlots, s);
                 }
             }
-            tc_commit(smem_u32(&mma_bar));
-        };
-        if (tid == 0) {
-            if (it > 0) issue_mma();
-            bulk_wait_read0();   // the previous tile's store has read the output buffer
+            // no commit may still be in flight when the CTA exits
+            for (int b = 0; b < 2; ++b)
+                if (commits[b] > waited[b] && !mbar_wait(smem_u32(&bar.b_free[b]), (uint32_t)waited[b] & 1u))
+                    record_error(p.err, kErrTimeoutMma);
         }
+        __syncwarp();
+    } else {
+        // ===================== compute: local branch, mix, store
+        const int g = lane >> 2, q4 = lane & 3;
+        // this warp's 2 x 8 block: TMEM lanes 16 blk .. 16 blk + 15 (inside its quadrant)
+        const int blk = 2 * (warp & 3) + (warp >> 2);
+        const int bi = blk % BR, bj = blk / BR;
+        const uint32_t lane_base = (uint32_t)(16 * blk) << 16;
 
-        // ---- local branch scores: Q block (16 x 64) against its 4 x 10 key window
-        float sc[5][4];
-        {
+        // Per-lane constants of the local branch.  Window key kappa indexes the
+        // 4 x 10 key window of the block: ka = kappa / 10, kb = kappa % 10.
+        // Score element (j, e) of this lane: row g + 8 (e >> 1), key 8 j + 2 q + (e & 1).
+        uint32_t win_mask = 0;   // bit j*4+e: key in the query's 3x3 window
+        uint32_t ctr_mask = 0;   // bit j*4+e: key is the query token itself
+#pragma unroll
+        for (int j = 0; j < 5; ++j)
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                const int kappa = 8 * j + 2 * q4 + b;
+                const int ka = kappa / 10, kb = kappa % 10;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int du = ka - h, dv = kb - g;
+                    if (du >= 0 && du <= 2 && dv >= 0 && dv <= 2) win_mask |= 1u << (j * 4 + 2 * h + b);
+                    if (du == 1 && dv == 1) ctr_mask |= 1u << (j * 4 + 2 * h + b);
+                }
+            }
+        uint32_t koff[3], voff[3];   // halo rows of the ldmatrix loads (static per warp)
+#pragma unroll
+        for (int pr = 0; pr < 3; ++pr) {
+            const int kk = 8 * (2 * pr + (lane >> 4)) + (lane & 7);       // scores: n-tile pairs
+            const int kv = 16 * pr + (lane & 7) + 8 * ((lane >> 3) & 1);   // values: k-steps
+            const int kk2 = kk < 40 ? kk : 0, kv2 = kv < 40 ? kv : 0;
+            koff[pr] = (uint32_t)((2 * bi + kk2 / 10) * hw + 8 * bj + kk2 % 10);
+            voff[pr] = (uint32_t)((2 * bi + kv2 / 10) * hw + 8 * bj + kv2 % 10);
+        }
+        const uint32_t qrow = (uint32_t)(16 * blk + (lane & 7) + 8 * ((lane >> 3) & 1));   // A-fragment row
+        const uint32_t out_w = base + L.out + (uint32_t)warp * 2u * kOutBuf;
+        const float c2 = 1.4426950408889634f * 0.125f;   // log2(e) / sqrt(64)
+
+        for (int t = t_begin, it = 0; t < t_end; ++t, ++it) {
+            const TileCoord tc = tile_coord(p, t);
+            const int s = it % kSlots;
+            const uint32_t ph = (uint32_t)(it / kSlots) & 1u;
+            const float alpha = p.alpha[tc.sl % p.heads];
+            const uint32_t tl = tmem + (uint32_t)(s * p.slot_cols) + lane_base;
+
+            // ---- the block's queries: A fragments, ReLU'd in registers and written
+            // back (with the tile's K rows) for the tensor-core products
+            if (!mbar_wait(smem_u32(&bar.qk_full[s]), ph)) record_error(p.err, kErrTimeoutLoad);
+            const uint32_t qb = base + L.q[s];
             uint32_t a[4][4];
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-                ldsm_x4(base + L.q + sw128_offset(qrow, 2 * ks + (lane >> 4)), a[ks][0], a[ks][1], a[ks][2], a[ks][3]);
+                ldsm_x4(qb + sw128_offset(qrow, 2 * ks + (lane >> 4)), a[ks][0], a[ks][1], a[ks][2], a[ks][3]);
+            if (p.relu) {
 #pragma unroll
-            for (int j = 0; j < 5; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+                for (int ks = 0; ks < 4; ++ks) {
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-#pragma unroll
-                for (int pr = 0; pr < 3; ++pr) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(base + L.kh + sw128_offset(koff[pr], 2 * ks + ((lane >> 3) & 1)), b0, b1, b2, b3);
-                    mma_bf16_16816(sc[2 * pr], a[ks][0], a[ks][1], a[ks][2], a[ks][3], b0, b1);
-                    if (pr < 2) mma_bf16_16816(sc[2 * pr + 1], a[ks][0], a[ks][1], a[ks][2], a[ks][3], b2, b3);
+                    for (int e = 0; e < 4; ++e) a[ks][e] = relu2(a[ks][e]);
+                    stsm_x4(qb + sw128_offset(qrow, 2 * ks + (lane >> 4)), a[ks][0], a[ks][1], a[ks][2], a[ks][3]);
                 }
-            }
-        }
-        __syncthreads();   // Q, K halo and (after the wait below) the B operand are free
-        if (it == 0) {
-            pdl_wait();    // the B operands (and the MLP image) of the previous kernel are ready
-            if (tid == 0) {
-                epi_load_bepi(p, L, base, smem_u32(&b_bar), tc.sl);
                 if (mlp) {
-                    mbar_arrive_expect_tx(smem_u32(&w1_bar), 2u * p.n_mlp * kRow);
-                    bulk_load(base + L.w1, p.w1img, 2u * p.n_mlp * kRow, smem_u32(&w1_bar));
+                    const uint32_t kb = base + L.kt[s];
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const uint32_t ad = kb + sw128_offset(qrow, 2 * ks + (lane >> 4));
+                        uint32_t r0, r1, r2, r3;
+                        ldsm_x4(ad, r0, r1, r2, r3);
+                        stsm_x4(ad, relu2(r0), relu2(r1), relu2(r2), relu2(r3));
+                    }
                 }
-                if (!mbar_wait(smem_u32(&b_bar), 0)) record_error(p.err, kErrTimeoutLoad);
-                if (mlp && !mbar_wait(smem_u32(&w1_bar), 0)) record_error(p.err, kErrTimeoutLoad);
-                issue_mma();
+                fence_proxy_async();
             }
-        }
-        if (tid == 0) {
-            if (!mbar_wait(smem_u32(&mma_bar), it & 1)) record_error(p.err, kErrTimeoutMma);
-            if (has_next) {
-                epi_load_qk(p, L, base, smem_u32(&qk_bar), tn, mlp, &mQ, &mKh, &mKt);
-                if (tn.sl != tc.sl) {
-                    epi_load_bepi(p, L, base, smem_u32(&b_bar), tn.sl);
-                }
-            }
-        }
-        if (has_next && tn.sl != tc.sl) ++b_loads;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bar.qrelu[s]));
 
-        const float alpha = p.alpha[tc.sl % p.heads];
-        const uint32_t tl = tmem + lane_base;
-        float w0[2], wk[2][LISA_MAX_T_MLP];
-        if (mlp) {
-            // adaptive step weights of rows g, g+8 from the MLP hidden layer in TMEM
-            if (!mbar_wait(smem_u32(&mma_bar), it & 1)) record_error(p.err, kErrTimeoutMma);
-            tc_fence_after();
-            uint32_t hr[8][4];
+            // ---- local branch scores: Q block (16 x 64) against its 4 x 10 key window
+            float sc[5][4];
+            {
+                const uint32_t khb = base + L.kh[s];
 #pragma unroll
-            for (int f8 = 0; f8 < 8; ++f8)
-                if (8 * f8 < p.n_mlp) tmem_ld_frag_nowait(tl + p.epi_rows + 8 * f8, hr[f8]);
-            tc_wait_ld();
+                for (int j = 0; j < 5; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
+                for (int ks = 0; ks < 4; ++ks) {
 #pragma unroll
-                for (int t2 = 0; t2 < LISA_MAX_T_MLP; ++t2) wk[h][t2] = 0.f;
-#pragma unroll
-            for (int f8 = 0; f8 < 8; ++f8) {
-                if (8 * f8 >= p.n_mlp) break;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int m = 8 * f8 + 2 * q4 + (e & 1);
-                    if (m < p.hidden) {
-                        const float hv = gelu_erf(__uint_as_float(hr[f8][e]) + p.b1[m]);
-#pragma unroll
-                        for (int t2 = 0; t2 < LISA_MAX_T_MLP; ++t2)
-                            if (t2 < p.T) wk[e >> 1][t2] = fmaf(p.W2[t2 * p.hidden + m], hv, wk[e >> 1][t2]);
+                    for (int pr = 0; pr < 3; ++pr) {
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4(khb + sw128_offset(koff[pr], 2 * ks + ((lane >> 3) & 1)), b0, b1, b2, b3);
+                        if (p.relu) {
+                            b0 = relu2(b0); b1 = relu2(b1); b2 = relu2(b2); b3 = relu2(b3);
+                        }
+                        mma_bf16_16816(sc[2 * pr], a[ks][0], a[ks][1], a[ks][2], a[ks][3], b0, b1);
+                        if (pr < 2) mma_bf16_16816(sc[2 * pr + 1], a[ks][0], a[ks][1], a[ks][2], a[ks][3], b2, b3);
                     }
                 }
             }
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                float zmax = -INFINITY;
-#pragma unroll
-                for (int t2 = 0; t2 < LISA_MAX_T_MLP; ++t2) {
-                    if (t2 >= p.T) break;
-                    float z = wk[h][t2];
-                    z += __shfl_xor_sync(0xffffffffu, z, 1);
-                    z += __shfl_xor_sync(0xffffffffu, z, 2);
-                    z += p.b2[t2];
-                    wk[h][t2] = z;
-                    zmax = fmaxf(zmax, z);
-                }
-                float zs = 0.f;
-#pragma unroll
-                for (int t2 = 0; t2 < LISA_MAX_T_MLP; ++t2) {
-                    if (t2 >= p.T) break;
-                    wk[h][t2] = expf(wk[h][t2] - zmax);
-                    zs += wk[h][t2];
-                }
-                const float zi = 1.f / zs;
-#pragma unroll
-                for (int t2 = 0; t2 < LISA_MAX_T_MLP; ++t2) wk[h][t2] *= zi;
-                w0[h] = wk[h][0];
-            }
-        } else {
-            w0[0] = w0[1] = p.w[0];
-        }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bar.qk_empty[s]));
 
-        // ---- masked softmax over the window; the weight matrix also carries
-        // alpha w_0 on the token itself, so P' V = (1 - alpha) l_i + alpha w_0 V_i
-        float lacc[8][4];
-        {
-            uint32_t mask = win_mask;
-            const int gr0 = tc.r0 + 2 * bi - 1, gc0 = tc.c0 + 8 * bj - 1;   // grid position of window (0, 0)
-            if (gr0 < 0 || gr0 + 3 >= p.H || gc0 < 0 || gc0 + 9 >= p.W) {
+            float w0[2], wk[2][LISA_MAX_T_MLP];
+            if (mlp) {
+                // adaptive step weights of rows g, g+8 from the MLP hidden layer in TMEM
+                if (!mbar_wait(smem_u32(&bar.mma_full[s]), ph)) record_error(p.err, kErrTimeoutMma);
+                tc_fence_after();
+                uint32_t hr[8][4];
+#pragma unroll
+                for (int f8 = 0; f8 < 8; ++f8)
+                    if (8 * f8 < p.n_mlp) tmem_ld_frag_nowait(tl + p.epi_rows + 8 * f8, hr[f8]);
+                tc_wait_ld();
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int t2 = 0; t2 < LISA_MAX_T_MLP; ++t2) wk[h][t2] = 0.f;
+#pragma unroll
+                for (int f8 = 0; f8 < 8; ++f8) {
+                    if (8 * f8 >= p.n_mlp) break;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int m = 8 * f8 + 2 * q4 + (e & 1);
+                        if (m < p.hidden) {
+                            const float hv = gelu_erf(__uint_as_float(hr[f8][e]) + p.b1[m]);
+#pragma unroll
+                            for (int t2 = 0; t2 < LISA_MAX_T_MLP; ++t2)
+                                if (t2 < p.T) wk[e >> 1][t2] = fmaf(p.W2[t2 * p.hidden + m], hv, wk[e >> 1][t2]);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    float zmax = -INFINITY;
+#pragma unroll
+                    for (int t2 = 0; t2 < LISA_MAX_T_MLP; ++t2) {
+                        if (t2 >= p.T) break;
+                        float z = wk[h][t2];
+                        z += __shfl_xor_sync(0xffffffffu, z, 1);
+                        z += __shfl_xor_sync(0xffffffffu, z, 2);
+                        z += p.b2[t2];
+                        wk[h][t2] = z;
+                        zmax = fmaxf(zmax, z);
+                    }
+                    float zs = 0.f;
+#pragma unroll
+                    for (int t2 = 0; t2 < LISA_MAX_T_MLP; ++t2) {
+                        if (t2 >= p.T) break;
+                        wk[h][t2] = expf(wk[h][t2] - zmax);
+                        zs += wk[h][t2];
+                    }
+                    const float zi = 1.f / zs;
+#pragma unroll
+                    for (int t2 = 0; t2 < LISA_MAX_T_MLP; ++t2) wk[h][t2] *= zi;
+                    w0[h] = wk[h][0];
+                }
+            } else {
+                w0[0] = w0[1] = p.w[0];
+            }
+
+            // ---- masked softmax over the window; the weight matrix also carries
+            // alpha w_0 on the token itself, so P' V = (1 - alpha) l_i + alpha w_0 V_i
+            float lacc[8][4];
+            {
+                uint32_t mask = win_mask;
+                const int gr0 = tc.r0 + 2 * bi - 1, gc0 = tc.c0 + 8 * bj - 1;   // grid position of window (0, 0)
+                if (gr0 < 0 || gr0 + 3 >= p.H || gc0 < 0 || gc0 + 9 >= p.W) {
+#pragma unroll
+                    for (int j = 0; j < 5; ++j)
+#pragma unroll
+                        for (int b = 0; b < 2; ++b) {
+                            const int kappa = 8 * j + 2 * q4 + b;
+                            const int gr = gr0 + kappa / 10, gc = gc0 + kappa % 10;
+                            if (gr < 0 || gr >= p.H || gc < 0 || gc >= p.W) mask &= ~(0x5u << (j * 4 + b));
+                        }
+                }
+                float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
                 for (int j = 0; j < 5; ++j)
 #pragma unroll
-                    for (int b = 0; b < 2; ++b) {
-                        const int kappa = 8 * j + 2 * q4 + b;
-                        const int gr = gr0 + kappa / 10, gc = gc0 + kappa % 10;
-                        if (gr < 0 || gr >= p.H || gc < 0 || gc >= p.W) mask &= ~(0x5u << (j * 4 + b));
+                    for (int e = 0; e < 4; ++e) {
+                        sc[j][e] = ((mask >> (j * 4 + e)) & 1u) ? sc[j][e] * c2 : -INFINITY;
+                        mx[e >> 1] = fmaxf(mx[e >> 1], sc[j][e]);
                     }
-            }
-            float mx[2] = {-INFINITY, -INFINITY};
+                float sum[2] = {0.f, 0.f};
 #pragma unroll
-            for (int j = 0; j < 5; ++j)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    sc[j][e] = ((mask >> (j * 4 + e)) & 1u) ? sc[j][e] * c2 : -INFINITY;
-                    mx[e >> 1] = fmaxf(mx[e >> 1], sc[j][e]);
+                for (int h = 0; h < 2; ++h) {
+                    mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+                    mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+                    if (mx[h] == -INFINITY) mx[h] = 0.f;
                 }
-            float sum[2] = {0.f, 0.f};
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
-                mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
-                if (mx[h] == -INFINITY) mx[h] = 0.f;
-            }
+                for (int j = 0; j < 5; ++j)
 #pragma unroll
-            for (int j = 0; j < 5; ++j)
+                    for (int e = 0; e < 4; ++e) {
+                        sc[j][e] = exp2f(sc[j][e] - mx[e >> 1]);
+                        sum[e >> 1] += sc[j][e];
+                    }
+                float scale[2], self[2];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    sc[j][e] = exp2f(sc[j][e] - mx[e >> 1]);
-                    sum[e >> 1] += sc[j][e];
+                for (int h = 0; h < 2; ++h) {
+                    sum[h] += __shfl_xor_sync(0xffffffffu, sum[h], 1);
+                    sum[h] += __shfl_xor_sync(0xffffffffu, sum[h], 2);
+                    scale[h] = sum[h] > 0.f ? (1.f - alpha) / sum[h] : 0.f;
+                    self[h] = alpha * w0[h];
                 }
-            float scale[2], self[2];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                sum[h] += __shfl_xor_sync(0xffffffffu, sum[h], 1);
-                sum[h] += __shfl_xor_sync(0xffffffffu, sum[h], 2);
-                scale[h] = sum[h] > 0.f ? (1.f - alpha) / sum[h] : 0.f;
-                self[h] = alpha * w0[h];
-            }
+                for (int j = 0; j < 5; ++j)
 #pragma unroll
-            for (int j = 0; j < 5; ++j)
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    sc[j][e] = fmaf(sc[j][e], scale[e >> 1], ((ctr_mask >> (j * 4 + e)) & 1u) ? self[e >> 1] : 0.f);
+                    for (int e = 0; e < 4; ++e)
+                        sc[j][e] = fmaf(sc[j][e], scale[e >> 1], ((ctr_mask >> (j * 4 + e)) & 1u) ? self[e >> 1] : 0.f);
 
-            if (!mbar_wait(smem_u32(&v_bar), it & 1)) record_error(p.err, kErrTimeoutLoad);
+                if (!mbar_wait(smem_u32(&bar.v_full[s]), ph)) record_error(p.err, kErrTimeoutLoad);
+                const uint32_t vhb = base + L.vh[s];
 #pragma unroll
-            for (int nt = 0; nt < 8; ++nt) lacc[nt][0] = lacc[nt][1] = lacc[nt][2] = lacc[nt][3] = 0.f;
+                for (int nt = 0; nt < 8; ++nt) lacc[nt][0] = lacc[nt][1] = lacc[nt][2] = lacc[nt][3] = 0.f;
 #pragma unroll
-            for (int ks = 0; ks < 3; ++ks) {
-                const int j0 = 2 * ks, j1 = 2 * ks + 1;
-                const uint32_t pa0 = pack_bf16(sc[j0][0], sc[j0][1]);
-                const uint32_t pa1 = pack_bf16(sc[j0][2], sc[j0][3]);
-                const uint32_t pa2 = j1 < 5 ? pack_bf16(sc[j1][0], sc[j1][1]) : 0u;
-                const uint32_t pa3 = j1 < 5 ? pack_bf16(sc[j1][2], sc[j1][3]) : 0u;
+                for (int ks = 0; ks < 3; ++ks) {
+                    const int j0 = 2 * ks, j1 = 2 * ks + 1;
+                    const uint32_t pa0 = pack_bf16(sc[j0][0], sc[j0][1]);
+                    const uint32_t pa1 = pack_bf16(sc[j0][2], sc[j0][3]);
+                    const uint32_t pa2 = j1 < 5 ? pack_bf16(sc[j1][0], sc[j1][1]) : 0u;
+                    const uint32_t pa3 = j1 < 5 ? pack_bf16(sc[j1][2], sc[j1][3]) : 0u;
 #pragma unroll
-                for (int np = 0; np < 4; ++np) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(base + L.vh + sw128_offset(voff[ks], 2 * np + (lane >> 4)), b0, b1, b2, b3);
-                    mma_bf16_16816(lacc[2 * np], pa0, pa1, pa2, pa3, b0, b1);
-                    mma_bf16_16816(lacc[2 * np + 1], pa0, pa1, pa2, pa3, b2, b3);
+                    for (int np = 0; np < 4; ++np) {
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4_t(vhb + sw128_offset(voff[ks], 2 * np + (lane >> 4)), b0, b1, b2, b3);
+                        mma_bf16_16816(lacc[2 * np], pa0, pa1, pa2, pa3, b0, b1);
+                        mma_bf16_16816(lacc[2 * np + 1], pa0, pa1, pa2, pa3, b2, b3);
+                    }
                 }
             }
-        }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bar.v_empty[s]));
 
-        // ---- global branch from TMEM (fragment layout) and output tile
-        if (!mlp && !mbar_wait(smem_u32(&mma_bar), it & 1)) record_error(p.err, kErrTimeoutMma);
-        tc_fence_after();
-        {
-            uint32_t rs[4], ru[32];
-            tmem_ld_frag_nowait(tl + p.n_umat * kD, rs);     // Q.s_hi, Q.s_lo: columns held by lane q4 = 0
-            tmem_ld_frag8_nowait(tl, ru);
-            tc_wait_ld();
-            const int src = lane & ~3;
-            const float d0 = __shfl_sync(0xffffffffu, __uint_as_float(rs[0]) + __uint_as_float(rs[1]), src);
-            const float d1 = __shfl_sync(0xffffffffu, __uint_as_float(rs[2]) + __uint_as_float(rs[3]), src);
-            // alpha / (Q_i . s + eps): the global term is alpha Q~_i U = alpha (Q_i U) / (Q_i . s + eps)
-            float arq[2] = {alpha / (d0 + p.eps), alpha / (d1 + p.eps)};
-            float acc[32];
-            if (mlp) {
+            // ---- global branch from TMEM (fragment layout), mix, output block
+            if (!mlp && !mbar_wait(smem_u32(&bar.mma_full[s]), ph)) record_error(p.err, kErrTimeoutMma);
+            tc_fence_after();
+            float acc[32], arq[2];
+            {
+                uint32_t rs[4], ru[32];
+                tmem_ld_frag_nowait(tl + p.n_umat * kD, rs);   // Q.s_hi, Q.s_lo: columns held by lane q4 = 0
+                tmem_ld_frag8_nowait(tl, ru);
+                tc_wait_ld();
+                const int src = lane & ~3;
+                const float d0 = __shfl_sync(0xffffffffu, __uint_as_float(rs[0]) + __uint_as_float(rs[1]), src);
+                const float d1 = __shfl_sync(0xffffffffu, __uint_as_float(rs[2]) + __uint_as_float(rs[3]), src);
+                // alpha / (Q_i . s + eps): the global term is alpha Q~_i U = alpha (Q_i U) / (Q_i . s + eps)
+                arq[0] = alpha / (d0 + p.eps);
+                arq[1] = alpha / (d1 + p.eps);
+                if (mlp) {
 #pragma unroll
-                for (int k = 0; k < 32; ++k) acc[k] = wk[(k >> 1) & 1][1] * __uint_as_float(ru[k]);
-                for (int u = 1; u < p.n_umat; ++u) {
-                    tmem_ld_frag8_nowait(tl + u * kD, ru);
-                    tc_wait_ld();
+                    for (int k = 0; k < 32; ++k) acc[k] = wk[(k >> 1) & 1][1] * __uint_as_float(ru[k]);
+                    for (int u = 1; u < p.n_umat; ++u) {
+                        tmem_ld_frag8_nowait(tl + u * kD, ru);
+                        tc_wait_ld();
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) acc[k] = fmaf(wk[(k >> 1) & 1][u + 1], __uint_as_float(ru[k]), acc[k]);
+                        for (int k = 0; k < 32; ++k)
+                            acc[k] = fmaf(wk[(k >> 1) & 1][u + 1], __uint_as_float(ru[k]), acc[k]);
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) acc[k] = __uint_as_float(ru[k]);
                 }
-            } else {
-#pragma unroll
-                for (int k = 0; k < 32; ++k) acc[k] = __uint_as_float(ru[k]);
             }
-            uint8_t *out = sm + L.out;
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bar.tmem_empty[s]));
+
+            const uint32_t ob = out_w + (uint32_t)(it & 1) * kOutBuf;
+            if (lane == 0) bulk_wait_read<1>();   // the store that last read this buffer is done with it
+            __syncwarp();
 #pragma unroll
             for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const float o0 = fmaf(arq[h], acc[4 * nt + 2 * h], lacc[nt][2 * h]);
                     const float o1 = fmaf(arq[h], acc[4 * nt + 2 * h + 1], lacc[nt][2 * h + 1]);
-                    *reinterpret_cast<uint32_t *>(out + obase[h] + ((nt ^ (orow[h] & 7u)) << 4)) = pack_bf16(o0, o1);
+                    const uint32_t row = (uint32_t)(8 * h + g);
+                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(ob + row * kRow + ((nt ^ g) << 4) + 4 * q4),
+                                 "r"(pack_bf16(o0, o1))
+                                 : "memory");
                 }
+            fence_proxy_async();
+            __syncwarp();
+            const int br = tc.r0 + 2 * bi, bc = tc.c0 + 8 * bj;
+            if (lane == 0 && br < p.H && bc < p.W) {
+                tma_store_4d(&mO, ob, 0, bc, br, tc.sl);
+                bulk_commit();
+            }
         }
-        fence_proxy_async();
-        tc_fence_before();
-        __syncthreads();   // output written; V halo and TMEM are free
-        if (tid == 0) {
-            for (int b2 = 0; b2 < BC; ++b2)
-                tma_store_4d(&mO, base + L.out + b2 * 16 * BR * kRow, 0, tc.c0 + 8 * b2, tc.r0, tc.sl);
-            bulk_commit();
-            if (has_next) epi_load_v(p, L, base, smem_u32(&v_bar), tn, &mVh);
-        }
+        if (lane == 0) bulk_wait0();
+        __syncwarp();
     }
-    if (tid == 0) bulk_wait0();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1261,6 +1341,25 @@ int sm_count() {
     return n;
 }
 
+constexpr int kSmemPerSm = 228 * 1024;        // shared memory of one SM
+constexpr int kSmemPerCta = 226 * 1024;       // dynamic shared memory one CTA may ask for
+
+// Epilogue configuration: two input slots if they fit one CTA's shared memory
+// and TMEM, else one; two B-operand buffers if they still fit, else one.
+void epi_config(const TcParams &t, bool mlp, int *slots, int *nb, int *smem) {
+    *slots = 0;
+    for (int s = 2; s >= 1; --s)
+        for (int b = 2; b >= 1; --b) {
+            const int bytes = (int)epi_layout(t.BR, t.BC, t.epi_rows, t.n_mlp, mlp, s, b).total + 1024;
+            if (bytes <= kSmemPerCta && s * t.slot_cols <= 512) {
+                *slots = s;
+                *nb = b;
+                *smem = bytes;
+                return;
+            }
+        }
+}
+
 }  // namespace
 
 // Epilogue tile: BR x BC blocks of 2 x 8 tokens (BR * BC = 8); fewest tiles.
@@ -1298,6 +1397,7 @@ cudaError_t launch_tc(const Problem &p, cudaStream_t st, int stage) {
     t.n_umat = mlp ? p.T - 1 : 1;
     t.epi_rows = 64 * t.n_umat + 16;
     t.n_mlp = mlp ? (p.hidden + 15) / 16 * 16 : 0;
+    t.slot_cols = (t.epi_rows + t.n_mlp + 31) / 32 * 32;
     t.s_part = p.s_part; t.part = p.tc_part; t.bepi = p.tc_bepi; t.w1img = p.tc_w1img; t.err = p.err;
     const bool fused = tc_fused(p.chunks, p.tc_cluster, p.chunk);
     // stage index of each kernel in this chain (-1: not part of it)
@@ -1369,28 +1469,33 @@ cudaError_t launch_tc(const Problem &p, cudaStream_t st, int stage) {
             !make_map_grid(&mkh, p.K, p.slices, p.H, p.W, th + 2, tw + 2) ||
             !make_map_grid(&mvh, p.V, p.slices, p.H, p.W, th + 2, tw + 2) ||
             !make_map_grid(&mkt, p.K, p.slices, p.H, p.W, th, 8) ||
-            !make_map_grid(&mo, p.O, p.slices, p.H, p.W, th, 8))
+            !make_map_grid(&mo, p.O, p.slices, p.H, p.W, 2, 8))   // one warp's 2 x 8 block
             return cudaErrorInvalidValue;
-        // fixed weights: two CTAs per SM (the warps of both hide each other's
-        // latencies); adaptive weights: one CTA per SM (registers)
-        const EpiLayout L = epi_layout(t.BR, t.BC, t.epi_rows, t.n_mlp, mlp);
-        t.epi_stages = 1;
-        const int per_sm = mlp ? 1 : 2;
-        const int smem = (int)L.total + 1024;
-        const uint32_t cols = pow2_cols(t.epi_rows + t.n_mlp);
+        int slots = 0, nb = 0, smem = 0;
+        epi_config(t, mlp, &slots, &nb, &smem);
+        if (slots == 0) return cudaErrorInvalidConfiguration;
+        t.epi_nbepi = nb;
+        const uint32_t cols = pow2_cols(slots * t.slot_cols);
+        int per_sm = kSmemPerSm / (smem + 1024);
+        if (per_sm > 2) per_sm = 2;
+        while (per_sm > 1 && per_sm * (int)cols > 512) --per_sm;
         const int nctas = per_sm * sm_count();
         cfg.gridDim = dim3((unsigned)(t.tiles < nctas ? t.tiles : nctas));
-        cfg.blockDim = dim3(256);
+        cfg.blockDim = dim3(kEpiThreads);
         cfg.dynamicSmemBytes = smem;
         cfg.attrs = attrs;
         cfg.numAttrs = 1;
-        if (mlp) {
-            if ((err = set_smem(tc_epilogue_kernel<true>, 2, smem)) != cudaSuccess) return err;
-            err = cudaLaunchKernelEx(&cfg, tc_epilogue_kernel<true>, mq, mkh, mvh, mkt, mo, t, cols);
-        } else {
-            if ((err = set_smem(tc_epilogue_kernel<false>, 3, smem)) != cudaSuccess) return err;
-            err = cudaLaunchKernelEx(&cfg, tc_epilogue_kernel<false>, mq, mkh, mvh, mkt, mo, t, cols);
-        }
+        auto launch = [&](auto kern, int slot) {
+            cudaError_t e = set_smem(kern, slot, smem);
+            if (e != cudaSuccess) return e;
+            return cudaLaunchKernelEx(&cfg, kern, mq, mkh, mvh, mkt, mo, t, cols);
+        };
+        if (mlp)
+            err = slots == 2 ? launch(tc_epilogue_kernel<true, 2, 1>, 2) : launch(tc_epilogue_kernel<true, 1, 1>, 3);
+        else if (slots == 2)
+            err = launch(tc_epilogue_kernel<false, 2, 1>, 4);
+        else
+            err = per_sm == 2 ? launch(tc_epilogue_kernel<false, 1, 2>, 5) : launch(tc_epilogue_kernel<false, 1, 1>, 6);
         if (err != cudaSuccess) return err;
     }
     return cudaGetLastError();
