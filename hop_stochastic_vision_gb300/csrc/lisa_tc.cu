@@ -994,6 +994,11 @@ __global__ void __launch_bounds__(kEpiThreads, kMinBlocks)
                     if (du == 1 && dv == 1) ctr_mask |= 1u << (j * 4 + 2 * h + b);
                 }
             }
+        float wbias[5][4];           // 0 inside the window, -inf outside (blocks off the grid border)
+#pragma unroll
+        for (int j = 0; j < 5; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) wbias[j][e] = ((win_mask >> (j * 4 + e)) & 1u) ? 0.f : -INFINITY;
         uint32_t koff[3], voff[3];   // halo rows of the ldmatrix loads (static per warp)
 #pragma unroll
         for (int pr = 0; pr < 3; ++pr) {
@@ -1007,8 +1012,19 @@ __global__ void __launch_bounds__(kEpiThreads, kMinBlocks)
         const uint32_t out_w = base + L.out + (uint32_t)warp * 2u * kOutBuf;
         const float c2 = 1.4426950408889634f * 0.125f;   // log2(e) / sqrt(64)
 
+        TileCoord tc = tile_coord(p, t_begin);
         for (int t = t_begin, it = 0; t < t_end; ++t, ++it) {
-            const TileCoord tc = tile_coord(p, t);
+            if (it > 0) {   // next tile in row-major order of the slice's tile grid
+                tc.c0 += 8 * BC;
+                if (tc.c0 >= 8 * BC * p.tiles_c) {
+                    tc.c0 = 0;
+                    tc.r0 += 2 * BR;
+                    if (tc.r0 >= 2 * BR * p.tiles_r) {
+                        tc.r0 = 0;
+                        ++tc.sl;
+                    }
+                }
+            }
             const int s = it % kSlots;
             const uint32_t ph = (uint32_t)(it / kSlots) & 1u;
             const float alpha = p.alpha[tc.sl % p.heads];
@@ -1128,9 +1144,10 @@ __global__ void __launch_bounds__(kEpiThreads, kMinBlocks)
             // alpha w_0 on the token itself, so P' V = (1 - alpha) l_i + alpha w_0 V_i
             float lacc[8][4];
             {
-                uint32_t mask = win_mask;
                 const int gr0 = tc.r0 + 2 * bi - 1, gc0 = tc.c0 + 8 * bj - 1;   // grid position of window (0, 0)
                 if (gr0 < 0 || gr0 + 3 >= p.H || gc0 < 0 || gc0 + 9 >= p.W) {
+                    // block on the grid border: drop the window keys outside the grid
+                    uint32_t mask = win_mask;
 #pragma unroll
                     for (int j = 0; j < 5; ++j)
 #pragma unroll
@@ -1139,15 +1156,21 @@ __global__ void __launch_bounds__(kEpiThreads, kMinBlocks)
                             const int gr = gr0 + kappa / 10, gc = gc0 + kappa % 10;
                             if (gr < 0 || gr >= p.H || gc < 0 || gc >= p.W) mask &= ~(0x5u << (j * 4 + b));
                         }
+#pragma unroll
+                    for (int j = 0; j < 5; ++j)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) sc[j][e] = ((mask >> (j * 4 + e)) & 1u) ? sc[j][e] * c2 : -INFINITY;
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 5; ++j)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) sc[j][e] = fmaf(sc[j][e], c2, wbias[j][e]);
                 }
                 float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
                 for (int j = 0; j < 5; ++j)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        sc[j][e] = ((mask >> (j * 4 + e)) & 1u) ? sc[j][e] * c2 : -INFINITY;
-                        mx[e >> 1] = fmaxf(mx[e >> 1], sc[j][e]);
-                    }
+                    for (int e = 0; e < 4; ++e) mx[e >> 1] = fmaxf(mx[e >> 1], sc[j][e]);
                 float sum[2] = {0.f, 0.f};
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
@@ -1212,8 +1235,8 @@ __global__ void __launch_bounds__(kEpiThreads, kMinBlocks)
                 const float d0 = __shfl_sync(0xffffffffu, __uint_as_float(rs[0]) + __uint_as_float(rs[1]), src);
                 const float d1 = __shfl_sync(0xffffffffu, __uint_as_float(rs[2]) + __uint_as_float(rs[3]), src);
                 // alpha / (Q_i . s + eps): the global term is alpha Q~_i U = alpha (Q_i U) / (Q_i . s + eps)
-                arq[0] = alpha / (d0 + p.eps);
-                arq[1] = alpha / (d1 + p.eps);
+                arq[0] = __fdividef(alpha, d0 + p.eps);
+                arq[1] = __fdividef(alpha, d1 + p.eps);
                 if (mlp) {
 #pragma unroll
                     for (int k = 0; k < 32; ++k) acc[k] = wk[(k >> 1) & 1][1] * __uint_as_float(ru[k]);
@@ -1236,17 +1259,21 @@ __global__ void __launch_bounds__(kEpiThreads, kMinBlocks)
             const uint32_t ob = out_w + (uint32_t)(it & 1) * kOutBuf;
             if (lane == 0) bulk_wait_read<1>();   // the store that last read this buffer is done with it
             __syncwarp();
+            // stmatrix: matrix m of a store is (nt0 + m / 2, rows 8 (m % 2) ..); lane l
+            // addresses row l % 8 of matrix l / 8 (swizzled 16-byte chunk nt ^ row)
 #pragma unroll
-            for (int nt = 0; nt < 8; ++nt)
+            for (int nt0 = 0; nt0 < 8; nt0 += 2) {
+                uint32_t r[4];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const float o0 = fmaf(arq[h], acc[4 * nt + 2 * h], lacc[nt][2 * h]);
-                    const float o1 = fmaf(arq[h], acc[4 * nt + 2 * h + 1], lacc[nt][2 * h + 1]);
-                    const uint32_t row = (uint32_t)(8 * h + g);
-                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(ob + row * kRow + ((nt ^ g) << 4) + 4 * q4),
-                                 "r"(pack_bf16(o0, o1))
-                                 : "memory");
+                for (int m = 0; m < 4; ++m) {
+                    const int nt = nt0 + (m >> 1), h = m & 1;
+                    r[m] = pack_bf16(fmaf(arq[h], acc[4 * nt + 2 * h], lacc[nt][2 * h]),
+                                     fmaf(arq[h], acc[4 * nt + 2 * h + 1], lacc[nt][2 * h + 1]));
                 }
+                const uint32_t mrow = (uint32_t)(lane & 7), mm = (uint32_t)(lane >> 3);
+                stsm_x4(ob + (8u * (mm & 1u) + mrow) * kRow + ((((uint32_t)nt0 + (mm >> 1)) ^ mrow) << 4), r[0], r[1],
+                        r[2], r[3]);
+            }
             fence_proxy_async();
             __syncwarp();
             const int br = tc.r0 + 2 * bi, bc = tc.c0 + 8 * bj;
