@@ -54,6 +54,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     return true;
 }
 
+// The same wait with a 64 ns back-off between polls, for a thread whose spinning
+// would take issue slots from the compute warps of its scheduler.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity) {
+    if (mbar_test_parity(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_test_parity(bar, parity)) {
+        __nanosleep(64);
+        if (clock64() - t0 > kWaitCycles) return false;
+    }
+    return true;
+}
 // ------------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

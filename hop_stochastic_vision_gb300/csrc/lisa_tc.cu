@@ -160,21 +160,30 @@ __device__ __forceinline__ float4 cluster_sum4(uint32_t local_addr, int CL) {
     return acc;
 }
 
-// U_next[i][a] = sum_b U[i][b] Mt[b][a] for `rows` rows (fp32, row stride 64),
-// four outputs of one row per work item.
+// U_next[i][a] = sum_b U[i][b] Mt[b][a] for `rows` rows (fp32, row stride 64,
+// 16-byte aligned).  A work item is one row and four consecutive columns; U
+// and Mt are read as float4, so each shared load feeds four FMAs; b in order.
 __device__ __forceinline__ void rows_times_mt(const float *U, const float *Mt, float *Un, int rows,
                                               int tid, int nthreads) {
     for (int item = tid; item < rows * 16; item += nthreads) {
-        const int i = item >> 4, a0 = item & 15;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const int i = item >> 4, c4 = item & 15;
+        const float4 *u4 = reinterpret_cast<const float4 *>(U + i * 64);
+        const float4 *m4 = reinterpret_cast<const float4 *>(Mt) + c4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-        for (int b = 0; b < 64; ++b) {
-            const float u = U[i * 64 + b];
+        for (int b4 = 0; b4 < 16; ++b4) {
+            const float4 u = u4[b4];
+            const float uu[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-            for (int k = 0; k < 4; ++k) acc[k] = fmaf(u, Mt[b * 64 + a0 + 16 * k], acc[k]);
+            for (int r = 0; r < 4; ++r) {
+                const float4 m = m4[(4 * b4 + r) * 16];
+                acc.x = fmaf(uu[r], m.x, acc.x);
+                acc.y = fmaf(uu[r], m.y, acc.y);
+                acc.z = fmaf(uu[r], m.z, acc.z);
+                acc.w = fmaf(uu[r], m.w, acc.w);
+            }
         }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) Un[i * 64 + a0 + 16 * k] = acc[k];
+        reinterpret_cast<float4 *>(Un + i * 64)[c4] = acc;
     }
 }
 
@@ -897,7 +906,7 @@ __global__ void __launch_bounds__(kEpiThreads, kMinBlocks)
             if (mlp) {
                 mbar_arrive_expect_tx(smem_u32(&bar.w1), 2u * p.n_mlp * kRow);
                 bulk_load(base + L.w1, p.w1img, 2u * p.n_mlp * kRow, smem_u32(&bar.w1));
-                if (!mbar_wait(smem_u32(&bar.w1), 0)) record_error(p.err, kErrTimeoutLoad);
+                if (!mbar_wait_sleep(smem_u32(&bar.w1), 0)) record_error(p.err, kErrTimeoutLoad);
             }
             const int nb = p.epi_nbepi;
             const uint32_t brow_bytes = (uint32_t)p.epi_rows * kRow;
@@ -912,19 +921,19 @@ __global__ void __launch_bounds__(kEpiThreads, kMinBlocks)
                     cur_b = n_loads % nb;
                     const int use = n_loads / nb;
                     if (use > 0) {
-                        if (!mbar_wait(smem_u32(&bar.b_free[cur_b]), (uint32_t)(use - 1) & 1u))
+                        if (!mbar_wait_sleep(smem_u32(&bar.b_free[cur_b]), (uint32_t)(use - 1) & 1u))
                             record_error(p.err, kErrTimeoutMma);
                         waited[cur_b] = use;
                     }
                     const uint32_t b = smem_u32(&bar.b_full[cur_b]);
                     mbar_arrive_expect_tx(b, brow_bytes);
                     bulk_load(base + L.bepi[cur_b], p.bepi + (size_t)sl * brow_bytes, brow_bytes, b);
-                    if (!mbar_wait(b, (uint32_t)use & 1u)) record_error(p.err, kErrTimeoutLoad);
+                    if (!mbar_wait_sleep(b, (uint32_t)use & 1u)) record_error(p.err, kErrTimeoutLoad);
                     ++n_loads;
                     cur_sl = sl;
                 }
-                if (!mbar_wait(smem_u32(&bar.qrelu[s]), ph)) record_error(p.err, kErrTimeoutLoad);
-                if (it >= kSlots && !mbar_wait(smem_u32(&bar.tmem_empty[s]), ph ^ 1u))
+                if (!mbar_wait_sleep(smem_u32(&bar.qrelu[s]), ph)) record_error(p.err, kErrTimeoutLoad);
+                if (it >= kSlots && !mbar_wait_sleep(smem_u32(&bar.tmem_empty[s]), ph ^ 1u))
                     record_error(p.err, kErrTimeoutMma);
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(s * p.slot_cols);
@@ -955,16 +964,16 @@ __global__ void __launch_bounds__(kEpiThreads, kMinBlocks)
                 }
                 // refill this slot with tile it + kSlots as soon as the warps and the MMA let go of it
                 if (t + kSlots < t_end) {
-                    if (!mbar_wait(smem_u32(&bar.qk_empty[s]), ph)) record_error(p.err, kErrTimeoutLoad);
-                    if (!mbar_wait(smem_u32(&bar.mma_full[s]), ph)) record_error(p.err, kErrTimeoutMma);
+                    if (!mbar_wait_sleep(smem_u32(&bar.qk_empty[s]), ph)) record_error(p.err, kErrTimeoutLoad);
+                    if (!mbar_wait_sleep(smem_u32(&bar.mma_full[s]), ph)) record_error(p.err, kErrTimeoutMma);
                     load_qk(t + kSlots, s);
-                    if (!mbar_wait(smem_u32(&bar.v_empty[s]), ph)) record_error(p.err, kErrTimeoutLoad);
+                    if (!mbar_wait_sleep(smem_u32(&bar.v_empty[s]), ph)) record_error(p.err, kErrTimeoutLoad);
                     load_v(t + kSlots, s);
                 }
             }
             // no commit may still be in flight when the CTA exits
             for (int b = 0; b < 2; ++b)
-                if (commits[b] > waited[b] && !mbar_wait(smem_u32(&bar.b_free[b]), (uint32_t)waited[b] & 1u))
+                if (commits[b] > waited[b] && !mbar_wait_sleep(smem_u32(&bar.b_free[b]), (uint32_t)waited[b] & 1u))
                     record_error(p.err, kErrTimeoutMma);
         }
         __syncwarp();
@@ -1368,23 +1377,23 @@ int sm_count() {
     return n;
 }
 
-constexpr int kSmemPerSm = 228 * 1024;        // shared memory of one SM
 constexpr int kSmemPerCta = 226 * 1024;       // dynamic shared memory one CTA may ask for
 
-// Epilogue configuration: two input slots if they fit one CTA's shared memory
-// and TMEM, else one; two B-operand buffers if they still fit, else one.
+// Epilogue configuration: one input slot, so that (fixed weights) an epilogue
+// CTA fits beside a statistics CTA and starts its loads and first local branch
+// while the statistics still run; two B-operand buffers if they fit, else one.
+// (Two slots at one CTA per SM measured slower on the PVT-T layer.)
 void epi_config(const TcParams &t, bool mlp, int *slots, int *nb, int *smem) {
     *slots = 0;
-    for (int s = 2; s >= 1; --s)
-        for (int b = 2; b >= 1; --b) {
-            const int bytes = (int)epi_layout(t.BR, t.BC, t.epi_rows, t.n_mlp, mlp, s, b).total + 1024;
-            if (bytes <= kSmemPerCta && s * t.slot_cols <= 512) {
-                *slots = s;
-                *nb = b;
-                *smem = bytes;
-                return;
-            }
+    for (int b = 2; b >= 1; --b) {
+        const int bytes = (int)epi_layout(t.BR, t.BC, t.epi_rows, t.n_mlp, mlp, 1, b).total + 1024;
+        if (bytes <= kSmemPerCta && t.slot_cols <= 512) {
+            *slots = 1;
+            *nb = b;
+            *smem = bytes;
+            return;
         }
+    }
 }
 
 }  // namespace
@@ -1503,10 +1512,7 @@ cudaError_t launch_tc(const Problem &p, cudaStream_t st, int stage) {
         if (slots == 0) return cudaErrorInvalidConfiguration;
         t.epi_nbepi = nb;
         const uint32_t cols = pow2_cols(slots * t.slot_cols);
-        int per_sm = kSmemPerSm / (smem + 1024);
-        if (per_sm > 2) per_sm = 2;
-        while (per_sm > 1 && per_sm * (int)cols > 512) --per_sm;
-        const int nctas = per_sm * sm_count();
+        const int nctas = sm_count();   // one persistent CTA per SM
         cfg.gridDim = dim3((unsigned)(t.tiles < nctas ? t.tiles : nctas));
         cfg.blockDim = dim3(kEpiThreads);
         cfg.dynamicSmemBytes = smem;
@@ -1517,12 +1523,7 @@ cudaError_t launch_tc(const Problem &p, cudaStream_t st, int stage) {
             if (e != cudaSuccess) return e;
             return cudaLaunchKernelEx(&cfg, kern, mq, mkh, mvh, mkt, mo, t, cols);
         };
-        if (mlp)
-            err = slots == 2 ? launch(tc_epilogue_kernel<true, 2, 1>, 2) : launch(tc_epilogue_kernel<true, 1, 1>, 3);
-        else if (slots == 2)
-            err = launch(tc_epilogue_kernel<false, 2, 1>, 4);
-        else
-            err = per_sm == 2 ? launch(tc_epilogue_kernel<false, 1, 2>, 5) : launch(tc_epilogue_kernel<false, 1, 1>, 6);
+        err = mlp ? launch(tc_epilogue_kernel<true, 1, 1>, 2) : launch(tc_epilogue_kernel<false, 1, 1>, 3);
         if (err != cudaSuccess) return err;
     }
     return cudaGetLastError();
