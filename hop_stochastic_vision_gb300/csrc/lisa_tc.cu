@@ -327,6 +327,11 @@ __global__ void __launch_bounds__(kStatsThreads) tc_stats_fused_kernel(const __g
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
+    // Launched as a programmatic dependent of whatever kernel precedes it on the
+    // stream: only set-up above this wait, which returns once that kernel has
+    // finished and its writes (Q, K, V, or a previous call's use of the
+    // workspace) are visible.  Dependents are released only after it.
+    pdl_wait();
     if (blockIdx.x == 0 && tid == 0) *p.err = 0;
     pdl_launch_dependents();
     bool ok = true;
@@ -516,6 +521,7 @@ __global__ void __launch_bounds__(kStatsThreads) tc_stats_fused_kernel(const __g
 __global__ void __launch_bounds__(256) tc_keysum_kernel(TcParams p) {
     __shared__ float red[32][kD + 1];
     const int sl = blockIdx.x / p.chunks, c = blockIdx.x % p.chunks;
+    pdl_wait();   // first kernel of the chain: the preceding kernel's writes are visible after this
     if (blockIdx.x == 0 && threadIdx.x == 0) *p.err = 0;
     pdl_launch_dependents();
     const int t0 = c * p.chunk, t1 = min(p.n, t0 + p.chunk);
@@ -1452,12 +1458,12 @@ cudaError_t launch_tc(const Problem &p, cudaStream_t st, int stage) {
     cfg.stream = st;
     cudaError_t err = cudaSuccess;
 
-    if (run(s_keysum)) {   // first kernel of the split chain: plain stream order
+    if (run(s_keysum)) {   // first kernel of the split chain: programmatic launch, waits on entry
         cfg.gridDim = dim3((unsigned)(p.slices * p.chunks));
         cfg.blockDim = dim3(256);
         cfg.dynamicSmemBytes = 0;
-        cfg.attrs = nullptr;
-        cfg.numAttrs = 0;
+        cfg.attrs = attrs;
+        cfg.numAttrs = 1;
         if ((err = cudaLaunchKernelEx(&cfg, tc_keysum_kernel, t)) != cudaSuccess) return err;
     }
     if (run(s_stats)) {
@@ -1476,8 +1482,8 @@ cudaError_t launch_tc(const Problem &p, cudaStream_t st, int stage) {
             if ((err = set_smem(tc_stats_fused_kernel, 0, smem)) != cudaSuccess) return err;
             cfg.dynamicSmemBytes = smem;
             cfg.blockDim = dim3(kStatsThreads);
-            cfg.attrs = attrs + 1;    // first kernel of the fused chain: cluster only
-            cfg.numAttrs = 1;
+            cfg.attrs = attrs;        // first kernel of the fused chain: waits after its set-up
+            cfg.numAttrs = 2;
             if ((err = cudaLaunchKernelEx(&cfg, tc_stats_fused_kernel, mq, mk, mv, t, kres)) != cudaSuccess)
                 return err;
         } else {
