@@ -187,6 +187,65 @@ __device__ __forceinline__ void rows_times_mt(const float *U, const float *Mt, f
     }
 }
 
+// Row strides (floats) of the fused statistics kernel's recurrence buffers,
+// chosen so the tensor-path fragment loads below are free of bank conflicts:
+// U_k, U_next, the fold: 68 (rows g of a fragment land on banks 4 g + c);
+// M^T: 72 (rows k = q, q + 4 land on banks 8 q + n).
+constexpr int kUS = 68;
+constexpr int kMS = 72;
+
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ void mma_tf32_1688(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Un[i][a] = sum_b U[i][b] Mt[b][a] for `rows` rows on the tensor path in TF32
+// (operands rounded to 10-bit mantissas, fp32 accumulation): U and Un with row
+// stride kUS, M^T with row stride kMS.  Warp w of `nwarps` takes the 8-column
+// tiles w, w + nwarps, ...; rows in tiles of 16 (missing rows read as zero and
+// are not stored).  The A fragments of a k-step are loaded once per row tile.
+__device__ __forceinline__ void rows_times_mt_tf32(const float *U, const float *Mt, float *Un, int rows, int warp,
+                                                   int lane, int nwarps) {
+    const int g = lane >> 2, q4 = lane & 3;
+    for (int m0 = 0; m0 < rows; m0 += 16) {
+        const int r0 = m0 + g, r1 = m0 + g + 8;
+        uint32_t a[8][4];
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            const int b = 8 * ks + q4;
+            a[ks][0] = r0 < rows ? to_tf32(U[r0 * kUS + b]) : 0u;
+            a[ks][1] = r1 < rows ? to_tf32(U[r1 * kUS + b]) : 0u;
+            a[ks][2] = r0 < rows ? to_tf32(U[r0 * kUS + b + 4]) : 0u;
+            a[ks][3] = r1 < rows ? to_tf32(U[r1 * kUS + b + 4]) : 0u;
+        }
+        for (int nt = warp; nt < 8; nt += nwarps) {
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const int b = 8 * ks + q4;
+                mma_tf32_1688(d, a[ks][0], a[ks][1], a[ks][2], a[ks][3], to_tf32(Mt[b * kMS + 8 * nt + g]),
+                              to_tf32(Mt[(b + 4) * kMS + 8 * nt + g]));
+            }
+            if (r0 < rows) {
+                Un[r0 * kUS + 8 * nt + 2 * q4] = d[0];
+                Un[r0 * kUS + 8 * nt + 2 * q4 + 1] = d[1];
+            }
+            if (r1 < rows) {
+                Un[r1 * kUS + 8 * nt + 2 * q4] = d[2];
+                Un[r1 * kUS + 8 * nt + 2 * q4 + 1] = d[3];
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------- shared stats steps
 // Q~_j = Q_j / (Q_j . s + eps) in place for the 64 tokens of a stage (128
 // threads, two per token, 32 features each); ReLU on load when asked.
@@ -453,8 +512,8 @@ __global__ void __launch_bounds__(kStatsThreads) tc_stats_fused_kernel(const __g
     // and pushes each reduced M^T row into every CTA's copy of M^T; its own
     // U_1^T rows stay local.
     float *red = reinterpret_cast<float *>(sm);                    // [128][68]
-    float *Mt = reinterpret_cast<float *>(sm + 36 * 1024);         // [64][64], filled by the owners
-    float *Ucur = reinterpret_cast<float *>(sm + 52 * 1024);       // [my_u][64]
+    float *Mt = reinterpret_cast<float *>(sm + 36 * 1024);         // [64][kMS], filled by the owners
+    float *Ucur = reinterpret_cast<float *>(sm + 54 * 1024);       // [my_u][kUS]
     const int my_u = (64 - (int)rank + CL - 1) / CL;               // own rows e < 64
     if (warp < 4) tmem_rows_to_smem(tmem, red, warp, lane);
     tc_fence_before();
@@ -468,9 +527,9 @@ __global__ void __launch_bounds__(kStatsThreads) tc_stats_fused_kernel(const __g
             const int rr = (int)rank + CL * k;
             const float4 v = cluster_sum4(red_addr + (uint32_t)(rr * kRedStride + 4 * f) * 4u, CL);
             if (rr < 64) {
-                reinterpret_cast<float4 *>(Ucur + k * kD)[f] = v;
+                reinterpret_cast<float4 *>(Ucur + k * kUS)[f] = v;
             } else {
-                const uint32_t dst = mt_addr + (uint32_t)((rr - 64) * kD + 4 * f) * 4u;
+                const uint32_t dst = mt_addr + (uint32_t)((rr - 64) * kMS + 4 * f) * 4u;
 #pragma unroll
                 for (int q = 0; q < 8; ++q)
                     if (q < CL) st_dsmem4(map_rank(dst, (uint32_t)q), v);
@@ -480,25 +539,35 @@ __global__ void __launch_bounds__(kStatsThreads) tc_stats_fused_kernel(const __g
     cluster_sync();                                                // (C) M^T complete everywhere
 
     // ---- U_k^T = U_(k-1)^T M^T on the own rows; B operand rows
-    float *Unext = reinterpret_cast<float *>(sm);
-    float *Fold = reinterpret_cast<float *>(sm + 16 * 1024);
+    float *Unext = reinterpret_cast<float *>(sm);                  // [my_u][kUS]
+    float *Fold = reinterpret_cast<float *>(sm + 18 * 1024);       // [my_u][kUS]
     const bool folded = (p.wmode != LISA_W_MLP);
     uint8_t *img = p.bepi + (size_t)sl * p.epi_rows * kRow;
-    for (int idx = tid; idx < my_u * kD; idx += kStatsThreads) Fold[idx] = 0.f;
+    for (int item = tid; item < my_u * 16; item += kStatsThreads)
+        reinterpret_cast<float4 *>(Fold + (item >> 4) * kUS)[item & 15] = make_float4(0.f, 0.f, 0.f, 0.f);
     __syncthreads();
     for (int k = 1; k < p.T; ++k) {
         if (k > 1) {
-            rows_times_mt(Ucur, Mt, Unext, my_u, tid, kStatsThreads);
+            if (warp < 4) rows_times_mt_tf32(Ucur, Mt, Unext, my_u, warp, lane, 4);
             __syncthreads();
-            for (int idx = tid; idx < my_u * kD; idx += kStatsThreads) Ucur[idx] = Unext[idx];
+            for (int item = tid; item < my_u * 16; item += kStatsThreads)
+                reinterpret_cast<float4 *>(Ucur + (item >> 4) * kUS)[item & 15] =
+                    reinterpret_cast<const float4 *>(Unext + (item >> 4) * kUS)[item & 15];
             __syncthreads();
         }
         if (folded) {
-            for (int idx = tid; idx < my_u * kD; idx += kStatsThreads) Fold[idx] = fmaf(p.w[k], Ucur[idx], Fold[idx]);
+            const float wk = p.w[k];
+            for (int item = tid; item < my_u * 16; item += kStatsThreads) {
+                float4 *f4 = reinterpret_cast<float4 *>(Fold + (item >> 4) * kUS) + (item & 15);
+                const float4 u = reinterpret_cast<const float4 *>(Ucur + (item >> 4) * kUS)[item & 15];
+                float4 f = *f4;
+                f.x = fmaf(wk, u.x, f.x); f.y = fmaf(wk, u.y, f.y); f.z = fmaf(wk, u.z, f.z); f.w = fmaf(wk, u.w, f.w);
+                *f4 = f;
+            }
         } else {
             for (int item = tid; item < my_u * 8; item += kStatsThreads) {
                 const int i = item >> 3, chunk = item & 7;
-                put_row_bf16(img, (k - 1) * kD + (int)rank + CL * i, Ucur + i * kD + chunk * 8, chunk);
+                put_row_bf16(img, (k - 1) * kD + (int)rank + CL * i, Ucur + i * kUS + chunk * 8, chunk);
             }
         }
         __syncthreads();
@@ -506,7 +575,7 @@ __global__ void __launch_bounds__(kStatsThreads) tc_stats_fused_kernel(const __g
     if (folded)
         for (int item = tid; item < my_u * 8; item += kStatsThreads) {
             const int i = item >> 3, chunk = item & 7;
-            put_row_bf16(img, (int)rank + CL * i, Fold + i * kD + chunk * 8, chunk);
+            put_row_bf16(img, (int)rank + CL * i, Fold + i * kUS + chunk * 8, chunk);
         }
     if (rank == 0) put_s_rows(img, p.n_umat * kD, s_sh, tid);
     if (!folded && sl == 0 && rank == 0) put_w1_image(p, tid, kStatsThreads);
@@ -912,7 +981,7 @@ __global__ void __launch_bounds__(kEpiThreads, kMinBlocks)
             if (mlp) {
                 mbar_arrive_expect_tx(smem_u32(&bar.w1), 2u * p.n_mlp * kRow);
                 bulk_load(base + L.w1, p.w1img, 2u * p.n_mlp * kRow, smem_u32(&bar.w1));
-                if (!mbar_wait_sleep(smem_u32(&bar.w1), 0)) record_error(p.err, kErrTimeoutLoad);
+                if (!mbar_wait(smem_u32(&bar.w1), 0)) record_error(p.err, kErrTimeoutLoad);
             }
             const int nb = p.epi_nbepi;
             const uint32_t brow_bytes = (uint32_t)p.epi_rows * kRow;
@@ -927,19 +996,19 @@ __global__ void __launch_bounds__(kEpiThreads, kMinBlocks)
                     cur_b = n_loads % nb;
                     const int use = n_loads / nb;
                     if (use > 0) {
-                        if (!mbar_wait_sleep(smem_u32(&bar.b_free[cur_b]), (uint32_t)(use - 1) & 1u))
+                        if (!mbar_wait(smem_u32(&bar.b_free[cur_b]), (uint32_t)(use - 1) & 1u))
                             record_error(p.err, kErrTimeoutMma);
                         waited[cur_b] = use;
                     }
                     const uint32_t b = smem_u32(&bar.b_full[cur_b]);
                     mbar_arrive_expect_tx(b, brow_bytes);
                     bulk_load(base + L.bepi[cur_b], p.bepi + (size_t)sl * brow_bytes, brow_bytes, b);
-                    if (!mbar_wait_sleep(b, (uint32_t)use & 1u)) record_error(p.err, kErrTimeoutLoad);
+                    if (!mbar_wait(b, (uint32_t)use & 1u)) record_error(p.err, kErrTimeoutLoad);
                     ++n_loads;
                     cur_sl = sl;
                 }
-                if (!mbar_wait_sleep(smem_u32(&bar.qrelu[s]), ph)) record_error(p.err, kErrTimeoutLoad);
-                if (it >= kSlots && !mbar_wait_sleep(smem_u32(&bar.tmem_empty[s]), ph ^ 1u))
+                if (!mbar_wait(smem_u32(&bar.qrelu[s]), ph)) record_error(p.err, kErrTimeoutLoad);
+                if (it >= kSlots && !mbar_wait(smem_u32(&bar.tmem_empty[s]), ph ^ 1u))
                     record_error(p.err, kErrTimeoutMma);
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(s * p.slot_cols);
@@ -970,16 +1039,16 @@ __global__ void __launch_bounds__(kEpiThreads, kMinBlocks)
                 }
                 // refill this slot with tile it + kSlots as soon as the warps and the MMA let go of it
                 if (t + kSlots < t_end) {
-                    if (!mbar_wait_sleep(smem_u32(&bar.qk_empty[s]), ph)) record_error(p.err, kErrTimeoutLoad);
-                    if (!mbar_wait_sleep(smem_u32(&bar.mma_full[s]), ph)) record_error(p.err, kErrTimeoutMma);
+                    if (!mbar_wait(smem_u32(&bar.qk_empty[s]), ph)) record_error(p.err, kErrTimeoutLoad);
+                    if (!mbar_wait(smem_u32(&bar.mma_full[s]), ph)) record_error(p.err, kErrTimeoutMma);
                     load_qk(t + kSlots, s);
-                    if (!mbar_wait_sleep(smem_u32(&bar.v_empty[s]), ph)) record_error(p.err, kErrTimeoutLoad);
+                    if (!mbar_wait(smem_u32(&bar.v_empty[s]), ph)) record_error(p.err, kErrTimeoutLoad);
                     load_v(t + kSlots, s);
                 }
             }
             // no commit may still be in flight when the CTA exits
             for (int b = 0; b < 2; ++b)
-                if (commits[b] > waited[b] && !mbar_wait_sleep(smem_u32(&bar.b_free[b]), (uint32_t)waited[b] & 1u))
+                if (commits[b] > waited[b] && !mbar_wait(smem_u32(&bar.b_free[b]), (uint32_t)waited[b] & 1u))
                     record_error(p.err, kErrTimeoutMma);
         }
         __syncwarp();
