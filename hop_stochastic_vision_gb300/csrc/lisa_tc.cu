@@ -212,8 +212,10 @@ __device__ __forceinline__ void mma_tf32_1688(float (&d)[4], uint32_t a0, uint32
 // stride kUS, M^T with row stride kMS.  Warp w of `nwarps` takes the 8-column
 // tiles w, w + nwarps, ...; rows in tiles of 16 (missing rows read as zero and
 // are not stored).  The A fragments of a k-step are loaded once per row tile.
+// With `fold`, also fold[i][a] += wk * Un[i][a] (stride kUS; each element is
+// owned by the thread that computes it).
 __device__ __forceinline__ void rows_times_mt_tf32(const float *U, const float *Mt, float *Un, int rows, int warp,
-                                                   int lane, int nwarps) {
+                                                   int lane, int nwarps, float *fold, float wk) {
     const int g = lane >> 2, q4 = lane & 3;
     for (int m0 = 0; m0 < rows; m0 += 16) {
         const int r0 = m0 + g, r1 = m0 + g + 8;
@@ -234,13 +236,22 @@ __device__ __forceinline__ void rows_times_mt_tf32(const float *U, const float *
                 mma_tf32_1688(d, a[ks][0], a[ks][1], a[ks][2], a[ks][3], to_tf32(Mt[b * kMS + 8 * nt + g]),
                               to_tf32(Mt[(b + 4) * kMS + 8 * nt + g]));
             }
+            const int c = 8 * nt + 2 * q4;
             if (r0 < rows) {
-                Un[r0 * kUS + 8 * nt + 2 * q4] = d[0];
-                Un[r0 * kUS + 8 * nt + 2 * q4 + 1] = d[1];
+                Un[r0 * kUS + c] = d[0];
+                Un[r0 * kUS + c + 1] = d[1];
+                if (fold) {
+                    fold[r0 * kUS + c] = fmaf(wk, d[0], fold[r0 * kUS + c]);
+                    fold[r0 * kUS + c + 1] = fmaf(wk, d[1], fold[r0 * kUS + c + 1]);
+                }
             }
             if (r1 < rows) {
-                Un[r1 * kUS + 8 * nt + 2 * q4] = d[2];
-                Un[r1 * kUS + 8 * nt + 2 * q4 + 1] = d[3];
+                Un[r1 * kUS + c] = d[2];
+                Un[r1 * kUS + c + 1] = d[3];
+                if (fold) {
+                    fold[r1 * kUS + c] = fmaf(wk, d[2], fold[r1 * kUS + c]);
+                    fold[r1 * kUS + c + 1] = fmaf(wk, d[3], fold[r1 * kUS + c + 1]);
+                }
             }
         }
     }
@@ -543,34 +554,35 @@ __global__ void __launch_bounds__(kStatsThreads) tc_stats_fused_kernel(const __g
     float *Fold = reinterpret_cast<float *>(sm + 18 * 1024);       // [my_u][kUS]
     const bool folded = (p.wmode != LISA_W_MLP);
     uint8_t *img = p.bepi + (size_t)sl * p.epi_rows * kRow;
-    for (int item = tid; item < my_u * 16; item += kStatsThreads)
-        reinterpret_cast<float4 *>(Fold + (item >> 4) * kUS)[item & 15] = make_float4(0.f, 0.f, 0.f, 0.f);
-    __syncthreads();
-    for (int k = 1; k < p.T; ++k) {
-        if (k > 1) {
-            if (warp < 4) rows_times_mt_tf32(Ucur, Mt, Unext, my_u, warp, lane, 4);
-            __syncthreads();
-            for (int item = tid; item < my_u * 16; item += kStatsThreads)
-                reinterpret_cast<float4 *>(Ucur + (item >> 4) * kUS)[item & 15] =
-                    reinterpret_cast<const float4 *>(Unext + (item >> 4) * kUS)[item & 15];
-            __syncthreads();
+    // k = 1: the fold starts at w_1 U_1 (or U_1's rows go out); then U_k = U_(k-1) M^T
+    // on the tensor path into the other buffer, with the fold updated from the
+    // result fragments
+    if (folded) {
+        const float w1 = p.T > 1 ? p.w[1] : 0.f;   // T = 1: no hop terms, the fold stays zero
+        for (int item = tid; item < my_u * 16; item += kStatsThreads) {
+            const float4 u = reinterpret_cast<const float4 *>(Ucur + (item >> 4) * kUS)[item & 15];
+            reinterpret_cast<float4 *>(Fold + (item >> 4) * kUS)[item & 15] =
+                make_float4(w1 * u.x, w1 * u.y, w1 * u.z, w1 * u.w);
         }
-        if (folded) {
-            const float wk = p.w[k];
-            for (int item = tid; item < my_u * 16; item += kStatsThreads) {
-                float4 *f4 = reinterpret_cast<float4 *>(Fold + (item >> 4) * kUS) + (item & 15);
-                const float4 u = reinterpret_cast<const float4 *>(Ucur + (item >> 4) * kUS)[item & 15];
-                float4 f = *f4;
-                f.x = fmaf(wk, u.x, f.x); f.y = fmaf(wk, u.y, f.y); f.z = fmaf(wk, u.z, f.z); f.w = fmaf(wk, u.w, f.w);
-                *f4 = f;
-            }
-        } else {
+    } else {
+        for (int item = tid; item < my_u * 8; item += kStatsThreads) {
+            const int i = item >> 3, chunk = item & 7;
+            put_row_bf16(img, (int)rank + CL * i, Ucur + i * kUS + chunk * 8, chunk);
+        }
+    }
+    __syncthreads();
+    float *Ua = Ucur, *Ub = Unext;
+    for (int k = 2; k < p.T; ++k) {
+        if (warp < 4) rows_times_mt_tf32(Ua, Mt, Ub, my_u, warp, lane, 4, folded ? Fold : nullptr, p.w[k]);
+        __syncthreads();
+        if (!folded)
             for (int item = tid; item < my_u * 8; item += kStatsThreads) {
                 const int i = item >> 3, chunk = item & 7;
-                put_row_bf16(img, (k - 1) * kD + (int)rank + CL * i, Ucur + i * kUS + chunk * 8, chunk);
+                put_row_bf16(img, (k - 1) * kD + (int)rank + CL * i, Ub + i * kUS + chunk * 8, chunk);
             }
-        }
-        __syncthreads();
+        float *tmp = Ua;
+        Ua = Ub;
+        Ub = tmp;
     }
     if (folded)
         for (int item = tid; item < my_u * 8; item += kStatsThreads) {
