@@ -877,6 +877,13 @@ __host__ __device__ inline EpiLayout epi_layout(int BR, int BC, int epi_rows, in
     return L;
 }
 
+// 2^x on the special-function unit (PTX ex2.approx, flush-to-zero); 2^-inf = +0.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ float gelu_erf(float x) {
     return 0.5f * x * (1.f + erff(x * 0.70710678118654752f));
 }
@@ -1262,12 +1269,16 @@ __global__ void __launch_bounds__(kEpiThreads, kMinBlocks)
 #pragma unroll
                         for (int e = 0; e < 4; ++e) sc[j][e] = fmaf(sc[j][e], c2, wbias[j][e]);
                 }
-                float mx[2] = {-INFINITY, -INFINITY};
+                // row maxima and sums as balanced trees over the 10 elements of each row
+                float mx[2];
 #pragma unroll
-                for (int j = 0; j < 5; ++j)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) mx[e >> 1] = fmaxf(mx[e >> 1], sc[j][e]);
-                float sum[2] = {0.f, 0.f};
+                for (int h = 0; h < 2; ++h) {
+                    const float a0 = fmaxf(sc[0][2 * h], sc[0][2 * h + 1]), a1 = fmaxf(sc[1][2 * h], sc[1][2 * h + 1]);
+                    const float a2 = fmaxf(sc[2][2 * h], sc[2][2 * h + 1]), a3 = fmaxf(sc[3][2 * h], sc[3][2 * h + 1]);
+                    const float a4 = fmaxf(sc[4][2 * h], sc[4][2 * h + 1]);
+                    mx[h] = fmaxf(fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)), a4);
+                }
+                float sum[2];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
@@ -1277,10 +1288,14 @@ __global__ void __launch_bounds__(kEpiThreads, kMinBlocks)
 #pragma unroll
                 for (int j = 0; j < 5; ++j)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        sc[j][e] = exp2f(sc[j][e] - mx[e >> 1]);
-                        sum[e >> 1] += sc[j][e];
-                    }
+                    for (int e = 0; e < 4; ++e) sc[j][e] = ex2_approx(sc[j][e] - mx[e >> 1]);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float a0 = sc[0][2 * h] + sc[0][2 * h + 1], a1 = sc[1][2 * h] + sc[1][2 * h + 1];
+                    const float a2 = sc[2][2 * h] + sc[2][2 * h + 1], a3 = sc[3][2 * h] + sc[3][2 * h + 1];
+                    const float a4 = sc[4][2 * h] + sc[4][2 * h + 1];
+                    sum[h] = ((a0 + a1) + (a2 + a3)) + a4;
+                }
                 float scale[2], self[2];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
