@@ -1116,6 +1116,8 @@ __global__ void __launch_bounds__(kEpiThreads, kMinBlocks)
         const float c2 = 1.4426950408889634f * 0.125f;   // log2(e) / sqrt(64)
 
         TileCoord tc = tile_coord(p, t_begin);
+        int alpha_sl = -1;   // the head's alpha is read from global memory once per slice
+        float alpha = 0.f;
         for (int t = t_begin, it = 0; t < t_end; ++t, ++it) {
             if (it > 0) {   // next tile in row-major order of the slice's tile grid
                 tc.c0 += 8 * BC;
@@ -1130,7 +1132,10 @@ __global__ void __launch_bounds__(kEpiThreads, kMinBlocks)
             }
             const int s = it % kSlots;
             const uint32_t ph = (uint32_t)(it / kSlots) & 1u;
-            const float alpha = p.alpha[tc.sl % p.heads];
+            if (tc.sl != alpha_sl) {
+                alpha = p.alpha[tc.sl % p.heads];
+                alpha_sl = tc.sl;
+            }
             const uint32_t tl = tmem + (uint32_t)(s * p.slot_cols) + lane_base;
 
             // ---- the block's queries: A fragments, ReLU'd in registers and written
@@ -1301,7 +1306,7 @@ __global__ void __launch_bounds__(kEpiThreads, kMinBlocks)
                 for (int h = 0; h < 2; ++h) {
                     sum[h] += __shfl_xor_sync(0xffffffffu, sum[h], 1);
                     sum[h] += __shfl_xor_sync(0xffffffffu, sum[h], 2);
-                    scale[h] = sum[h] > 0.f ? (1.f - alpha) / sum[h] : 0.f;
+                    scale[h] = sum[h] > 0.f ? __fdividef(1.f - alpha, sum[h]) : 0.f;
                     self[h] = alpha * w0[h];
                 }
 #pragma unroll
