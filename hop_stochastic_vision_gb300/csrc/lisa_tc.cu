@@ -449,18 +449,25 @@ __global__ void __launch_bounds__(kStatsThreads) tc_stats_fused_kernel(const __g
             float acc[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-            for (int j = jl; j < nsub * kSub; j += 16) {
-                uint4 *ptr = reinterpret_cast<uint4 *>(kres + sw128_offset(j, cg));
-                uint4 v = *ptr;
-                if (p.relu) {
-                    v = relu4(v);
-                    *ptr = v;
-                }
-                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+            for (int j0 = jl; j0 < nsub * kSub; j0 += 64) {   // four tokens per thread in flight
+                uint4 v[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    acc[2 * e] += bf16_lo(w4[e]);
-                    acc[2 * e + 1] += bf16_hi(w4[e]);
+                for (int u = 0; u < 4; ++u) v[u] = *reinterpret_cast<const uint4 *>(kres + sw128_offset(j0 + 16 * u, cg));
+                if (p.relu) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        v[u] = relu4(v[u]);
+                        *reinterpret_cast<uint4 *>(kres + sw128_offset(j0 + 16 * u, cg)) = v[u];
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        acc[2 * e] += bf16_lo(w4[e]);
+                        acc[2 * e + 1] += bf16_hi(w4[e]);
+                    }
                 }
             }
 #pragma unroll
