@@ -104,7 +104,9 @@ def forward(xq, xk, v, grid, T, *, alpha, beta=None, w=None, mlp=None, eps=1e-6,
     xq, xk: [B, heads, n, d_h]; v: [B, heads, n, d_v]; grid = (H, W), n = H*W.
     Exactly one of ``beta`` (geometric weights), ``w`` (fixed weights, length
     T) or ``mlp`` = (W1 [hidden, 2 d_h], b1 [hidden], W2 [T, hidden], b2 [T])
-    selects the walk weights.  ``alpha`` is a scalar or [heads].
+    selects the walk weights.  ``T = 0`` with ``beta`` is the untruncated
+    geometric walk, g = (1 - beta) (I - beta S)^-1 V.  ``alpha`` is a scalar
+    or [heads].
     Returns O, or (O, G, L) with the global and local branches when
     ``branches`` is set.
     """
@@ -120,6 +122,8 @@ def forward(xq, xk, v, grid, T, *, alpha, beta=None, w=None, mlp=None, eps=1e-6,
     wmode, wv, W1 = W_GEOMETRIC, None, None
     b1 = W2 = b2 = None
     hidden = 0
+    if T == 0 and (beta is None or w is not None or mlp is not None):
+        raise ValueError("T = 0 (untruncated walk) needs geometric weights (beta)")
     if w is not None:
         wmode, wv = W_FIXED, _f64(w)
         if wv.shape != (T,):

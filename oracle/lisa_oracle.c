@@ -29,10 +29,20 @@
  *     zero-padded), softmax over those, applied to V.
  *   - alpha is used as given, one value per head.
  *
+ * Untruncated walk (T = 0 with geometric weights): the note (§2.3, the
+ * closing remark on the geometric series) observes that without truncation
+ * the series has a closed form; with weights (1-beta) beta^k for every k >= 0
+ * it is g = (1-beta) (I - beta S)^(-1) V.
+ *
  * Two evaluation modes give the same global branch by different routes:
  *   EXPLICIT: rows of S are formed one at a time and Y_k = S Y_(k-1) is
  *             iterated over n x n products (O(T n^2 d)); S is never stored.
  *   LOWRANK:  s, M = K^T Q~, U_1 = K^T V, U_k = M U_(k-1), Y_k = Q~ U_k.
+ * and, for the untruncated walk,
+ *   EXPLICIT: the n x n system (I - beta S) X = V solved densely;
+ *   LOWRANK:  (I - beta Q~ K^T)^(-1) = I + beta Q~ (I - beta M)^(-1) K^T (the
+ *             push-through identity, a derivation of ours, not the note's), so
+ *             g = (1-beta) (V + beta Q~ Z) with (I - beta M) Z = U_1, d x d.
  *
  * Every array is row-major, double precision, contiguous:
  *   Q, K  [B][heads][n][d_h]      V, O, G, L  [B][heads][n][d_v]
@@ -199,6 +209,106 @@ static void walk_terms_lowrank(const double *Qt, const double *K,
 }
 
 /* ---------------------------------------------------------------------- */
+/* Dense linear solve A X = R (A: n x n, R: n x m, row-major; both are      */
+/* overwritten, X is left in R) by Gaussian elimination with partial        */
+/* pivoting and back substitution.  Returns 3 for a singular A.             */
+/* ---------------------------------------------------------------------- */
+static int solve_dense(double *A, double *R, int n, int m)
+{
+    for (int p = 0; p < n; ++p) {
+        int piv = p;
+        double best = fabs(A[(long)p * n + p]);
+        for (int i = p + 1; i < n; ++i)
+            if (fabs(A[(long)i * n + p]) > best) {
+                best = fabs(A[(long)i * n + p]);
+                piv = i;
+            }
+        if (!(best > 0.0)) return 3;
+        if (piv != p) {
+            for (int j = 0; j < n; ++j) {
+                double t = A[(long)p * n + j];
+                A[(long)p * n + j] = A[(long)piv * n + j];
+                A[(long)piv * n + j] = t;
+            }
+            for (int e = 0; e < m; ++e) {
+                double t = R[(long)p * m + e];
+                R[(long)p * m + e] = R[(long)piv * m + e];
+                R[(long)piv * m + e] = t;
+            }
+        }
+#pragma omp parallel for schedule(static)
+        for (int i = p + 1; i < n; ++i) {
+            const double f = A[(long)i * n + p] / A[(long)p * n + p];
+            A[(long)i * n + p] = 0.0;
+            for (int j = p + 1; j < n; ++j) A[(long)i * n + j] -= f * A[(long)p * n + j];
+            for (int e = 0; e < m; ++e) R[(long)i * m + e] -= f * R[(long)p * m + e];
+        }
+    }
+    for (int p = n - 1; p >= 0; --p)
+        for (int e = 0; e < m; ++e) {
+            double acc = R[(long)p * m + e];
+            for (int j = p + 1; j < n; ++j) acc -= A[(long)p * n + j] * R[(long)j * m + e];
+            R[(long)p * m + e] = acc / A[(long)p * n + p];
+        }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Untruncated geometric walk: g = (1-beta) sum_{k>=0} beta^k S^k V         */
+/*                               = (1-beta) (I - beta S)^(-1) V.            */
+/* EXPLICIT solves the n x n system; LOWRANK the d x d one of the           */
+/* push-through identity, g = (1-beta) (V + beta Q~ Z), (I - beta M) Z = U_1.*/
+/* ---------------------------------------------------------------------- */
+static int walk_untruncated(const double *Qt, const double *K, const double *V, int n,
+                            int dh, int dv, double beta, int mode, double *g)
+{
+    int err = 0;
+    if (mode == ORACLE_EXPLICIT) {
+        double *A = malloc(sizeof(double) * (size_t)n * n);
+        if (!A) return 2;
+#pragma omp parallel for schedule(static)
+        for (int i = 0; i < n; ++i)
+            for (int j = 0; j < n; ++j) {
+                double sij = 0.0;
+                for (int a = 0; a < dh; ++a) sij += Qt[(long)i * dh + a] * K[(long)j * dh + a];
+                A[(long)i * n + j] = (i == j ? 1.0 : 0.0) - beta * sij;
+            }
+        memcpy(g, V, sizeof(double) * (size_t)n * dv);
+        err = solve_dense(A, g, n, dv);
+        for (long t = 0; t < (long)n * dv; ++t) g[t] *= 1.0 - beta;
+        free(A);
+        return err;
+    }
+    double *A = malloc(sizeof(double) * (size_t)dh * dh);
+    double *Z = malloc(sizeof(double) * (size_t)dh * dv);
+    if (!A || !Z) { free(A); free(Z); return 2; }
+    for (int a = 0; a < dh; ++a)
+        for (int b = 0; b < dh; ++b) {
+            double acc = 0.0;   /* M_ab = sum_j K_j[a] Q~_j[b] */
+            for (int j = 0; j < n; ++j) acc += K[(long)j * dh + a] * Qt[(long)j * dh + b];
+            A[a * dh + b] = (a == b ? 1.0 : 0.0) - beta * acc;
+        }
+    for (int a = 0; a < dh; ++a)
+        for (int e = 0; e < dv; ++e) {
+            double acc = 0.0;   /* (U_1)_ae = sum_j K_j[a] V_j[e] */
+            for (int j = 0; j < n; ++j) acc += K[(long)j * dh + a] * V[(long)j * dv + e];
+            Z[a * dv + e] = acc;
+        }
+    err = solve_dense(A, Z, dh, dv);
+    if (!err) {
+#pragma omp parallel for schedule(static)
+        for (int i = 0; i < n; ++i)
+            for (int e = 0; e < dv; ++e) {
+                double acc = 0.0;
+                for (int a = 0; a < dh; ++a) acc += Qt[(long)i * dh + a] * Z[a * dv + e];
+                g[(long)i * dv + e] = (1.0 - beta) * (V[(long)i * dv + e] + beta * acc);
+            }
+    }
+    free(A); free(Z);
+    return err;
+}
+
+/* ---------------------------------------------------------------------- */
 /* Adaptive step weights [note §2.4] (paper Eq. 10, Supp. Sec. 8):          */
 /* x = concat(q_i, k_i);  h = GELU(W1 x + b1);  z = W2 h + b2;              */
 /* w(i) = softmax(z) over the T walk lengths.  W1 is [hidden][2*dh] and     */
@@ -281,8 +391,8 @@ static void local_branch(const double *Qf, const double *Kf, const double *V,
 /* alpha mix  o = alpha * g + (1 - alpha) * l  [note §2.4] (paper Fig. 2).   */
 /* ---------------------------------------------------------------------- */
 typedef struct {
-    int H, W, dh, dv, T, wmode, hidden, mode, relu;
-    double eps;
+    int H, W, dh, dv, T, wmode, hidden, mode, relu;   /* T = 0: untruncated walk */
+    double eps, beta;
     const double *w, *W1, *b1, *W2, *b2;
 } slice_args;
 
@@ -294,7 +404,7 @@ static int forward_slice(const slice_args *A, const double *Xq, const double *Xk
     double *Qf = malloc(sizeof(double) * (size_t)n * dh);
     double *Kf = malloc(sizeof(double) * (size_t)n * dh);
     double *Qt = malloc(sizeof(double) * (size_t)n * dh);
-    double *Y = malloc(sizeof(double) * (size_t)T * n * dv);
+    double *Y = malloc(sizeof(double) * (size_t)(T > 0 ? T : 1) * n * dv);
     double *g = malloc(sizeof(double) * (size_t)n * dv);
     double *l = malloc(sizeof(double) * (size_t)n * dv);
     double *Srows = malloc(sizeof(double) * (size_t)n * omp_threads());
@@ -311,12 +421,16 @@ static int forward_slice(const slice_args *A, const double *Xq, const double *Xk
     feature_map(Xk, Kf, (long)n * dh, A->relu);
     key_sum(Kf, n, dh, s);
     normalised_queries(Qf, s, n, dh, A->eps, Qt);
-    if (A->mode == ORACLE_EXPLICIT)
+    if (T == 0) {
+        err = walk_untruncated(Qt, Kf, V, n, dh, dv, A->beta, A->mode, g);
+        if (err) goto done;
+    } else if (A->mode == ORACLE_EXPLICIT)
         walk_terms_explicit(Qt, Kf, V, n, dh, dv, T, Y, Srows);
     else
         walk_terms_lowrank(Qt, Kf, V, n, dh, dv, T, Y, M, U, Un);
 
     /* g_i = sum_k w_k(i) Y_k,i with the token's own weights in MLP mode */
+    if (T > 0) {
 #pragma omp parallel for schedule(static)
     for (int i = 0; i < n; ++i) {
         double wk[ORACLE_MAX_T], h[ORACLE_MAX_HIDDEN];
@@ -330,6 +444,7 @@ static int forward_slice(const slice_args *A, const double *Xq, const double *Xk
             for (int k = 0; k < T; ++k) acc += wk[k] * Y[(size_t)k * n * dv + (long)i * dv + x];
             g[(long)i * dv + x] = acc;
         }
+    }
     }
     local_branch(Qf, Kf, V, A->H, A->W, dh, dv, l);
     for (long t = 0; t < (long)n * dv; ++t) {
@@ -346,11 +461,13 @@ done:
 /*
  * Full layer over B x heads independent slices.
  *   wmode   0 geometric (beta), 1 fixed (w[T]), 2 MLP (W1,b1,W2,b2,hidden)
+ *   T       walk truncation depth >= 1; 0 with geometric weights: untruncated
  *   alpha   [heads]
  *   mode    0 EXPLICIT, 1 LOWRANK
  *   O, G, L may each be NULL; G and L receive the global and local branches.
  *   nthreads <= 0 uses the OpenMP default.
- * Returns 0 on success, 1 on a bad argument, 2 on allocation failure.
+ * Returns 0 on success, 1 on a bad argument, 2 on allocation failure, 3 when
+ * an untruncated walk meets a singular system.
  */
 int lisa_oracle_forward(const double *Xq, const double *Xk, const double *V,
                         double *O, double *G, double *L, int B, int heads,
@@ -360,13 +477,16 @@ int lisa_oracle_forward(const double *Xq, const double *Xk, const double *V,
                         int hidden, const double *alpha, double eps,
                         int relu_inputs, int mode, int nthreads)
 {
-    if (B < 0 || heads < 0 || H < 1 || W < 1 || dh < 1 || dh > 256 || dv < 1 || T < 1 ||
+    if (B < 0 || heads < 0 || H < 1 || W < 1 || dh < 1 || dh > 256 || dv < 1 || T < 0 ||
         T > ORACLE_MAX_T)
         return 1;
     if (eps < 0.0 || !alpha) return 1;
-    double *wts = malloc(sizeof(double) * (size_t)T);
+    if (T == 0 && (wmode != ORACLE_W_GEOMETRIC || !(beta >= 0.0) || !(beta < 1.0))) return 1;
+    double *wts = malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
     if (!wts) return 2;
-    if (wmode == ORACLE_W_GEOMETRIC) {
+    if (T == 0) {
+        wts[0] = 1.0 - beta;   /* w_0 of the untruncated walk; the hops go through the solve */
+    } else if (wmode == ORACLE_W_GEOMETRIC) {
         if (lisa_oracle_geometric_weights(beta, T, wts)) { free(wts); return 1; }
     } else if (wmode == ORACLE_W_FIXED) {
         if (!w) { free(wts); return 1; }
@@ -380,7 +500,7 @@ int lisa_oracle_forward(const double *Xq, const double *Xk, const double *V,
         free(wts);
         return 1;
     }
-    slice_args A = {H, W, dh, dv, T, wmode, hidden, mode, relu_inputs, eps,
+    slice_args A = {H, W, dh, dv, T, wmode, hidden, mode, relu_inputs, eps, beta,
                     wts, W1, b1, W2, b2};
     const long n = (long)H * W;
     const long slices = (long)B * heads;
@@ -390,8 +510,9 @@ int lisa_oracle_forward(const double *Xq, const double *Xk, const double *V,
 #endif
     for (long sl = 0; sl < slices; ++sl) {
         long hq = sl * n * dh, hv = sl * n * dv;
-        err |= forward_slice(&A, Xq + hq, Xk + hq, V + hv, alpha[sl % heads],
-                             O ? O + hv : NULL, G ? G + hv : NULL, L ? L + hv : NULL);
+        const int e = forward_slice(&A, Xq + hq, Xk + hq, V + hv, alpha[sl % heads],
+                                    O ? O + hv : NULL, G ? G + hv : NULL, L ? L + hv : NULL);
+        if (e && !err) err = e;
     }
     free(wts);
     return err;

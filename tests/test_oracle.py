@@ -210,6 +210,84 @@ def test_truncation_tail_norm(T):
     assert abs(np.abs(R).sum() - n * beta ** T) <= 1e-9 * n
 
 
+# -- untruncated walk (T = 0): (1-beta)(I - beta S)^-1 V, note section 2.3 -----------
+
+@pytest.mark.parametrize("beta", [0.0, 0.3, 0.5, 0.9])
+def test_untruncated_routes_agree_with_library_solve(beta):
+    """The oracle's two untruncated routes (dense n x n elimination, and the
+    d x d push-through solve) against LAPACK's solve of the n x n system."""
+    grid, d, n = (4, 5), 6, 20
+    xq, xk, v = _rand(2, 1, n, d), _rand(2, 1, n, d), _rand(2, 1, n, 7)
+    _, Ge, _ = oracle.forward(xq, xk, v, grid, 0, alpha=1.0, beta=beta, mode=oracle.EXPLICIT, branches=True)
+    _, Gl, _ = oracle.forward(xq, xk, v, grid, 0, alpha=1.0, beta=beta, mode=oracle.LOWRANK, branches=True)
+    for b in range(2):
+        S = oracle.transition(xq[b, 0], xk[b, 0], eps=1e-6)
+        want = (1 - beta) * np.linalg.solve(np.eye(n) - beta * S, v[b, 0])
+        np.testing.assert_allclose(Ge[b, 0], want, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(Gl[b, 0], want, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("beta", [0.25, 0.5, 0.8])
+def test_untruncated_is_limit_of_truncated_series(beta):
+    """The untruncated walk is the T -> infinity limit of the renormalised
+    truncated one (paper Eq. 4 with 1 - beta^T -> 1), reached through the
+    independently pinned power-series route; the gap falls like beta^T."""
+    grid, d, n = (6, 6), 8, 36
+    xq, xk, v = _rand(1, 2, n, d), _rand(1, 2, n, d), _rand(1, 2, n, d)
+    _, Ginf, _ = oracle.forward(xq, xk, v, grid, 0, alpha=1.0, beta=beta, branches=True)
+    gaps = []
+    for T in (2, 4, 8, 16):
+        _, G, _ = oracle.forward(xq, xk, v, grid, T, alpha=1.0, beta=beta, branches=True)
+        gaps.append(np.abs(G - Ginf).max())
+    assert all(b < a for a, b in zip(gaps, gaps[1:]))
+    _, Gfar, _ = oracle.forward(xq, xk, v, grid, 200, alpha=1.0, beta=beta, branches=True)
+    assert np.abs(Gfar - Ginf).max() < 1e-11
+
+
+@pytest.mark.parametrize("T", [1, 2, 4, 7])
+def test_untruncated_tail_norm_through_the_oracle(T):
+    """With eps = 0 (S exactly row-stochastic), V = I_n makes the global branch
+    the walk matrix itself: the untruncated P minus the unnormalised truncated
+    sum (1-beta) beta^k S^k, k < T, is the tail R_T with entrywise l1 norm
+    n beta^T (note section 2.5, paper Supp. Sec. 6)."""
+    beta, n, grid = 0.5, 12, (3, 4)
+    xq = np.abs(RNG.standard_normal((1, 1, n, 5))) + 0.1
+    xk = np.abs(RNG.standard_normal((1, 1, n, 5))) + 0.1
+    eye = np.eye(n)[None, None]
+    _, P, _ = oracle.forward(xq, xk, eye, grid, 0, alpha=1.0, beta=beta, eps=0.0, branches=True)
+    w = (1 - beta) * beta ** np.arange(T)
+    _, PT, _ = oracle.forward(xq, xk, eye, grid, T, alpha=1.0, w=w, eps=0.0, branches=True)
+    R = P[0, 0] - PT[0, 0]
+    assert (R >= -1e-14).all()
+    assert abs(np.abs(R).sum() - n * beta ** T) <= 1e-9 * n
+    np.testing.assert_allclose(P[0, 0].sum(axis=1), 1.0, rtol=0, atol=1e-12)   # P row-stochastic
+
+
+def test_untruncated_special_values():
+    """beta = 0 keeps only the self-loop (g = V); a constant value field is
+    preserved (P row-stochastic up to eps); a zero query row gets (1-beta) V_i."""
+    grid, n, d = (3, 5), 15, 6
+    xq, xk, v = _rand(1, 1, n, d), _rand(1, 1, n, d), _rand(1, 1, n, d)
+    _, G, _ = oracle.forward(xq, xk, v, grid, 0, alpha=1.0, beta=0.0, branches=True)
+    assert np.array_equal(G, v)
+    c = np.full((1, 1, n, d), -1.75)
+    for mode in (oracle.EXPLICIT, oracle.LOWRANK):
+        _, G, _ = oracle.forward(xq, xk, c, grid, 0, alpha=1.0, beta=0.7, eps=0.0, mode=mode, branches=True)
+        np.testing.assert_allclose(G, -1.75, rtol=1e-13)
+    xz = xq.copy()
+    xz[0, 0, 4] = -1.0     # ReLU'd to a zero query row: Q~_4 = 0
+    _, G, _ = oracle.forward(xz, xk, v, grid, 0, alpha=1.0, beta=0.6, branches=True)
+    np.testing.assert_allclose(G[0, 0, 4], 0.4 * v[0, 0, 4], rtol=1e-14)
+
+
+def test_untruncated_rejects_non_geometric_weights():
+    xq = _rand(1, 1, 4, 2)
+    with pytest.raises(ValueError):
+        oracle.forward(xq, xq, xq, (2, 2), 0, alpha=1.0, w=[1.0])
+    with pytest.raises(ValueError):
+        oracle.forward(xq, xq, xq, (2, 2), 0, alpha=1.0, beta=1.0)
+
+
 # -- local branch (note section 2.4) -------------------------------------------------
 
 def _box_mean(v, H, W):
