@@ -250,9 +250,10 @@ def reference_arm(args, shape):
 
 
 def config_of(shape, reference=False, sets=None):
-    cfg = {"workload": "%s: LiSA forward layer, B=%d heads=%d grid %dx%d (n=%d) d_h=d_v=%d T=%d %s "
+    depth = "T=%d" % shape.T if shape.T else "untruncated walk (T=0)"
+    cfg = {"workload": "%s: LiSA forward layer, B=%d heads=%d grid %dx%d (n=%d) d_h=d_v=%d %s %s "
                        "weights%s, alpha %s, eps=1e-6" %
-                       (shape.name, shape.B, shape.heads, shape.H, shape.W, shape.n, shape.d, shape.T,
+                       (shape.name, shape.B, shape.heads, shape.H, shape.W, shape.n, shape.d, depth,
                         shape.weights, " beta=%.2f" % shape.beta if shape.weights == "geometric" else "",
                         shape.alpha),
            "B": shape.B, "heads": shape.heads, "grid": [shape.H, shape.W], "n": shape.n,

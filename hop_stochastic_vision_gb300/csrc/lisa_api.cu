@@ -101,7 +101,7 @@ namespace {
 lisa_status check_sizes(int B, int heads, int H, int W, int d_h, int d_v, int T, int dtype) {
     if (B < 0 || heads < 0 || H < 0 || W < 0) return LISA_ERR_INVALID_ARG;
     if (dtype != LISA_F32 && dtype != LISA_BF16) return LISA_ERR_INVALID_ARG;
-    if (d_h < 1 || d_v < 1 || T < 1) return LISA_ERR_INVALID_ARG;
+    if (d_h < 1 || d_v < 1 || T < 0) return LISA_ERR_INVALID_ARG;   // T = 0: untruncated walk
     if (!supported_dim(d_h) || d_v != d_h) return LISA_ERR_UNSUPPORTED;
     if (T > LISA_MAX_T) return LISA_ERR_UNSUPPORTED;
     const long long slices = (long long)B * heads, n = (long long)H * W;
@@ -109,6 +109,10 @@ lisa_status check_sizes(int B, int heads, int H, int W, int d_h, int d_v, int T,
         return LISA_ERR_UNSUPPORTED;
     return LISA_OK;
 }
+
+// The untruncated walk (T = 0) runs the kernels of a T = 2 fixed-weight walk
+// whose single hop matrix comes from the d x d solve.
+int effective_T(int T) { return T == 0 ? 2 : T; }
 
 }  // namespace
 }  // namespace lisa
@@ -120,6 +124,7 @@ extern "C" size_t lisa_workspace_bytes(int B, int heads, int H, int W, int d_h, 
     if (check_sizes(B, heads, H, W, d_h, d_v, T, dtype) != LISA_OK) return 0;
     const long long slices = (long long)B * heads, n = (long long)H * W;
     if (slices == 0 || n == 0) return 0;
+    T = effective_T(T);
     // the weight mode is not known here: size for whichever needs more
     size_t need = make_plan((int)slices, (int)n, d_h, T, dtype, LISA_W_FIXED, 0).total;
     for (int hidden : {16, LISA_MAX_HIDDEN}) {
@@ -145,11 +150,23 @@ lisa_status prepare(Problem &p, bool &empty, const void *Q, const void *K, const
     if (relu_inputs != 0 && relu_inputs != 1) return LISA_ERR_INVALID_ARG;
 
     p = Problem{};
-    p.T = T;
+    p.T = effective_T(T);
+    if (T == 0 && wts->mode != LISA_W_GEOMETRIC) return LISA_ERR_INVALID_ARG;
     switch (wts->mode) {
         case LISA_W_GEOMETRIC: {
             const double beta = (double)wts->beta;
             if (!(beta >= 0.0 && beta < 1.0)) return LISA_ERR_INVALID_ARG;
+            if (T == 0) {
+                // untruncated: w_0 = 1 - beta on V; the hop terms sum to
+                // beta (1-beta) Q~ (I - beta M)^-1 U_1, so w_1 = beta (1-beta)
+                // scales the solved matrix
+                p.w[0] = (float)(1.0 - beta);
+                p.w[1] = (float)(beta * (1.0 - beta));
+                p.untruncated = 1;
+                p.beta = (float)beta;
+                p.wmode = LISA_W_FIXED;
+                break;
+            }
             // paper Eq. 4: (1-beta) beta^k renormalised over k < T, in double
             const double norm = 1.0 - std::pow(beta, (double)T);
             for (int k = 0; k < T; ++k)
@@ -190,7 +207,7 @@ lisa_status prepare(Problem &p, bool &empty, const void *Q, const void *K, const
     if (overlaps(O, bytes, Q, bytes) || overlaps(O, bytes, K, bytes) || overlaps(O, bytes, V, bytes))
         return LISA_ERR_INVALID_ARG;
 
-    const Plan pl = make_plan((int)slices, (int)n, d_h, T, dtype, p.wmode, p.hidden);
+    const Plan pl = make_plan((int)slices, (int)n, d_h, p.T, dtype, p.wmode, p.hidden);
     if (!workspace || workspace_bytes < pl.total) return LISA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return LISA_ERR_INVALID_ARG;
 
@@ -284,7 +301,7 @@ int stage_info(int B, int heads, int H, int W, int d_h, int T, int dtype, const 
     if (!wts || check_sizes(B, heads, H, W, d_h, d_h, T, dtype) != LISA_OK) return 0;
     const long long slices = (long long)B * heads, n = (long long)H * W;
     if (slices == 0 || n == 0) return 0;
-    const Plan pl = make_plan((int)slices, (int)n, d_h, T, dtype, weights_mode(wts), wts->hidden);
+    const Plan pl = make_plan((int)slices, (int)n, d_h, effective_T(T), dtype, weights_mode(wts), wts->hidden);
     if (pl.family == kFamilyTc) {
         if (name) *name = tc_stage_name(pl.chunks, pl.cluster, pl.chunk, stage);
         return tc_num_stages(pl.chunks, pl.cluster, pl.chunk);
@@ -386,8 +403,8 @@ extern "C" lisa_status lisa_forward_noalloc(const void *Q, const void *K, const 
     const long long slices = (long long)B * heads, n = (long long)H * W;
     const size_t need = (slices == 0 || n == 0 || !wts)
                             ? 0
-                            : make_plan((int)slices, (int)n, d_h, T, dtype, weights_mode(wts),
-                                        wts->hidden)
+                            : make_plan((int)slices, (int)n, d_h, effective_T(T), dtype,
+                                        weights_mode(wts), wts->hidden)
                                   .total;
     if (need > (size_t)LISA_NOALLOC_SCRATCH_BYTES) return LISA_ERR_WORKSPACE;
     void *scratch = nullptr;

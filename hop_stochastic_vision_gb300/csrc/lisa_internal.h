@@ -20,7 +20,9 @@ struct Problem {
     int heads;
     int H, W, n;       // grid and tokens per slice
     int D;             // d_h = d_v
-    int T;             // truncation depth
+    int T;             // truncation depth (2 for the untruncated walk: w_0 V + Q~ U-bar)
+    int untruncated;   // geometric walk without truncation: U-bar = beta (1-beta) (I - beta M)^-1 U_1
+    float beta;        // its continue probability
     int relu;          // apply ReLU to Q and K on load
     float eps;
     const float *alpha;  // device [heads]

@@ -20,6 +20,7 @@
 #include <cuda_runtime.h>
 
 #include "lisa_internal.h"
+#include "lisa_solve.cuh"
 
 namespace lisa {
 namespace {
@@ -177,6 +178,21 @@ __global__ void __launch_bounds__(kThreads) recur_kernel(Problem p) {
         p.s_red[(size_t)sl * D + tid] = acc;
     }
     __syncthreads();
+    if (p.untruncated) {
+        // U_1 <- (I - beta M)^-1 U_1: A = I - beta M stored transposed in Un, R = U_1
+        // transposed in M, the solve's scratch in U (free meanwhile)
+        for (int idx = tid; idx < D * D; idx += kThreads) {
+            const int a = idx / D, b = idx % D;
+            Un[b][a] = (a == b ? 1.f : 0.f) - p.beta * M[a][b];
+        }
+        __syncthreads();
+        for (int idx = tid; idx < D * D; idx += kThreads) M[idx % D][idx / D] = U[idx / D][idx % D];
+        __syncthreads();
+        solve_walk_system<kThreads / 32, (2 * D + kThreads / 32 - 1) / (kThreads / 32)>(&Un[0][0], D, &M[0][0], D, D, D,
+                                                                                  &U[0][0], tid);
+        for (int idx = tid; idx < D * D; idx += kThreads) U[idx / D][idx % D] = M[idx % D][idx / D];
+        __syncthreads();
+    }
     const bool folded = (p.wmode != LISA_W_MLP);
     float *out = p.ucat + (size_t)sl * (folded ? 1 : (p.T - 1 > 0 ? p.T - 1 : 1)) * D * D;
     // acc holds sum_k w_k U_k for the entries this thread owns (FIXED mode)

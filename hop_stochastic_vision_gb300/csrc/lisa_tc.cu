@@ -44,6 +44,7 @@
 
 #include "lisa_internal.h"
 #include "lisa_sm100.cuh"
+#include "lisa_solve.cuh"
 
 namespace lisa {
 namespace {
@@ -65,7 +66,8 @@ constexpr int kErrTimeoutMma = 2;
 
 struct TcParams {
     int slices, heads, H, W, n, T, relu, wmode, hidden;
-    float eps;
+    int untruncated;                 // U-bar = beta (1-beta) (I - beta M)^-1 U_1 instead of the series
+    float eps, beta;
     const float *alpha;
     float w[LISA_MAX_T];
     const float *W1, *b1, *W2, *b2;
@@ -358,6 +360,7 @@ __device__ __forceinline__ bool named_sync_and(bool v) {
 // the TMA loads and refills each ring stage as soon as its MMA completed.
 constexpr int kStatsThreads = 160;
 
+template <bool kUntruncated>
 __global__ void __launch_bounds__(kStatsThreads) tc_stats_fused_kernel(const __grid_constant__ CUtensorMap mQ,
                                                                        const __grid_constant__ CUtensorMap mK,
                                                                        const __grid_constant__ CUtensorMap mV,
@@ -555,6 +558,20 @@ __global__ void __launch_bounds__(kStatsThreads) tc_stats_fused_kernel(const __g
         }
     }
     cluster_sync();                                                // (C) M^T complete everywhere
+    if (kUntruncated) {
+        // own rows of U_1^T become those of ((I - beta M)^-1 U_1)^T: A = I - beta M
+        // in place of M^T (element (a, b) at Mt[b][a]), the own U_1 columns as R
+        for (int idx = tid; idx < 64 * 64; idx += kStatsThreads) {
+            const int b = idx >> 6, a = idx & 63;
+            Mt[b * kMS + a] = (a == b ? 1.f : 0.f) - p.beta * Mt[b * kMS + a];
+        }
+        __syncthreads();
+        constexpr int kW = kStatsThreads / 32;
+        if (my_u <= 16)   // clusters of 4 or more CTAs: at most 80 columns
+            solve_walk_system<kW, (80 + kW - 1) / kW>(Mt, kMS, Ucur, kUS, 64, my_u, &s_red[0][0], tid);
+        else
+            solve_walk_system<kW, (128 + kW - 1) / kW>(Mt, kMS, Ucur, kUS, 64, my_u, &s_red[0][0], tid);
+    }
 
     // ---- U_k^T = U_(k-1)^T M^T on the own rows; B operand rows
     float *Unext = reinterpret_cast<float *>(sm);                  // [my_u][kUS]
@@ -767,6 +784,7 @@ __global__ void __launch_bounds__(256) tc_recur_kernel(TcParams p) {
     __shared__ __align__(16) float Un[16][kD];
     __shared__ __align__(16) float Fold[16][kD];
     __shared__ float s_sh[kD];
+    __shared__ float fac[3 * kD];                  // solve scratch (untruncated walk)
     const int tid = threadIdx.x;
     const int sl = blockIdx.x / kRecurRowBlocks, rb = blockIdx.x % kRecurRowBlocks;
     pdl_launch_dependents();
@@ -804,6 +822,14 @@ __global__ void __launch_bounds__(256) tc_recur_kernel(TcParams p) {
         s_sh[tid] = s;
     }
     __syncthreads();
+    if (p.untruncated) {   // own rows of U_1^T -> those of ((I - beta M)^-1 U_1)^T
+        for (int idx = tid; idx < kD * kD; idx += 256) {
+            const int b = idx >> 6, a = idx & 63;
+            Mt[b][a] = (a == b ? 1.f : 0.f) - p.beta * Mt[b][a];
+        }
+        __syncthreads();
+        solve_walk_system<8, 10>(&Mt[0][0], kD, &Ut[0][0], kD, kD, 16, fac, tid);
+    }
     const bool folded = (p.wmode != LISA_W_MLP);
     uint8_t *img = p.bepi + (size_t)sl * p.epi_rows * kRow;
     for (int k = 1; k < p.T; ++k) {
@@ -1536,6 +1562,7 @@ cudaError_t launch_tc(const Problem &p, cudaStream_t st, int stage) {
     TcParams t{};
     t.slices = p.slices; t.heads = p.heads; t.H = p.H; t.W = p.W; t.n = p.n; t.T = p.T;
     t.relu = p.relu; t.wmode = p.wmode; t.hidden = p.hidden; t.eps = p.eps; t.alpha = p.alpha;
+    t.untruncated = p.untruncated; t.beta = p.beta;
     for (int k = 0; k < LISA_MAX_T; ++k) t.w[k] = p.w[k];
     t.W1 = p.W1; t.b1 = p.b1; t.W2 = p.W2; t.b2 = p.b2; t.K = p.K;
     t.chunks = p.chunks; t.chunk = p.chunk; t.cl = p.tc_cluster; t.parts = p.chunks / p.tc_cluster;
@@ -1587,13 +1614,14 @@ cudaError_t launch_tc(const Problem &p, cudaStream_t st, int stage) {
             const int ring = kStages * 2 * kSubBytes;
             if (kres + ring < kFusedWork) kres = kFusedWork - ring;
             const int smem = kres + ring + 1024;
-            if ((err = set_smem(tc_stats_fused_kernel, 0, smem)) != cudaSuccess) return err;
+            // the untruncated walk has its own instance (the solve's call costs registers)
+            auto kern = p.untruncated ? tc_stats_fused_kernel<true> : tc_stats_fused_kernel<false>;
+            if ((err = set_smem(kern, p.untruncated ? 4 : 0, smem)) != cudaSuccess) return err;
             cfg.dynamicSmemBytes = smem;
             cfg.blockDim = dim3(kStatsThreads);
             cfg.attrs = attrs;        // first kernel of the fused chain: waits after its set-up
             cfg.numAttrs = 2;
-            if ((err = cudaLaunchKernelEx(&cfg, tc_stats_fused_kernel, mq, mk, mv, t, kres)) != cudaSuccess)
-                return err;
+            if ((err = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, t, kres)) != cudaSuccess) return err;
         } else {
             const int smem = kStages * 3 * kSubBytes + 1024;
             if ((err = set_smem(tc_stats_split_kernel, 1, smem)) != cudaSuccess) return err;

@@ -13,6 +13,9 @@
  *                                                   [note §2.3; paper Eq. 8]
  *   walk weights     geometric w_k = (1-beta) beta^k / (1-beta^T)
  *                                                   [note §2.2; paper Eq. 4]
+ *                    or, untruncated (T = 0), (1-beta) beta^k for every
+ *                    k >= 0: g = (1-beta) (I - beta S)^-1 V  [note §2.3, the
+ *                    closing remark on the geometric series]
  *                    or per token and head: softmax(W2 GELU(W1 [q_i;k_i] + b1) + b2)
  *                                          [note §2.4; paper Eq. 10, Supp. 8]
  *   local branch     softmax over the token and its in-grid 8-neighbours of
@@ -83,6 +86,7 @@ typedef struct lisa_weights {
  * would reject.  The workspace holds the split-K partial sums of sum_j K_j,
  * K^T V and K^T Q~ [note §2.3], the reduced statistics and U_1..U_(T-1);
  * lisa_forward overwrites all of it, so it needs no initialisation.
+ * T = 0 (the untruncated walk) is accepted and sized like T = 2.
  */
 size_t lisa_workspace_bytes(int B, int heads, int H, int W, int d_h, int d_v, int T,
                             int dtype);
@@ -94,7 +98,15 @@ size_t lisa_workspace_bytes(int B, int heads, int H, int W, int d_h, int d_v, in
  *               feature-mapped (non-negative) when relu_inputs = 0.
  *   V           device [B][heads][H*W][d_v], dtype.
  *   O           device [B][heads][H*W][d_v], dtype; written.
- *   T           truncation depth, 1..LISA_MAX_T (1..LISA_MAX_T_MLP for MLP).
+ *   T           truncation depth, 1..LISA_MAX_T (1..LISA_MAX_T_MLP for MLP);
+ *               0 with LISA_W_GEOMETRIC: the untruncated walk,
+ *               g = (1-beta) (I - beta S)^-1 V.  The library evaluates it as
+ *               g = (1-beta) (V + beta Q~ X) with (I - beta M) X = U_1,
+ *               M = K^T Q~ (the push-through identity; a d x d solve per
+ *               slice).  That system is well posed because the features
+ *               are non-negative (relu_inputs = 1, or inputs that already
+ *               are): I - beta M is then a nonsingular M-matrix.  T = 0 with
+ *               LISA_W_FIXED or LISA_W_MLP is LISA_ERR_INVALID_ARG.
  *   wts         host struct; see lisa_weights.
  *   alpha       device fp32 [heads]: branch mix per head, used as given.
  *   eps         stabiliser of the row normaliser, > 0 (the paper's setting: 1e-6).

@@ -30,7 +30,7 @@ class LayerShape:
     H: int
     W: int
     d: int                # d_h = d_v
-    T: int
+    T: int                # walk truncation depth; 0 = untruncated (geometric weights only)
     weights: str          # "geometric" or "mlp"
     beta: float = 0.5
     alpha: str = "0.5"    # "0.5" or "uniform(0.3,0.7)" (one value per head)
@@ -53,6 +53,9 @@ SHAPES = {
     "deit_t384_24x24_mlp": LayerShape("deit_t384_24x24_mlp", "bf16", 64, 3, 24, 24, 64, 3, "mlp"),
     "pvt_t_s1_56x56_T3": LayerShape("pvt_t_s1_56x56_T3", "bf16", 32, 1, 56, 56, 64, 3, "geometric"),
     "pvt_t_s1_56x56_T5": LayerShape("pvt_t_s1_56x56_T5", "bf16", 32, 1, 56, 56, 64, 5, "geometric"),
+    # the same layer with the untruncated geometric walk (T = 0)
+    "pvt_t_s1_56x56_untruncated": LayerShape("pvt_t_s1_56x56_untruncated", "bf16", 32, 1, 56, 56, 64, 0,
+                                             "geometric"),
 }
 for _g in (64, 128, 256):
     for _T in (3, 5):

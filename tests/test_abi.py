@@ -55,7 +55,9 @@ def test_workspace_bytes():
     assert ws(0, 1, 56, 56, 64, 64, 3, lisa.LISA_BF16) == 0          # empty problem
     assert ws(1, 1, 4, 4, 48, 48, 3, lisa.LISA_BF16) == 0            # unsupported d
     assert ws(1, 1, 4, 4, 64, 32, 3, lisa.LISA_BF16) == 0            # d_v != d_h
-    assert ws(1, 1, 4, 4, 64, 64, 0, lisa.LISA_BF16) == 0            # T < 1
+    assert ws(1, 1, 4, 4, 64, 64, -1, lisa.LISA_BF16) == 0           # T < 0
+    assert ws(1, 1, 4, 4, 64, 64, 0, lisa.LISA_BF16) > 0             # T = 0: untruncated walk
+    assert ws(1, 1, 4, 4, 16, 16, 0, lisa.LISA_F32) == ws(1, 1, 4, 4, 16, 16, 2, lisa.LISA_F32)
     assert ws(1, 1, 4, 4, 64, 64, 3, 7) == 0                         # bad dtype
     assert ws(-1, 1, 4, 4, 64, 64, 3, lisa.LISA_F32) == 0
     assert ws(1, 1, 4, 4, 16, 16, 16, lisa.LISA_F32) > 0
@@ -89,7 +91,9 @@ def _call(**over):
     (dict(O=FAKE + 4096), lisa.LISA_ERR_INVALID_ARG),               # O overlaps K
     (dict(B=-1), lisa.LISA_ERR_INVALID_ARG),
     (dict(H=-2), lisa.LISA_ERR_INVALID_ARG),
-    (dict(T=0), lisa.LISA_ERR_INVALID_ARG),
+    (dict(T=-1), lisa.LISA_ERR_INVALID_ARG),
+    (dict(T=0, beta=1.0), lisa.LISA_ERR_INVALID_ARG),              # untruncated needs beta < 1
+    (dict(T=0, wbytes=16), lisa.LISA_ERR_WORKSPACE),
     (dict(T=17), lisa.LISA_ERR_UNSUPPORTED),
     (dict(d_h=48, d_v=48), lisa.LISA_ERR_UNSUPPORTED),
     (dict(d_h=128, d_v=128), lisa.LISA_ERR_UNSUPPORTED),
@@ -131,6 +135,11 @@ def test_weight_struct_checks():
     assert _call(wt=wt) == lisa.LISA_ERR_UNSUPPORTED
     wt.hidden = 32
     assert _call(wt=wt, T=9) == lisa.LISA_ERR_UNSUPPORTED
+    assert _call(wt=wt, T=0) == lisa.LISA_ERR_INVALID_ARG      # untruncated walk: geometric only
+    wt = lisa.lisa_weights()
+    wt.mode = lisa.LISA_W_FIXED
+    wt.w = ctypes.cast(arr, ctypes.POINTER(ctypes.c_float))
+    assert _call(wt=wt, T=0) == lisa.LISA_ERR_INVALID_ARG
     # a null weight struct
     lib = lisa.load()
     rc = lib.lisa_forward(FAKE, FAKE, FAKE, FAKE, 1, 1, 4, 4, 16, 16, 3, None, FAKE, 1e-6, 1, 0,
