@@ -67,6 +67,9 @@ def _load():
         lib.lisa_oracle_transition.restype = i
         lib.lisa_oracle_step_weights.argtypes = [dp, dp, i, i, i, dp, dp, dp, dp, i, i, dp]
         lib.lisa_oracle_step_weights.restype = i
+        lib.lisa_oracle_backward.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, i, i, i, i, i, i, i, i, d,
+                                             dp, dp, d, i]
+        lib.lisa_oracle_backward.restype = i
         lib.lisa_oracle_max_threads.argtypes = []
         lib.lisa_oracle_max_threads.restype = i
         _lib = lib
@@ -146,6 +149,36 @@ def forward(xq, xk, v, grid, T, *, alpha, beta=None, w=None, mlp=None, eps=1e-6,
     if rc != 0:
         raise ValueError("lisa_oracle_forward failed with code %d" % rc)
     return (O, G, L) if branches else O
+
+
+def backward(xq, xk, v, dO, grid, T, *, alpha, beta=None, w=None, eps=1e-6, relu=True):
+    """Gradients of the LiSA forward (fixed or geometric walk weights; T = 0
+    with ``beta`` is the untruncated walk) for the upstream gradient ``dO``:
+    returns (dXq, dXk, dV, dalpha), dalpha summed over the batch per head."""
+    xq, xk, v, dO = _f64(xq), _f64(xk), _f64(v), _f64(dO)
+    B, heads, n, dh = xq.shape
+    dv = v.shape[3]
+    H, W = grid
+    if H * W != n or dO.shape != v.shape or xk.shape != xq.shape:
+        raise ValueError("bad shapes")
+    alpha = np.broadcast_to(np.asarray(alpha, dtype=np.float64), (heads,)).copy()
+    if w is not None:
+        wmode, wv = W_FIXED, _f64(w)
+        if T == 0 or wv.shape != (T,):
+            raise ValueError("fixed weights need length T >= 1")
+    elif beta is not None:
+        wmode, wv = W_GEOMETRIC, None
+    else:
+        raise ValueError("give beta or w")
+    dXq, dXk, dV = np.empty_like(xq), np.empty_like(xk), np.empty_like(v)
+    da = np.empty(heads)
+    rc = _load().lisa_oracle_backward(
+        _ptr(xq), _ptr(xk), _ptr(v), _ptr(dO), _ptr(dXq), _ptr(dXk), _ptr(dV), _ptr(da), B, heads, H, W,
+        dh, dv, int(T), wmode, float(beta if beta is not None else 0.0), _ptr(wv), _ptr(alpha), float(eps),
+        int(bool(relu)))
+    if rc != 0:
+        raise ValueError("lisa_oracle_backward failed with code %d" % rc)
+    return dXq, dXk, dV, da
 
 
 def transition(xq, xk, eps=1e-6, relu=True):

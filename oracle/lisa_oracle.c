@@ -518,6 +518,293 @@ int lisa_oracle_forward(const double *Xq, const double *Xk, const double *V,
     return err;
 }
 
+/* ---------------------------------------------------------------------- */
+/* Backward pass of one slice with fixed walk weights (geometric resolved   */
+/* to fixed), by the chain rule through the forward above, in the order of  */
+/* the forward's steps taken backwards.  Given dO = dL/dO:                  */
+/*   o = alpha g + (1-alpha) l:  dalpha = sum_i dO_i . (g_i - l_i),         */
+/*                               dg = alpha dO,  dl = (1-alpha) dO          */
+/*   g_i = w_0 V_i + Q~_i Ubar, Ubar = sum_{k>=1} w_k U_k:                  */
+/*        dV += w_0 dg,  dQ~ = dg Ubar^T,  dUbar = Q~^T dg                  */
+/*   U_k = M U_(k-1):  G_(T-1) = w_(T-1) dUbar, G_k = w_k dUbar + M^T G_(k+1)*/
+/*        (G_k = dL/dU_k),  dM = sum_{k>=2} G_k U_(k-1)^T,  dU_1 = G_1      */
+/*   U_1 = K^T V:  dK_j += dU_1 V_j,  dV_j += dU_1^T K_j                    */
+/*   M = K^T Q~:   dK_j += dM Q~_j,   dQ~_j += dM^T K_j                     */
+/*   Q~_i = Q_i / r_i, r_i = Q_i . s + eps:  c_i = (dQ~_i . Q~_i) / r_i,    */
+/*        dQ_i += dQ~_i / r_i - c_i s,  ds = -sum_i c_i Q_i                 */
+/*   s = sum_j K_j:  dK_j += ds                                             */
+/*   local, e_ij = q_i . k_j / sqrt(dh), a = softmax_j, l_i = sum a_ij V_j: */
+/*        dV_j += a_ij dl_i,  de_ij = a_ij (dl_i . V_j - dl_i . l_i),       */
+/*        dQ_i += sum_j de_ij K_j / sqrt(dh), dK_j += de_ij Q_i / sqrt(dh)  */
+/*   feature map: dXq = dQ [Xq > 0], dXk = dK [Xk > 0] (relu set).          */
+/* Untruncated walk (T = 0): Ubar = beta (1-beta) Z, (I - beta M) Z = U_1,  */
+/*   so with A = I - beta M and dZ = beta (1-beta) dUbar:                   */
+/*   dU_1 = A^-T dZ,  dM = beta (A^-T dZ) Z^T, and w_0 = 1 - beta.           */
+/* ---------------------------------------------------------------------- */
+static int backward_slice(const slice_args *A, const double *Xq, const double *Xk,
+                          const double *V, const double *dO, double alpha,
+                          double *dXq, double *dXk, double *dV, double *dalpha)
+{
+    const int H = A->H, W = A->W, n = H * W, dh = A->dh, dv = A->dv;
+    const int T = A->T, nh = T == 0 ? 1 : (T > 1 ? T - 1 : 1);   /* stored U_k */
+    const size_t nd = (size_t)n * dh, nv = (size_t)n * dv;
+    double *Q = malloc(sizeof(double) * nd), *K = malloc(sizeof(double) * nd);
+    double *Qt = malloc(sizeof(double) * nd), *r = malloc(sizeof(double) * n);
+    double *M = malloc(sizeof(double) * dh * dh), *Uk = malloc(sizeof(double) * nh * dh * dv);
+    double *Ub = malloc(sizeof(double) * dh * dv), *dUb = malloc(sizeof(double) * dh * dv);
+    double *G = malloc(sizeof(double) * nh * dh * dv), *dM = malloc(sizeof(double) * dh * dh);
+    double *dU1 = malloc(sizeof(double) * dh * dv), *Amat = malloc(sizeof(double) * dh * dh);
+    double *g = malloc(sizeof(double) * nv), *l = malloc(sizeof(double) * nv);
+    double *dQt = malloc(sizeof(double) * nd), *dQ = malloc(sizeof(double) * nd);
+    double *dK = malloc(sizeof(double) * nd);
+    double s[256], ds[256];
+    const double scale = 1.0 / sqrt((double)dh);
+    int err = 0;
+    if (!Q || !K || !Qt || !r || !M || !Uk || !Ub || !dUb || !G || !dM || !dU1 || !Amat || !g || !l ||
+        !dQt || !dQ || !dK) {
+        err = 2;
+        goto done;
+    }
+    /* ---- forward quantities */
+    feature_map(Xq, Q, (long)nd, A->relu);
+    feature_map(Xk, K, (long)nd, A->relu);
+    key_sum(K, n, dh, s);
+    for (int i = 0; i < n; ++i) {
+        double den = A->eps;
+        for (int a = 0; a < dh; ++a) den += Q[(long)i * dh + a] * s[a];
+        r[i] = den;
+        for (int a = 0; a < dh; ++a) Qt[(long)i * dh + a] = Q[(long)i * dh + a] / den;
+    }
+    for (int a = 0; a < dh; ++a)
+        for (int b = 0; b < dh; ++b) {
+            double acc = 0.0;
+            for (int j = 0; j < n; ++j) acc += K[(long)j * dh + a] * Qt[(long)j * dh + b];
+            M[a * dh + b] = acc;
+        }
+    for (int a = 0; a < dh; ++a)   /* U_1 into Uk[0] */
+        for (int e = 0; e < dv; ++e) {
+            double acc = 0.0;
+            for (int j = 0; j < n; ++j) acc += K[(long)j * dh + a] * V[(long)j * dv + e];
+            Uk[a * dv + e] = acc;
+        }
+    const double w0 = T == 0 ? 1.0 - A->beta : A->w[0];
+    memset(Ub, 0, sizeof(double) * dh * dv);
+    if (T == 0) {
+        /* Z = (I - beta M)^-1 U_1 into Uk[0]; Ubar = beta (1-beta) Z */
+        for (int a = 0; a < dh; ++a)
+            for (int b = 0; b < dh; ++b) Amat[a * dh + b] = (a == b ? 1.0 : 0.0) - A->beta * M[a * dh + b];
+        if ((err = solve_dense(Amat, Uk, dh, dv))) goto done;
+        for (int t = 0; t < dh * dv; ++t) Ub[t] = A->beta * (1.0 - A->beta) * Uk[t];
+    } else {
+        for (int k = 1; k < T; ++k) {
+            double *cur = Uk + (size_t)(k - 1) * dh * dv;
+            if (k > 1) {
+                const double *prev = Uk + (size_t)(k - 2) * dh * dv;
+                for (int a = 0; a < dh; ++a)
+                    for (int e = 0; e < dv; ++e) {
+                        double acc = 0.0;
+                        for (int b = 0; b < dh; ++b) acc += M[a * dh + b] * prev[b * dv + e];
+                        cur[a * dv + e] = acc;
+                    }
+            }
+            for (int t = 0; t < dh * dv; ++t) Ub[t] += A->w[k] * cur[t];
+        }
+    }
+    for (int i = 0; i < n; ++i)
+        for (int e = 0; e < dv; ++e) {
+            double acc = w0 * V[(long)i * dv + e];
+            for (int a = 0; a < dh; ++a) acc += Qt[(long)i * dh + a] * Ub[a * dv + e];
+            g[(long)i * dv + e] = acc;
+        }
+    local_branch(Q, K, V, H, W, dh, dv, l);
+
+    /* ---- mix */
+    double da = 0.0;
+    for (size_t t = 0; t < nv; ++t) da += dO[t] * (g[t] - l[t]);
+    *dalpha += da;
+    /* dg = alpha dO, dl = (1-alpha) dO are formed where they are used */
+
+    /* ---- global branch */
+    for (size_t t = 0; t < nv; ++t) dV[t] = w0 * alpha * dO[t];
+    for (int i = 0; i < n; ++i)   /* dQ~ = dg Ubar^T */
+        for (int a = 0; a < dh; ++a) {
+            double acc = 0.0;
+            for (int e = 0; e < dv; ++e) acc += alpha * dO[(long)i * dv + e] * Ub[a * dv + e];
+            dQt[(long)i * dh + a] = acc;
+        }
+    for (int a = 0; a < dh; ++a)   /* dUbar = Q~^T dg */
+        for (int e = 0; e < dv; ++e) {
+            double acc = 0.0;
+            for (int i = 0; i < n; ++i) acc += Qt[(long)i * dh + a] * alpha * dO[(long)i * dv + e];
+            dUb[a * dv + e] = acc;
+        }
+    memset(dM, 0, sizeof(double) * dh * dh);
+    memset(dU1, 0, sizeof(double) * dh * dv);
+    if (T == 0) {
+        /* Y = A^-T dZ with dZ = beta (1-beta) dUbar: solve A^T Y = dZ */
+        for (int a = 0; a < dh; ++a)
+            for (int b = 0; b < dh; ++b) Amat[a * dh + b] = (a == b ? 1.0 : 0.0) - A->beta * M[b * dh + a];
+        for (int t = 0; t < dh * dv; ++t) dU1[t] = A->beta * (1.0 - A->beta) * dUb[t];
+        if ((err = solve_dense(Amat, dU1, dh, dv))) goto done;
+        for (int a = 0; a < dh; ++a)   /* dM = beta Y Z^T */
+            for (int b = 0; b < dh; ++b) {
+                double acc = 0.0;
+                for (int e = 0; e < dv; ++e) acc += dU1[a * dv + e] * Uk[b * dv + e];
+                dM[a * dh + b] = A->beta * acc;
+            }
+    } else if (T > 1) {
+        /* G_k for k = T-1 down to 1, stored at G[k-1] */
+        for (int k = T - 1; k >= 1; --k) {
+            double *Gk = G + (size_t)(k - 1) * dh * dv;
+            for (int t = 0; t < dh * dv; ++t) Gk[t] = A->w[k] * dUb[t];
+            if (k < T - 1) {
+                const double *Gn = G + (size_t)k * dh * dv;
+                for (int a = 0; a < dh; ++a)
+                    for (int e = 0; e < dv; ++e) {
+                        double acc = 0.0;
+                        for (int b = 0; b < dh; ++b) acc += M[b * dh + a] * Gn[b * dv + e];
+                        Gk[a * dv + e] += acc;
+                    }
+            }
+        }
+        for (int k = 2; k < T; ++k) {   /* dM += G_k U_(k-1)^T */
+            const double *Gk = G + (size_t)(k - 1) * dh * dv, *Up = Uk + (size_t)(k - 2) * dh * dv;
+            for (int a = 0; a < dh; ++a)
+                for (int b = 0; b < dh; ++b) {
+                    double acc = 0.0;
+                    for (int e = 0; e < dv; ++e) acc += Gk[a * dv + e] * Up[b * dv + e];
+                    dM[a * dh + b] += acc;
+                }
+        }
+        memcpy(dU1, G, sizeof(double) * dh * dv);
+    }
+    for (int j = 0; j < n; ++j) {
+        for (int a = 0; a < dh; ++a) {
+            double acc = 0.0;   /* dU_1 V_j + dM Q~_j */
+            for (int e = 0; e < dv; ++e) acc += dU1[a * dv + e] * V[(long)j * dv + e];
+            for (int b = 0; b < dh; ++b) acc += dM[a * dh + b] * Qt[(long)j * dh + b];
+            dK[(long)j * dh + a] = acc;
+        }
+        for (int e = 0; e < dv; ++e) {
+            double acc = 0.0;   /* dU_1^T K_j */
+            for (int a = 0; a < dh; ++a) acc += dU1[a * dv + e] * K[(long)j * dh + a];
+            dV[(long)j * dv + e] += acc;
+        }
+        for (int b = 0; b < dh; ++b) {
+            double acc = 0.0;   /* dM^T K_j */
+            for (int a = 0; a < dh; ++a) acc += dM[a * dh + b] * K[(long)j * dh + a];
+            dQt[(long)j * dh + b] += acc;
+        }
+    }
+    for (int a = 0; a < dh; ++a) ds[a] = 0.0;
+    for (int i = 0; i < n; ++i) {
+        double c = 0.0;
+        for (int a = 0; a < dh; ++a) c += dQt[(long)i * dh + a] * Qt[(long)i * dh + a];
+        c /= r[i];
+        for (int a = 0; a < dh; ++a) {
+            dQ[(long)i * dh + a] = dQt[(long)i * dh + a] / r[i] - c * s[a];
+            ds[a] -= c * Q[(long)i * dh + a];
+        }
+    }
+    for (int j = 0; j < n; ++j)
+        for (int a = 0; a < dh; ++a) dK[(long)j * dh + a] += ds[a];
+
+    /* ---- local branch */
+    for (int rr = 0; rr < H; ++rr)
+        for (int cc = 0; cc < W; ++cc) {
+            const int i = rr * W + cc;
+            int nb[9], cnt = 0;
+            double e[9];
+            for (int dr = -1; dr <= 1; ++dr)
+                for (int dc = -1; dc <= 1; ++dc) {
+                    const int r2 = rr + dr, c2 = cc + dc;
+                    if (r2 < 0 || r2 >= H || c2 < 0 || c2 >= W) continue;
+                    nb[cnt++] = r2 * W + c2;
+                }
+            double emax = -INFINITY, den = 0.0;
+            for (int t = 0; t < cnt; ++t) {
+                double acc = 0.0;
+                for (int a = 0; a < dh; ++a) acc += Q[(long)i * dh + a] * K[(long)nb[t] * dh + a];
+                e[t] = acc * scale;
+                if (e[t] > emax) emax = e[t];
+            }
+            for (int t = 0; t < cnt; ++t) {
+                e[t] = exp(e[t] - emax);
+                den += e[t];
+            }
+            double dll = 0.0;   /* dl_i . l_i */
+            for (int x = 0; x < dv; ++x) dll += (1.0 - alpha) * dO[(long)i * dv + x] * l[(long)i * dv + x];
+            for (int t = 0; t < cnt; ++t) {
+                const double a_ij = e[t] / den;
+                const int j = nb[t];
+                double dlv = 0.0;   /* dl_i . V_j */
+                for (int x = 0; x < dv; ++x) {
+                    const double dl = (1.0 - alpha) * dO[(long)i * dv + x];
+                    dlv += dl * V[(long)j * dv + x];
+                    dV[(long)j * dv + x] += a_ij * dl;
+                }
+                const double de = a_ij * (dlv - dll) * scale;
+                for (int a = 0; a < dh; ++a) {
+                    dQ[(long)i * dh + a] += de * K[(long)j * dh + a];
+                    dK[(long)j * dh + a] += de * Q[(long)i * dh + a];
+                }
+            }
+        }
+
+    /* ---- feature map */
+    for (size_t t = 0; t < nd; ++t) {
+        dXq[t] = (A->relu && !(Xq[t] > 0.0)) ? 0.0 : dQ[t];
+        dXk[t] = (A->relu && !(Xk[t] > 0.0)) ? 0.0 : dK[t];
+    }
+done:
+    free(Q); free(K); free(Qt); free(r); free(M); free(Uk); free(Ub); free(dUb); free(G);
+    free(dM); free(dU1); free(Amat); free(g); free(l); free(dQt); free(dQ); free(dK);
+    return err;
+}
+
+/*
+ * Backward pass of the layer over B x heads slices: dL/dXq, dL/dXk, dL/dV
+ * ([B][heads][n][d], overwritten) and dL/dalpha ([heads], overwritten: the
+ * sum over the batch) for the upstream gradient dO.  Walk weights as for
+ * lisa_oracle_forward, geometric (T >= 1, or T = 0 untruncated) or fixed;
+ * the adaptive (MLP) weights are not covered (returns 1).
+ */
+int lisa_oracle_backward(const double *Xq, const double *Xk, const double *V,
+                         const double *dO, double *dXq, double *dXk, double *dV,
+                         double *dalpha, int B, int heads, int H, int W, int dh, int dv,
+                         int T, int wmode, double beta, const double *w,
+                         const double *alpha, double eps, int relu_inputs)
+{
+    if (B < 0 || heads < 1 || H < 1 || W < 1 || dh < 1 || dh > 256 || dv < 1 || T < 0 ||
+        T > ORACLE_MAX_T || eps < 0.0 || !alpha)
+        return 1;
+    if (wmode == ORACLE_W_MLP || (T == 0 && wmode != ORACLE_W_GEOMETRIC)) return 1;
+    double *wts = malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+    if (!wts) return 2;
+    if (T == 0) {
+        if (!(beta >= 0.0 && beta < 1.0)) { free(wts); return 1; }
+        wts[0] = 1.0 - beta;
+    } else if (wmode == ORACLE_W_GEOMETRIC) {
+        if (lisa_oracle_geometric_weights(beta, T, wts)) { free(wts); return 1; }
+    } else {
+        if (!w) { free(wts); return 1; }
+        memcpy(wts, w, sizeof(double) * (size_t)T);
+    }
+    slice_args A = {H, W, dh, dv, T, wmode, 0, ORACLE_LOWRANK, relu_inputs, eps, beta,
+                    wts, NULL, NULL, NULL, NULL};
+    const long n = (long)H * W;
+    for (int h = 0; h < heads; ++h) dalpha[h] = 0.0;
+    int err = 0;
+    for (long sl = 0; sl < (long)B * heads; ++sl) {
+        const long hq = sl * n * dh, hv = sl * n * dv;
+        const int e = backward_slice(&A, Xq + hq, Xk + hq, V + hv, dO + hv, alpha[sl % heads],
+                                     dXq + hq, dXk + hq, dV + hv, dalpha + sl % heads);
+        if (e && !err) err = e;
+    }
+    free(wts);
+    return err;
+}
+
 /*
  * Dense transition matrix of one slice, S_ij = Q~_i . K_j  [note §2.2], for
  * small n only (n x n doubles).  Used by the tests that check that S is

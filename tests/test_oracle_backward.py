@@ -1,0 +1,145 @@
+"""Pins of the oracle's backward pass (dL/dXq, dL/dXk, dL/dV, dL/dalpha).
+
+The oracle's backward is the chain rule written out by hand through the
+forward's steps.  It is checked against routes that share nothing with that
+derivation: central finite differences of the (separately pinned) forward,
+and torch autograd through a dense n x n restatement of the layer (S formed,
+walk powers S^k V, the 3x3 window as a masked softmax).  Plus closed forms:
+T = 1 with alpha = 1 makes the layer the identity on V, and the gradient is
+linear in the upstream gradient.
+
+Source: "LiSA: Linear Stochastic Attention for Long-Range Visual Modeling"
+(reading note of arXiv 2611.04216v2), sections 2.1-2.5.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+RNG = np.random.default_rng(4321)
+
+
+def _case(B, heads, H, W, d, scale=1.0):
+    n = H * W
+    return [scale * RNG.standard_normal((B, heads, n, d)) for _ in range(4)]
+
+
+def _loss(xq, xk, v, dO, grid, T, alpha, **kw):
+    return float((oracle.forward(xq, xk, v, grid, T, alpha=alpha, **kw) * dO).sum())
+
+
+WEIGHTS = [(3, {"beta": 0.5}), (4, {"w": [0.2, -0.5, 1.3, 0.7]}), (1, {"beta": 0.5}), (0, {"beta": 0.6}),
+           (6, {"beta": 0.8})]
+
+
+@pytest.mark.parametrize("T,kw", WEIGHTS)
+@pytest.mark.parametrize("grid", [(3, 4), (1, 5), (4, 1)])
+def test_backward_matches_finite_differences(T, kw, grid):
+    H, W = grid
+    xq, xk, v, dO = _case(1, 2, H, W, 5)
+    alpha = np.array([0.3, 0.7])
+    gq, gk, gv, ga = oracle.backward(xq, xk, v, dO, grid, T, alpha=alpha, **kw)
+    h = 1e-6
+    for arr, grad in ((xq, gq), (xk, gk), (v, gv)):
+        num = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            keep = arr[idx]
+            arr[idx] = keep + h
+            up = _loss(xq, xk, v, dO, grid, T, alpha, **kw)
+            arr[idx] = keep - h
+            dn = _loss(xq, xk, v, dO, grid, T, alpha, **kw)
+            arr[idx] = keep
+            num[idx] = (up - dn) / (2 * h)
+        assert np.abs(num - grad).max() <= 1e-6 * max(np.abs(grad).max(), 1.0)
+    for hd in range(2):
+        e = np.zeros(2)
+        e[hd] = h
+        num = (_loss(xq, xk, v, dO, grid, T, alpha + e, **kw) - _loss(xq, xk, v, dO, grid, T, alpha - e, **kw)) / (2 * h)
+        assert abs(num - ga[hd]) <= 1e-6 * max(abs(ga[hd]), 1.0)
+
+
+def test_backward_without_feature_map():
+    """relu = False: the inputs are the (non-negative) features themselves."""
+    xq, xk, v, dO = _case(1, 1, 3, 3, 4)
+    xq, xk = np.abs(xq) + 0.05, np.abs(xk) + 0.05
+    grid, T = (3, 3), 3
+    gq, gk, gv, _ = oracle.backward(xq, xk, v, dO, grid, T, alpha=0.4, beta=0.5, relu=False)
+    h = 1e-6
+    for arr, grad in ((xq, gq), (xk, gk)):
+        for idx in [(0, 0, 0, 0), (0, 0, 4, 2), (0, 0, 8, 3)]:
+            keep = arr[idx]
+            arr[idx] = keep + h
+            up = _loss(xq, xk, v, dO, grid, T, 0.4, beta=0.5, relu=False)
+            arr[idx] = keep - h
+            dn = _loss(xq, xk, v, dO, grid, T, 0.4, beta=0.5, relu=False)
+            arr[idx] = keep
+            assert abs((up - dn) / (2 * h) - grad[idx]) <= 1e-6 * max(abs(grad[idx]), 1.0)
+
+
+def _dense_torch_layer(xq, xk, v, grid, T, alpha, w, eps=1e-6):
+    """The layer restated densely in torch (autograd's route): S = Q~ K^T
+    formed, g = sum_k w_k S^k V, the local window as a masked softmax."""
+    H, W = grid
+    n = H * W
+    q, k = torch.relu(xq), torch.relu(xk)
+    s = k.sum(0)
+    qt = q / (q @ s + eps)[:, None]
+    S = qt @ k.T
+    g, y = w[0] * v, v
+    for t in range(1, T):
+        y = S @ y
+        g = g + w[t] * y
+    rr, cc = np.divmod(np.arange(n), W)
+    near = (np.abs(rr[:, None] - rr[None, :]) <= 1) & (np.abs(cc[:, None] - cc[None, :]) <= 1)
+    e = (q @ k.T) / np.sqrt(q.shape[1])
+    e = e.masked_fill(torch.from_numpy(~near), float("-inf"))
+    l = torch.softmax(e, dim=1) @ v
+    return alpha * g + (1 - alpha) * l
+
+
+@pytest.mark.parametrize("T,w", [(3, [4 / 7, 2 / 7, 1 / 7]), (4, [0.1, 0.4, -0.3, 0.8])])
+def test_backward_matches_autograd_of_dense_layer(T, w):
+    grid = (5, 4)
+    xq, xk, v, dO = _case(1, 1, 5, 4, 6)
+    alpha = 0.35
+    gq, gk, gv, ga = oracle.backward(xq, xk, v, dO, grid, T, alpha=alpha, w=w)
+    t = [torch.tensor(a[0, 0], requires_grad=True) for a in (xq, xk, v)]
+    ta = torch.tensor(alpha, dtype=torch.float64, requires_grad=True)
+    out = _dense_torch_layer(t[0], t[1], t[2], grid, T, ta, w)
+    np.testing.assert_allclose(out.detach().numpy(), oracle.forward(xq, xk, v, grid, T, alpha=alpha, w=w)[0, 0],
+                               rtol=0, atol=1e-12)
+    (out * torch.from_numpy(dO[0, 0])).sum().backward()
+    for got, ref in ((gq, t[0]), (gk, t[1]), (gv, t[2])):
+        np.testing.assert_allclose(got[0, 0], ref.grad.numpy(), rtol=0, atol=1e-10)
+    assert abs(ga[0] - ta.grad.item()) <= 1e-10
+
+
+def test_identity_layer_gradients():
+    """T = 1, alpha = 1: O = V exactly, so dXq = dXk = 0, dV = dO, and
+    dalpha = sum dO . (V - l) (the local branch still enters through alpha)."""
+    xq, xk, v, dO = _case(2, 1, 4, 3, 4)
+    gq, gk, gv, ga = oracle.backward(xq, xk, v, dO, (4, 3), 1, alpha=1.0, beta=0.5)
+    assert np.all(gq == 0) and np.all(gk == 0)
+    np.testing.assert_allclose(gv, dO, rtol=0, atol=1e-15)
+    _, _, L = oracle.forward(xq, xk, v, (4, 3), 1, alpha=1.0, beta=0.5, branches=True)
+    np.testing.assert_allclose(ga[0], (dO * (v - L)).sum(), rtol=1e-13)
+
+
+def test_backward_is_linear_in_upstream_gradient():
+    xq, xk, v, d1 = _case(1, 2, 3, 5, 4)
+    d2 = RNG.standard_normal(d1.shape)
+    kw = dict(alpha=[0.2, 0.6], beta=0.5)
+    a = oracle.backward(xq, xk, v, d1, (3, 5), 3, **kw)
+    b = oracle.backward(xq, xk, v, d2, (3, 5), 3, **kw)
+    c = oracle.backward(xq, xk, v, d1 + 2 * d2, (3, 5), 3, **kw)
+    for x, y, z in zip(a, b, c):
+        np.testing.assert_allclose(z, x + 2 * y, rtol=1e-12, atol=1e-12)
+
+
+def test_backward_rejects_mlp_and_bad_args():
+    xq, xk, v, dO = _case(1, 1, 2, 2, 3)
+    with pytest.raises(ValueError):
+        oracle.backward(xq, xk, v, dO, (2, 2), 0, alpha=0.5, w=[1.0])
+    with pytest.raises(ValueError):
+        oracle.backward(xq, xk, v, dO, (2, 3), 3, alpha=0.5, beta=0.5)
