@@ -114,42 +114,8 @@ lisa_status check_sizes(int B, int heads, int H, int W, int d_h, int d_v, int T,
 // whose single hop matrix comes from the d x d solve.
 int effective_T(int T) { return T == 0 ? 2 : T; }
 
-}  // namespace
-}  // namespace lisa
-
-using namespace lisa;
-
-extern "C" size_t lisa_workspace_bytes(int B, int heads, int H, int W, int d_h, int d_v, int T,
-                                       int dtype) {
-    if (check_sizes(B, heads, H, W, d_h, d_v, T, dtype) != LISA_OK) return 0;
-    const long long slices = (long long)B * heads, n = (long long)H * W;
-    if (slices == 0 || n == 0) return 0;
-    T = effective_T(T);
-    // the weight mode is not known here: size for whichever needs more
-    size_t need = make_plan((int)slices, (int)n, d_h, T, dtype, LISA_W_FIXED, 0).total;
-    for (int hidden : {16, LISA_MAX_HIDDEN}) {
-        const size_t m = make_plan((int)slices, (int)n, d_h, T, dtype, LISA_W_MLP, hidden).total;
-        if (m > need) need = m;
-    }
-    return need;
-}
-
-namespace {
-
-// Checks every argument of a forward call and fills the Problem.  Sets
-// *empty when there is nothing to compute.  Launches nothing.
-lisa_status prepare(Problem &p, bool &empty, const void *Q, const void *K, const void *V, void *O,
-                    int B, int heads, int H, int W, int d_h, int d_v, int T,
-                    const lisa_weights *wts, const float *alpha, float eps, int relu_inputs,
-                    int dtype, void *workspace, size_t workspace_bytes) {
-    empty = false;
-    lisa_status st = check_sizes(B, heads, H, W, d_h, d_v, T, dtype);
-    if (st != LISA_OK) return st;
-    if (!wts) return LISA_ERR_INVALID_ARG;
-    if (!(eps > 0.f) || !std::isfinite(eps)) return LISA_ERR_INVALID_ARG;
-    if (relu_inputs != 0 && relu_inputs != 1) return LISA_ERR_INVALID_ARG;
-
-    p = Problem{};
+// Walk weights of a call into p (T, w, wmode, the untruncated flag).
+lisa_status resolve_weights(Problem &p, const lisa_weights *wts, int T) {
     p.T = effective_T(T);
     if (T == 0 && wts->mode != LISA_W_GEOMETRIC) return LISA_ERR_INVALID_ARG;
     switch (wts->mode) {
@@ -193,28 +159,17 @@ lisa_status prepare(Problem &p, bool &empty, const void *Q, const void *K, const
         default:
             return LISA_ERR_INVALID_ARG;
     }
+    return LISA_OK;
+}
 
-    const long long slices = (long long)B * heads, n = (long long)H * W;
-    if (slices == 0 || n == 0) {  // empty problem: nothing to launch
-        empty = true;
-        return LISA_OK;
-    }
-    if (!Q || !K || !V || !O || !alpha) return LISA_ERR_INVALID_ARG;
-    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O))
-        return LISA_ERR_INVALID_ARG;
-    const size_t esz = (dtype == LISA_BF16) ? 2 : 4;
-    const size_t bytes = (size_t)slices * (size_t)n * (size_t)d_h * esz;
-    if (overlaps(O, bytes, Q, bytes) || overlaps(O, bytes, K, bytes) || overlaps(O, bytes, V, bytes))
-        return LISA_ERR_INVALID_ARG;
-
-    const Plan pl = make_plan((int)slices, (int)n, d_h, p.T, dtype, p.wmode, p.hidden);
-    if (!workspace || workspace_bytes < pl.total) return LISA_ERR_WORKSPACE;
-    if (!aligned16(workspace)) return LISA_ERR_INVALID_ARG;
-
+// Sizes, inputs and workspace views of a checked call.
+void fill_problem(Problem &p, const Plan &pl, const void *Q, const void *K, const void *V, void *O, int slices,
+                  int heads, int H, int W, int d_h, int relu_inputs, float eps, const float *alpha, int dtype,
+                  void *workspace) {
     p.Q = Q; p.K = K; p.V = V; p.O = O;
-    p.slices = (int)slices;
+    p.slices = slices;
     p.heads = heads;
-    p.H = H; p.W = W; p.n = (int)n;
+    p.H = H; p.W = W; p.n = H * W;
     p.D = d_h;
     p.relu = relu_inputs;
     p.eps = eps;
@@ -237,6 +192,64 @@ lisa_status prepare(Problem &p, bool &empty, const void *Q, const void *K, const
         p.tc_bepi = reinterpret_cast<uint8_t *>(ws + pl.off_tc_bepi);
         p.tc_w1img = reinterpret_cast<uint8_t *>(ws + pl.off_tc_w1img);
     }
+}
+
+}  // namespace
+}  // namespace lisa
+
+using namespace lisa;
+
+extern "C" size_t lisa_workspace_bytes(int B, int heads, int H, int W, int d_h, int d_v, int T,
+                                       int dtype) {
+    if (check_sizes(B, heads, H, W, d_h, d_v, T, dtype) != LISA_OK) return 0;
+    const long long slices = (long long)B * heads, n = (long long)H * W;
+    if (slices == 0 || n == 0) return 0;
+    T = effective_T(T);
+    // the weight mode is not known here: size for whichever needs more
+    size_t need = make_plan((int)slices, (int)n, d_h, T, dtype, LISA_W_FIXED, 0).total;
+    for (int hidden : {16, LISA_MAX_HIDDEN}) {
+        const size_t m = make_plan((int)slices, (int)n, d_h, T, dtype, LISA_W_MLP, hidden).total;
+        if (m > need) need = m;
+    }
+    return need;
+}
+
+namespace {
+
+// Checks every argument of a forward call and fills the Problem.  Sets
+// *empty when there is nothing to compute.  Launches nothing.
+lisa_status prepare(Problem &p, bool &empty, const void *Q, const void *K, const void *V, void *O,
+                    int B, int heads, int H, int W, int d_h, int d_v, int T,
+                    const lisa_weights *wts, const float *alpha, float eps, int relu_inputs,
+                    int dtype, void *workspace, size_t workspace_bytes) {
+    empty = false;
+    lisa_status st = check_sizes(B, heads, H, W, d_h, d_v, T, dtype);
+    if (st != LISA_OK) return st;
+    if (!wts) return LISA_ERR_INVALID_ARG;
+    if (!(eps > 0.f) || !std::isfinite(eps)) return LISA_ERR_INVALID_ARG;
+    if (relu_inputs != 0 && relu_inputs != 1) return LISA_ERR_INVALID_ARG;
+
+    p = Problem{};
+    st = resolve_weights(p, wts, T);
+    if (st != LISA_OK) return st;
+
+    const long long slices = (long long)B * heads, n = (long long)H * W;
+    if (slices == 0 || n == 0) {  // empty problem: nothing to launch
+        empty = true;
+        return LISA_OK;
+    }
+    if (!Q || !K || !V || !O || !alpha) return LISA_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O))
+        return LISA_ERR_INVALID_ARG;
+    const size_t esz = (dtype == LISA_BF16) ? 2 : 4;
+    const size_t bytes = (size_t)slices * (size_t)n * (size_t)d_h * esz;
+    if (overlaps(O, bytes, Q, bytes) || overlaps(O, bytes, K, bytes) || overlaps(O, bytes, V, bytes))
+        return LISA_ERR_INVALID_ARG;
+
+    const Plan pl = make_plan((int)slices, (int)n, d_h, p.T, dtype, p.wmode, p.hidden);
+    if (!workspace || workspace_bytes < pl.total) return LISA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return LISA_ERR_INVALID_ARG;
+    fill_problem(p, pl, Q, K, V, O, (int)slices, heads, H, W, d_h, relu_inputs, eps, alpha, dtype, workspace);
     return LISA_OK;
 }
 
@@ -353,7 +366,7 @@ extern "C" const char *lisa_status_string(int status) {
     }
 }
 
-extern "C" int lisa_abi_version(void) { return 100; }
+extern "C" int lisa_abi_version(void) { return 101; }
 
 // ---------------------------------------------------------------------------
 // lisa_forward_noalloc -- the layer for callers that may not allocate device
@@ -414,4 +427,127 @@ extern "C" lisa_status lisa_forward_noalloc(const void *Q, const void *K, const 
     }
     return lisa_forward(Q, K, V, O, B, heads, H, W, d_h, d_v, T, wts, alpha, eps, relu_inputs, dtype,
                         scratch, (size_t)LISA_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+// ---------------------------------------------------------------------------
+// lisa_backward -- gradients of the layer (see include/lisa.h).
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kBwdTokensPerBlock = 32;   // per-token kernels: 8 warps x 4 tokens
+
+struct BwdPlan {
+    Plan fwd;   // SIMT statistics partials (s, K^T V, K^T Q~) and s
+    int nh, nblk;
+    size_t off_mred, off_uk, off_ubar, off_dub, off_lstat, off_dalp, off_dsp, off_dm, off_du1, off_dsr,
+        off_dals, off_dkp;
+    size_t total;
+};
+
+// The backward always runs the SIMT statistics kernels; its own buffers
+// follow the forward plan's.
+BwdPlan make_bwd_plan(int slices, int n, int D, int T, int dtype) {
+    BwdPlan b{};
+    b.fwd = make_plan(slices, n, D, T, LISA_F32, LISA_W_FIXED, 0);   // SIMT family, any dtype
+    (void)dtype;
+    b.nh = T > 1 ? T - 1 : 1;
+    b.nblk = (n + kBwdTokensPerBlock - 1) / kBwdTokensPerBlock;
+    const size_t S = (size_t)slices, C = (size_t)b.fwd.chunks, d = (size_t)D, dd = d * d;
+    size_t off = b.fwd.total;
+    b.off_mred = off;  off = align_up(off + S * dd * sizeof(float));
+    b.off_uk = off;    off = align_up(off + S * b.nh * dd * sizeof(float));
+    b.off_ubar = off;  off = align_up(off + S * dd * sizeof(float));
+    b.off_dub = off;   off = align_up(off + S * C * dd * sizeof(float));
+    b.off_lstat = off; off = align_up(off + S * (size_t)n * 4 * sizeof(float));
+    b.off_dalp = off;  off = align_up(off + S * b.nblk * sizeof(float));
+    b.off_dsp = off;   off = align_up(off + S * b.nblk * d * sizeof(float));
+    b.off_dm = off;    off = align_up(off + S * dd * sizeof(float));
+    b.off_du1 = off;   off = align_up(off + S * dd * sizeof(float));
+    b.off_dsr = off;   off = align_up(off + S * d * sizeof(float));
+    b.off_dals = off;  off = align_up(off + S * sizeof(float));
+    b.off_dkp = off;   off = align_up(off + S * (size_t)n * d * sizeof(float));
+    b.total = off;
+    return b;
+}
+
+}  // namespace
+
+extern "C" size_t lisa_backward_workspace_bytes(int B, int heads, int H, int W, int d_h, int d_v, int T,
+                                                int dtype) {
+    if (check_sizes(B, heads, H, W, d_h, d_v, T, dtype) != LISA_OK) return 0;
+    const long long slices = (long long)B * heads, n = (long long)H * W;
+    if (slices == 0 || n == 0) return 0;
+    return make_bwd_plan((int)slices, (int)n, d_h, effective_T(T), dtype).total;
+}
+
+extern "C" lisa_status lisa_backward(const void *Q, const void *K, const void *V, const void *dO, void *dQ,
+                                     void *dK, void *dV, float *dalpha, int B, int heads, int H, int W,
+                                     int d_h, int d_v, int T, const lisa_weights *wts, const float *alpha,
+                                     float eps, int relu_inputs, int dtype, void *workspace,
+                                     size_t workspace_bytes, void *stream) {
+    lisa_status st = check_sizes(B, heads, H, W, d_h, d_v, T, dtype);
+    if (st != LISA_OK) return st;
+    if (!wts) return LISA_ERR_INVALID_ARG;
+    if (wts->mode == LISA_W_MLP) return LISA_ERR_UNSUPPORTED;
+    if (!(eps > 0.f) || !std::isfinite(eps)) return LISA_ERR_INVALID_ARG;
+    if (relu_inputs != 0 && relu_inputs != 1) return LISA_ERR_INVALID_ARG;
+    BwdProblem b{};
+    st = resolve_weights(b.fwd, wts, T);
+    if (st != LISA_OK) return st;
+    const long long slices = (long long)B * heads, n = (long long)H * W;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (slices == 0 || n == 0) {   // nothing to differentiate: dalpha = 0
+        if (heads > 0) {
+            if (!dalpha) return LISA_ERR_INVALID_ARG;
+            if (cudaMemsetAsync(dalpha, 0, (size_t)heads * sizeof(float), cs) != cudaSuccess)
+                return LISA_ERR_CUDA;
+        }
+        return LISA_OK;
+    }
+    if (!Q || !K || !V || !dO || !dQ || !dK || !dV || !dalpha || !alpha) return LISA_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(dO) || !aligned16(dQ) ||
+        !aligned16(dK) || !aligned16(dV))
+        return LISA_ERR_INVALID_ARG;
+    const size_t esz = (dtype == LISA_BF16) ? 2 : 4;
+    const size_t bytes = (size_t)slices * (size_t)n * (size_t)d_h * esz;
+    const void *ins[4] = {Q, K, V, dO};
+    void *outs[3] = {dQ, dK, dV};
+    for (void *o : outs) {
+        for (const void *in : ins)
+            if (overlaps(o, bytes, in, bytes)) return LISA_ERR_INVALID_ARG;
+        if (overlaps(o, bytes, dalpha, (size_t)heads * sizeof(float))) return LISA_ERR_INVALID_ARG;
+    }
+    if (overlaps(dQ, bytes, dK, bytes) || overlaps(dQ, bytes, dV, bytes) || overlaps(dK, bytes, dV, bytes))
+        return LISA_ERR_INVALID_ARG;
+    if (overlaps(dalpha, (size_t)heads * sizeof(float), alpha, (size_t)heads * sizeof(float)))
+        return LISA_ERR_INVALID_ARG;
+
+    const BwdPlan pl = make_bwd_plan((int)slices, (int)n, d_h, b.fwd.T, dtype);
+    if (!workspace || workspace_bytes < pl.total) return LISA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return LISA_ERR_INVALID_ARG;
+    fill_problem(b.fwd, pl.fwd, Q, K, V, nullptr, (int)slices, heads, H, W, d_h, relu_inputs, eps, alpha, dtype,
+                 workspace);
+    b.fwd.dtype = dtype;
+    b.dO = dO;
+    b.dQ = dQ;
+    b.dK = dK;
+    b.dV = dV;
+    b.dalpha = dalpha;
+    b.tpb = kBwdTokensPerBlock;
+    b.nblk = pl.nblk;
+    b.nh = pl.nh;
+    char *ws = static_cast<char *>(workspace);
+    b.Mred = reinterpret_cast<float *>(ws + pl.off_mred);
+    b.Uk = reinterpret_cast<float *>(ws + pl.off_uk);
+    b.Ubar = reinterpret_cast<float *>(ws + pl.off_ubar);
+    b.dub_part = reinterpret_cast<float *>(ws + pl.off_dub);
+    b.lstat = reinterpret_cast<float *>(ws + pl.off_lstat);
+    b.dal_part = reinterpret_cast<float *>(ws + pl.off_dalp);
+    b.ds_part = reinterpret_cast<float *>(ws + pl.off_dsp);
+    b.dM = reinterpret_cast<float *>(ws + pl.off_dm);
+    b.dU1 = reinterpret_cast<float *>(ws + pl.off_du1);
+    b.ds_red = reinterpret_cast<float *>(ws + pl.off_dsr);
+    b.dal_slice = reinterpret_cast<float *>(ws + pl.off_dals);
+    b.dk_part = reinterpret_cast<float *>(ws + pl.off_dkp);
+    return launch_bwd(b, cs) == cudaSuccess ? LISA_OK : LISA_ERR_CUDA;
 }

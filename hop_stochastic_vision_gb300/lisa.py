@@ -34,8 +34,8 @@ LISA_MAX_T_MLP = 8
 LISA_MAX_HIDDEN = 64
 
 EXPORTED = ("lisa_workspace_bytes", "lisa_forward", "lisa_forward_host", "lisa_num_stages",
-            "lisa_stage_name", "lisa_forward_stage", "lisa_forward_noalloc", "lisa_status_string",
-            "lisa_abi_version")
+            "lisa_stage_name", "lisa_forward_stage", "lisa_forward_noalloc", "lisa_backward_workspace_bytes",
+            "lisa_backward", "lisa_status_string", "lisa_abi_version")
 
 LISA_NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -89,6 +89,11 @@ def load(path: str = LIB_PATH):
         lib.lisa_forward_stage.restype = i
         lib.lisa_forward_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, wp, vp, f, i, i, vp]
         lib.lisa_forward_noalloc.restype = i
+        lib.lisa_backward_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i]
+        lib.lisa_backward_workspace_bytes.restype = sz
+        lib.lisa_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, wp, vp, f, i, i,
+                                      vp, sz, vp]
+        lib.lisa_backward.restype = i
         lib.lisa_status_string.argtypes = [i]
         lib.lisa_status_string.restype = ctypes.c_char_p
         lib.lisa_abi_version.argtypes = []
@@ -140,6 +145,17 @@ def lisa_forward_noalloc(Q, K, V, O, B, heads, H, W, d_h, d_v, T, wts, alpha, ep
     library's own fixed scratch array replaces the workspace (see lisa.h)."""
     return int(load().lisa_forward_noalloc(Q, K, V, O, B, heads, H, W, d_h, d_v, T, ctypes.byref(wts),
                                            alpha, eps, relu_inputs, dtype, stream))
+
+
+def lisa_backward_workspace_bytes(B, heads, H, W, d_h, d_v, T, dtype) -> int:
+    return int(load().lisa_backward_workspace_bytes(B, heads, H, W, d_h, d_v, T, dtype))
+
+
+def lisa_backward(Q, K, V, dO, dQ, dK, dV, dalpha, B, heads, H, W, d_h, d_v, T, wts, alpha, eps, relu_inputs,
+                  dtype, workspace, workspace_bytes, stream) -> int:
+    return int(load().lisa_backward(Q, K, V, dO, dQ, dK, dV, dalpha, B, heads, H, W, d_h, d_v, T,
+                                    ctypes.byref(wts), alpha, eps, relu_inputs, dtype, workspace,
+                                    workspace_bytes, stream))
 
 
 def lisa_forward_host(hQ, hK, hV, hO, dQ, dK, dV, dO, B, heads, H, W, d_h, d_v, T, wts, alpha, eps,
@@ -218,3 +234,38 @@ def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, grid, T: int, *, 
     if status != LISA_OK:
         raise LisaError(status)
     return O
+
+
+def backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, dO: torch.Tensor, grid, T: int, *,
+             alpha: torch.Tensor, beta=None, w=None, eps: float = 1e-6, relu: bool = True, workspace=None,
+             stream=None):
+    """Gradients of the LiSA forward on CUDA tensors [B, heads, H*W, d]
+    (fp32 or bf16) for the upstream gradient ``dO``: returns
+    (dq, dk, dv, dalpha), dalpha fp32 [heads] summed over the batch."""
+    for t in (q, k, v, dO, alpha):
+        if not t.is_cuda:
+            raise ValueError("lisa.backward runs on CUDA tensors only")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+    if q.dtype not in _DTYPES or k.dtype != q.dtype or v.dtype != q.dtype or dO.dtype != q.dtype:
+        raise ValueError("q, k, v, dO must share dtype float32 or bfloat16")
+    if alpha.dtype != torch.float32:
+        raise ValueError("alpha must be fp32")
+    B, heads, n, d = q.shape
+    H, W = grid
+    dv = v.shape[-1]
+    dq, dk, dvv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dalpha = torch.empty(heads, dtype=torch.float32, device=q.device)
+    wt, keep = make_weights(T, beta=beta, w=w)
+    dt = _DTYPES[q.dtype]
+    nbytes = lisa_backward_workspace_bytes(B, heads, H, W, d, dv, T, dt)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    st = torch.cuda.current_stream(q.device).cuda_stream if stream is None else stream
+    status = lisa_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), dO.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                           dvv.data_ptr(), dalpha.data_ptr(), B, heads, H, W, d, dv, T, wt, alpha.data_ptr(),
+                           float(eps), int(bool(relu)), dt, workspace.data_ptr(), workspace.numel(), st)
+    del keep
+    if status != LISA_OK:
+        raise LisaError(status)
+    return dq, dk, dvv, dalpha

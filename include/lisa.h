@@ -190,6 +190,35 @@ lisa_status lisa_forward_noalloc(const void *Q, const void *K, const void *V, vo
                                  const lisa_weights *wts, const float *alpha, float eps,
                                  int relu_inputs, int dtype, void *stream);
 
+/*
+ * Backward pass of the layer: the gradients of a loss L with respect to the
+ * layer's inputs, given dO = dL/dO (the chain rule through the forward
+ * above; the paper trains LiSA backbones end to end [note §3]).
+ *   Q, K, V     the forward's inputs (device, dtype, [B][heads][H*W][d]).
+ *   dO          device [B][heads][H*W][d_v], dtype: upstream gradient.
+ *   dQ, dK, dV  device, dtype, same shapes; written: dL/dQ, dL/dK, dL/dV
+ *               of the raw inputs (through the ReLU feature map when
+ *               relu_inputs = 1: zero where the input is <= 0).
+ *   dalpha      device fp32 [heads]; written (not accumulated): dL/dalpha_h,
+ *               summed over the batch.
+ * Weights: LISA_W_GEOMETRIC (T >= 1, or T = 0 untruncated) and LISA_W_FIXED;
+ * LISA_W_MLP returns LISA_ERR_UNSUPPORTED.  Outputs may not overlap each
+ * other or any input.  Arithmetic is fp32 (bf16 inputs widened, bf16
+ * outputs rounded to nearest even); every sum runs in a fixed order, so the
+ * result is the same on every run.  The workspace (>= the bytes
+ * lisa_backward_workspace_bytes returns, 16-byte aligned) needs no
+ * initialisation.  Checks, statuses and stream behaviour as for
+ * lisa_forward.  An empty problem (B * heads * H * W == 0) only zeroes
+ * dalpha.
+ */
+size_t lisa_backward_workspace_bytes(int B, int heads, int H, int W, int d_h, int d_v, int T,
+                                     int dtype);
+lisa_status lisa_backward(const void *Q, const void *K, const void *V, const void *dO, void *dQ,
+                          void *dK, void *dV, float *dalpha, int B, int heads, int H, int W,
+                          int d_h, int d_v, int T, const lisa_weights *wts, const float *alpha,
+                          float eps, int relu_inputs, int dtype, void *workspace,
+                          size_t workspace_bytes, void *stream);
+
 /* Static, human-readable name of a status code. */
 const char *lisa_status_string(int status);
 

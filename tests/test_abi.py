@@ -162,3 +162,61 @@ def test_forward_host_checks_before_copies():
     args[0] = 0
     args[-3], args[-2] = FAKE, 1 << 30
     assert lisa.lisa_forward_host(*args) == lisa.LISA_ERR_INVALID_ARG
+
+
+def _bwd(**over):
+    args = dict(Q=FAKE, K=FAKE + 4096, V=FAKE + 8192, dO=FAKE + 12288, dQ=FAKE + 16384, dK=FAKE + 20480,
+                dV=FAKE + 24576, dalpha=FAKE + 28672, B=1, heads=1, H=4, W=4, d_h=16, d_v=16, T=3,
+                alpha=FAKE + 28688, eps=1e-6, relu=1, dtype=lisa.LISA_F32, workspace=FAKE + 65536,
+                wbytes=1 << 30, beta=0.5)
+    args.update(over)
+    wt = args.get("wt") or lisa.make_weights(max(args["T"], 1), beta=args["beta"])[0]
+    return lisa.lisa_backward(args["Q"], args["K"], args["V"], args["dO"], args["dQ"], args["dK"], args["dV"],
+                              args["dalpha"], args["B"], args["heads"], args["H"], args["W"], args["d_h"],
+                              args["d_v"], args["T"], wt, args["alpha"], args["eps"], args["relu"],
+                              args["dtype"], args["workspace"], args["wbytes"], 0)
+
+
+def test_backward_workspace_bytes():
+    ws = lisa.lisa_backward_workspace_bytes
+    assert ws(32, 1, 56, 56, 64, 64, 3, lisa.LISA_BF16) > ws(1, 1, 56, 56, 64, 64, 3, lisa.LISA_BF16) > 0
+    assert ws(1, 1, 4, 4, 64, 64, 0, lisa.LISA_BF16) > 0
+    assert ws(0, 1, 4, 4, 64, 64, 3, lisa.LISA_BF16) == 0
+    assert ws(1, 1, 4, 4, 48, 48, 3, lisa.LISA_BF16) == 0
+    assert ws(1, 1, 4, 4, 64, 64, 17, lisa.LISA_BF16) == 0
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(dO=0), lisa.LISA_ERR_INVALID_ARG),
+    (dict(dQ=0), lisa.LISA_ERR_INVALID_ARG),
+    (dict(dalpha=0), lisa.LISA_ERR_INVALID_ARG),
+    (dict(dK=FAKE + 8), lisa.LISA_ERR_INVALID_ARG),                 # misaligned
+    (dict(dV=FAKE + 8192), lisa.LISA_ERR_INVALID_ARG),              # dV overlaps V
+    (dict(dK=FAKE + 16384), lisa.LISA_ERR_INVALID_ARG),             # dK overlaps dQ
+    (dict(dalpha=FAKE + 28688), lisa.LISA_ERR_INVALID_ARG),         # dalpha overlaps alpha
+    (dict(T=-1), lisa.LISA_ERR_INVALID_ARG),
+    (dict(T=17), lisa.LISA_ERR_UNSUPPORTED),
+    (dict(d_h=48, d_v=48), lisa.LISA_ERR_UNSUPPORTED),
+    (dict(eps=0.0), lisa.LISA_ERR_INVALID_ARG),
+    (dict(beta=1.0), lisa.LISA_ERR_INVALID_ARG),
+    (dict(relu=3), lisa.LISA_ERR_INVALID_ARG),
+    (dict(workspace=0), lisa.LISA_ERR_WORKSPACE),
+    (dict(wbytes=1024), lisa.LISA_ERR_WORKSPACE),
+    (dict(T=0, wbytes=1024), lisa.LISA_ERR_WORKSPACE),
+])
+def test_backward_rejects_before_launch(over, status):
+    assert _bwd(**over) == status
+
+
+def test_backward_weight_modes():
+    wt = lisa.lisa_weights()
+    wt.mode = lisa.LISA_W_MLP
+    wt.W1 = wt.b1 = wt.W2 = wt.b2 = FAKE
+    wt.hidden = 32
+    assert _bwd(wt=wt) == lisa.LISA_ERR_UNSUPPORTED             # adaptive weights: not covered
+    wt = lisa.lisa_weights()
+    wt.mode = lisa.LISA_W_FIXED
+    arr = (ctypes.c_float * 3)(0.5, 0.25, 0.25)
+    wt.w = ctypes.cast(arr, ctypes.POINTER(ctypes.c_float))
+    assert _bwd(wt=wt, T=0) == lisa.LISA_ERR_INVALID_ARG        # untruncated: geometric only
+    assert _bwd(wt=wt, wbytes=16) == lisa.LISA_ERR_WORKSPACE

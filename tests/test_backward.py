@@ -1,0 +1,138 @@
+"""GPU parity of the backward pass (lisa_backward) against the oracle's
+hand-derived, finite-difference-pinned backward, on the same seeded inputs
+and upstream gradient.
+
+Tolerance: the normwise error of each slice's whole gradient (dXq, dXk,
+dV), max over (batch, head) slices of max_t ||gpu_t - oracle_t||_inf /
+max_t ||oracle_t||_inf, <= 1e-4 (fp32) or 2e-2 (bf16 outputs, fp32
+arithmetic) -- the forward's bounds; dalpha (fp32 in both) within 1e-3
+relative plus 1e-5 of sum_i |dO_i| (|g_i| + |l_i|), its own rounding scale.  The joint norm matters where one gradient is nearly zero by
+cancellation: on a 1 x 1 grid S = Q~K^T = Q.K/(Q.K + eps), so dXq and dXk
+are O(eps) differences of O(1) terms and fp32 rounding is as large as they
+are, while dV is O(1)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from lisa_synth import SHAPES, LayerShape, make_inputs, to_f64
+
+from helpers import TOL, max_rel_err, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda_lib():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    from hop_stochastic_vision_gb300 import build, lisa
+    build.build()
+    lisa.load()
+
+
+def joint_rel_err(got, want):
+    """max over slices of max_t ||got_t - want_t||_inf / max_t ||want_t||_inf."""
+    S = got[0].shape[0] * got[0].shape[1]
+    num = np.max([np.abs(g - w).reshape(S, -1).max(axis=1) for g, w in zip(got, want)], axis=0)
+    den = np.max([np.abs(w).reshape(S, -1).max(axis=1) for w in want], axis=0)
+    return float((num / np.where(den > 0, den, 1.0)).max())
+
+
+def _upstream(shape, B, heads, seed=7):
+    g = torch.Generator("cpu").manual_seed(seed)
+    dO = torch.randn(B, heads, shape.n, shape.d, generator=g)
+    return dO.to(torch.bfloat16 if shape.dtype == "bf16" else torch.float32)
+
+
+def _check(shape, *, B=None, heads=None, beta=0.5, w=None, relu=True, seed=0, structured=False, alpha=None):
+    from hop_stochastic_vision_gb300 import lisa
+    inp = make_inputs(shape, seed=seed, B=B, heads=heads, structured=structured)
+    B, heads = inp["xq"].shape[:2]
+    if alpha is not None:
+        inp["alpha"] = torch.full_like(inp["alpha"], float(alpha))
+    if not relu:
+        inp["xq"], inp["xk"] = inp["xq"].clamp_min(0), inp["xk"].clamp_min(0)
+    dO = _upstream(shape, B, heads)
+    d = to_device(inp)
+    kw = {"w": list(w)} if w is not None else {"beta": beta}
+    dq, dk, dv, da = lisa.backward(d["xq"], d["xk"], d["v"], dO.cuda(), (shape.H, shape.W), shape.T,
+                                   alpha=d["alpha"], relu=relu, **kw)
+    torch.cuda.synchronize()
+    okw = {"w": np.asarray(w, dtype=np.float64)} if w is not None else {"beta": beta}
+    want = oracle.backward(to_f64(inp["xq"]), to_f64(inp["xk"]), to_f64(inp["v"]), to_f64(dO),
+                           (shape.H, shape.W), shape.T, alpha=inp["alpha"].double().numpy(), relu=relu, **okw)
+    got = [to_f64(x.cpu()) for x in (dq, dk, dv)]
+    for g in got:
+        assert np.isfinite(g).all()
+    err = joint_rel_err(got, want[:3])
+    assert err <= TOL[shape.dtype], "gradient normwise err %.3e (%s)" % (err, shape.dtype)
+    errs = [max_rel_err(g, r) for g, r in zip(got, want[:3])]
+    # dalpha = sum_i dO_i . (g_i - l_i): its rounding scales with sum |dO| (|g| + |l|)
+    _, G, L = oracle.forward(to_f64(inp["xq"]), to_f64(inp["xk"]), to_f64(inp["v"]), (shape.H, shape.W), shape.T,
+                             alpha=inp["alpha"].double().numpy(), relu=relu, branches=True, **okw)
+    mag = (np.abs(to_f64(dO)) * (np.abs(G) + np.abs(L))).sum(axis=(2, 3)).sum(axis=0)
+    da_err = np.abs(da.cpu().double().numpy() - want[3])
+    assert (da_err <= 1e-3 * np.abs(want[3]) + 1e-5 * mag).all(), (da_err, want[3], mag)
+    return errs
+
+
+def _shape(dtype, d, H, W, T, B=2, heads=2, alpha="uniform(0.3,0.7)"):
+    return LayerShape("bwd", dtype, B, heads, H, W, d, T, "geometric", alpha=alpha)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d", [16, 32, 64])
+def test_widths(dtype, d):
+    _check(_shape(dtype, d, 7, 9, 3))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("T", [1, 2, 5, 8])
+def test_depths(dtype, T):
+    _check(_shape(dtype, 32, 11, 10, T))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_fixed_weights_and_untruncated(dtype):
+    _check(_shape(dtype, 64, 9, 12, 4), w=(0.2, -0.5, 1.3, 0.7))
+    _check(_shape(dtype, 64, 9, 12, 0), beta=0.5)
+    _check(_shape(dtype, 32, 9, 12, 0), beta=0.85)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("grid", [(1, 1), (1, 7), (9, 1), (57, 55)])
+def test_grids(dtype, grid):
+    _check(_shape(dtype, 64, grid[0], grid[1], 3))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_structured_and_without_feature_map(dtype):
+    _check(_shape(dtype, 64, 24, 20, 3, alpha="0.5"), structured=True)
+    _check(_shape(dtype, 64, 11, 13, 3), relu=False)
+
+
+@pytest.mark.parametrize("alpha", [0.0, 1.0])
+def test_single_branch(alpha):
+    _check(_shape("f32", 32, 10, 11, 3), alpha=alpha)
+
+
+def test_full_size_pvt_layer():
+    """The PVT stage-1 layer (32 slices, 56 x 56, d = 64, bf16, T = 3)."""
+    shape = SHAPES["pvt_t_s1_56x56_T3"]
+    _check(shape)
+
+
+def test_deterministic_and_empty():
+    from hop_stochastic_vision_gb300 import lisa
+    shape = _shape("bf16", 64, 28, 28, 3, B=4, heads=3)
+    inp = to_device(make_inputs(shape))
+    dO = _upstream(shape, 4, 3).cuda()
+    a = lisa.backward(inp["xq"], inp["xk"], inp["v"], dO, (28, 28), 3, alpha=inp["alpha"], beta=0.5)
+    b = lisa.backward(inp["xq"], inp["xk"], inp["v"], dO, (28, 28), 3, alpha=inp["alpha"], beta=0.5)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    q = torch.empty(0, 3, 196, 64, dtype=torch.bfloat16, device="cuda")
+    dq, dk, dv, da = lisa.backward(q, q, q, q, (14, 14), 3, alpha=torch.full((3,), 0.5, device="cuda"),
+                                   beta=0.5)
+    assert dq.shape == q.shape and torch.equal(da.cpu(), torch.zeros(3))
