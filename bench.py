@@ -55,6 +55,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--pass", dest="direction", choices=["forward", "backward"], default="forward",
+                    help="forward (the headline) or the backward pass (lisa_backward)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="wall-time budget of the cpu_baseline sample")
@@ -476,12 +478,147 @@ def ours_arm(args, shape):
     del keep
 
 
+# -- the backward pass ------------------------------------------------------------------
+
+BWD_METRIC = "LiSA bwd tokens·heads/s at n=3136 bf16 (dXq, dXk, dV, dalpha); % of HBM roofline"
+# algorithmic bytes per token*head: read Q, K, V, dO, write dQ, dK, dV (d = 64, bf16)
+BWD_BYTES_PER_TOKEN = 7 * 64 * 2
+
+
+def oracle_backward_runner(shape, seed=0):
+    import oracle
+    from lisa_synth import make_inputs, to_f64
+    inp = make_inputs(shape, seed=seed, B=1, heads=1)
+    xq, xk, v = to_f64(inp["xq"]), to_f64(inp["xk"]), to_f64(inp["v"])
+    import numpy as np
+    dO = np.random.default_rng(seed).standard_normal(v.shape)
+    alpha = inp["alpha"].double().numpy()
+
+    def run():
+        oracle.backward(xq, xk, v, dO, (shape.H, shape.W), shape.T, alpha=alpha, beta=shape.beta)
+    return run
+
+
+def backward_arm(args, shape):
+    """One step = one lisa_backward over the workload's batch (inputs and
+    upstream gradient resident in HBM, rotated over sets larger than 3x L2)."""
+    import ctypes
+
+    import torch
+
+    from hop_stochastic_vision_gb300 import build as lisa_build
+    from hop_stochastic_vision_gb300 import lisa
+    from lisa_synth import make_inputs
+
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    if shape.weights != "geometric":
+        raise SystemExit("the backward pass covers geometric and fixed walk weights")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lisa_build.build()
+    lib = lisa.load()
+    inp = make_inputs(shape)
+    B, heads, n, D, T = shape.B, shape.heads, shape.n, shape.d, shape.T
+    units = B * heads * n
+    set_bytes = 7 * inp["xq"].numel() * inp["xq"].element_size()
+    R = max(2, -(-3 * L2_BYTES // set_bytes))
+    g = torch.Generator("cpu").manual_seed(1)
+    sets = []
+    for _ in range(R):
+        st = {k: inp[k].to(dev).contiguous() for k in ("xq", "xk", "v")}
+        st["dO"] = torch.randn(inp["v"].shape, generator=g).to(inp["v"].dtype).to(dev)
+        st["dq"], st["dk"], st["dv"] = (torch.empty_like(st["v"]) for _ in range(3))
+        sets.append(st)
+    alpha = inp["alpha"].to(dev)
+    dalpha = torch.empty(heads, dtype=torch.float32, device=dev)
+    wt, keep = lisa.make_weights(T, beta=shape.beta)
+    dt = lisa.LISA_BF16 if shape.dtype == "bf16" else lisa.LISA_F32
+    nbytes = lisa.lisa_backward_workspace_bytes(B, heads, shape.H, shape.W, D, D, T, dt)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(dev)
+    call = [(s_["xq"].data_ptr(), s_["xk"].data_ptr(), s_["v"].data_ptr(), s_["dO"].data_ptr(), s_["dq"].data_ptr(),
+             s_["dk"].data_ptr(), s_["dv"].data_ptr(), dalpha.data_ptr(), B, heads, shape.H, shape.W, D, D, T,
+             ctypes.byref(wt), alpha.data_ptr(), 1e-6, 1, dt, ws.data_ptr(), nbytes, stream.cuda_stream)
+            for s_ in sets]
+
+    def step(i):
+        rc = lib.lisa_backward(*call[i % R])
+        if rc != 0:
+            raise RuntimeError("lisa_backward: " + lisa.lisa_status_string(rc))
+
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 1)):
+            step(i)
+    torch.cuda.synchronize(dev)
+    G = min(args.steps, 50)
+    reps, rem = divmod(args.steps, G)
+    graphs = []
+    for count in ([G] if reps else []) + ([rem] if rem else []):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            for i in range(count):
+                step(i)
+        graphs.append(gr)
+    with torch.cuda.stream(stream):
+        graphs[0].replay()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(None)
+    sampler.start()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(reps):
+            graphs[0].replay()
+        if rem:
+            graphs[-1].replay()
+        end.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    ms = start.elapsed_time(end)
+    value = units * args.steps / (ms / 1e3)
+    peak, peak_src = hbm_peak()
+    esz = 2 if shape.dtype == "bf16" else 4
+    bytes_step = 7 * D * esz * units
+    achieved = bytes_step / (ms / 1e3 / args.steps) / 1e9
+    cpu = None
+    if not args.no_cpu_baseline:
+        run = oracle_backward_runner(shape)
+        run()
+        reps_c, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < args.cpu_seconds:
+            run()
+            reps_c += 1
+        el = time.perf_counter() - t0
+        cpu = {"value": reps_c * n / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": "%d repetitions of one (batch, head) slice (n=%d), double-precision oracle backward, "
+                         "%.1f s" % (reps_c, n, el)}
+    line = {
+        "metric": BWD_METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": shape.dtype,
+        "data": "synthetic (seeded N(0,1) inputs and upstream gradient; no dataset or weights)",
+        "config": dict(config_of(shape, sets=(R, R * set_bytes)), direction="backward"),
+        "clocks": clocks,
+        "gpu_launches": args.steps * 10,
+        "roofline": {"bound": "hbm", "kernel": "whole backward (10 kernels)", "achieved": achieved,
+                     "peak": peak, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                     "peak_source": peak_src, "bytes_per_step": bytes_step},
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    del keep
+
+
 def main():
     args = parse_args()
     from lisa_synth import SHAPES
     shape = SHAPES[args.workload]
     if args.impl == "reference":
         reference_arm(args, shape)
+    elif args.direction == "backward":
+        backward_arm(args, shape)
     else:
         ours_arm(args, shape)
 

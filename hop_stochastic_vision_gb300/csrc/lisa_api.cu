@@ -439,8 +439,8 @@ constexpr int kBwdTokensPerBlock = 32;   // per-token kernels: 8 warps x 4 token
 struct BwdPlan {
     Plan fwd;   // SIMT statistics partials (s, K^T V, K^T Q~) and s
     int nh, nblk;
-    size_t off_mred, off_uk, off_ubar, off_dub, off_lstat, off_dalp, off_dsp, off_dm, off_du1, off_dsr,
-        off_dals, off_dkp;
+    size_t off_mred, off_uk, off_ubar, off_ubart, off_dub, off_lstat, off_dalp, off_dsp, off_dm, off_du1,
+        off_dmt, off_du1t, off_dsr, off_dals, off_dkp;
     size_t total;
 };
 
@@ -457,12 +457,15 @@ BwdPlan make_bwd_plan(int slices, int n, int D, int T, int dtype) {
     b.off_mred = off;  off = align_up(off + S * dd * sizeof(float));
     b.off_uk = off;    off = align_up(off + S * b.nh * dd * sizeof(float));
     b.off_ubar = off;  off = align_up(off + S * dd * sizeof(float));
+    b.off_ubart = off; off = align_up(off + S * dd * sizeof(float));
     b.off_dub = off;   off = align_up(off + S * C * dd * sizeof(float));
     b.off_lstat = off; off = align_up(off + S * (size_t)n * 4 * sizeof(float));
     b.off_dalp = off;  off = align_up(off + S * b.nblk * sizeof(float));
     b.off_dsp = off;   off = align_up(off + S * b.nblk * d * sizeof(float));
     b.off_dm = off;    off = align_up(off + S * dd * sizeof(float));
     b.off_du1 = off;   off = align_up(off + S * dd * sizeof(float));
+    b.off_dmt = off;   off = align_up(off + S * dd * sizeof(float));
+    b.off_du1t = off;  off = align_up(off + S * dd * sizeof(float));
     b.off_dsr = off;   off = align_up(off + S * d * sizeof(float));
     b.off_dals = off;  off = align_up(off + S * sizeof(float));
     b.off_dkp = off;   off = align_up(off + S * (size_t)n * d * sizeof(float));
@@ -540,12 +543,15 @@ extern "C" lisa_status lisa_backward(const void *Q, const void *K, const void *V
     b.Mred = reinterpret_cast<float *>(ws + pl.off_mred);
     b.Uk = reinterpret_cast<float *>(ws + pl.off_uk);
     b.Ubar = reinterpret_cast<float *>(ws + pl.off_ubar);
+    b.UbarT = reinterpret_cast<float *>(ws + pl.off_ubart);
     b.dub_part = reinterpret_cast<float *>(ws + pl.off_dub);
     b.lstat = reinterpret_cast<float *>(ws + pl.off_lstat);
     b.dal_part = reinterpret_cast<float *>(ws + pl.off_dalp);
     b.ds_part = reinterpret_cast<float *>(ws + pl.off_dsp);
     b.dM = reinterpret_cast<float *>(ws + pl.off_dm);
     b.dU1 = reinterpret_cast<float *>(ws + pl.off_du1);
+    b.dMT = reinterpret_cast<float *>(ws + pl.off_dmt);
+    b.dU1T = reinterpret_cast<float *>(ws + pl.off_du1t);
     b.ds_red = reinterpret_cast<float *>(ws + pl.off_dsr);
     b.dal_slice = reinterpret_cast<float *>(ws + pl.off_dals);
     b.dk_part = reinterpret_cast<float *>(ws + pl.off_dkp);

@@ -26,8 +26,9 @@
 //   3. bwd_token_a    warp per token: window softmax max / sum, dl_i . l_i,
 //                     dalpha terms (per-block partial sums)
 //   4. bwd_recur_back per slice: reduce dUbar; G_k; dM, dU_1 (or the solve)
-//   5. bwd_token_b    warp per token: dXq, dV, the ds terms (per-block
-//                     partial sums) and dK without ds (fp32, workspace)
+//   5. bwd_token_b    per block of 32 tokens: the d x d products from shared
+//                     memory, then a warp per token: dXq, dV, the ds terms
+//                     (per-block sums), dK without ds (fp32, workspace)
 //   6. bwd_reduce     per slice: ds and the slice's dalpha
 //   7. bwd_finish_k   warp per token: dXk = (dK + ds) [Xk > 0]
 //   8. bwd_dalpha     dalpha per head = sum over the batch
@@ -87,7 +88,7 @@ __global__ void __launch_bounds__(kThreads) bwd_recur(BwdProblem b) {
         p.s_red[(size_t)sl * D + tid] = acc;
     }
     __syncthreads();
-    float *Uk = b.Uk + (size_t)sl * b.nh * D * D;
+    float *Uk = b.Uk + (size_t)sl * b.nh * D * D;   // transposed: Uk[c][a] = U_k[a][c]
     float ub[EPT];
     if (p.untruncated) {
         // A = I - beta M stored by columns in Un, R = U_1 by columns in M
@@ -104,14 +105,14 @@ __global__ void __launch_bounds__(kThreads) bwd_recur(BwdProblem b) {
 #pragma unroll
         for (int x = 0; x < EPT; ++x) {
             const int idx = tid + x * kThreads;
-            Uk[idx] = U[idx / D][idx % D];
+            Uk[idx] = U[idx % D][idx / D];
             ub[x] = p.beta * (1.f - p.beta) * U[idx / D][idx % D];
         }
     } else {
 #pragma unroll
         for (int x = 0; x < EPT; ++x) {
             const int idx = tid + x * kThreads;
-            Uk[idx] = U[idx / D][idx % D];
+            Uk[idx] = U[idx % D][idx / D];
             ub[x] = p.T > 1 ? p.w[1] * U[idx / D][idx % D] : 0.f;
         }
         for (int k = 2; k < p.T; ++k) {
@@ -127,14 +128,19 @@ __global__ void __launch_bounds__(kThreads) bwd_recur(BwdProblem b) {
                 const int idx = tid + x * kThreads;
                 const float u = Un[idx / D][idx % D];
                 U[idx / D][idx % D] = u;
-                Uk[(size_t)(k - 1) * D * D + idx] = u;
                 ub[x] = fmaf(p.w[k], u, ub[x]);
             }
             __syncthreads();
+            for (int idx = tid; idx < D * D; idx += kThreads)
+                Uk[(size_t)(k - 1) * D * D + idx] = U[idx % D][idx / D];
         }
     }
 #pragma unroll
-    for (int x = 0; x < EPT; ++x) b.Ubar[(size_t)sl * D * D + tid + x * kThreads] = ub[x];
+    for (int x = 0; x < EPT; ++x) {
+        const int idx = tid + x * kThreads;
+        b.Ubar[(size_t)sl * D * D + idx] = ub[x];
+        b.UbarT[(size_t)sl * D * D + (idx % D) * D + idx / D] = ub[x];
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -142,8 +148,7 @@ __global__ void __launch_bounds__(kThreads) bwd_recur(BwdProblem b) {
 // ---------------------------------------------------------------------------
 template <typename TIn, int D>
 __global__ void __launch_bounds__(kThreads) bwd_stats_dub(BwdProblem b) {
-    constexpr int EPT = D * D / kThreads;
-    constexpr int PER_ROW = D / EPT;
+    constexpr int RB = D / 16;   // each thread: an RB x RB block of the D x D result
     __shared__ float Qs[kTile][D];
     __shared__ float Gs[kTile][D];
     __shared__ float s[D];
@@ -156,10 +161,12 @@ __global__ void __launch_bounds__(kThreads) bwd_stats_dub(BwdProblem b) {
     const TIn *Q = static_cast<const TIn *>(p.Q) + (size_t)sl * p.n * D;
     const TIn *dO = static_cast<const TIn *>(b.dO) + (size_t)sl * p.n * D;
     const float al = p.alpha[sl % p.heads];
-    const int a = tid / PER_ROW, e0 = (tid % PER_ROW) * EPT;
-    float acc[EPT];
+    const int a0 = (tid / 16) * RB, e0 = (tid % 16) * RB;
+    float acc[RB][RB];
 #pragma unroll
-    for (int x = 0; x < EPT; ++x) acc[x] = 0.f;
+    for (int r = 0; r < RB; ++r)
+#pragma unroll
+        for (int x = 0; x < RB; ++x) acc[r][x] = 0.f;
     for (int base = t0; base < t1; base += kTile) {
         const int cnt = min(kTile, t1 - base);
         for (int idx = tid; idx < kTile * D; idx += kThreads) {
@@ -182,15 +189,24 @@ __global__ void __launch_bounds__(kThreads) bwd_stats_dub(BwdProblem b) {
         }
         __syncthreads();
         for (int j = 0; j < cnt; ++j) {
-            const float qa = Qs[j][a];
+            float ra[RB], rb[RB];
 #pragma unroll
-            for (int x = 0; x < EPT; ++x) acc[x] = fmaf(qa, Gs[j][e0 + x], acc[x]);
+            for (int r = 0; r < RB; ++r) {
+                ra[r] = Qs[j][a0 + r];
+                rb[r] = Gs[j][e0 + r];
+            }
+#pragma unroll
+            for (int r = 0; r < RB; ++r)
+#pragma unroll
+                for (int x = 0; x < RB; ++x) acc[r][x] = fmaf(ra[r], rb[x], acc[r][x]);
         }
         __syncthreads();
     }
     float *out = b.dub_part + ((size_t)sl * p.chunks + c) * D * D;
 #pragma unroll
-    for (int x = 0; x < EPT; ++x) out[a * D + e0 + x] = acc[x];
+    for (int r = 0; r < RB; ++r)
+#pragma unroll
+        for (int x = 0; x < RB; ++x) out[(a0 + r) * D + e0 + x] = acc[r][x];
 }
 
 // In-grid 3x3 window of token i on the H x W grid (the token itself first
@@ -205,6 +221,16 @@ __device__ __forceinline__ int window(int i, int H, int W, int (&nb)[9]) {
             nb[cnt++] = rr * W + cc;
         }
     return cnt;
+}
+
+// Warp sums of n independent per-lane partials, the butterflies interleaved so
+// their shuffle latencies overlap.
+template <int N>
+__device__ __forceinline__ void warp_sum_n(float (&x)[N]) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int t = 0; t < N; ++t) x[t] += __shfl_xor_sync(0xffffffffu, x[t], o);
 }
 
 // Lane l holds channels l and l + 32 (those below D).
@@ -267,26 +293,34 @@ __global__ void __launch_bounds__(kThreads) bwd_token_a(BwdProblem b) {
         }
 #pragma unroll
         for (int t = 0; t < NC; ++t) g[t] = fmaf(rq, g[t], w0 * v[t]);
-        // local window
+        // local window: every neighbour row loaded, then the nine scores reduced together
         int nb[9];
         const int cnt = window(i, p.H, p.W, nb);
-        float e[9], emax = -INFINITY;
-        for (int t9 = 0; t9 < cnt; ++t9) {
-            float kr[NC];
-            load_row<TIn, D>(K + (size_t)nb[t9] * D, kr, lane, p.relu);
-            e[t9] = dot_row<D>(q, kr) * scale;
-            emax = fmaxf(emax, e[t9]);
+        float kr[9][NC], vr[9][NC], e[9];
+#pragma unroll
+        for (int t9 = 0; t9 < 9; ++t9) {
+            const int row = t9 < cnt ? nb[t9] : i;
+            load_row<TIn, D>(K + (size_t)row * D, kr[t9], lane, p.relu);
+            load_row<TIn, D>(V + (size_t)row * D, vr[t9], lane, 0);
+            e[t9] = 0.f;
+#pragma unroll
+            for (int t = 0; t < NC; ++t) e[t9] = fmaf(q[t], kr[t9][t], e[t9]);
         }
+        warp_sum_n(e);
+        float emax = -INFINITY;
+#pragma unroll
+        for (int t9 = 0; t9 < 9; ++t9)
+            if (t9 < cnt) emax = fmaxf(emax, e[t9] * scale);
         float l[NC], esum = 0.f;
 #pragma unroll
         for (int t = 0; t < NC; ++t) l[t] = 0.f;
-        for (int t9 = 0; t9 < cnt; ++t9) {
-            const float a = expf(e[t9] - emax);
-            esum += a;
-            float vr[NC];
-            load_row<TIn, D>(V + (size_t)nb[t9] * D, vr, lane, 0);
 #pragma unroll
-            for (int t = 0; t < NC; ++t) l[t] = fmaf(a, vr[t], l[t]);
+        for (int t9 = 0; t9 < 9; ++t9) {
+            if (t9 >= cnt) break;
+            const float a = expf(e[t9] * scale - emax);
+            esum += a;
+#pragma unroll
+            for (int t = 0; t < NC; ++t) l[t] = fmaf(a, vr[t9][t], l[t]);
         }
         const float inv = 1.f / esum;
         float dgl = 0.f, dll = 0.f;
@@ -296,8 +330,10 @@ __global__ void __launch_bounds__(kThreads) bwd_token_a(BwdProblem b) {
             dgl = fmaf(go[t], g[t] - l[t], dgl);
             dll = fmaf(go[t], l[t], dll);
         }
-        dgl = warp_sum(dgl);
-        dll = warp_sum(dll) * (1.f - al);
+        float red[2] = {dgl, dll};
+        warp_sum_n(red);
+        dgl = red[0];
+        dll = red[1] * (1.f - al);
         dal += dgl;
         if (lane == 0)
             reinterpret_cast<float4 *>(b.lstat)[(size_t)sl * p.n + i] = make_float4(emax, esum, dll, 0.f);
@@ -333,7 +369,7 @@ __global__ void __launch_bounds__(kThreads) bwd_recur_back(BwdProblem b) {
         M[idx / D][idx % D] = b.Mred[(size_t)sl * D * D + idx];
     }
     float *dM = b.dM + (size_t)sl * D * D, *dU1 = b.dU1 + (size_t)sl * D * D;
-    const float *Uk = b.Uk + (size_t)sl * b.nh * D * D;
+    const float *Uk = b.Uk + (size_t)sl * b.nh * D * D;   // transposed
     __syncthreads();
     if (p.untruncated) {
         // (I - beta M)^T Y = beta (1-beta) dUbar: A' = (I - beta M)^T by
@@ -354,8 +390,10 @@ __global__ void __launch_bounds__(kThreads) bwd_recur_back(BwdProblem b) {
             const int a = idx / D, c = idx % D;
             dU1[idx] = X[c][a];
             float acc = 0.f;
-            for (int e = 0; e < D; ++e) acc = fmaf(X[e][a], Uk[(size_t)c * D + e], acc);
+            for (int e = 0; e < D; ++e) acc = fmaf(X[e][a], Uk[(size_t)e * D + c], acc);
             dM[idx] = p.beta * acc;
+            b.dMT[(size_t)sl * D * D + c * D + a] = p.beta * acc;
+            b.dU1T[(size_t)sl * D * D + c * D + a] = X[c][a];
         }
         return;
     }
@@ -377,7 +415,7 @@ __global__ void __launch_bounds__(kThreads) bwd_recur_back(BwdProblem b) {
                 const int idx = tid + x * kThreads;
                 const int a = idx / D, c = idx % D;
                 float acc = 0.f;
-                for (int e = 0; e < D; ++e) acc = fmaf(G[a][e], Up[(size_t)c * D + e], acc);
+                for (int e = 0; e < D; ++e) acc = fmaf(G[a][e], Up[(size_t)e * D + c], acc);
                 dm[x] += acc;
             }
 #pragma unroll
@@ -400,22 +438,45 @@ __global__ void __launch_bounds__(kThreads) bwd_recur_back(BwdProblem b) {
 #pragma unroll
     for (int x = 0; x < EPT; ++x) {
         const int idx = tid + x * kThreads;
+        const int a = idx / D, c = idx % D;
+        const float u1 = p.T > 1 ? G[a][c] : 0.f;
         dM[idx] = dm[x];
-        dU1[idx] = p.T > 1 ? G[idx / D][idx % D] : 0.f;
+        dU1[idx] = u1;
+        b.dMT[(size_t)sl * D * D + c * D + a] = dm[x];
+        b.dU1T[(size_t)sl * D * D + c * D + a] = u1;
     }
 }
 
 // ---------------------------------------------------------------------------
 // 5. per token j: dXq_j, dV_j, the ds terms -c_j Q_j (per-block sums), and
-// dK_j without ds (fp32).
+// dK_j without ds (fp32).  The block's kTpb tokens first go through the three
+// d x d products together, from shared memory:
+//   dQ~_j = alpha dO_j Ubar^T + K_j dM,  dV_j = w_0 alpha dO_j + K_j dU_1,
+//   dK_j  = V_j dU_1^T + Q~_j dM^T
+// (thread: 4 channels x the tokens of its group), then one warp per token
+// takes the normaliser, the window and the stores.
 // ---------------------------------------------------------------------------
+constexpr int kTpb = 32;   // tokens per block of the per-token kernels
+
+template <int D>
+constexpr int token_b_smem_floats() { return 5 * D * D + 7 * kTpb * D; }
+
 template <typename TIn, int D>
 __global__ void __launch_bounds__(kThreads) bwd_token_b(BwdProblem b) {
     constexpr int NC = (D + 31) / 32;
+    constexpr int CG = D / 4;                    // channel groups of 4
+    constexpr int TG = kThreads / CG;            // token groups
+    extern __shared__ float4 smem_b[];
+    float *UbT = reinterpret_cast<float *>(smem_b);
+    float *dMs = UbT + D * D, *dU1s = dMs + D * D, *dU1T = dU1s + D * D, *dMT = dU1T + D * D;
+    float *Qr = dMT + D * D, *Gr = Qr + kTpb * D, *Kr = Gr + kTpb * D, *Vr = Kr + kTpb * D;
+    float *oQ = Vr + kTpb * D, *oV = oQ + kTpb * D, *oK = oV + kTpb * D;
+    __shared__ float rqs[kTpb];
     __shared__ float dsw[kWarps][D];
     const Problem &p = b.fwd;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int sl = blockIdx.x / b.nblk, blk = blockIdx.x % b.nblk;
+    const int j0 = blk * kTpb, cnt = min(kTpb, p.n - j0);
     const size_t sbase = (size_t)sl * p.n * D;
     const TIn *Q = static_cast<const TIn *>(p.Q) + sbase;
     const TIn *K = static_cast<const TIn *>(p.K) + sbase;
@@ -426,51 +487,100 @@ __global__ void __launch_bounds__(kThreads) bwd_token_b(BwdProblem b) {
     float *dKp = b.dk_part + sbase;
     const float4 *lst = reinterpret_cast<const float4 *>(b.lstat) + (size_t)sl * p.n;
     const float *s = p.s_red + (size_t)sl * D;
-    const float *Ub = b.Ubar + (size_t)sl * D * D;
-    const float *dM = b.dM + (size_t)sl * D * D, *dU1 = b.dU1 + (size_t)sl * D * D;
     const float al = p.alpha[sl % p.heads], w0 = p.w[0];
     const float scale = rsqrtf((float)D);
+
+    // ---- stage the slice's matrices and the block's token rows
+    {
+        const size_t mo = (size_t)sl * D * D / 4;
+        const float4 *src[5] = {reinterpret_cast<const float4 *>(b.UbarT) + mo,
+                                reinterpret_cast<const float4 *>(b.dM) + mo,
+                                reinterpret_cast<const float4 *>(b.dU1) + mo,
+                                reinterpret_cast<const float4 *>(b.dU1T) + mo,
+                                reinterpret_cast<const float4 *>(b.dMT) + mo};
+#pragma unroll
+        for (int m = 0; m < 5; ++m)
+            for (int x = tid; x < D * D / 4; x += kThreads) smem_b[m * D * D / 4 + x] = src[m][x];
+    }
+    for (int x = tid; x < kTpb * D; x += kThreads) {
+        const int j = x / D, ch = x % D;
+        float q = 0.f, g = 0.f, k = 0.f, v = 0.f;
+        if (j < cnt) {
+            const size_t o = (size_t)(j0 + j) * D + ch;
+            q = relu_if(ld(Q + o), p.relu);
+            g = ld(dO + o);
+            k = relu_if(ld(K + o), p.relu);
+            v = ld(V + o);
+        }
+        Qr[x] = q;
+        Gr[x] = g;
+        Kr[x] = k;
+        Vr[x] = v;
+    }
+    __syncthreads();
+    for (int j = warp; j < kTpb; j += kWarps) {   // 1 / (Q_j . s + eps)
+        float d = 0.f;
+        for (int ch = lane; ch < D; ch += 32) d += Qr[j * D + ch] * s[ch];
+        d = warp_sum(d);
+        if (lane == 0) rqs[j] = 1.f / (d + p.eps);
+    }
+    __syncthreads();
+
+    // ---- the three products: thread = channels 4 cg .. 4 cg + 3 of tokens tg, tg + TG, ...
+    {
+        const int cg = tid % CG, tg = tid / CG;
+        for (int j = tg; j < kTpb; j += TG) {
+            float4 dq = make_float4(0.f, 0.f, 0.f, 0.f), dv = dq, dk = dq;
+            const float rq = rqs[j];
+            for (int c = 0; c < D; ++c) {
+                const float go = al * Gr[j * D + c], kc = Kr[j * D + c], vc = Vr[j * D + c];
+                const float qc = Qr[j * D + c] * rq;
+                const float4 ub = reinterpret_cast<const float4 *>(UbT + c * D)[cg];
+                const float4 dm = reinterpret_cast<const float4 *>(dMs + c * D)[cg];
+                const float4 du = reinterpret_cast<const float4 *>(dU1s + c * D)[cg];
+                const float4 duT = reinterpret_cast<const float4 *>(dU1T + c * D)[cg];
+                const float4 dmT = reinterpret_cast<const float4 *>(dMT + c * D)[cg];
+                dq.x = fmaf(go, ub.x, fmaf(kc, dm.x, dq.x));
+                dq.y = fmaf(go, ub.y, fmaf(kc, dm.y, dq.y));
+                dq.z = fmaf(go, ub.z, fmaf(kc, dm.z, dq.z));
+                dq.w = fmaf(go, ub.w, fmaf(kc, dm.w, dq.w));
+                dv.x = fmaf(kc, du.x, dv.x);
+                dv.y = fmaf(kc, du.y, dv.y);
+                dv.z = fmaf(kc, du.z, dv.z);
+                dv.w = fmaf(kc, du.w, dv.w);
+                dk.x = fmaf(vc, duT.x, fmaf(qc, dmT.x, dk.x));
+                dk.y = fmaf(vc, duT.y, fmaf(qc, dmT.y, dk.y));
+                dk.z = fmaf(vc, duT.z, fmaf(qc, dmT.z, dk.z));
+                dk.w = fmaf(vc, duT.w, fmaf(qc, dmT.w, dk.w));
+            }
+            reinterpret_cast<float4 *>(oQ + j * D)[cg] = dq;
+            reinterpret_cast<float4 *>(oV + j * D)[cg] = dv;
+            reinterpret_cast<float4 *>(oK + j * D)[cg] = dk;
+        }
+    }
+    __syncthreads();
+
+    // ---- one warp per token: normaliser, window, stores
     float ds[NC];
 #pragma unroll
     for (int t = 0; t < NC; ++t) ds[t] = 0.f;
-    for (int u = warp; u < b.tpb; u += kWarps) {
-        const int j = blk * b.tpb + u;
-        if (j >= p.n) break;
-        float q[NC], k[NC], v[NC], go[NC], sv[NC];
-        load_row<TIn, D>(Q + (size_t)j * D, q, lane, p.relu);
-        load_row<TIn, D>(K + (size_t)j * D, k, lane, p.relu);
-        load_row<TIn, D>(V + (size_t)j * D, v, lane, 0);
-        load_row<TIn, D>(dO + (size_t)j * D, go, lane, 0);
-#pragma unroll
-        for (int t = 0; t < NC; ++t) sv[t] = lane + 32 * t < D ? s[lane + 32 * t] : 0.f;
-        const float rq = 1.f / (dot_row<D>(q, sv) + p.eps);
-        // dQ~_j[a] = alpha sum_e dO_j[e] Ubar[a][e] + sum_c dM[c][a] K_j[c]
-        // dV_j[e]  = w_0 alpha dO_j[e] + sum_a dU_1[a][e] K_j[a]
-        // dK_j[a]  = sum_e dU_1[a][e] V_j[e] + sum_c dM[a][c] Q~_j[c]
-        float dqt[NC], dv[NC], dk[NC];
+    for (int u = warp; u < cnt; u += kWarps) {
+        const int j = j0 + u;
+        float q[NC], k[NC], v[NC], go[NC], sv[NC], dqt[NC], dv[NC], dk[NC];
 #pragma unroll
         for (int t = 0; t < NC; ++t) {
-            dqt[t] = 0.f;
-            dv[t] = w0 * al * go[t];
-            dk[t] = 0.f;
+            const int ch = lane + 32 * t;
+            const bool in = ch < D;
+            q[t] = in ? Qr[u * D + ch] : 0.f;
+            k[t] = in ? Kr[u * D + ch] : 0.f;
+            v[t] = in ? Vr[u * D + ch] : 0.f;
+            go[t] = in ? Gr[u * D + ch] : 0.f;
+            sv[t] = in ? s[ch] : 0.f;
+            dqt[t] = in ? oQ[u * D + ch] : 0.f;
+            dv[t] = in ? fmaf(w0 * al, go[t], oV[u * D + ch]) : 0.f;
+            dk[t] = in ? oK[u * D + ch] : 0.f;
         }
-        for (int c = 0; c < D; ++c) {
-            const float gc = __shfl_sync(0xffffffffu, go[c / 32], c % 32);
-            const float kc = __shfl_sync(0xffffffffu, k[c / 32], c % 32);
-            const float vc = __shfl_sync(0xffffffffu, v[c / 32], c % 32);
-            const float qc = __shfl_sync(0xffffffffu, q[c / 32], c % 32) * rq;
-#pragma unroll
-            for (int t = 0; t < NC; ++t) {
-                const int a = lane + 32 * t;
-                if (a < D) {
-                    dqt[t] = fmaf(al * gc, Ub[(size_t)a * D + c], dqt[t]);
-                    dqt[t] = fmaf(kc, dM[(size_t)c * D + a], dqt[t]);
-                    dv[t] = fmaf(kc, dU1[(size_t)c * D + a], dv[t]);
-                    dk[t] = fmaf(vc, dU1[(size_t)a * D + c], dk[t]);
-                    dk[t] = fmaf(qc, dM[(size_t)a * D + c], dk[t]);
-                }
-            }
-        }
+        const float rq = rqs[u];
         // through Q~ = Q / r:  c_j = (dQ~_j . Q_j) / r_j^2
         const float cj = dot_row<D>(dqt, q) * rq * rq;
         float dq[NC];
@@ -479,35 +589,63 @@ __global__ void __launch_bounds__(kThreads) bwd_token_b(BwdProblem b) {
             dq[t] = dqt[t] * rq - cj * sv[t];
             ds[t] = fmaf(-cj, q[t], ds[t]);
         }
-        // local window: j as the query (its own softmax row) ...
+        // local window: j as the query (its own softmax row) and as a key /
+        // value of each neighbour i's row (N is symmetric).  All neighbour
+        // rows are loaded first; the 36 dot products are reduced together.
         int nb[9];
-        const int cnt = window(j, p.H, p.W, nb);
+        const int nn = window(j, p.H, p.W, nb);
         const float4 sj = lst[j];
         const float izj = 1.f / sj.y;
-        for (int t9 = 0; t9 < cnt; ++t9) {
-            float kr[NC], vr[NC];
-            load_row<TIn, D>(K + (size_t)nb[t9] * D, kr, lane, p.relu);
-            load_row<TIn, D>(V + (size_t)nb[t9] * D, vr, lane, 0);
-            const float a = expf(dot_row<D>(q, kr) * scale - sj.x) * izj;
-            const float dlv = dot_row<D>(go, vr) * (1.f - al);
-            const float de = a * (dlv - sj.z) * scale;
+        {
+            float kr[9][NC], vr[9][NC], d1[18];
 #pragma unroll
-            for (int t = 0; t < NC; ++t) dq[t] = fmaf(de, kr[t], dq[t]);
+            for (int t9 = 0; t9 < 9; ++t9) {
+                const int row = t9 < nn ? nb[t9] : j;
+                load_row<TIn, D>(K + (size_t)row * D, kr[t9], lane, p.relu);
+                load_row<TIn, D>(V + (size_t)row * D, vr[t9], lane, 0);
+                d1[t9] = d1[9 + t9] = 0.f;
+#pragma unroll
+                for (int t = 0; t < NC; ++t) {
+                    d1[t9] = fmaf(q[t], kr[t9][t], d1[t9]);
+                    d1[9 + t9] = fmaf(go[t], vr[t9][t], d1[9 + t9]);
+                }
+            }
+            warp_sum_n(d1);
+#pragma unroll
+            for (int t9 = 0; t9 < 9; ++t9) {
+                if (t9 >= nn) break;
+                const float a = expf(d1[t9] * scale - sj.x) * izj;
+                const float de = a * (d1[9 + t9] * (1.f - al) - sj.z) * scale;
+#pragma unroll
+                for (int t = 0; t < NC; ++t) dq[t] = fmaf(de, kr[t9][t], dq[t]);
+            }
         }
-        // ... and j as a key / value of each neighbour i's row (N is symmetric)
-        for (int t9 = 0; t9 < cnt; ++t9) {
-            const int i = nb[t9];
-            float qi[NC], gi[NC];
-            load_row<TIn, D>(Q + (size_t)i * D, qi, lane, p.relu);
-            load_row<TIn, D>(dO + (size_t)i * D, gi, lane, 0);
-            const float4 si = lst[i];
-            const float a = expf(dot_row<D>(qi, k) * scale - si.x) / si.y;
-            const float dlv = dot_row<D>(gi, v) * (1.f - al);
-            const float de = a * (dlv - si.z) * scale;
+        {
+            float qi[9][NC], gi[9][NC], d2[18];
 #pragma unroll
-            for (int t = 0; t < NC; ++t) {
-                dv[t] = fmaf(a * (1.f - al), gi[t], dv[t]);
-                dk[t] = fmaf(de, qi[t], dk[t]);
+            for (int t9 = 0; t9 < 9; ++t9) {
+                const int row = t9 < nn ? nb[t9] : j;
+                load_row<TIn, D>(Q + (size_t)row * D, qi[t9], lane, p.relu);
+                load_row<TIn, D>(dO + (size_t)row * D, gi[t9], lane, 0);
+                d2[t9] = d2[9 + t9] = 0.f;
+#pragma unroll
+                for (int t = 0; t < NC; ++t) {
+                    d2[t9] = fmaf(qi[t9][t], k[t], d2[t9]);
+                    d2[9 + t9] = fmaf(gi[t9][t], v[t], d2[9 + t9]);
+                }
+            }
+            warp_sum_n(d2);
+#pragma unroll
+            for (int t9 = 0; t9 < 9; ++t9) {
+                if (t9 >= nn) break;
+                const float4 si = lst[nb[t9]];
+                const float a = expf(d2[t9] * scale - si.x) / si.y;
+                const float de = a * (d2[9 + t9] * (1.f - al) - si.z) * scale;
+#pragma unroll
+                for (int t = 0; t < NC; ++t) {
+                    dv[t] = fmaf(a * (1.f - al), gi[t9][t], dv[t]);
+                    dk[t] = fmaf(de, qi[t9][t], dk[t]);
+                }
             }
         }
 #pragma unroll
@@ -525,7 +663,7 @@ __global__ void __launch_bounds__(kThreads) bwd_token_b(BwdProblem b) {
     for (int t = 0; t < NC; ++t)
         if (lane + 32 * t < D) dsw[warp][lane + 32 * t] = ds[t];
     __syncthreads();
-    for (int ch = threadIdx.x; ch < D; ch += kThreads) {
+    for (int ch = tid; ch < D; ch += kThreads) {
         float acc = 0.f;
         for (int w = 0; w < kWarps; ++w) acc += dsw[w][ch];
         b.ds_part[((size_t)sl * b.nblk + blk) * D + ch] = acc;
@@ -584,6 +722,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dalpha(BwdProblem b) {
 template <typename TIn, int D>
 cudaError_t launch_bwd_all(const BwdProblem &b, cudaStream_t st) {
     const Problem &p = b.fwd;
+    if (b.tpb != kTpb) return cudaErrorInvalidValue;   // the plan's blocks are kTpb tokens
     cudaError_t err = launch_simt(p, st, 0);   // partial s, K^T V
     if (err != cudaSuccess) return err;
     if ((err = launch_simt(p, st, 1)) != cudaSuccess) return err;   // partial K^T Q~
@@ -593,7 +732,11 @@ cudaError_t launch_bwd_all(const BwdProblem &b, cudaStream_t st) {
     bwd_stats_dub<TIn, D><<<grid_stats, kThreads, 0, st>>>(b);
     bwd_token_a<TIn, D><<<grid_tok, kThreads, 0, st>>>(b);
     bwd_recur_back<D><<<p.slices, kThreads, 0, st>>>(b);
-    bwd_token_b<TIn, D><<<grid_tok, kThreads, 0, st>>>(b);
+    constexpr int smem_b = token_b_smem_floats<D>() * (int)sizeof(float);
+    if ((err = cudaFuncSetAttribute(bwd_token_b<TIn, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_b)) !=
+        cudaSuccess)
+        return err;
+    bwd_token_b<TIn, D><<<grid_tok, kThreads, smem_b, st>>>(b);
     bwd_reduce<D><<<p.slices, kThreads, 0, st>>>(b);
     const long long total = (long long)p.slices * p.n * D;
     long long blocks = (total + kThreads - 1) / kThreads;

@@ -43,12 +43,11 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 // ---------------------------------------------------------------------------
 // 1. partial s and U_1 = K^T V over one chunk of one slice.
-// Thread t owns U entries (a, e0 .. e0+EPT-1), EPT = D*D/256.
+// Thread t owns a (D/16) x (D/16) block of U (rows a0.., columns e0..).
 // ---------------------------------------------------------------------------
 template <typename TIn, int D>
 __global__ void __launch_bounds__(kThreads) stats_kv_kernel(Problem p) {
-    constexpr int EPT = D * D / kThreads;
-    constexpr int PER_ROW = D / EPT;
+    constexpr int RB = D / 16;   // each thread: an RB x RB block of the D x D result
     __shared__ float Ks[kTile][D];
     __shared__ float Vs[kTile][D];
     const int c = blockIdx.x % p.chunks, sl = blockIdx.x / p.chunks, tid = threadIdx.x;
@@ -56,10 +55,12 @@ __global__ void __launch_bounds__(kThreads) stats_kv_kernel(Problem p) {
     const int t1 = min(p.n, t0 + p.chunk);
     const TIn *K = static_cast<const TIn *>(p.K) + (size_t)sl * p.n * D;
     const TIn *V = static_cast<const TIn *>(p.V) + (size_t)sl * p.n * D;
-    const int a = tid / PER_ROW, e0 = (tid % PER_ROW) * EPT;
-    float acc[EPT];
+    const int a0 = (tid / 16) * RB, e0 = (tid % 16) * RB;
+    float acc[RB][RB];
 #pragma unroll
-    for (int x = 0; x < EPT; ++x) acc[x] = 0.f;
+    for (int r = 0; r < RB; ++r)
+#pragma unroll
+        for (int x = 0; x < RB; ++x) acc[r][x] = 0.f;
     float ssum = 0.f;
     for (int base = t0; base < t1; base += kTile) {
         const int cnt = min(kTile, t1 - base);
@@ -75,9 +76,16 @@ __global__ void __launch_bounds__(kThreads) stats_kv_kernel(Problem p) {
         }
         __syncthreads();
         for (int j = 0; j < cnt; ++j) {
-            const float ka = Ks[j][a];
+            float ra[RB], rb[RB];
 #pragma unroll
-            for (int x = 0; x < EPT; ++x) acc[x] = fmaf(ka, Vs[j][e0 + x], acc[x]);
+            for (int r = 0; r < RB; ++r) {
+                ra[r] = Ks[j][a0 + r];
+                rb[r] = Vs[j][e0 + r];
+            }
+#pragma unroll
+            for (int r = 0; r < RB; ++r)
+#pragma unroll
+                for (int x = 0; x < RB; ++x) acc[r][x] = fmaf(ra[r], rb[x], acc[r][x]);
         }
         if (tid < D)
             for (int j = 0; j < cnt; ++j) ssum += Ks[j][tid];
@@ -86,7 +94,9 @@ __global__ void __launch_bounds__(kThreads) stats_kv_kernel(Problem p) {
     const size_t pc = (size_t)sl * p.chunks + c;
     float *U = p.u_part + pc * D * D;
 #pragma unroll
-    for (int x = 0; x < EPT; ++x) U[a * D + e0 + x] = acc[x];
+    for (int r = 0; r < RB; ++r)
+#pragma unroll
+        for (int x = 0; x < RB; ++x) U[(a0 + r) * D + e0 + x] = acc[r][x];
     if (tid < D) p.s_part[pc * D + tid] = ssum;
 }
 
@@ -95,8 +105,7 @@ __global__ void __launch_bounds__(kThreads) stats_kv_kernel(Problem p) {
 // ---------------------------------------------------------------------------
 template <typename TIn, int D>
 __global__ void __launch_bounds__(kThreads) stats_kq_kernel(Problem p) {
-    constexpr int EPT = D * D / kThreads;
-    constexpr int PER_ROW = D / EPT;
+    constexpr int RB = D / 16;   // each thread: an RB x RB block of the D x D result
     __shared__ float Ks[kTile][D];
     __shared__ float Qs[kTile][D];
     __shared__ float s[D];
@@ -112,10 +121,12 @@ __global__ void __launch_bounds__(kThreads) stats_kq_kernel(Problem p) {
     const int t1 = min(p.n, t0 + p.chunk);
     const TIn *Q = static_cast<const TIn *>(p.Q) + (size_t)sl * p.n * D;
     const TIn *K = static_cast<const TIn *>(p.K) + (size_t)sl * p.n * D;
-    const int a = tid / PER_ROW, e0 = (tid % PER_ROW) * EPT;
-    float acc[EPT];
+    const int a0 = (tid / 16) * RB, e0 = (tid % 16) * RB;
+    float acc[RB][RB];
 #pragma unroll
-    for (int x = 0; x < EPT; ++x) acc[x] = 0.f;
+    for (int r = 0; r < RB; ++r)
+#pragma unroll
+        for (int x = 0; x < RB; ++x) acc[r][x] = 0.f;
     for (int base = t0; base < t1; base += kTile) {
         const int cnt = min(kTile, t1 - base);
         for (int idx = tid; idx < kTile * D; idx += kThreads) {
@@ -140,15 +151,24 @@ __global__ void __launch_bounds__(kThreads) stats_kq_kernel(Problem p) {
         }
         __syncthreads();
         for (int j = 0; j < cnt; ++j) {
-            const float ka = Ks[j][a];
+            float ra[RB], rb[RB];
 #pragma unroll
-            for (int x = 0; x < EPT; ++x) acc[x] = fmaf(ka, Qs[j][e0 + x], acc[x]);
+            for (int r = 0; r < RB; ++r) {
+                ra[r] = Ks[j][a0 + r];
+                rb[r] = Qs[j][e0 + r];
+            }
+#pragma unroll
+            for (int r = 0; r < RB; ++r)
+#pragma unroll
+                for (int x = 0; x < RB; ++x) acc[r][x] = fmaf(ra[r], rb[x], acc[r][x]);
         }
         __syncthreads();
     }
     float *M = p.m_part + ((size_t)sl * p.chunks + c) * D * D;
 #pragma unroll
-    for (int x = 0; x < EPT; ++x) M[a * D + e0 + x] = acc[x];
+    for (int r = 0; r < RB; ++r)
+#pragma unroll
+        for (int x = 0; x < RB; ++x) M[(a0 + r) * D + e0 + x] = acc[r][x];
 }
 
 // ---------------------------------------------------------------------------
