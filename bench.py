@@ -166,12 +166,19 @@ def hbm_peak():
         return 6800.0, "fallback"
 
 
+# The files the tensor-core forward kernels are built from (the kernels whose
+# DRAM traffic profiles/traffic.json records): a change to any of them voids
+# the recorded counters; other kernels' sources do not.
+TRAFFIC_SOURCES = ("hop_stochastic_vision_gb300/csrc/lisa_tc.cu", "hop_stochastic_vision_gb300/csrc/lisa_sm100.cuh",
+                   "hop_stochastic_vision_gb300/csrc/lisa_solve.cuh",
+                   "hop_stochastic_vision_gb300/csrc/lisa_internal.h", "include/lisa.h")
+
+
 def source_hash() -> str:
     h = hashlib.sha256()
-    pkg = os.path.join(ROOT, "hop_stochastic_vision_gb300", "csrc")
-    for p in sorted(glob.glob(os.path.join(pkg, "*")) + glob.glob(os.path.join(ROOT, "include", "*.h"))):
-        with open(p, "rb") as f:
-            h.update(os.path.basename(p).encode() + b"\0" + f.read())
+    for rel in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(os.path.basename(rel).encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
