@@ -28,7 +28,6 @@ from __future__ import annotations
 
 import argparse
 import csv
-import glob
 import hashlib
 import io
 import json

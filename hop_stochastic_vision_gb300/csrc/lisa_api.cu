@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 
 #include "lisa.h"
+#include "lisa_bwd.h"
 #include "lisa_internal.h"
 
 namespace lisa {
@@ -440,7 +441,7 @@ struct BwdPlan {
     Plan fwd;   // SIMT statistics partials (s, K^T V, K^T Q~) and s
     int nh, nblk;
     size_t off_mred, off_uk, off_ubar, off_ubart, off_dub, off_lstat, off_dalp, off_dsp, off_dm, off_du1,
-        off_dmt, off_du1t, off_dsr, off_dals, off_dkp;
+        off_dmt, off_du1t, off_dsr, off_dals, off_dkp, off_bimg;
     size_t total;
 };
 
@@ -469,6 +470,7 @@ BwdPlan make_bwd_plan(int slices, int n, int D, int T, int dtype) {
     b.off_dsr = off;   off = align_up(off + S * d * sizeof(float));
     b.off_dals = off;  off = align_up(off + S * sizeof(float));
     b.off_dkp = off;   off = align_up(off + S * (size_t)n * d * sizeof(float));
+    b.off_bimg = off;  off = align_up(off + S * 5 * dd * sizeof(uint16_t));
     b.total = off;
     return b;
 }
@@ -555,5 +557,6 @@ extern "C" lisa_status lisa_backward(const void *Q, const void *K, const void *V
     b.ds_red = reinterpret_cast<float *>(ws + pl.off_dsr);
     b.dal_slice = reinterpret_cast<float *>(ws + pl.off_dals);
     b.dk_part = reinterpret_cast<float *>(ws + pl.off_dkp);
+    b.bimg = reinterpret_cast<uint16_t *>(ws + pl.off_bimg);
     return launch_bwd(b, cs) == cudaSuccess ? LISA_OK : LISA_ERR_CUDA;
 }

@@ -27,8 +27,9 @@
 //                     dalpha terms (per-block partial sums)
 //   4. bwd_recur_back per slice: reduce dUbar; G_k; dM, dU_1 (or the solve)
 //   5. bwd_token_b    per block of 32 tokens: the d x d products from shared
-//                     memory, then a warp per token: dXq, dV, the ds terms
-//                     (per-block sums), dK without ds (fp32, workspace)
+//                     memory (bf16, d = 64: on the tensor cores, from a bf16
+//                     operand image built by bwd_bimg), then a warp per token:
+//                     dXq, dV, the ds terms (per-block sums), dK without ds
 //   6. bwd_reduce     per slice: ds and the slice's dalpha
 //   7. bwd_finish_k   warp per token: dXk = (dK + ds) [Xk > 0]
 //   8. bwd_dalpha     dalpha per head = sum over the batch
@@ -37,7 +38,11 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
+#include "lisa_bwd.h"
 #include "lisa_internal.h"
+#include "lisa_sm100.cuh"
 #include "lisa_solve.cuh"
 
 namespace lisa {
@@ -671,6 +676,237 @@ __global__ void __launch_bounds__(kThreads) bwd_token_b(BwdProblem b) {
 }
 
 // ---------------------------------------------------------------------------
+// 5'. bf16, d = 64: the same per-token gradients with the three d x d
+// products on the tensor cores (mma.sync m16n8k16, bf16 operands, fp32
+// accumulation):
+//   dQ~ = [dO | K] [alpha Ubar^T ; dM],  dK = [V | Q~] [dU_1^T ; dM^T],  dV = K dU_1
+// The B operands come from a bf16 image built once per slice (bwd_bimg); Q~
+// is rounded to bf16 as an operand, the inputs are bf16 already.
+// ---------------------------------------------------------------------------
+constexpr int kImgRows = 5 * 64;   // [alpha Ubar^T; dM; dU_1^T; dM^T; dU_1], 64 columns each
+constexpr int kBS = 72;            // B-image row stride in shared memory, bf16 (144 B: ldmatrix conflict-free)
+constexpr int kAS = 136;           // A row stride, bf16 (272 B)
+constexpr int kTcSmemBytes = kImgRows * kBS * 2 + 2 * kTpb * kAS * 2 + kTpb * 64 * 2 + 3 * kTpb * 64 * 4;
+
+__global__ void __launch_bounds__(kThreads) bwd_bimg(BwdProblem b) {
+    const int sl = blockIdx.x;
+    const float al = b.fwd.alpha[sl % b.fwd.heads];
+    const size_t mo = (size_t)sl * 64 * 64;
+    const float *src[5] = {b.UbarT + mo, b.dM + mo, b.dU1T + mo, b.dMT + mo, b.dU1 + mo};
+    __nv_bfloat16 *img = reinterpret_cast<__nv_bfloat16 *>(b.bimg) + (size_t)sl * kImgRows * 64;
+    for (int x = threadIdx.x; x < kImgRows * 64; x += kThreads) {
+        const int m = x / (64 * 64), r = x % (64 * 64);
+        img[x] = __float2bfloat16_rn(m == 0 ? al * src[0][r] : src[m][r]);
+    }
+}
+
+__device__ __forceinline__ uint32_t relu_bf16x2(uint32_t v) {
+    __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162 *>(&v);
+    x = __hmax2(x, __float2bfloat162_rn(0.f));
+    return *reinterpret_cast<uint32_t *>(&x);
+}
+
+__global__ void __launch_bounds__(kThreads) bwd_token_b_tc(BwdProblem b) {
+    constexpr int D = 64, NC = 2;
+    using namespace sm100;
+    extern __shared__ float4 smem_tc[];
+    __nv_bfloat16 *Bs = reinterpret_cast<__nv_bfloat16 *>(smem_tc);
+    __nv_bfloat16 *A1 = Bs + kImgRows * kBS;   // [dO | K] rows
+    __nv_bfloat16 *A3 = A1 + kTpb * kAS;       // [V | Q~] rows
+    __nv_bfloat16 *Qb = A3 + kTpb * kAS;       // Q rows (feature-mapped)
+    float *oQ = reinterpret_cast<float *>(Qb + kTpb * D), *oV = oQ + kTpb * D, *oK = oV + kTpb * D;
+    __shared__ float rqs[kTpb];
+    __shared__ float dsw[kWarps][D];
+    const Problem &p = b.fwd;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int sl = blockIdx.x / b.nblk, blk = blockIdx.x % b.nblk;
+    const int j0 = blk * kTpb, cnt = min(kTpb, p.n - j0);
+    const size_t sbase = (size_t)sl * p.n * D;
+    const __nv_bfloat16 *Q = static_cast<const __nv_bfloat16 *>(p.Q) + sbase;
+    const __nv_bfloat16 *K = static_cast<const __nv_bfloat16 *>(p.K) + sbase;
+    const __nv_bfloat16 *V = static_cast<const __nv_bfloat16 *>(p.V) + sbase;
+    const __nv_bfloat16 *dO = static_cast<const __nv_bfloat16 *>(b.dO) + sbase;
+    __nv_bfloat16 *dQo = static_cast<__nv_bfloat16 *>(b.dQ) + sbase;
+    __nv_bfloat16 *dVo = static_cast<__nv_bfloat16 *>(b.dV) + sbase;
+    float *dKp = b.dk_part + sbase;
+    const float4 *lst = reinterpret_cast<const float4 *>(b.lstat) + (size_t)sl * p.n;
+    const float *s = p.s_red + (size_t)sl * D;
+    const float al = p.alpha[sl % p.heads], w0 = p.w[0];
+    const float scale = rsqrtf((float)D);
+
+    // ---- stage the B image and the block's rows (16-byte pieces)
+    {
+        const uint4 *img = reinterpret_cast<const uint4 *>(b.bimg + (size_t)sl * kImgRows * D);
+        for (int x = tid; x < kImgRows * 8; x += kThreads)
+            *reinterpret_cast<uint4 *>(Bs + (x >> 3) * kBS + (x & 7) * 8) = img[x];
+    }
+    for (int x = tid; x < kTpb * 8; x += kThreads) {
+        const int j = x >> 3, c = x & 7;
+        uint4 g = make_uint4(0, 0, 0, 0), k = g, v = g, q = g;
+        if (j < cnt) {
+            const size_t o = ((size_t)(j0 + j) * D) / 8 + c;
+            g = reinterpret_cast<const uint4 *>(dO)[o];
+            k = reinterpret_cast<const uint4 *>(K)[o];
+            v = reinterpret_cast<const uint4 *>(V)[o];
+            q = reinterpret_cast<const uint4 *>(Q)[o];
+            if (p.relu) {
+                k = make_uint4(relu_bf16x2(k.x), relu_bf16x2(k.y), relu_bf16x2(k.z), relu_bf16x2(k.w));
+                q = make_uint4(relu_bf16x2(q.x), relu_bf16x2(q.y), relu_bf16x2(q.z), relu_bf16x2(q.w));
+            }
+        }
+        *reinterpret_cast<uint4 *>(A1 + j * kAS + c * 8) = g;
+        *reinterpret_cast<uint4 *>(A1 + j * kAS + 64 + c * 8) = k;
+        *reinterpret_cast<uint4 *>(A3 + j * kAS + c * 8) = v;
+        *reinterpret_cast<uint4 *>(Qb + j * D + c * 8) = q;
+    }
+    __syncthreads();
+    for (int j = warp; j < kTpb; j += kWarps) {   // 1 / (Q_j . s + eps)
+        float d = 0.f;
+        for (int ch = lane; ch < D; ch += 32) d += __bfloat162float(Qb[j * D + ch]) * s[ch];
+        d = warp_sum(d);
+        if (lane == 0) rqs[j] = 1.f / (d + p.eps);
+    }
+    __syncthreads();
+    for (int x = tid; x < kTpb * D; x += kThreads) {   // Q~ half of A3, rounded to bf16
+        const int j = x / D, ch = x % D;
+        A3[j * kAS + 64 + ch] = __float2bfloat16_rn(__bfloat162float(Qb[j * D + ch]) * rqs[j]);
+    }
+    __syncthreads();
+
+    // ---- the three products: warp = 16 tokens (mt) x 16 columns (sb) of each
+    {
+        const int mt = warp & 1, sb = warp >> 1;
+        const uint32_t bs = smem_u32(Bs), a1 = smem_u32(A1), a3 = smem_u32(A3);
+        const int arow = 16 * mt + (lane & 15), acol = (lane >> 4) * 8;
+        const int mi = lane >> 3, brow = (mi & 1) * 8 + (lane & 7), bcol = 16 * sb + (mi >> 1) * 8;
+#pragma unroll
+        for (int pr = 0; pr < 3; ++pr) {
+            const uint32_t abase = (pr == 1 ? a3 : a1) + (uint32_t)(arow * kAS + (pr == 2 ? 64 : 0) + acol) * 2u;
+            const int brow0 = pr == 0 ? 0 : (pr == 1 ? 128 : 256);
+            const int ksteps = pr == 2 ? 4 : 8;
+            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            for (int ks = 0; ks < ksteps; ++ks) {
+                uint32_t a0, a1r, a2, a3r, b0, b1, b2, b3;
+                ldsm_x4(abase + (uint32_t)(16 * ks) * 2u, a0, a1r, a2, a3r);
+                ldsm_x4_t(bs + (uint32_t)((brow0 + 16 * ks + brow) * kBS + bcol) * 2u, b0, b1, b2, b3);
+                mma_bf16_16816(acc[0], a0, a1r, a2, a3r, b0, b1);
+                mma_bf16_16816(acc[1], a0, a1r, a2, a3r, b2, b3);
+            }
+            float *out = pr == 0 ? oQ : (pr == 1 ? oK : oV);
+            const int row = 16 * mt + (lane >> 2);
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int col = 16 * sb + 8 * nt + 2 * (lane & 3);
+                out[row * D + col] = acc[nt][0];
+                out[row * D + col + 1] = acc[nt][1];
+                out[(row + 8) * D + col] = acc[nt][2];
+                out[(row + 8) * D + col + 1] = acc[nt][3];
+            }
+        }
+    }
+    __syncthreads();
+
+    // ---- one warp per token: normaliser, window, stores (as in the SIMT kernel)
+    float ds[NC] = {0.f, 0.f};
+    for (int u = warp; u < cnt; u += kWarps) {
+        const int j = j0 + u;
+        float q[NC], k[NC], v[NC], go[NC], sv[NC], dqt[NC], dv[NC], dk[NC];
+#pragma unroll
+        for (int t = 0; t < NC; ++t) {
+            const int ch = lane + 32 * t;
+            q[t] = __bfloat162float(Qb[u * D + ch]);
+            go[t] = __bfloat162float(A1[u * kAS + ch]);
+            k[t] = __bfloat162float(A1[u * kAS + 64 + ch]);
+            v[t] = __bfloat162float(A3[u * kAS + ch]);
+            sv[t] = s[ch];
+            dqt[t] = oQ[u * D + ch];
+            dv[t] = fmaf(w0 * al, go[t], oV[u * D + ch]);
+            dk[t] = oK[u * D + ch];
+        }
+        const float rq = rqs[u];
+        const float cj = dot_row<D>(dqt, q) * rq * rq;
+        float dq[NC];
+#pragma unroll
+        for (int t = 0; t < NC; ++t) {
+            dq[t] = dqt[t] * rq - cj * sv[t];
+            ds[t] = fmaf(-cj, q[t], ds[t]);
+        }
+        int nb[9];
+        const int nn = window(j, p.H, p.W, nb);
+        const float4 sj = lst[j];
+        const float izj = 1.f / sj.y;
+        {
+            float kr[9][NC], vr[9][NC], d1[18];
+#pragma unroll
+            for (int t9 = 0; t9 < 9; ++t9) {
+                const int row = t9 < nn ? nb[t9] : j;
+                load_row<__nv_bfloat16, D>(K + (size_t)row * D, kr[t9], lane, p.relu);
+                load_row<__nv_bfloat16, D>(V + (size_t)row * D, vr[t9], lane, 0);
+                d1[t9] = d1[9 + t9] = 0.f;
+#pragma unroll
+                for (int t = 0; t < NC; ++t) {
+                    d1[t9] = fmaf(q[t], kr[t9][t], d1[t9]);
+                    d1[9 + t9] = fmaf(go[t], vr[t9][t], d1[9 + t9]);
+                }
+            }
+            warp_sum_n(d1);
+#pragma unroll
+            for (int t9 = 0; t9 < 9; ++t9) {
+                if (t9 >= nn) break;
+                const float a = expf(d1[t9] * scale - sj.x) * izj;
+                const float de = a * (d1[9 + t9] * (1.f - al) - sj.z) * scale;
+#pragma unroll
+                for (int t = 0; t < NC; ++t) dq[t] = fmaf(de, kr[t9][t], dq[t]);
+            }
+        }
+        {
+            float qi[9][NC], gi[9][NC], d2[18];
+#pragma unroll
+            for (int t9 = 0; t9 < 9; ++t9) {
+                const int row = t9 < nn ? nb[t9] : j;
+                load_row<__nv_bfloat16, D>(Q + (size_t)row * D, qi[t9], lane, p.relu);
+                load_row<__nv_bfloat16, D>(dO + (size_t)row * D, gi[t9], lane, 0);
+                d2[t9] = d2[9 + t9] = 0.f;
+#pragma unroll
+                for (int t = 0; t < NC; ++t) {
+                    d2[t9] = fmaf(qi[t9][t], k[t], d2[t9]);
+                    d2[9 + t9] = fmaf(gi[t9][t], v[t], d2[9 + t9]);
+                }
+            }
+            warp_sum_n(d2);
+#pragma unroll
+            for (int t9 = 0; t9 < 9; ++t9) {
+                if (t9 >= nn) break;
+                const float4 si = lst[nb[t9]];
+                const float a = expf(d2[t9] * scale - si.x) / si.y;
+                const float de = a * (d2[9 + t9] * (1.f - al) - si.z) * scale;
+#pragma unroll
+                for (int t = 0; t < NC; ++t) {
+                    dv[t] = fmaf(a * (1.f - al), gi[t9][t], dv[t]);
+                    dk[t] = fmaf(de, qi[t9][t], dk[t]);
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < NC; ++t) {
+            const int ch = lane + 32 * t;
+            const float xq = __bfloat162float(Q[(size_t)j * D + ch]);
+            dQo[(size_t)j * D + ch] = __float2bfloat16_rn((p.relu && !(xq > 0.f)) ? 0.f : dq[t]);
+            dVo[(size_t)j * D + ch] = __float2bfloat16_rn(dv[t]);
+            dKp[(size_t)j * D + ch] = dk[t];
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < NC; ++t) dsw[warp][lane + 32 * t] = ds[t];
+    __syncthreads();
+    for (int ch = tid; ch < D; ch += kThreads) {
+        float acc = 0.f;
+        for (int w = 0; w < kWarps; ++w) acc += dsw[w][ch];
+        b.ds_part[((size_t)sl * b.nblk + blk) * D + ch] = acc;
+    }
+}
+
+// ---------------------------------------------------------------------------
 // 6. per slice: ds = sum of the block partials; the slice's dalpha.
 // ---------------------------------------------------------------------------
 template <int D>
@@ -732,11 +968,19 @@ cudaError_t launch_bwd_all(const BwdProblem &b, cudaStream_t st) {
     bwd_stats_dub<TIn, D><<<grid_stats, kThreads, 0, st>>>(b);
     bwd_token_a<TIn, D><<<grid_tok, kThreads, 0, st>>>(b);
     bwd_recur_back<D><<<p.slices, kThreads, 0, st>>>(b);
-    constexpr int smem_b = token_b_smem_floats<D>() * (int)sizeof(float);
-    if ((err = cudaFuncSetAttribute(bwd_token_b<TIn, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_b)) !=
-        cudaSuccess)
-        return err;
-    bwd_token_b<TIn, D><<<grid_tok, kThreads, smem_b, st>>>(b);
+    if constexpr (std::is_same<TIn, __nv_bfloat16>::value && D == 64) {
+        bwd_bimg<<<p.slices, kThreads, 0, st>>>(b);
+        if ((err = cudaFuncSetAttribute(bwd_token_b_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        kTcSmemBytes)) != cudaSuccess)
+            return err;
+        bwd_token_b_tc<<<grid_tok, kThreads, kTcSmemBytes, st>>>(b);
+    } else {
+        constexpr int smem_b = token_b_smem_floats<D>() * (int)sizeof(float);
+        if ((err = cudaFuncSetAttribute(bwd_token_b<TIn, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        smem_b)) != cudaSuccess)
+            return err;
+        bwd_token_b<TIn, D><<<grid_tok, kThreads, smem_b, st>>>(b);
+    }
     bwd_reduce<D><<<p.slices, kThreads, 0, st>>>(b);
     const long long total = (long long)p.slices * p.n * D;
     long long blocks = (total + kThreads - 1) / kThreads;

@@ -1,0 +1,39 @@
+// lisa_bwd.h -- host-side problem of one lisa_backward call and its
+// launcher.  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+
+#include "lisa_internal.h"
+
+namespace lisa {
+
+// One lisa_backward call: the forward's problem (sizes, weights, inputs and
+// the statistics partials the forward's SIMT kernels fill) plus the
+// upstream gradient, the outputs and the backward's workspace views.
+struct BwdProblem {
+    Problem fwd;
+    const void *dO;
+    void *dQ, *dK, *dV;
+    float *dalpha;       // device [heads], overwritten
+    int tpb, nblk;       // tokens per block of the per-token kernels; blocks per slice
+    int nh;              // stored U_k matrices: max(T - 1, 1)
+    float *Mred;         // [S][D][D]      M = K^T Q~
+    float *Uk;           // [S][nh][D][D]  U_1 .. U_(T-1) (untruncated: Z), transposed
+    float *Ubar;         // [S][D][D]
+    float *UbarT;        // [S][D][D]      Ubar transposed
+    float *dub_part;     // [S][C][D][D]   partial dUbar
+    float *lstat;        // [S][n][4]      window softmax max, sum, dl_i . l_i
+    float *dal_part;     // [S][nblk]
+    float *ds_part;      // [S][nblk][D]
+    float *dM, *dU1;     // [S][D][D]
+    float *dMT, *dU1T;   // [S][D][D]      the same, transposed
+    uint16_t *bimg;      // [S][5 D][D] bf16: [alpha Ubar^T; dM; dU_1^T; dM^T; dU_1] (bf16, d = 64)
+    float *ds_red;       // [S][D]
+    float *dal_slice;    // [S]
+    float *dk_part;      // [S][n][D]      dK without ds, fp32
+};
+
+cudaError_t launch_bwd(const BwdProblem &b, cudaStream_t stream);
+
+}  // namespace lisa
