@@ -688,15 +688,17 @@ constexpr int kBS = 72;            // B-image row stride in shared memory, bf16 
 constexpr int kAS = 136;           // A row stride, bf16 (272 B)
 constexpr int kTcSmemBytes = kImgRows * kBS * 2 + 2 * kTpb * kAS * 2 + kTpb * 64 * 2 + 3 * kTpb * 64 * 4;
 
+// grid (slices, 5): block (sl, m) converts matrix m of slice sl, four floats per thread and step
 __global__ void __launch_bounds__(kThreads) bwd_bimg(BwdProblem b) {
-    const int sl = blockIdx.x;
-    const float al = b.fwd.alpha[sl % b.fwd.heads];
+    const int sl = blockIdx.x, m = blockIdx.y;
     const size_t mo = (size_t)sl * 64 * 64;
-    const float *src[5] = {b.UbarT + mo, b.dM + mo, b.dU1T + mo, b.dMT + mo, b.dU1 + mo};
-    __nv_bfloat16 *img = reinterpret_cast<__nv_bfloat16 *>(b.bimg) + (size_t)sl * kImgRows * 64;
-    for (int x = threadIdx.x; x < kImgRows * 64; x += kThreads) {
-        const int m = x / (64 * 64), r = x % (64 * 64);
-        img[x] = __float2bfloat16_rn(m == 0 ? al * src[0][r] : src[m][r]);
+    const float *srcs[5] = {b.UbarT, b.dM, b.dU1T, b.dMT, b.dU1};
+    const float4 *src = reinterpret_cast<const float4 *>(srcs[m] + mo);
+    const float f = m == 0 ? b.fwd.alpha[sl % b.fwd.heads] : 1.f;
+    uint2 *img = reinterpret_cast<uint2 *>(b.bimg + ((size_t)sl * kImgRows + (size_t)m * 64) * 64);
+    for (int x = threadIdx.x; x < 64 * 64 / 4; x += kThreads) {
+        const float4 v = src[x];
+        img[x] = make_uint2(sm100::pack_bf16(f * v.x, f * v.y), sm100::pack_bf16(f * v.z, f * v.w));
     }
 }
 
@@ -969,7 +971,7 @@ cudaError_t launch_bwd_all(const BwdProblem &b, cudaStream_t st) {
     bwd_token_a<TIn, D><<<grid_tok, kThreads, 0, st>>>(b);
     bwd_recur_back<D><<<p.slices, kThreads, 0, st>>>(b);
     if constexpr (std::is_same<TIn, __nv_bfloat16>::value && D == 64) {
-        bwd_bimg<<<p.slices, kThreads, 0, st>>>(b);
+        bwd_bimg<<<dim3((unsigned)p.slices, 5), kThreads, 0, st>>>(b);
         if ((err = cudaFuncSetAttribute(bwd_token_b_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         kTcSmemBytes)) != cudaSuccess)
             return err;
