@@ -68,7 +68,7 @@ def _load():
         lib.lisa_oracle_step_weights.argtypes = [dp, dp, i, i, i, dp, dp, dp, dp, i, i, dp]
         lib.lisa_oracle_step_weights.restype = i
         lib.lisa_oracle_backward.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, i, i, i, i, i, i, i, i, d,
-                                             dp, dp, d, i]
+                                             dp, dp, dp, dp, dp, i, dp, dp, dp, dp, dp, d, i]
         lib.lisa_oracle_backward.restype = i
         lib.lisa_oracle_max_threads.argtypes = []
         lib.lisa_oracle_max_threads.restype = i
@@ -151,10 +151,12 @@ def forward(xq, xk, v, grid, T, *, alpha, beta=None, w=None, mlp=None, eps=1e-6,
     return (O, G, L) if branches else O
 
 
-def backward(xq, xk, v, dO, grid, T, *, alpha, beta=None, w=None, eps=1e-6, relu=True):
-    """Gradients of the LiSA forward (fixed or geometric walk weights; T = 0
-    with ``beta`` is the untruncated walk) for the upstream gradient ``dO``:
-    returns (dXq, dXk, dV, dalpha), dalpha summed over the batch per head."""
+def backward(xq, xk, v, dO, grid, T, *, alpha, beta=None, w=None, mlp=None, eps=1e-6, relu=True):
+    """Gradients of the LiSA forward for the upstream gradient ``dO``:
+    returns (dXq, dXk, dV, dalpha), dalpha summed over the batch per head.
+    Weights as for ``forward`` (T = 0 with ``beta``: the untruncated walk).
+    With ``mlp`` = (W1, b1, W2, b2) it returns a fifth item, (dW1, db1, dW2,
+    db2), the parameter gradients summed over every slice."""
     xq, xk, v, dO = _f64(xq), _f64(xk), _f64(v), _f64(dO)
     B, heads, n, dh = xq.shape
     dv = v.shape[3]
@@ -162,22 +164,35 @@ def backward(xq, xk, v, dO, grid, T, *, alpha, beta=None, w=None, eps=1e-6, relu
     if H * W != n or dO.shape != v.shape or xk.shape != xq.shape:
         raise ValueError("bad shapes")
     alpha = np.broadcast_to(np.asarray(alpha, dtype=np.float64), (heads,)).copy()
+    W1 = b1 = W2 = b2 = gW1 = gb1 = gW2 = gb2 = None
+    hidden = 0
     if w is not None:
         wmode, wv = W_FIXED, _f64(w)
         if T == 0 or wv.shape != (T,):
             raise ValueError("fixed weights need length T >= 1")
+    elif mlp is not None:
+        wmode, wv = W_MLP, None
+        W1, b1, W2, b2 = (_f64(x) for x in mlp)
+        hidden = W1.shape[0]
+        if T < 1 or W1.shape != (hidden, 2 * dh) or b1.shape != (hidden,) or W2.shape != (T, hidden) or \
+                b2.shape != (T,):
+            raise ValueError("bad MLP parameter shapes")
+        gW1, gb1, gW2, gb2 = np.empty_like(W1), np.empty_like(b1), np.empty_like(W2), np.empty_like(b2)
     elif beta is not None:
         wmode, wv = W_GEOMETRIC, None
     else:
-        raise ValueError("give beta or w")
+        raise ValueError("give beta, w or mlp")
     dXq, dXk, dV = np.empty_like(xq), np.empty_like(xk), np.empty_like(v)
     da = np.empty(heads)
     rc = _load().lisa_oracle_backward(
         _ptr(xq), _ptr(xk), _ptr(v), _ptr(dO), _ptr(dXq), _ptr(dXk), _ptr(dV), _ptr(da), B, heads, H, W,
-        dh, dv, int(T), wmode, float(beta if beta is not None else 0.0), _ptr(wv), _ptr(alpha), float(eps),
+        dh, dv, int(T), wmode, float(beta if beta is not None else 0.0), _ptr(wv), _ptr(W1), _ptr(b1),
+        _ptr(W2), _ptr(b2), hidden, _ptr(gW1), _ptr(gb1), _ptr(gW2), _ptr(gb2), _ptr(alpha), float(eps),
         int(bool(relu)))
     if rc != 0:
         raise ValueError("lisa_oracle_backward failed with code %d" % rc)
+    if mlp is not None:
+        return dXq, dXk, dV, da, (gW1, gb1, gW2, gb2)
     return dXq, dXk, dV, da
 
 

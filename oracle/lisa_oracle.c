@@ -541,9 +541,166 @@ int lisa_oracle_forward(const double *Xq, const double *Xk, const double *V,
 /*   so with A = I - beta M and dZ = beta (1-beta) dUbar:                   */
 /*   dU_1 = A^-T dZ,  dM = beta (A^-T dZ) Z^T, and w_0 = 1 - beta.           */
 /* ---------------------------------------------------------------------- */
+/* GELU (exact erf form) and its derivative 0.5 (1 + erf(a/sqrt 2)) + a phi(a). */
+static double gelu_erf_grad(double a)
+{
+    const double pi = 3.14159265358979323846;
+    return 0.5 * (1.0 + erf(a / sqrt(2.0))) + a * exp(-0.5 * a * a) / sqrt(2.0 * pi);
+}
+
+/* ---------------------------------------------------------------------- */
+/* Global branch of the backward pass with the adaptive (per-token) walk    */
+/* weights [note §2.4] (paper Eq. 10, Supp. Sec. 8).  Forward, per token i: */
+/*   x_i = [q_i; k_i], a_i = W1 x_i + b1, h_i = GELU(a_i), z_i = W2 h_i + b2,*/
+/*   w_i = softmax(z_i),  g_i = w_i0 V_i + sum_{k>=1} w_ik Y_k,i,            */
+/*   Y_k = Q~ U_k.  Backward, with dg = alpha dO:                           */
+/*   dw_ik = dg_i . Y_k,i (Y_0 = V);  dz_i = w_i (dw_i - w_i . dw_i);       */
+/*   dW2 += dz_i h_i^T, db2 += dz_i;  da_i = (W2^T dz_i) GELU'(a_i);        */
+/*   dW1 += da_i x_i^T, db1 += da_i;  [dq_i; dk_i] += W1^T da_i  (the MLP's */
+/*   share of the feature gradients);                                       */
+/*   dV_i = w_i0 dg_i;  dQ~_i = sum_{k>=1} w_ik dg_i U_k^T;                 */
+/*   dU_k = sum_i Q~_i (w_ik dg_i)^T;  G_(T-1) = dU_(T-1),                  */
+/*   G_k = dU_k + M^T G_(k+1), dM = sum_{k>=2} G_k U_(k-1)^T, dU_1 = G_1.   */
+/* Writes g, dV, dQ~, dM, dU_1, the MLP's feature gradients dqm, dkm, and   */
+/* adds the parameter gradients into dW1, db1, dW2, db2.                    */
+/* ---------------------------------------------------------------------- */
+static int mlp_walk_backward(const slice_args *A, const double *Q, const double *K, const double *Qt,
+                             const double *V, const double *dO, double alpha, const double *M,
+                             const double *Uk, double *g, double *dV, double *dQt, double *dM,
+                             double *dU1, double *dqm, double *dkm, double *dW1, double *db1,
+                             double *dW2, double *db2)
+{
+    const int n = A->H * A->W, dh = A->dh, dv = A->dv, T = A->T, hid = A->hidden;
+    const size_t dd = (size_t)dh * dv;
+    double *wt = malloc(sizeof(double) * (size_t)n * T), *pre = malloc(sizeof(double) * (size_t)n * hid);
+    double *hh = malloc(sizeof(double) * (size_t)n * hid), *dUk = calloc((size_t)(T > 1 ? T - 1 : 1) * dd, sizeof(double));
+    double *G = malloc(sizeof(double) * (size_t)(T > 1 ? T - 1 : 1) * dd);
+    double *Y = malloc(sizeof(double) * (size_t)T * dv), *dw = malloc(sizeof(double) * (size_t)T);
+    double *dz = malloc(sizeof(double) * (size_t)T), *da = malloc(sizeof(double) * (size_t)hid);
+    int err = 0;
+    if (!wt || !pre || !hh || !dUk || !G || !Y || !dw || !dz || !da) {
+        err = 2;
+        goto out;
+    }
+    for (int i = 0; i < n; ++i) {
+        const double *q = Q + (long)i * dh, *k = K + (long)i * dh;
+        /* forward through the MLP, keeping the pre-activations */
+        for (int m = 0; m < hid; ++m) {
+            const double *row = A->W1 + (long)m * 2 * dh;
+            double acc = A->b1[m];
+            for (int c = 0; c < dh; ++c) acc += row[c] * q[c] + row[dh + c] * k[c];
+            pre[(long)i * hid + m] = acc;
+            hh[(long)i * hid + m] = gelu_erf(acc);
+        }
+        double zmax = -INFINITY, zs = 0.0;
+        double *w = wt + (long)i * T;
+        for (int t = 0; t < T; ++t) {
+            double acc = A->b2[t];
+            for (int m = 0; m < hid; ++m) acc += A->W2[(long)t * hid + m] * hh[(long)i * hid + m];
+            w[t] = acc;
+            if (acc > zmax) zmax = acc;
+        }
+        for (int t = 0; t < T; ++t) {
+            w[t] = exp(w[t] - zmax);
+            zs += w[t];
+        }
+        for (int t = 0; t < T; ++t) w[t] /= zs;
+        /* walk terms Y_k,i and the token's global value */
+        for (int e = 0; e < dv; ++e) Y[e] = V[(long)i * dv + e];
+        for (int kk = 1; kk < T; ++kk)
+            for (int e = 0; e < dv; ++e) {
+                double acc = 0.0;
+                for (int a = 0; a < dh; ++a) acc += Qt[(long)i * dh + a] * Uk[(size_t)(kk - 1) * dd + a * dv + e];
+                Y[(size_t)kk * dv + e] = acc;
+            }
+        for (int e = 0; e < dv; ++e) {
+            double acc = 0.0;
+            for (int t = 0; t < T; ++t) acc += w[t] * Y[(size_t)t * dv + e];
+            g[(long)i * dv + e] = acc;
+        }
+        /* weights: dw, dz through the softmax */
+        double wdw = 0.0;
+        for (int t = 0; t < T; ++t) {
+            double acc = 0.0;
+            for (int e = 0; e < dv; ++e) acc += alpha * dO[(long)i * dv + e] * Y[(size_t)t * dv + e];
+            dw[t] = acc;
+            wdw += w[t] * acc;
+        }
+        for (int t = 0; t < T; ++t) dz[t] = w[t] * (dw[t] - wdw);
+        /* MLP parameters and inputs */
+        for (int t = 0; t < T; ++t) {
+            db2[t] += dz[t];
+            for (int m = 0; m < hid; ++m) dW2[(long)t * hid + m] += dz[t] * hh[(long)i * hid + m];
+        }
+        for (int m = 0; m < hid; ++m) {
+            double acc = 0.0;
+            for (int t = 0; t < T; ++t) acc += A->W2[(long)t * hid + m] * dz[t];
+            da[m] = acc * gelu_erf_grad(pre[(long)i * hid + m]);
+            db1[m] += da[m];
+            for (int c = 0; c < dh; ++c) {
+                dW1[(long)m * 2 * dh + c] += da[m] * q[c];
+                dW1[(long)m * 2 * dh + dh + c] += da[m] * k[c];
+            }
+        }
+        for (int c = 0; c < dh; ++c) {
+            double aq = 0.0, ak = 0.0;
+            for (int m = 0; m < hid; ++m) {
+                aq += A->W1[(long)m * 2 * dh + c] * da[m];
+                ak += A->W1[(long)m * 2 * dh + dh + c] * da[m];
+            }
+            dqm[(long)i * dh + c] = aq;
+            dkm[(long)i * dh + c] = ak;
+        }
+        /* the walk terms */
+        for (int e = 0; e < dv; ++e) dV[(long)i * dv + e] = w[0] * alpha * dO[(long)i * dv + e];
+        for (int a = 0; a < dh; ++a) {
+            double acc = 0.0;
+            for (int kk = 1; kk < T; ++kk)
+                for (int e = 0; e < dv; ++e)
+                    acc += w[kk] * alpha * dO[(long)i * dv + e] * Uk[(size_t)(kk - 1) * dd + a * dv + e];
+            dQt[(long)i * dh + a] = acc;
+        }
+        for (int kk = 1; kk < T; ++kk)
+            for (int a = 0; a < dh; ++a)
+                for (int e = 0; e < dv; ++e)
+                    dUk[(size_t)(kk - 1) * dd + a * dv + e] += Qt[(long)i * dh + a] * w[kk] * alpha * dO[(long)i * dv + e];
+    }
+    memset(dM, 0, sizeof(double) * dh * dh);
+    memset(dU1, 0, sizeof(double) * dd);
+    if (T > 1) {
+        for (int kk = T - 1; kk >= 1; --kk) {
+            double *Gk = G + (size_t)(kk - 1) * dd;
+            memcpy(Gk, dUk + (size_t)(kk - 1) * dd, sizeof(double) * dd);
+            if (kk < T - 1) {
+                const double *Gn = G + (size_t)kk * dd;
+                for (int a = 0; a < dh; ++a)
+                    for (int e = 0; e < dv; ++e) {
+                        double acc = 0.0;
+                        for (int b = 0; b < dh; ++b) acc += M[b * dh + a] * Gn[b * dv + e];
+                        Gk[a * dv + e] += acc;
+                    }
+            }
+        }
+        for (int kk = 2; kk < T; ++kk) {
+            const double *Gk = G + (size_t)(kk - 1) * dd, *Up = Uk + (size_t)(kk - 2) * dd;
+            for (int a = 0; a < dh; ++a)
+                for (int b = 0; b < dh; ++b) {
+                    double acc = 0.0;
+                    for (int e = 0; e < dv; ++e) acc += Gk[a * dv + e] * Up[b * dv + e];
+                    dM[a * dh + b] += acc;
+                }
+        }
+        memcpy(dU1, G, sizeof(double) * dd);
+    }
+out:
+    free(wt); free(pre); free(hh); free(dUk); free(G); free(Y); free(dw); free(dz); free(da);
+    return err;
+}
+
 static int backward_slice(const slice_args *A, const double *Xq, const double *Xk,
                           const double *V, const double *dO, double alpha,
-                          double *dXq, double *dXk, double *dV, double *dalpha)
+                          double *dXq, double *dXk, double *dV, double *dalpha,
+                          double *dW1, double *db1, double *dW2, double *db2)
 {
     const int H = A->H, W = A->W, n = H * W, dh = A->dh, dv = A->dv;
     const int T = A->T, nh = T == 0 ? 1 : (T > 1 ? T - 1 : 1);   /* stored U_k */
@@ -557,6 +714,8 @@ static int backward_slice(const slice_args *A, const double *Xq, const double *X
     double *g = malloc(sizeof(double) * nv), *l = malloc(sizeof(double) * nv);
     double *dQt = malloc(sizeof(double) * nd), *dQ = malloc(sizeof(double) * nd);
     double *dK = malloc(sizeof(double) * nd);
+    double *dqm = NULL, *dkm = NULL;   /* the MLP's share of dQ, dK (adaptive weights) */
+    const int mlp = A->wmode == ORACLE_W_MLP;
     double s[256], ds[256];
     const double scale = 1.0 / sqrt((double)dh);
     int err = 0;
@@ -587,7 +746,7 @@ static int backward_slice(const slice_args *A, const double *Xq, const double *X
             for (int j = 0; j < n; ++j) acc += K[(long)j * dh + a] * V[(long)j * dv + e];
             Uk[a * dv + e] = acc;
         }
-    const double w0 = T == 0 ? 1.0 - A->beta : A->w[0];
+    const double w0 = T == 0 ? 1.0 - A->beta : (mlp ? 0.0 : A->w[0]);
     memset(Ub, 0, sizeof(double) * dh * dv);
     if (T == 0) {
         /* Z = (I - beta M)^-1 U_1 into Uk[0]; Ubar = beta (1-beta) Z */
@@ -607,15 +766,26 @@ static int backward_slice(const slice_args *A, const double *Xq, const double *X
                         cur[a * dv + e] = acc;
                     }
             }
-            for (int t = 0; t < dh * dv; ++t) Ub[t] += A->w[k] * cur[t];
+            if (!mlp)
+                for (int t = 0; t < dh * dv; ++t) Ub[t] += A->w[k] * cur[t];
         }
     }
-    for (int i = 0; i < n; ++i)
-        for (int e = 0; e < dv; ++e) {
-            double acc = w0 * V[(long)i * dv + e];
-            for (int a = 0; a < dh; ++a) acc += Qt[(long)i * dh + a] * Ub[a * dv + e];
-            g[(long)i * dv + e] = acc;
-        }
+    if (mlp) {
+        /* per-token weights: g, dV, dQ~, dM, dU_1 and the MLP's gradients at once */
+        dqm = malloc(sizeof(double) * nd);
+        dkm = malloc(sizeof(double) * nd);
+        if (!dqm || !dkm) { err = 2; goto done; }
+        if ((err = mlp_walk_backward(A, Q, K, Qt, V, dO, alpha, M, Uk, g, dV, dQt, dM, dU1, dqm, dkm,
+                                     dW1, db1, dW2, db2)))
+            goto done;
+    } else {
+        for (int i = 0; i < n; ++i)
+            for (int e = 0; e < dv; ++e) {
+                double acc = w0 * V[(long)i * dv + e];
+                for (int a = 0; a < dh; ++a) acc += Qt[(long)i * dh + a] * Ub[a * dv + e];
+                g[(long)i * dv + e] = acc;
+            }
+    }
     local_branch(Q, K, V, H, W, dh, dv, l);
 
     /* ---- mix */
@@ -624,7 +794,8 @@ static int backward_slice(const slice_args *A, const double *Xq, const double *X
     *dalpha += da;
     /* dg = alpha dO, dl = (1-alpha) dO are formed where they are used */
 
-    /* ---- global branch */
+    /* ---- global branch (fixed weights; the adaptive ones were done above) */
+    if (mlp) goto stats_tail;
     for (size_t t = 0; t < nv; ++t) dV[t] = w0 * alpha * dO[t];
     for (int i = 0; i < n; ++i)   /* dQ~ = dg Ubar^T */
         for (int a = 0; a < dh; ++a) {
@@ -678,6 +849,7 @@ static int backward_slice(const slice_args *A, const double *Xq, const double *X
         }
         memcpy(dU1, G, sizeof(double) * dh * dv);
     }
+stats_tail:
     for (int j = 0; j < n; ++j) {
         for (int a = 0; a < dh; ++a) {
             double acc = 0.0;   /* dU_1 V_j + dM Q~_j */
@@ -708,6 +880,11 @@ static int backward_slice(const slice_args *A, const double *Xq, const double *X
     }
     for (int j = 0; j < n; ++j)
         for (int a = 0; a < dh; ++a) dK[(long)j * dh + a] += ds[a];
+    if (mlp)
+        for (size_t t = 0; t < nd; ++t) {
+            dQ[t] += dqm[t];
+            dK[t] += dkm[t];
+        }
 
     /* ---- local branch */
     for (int rr = 0; rr < H; ++rr)
@@ -759,6 +936,7 @@ static int backward_slice(const slice_args *A, const double *Xq, const double *X
 done:
     free(Q); free(K); free(Qt); free(r); free(M); free(Uk); free(Ub); free(dUb); free(G);
     free(dM); free(dU1); free(Amat); free(g); free(l); free(dQt); free(dQ); free(dK);
+    free(dqm); free(dkm);
     return err;
 }
 
@@ -766,22 +944,35 @@ done:
  * Backward pass of the layer over B x heads slices: dL/dXq, dL/dXk, dL/dV
  * ([B][heads][n][d], overwritten) and dL/dalpha ([heads], overwritten: the
  * sum over the batch) for the upstream gradient dO.  Walk weights as for
- * lisa_oracle_forward, geometric (T >= 1, or T = 0 untruncated) or fixed;
- * the adaptive (MLP) weights are not covered (returns 1).
+ * lisa_oracle_forward: geometric (T >= 1, or T = 0 untruncated), fixed, or
+ * adaptive (MLP; then dW1 [hidden][2 dh], db1 [hidden], dW2 [T][hidden], db2
+ * [T] are overwritten with the parameter gradients summed over every slice;
+ * they may be NULL otherwise).
  */
 int lisa_oracle_backward(const double *Xq, const double *Xk, const double *V,
                          const double *dO, double *dXq, double *dXk, double *dV,
                          double *dalpha, int B, int heads, int H, int W, int dh, int dv,
                          int T, int wmode, double beta, const double *w,
-                         const double *alpha, double eps, int relu_inputs)
+                         const double *W1, const double *b1, const double *W2,
+                         const double *b2, int hidden, double *dW1, double *db1,
+                         double *dW2, double *db2, const double *alpha, double eps,
+                         int relu_inputs)
 {
     if (B < 0 || heads < 1 || H < 1 || W < 1 || dh < 1 || dh > 256 || dv < 1 || T < 0 ||
         T > ORACLE_MAX_T || eps < 0.0 || !alpha)
         return 1;
-    if (wmode == ORACLE_W_MLP || (T == 0 && wmode != ORACLE_W_GEOMETRIC)) return 1;
-    double *wts = malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+    if (T == 0 && wmode != ORACLE_W_GEOMETRIC) return 1;
+    if (wmode == ORACLE_W_MLP && (T < 1 || !W1 || !b1 || !W2 || !b2 || hidden < 1 ||
+                                  hidden > ORACLE_MAX_HIDDEN || !dW1 || !db1 || !dW2 || !db2))
+        return 1;
+    double *wts = calloc((size_t)(T > 0 ? T : 1), sizeof(double));
     if (!wts) return 2;
-    if (T == 0) {
+    if (wmode == ORACLE_W_MLP) {
+        memset(dW1, 0, sizeof(double) * (size_t)hidden * 2 * dh);
+        memset(db1, 0, sizeof(double) * (size_t)hidden);
+        memset(dW2, 0, sizeof(double) * (size_t)T * hidden);
+        memset(db2, 0, sizeof(double) * (size_t)T);
+    } else if (T == 0) {
         if (!(beta >= 0.0 && beta < 1.0)) { free(wts); return 1; }
         wts[0] = 1.0 - beta;
     } else if (wmode == ORACLE_W_GEOMETRIC) {
@@ -790,15 +981,16 @@ int lisa_oracle_backward(const double *Xq, const double *Xk, const double *V,
         if (!w) { free(wts); return 1; }
         memcpy(wts, w, sizeof(double) * (size_t)T);
     }
-    slice_args A = {H, W, dh, dv, T, wmode, 0, ORACLE_LOWRANK, relu_inputs, eps, beta,
-                    wts, NULL, NULL, NULL, NULL};
+    slice_args A = {H, W, dh, dv, T, wmode, hidden, ORACLE_LOWRANK, relu_inputs, eps, beta,
+                    wts, W1, b1, W2, b2};
     const long n = (long)H * W;
     for (int h = 0; h < heads; ++h) dalpha[h] = 0.0;
     int err = 0;
     for (long sl = 0; sl < (long)B * heads; ++sl) {
         const long hq = sl * n * dh, hv = sl * n * dv;
         const int e = backward_slice(&A, Xq + hq, Xk + hq, V + hv, dO + hv, alpha[sl % heads],
-                                     dXq + hq, dXk + hq, dV + hv, dalpha + sl % heads);
+                                     dXq + hq, dXk + hq, dV + hv, dalpha + sl % heads, dW1, db1,
+                                     dW2, db2);
         if (e && !err) err = e;
     }
     free(wts);

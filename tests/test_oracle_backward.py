@@ -143,3 +143,89 @@ def test_backward_rejects_mlp_and_bad_args():
         oracle.backward(xq, xk, v, dO, (2, 2), 0, alpha=0.5, w=[1.0])
     with pytest.raises(ValueError):
         oracle.backward(xq, xk, v, dO, (2, 3), 3, alpha=0.5, beta=0.5)
+
+
+# -- adaptive (MLP) walk weights (note section 2.4; paper Eq. 10, Supp. Sec. 8) ----------
+
+def _mlp_params(d, T, hidden=6, seed=5):
+    r = np.random.default_rng(seed)
+    return (0.4 * r.standard_normal((hidden, 2 * d)), 0.3 * r.standard_normal(hidden),
+            0.5 * r.standard_normal((T, hidden)), 0.2 * r.standard_normal(T))
+
+
+@pytest.mark.parametrize("T", [1, 3, 4])
+def test_mlp_backward_matches_finite_differences(T):
+    grid, d = (3, 4), 5
+    xq, xk, v, dO = _case(1, 2, 3, 4, d)
+    mlp = _mlp_params(d, T)
+    alpha = np.array([0.3, 0.7])
+    gq, gk, gv, ga, gp = oracle.backward(xq, xk, v, dO, grid, T, alpha=alpha, mlp=mlp)
+    args = [xq, xk, v, alpha] + [np.array(x) for x in mlp]
+    grads = [gq, gk, gv, ga] + list(gp)
+
+    def loss():
+        return float((oracle.forward(args[0], args[1], args[2], grid, T, alpha=args[3],
+                                     mlp=tuple(args[4:])) * dO).sum())
+    h = 1e-6
+    for arr, grad in zip(args, grads):
+        num = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            keep = arr[idx]
+            arr[idx] = keep + h
+            up = loss()
+            arr[idx] = keep - h
+            dn = loss()
+            arr[idx] = keep
+            num[idx] = (up - dn) / (2 * h)
+        assert np.abs(num - grad).max() <= 1e-6 * max(np.abs(grad).max(), 1.0)
+
+
+def test_mlp_backward_matches_autograd_of_dense_layer():
+    grid, T, d = (4, 4), 3, 4
+    xq, xk, v, dO = _case(1, 1, 4, 4, d)
+    W1, b1, W2, b2 = _mlp_params(d, T, hidden=5, seed=9)
+    alpha = 0.6
+    gq, gk, gv, ga, (gW1, gb1, gW2, gb2) = oracle.backward(xq, xk, v, dO, grid, T, alpha=alpha,
+                                                           mlp=(W1, b1, W2, b2))
+    t = [torch.tensor(a[0, 0], requires_grad=True) for a in (xq, xk, v)]
+    tp = [torch.tensor(p, requires_grad=True) for p in (W1, b1, W2, b2)]
+    ta = torch.tensor(alpha, dtype=torch.float64, requires_grad=True)
+    q, k = torch.relu(t[0]), torch.relu(t[1])
+    hdn = torch.nn.functional.gelu(torch.cat([q, k], 1) @ tp[0].T + tp[1])   # exact erf GELU
+    w = torch.softmax(hdn @ tp[2].T + tp[3], dim=1)                          # [n, T]
+    s = k.sum(0)
+    qt = q / (q @ s + 1e-6)[:, None]
+    S = qt @ k.T
+    y, g = t[2], w[:, :1] * t[2]
+    for kk in range(1, T):
+        y = S @ y
+        g = g + w[:, kk:kk + 1] * y
+    n = 16
+    rr, cc = np.divmod(np.arange(n), 4)
+    near = (np.abs(rr[:, None] - rr[None, :]) <= 1) & (np.abs(cc[:, None] - cc[None, :]) <= 1)
+    e = ((q @ k.T) / np.sqrt(d)).masked_fill(torch.from_numpy(~near), float("-inf"))
+    out = ta * g + (1 - ta) * (torch.softmax(e, 1) @ t[2])
+    (out * torch.from_numpy(dO[0, 0])).sum().backward()
+    for got, ref in ((gq, t[0]), (gk, t[1]), (gv, t[2])):
+        np.testing.assert_allclose(got[0, 0], ref.grad.numpy(), rtol=0, atol=1e-10)
+    for got, ref in zip((gW1, gb1, gW2, gb2), tp):
+        np.testing.assert_allclose(got, ref.grad.numpy(), rtol=0, atol=1e-10)
+    assert abs(ga[0] - ta.grad.item()) <= 1e-10
+
+
+def test_mlp_backward_reduces_to_geometric():
+    """W2 = 0, b2 = log w_geo: every token gets the geometric weights, so the
+    adaptive route (per-token dU_k) gives the geometric backward's feature
+    gradients, and the MLP's share of them vanishes (W2^T dz = 0)."""
+    grid, T, d = (4, 5), 4, 6
+    xq, xk, v, dO = _case(2, 2, 4, 5, d)
+    wg = oracle.geometric_weights(0.5, T)
+    W1, b1, _, _ = _mlp_params(d, T)
+    mlp = (W1, b1, np.zeros((T, W1.shape[0])), np.log(wg))
+    a = oracle.backward(xq, xk, v, dO, grid, T, alpha=[0.3, 0.8], mlp=mlp)
+    b = oracle.backward(xq, xk, v, dO, grid, T, alpha=[0.3, 0.8], beta=0.5)
+    for x, y in zip(a[:4], b):
+        np.testing.assert_allclose(x, y, rtol=1e-11, atol=1e-12)
+    gW1, gb1, gW2, gb2 = a[4]
+    assert np.all(gW1 == 0) and np.all(gb1 == 0)
+    np.testing.assert_allclose(gb2.sum(), 0.0, atol=1e-12)     # softmax: dz sums to zero per token
