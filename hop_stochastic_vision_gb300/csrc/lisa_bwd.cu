@@ -31,7 +31,7 @@
 //                     operand image built by bwd_bimg), then a warp per token:
 //                     dXq, dV, the ds terms (per-block sums), dK without ds
 //   6. bwd_reduce     per slice: ds and the slice's dalpha
-//   7. bwd_finish_k   warp per token: dXk = (dK + ds) [Xk > 0]
+//   7. bwd_finish_k   one thread per element: dXk = (dK + ds) [Xk > 0]
 //   8. bwd_dalpha     dalpha per head = sum over the batch
 // Every reduction runs in a fixed order: the result does not depend on
 // scheduling.
