@@ -500,8 +500,11 @@ def oracle_backward_runner(shape, seed=0):
     dO = np.random.default_rng(seed).standard_normal(v.shape)
     alpha = inp["alpha"].double().numpy()
 
+    kw = {"beta": shape.beta} if shape.weights == "geometric" else \
+        {"mlp": tuple(inp[k].double().numpy() for k in ("W1", "b1", "W2", "b2"))}
+
     def run():
-        oracle.backward(xq, xk, v, dO, (shape.H, shape.W), shape.T, alpha=alpha, beta=shape.beta)
+        oracle.backward(xq, xk, v, dO, (shape.H, shape.W), shape.T, alpha=alpha, **kw)
     return run
 
 
@@ -519,8 +522,7 @@ def backward_arm(args, shape):
     rank, world, local = dist_env()
     if rank != 0:
         return
-    if shape.weights != "geometric":
-        raise SystemExit("the backward pass covers geometric and fixed walk weights")
+    mlp = shape.weights == "mlp"
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     lisa_build.build()
@@ -539,18 +541,31 @@ def backward_arm(args, shape):
         sets.append(st)
     alpha = inp["alpha"].to(dev)
     dalpha = torch.empty(heads, dtype=torch.float32, device=dev)
-    wt, keep = lisa.make_weights(T, beta=shape.beta)
     dt = lisa.LISA_BF16 if shape.dtype == "bf16" else lisa.LISA_F32
-    nbytes = lisa.lisa_backward_workspace_bytes(B, heads, shape.H, shape.W, D, D, T, dt)
-    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(dev)
-    call = [(s_["xq"].data_ptr(), s_["xk"].data_ptr(), s_["v"].data_ptr(), s_["dO"].data_ptr(), s_["dq"].data_ptr(),
-             s_["dk"].data_ptr(), s_["dv"].data_ptr(), dalpha.data_ptr(), B, heads, shape.H, shape.W, D, D, T,
-             ctypes.byref(wt), alpha.data_ptr(), 1e-6, 1, dt, ws.data_ptr(), nbytes, stream.cuda_stream)
-            for s_ in sets]
+    if mlp:   # adaptive weights: lisa_backward_mlp, with the parameters' gradients
+        params = tuple(inp[k].to(dev) for k in ("W1", "b1", "W2", "b2"))
+        pgrads = tuple(torch.empty_like(x) for x in params)
+        wt, keep = lisa.make_weights(T, mlp=params)
+        mg = lisa.lisa_mlp_grads(*(x.data_ptr() for x in pgrads))
+        nbytes = lisa.lisa_backward_mlp_workspace_bytes(B, heads, shape.H, shape.W, D, D, T, shape.hidden, dt)
+        fn = lib.lisa_backward_mlp
+    else:
+        wt, keep = lisa.make_weights(T, beta=shape.beta)
+        nbytes = lisa.lisa_backward_workspace_bytes(B, heads, shape.H, shape.W, D, D, T, dt)
+        fn = lib.lisa_backward
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+
+    def args_of(s_):
+        head = (s_["xq"].data_ptr(), s_["xk"].data_ptr(), s_["v"].data_ptr(), s_["dO"].data_ptr(), s_["dq"].data_ptr(),
+                s_["dk"].data_ptr(), s_["dv"].data_ptr(), dalpha.data_ptr())
+        tail = (B, heads, shape.H, shape.W, D, D, T, ctypes.byref(wt), alpha.data_ptr(), 1e-6, 1, dt, ws.data_ptr(),
+                nbytes, stream.cuda_stream)
+        return head + ((ctypes.byref(mg),) if mlp else ()) + tail
+    call = [args_of(s_) for s_ in sets]
 
     def step(i):
-        rc = lib.lisa_backward(*call[i % R])
+        rc = fn(*call[i % R])
         if rc != 0:
             raise RuntimeError("lisa_backward: " + lisa.lisa_status_string(rc))
 
@@ -584,8 +599,9 @@ def backward_arm(args, shape):
     clocks = sampler.stop()
     ms = start.elapsed_time(end)
     value = units * args.steps / (ms / 1e3)
-    # kernels per backward: 2 statistics + 8, plus the bf16 operand image at d = 64
-    nk = 10 + (1 if (shape.dtype == "bf16" and D == 64) else 0)
+    # kernels per backward: 2 statistics + 8, plus the bf16 operand image at d = 64;
+    # adaptive weights: the MLP pass replaces two, one dU_k pass if T > 1, two for the parameters
+    nk = 10 + (1 if (shape.dtype == "bf16" and D == 64) else 0) + ((1 if T > 1 else 0) + 1 if mlp else 0)
     peak, peak_src = hbm_peak()
     esz = 2 if shape.dtype == "bf16" else 4
     bytes_step = 7 * D * esz * units

@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 
 #include "lisa.h"
+#include "lisa_backward_mlp.h"
 #include "lisa_bwd.h"
 #include "lisa_internal.h"
 
@@ -367,7 +368,7 @@ extern "C" const char *lisa_status_string(int status) {
     }
 }
 
-extern "C" int lisa_abi_version(void) { return 101; }
+extern "C" int lisa_abi_version(void) { return 102; }
 
 // ---------------------------------------------------------------------------
 // lisa_forward_noalloc -- the layer for callers that may not allocate device
@@ -442,25 +443,26 @@ struct BwdPlan {
     int nh, nblk;
     size_t off_mred, off_uk, off_ubar, off_ubart, off_dub, off_lstat, off_dalp, off_dsp, off_dm, off_du1,
         off_dmt, off_du1t, off_dsr, off_dals, off_dkp, off_bimg;
+    // adaptive weights only
+    size_t off_ukn, off_wtok, off_dz, off_h, off_da, off_dxm, off_dukp, off_pw1, off_pb1, off_pw2, off_pb2;
     size_t total;
 };
 
 // The backward always runs the SIMT statistics kernels; its own buffers
-// follow the forward plan's.
-BwdPlan make_bwd_plan(int slices, int n, int D, int T, int dtype) {
+// follow the forward plan's.  hidden > 0: the adaptive weights' buffers too.
+BwdPlan make_bwd_plan(int slices, int n, int D, int T, int hidden) {
     BwdPlan b{};
     b.fwd = make_plan(slices, n, D, T, LISA_F32, LISA_W_FIXED, 0);   // SIMT family, any dtype
-    (void)dtype;
     b.nh = T > 1 ? T - 1 : 1;
     b.nblk = (n + kBwdTokensPerBlock - 1) / kBwdTokensPerBlock;
-    const size_t S = (size_t)slices, C = (size_t)b.fwd.chunks, d = (size_t)D, dd = d * d;
+    const size_t S = (size_t)slices, C = (size_t)b.fwd.chunks, d = (size_t)D, dd = d * d, N = (size_t)n;
     size_t off = b.fwd.total;
     b.off_mred = off;  off = align_up(off + S * dd * sizeof(float));
     b.off_uk = off;    off = align_up(off + S * b.nh * dd * sizeof(float));
     b.off_ubar = off;  off = align_up(off + S * dd * sizeof(float));
     b.off_ubart = off; off = align_up(off + S * dd * sizeof(float));
     b.off_dub = off;   off = align_up(off + S * C * dd * sizeof(float));
-    b.off_lstat = off; off = align_up(off + S * (size_t)n * 4 * sizeof(float));
+    b.off_lstat = off; off = align_up(off + S * N * 4 * sizeof(float));
     b.off_dalp = off;  off = align_up(off + S * b.nblk * sizeof(float));
     b.off_dsp = off;   off = align_up(off + S * b.nblk * d * sizeof(float));
     b.off_dm = off;    off = align_up(off + S * dd * sizeof(float));
@@ -469,42 +471,55 @@ BwdPlan make_bwd_plan(int slices, int n, int D, int T, int dtype) {
     b.off_du1t = off;  off = align_up(off + S * dd * sizeof(float));
     b.off_dsr = off;   off = align_up(off + S * d * sizeof(float));
     b.off_dals = off;  off = align_up(off + S * sizeof(float));
-    b.off_dkp = off;   off = align_up(off + S * (size_t)n * d * sizeof(float));
+    b.off_dkp = off;   off = align_up(off + S * N * d * sizeof(float));
     b.off_bimg = off;  off = align_up(off + S * 5 * dd * sizeof(uint16_t));
+    if (hidden > 0) {
+        const size_t Tz = (size_t)T, Hd = (size_t)hidden, nk = (size_t)b.nh;
+        b.off_ukn = off;  off = align_up(off + S * nk * dd * sizeof(float));
+        b.off_wtok = off; off = align_up(off + S * N * Tz * sizeof(float));
+        b.off_dz = off;   off = align_up(off + S * N * Tz * sizeof(float));
+        b.off_h = off;    off = align_up(off + S * N * Hd * sizeof(float));
+        b.off_da = off;   off = align_up(off + S * N * Hd * sizeof(float));
+        b.off_dxm = off;  off = align_up(off + S * N * 2 * d * sizeof(float));
+        b.off_dukp = off; off = align_up(off + S * C * nk * dd * sizeof(float));
+        b.off_pw1 = off;  off = align_up(off + S * C * Hd * 2 * d * sizeof(float));
+        b.off_pb1 = off;  off = align_up(off + S * C * Hd * sizeof(float));
+        b.off_pw2 = off;  off = align_up(off + S * C * Tz * Hd * sizeof(float));
+        b.off_pb2 = off;  off = align_up(off + S * C * Tz * sizeof(float));
+    }
     b.total = off;
     return b;
 }
 
-}  // namespace
-
-extern "C" size_t lisa_backward_workspace_bytes(int B, int heads, int H, int W, int d_h, int d_v, int T,
-                                                int dtype) {
-    if (check_sizes(B, heads, H, W, d_h, d_v, T, dtype) != LISA_OK) return 0;
-    const long long slices = (long long)B * heads, n = (long long)H * W;
-    if (slices == 0 || n == 0) return 0;
-    return make_bwd_plan((int)slices, (int)n, d_h, effective_T(T), dtype).total;
-}
-
-extern "C" lisa_status lisa_backward(const void *Q, const void *K, const void *V, const void *dO, void *dQ,
-                                     void *dK, void *dV, float *dalpha, int B, int heads, int H, int W,
-                                     int d_h, int d_v, int T, const lisa_weights *wts, const float *alpha,
-                                     float eps, int relu_inputs, int dtype, void *workspace,
-                                     size_t workspace_bytes, void *stream) {
+// Everything lisa_backward and lisa_backward_mlp share: checks, plan,
+// workspace views, launch.  mg is non-null exactly for the adaptive weights.
+lisa_status run_backward(const void *Q, const void *K, const void *V, const void *dO, void *dQ, void *dK,
+                         void *dV, float *dalpha, const lisa_mlp_grads *mg, int B, int heads, int H, int W,
+                         int d_h, int d_v, int T, const lisa_weights *wts, const float *alpha, float eps,
+                         int relu_inputs, int dtype, void *workspace, size_t workspace_bytes, void *stream) {
     lisa_status st = check_sizes(B, heads, H, W, d_h, d_v, T, dtype);
     if (st != LISA_OK) return st;
-    if (!wts) return LISA_ERR_INVALID_ARG;
-    if (wts->mode == LISA_W_MLP) return LISA_ERR_UNSUPPORTED;
     if (!(eps > 0.f) || !std::isfinite(eps)) return LISA_ERR_INVALID_ARG;
     if (relu_inputs != 0 && relu_inputs != 1) return LISA_ERR_INVALID_ARG;
     BwdProblem b{};
     st = resolve_weights(b.fwd, wts, T);
     if (st != LISA_OK) return st;
+    const bool mlp = mg != nullptr;
+    if (mlp && (!mg->dW1 || !mg->db1 || !mg->dW2 || !mg->db2)) return LISA_ERR_INVALID_ARG;
     const long long slices = (long long)B * heads, n = (long long)H * W;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    if (slices == 0 || n == 0) {   // nothing to differentiate: dalpha = 0
+    if (slices == 0 || n == 0) {   // nothing to differentiate: dalpha (and the MLP's gradients) = 0
         if (heads > 0) {
             if (!dalpha) return LISA_ERR_INVALID_ARG;
             if (cudaMemsetAsync(dalpha, 0, (size_t)heads * sizeof(float), cs) != cudaSuccess)
+                return LISA_ERR_CUDA;
+        }
+        if (mlp) {
+            const size_t hd = (size_t)b.fwd.hidden;
+            if (cudaMemsetAsync(mg->dW1, 0, hd * 2 * d_h * sizeof(float), cs) != cudaSuccess ||
+                cudaMemsetAsync(mg->db1, 0, hd * sizeof(float), cs) != cudaSuccess ||
+                cudaMemsetAsync(mg->dW2, 0, (size_t)T * hd * sizeof(float), cs) != cudaSuccess ||
+                cudaMemsetAsync(mg->db2, 0, (size_t)T * sizeof(float), cs) != cudaSuccess)
                 return LISA_ERR_CUDA;
         }
         return LISA_OK;
@@ -527,7 +542,7 @@ extern "C" lisa_status lisa_backward(const void *Q, const void *K, const void *V
     if (overlaps(dalpha, (size_t)heads * sizeof(float), alpha, (size_t)heads * sizeof(float)))
         return LISA_ERR_INVALID_ARG;
 
-    const BwdPlan pl = make_bwd_plan((int)slices, (int)n, d_h, b.fwd.T, dtype);
+    const BwdPlan pl = make_bwd_plan((int)slices, (int)n, d_h, b.fwd.T, mlp ? b.fwd.hidden : 0);
     if (!workspace || workspace_bytes < pl.total) return LISA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return LISA_ERR_INVALID_ARG;
     fill_problem(b.fwd, pl.fwd, Q, K, V, nullptr, (int)slices, heads, H, W, d_h, relu_inputs, eps, alpha, dtype,
@@ -542,21 +557,84 @@ extern "C" lisa_status lisa_backward(const void *Q, const void *K, const void *V
     b.nblk = pl.nblk;
     b.nh = pl.nh;
     char *ws = static_cast<char *>(workspace);
-    b.Mred = reinterpret_cast<float *>(ws + pl.off_mred);
-    b.Uk = reinterpret_cast<float *>(ws + pl.off_uk);
-    b.Ubar = reinterpret_cast<float *>(ws + pl.off_ubar);
-    b.UbarT = reinterpret_cast<float *>(ws + pl.off_ubart);
-    b.dub_part = reinterpret_cast<float *>(ws + pl.off_dub);
-    b.lstat = reinterpret_cast<float *>(ws + pl.off_lstat);
-    b.dal_part = reinterpret_cast<float *>(ws + pl.off_dalp);
-    b.ds_part = reinterpret_cast<float *>(ws + pl.off_dsp);
-    b.dM = reinterpret_cast<float *>(ws + pl.off_dm);
-    b.dU1 = reinterpret_cast<float *>(ws + pl.off_du1);
-    b.dMT = reinterpret_cast<float *>(ws + pl.off_dmt);
-    b.dU1T = reinterpret_cast<float *>(ws + pl.off_du1t);
-    b.ds_red = reinterpret_cast<float *>(ws + pl.off_dsr);
-    b.dal_slice = reinterpret_cast<float *>(ws + pl.off_dals);
-    b.dk_part = reinterpret_cast<float *>(ws + pl.off_dkp);
+    auto f32 = [ws](size_t off) { return reinterpret_cast<float *>(ws + off); };
+    b.Mred = f32(pl.off_mred);
+    b.Uk = f32(pl.off_uk);
+    b.Ubar = f32(pl.off_ubar);
+    b.UbarT = f32(pl.off_ubart);
+    b.dub_part = f32(pl.off_dub);
+    b.lstat = f32(pl.off_lstat);
+    b.dal_part = f32(pl.off_dalp);
+    b.ds_part = f32(pl.off_dsp);
+    b.dM = f32(pl.off_dm);
+    b.dU1 = f32(pl.off_du1);
+    b.dMT = f32(pl.off_dmt);
+    b.dU1T = f32(pl.off_du1t);
+    b.ds_red = f32(pl.off_dsr);
+    b.dal_slice = f32(pl.off_dals);
+    b.dk_part = f32(pl.off_dkp);
     b.bimg = reinterpret_cast<uint16_t *>(ws + pl.off_bimg);
+    if (mlp) {
+        b.mlp = 1;
+        b.Ukn = f32(pl.off_ukn);
+        b.wtok = f32(pl.off_wtok);
+        b.dzbuf = f32(pl.off_dz);
+        b.hbuf = f32(pl.off_h);
+        b.dabuf = f32(pl.off_da);
+        b.dxm = f32(pl.off_dxm);
+        b.dukp = f32(pl.off_dukp);
+        b.pw1 = f32(pl.off_pw1);
+        b.pb1 = f32(pl.off_pb1);
+        b.pw2 = f32(pl.off_pw2);
+        b.pb2 = f32(pl.off_pb2);
+        b.dW1 = mg->dW1;
+        b.db1 = mg->db1;
+        b.dW2 = mg->dW2;
+        b.db2 = mg->db2;
+    }
     return launch_bwd(b, cs) == cudaSuccess ? LISA_OK : LISA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" size_t lisa_backward_workspace_bytes(int B, int heads, int H, int W, int d_h, int d_v, int T,
+                                                int dtype) {
+    if (check_sizes(B, heads, H, W, d_h, d_v, T, dtype) != LISA_OK) return 0;
+    const long long slices = (long long)B * heads, n = (long long)H * W;
+    if (slices == 0 || n == 0) return 0;
+    return make_bwd_plan((int)slices, (int)n, d_h, effective_T(T), 0).total;
+}
+
+extern "C" lisa_status lisa_backward(const void *Q, const void *K, const void *V, const void *dO, void *dQ,
+                                     void *dK, void *dV, float *dalpha, int B, int heads, int H, int W,
+                                     int d_h, int d_v, int T, const lisa_weights *wts, const float *alpha,
+                                     float eps, int relu_inputs, int dtype, void *workspace,
+                                     size_t workspace_bytes, void *stream) {
+    if (!wts) return LISA_ERR_INVALID_ARG;
+    if (wts->mode == LISA_W_MLP) {   // sizes still checked first: T or d out of range stays UNSUPPORTED
+        const lisa_status st = check_sizes(B, heads, H, W, d_h, d_v, T, dtype);
+        return st != LISA_OK ? st : LISA_ERR_UNSUPPORTED;
+    }
+    return run_backward(Q, K, V, dO, dQ, dK, dV, dalpha, nullptr, B, heads, H, W, d_h, d_v, T, wts, alpha, eps,
+                        relu_inputs, dtype, workspace, workspace_bytes, stream);
+}
+
+extern "C" size_t lisa_backward_mlp_workspace_bytes(int B, int heads, int H, int W, int d_h, int d_v, int T,
+                                                    int hidden, int dtype) {
+    if (check_sizes(B, heads, H, W, d_h, d_v, T, dtype) != LISA_OK) return 0;
+    if (T < 1 || T > LISA_MAX_T_MLP || hidden < 1 || hidden > LISA_MAX_HIDDEN) return 0;
+    const long long slices = (long long)B * heads, n = (long long)H * W;
+    if (slices == 0 || n == 0) return 0;
+    return make_bwd_plan((int)slices, (int)n, d_h, T, hidden).total;
+}
+
+extern "C" lisa_status lisa_backward_mlp(const void *Q, const void *K, const void *V, const void *dO, void *dQ,
+                                         void *dK, void *dV, float *dalpha, const lisa_mlp_grads *mgrads,
+                                         int B, int heads, int H, int W, int d_h, int d_v, int T,
+                                         const lisa_weights *wts, const float *alpha, float eps,
+                                         int relu_inputs, int dtype, void *workspace, size_t workspace_bytes,
+                                         void *stream) {
+    if (!wts || wts->mode != LISA_W_MLP || !mgrads) return LISA_ERR_INVALID_ARG;
+    return run_backward(Q, K, V, dO, dQ, dK, dV, dalpha, mgrads, B, heads, H, W, d_h, d_v, T, wts, alpha, eps,
+                        relu_inputs, dtype, workspace, workspace_bytes, stream);
 }

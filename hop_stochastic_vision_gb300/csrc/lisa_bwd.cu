@@ -33,6 +33,11 @@
 //   6. bwd_reduce     per slice: ds and the slice's dalpha
 //   7. bwd_finish_k   one thread per element: dXk = (dK + ds) [Xk > 0]
 //   8. bwd_dalpha     dalpha per head = sum over the batch
+// With the adaptive (MLP) weights, steps 2-3 become bwd_token_mlp (the
+// window statistics, the MLP's forward and backward per token) and
+// bwd_stats_duk (one split-K dU_k = sum_i w_ik Q~_i^T dg_i per walk length);
+// step 5 adds each token's own walk terms; bwd_mlp_params and
+// bwd_mlp_reduce produce dW1, db1, dW2, db2.
 // Every reduction runs in a fixed order: the result does not depend on
 // scheduling.
 #include <cuda_bf16.h>
@@ -119,6 +124,7 @@ __global__ void __launch_bounds__(kThreads) bwd_recur(BwdProblem b) {
             const int idx = tid + x * kThreads;
             Uk[idx] = U[idx % D][idx / D];
             ub[x] = p.T > 1 ? p.w[1] * U[idx / D][idx % D] : 0.f;
+            if (b.mlp) b.Ukn[(size_t)sl * b.nh * D * D + idx] = U[idx / D][idx % D];
         }
         for (int k = 2; k < p.T; ++k) {
             for (int idx = tid; idx < D * D; idx += kThreads) {
@@ -136,8 +142,10 @@ __global__ void __launch_bounds__(kThreads) bwd_recur(BwdProblem b) {
                 ub[x] = fmaf(p.w[k], u, ub[x]);
             }
             __syncthreads();
-            for (int idx = tid; idx < D * D; idx += kThreads)
+            for (int idx = tid; idx < D * D; idx += kThreads) {
                 Uk[(size_t)(k - 1) * D * D + idx] = U[idx % D][idx / D];
+                if (b.mlp) b.Ukn[((size_t)sl * b.nh + (k - 1)) * D * D + idx] = U[idx / D][idx % D];
+            }
         }
     }
 #pragma unroll
@@ -208,6 +216,74 @@ __global__ void __launch_bounds__(kThreads) bwd_stats_dub(BwdProblem b) {
         __syncthreads();
     }
     float *out = b.dub_part + ((size_t)sl * p.chunks + c) * D * D;
+#pragma unroll
+    for (int r = 0; r < RB; ++r)
+#pragma unroll
+        for (int x = 0; x < RB; ++x) out[(a0 + r) * D + e0 + x] = acc[r][x];
+}
+
+// ---------------------------------------------------------------------------
+// 2'. adaptive weights: partial dU_k = sum_j Q~_j (w_jk alpha dO_j)^T over one
+// chunk, one k per blockIdx.y (k = 1 + blockIdx.y).
+// ---------------------------------------------------------------------------
+template <typename TIn, int D>
+__global__ void __launch_bounds__(kThreads) bwd_stats_duk(BwdProblem b) {
+    constexpr int RB = D / 16;
+    __shared__ float Qs[kTile][D];
+    __shared__ float Gs[kTile][D];
+    __shared__ float s[D];
+    const Problem &p = b.fwd;
+    const int c = blockIdx.x % p.chunks, sl = blockIdx.x / p.chunks, k = 1 + blockIdx.y, tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    if (tid < D) s[tid] = p.s_red[(size_t)sl * D + tid];
+    __syncthreads();
+    const int t0 = c * p.chunk, t1 = min(p.n, t0 + p.chunk);
+    const TIn *Q = static_cast<const TIn *>(p.Q) + (size_t)sl * p.n * D;
+    const TIn *dO = static_cast<const TIn *>(b.dO) + (size_t)sl * p.n * D;
+    const float *wt = b.wtok + (size_t)sl * p.n * p.T;
+    const float al = p.alpha[sl % p.heads];
+    const int a0 = (tid / 16) * RB, e0 = (tid % 16) * RB;
+    float acc[RB][RB];
+#pragma unroll
+    for (int r = 0; r < RB; ++r)
+#pragma unroll
+        for (int x = 0; x < RB; ++x) acc[r][x] = 0.f;
+    for (int base = t0; base < t1; base += kTile) {
+        const int cnt = min(kTile, t1 - base);
+        for (int idx = tid; idx < kTile * D; idx += kThreads) {
+            const int j = idx / D, ch = idx % D;
+            float qv = 0.f, gv = 0.f;
+            if (j < cnt) {
+                qv = relu_if(ld(Q + (size_t)(base + j) * D + ch), p.relu);
+                gv = al * wt[(size_t)(base + j) * p.T + k] * ld(dO + (size_t)(base + j) * D + ch);
+            }
+            Qs[j][ch] = qv;
+            Gs[j][ch] = gv;
+        }
+        __syncthreads();
+        for (int j = warp; j < kTile; j += kWarps) {   // Q~_j = Q_j / (Q_j . s + eps)
+            float d = 0.f;
+            for (int ch = lane; ch < D; ch += 32) d += Qs[j][ch] * s[ch];
+            const float r = 1.f / (warp_sum(d) + p.eps);
+            __syncwarp();
+            for (int ch = lane; ch < D; ch += 32) Qs[j][ch] *= r;
+        }
+        __syncthreads();
+        for (int j = 0; j < cnt; ++j) {
+            float ra[RB], rb[RB];
+#pragma unroll
+            for (int r = 0; r < RB; ++r) {
+                ra[r] = Qs[j][a0 + r];
+                rb[r] = Gs[j][e0 + r];
+            }
+#pragma unroll
+            for (int r = 0; r < RB; ++r)
+#pragma unroll
+                for (int x = 0; x < RB; ++x) acc[r][x] = fmaf(ra[r], rb[x], acc[r][x]);
+        }
+        __syncthreads();
+    }
+    float *out = b.dukp + (((size_t)sl * p.chunks + c) * b.nh + (k - 1)) * D * D;
 #pragma unroll
     for (int r = 0; r < RB; ++r)
 #pragma unroll
@@ -353,6 +429,196 @@ __global__ void __launch_bounds__(kThreads) bwd_token_a(BwdProblem b) {
 }
 
 // ---------------------------------------------------------------------------
+// 3'. adaptive weights, per token i (replaces bwd_token_a): the window's
+// softmax statistics and the dalpha terms as there, with the token's own
+// weights; and the MLP's backward:
+//   x_i = [q_i; k_i], a_i = W1 x_i + b1, h_i = GELU(a_i), w_i = softmax(W2 h_i + b2)
+//   dw_ik = alpha dO_i . Y_k,i (Y_0 = V_i, Y_k = Q~_i U_k), dz_i = w_i (dw_i - w_i . dw_i)
+//   da_i = (W2^T dz_i) GELU'(a_i),  the MLP's share of [dq_i; dk_i] = W1^T da_i
+// Stored per token: w_i and dz_i (T), h_i and da_i (hidden), the share (2 d).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float gelu_exact(float x) { return 0.5f * x * (1.f + erff(x * 0.70710678118654752f)); }
+__device__ __forceinline__ float gelu_exact_grad(float x) {
+    return 0.5f * (1.f + erff(x * 0.70710678118654752f)) + x * 0.39894228040143268f * expf(-0.5f * x * x);
+}
+
+template <typename TIn, int D>
+__global__ void __launch_bounds__(kThreads) bwd_token_mlp(BwdProblem b) {
+    constexpr int NC = (D + 31) / 32;
+    constexpr int TM = LISA_MAX_T_MLP;
+    __shared__ float part[kWarps];
+    __shared__ float pre_s[kWarps][LISA_MAX_HIDDEN];
+    __shared__ float h_s[kWarps][LISA_MAX_HIDDEN];
+    __shared__ float da_s[kWarps][LISA_MAX_HIDDEN];
+    const Problem &p = b.fwd;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int sl = blockIdx.x / b.nblk, blk = blockIdx.x % b.nblk;
+    const int T = p.T, hid = p.hidden;
+    const size_t sbase = (size_t)sl * p.n * D;
+    const TIn *Q = static_cast<const TIn *>(p.Q) + sbase;
+    const TIn *K = static_cast<const TIn *>(p.K) + sbase;
+    const TIn *V = static_cast<const TIn *>(p.V) + sbase;
+    const TIn *dO = static_cast<const TIn *>(b.dO) + sbase;
+    const float *s = p.s_red + (size_t)sl * D;
+    const float al = p.alpha[sl % p.heads];
+    const float scale = rsqrtf((float)D);
+    float dal = 0.f;
+    for (int u = warp; u < b.tpb; u += kWarps) {
+        const int i = blk * b.tpb + u;
+        if (i >= p.n) break;
+        float q[NC], k[NC], v[NC], go[NC], sv[NC];
+        load_row<TIn, D>(Q + (size_t)i * D, q, lane, p.relu);
+        load_row<TIn, D>(K + (size_t)i * D, k, lane, p.relu);
+        load_row<TIn, D>(V + (size_t)i * D, v, lane, 0);
+        load_row<TIn, D>(dO + (size_t)i * D, go, lane, 0);
+#pragma unroll
+        for (int t = 0; t < NC; ++t) sv[t] = lane + 32 * t < D ? s[lane + 32 * t] : 0.f;
+        const float rq = 1.f / (dot_row<D>(q, sv) + p.eps);
+        // the MLP forward (pre-activations and h in shared memory, per warp)
+        for (int m = 0; m < hid; ++m) {
+            const float *row = p.W1 + (size_t)m * 2 * D;
+            float acc = 0.f;
+#pragma unroll
+            for (int t = 0; t < NC; ++t) {
+                const int ch = lane + 32 * t;
+                if (ch < D) acc = fmaf(row[ch], q[t], fmaf(row[D + ch], k[t], acc));
+            }
+            acc = warp_sum(acc) + p.b1[m];
+            if (lane == 0) {
+                pre_s[warp][m] = acc;
+                h_s[warp][m] = gelu_exact(acc);
+            }
+        }
+        __syncwarp();
+        float w[TM], zmax = -INFINITY, zs = 0.f;
+#pragma unroll
+        for (int t = 0; t < TM; ++t) {
+            w[t] = 0.f;
+            if (t < T) {
+                float z = p.b2[t];
+                for (int m = 0; m < hid; ++m) z = fmaf(p.W2[(size_t)t * hid + m], h_s[warp][m], z);
+                w[t] = z;
+                zmax = fmaxf(zmax, z);
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < TM; ++t)
+            if (t < T) {
+                w[t] = expf(w[t] - zmax);
+                zs += w[t];
+            }
+        const float izs = 1.f / zs;
+#pragma unroll
+        for (int t = 0; t < TM; ++t) w[t] = t < T ? w[t] * izs : 0.f;
+        // walk terms Y_k (k >= 1), g_i, and the partial sums of dw
+        float g[NC], dw[TM];
+#pragma unroll
+        for (int t = 0; t < TM; ++t) dw[t] = 0.f;
+#pragma unroll
+        for (int t = 0; t < NC; ++t) {
+            g[t] = w[0] * v[t];
+            dw[0] = fmaf(al * go[t], v[t], dw[0]);
+        }
+#pragma unroll
+        for (int kk = 1; kk < TM; ++kk) {
+            if (kk >= T) break;
+            const float *Un = b.Ukn + ((size_t)sl * b.nh + (kk - 1)) * D * D;
+            float y[NC];
+#pragma unroll
+            for (int t = 0; t < NC; ++t) y[t] = 0.f;
+            for (int a = 0; a < D; ++a) {
+                const float qa = __shfl_sync(0xffffffffu, q[a / 32], a % 32) * rq;
+#pragma unroll
+                for (int t = 0; t < NC; ++t)
+                    if (lane + 32 * t < D) y[t] = fmaf(qa, Un[(size_t)a * D + lane + 32 * t], y[t]);
+            }
+#pragma unroll
+            for (int t = 0; t < NC; ++t) {
+                g[t] = fmaf(w[kk], y[t], g[t]);
+                dw[kk] = fmaf(al * go[t], y[t], dw[kk]);
+            }
+        }
+        warp_sum_n(dw);
+        // local window (as bwd_token_a)
+        int nb[9];
+        const int cnt = window(i, p.H, p.W, nb);
+        float kr[9][NC], vr[9][NC], e[9];
+#pragma unroll
+        for (int t9 = 0; t9 < 9; ++t9) {
+            const int row = t9 < cnt ? nb[t9] : i;
+            load_row<TIn, D>(K + (size_t)row * D, kr[t9], lane, p.relu);
+            load_row<TIn, D>(V + (size_t)row * D, vr[t9], lane, 0);
+            e[t9] = 0.f;
+#pragma unroll
+            for (int t = 0; t < NC; ++t) e[t9] = fmaf(q[t], kr[t9][t], e[t9]);
+        }
+        warp_sum_n(e);
+        float emax = -INFINITY;
+#pragma unroll
+        for (int t9 = 0; t9 < 9; ++t9)
+            if (t9 < cnt) emax = fmaxf(emax, e[t9] * scale);
+        float l[NC], esum = 0.f;
+#pragma unroll
+        for (int t = 0; t < NC; ++t) l[t] = 0.f;
+#pragma unroll
+        for (int t9 = 0; t9 < 9; ++t9) {
+            if (t9 >= cnt) break;
+            const float a = expf(e[t9] * scale - emax);
+            esum += a;
+#pragma unroll
+            for (int t = 0; t < NC; ++t) l[t] = fmaf(a, vr[t9][t], l[t]);
+        }
+        const float inv = 1.f / esum;
+        float red[2] = {0.f, 0.f};
+#pragma unroll
+        for (int t = 0; t < NC; ++t) {
+            l[t] *= inv;
+            red[0] = fmaf(go[t], g[t] - l[t], red[0]);
+            red[1] = fmaf(go[t], l[t], red[1]);
+        }
+        warp_sum_n(red);
+        dal += red[0];
+        const size_t ti = (size_t)sl * p.n + i;
+        if (lane == 0) reinterpret_cast<float4 *>(b.lstat)[ti] = make_float4(emax, esum, red[1] * (1.f - al), 0.f);
+        // softmax and MLP backward
+        float wdw = 0.f, dz[TM];
+#pragma unroll
+        for (int t = 0; t < TM; ++t) wdw = fmaf(w[t], dw[t], wdw);
+#pragma unroll
+        for (int t = 0; t < TM; ++t) dz[t] = w[t] * (dw[t] - wdw);
+        for (int m = lane; m < hid; m += 32) {
+            float dh = 0.f;
+#pragma unroll
+            for (int t = 0; t < TM; ++t)
+                if (t < T) dh = fmaf(p.W2[(size_t)t * hid + m], dz[t], dh);
+            da_s[warp][m] = dh * gelu_exact_grad(pre_s[warp][m]);
+            b.hbuf[ti * hid + m] = h_s[warp][m];
+        }
+        __syncwarp();
+#pragma unroll
+        for (int t = 0; t < TM; ++t)
+            if (t < T && lane == t) {
+                b.wtok[ti * T + t] = w[t];
+                b.dzbuf[ti * T + t] = dz[t];
+            }
+        for (int m = lane; m < hid; m += 32) b.dabuf[ti * hid + m] = da_s[warp][m];
+        for (int c = lane; c < 2 * D; c += 32) {
+            float acc = 0.f;
+            for (int m = 0; m < hid; ++m) acc = fmaf(p.W1[(size_t)m * 2 * D + c], da_s[warp][m], acc);
+            b.dxm[ti * 2 * D + c] = acc;
+        }
+        __syncwarp();   // the next token of this warp rewrites pre_s, h_s, da_s
+    }
+    if (lane == 0) part[warp] = dal;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float acc = 0.f;
+        for (int w2 = 0; w2 < kWarps; ++w2) acc += part[w2];
+        b.dal_part[(size_t)sl * b.nblk + blk] = acc;
+    }
+}
+
+// ---------------------------------------------------------------------------
 // 4. reduce dUbar; the walk's backward recurrence (or the transposed solve)
 // gives dM and dU_1.
 // ---------------------------------------------------------------------------
@@ -369,10 +635,21 @@ __global__ void __launch_bounds__(kThreads) bwd_recur_back(BwdProblem b) {
     for (int x = 0; x < EPT; ++x) {
         const int idx = tid + x * kThreads;
         float acc = 0.f;
-        for (int c = 0; c < p.chunks; ++c) acc += b.dub_part[((size_t)sl * p.chunks + c) * D * D + idx];
+        if (!b.mlp)
+            for (int c = 0; c < p.chunks; ++c) acc += b.dub_part[((size_t)sl * p.chunks + c) * D * D + idx];
         dub[x] = acc;
         M[idx / D][idx % D] = b.Mred[(size_t)sl * D * D + idx];
     }
+    // the direct term of dL/dU_k at entry x: w_k dUbar, or with the adaptive
+    // weights sum_i w_ik Q~_i^T dg_i (its split-K partials, in chunk order)
+    auto level = [&](int k, int x) -> float {
+        if (!b.mlp) return p.w[k] * dub[x];
+        const int idx = tid + x * kThreads;
+        float acc = 0.f;
+        for (int c = 0; c < p.chunks; ++c)
+            acc += b.dukp[(((size_t)sl * p.chunks + c) * b.nh + (k - 1)) * D * D + idx];
+        return acc;
+    };
     float *dM = b.dM + (size_t)sl * D * D, *dU1 = b.dU1 + (size_t)sl * D * D;
     const float *Uk = b.Uk + (size_t)sl * b.nh * D * D;   // transposed
     __syncthreads();
@@ -409,11 +686,11 @@ __global__ void __launch_bounds__(kThreads) bwd_recur_back(BwdProblem b) {
 #pragma unroll
         for (int x = 0; x < EPT; ++x) {
             const int idx = tid + x * kThreads;
-            G[idx / D][idx % D] = p.w[p.T - 1] * dub[x];
+            G[idx / D][idx % D] = level(p.T - 1, x);
         }
         __syncthreads();
         for (int k = p.T - 1; k >= 2; --k) {
-            // dM += G_k U_(k-1)^T, then G_(k-1) = w_(k-1) dUbar + M^T G_k
+            // dM += G_k U_(k-1)^T, then G_(k-1) = (direct term of U_(k-1)) + M^T G_k
             const float *Up = Uk + (size_t)(k - 2) * D * D;
 #pragma unroll
             for (int x = 0; x < EPT; ++x) {
@@ -427,7 +704,7 @@ __global__ void __launch_bounds__(kThreads) bwd_recur_back(BwdProblem b) {
             for (int x = 0; x < EPT; ++x) {
                 const int idx = tid + x * kThreads;
                 const int a = idx / D, e = idx % D;
-                float acc = p.w[k - 1] * dub[x];
+                float acc = level(k - 1, x);
                 for (int c = 0; c < D; ++c) acc = fmaf(M[c][a], G[c][e], acc);
                 X[a][e] = acc;
             }
@@ -461,6 +738,31 @@ __global__ void __launch_bounds__(kThreads) bwd_recur_back(BwdProblem b) {
 // (thread: 4 channels x the tokens of its group), then one warp per token
 // takes the normaliser, the window and the stores.
 // ---------------------------------------------------------------------------
+// Adaptive weights: the token's own walk terms, which the block's shared
+// products leave out (they see w = 0 and Ubar = 0):
+//   dV_j += w_j0 alpha dO_j,  dQ~_j += alpha sum_{k>=1} w_jk dO_j U_k^T
+// U_k^T is read from the transposed copy (coalesced over the output channel).
+template <int D>
+__device__ __forceinline__ void mlp_walk_terms(const BwdProblem &b, int sl, int j, int lane, float al,
+                                               const float (&go)[(D + 31) / 32], float (&dqt)[(D + 31) / 32],
+                                               float (&dv)[(D + 31) / 32]) {
+    constexpr int NC = (D + 31) / 32;
+    const int T = b.fwd.T;
+    const float *wt = b.wtok + ((size_t)sl * b.fwd.n + j) * T;
+#pragma unroll
+    for (int t = 0; t < NC; ++t) dv[t] = fmaf(wt[0] * al, go[t], dv[t]);
+    for (int kk = 1; kk < T; ++kk) {
+        const float wk = al * wt[kk];
+        const float *UT = b.Uk + ((size_t)sl * b.nh + (kk - 1)) * D * D;   // UT[c][a] = U_k[a][c]
+        for (int c = 0; c < D; ++c) {
+            const float gc = __shfl_sync(0xffffffffu, go[c / 32], c % 32) * wk;
+#pragma unroll
+            for (int t = 0; t < NC; ++t)
+                if (lane + 32 * t < D) dqt[t] = fmaf(gc, UT[(size_t)c * D + lane + 32 * t], dqt[t]);
+        }
+    }
+}
+
 constexpr int kTpb = 32;   // tokens per block of the per-token kernels
 
 template <int D>
@@ -585,6 +887,7 @@ __global__ void __launch_bounds__(kThreads) bwd_token_b(BwdProblem b) {
             dv[t] = in ? fmaf(w0 * al, go[t], oV[u * D + ch]) : 0.f;
             dk[t] = in ? oK[u * D + ch] : 0.f;
         }
+        if (b.mlp) mlp_walk_terms<D>(b, sl, j, lane, al, go, dqt, dv);
         const float rq = rqs[u];
         // through Q~ = Q / r:  c_j = (dQ~_j . Q_j) / r_j^2
         const float cj = dot_row<D>(dqt, q) * rq * rq;
@@ -593,6 +896,15 @@ __global__ void __launch_bounds__(kThreads) bwd_token_b(BwdProblem b) {
         for (int t = 0; t < NC; ++t) {
             dq[t] = dqt[t] * rq - cj * sv[t];
             ds[t] = fmaf(-cj, q[t], ds[t]);
+        }
+        if (b.mlp) {   // the MLP's share of dq_j, dk_j
+            const float *xm = b.dxm + ((size_t)sl * p.n + j) * 2 * D;
+#pragma unroll
+            for (int t = 0; t < NC; ++t)
+                if (lane + 32 * t < D) {
+                    dq[t] += xm[lane + 32 * t];
+                    dk[t] += xm[D + lane + 32 * t];
+                }
         }
         // local window: j as the query (its own softmax row) and as a key /
         // value of each neighbour i's row (N is symmetric).  All neighbour
@@ -825,6 +1137,7 @@ __global__ void __launch_bounds__(kThreads) bwd_token_b_tc(BwdProblem b) {
             dv[t] = fmaf(w0 * al, go[t], oV[u * D + ch]);
             dk[t] = oK[u * D + ch];
         }
+        if (b.mlp) mlp_walk_terms<D>(b, sl, j, lane, al, go, dqt, dv);
         const float rq = rqs[u];
         const float cj = dot_row<D>(dqt, q) * rq * rq;
         float dq[NC];
@@ -832,6 +1145,14 @@ __global__ void __launch_bounds__(kThreads) bwd_token_b_tc(BwdProblem b) {
         for (int t = 0; t < NC; ++t) {
             dq[t] = dqt[t] * rq - cj * sv[t];
             ds[t] = fmaf(-cj, q[t], ds[t]);
+        }
+        if (b.mlp) {   // the MLP's share of dq_j, dk_j
+            const float *xm = b.dxm + ((size_t)sl * p.n + j) * 2 * D;
+#pragma unroll
+            for (int t = 0; t < NC; ++t) {
+                dq[t] += xm[lane + 32 * t];
+                dk[t] += xm[D + lane + 32 * t];
+            }
         }
         int nb[9];
         const int nn = window(j, p.H, p.W, nb);
@@ -909,6 +1230,103 @@ __global__ void __launch_bounds__(kThreads) bwd_token_b_tc(BwdProblem b) {
 }
 
 // ---------------------------------------------------------------------------
+// adaptive weights: the MLP parameters' gradients.  Per (slice, chunk):
+//   dW1 += sum_i da_i x_i^T (x_i = [q_i; k_i]), db1 += sum_i da_i,
+//   dW2 += sum_i dz_i h_i^T, db2 += sum_i dz_i
+// as partial sums; bwd_mlp_reduce adds the partials of every slice and chunk
+// in a fixed order.
+// ---------------------------------------------------------------------------
+template <typename TIn, int D>
+__global__ void __launch_bounds__(kThreads) bwd_mlp_params(BwdProblem b) {
+    constexpr int kTok = 16;
+    constexpr int kMaxPer = LISA_MAX_HIDDEN * 2 * D / kThreads;   // dW1 entries per thread
+    __shared__ float Xs[kTok][2 * D];
+    __shared__ float As[kTok][LISA_MAX_HIDDEN];
+    __shared__ float Hs[kTok][LISA_MAX_HIDDEN];
+    __shared__ float Zs[kTok][LISA_MAX_T_MLP];
+    const Problem &p = b.fwd;
+    const int c = blockIdx.x % p.chunks, sl = blockIdx.x / p.chunks, tid = threadIdx.x;
+    const int T = p.T, hid = p.hidden;
+    const int t0 = c * p.chunk, t1 = min(p.n, t0 + p.chunk);
+    const size_t sbase = (size_t)sl * p.n * D;
+    const TIn *Q = static_cast<const TIn *>(p.Q) + sbase;
+    const TIn *K = static_cast<const TIn *>(p.K) + sbase;
+    const size_t tb = (size_t)sl * p.n;
+    float w1[kMaxPer], w2[2], bb = 0.f;
+#pragma unroll
+    for (int r = 0; r < kMaxPer; ++r) w1[r] = 0.f;
+    w2[0] = w2[1] = 0.f;
+    for (int base = t0; base < t1; base += kTok) {
+        const int cnt = min(kTok, t1 - base);
+        for (int x = tid; x < kTok * 2 * D; x += kThreads) {
+            const int j = x / (2 * D), ch = x % (2 * D);
+            float v = 0.f;
+            if (j < cnt) v = relu_if(ld((ch < D ? Q : K) + (size_t)(base + j) * D + (ch % D)), p.relu);
+            Xs[j][ch] = v;
+        }
+        for (int x = tid; x < kTok * LISA_MAX_HIDDEN; x += kThreads) {
+            const int j = x / LISA_MAX_HIDDEN, m = x % LISA_MAX_HIDDEN;
+            const bool in = j < cnt && m < hid;
+            As[j][m] = in ? b.dabuf[(tb + base + j) * hid + m] : 0.f;
+            Hs[j][m] = in ? b.hbuf[(tb + base + j) * hid + m] : 0.f;
+        }
+        for (int x = tid; x < kTok * LISA_MAX_T_MLP; x += kThreads) {
+            const int j = x / LISA_MAX_T_MLP, t = x % LISA_MAX_T_MLP;
+            Zs[j][t] = (j < cnt && t < T) ? b.dzbuf[(tb + base + j) * T + t] : 0.f;
+        }
+        __syncthreads();
+        for (int j = 0; j < cnt; ++j) {
+#pragma unroll
+            for (int r = 0; r < kMaxPer; ++r) {
+                const int e = tid + r * kThreads, m = e / (2 * D), ch = e % (2 * D);
+                w1[r] = fmaf(As[j][m], Xs[j][ch], w1[r]);
+            }
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int e = tid + r * kThreads, t = e / LISA_MAX_HIDDEN, m = e % LISA_MAX_HIDDEN;
+                if (t < LISA_MAX_T_MLP) w2[r] = fmaf(Zs[j][t], Hs[j][m], w2[r]);
+            }
+            if (tid < LISA_MAX_HIDDEN) bb += As[j][tid];
+            else if (tid - LISA_MAX_HIDDEN < LISA_MAX_T_MLP) bb += Zs[j][tid - LISA_MAX_HIDDEN];
+        }
+        __syncthreads();
+    }
+    const size_t pc = (size_t)sl * p.chunks + c;
+#pragma unroll
+    for (int r = 0; r < kMaxPer; ++r) {
+        const int e = tid + r * kThreads, m = e / (2 * D);
+        if (m < hid) b.pw1[pc * hid * 2 * D + e] = w1[r];
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const int e = tid + r * kThreads, t = e / LISA_MAX_HIDDEN, m = e % LISA_MAX_HIDDEN;
+        if (t < T && m < hid) b.pw2[(pc * T + t) * hid + m] = w2[r];
+    }
+    if (tid < hid) b.pb1[pc * hid + tid] = bb;
+    else if (tid >= LISA_MAX_HIDDEN && tid - LISA_MAX_HIDDEN < T) b.pb2[pc * T + tid - LISA_MAX_HIDDEN] = bb;
+}
+
+__global__ void __launch_bounds__(kThreads) bwd_mlp_reduce(BwdProblem b, int D) {
+    const Problem &p = b.fwd;
+    const int T = p.T, hid = p.hidden;
+    const int n1 = hid * 2 * D, n2 = T * hid;
+    const int total = n1 + hid + n2 + T;
+    const size_t parts = (size_t)p.slices * p.chunks;
+    for (int e = blockIdx.x * kThreads + threadIdx.x; e < total; e += gridDim.x * kThreads) {
+        const float *src;
+        float *dst;
+        int stride, off;
+        if (e < n1) { src = b.pw1; dst = b.dW1; stride = n1; off = e; }
+        else if (e < n1 + hid) { src = b.pb1; dst = b.db1; stride = hid; off = e - n1; }
+        else if (e < n1 + hid + n2) { src = b.pw2; dst = b.dW2; stride = n2; off = e - n1 - hid; }
+        else { src = b.pb2; dst = b.db2; stride = T; off = e - n1 - hid - n2; }
+        float acc = 0.f;
+        for (size_t q = 0; q < parts; ++q) acc += src[q * stride + off];
+        dst[off] = acc;
+    }
+}
+
+// ---------------------------------------------------------------------------
 // 6. per slice: ds = sum of the block partials; the slice's dalpha.
 // ---------------------------------------------------------------------------
 template <int D>
@@ -967,8 +1385,13 @@ cudaError_t launch_bwd_all(const BwdProblem &b, cudaStream_t st) {
     const unsigned grid_stats = (unsigned)p.slices * (unsigned)p.chunks;
     const unsigned grid_tok = (unsigned)p.slices * (unsigned)b.nblk;
     bwd_recur<D><<<p.slices, kThreads, 0, st>>>(b);
-    bwd_stats_dub<TIn, D><<<grid_stats, kThreads, 0, st>>>(b);
-    bwd_token_a<TIn, D><<<grid_tok, kThreads, 0, st>>>(b);
+    if (b.mlp) {   // per-token weights: the MLP's backward, then one dU_k per walk length
+        bwd_token_mlp<TIn, D><<<grid_tok, kThreads, 0, st>>>(b);
+        if (p.T > 1) bwd_stats_duk<TIn, D><<<dim3(grid_stats, (unsigned)(p.T - 1)), kThreads, 0, st>>>(b);
+    } else {
+        bwd_stats_dub<TIn, D><<<grid_stats, kThreads, 0, st>>>(b);
+        bwd_token_a<TIn, D><<<grid_tok, kThreads, 0, st>>>(b);
+    }
     bwd_recur_back<D><<<p.slices, kThreads, 0, st>>>(b);
     if constexpr (std::is_same<TIn, __nv_bfloat16>::value && D == 64) {
         bwd_bimg<<<dim3((unsigned)p.slices, 5), kThreads, 0, st>>>(b);
@@ -989,6 +1412,11 @@ cudaError_t launch_bwd_all(const BwdProblem &b, cudaStream_t st) {
     if (blocks > 152 * 16) blocks = 152 * 16;
     bwd_finish_k<TIn, D><<<(unsigned)blocks, kThreads, 0, st>>>(b);
     bwd_dalpha<<<(p.heads + kThreads - 1) / kThreads, kThreads, 0, st>>>(b);
+    if (b.mlp) {
+        bwd_mlp_params<TIn, D><<<grid_stats, kThreads, 0, st>>>(b);
+        const int total = p.hidden * 2 * D + p.hidden + p.T * p.hidden + p.T;
+        bwd_mlp_reduce<<<(total + kThreads - 1) / kThreads, kThreads, 0, st>>>(b, D);
+    }
     return cudaGetLastError();
 }
 

@@ -32,6 +32,17 @@ struct BwdProblem {
     float *ds_red;       // [S][D]
     float *dal_slice;    // [S]
     float *dk_part;      // [S][n][D]      dK without ds, fp32
+    // adaptive (MLP) walk weights only (null otherwise)
+    float *Ukn;          // [S][nh][D][D]  U_1 .. U_(T-1), row-major
+    float *wtok;         // [S][n][T]      per-token walk weights w_i
+    float *dzbuf;        // [S][n][T]      dL/dz_i (softmax logits)
+    float *hbuf;         // [S][n][hid]    h_i = GELU(W1 x_i + b1)
+    float *dabuf;        // [S][n][hid]    dL/d(W1 x_i + b1)
+    float *dxm;          // [S][n][2 D]    the MLP's share of dL/dq_i, dL/dk_i
+    float *dukp;         // [S][C][T-1][D][D]  partial dU_k = sum_i w_ik Q~_i^T dg_i
+    float *pw1, *pb1, *pw2, *pb2;   // [S][C][...] partial parameter gradients
+    float *dW1, *db1, *dW2, *db2;   // caller's outputs
+    int mlp;             // adaptive weights: the fields above are set
 };
 
 cudaError_t launch_bwd(const BwdProblem &b, cudaStream_t stream);

@@ -35,7 +35,8 @@ LISA_MAX_HIDDEN = 64
 
 EXPORTED = ("lisa_workspace_bytes", "lisa_forward", "lisa_forward_host", "lisa_num_stages",
             "lisa_stage_name", "lisa_forward_stage", "lisa_forward_noalloc", "lisa_backward_workspace_bytes",
-            "lisa_backward", "lisa_status_string", "lisa_abi_version")
+            "lisa_backward", "lisa_backward_mlp_workspace_bytes", "lisa_backward_mlp", "lisa_status_string",
+            "lisa_abi_version")
 
 LISA_NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -51,6 +52,11 @@ class lisa_weights(ctypes.Structure):
         ("b2", ctypes.c_void_p),
         ("hidden", ctypes.c_int),
     ]
+
+
+class lisa_mlp_grads(ctypes.Structure):
+    _fields_ = [("dW1", ctypes.c_void_p), ("db1", ctypes.c_void_p), ("dW2", ctypes.c_void_p),
+                ("db2", ctypes.c_void_p)]
 
 
 class LisaError(RuntimeError):
@@ -94,6 +100,11 @@ def load(path: str = LIB_PATH):
         lib.lisa_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, wp, vp, f, i, i,
                                       vp, sz, vp]
         lib.lisa_backward.restype = i
+        lib.lisa_backward_mlp_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i, i]
+        lib.lisa_backward_mlp_workspace_bytes.restype = sz
+        lib.lisa_backward_mlp.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ctypes.POINTER(lisa_mlp_grads), i, i, i,
+                                          i, i, i, i, wp, vp, f, i, i, vp, sz, vp]
+        lib.lisa_backward_mlp.restype = i
         lib.lisa_status_string.argtypes = [i]
         lib.lisa_status_string.restype = ctypes.c_char_p
         lib.lisa_abi_version.argtypes = []
@@ -156,6 +167,19 @@ def lisa_backward(Q, K, V, dO, dQ, dK, dV, dalpha, B, heads, H, W, d_h, d_v, T, 
     return int(load().lisa_backward(Q, K, V, dO, dQ, dK, dV, dalpha, B, heads, H, W, d_h, d_v, T,
                                     ctypes.byref(wts), alpha, eps, relu_inputs, dtype, workspace,
                                     workspace_bytes, stream))
+
+
+def lisa_backward_mlp_workspace_bytes(B, heads, H, W, d_h, d_v, T, hidden, dtype) -> int:
+    return int(load().lisa_backward_mlp_workspace_bytes(B, heads, H, W, d_h, d_v, T, hidden, dtype))
+
+
+def lisa_backward_mlp(Q, K, V, dO, dQ, dK, dV, dalpha, mgrads, B, heads, H, W, d_h, d_v, T, wts, alpha, eps,
+                      relu_inputs, dtype, workspace, workspace_bytes, stream) -> int:
+    """mgrads: a lisa_mlp_grads (or None for a null pointer)."""
+    return int(load().lisa_backward_mlp(Q, K, V, dO, dQ, dK, dV, dalpha,
+                                        None if mgrads is None else ctypes.byref(mgrads), B, heads, H, W, d_h,
+                                        d_v, T, ctypes.byref(wts), alpha, eps, relu_inputs, dtype, workspace,
+                                        workspace_bytes, stream))
 
 
 def lisa_forward_host(hQ, hK, hV, hO, dQ, dK, dV, dO, B, heads, H, W, d_h, d_v, T, wts, alpha, eps,
@@ -237,11 +261,13 @@ def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, grid, T: int, *, 
 
 
 def backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, dO: torch.Tensor, grid, T: int, *,
-             alpha: torch.Tensor, beta=None, w=None, eps: float = 1e-6, relu: bool = True, workspace=None,
-             stream=None):
+             alpha: torch.Tensor, beta=None, w=None, mlp=None, eps: float = 1e-6, relu: bool = True,
+             workspace=None, stream=None):
     """Gradients of the LiSA forward on CUDA tensors [B, heads, H*W, d]
     (fp32 or bf16) for the upstream gradient ``dO``: returns
-    (dq, dk, dv, dalpha), dalpha fp32 [heads] summed over the batch."""
+    (dq, dk, dv, dalpha), dalpha fp32 [heads] summed over the batch.  With
+    ``mlp`` = (W1, b1, W2, b2) (adaptive weights) it returns a fifth item,
+    (dW1, db1, dW2, db2), the parameters' gradients summed over every slice."""
     for t in (q, k, v, dO, alpha):
         if not t.is_cuda:
             raise ValueError("lisa.backward runs on CUDA tensors only")
@@ -256,16 +282,31 @@ def backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, dO: torch.Tensor
     dv = v.shape[-1]
     dq, dk, dvv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     dalpha = torch.empty(heads, dtype=torch.float32, device=q.device)
-    wt, keep = make_weights(T, beta=beta, w=w)
+    wt, keep = make_weights(T, beta=beta, w=w, mlp=mlp)
     dt = _DTYPES[q.dtype]
-    nbytes = lisa_backward_workspace_bytes(B, heads, H, W, d, dv, T, dt)
+    st = torch.cuda.current_stream(q.device).cuda_stream if stream is None else stream
+    if mlp is None:
+        nbytes = lisa_backward_workspace_bytes(B, heads, H, W, d, dv, T, dt)
+    else:
+        hidden = int(mlp[0].shape[0])
+        nbytes = lisa_backward_mlp_workspace_bytes(B, heads, H, W, d, dv, T, hidden, dt)
+        pg = tuple(torch.empty_like(x) for x in mlp)
+        mg = lisa_mlp_grads(pg[0].data_ptr(), pg[1].data_ptr(), pg[2].data_ptr(), pg[3].data_ptr())
     if workspace is None:
         workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
-    st = torch.cuda.current_stream(q.device).cuda_stream if stream is None else stream
-    status = lisa_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), dO.data_ptr(), dq.data_ptr(), dk.data_ptr(),
-                           dvv.data_ptr(), dalpha.data_ptr(), B, heads, H, W, d, dv, T, wt, alpha.data_ptr(),
-                           float(eps), int(bool(relu)), dt, workspace.data_ptr(), workspace.numel(), st)
+    if mlp is None:
+        status = lisa_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), dO.data_ptr(), dq.data_ptr(),
+                               dk.data_ptr(), dvv.data_ptr(), dalpha.data_ptr(), B, heads, H, W, d, dv, T, wt,
+                               alpha.data_ptr(), float(eps), int(bool(relu)), dt, workspace.data_ptr(),
+                               workspace.numel(), st)
+    else:
+        status = lisa_backward_mlp(q.data_ptr(), k.data_ptr(), v.data_ptr(), dO.data_ptr(), dq.data_ptr(),
+                                   dk.data_ptr(), dvv.data_ptr(), dalpha.data_ptr(), mg, B, heads, H, W, d, dv, T,
+                                   wt, alpha.data_ptr(), float(eps), int(bool(relu)), dt, workspace.data_ptr(),
+                                   workspace.numel(), st)
     del keep
     if status != LISA_OK:
         raise LisaError(status)
+    if mlp is not None:
+        return dq, dk, dvv, dalpha, pg
     return dq, dk, dvv, dalpha

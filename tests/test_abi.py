@@ -220,3 +220,44 @@ def test_backward_weight_modes():
     wt.w = ctypes.cast(arr, ctypes.POINTER(ctypes.c_float))
     assert _bwd(wt=wt, T=0) == lisa.LISA_ERR_INVALID_ARG        # untruncated: geometric only
     assert _bwd(wt=wt, wbytes=16) == lisa.LISA_ERR_WORKSPACE
+
+
+def _bwd_mlp(wt=None, mg=True, **over):
+    args = dict(Q=FAKE, K=FAKE + 4096, V=FAKE + 8192, dO=FAKE + 12288, dQ=FAKE + 16384, dK=FAKE + 20480,
+                dV=FAKE + 24576, dalpha=FAKE + 28672, B=1, heads=1, H=4, W=4, d_h=16, d_v=16, T=3,
+                alpha=FAKE + 28688, eps=1e-6, relu=1, dtype=lisa.LISA_F32, workspace=FAKE + 65536,
+                wbytes=1 << 30, hidden=32)
+    args.update(over)
+    if wt is None:
+        wt = lisa.lisa_weights()
+        wt.mode = lisa.LISA_W_MLP
+        wt.W1 = wt.b1 = wt.W2 = wt.b2 = FAKE + 40960
+        wt.hidden = args["hidden"]
+    grads = lisa.lisa_mlp_grads(FAKE + 49152, FAKE + 50176, FAKE + 51200, FAKE + 52224) if mg is True else mg
+    return lisa.lisa_backward_mlp(args["Q"], args["K"], args["V"], args["dO"], args["dQ"], args["dK"], args["dV"],
+                                  args["dalpha"], grads, args["B"], args["heads"], args["H"], args["W"],
+                                  args["d_h"], args["d_v"], args["T"], wt, args["alpha"], args["eps"],
+                                  args["relu"], args["dtype"], args["workspace"], args["wbytes"], 0)
+
+
+def test_backward_mlp_workspace_bytes():
+    ws = lisa.lisa_backward_mlp_workspace_bytes
+    assert ws(8, 3, 24, 24, 64, 64, 3, 32, lisa.LISA_BF16) > lisa.lisa_backward_workspace_bytes(
+        8, 3, 24, 24, 64, 64, 3, lisa.LISA_BF16)
+    assert ws(1, 1, 4, 4, 64, 64, 9, 32, lisa.LISA_BF16) == 0        # T > LISA_MAX_T_MLP
+    assert ws(1, 1, 4, 4, 64, 64, 0, 32, lisa.LISA_BF16) == 0        # no untruncated adaptive walk
+    assert ws(1, 1, 4, 4, 64, 64, 3, 65, lisa.LISA_BF16) == 0        # hidden too wide
+    assert ws(1, 1, 4, 4, 64, 64, 3, 0, lisa.LISA_BF16) == 0
+
+
+def test_backward_mlp_rejects_before_launch():
+    assert _bwd_mlp(wbytes=1024) == lisa.LISA_ERR_WORKSPACE
+    assert _bwd_mlp(mg=None) == lisa.LISA_ERR_INVALID_ARG
+    assert _bwd_mlp(mg=lisa.lisa_mlp_grads(FAKE, 0, FAKE, FAKE)) == lisa.LISA_ERR_INVALID_ARG
+    assert _bwd_mlp(T=9) == lisa.LISA_ERR_UNSUPPORTED
+    assert _bwd_mlp(hidden=65) == lisa.LISA_ERR_UNSUPPORTED
+    assert _bwd_mlp(hidden=0) == lisa.LISA_ERR_INVALID_ARG
+    assert _bwd_mlp(dO=0) == lisa.LISA_ERR_INVALID_ARG
+    assert _bwd_mlp(eps=0.0) == lisa.LISA_ERR_INVALID_ARG
+    geo, _ = lisa.make_weights(3, beta=0.5)
+    assert _bwd_mlp(wt=geo) == lisa.LISA_ERR_INVALID_ARG         # adaptive weights only

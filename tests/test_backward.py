@@ -136,3 +136,59 @@ def test_deterministic_and_empty():
     dq, dk, dv, da = lisa.backward(q, q, q, q, (14, 14), 3, alpha=torch.full((3,), 0.5, device="cuda"),
                                    beta=0.5)
     assert dq.shape == q.shape and torch.equal(da.cpu(), torch.zeros(3))
+
+
+# -- adaptive (MLP) walk weights: lisa_backward_mlp ----------------------------------------
+
+def _check_mlp(dtype, d, H, W, T, *, B=2, heads=2, hidden=32, scale=1.0, seed=0, relu=True):
+    from hop_stochastic_vision_gb300 import lisa
+    shape = LayerShape("bwd_mlp", dtype, B, heads, H, W, d, T, "mlp", alpha="uniform(0.3,0.7)", hidden=hidden)
+    inp = make_inputs(shape, seed=seed)
+    for key in ("W1", "b1", "W2", "b2"):   # the paper's N(0, 0.02) init, optionally scaled up
+        inp[key] = inp[key] * scale
+    if not relu:
+        inp["xq"], inp["xk"] = inp["xq"].clamp_min(0), inp["xk"].clamp_min(0)
+    dO = _upstream(shape, B, heads)
+    dev = to_device(inp)
+    mlp_dev = tuple(dev[k] for k in ("W1", "b1", "W2", "b2"))
+    dq, dk, dv, da, pg = lisa.backward(dev["xq"], dev["xk"], dev["v"], dO.cuda(), (H, W), T, alpha=dev["alpha"],
+                                       mlp=mlp_dev, relu=relu)
+    torch.cuda.synchronize()
+    mlp = tuple(inp[k].double().numpy() for k in ("W1", "b1", "W2", "b2"))
+    want = oracle.backward(to_f64(inp["xq"]), to_f64(inp["xk"]), to_f64(inp["v"]), to_f64(dO), (H, W), T,
+                           alpha=inp["alpha"].double().numpy(), mlp=mlp, relu=relu)
+    got = [to_f64(x.cpu()) for x in (dq, dk, dv)]
+    for g in got:
+        assert np.isfinite(g).all()
+    err = joint_rel_err(got, want[:3])
+    assert err <= TOL[dtype], "gradient normwise err %.3e (%s d=%d T=%d)" % (err, dtype, d, T)
+    ptol = 1e-3 if dtype == "f32" else 2e-2
+    for name, g, ref in zip(("dW1", "db1", "dW2", "db2"), pg, want[4]):
+        g = g.cpu().double().numpy()
+        scale_ref = max(np.abs(ref).max(), 1e-30)
+        assert np.abs(g - ref).max() <= ptol * scale_ref, "%s err %.3e" % (name, np.abs(g - ref).max() / scale_ref)
+    np.testing.assert_allclose(da.cpu().double().numpy(), want[3], rtol=1e-3, atol=1e-3 * np.abs(want[3]).max())
+    return err
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d", [16, 32, 64])
+def test_mlp_widths(dtype, d):
+    _check_mlp(dtype, d, 7, 9, 3, scale=20.0)
+
+
+@pytest.mark.parametrize("T", [1, 2, 5, 8])
+def test_mlp_depths(T):
+    _check_mlp("f32", 32, 10, 11, T, scale=20.0)
+    _check_mlp("bf16", 64, 10, 11, T, scale=20.0)
+
+
+def test_mlp_hidden64_paper_init_and_no_feature_map():
+    _check_mlp("bf16", 64, 9, 12, 4, hidden=64, scale=20.0)
+    _check_mlp("bf16", 64, 12, 12, 3)                       # the paper's N(0, 0.02) init
+    _check_mlp("f32", 32, 8, 9, 3, scale=20.0, relu=False)
+
+
+def test_mlp_ragged_grid_and_full_size_deit384():
+    _check_mlp("bf16", 64, 57, 55, 3, B=1, heads=2, scale=20.0)
+    _check_mlp("bf16", 64, 24, 24, 3, B=64, heads=3, scale=20.0)   # the DeiT-T/384 layer's shape
