@@ -486,7 +486,7 @@ def ours_arm(args, shape):
 
 # -- the backward pass ------------------------------------------------------------------
 
-BWD_METRIC = "LiSA bwd tokens·heads/s at n=3136 bf16 (dXq, dXk, dV, dalpha); % of HBM roofline"
+BWD_METRIC = "LiSA bwd tokens·heads/s (gradients of Xq, Xk, V, alpha%s); % of HBM roofline"
 # algorithmic bytes per token*head: read Q, K, V, dO, write dQ, dK, dV (d = 64, bf16)
 BWD_BYTES_PER_TOKEN = 7 * 64 * 2
 
@@ -619,7 +619,8 @@ def backward_arm(args, shape):
                "sample": "%d repetitions of one (batch, head) slice (n=%d), double-precision oracle backward, "
                          "%.1f s" % (reps_c, n, el)}
     line = {
-        "metric": BWD_METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "metric": BWD_METRIC % (" and the MLP parameters" if mlp else ""), "value": value, "unit": UNIT,
+        "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": shape.dtype,
         "data": "synthetic (seeded N(0,1) inputs and upstream gradient; no dataset or weights)",
