@@ -82,6 +82,17 @@ def _f64(a):
     return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
 
 
+FEATURE_MAPS = {False: 0, True: 1, "none": 0, "relu": 1, "elu1": 2}
+
+
+def _fmap(relu):
+    """The feature-map code: relu=True (ReLU, the default), False (inputs are
+    the features), or "elu1" for phi(x) = ELU(x) + 1."""
+    if relu not in FEATURE_MAPS:
+        raise ValueError("relu must be True, False, 'none', 'relu' or 'elu1'")
+    return FEATURE_MAPS[relu]
+
+
 def _ptr(a):
     if a is None:
         return None
@@ -109,7 +120,8 @@ def forward(xq, xk, v, grid, T, *, alpha, beta=None, w=None, mlp=None, eps=1e-6,
     T) or ``mlp`` = (W1 [hidden, 2 d_h], b1 [hidden], W2 [T, hidden], b2 [T])
     selects the walk weights.  ``T = 0`` with ``beta`` is the untruncated
     geometric walk, g = (1 - beta) (I - beta S)^-1 V.  ``alpha`` is a scalar
-    or [heads].
+    or [heads].  ``relu``: the feature map -- True (ReLU, the paper's
+    default), False (the inputs are the features) or "elu1" (ELU(x) + 1).
     Returns O, or (O, G, L) with the global and local branches when
     ``branches`` is set.
     """
@@ -145,7 +157,7 @@ def forward(xq, xk, v, grid, T, *, alpha, beta=None, w=None, mlp=None, eps=1e-6,
     rc = _load().lisa_oracle_forward(
         _ptr(xq), _ptr(xk), _ptr(v), _ptr(O), _ptr(G), _ptr(L), B, heads, H, W, dh, dv, int(T),
         wmode, float(beta if beta is not None else 0.0), _ptr(wv), _ptr(W1), _ptr(b1), _ptr(W2),
-        _ptr(b2), hidden, _ptr(alpha), float(eps), int(bool(relu)), int(mode), int(nthreads))
+        _ptr(b2), hidden, _ptr(alpha), float(eps), _fmap(relu), int(mode), int(nthreads))
     if rc != 0:
         raise ValueError("lisa_oracle_forward failed with code %d" % rc)
     return (O, G, L) if branches else O
@@ -188,7 +200,7 @@ def backward(xq, xk, v, dO, grid, T, *, alpha, beta=None, w=None, mlp=None, eps=
         _ptr(xq), _ptr(xk), _ptr(v), _ptr(dO), _ptr(dXq), _ptr(dXk), _ptr(dV), _ptr(da), B, heads, H, W,
         dh, dv, int(T), wmode, float(beta if beta is not None else 0.0), _ptr(wv), _ptr(W1), _ptr(b1),
         _ptr(W2), _ptr(b2), hidden, _ptr(gW1), _ptr(gb1), _ptr(gW2), _ptr(gb2), _ptr(alpha), float(eps),
-        int(bool(relu)))
+        _fmap(relu))
     if rc != 0:
         raise ValueError("lisa_oracle_backward failed with code %d" % rc)
     if mlp is not None:
@@ -201,7 +213,7 @@ def transition(xq, xk, eps=1e-6, relu=True):
     xq, xk = _f64(xq), _f64(xk)
     n, dh = xq.shape
     S = np.empty((n, n))
-    if _load().lisa_oracle_transition(_ptr(xq), _ptr(xk), n, dh, float(eps), int(bool(relu)), _ptr(S)):
+    if _load().lisa_oracle_transition(_ptr(xq), _ptr(xk), n, dh, float(eps), _fmap(relu), _ptr(S)):
         raise ValueError("lisa_oracle_transition failed")
     return S
 
@@ -213,7 +225,7 @@ def step_weights(xq, xk, mlp, T, relu=True):
     W1, b1, W2, b2 = (_f64(x) for x in mlp)
     out = np.empty((n, T))
     rc = _load().lisa_oracle_step_weights(_ptr(xq), _ptr(xk), n, dh, int(T), _ptr(W1), _ptr(b1),
-                                          _ptr(W2), _ptr(b2), W1.shape[0], int(bool(relu)), _ptr(out))
+                                          _ptr(W2), _ptr(b2), W1.shape[0], _fmap(relu), _ptr(out))
     if rc:
         raise ValueError("lisa_oracle_step_weights failed")
     return out

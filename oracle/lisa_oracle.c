@@ -98,14 +98,35 @@ int lisa_oracle_geometric_weights(double beta, int T, double *w)
     return 0;
 }
 
-/* Feature map [note §2.1]: Q = ReLU(Xq), K = ReLU(Xk), or a plain copy when
- * the caller has already applied it. */
-static void feature_map(const double *X, double *out, long count, int relu)
+/* Feature map [note §2.1]: the argument `fmap` of every entry point is
+ *   0  none: the inputs are the features (already non-negative);
+ *   1  ReLU: Q = max(Xq, 0), K = max(Xk, 0) (the paper's default);
+ *   2  ELU + 1: phi(x) = x + 1 for x > 0, exp(x) otherwise.  The note (§2.1;
+ *      paper Table 8) compares an ELU feature map with ReLU; the non-negative
+ *      form ELU(x) + 1 is the reading taken, since the transition S must stay
+ *      non-negative and row-stochastic. */
+#define ORACLE_FMAP_NONE 0
+#define ORACLE_FMAP_RELU 1
+#define ORACLE_FMAP_ELU1 2
+
+static double feature_value(double x, int fmap)
 {
-    for (long t = 0; t < count; ++t) {
-        double x = X[t];
-        out[t] = (relu && x < 0.0) ? 0.0 : x;
-    }
+    if (fmap == ORACLE_FMAP_RELU) return x < 0.0 ? 0.0 : x;
+    if (fmap == ORACLE_FMAP_ELU1) return x > 0.0 ? x + 1.0 : exp(x);
+    return x;
+}
+
+/* d phi / dx at x (the backward's mask or scale). */
+static double feature_slope(double x, int fmap)
+{
+    if (fmap == ORACLE_FMAP_RELU) return x > 0.0 ? 1.0 : 0.0;
+    if (fmap == ORACLE_FMAP_ELU1) return x > 0.0 ? 1.0 : exp(x);
+    return 1.0;
+}
+
+static void feature_map(const double *X, double *out, long count, int fmap)
+{
+    for (long t = 0; t < count; ++t) out[t] = feature_value(X[t], fmap);
 }
 
 /* s = sum over every token j of K_j  [note §2.2]. */
@@ -391,7 +412,7 @@ static void local_branch(const double *Qf, const double *Kf, const double *V,
 /* alpha mix  o = alpha * g + (1 - alpha) * l  [note §2.4] (paper Fig. 2).   */
 /* ---------------------------------------------------------------------- */
 typedef struct {
-    int H, W, dh, dv, T, wmode, hidden, mode, relu;   /* T = 0: untruncated walk */
+    int H, W, dh, dv, T, wmode, hidden, mode, relu;   /* T = 0: untruncated walk; relu: the fmap */
     double eps, beta;
     const double *w, *W1, *b1, *W2, *b2;
 } slice_args;
@@ -464,6 +485,7 @@ done:
  *   T       walk truncation depth >= 1; 0 with geometric weights: untruncated
  *   alpha   [heads]
  *   mode    0 EXPLICIT, 1 LOWRANK
+ *   relu_inputs  the feature map: 0 none, 1 ReLU, 2 ELU + 1
  *   O, G, L may each be NULL; G and L receive the global and local branches.
  *   nthreads <= 0 uses the OpenMP default.
  * Returns 0 on success, 1 on a bad argument, 2 on allocation failure, 3 when
@@ -480,7 +502,7 @@ int lisa_oracle_forward(const double *Xq, const double *Xk, const double *V,
     if (B < 0 || heads < 0 || H < 1 || W < 1 || dh < 1 || dh > 256 || dv < 1 || T < 0 ||
         T > ORACLE_MAX_T)
         return 1;
-    if (eps < 0.0 || !alpha) return 1;
+    if (eps < 0.0 || !alpha || relu_inputs < 0 || relu_inputs > 2) return 1;
     if (T == 0 && (wmode != ORACLE_W_GEOMETRIC || !(beta >= 0.0) || !(beta < 1.0))) return 1;
     double *wts = malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
     if (!wts) return 2;
@@ -930,8 +952,8 @@ stats_tail:
 
     /* ---- feature map */
     for (size_t t = 0; t < nd; ++t) {
-        dXq[t] = (A->relu && !(Xq[t] > 0.0)) ? 0.0 : dQ[t];
-        dXk[t] = (A->relu && !(Xk[t] > 0.0)) ? 0.0 : dK[t];
+        dXq[t] = feature_slope(Xq[t], A->relu) * dQ[t];
+        dXk[t] = feature_slope(Xk[t], A->relu) * dK[t];
     }
 done:
     free(Q); free(K); free(Qt); free(r); free(M); free(Uk); free(Ub); free(dUb); free(G);
@@ -959,7 +981,7 @@ int lisa_oracle_backward(const double *Xq, const double *Xk, const double *V,
                          int relu_inputs)
 {
     if (B < 0 || heads < 1 || H < 1 || W < 1 || dh < 1 || dh > 256 || dv < 1 || T < 0 ||
-        T > ORACLE_MAX_T || eps < 0.0 || !alpha)
+        T > ORACLE_MAX_T || eps < 0.0 || !alpha || relu_inputs < 0 || relu_inputs > 2)
         return 1;
     if (T == 0 && wmode != ORACLE_W_GEOMETRIC) return 1;
     if (wmode == ORACLE_W_MLP && (T < 1 || !W1 || !b1 || !W2 || !b2 || hidden < 1 ||

@@ -414,3 +414,45 @@ def test_zero_query_row_gives_w0_V():
     _, G, _ = oracle.forward(xq, xk, v, (3, 4), 3, alpha=1.0, beta=0.5, branches=True)
     w0 = oracle.geometric_weights(0.5, 3)[0]
     assert G[0, 0, 5].tolist() == (w0 * v[0, 0, 5]).tolist()
+
+
+# -- the ELU + 1 feature map (note section 2.1; paper Table 8 compares ELU with ReLU) -------
+
+def test_elu_feature_map_transition_is_row_stochastic_and_low_rank():
+    """phi(x) = ELU(x) + 1 > 0 keeps S non-negative with rows summing to
+    Q~_i . s < 1 by eps only, and of rank <= d_h, like the ReLU map."""
+    n, d = 30, 4
+    xq, xk = RNG.standard_normal((n, d)), RNG.standard_normal((n, d))
+    S = oracle.transition(xq, xk, eps=1e-6, relu="elu1")
+    assert (S > 0).all()                                   # every feature positive: no zero entries
+    np.testing.assert_allclose(S.sum(axis=1), 1.0, rtol=0, atol=1e-5)
+    assert np.linalg.matrix_rank(S, tol=1e-10) <= d
+    S0 = oracle.transition(xq, xk, eps=0.0, relu="elu1")
+    np.testing.assert_allclose(S0.sum(axis=1), 1.0, rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("T", [0, 1, 3, 5])
+def test_elu_feature_map_routes_agree(T):
+    grid, d = (4, 5), 6
+    xq, xk, v = _rand(1, 2, 20, d), _rand(1, 2, 20, d), _rand(1, 2, 20, d)
+    e = oracle.forward(xq, xk, v, grid, T, alpha=[0.4, 0.6], beta=0.5, relu="elu1", mode=oracle.EXPLICIT)
+    l = oracle.forward(xq, xk, v, grid, T, alpha=[0.4, 0.6], beta=0.5, relu="elu1", mode=oracle.LOWRANK)
+    np.testing.assert_allclose(e, l, rtol=0, atol=1e-10)
+
+
+def test_elu_feature_map_differs_from_relu_and_matches_on_positive_inputs_shifted():
+    """For inputs all > 0, ELU(x) + 1 = x + 1: the ELU layer on X equals the
+    no-feature-map layer on X + 1 (a closed form of the map)."""
+    grid, d = (3, 4), 5
+    xq, xk, v = np.abs(_rand(1, 1, 12, d)) + 0.1, np.abs(_rand(1, 1, 12, d)) + 0.1, _rand(1, 1, 12, d)
+    a = oracle.forward(xq, xk, v, grid, 3, alpha=0.5, beta=0.5, relu="elu1")
+    b = oracle.forward(xq + 1.0, xk + 1.0, v, grid, 3, alpha=0.5, beta=0.5, relu=False)
+    np.testing.assert_allclose(a, b, rtol=0, atol=1e-13)
+    c = oracle.forward(xq, xk, v, grid, 3, alpha=0.5, beta=0.5, relu=True)
+    assert np.abs(a - c).max() > 1e-3
+
+
+def test_feature_map_argument_checked():
+    xq = _rand(1, 1, 4, 2)
+    with pytest.raises(ValueError):
+        oracle.forward(xq, xq, xq, (2, 2), 3, alpha=0.5, beta=0.5, relu="elu")

@@ -229,3 +229,21 @@ def test_mlp_backward_reduces_to_geometric():
     gW1, gb1, gW2, gb2 = a[4]
     assert np.all(gW1 == 0) and np.all(gb1 == 0)
     np.testing.assert_allclose(gb2.sum(), 0.0, atol=1e-12)     # softmax: dz sums to zero per token
+
+
+@pytest.mark.parametrize("T,kw", [(3, {"beta": 0.5}), (0, {"beta": 0.6}), (3, {"mlp": _mlp_params(5, 3)})])
+def test_backward_through_elu_feature_map(T, kw):
+    """phi(x) = ELU(x) + 1: the feature map's slope is exp(x) for x <= 0."""
+    grid, d = (3, 3), 5
+    xq, xk, v, dO = _case(1, 1, 3, 3, d)
+    res = oracle.backward(xq, xk, v, dO, grid, T, alpha=0.45, relu="elu1", **kw)
+    h = 1e-6
+    for arr, grad in ((xq, res[0]), (xk, res[1])):
+        for idx in np.ndindex(arr.shape):
+            keep = arr[idx]
+            arr[idx] = keep + h
+            up = float((oracle.forward(xq, xk, v, grid, T, alpha=0.45, relu="elu1", **kw) * dO).sum())
+            arr[idx] = keep - h
+            dn = float((oracle.forward(xq, xk, v, grid, T, alpha=0.45, relu="elu1", **kw) * dO).sum())
+            arr[idx] = keep
+            assert abs((up - dn) / (2 * h) - grad[idx]) <= 1e-6 * max(np.abs(grad).max(), 1.0)
