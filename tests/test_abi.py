@@ -261,3 +261,26 @@ def test_backward_mlp_rejects_before_launch():
     assert _bwd_mlp(eps=0.0) == lisa.LISA_ERR_INVALID_ARG
     geo, _ = lisa.make_weights(3, beta=0.5)
     assert _bwd_mlp(wt=geo) == lisa.LISA_ERR_INVALID_ARG         # adaptive weights only
+
+
+def test_untruncated_walk_runs_the_T2_chain():
+    """T = 0 (untruncated) runs the kernels of a T = 2 fixed-weight walk."""
+    for args in ((32, 1, 56, 56, 64), (1, 4, 128, 128, 64), (2, 2, 11, 13, 16)):
+        for dt in (lisa.LISA_BF16, lisa.LISA_F32):
+            wt, _ = lisa.make_weights(1, beta=0.5)
+            n0 = lisa.lisa_num_stages(*args, 0, dt, wt)
+            assert n0 == lisa.lisa_num_stages(*args, 2, dt, wt) > 0
+            assert [lisa.lisa_stage_name(*args, 0, dt, wt, i) for i in range(n0)] == \
+                [lisa.lisa_stage_name(*args, 2, dt, wt, i) for i in range(n0)]
+            assert lisa.lisa_workspace_bytes(*args[:4], args[4], args[4], 0, dt) == \
+                lisa.lisa_workspace_bytes(*args[:4], args[4], args[4], 2, dt)
+
+
+def test_backward_workspaces_and_version():
+    assert lisa.lisa_abi_version() >= 102
+    for B, heads, H, W, d in ((32, 1, 56, 56, 64), (2, 3, 9, 11, 16)):
+        plain = lisa.lisa_backward_workspace_bytes(B, heads, H, W, d, d, 3, lisa.LISA_BF16)
+        for hidden in (1, 32, 64):
+            assert lisa.lisa_backward_mlp_workspace_bytes(B, heads, H, W, d, d, 3, hidden, lisa.LISA_BF16) > plain
+        assert lisa.lisa_backward_mlp_workspace_bytes(B, heads, H, W, d, d, 5, 32, lisa.LISA_BF16) > \
+            lisa.lisa_backward_mlp_workspace_bytes(B, heads, H, W, d, d, 3, 32, lisa.LISA_BF16)
