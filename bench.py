@@ -166,18 +166,27 @@ def hbm_peak():
 
 
 # The files the tensor-core forward kernels are built from (the kernels whose
-# DRAM traffic profiles/traffic.json records): a change to any of them voids
-# the recorded counters; other kernels' sources do not.
+# DRAM traffic profiles/traffic.json records): a change to their code voids
+# the recorded counters; comments and other kernels' sources do not.
 TRAFFIC_SOURCES = ("hop_stochastic_vision_gb300/csrc/lisa_tc.cu", "hop_stochastic_vision_gb300/csrc/lisa_sm100.cuh",
                    "hop_stochastic_vision_gb300/csrc/lisa_solve.cuh",
                    "hop_stochastic_vision_gb300/csrc/lisa_internal.h", "include/lisa.h")
 
 
+def _code_only(text: str) -> str:
+    """The source with its comments and blank space removed: what the compiler
+    sees of it, so an edit to a comment does not void the recorded counters."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def source_hash() -> str:
     h = hashlib.sha256()
     for rel in TRAFFIC_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(os.path.basename(rel).encode() + b"\0" + f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(os.path.basename(rel).encode() + b"\0" + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
