@@ -1,6 +1,7 @@
 // lisa_api.cu -- the C ABI of liblisa.so: argument checks, the split-K plan,
 // the workspace carve-up, host-side walk weights, and dispatch to the kernel
 // families.  Every check runs on the host before the first launch.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -116,6 +117,11 @@ lisa_status check_sizes(int B, int heads, int H, int W, int d_h, int d_v, int T,
 // whose single hop matrix comes from the d x d solve.
 int effective_T(int T) { return T == 0 ? 2 : T; }
 
+// The dtype that picks the kernel family: the ELU + 1 feature map
+// (relu_inputs = 2) runs the SIMT chain whatever the data type, since the
+// tensor-core kernels apply ReLU in their bf16 staging.
+int family_dtype(int dtype, int relu_inputs) { return relu_inputs == 2 ? (int)LISA_F32 : dtype; }
+
 // Walk weights of a call into p (T, w, wmode, the untruncated flag).
 lisa_status resolve_weights(Problem &p, const lisa_weights *wts, int T) {
     p.T = effective_T(T);
@@ -207,11 +213,13 @@ extern "C" size_t lisa_workspace_bytes(int B, int heads, int H, int W, int d_h, 
     const long long slices = (long long)B * heads, n = (long long)H * W;
     if (slices == 0 || n == 0) return 0;
     T = effective_T(T);
-    // the weight mode is not known here: size for whichever needs more
-    size_t need = make_plan((int)slices, (int)n, d_h, T, dtype, LISA_W_FIXED, 0).total;
-    for (int hidden : {16, LISA_MAX_HIDDEN}) {
-        const size_t m = make_plan((int)slices, (int)n, d_h, T, dtype, LISA_W_MLP, hidden).total;
-        if (m > need) need = m;
+    // neither the weight mode nor the feature map is known here: size for
+    // whichever needs more (the ELU map runs the SIMT chain for every dtype)
+    size_t need = 0;
+    for (int fam_dtype : {dtype, (int)LISA_F32}) {
+        need = std::max(need, make_plan((int)slices, (int)n, d_h, T, fam_dtype, LISA_W_FIXED, 0).total);
+        for (int hidden : {16, LISA_MAX_HIDDEN})
+            need = std::max(need, make_plan((int)slices, (int)n, d_h, T, fam_dtype, LISA_W_MLP, hidden).total);
     }
     return need;
 }
@@ -229,7 +237,7 @@ lisa_status prepare(Problem &p, bool &empty, const void *Q, const void *K, const
     if (st != LISA_OK) return st;
     if (!wts) return LISA_ERR_INVALID_ARG;
     if (!(eps > 0.f) || !std::isfinite(eps)) return LISA_ERR_INVALID_ARG;
-    if (relu_inputs != 0 && relu_inputs != 1) return LISA_ERR_INVALID_ARG;
+    if (relu_inputs < 0 || relu_inputs > 2) return LISA_ERR_INVALID_ARG;
 
     p = Problem{};
     st = resolve_weights(p, wts, T);
@@ -248,7 +256,7 @@ lisa_status prepare(Problem &p, bool &empty, const void *Q, const void *K, const
     if (overlaps(O, bytes, Q, bytes) || overlaps(O, bytes, K, bytes) || overlaps(O, bytes, V, bytes))
         return LISA_ERR_INVALID_ARG;
 
-    const Plan pl = make_plan((int)slices, (int)n, d_h, p.T, dtype, p.wmode, p.hidden);
+    const Plan pl = make_plan((int)slices, (int)n, d_h, p.T, family_dtype(dtype, relu_inputs), p.wmode, p.hidden);
     if (!workspace || workspace_bytes < pl.total) return LISA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return LISA_ERR_INVALID_ARG;
     fill_problem(p, pl, Q, K, V, O, (int)slices, heads, H, W, d_h, relu_inputs, eps, alpha, dtype, workspace);
@@ -350,6 +358,7 @@ extern "C" lisa_status lisa_forward_stage(int stage, const void *Q, const void *
     lisa_status st = prepare(p, empty, Q, K, V, O, B, heads, H, W, d_h, d_v, T, wts, alpha, eps,
                              relu_inputs, dtype, workspace, workspace_bytes);
     if (st != LISA_OK) return st;
+    if (relu_inputs == 2) return LISA_ERR_INVALID_ARG;   // the stage list describes the ReLU chains
     if (stage < 0 || stage >= lisa_num_stages(B, heads, H, W, d_h, T, dtype, wts))
         return LISA_ERR_INVALID_ARG;
     if (empty) return LISA_OK;
@@ -418,8 +427,8 @@ extern "C" lisa_status lisa_forward_noalloc(const void *Q, const void *K, const 
     const long long slices = (long long)B * heads, n = (long long)H * W;
     const size_t need = (slices == 0 || n == 0 || !wts)
                             ? 0
-                            : make_plan((int)slices, (int)n, d_h, effective_T(T), dtype,
-                                        weights_mode(wts), wts->hidden)
+                            : make_plan((int)slices, (int)n, d_h, effective_T(T),
+                                        family_dtype(dtype, relu_inputs), weights_mode(wts), wts->hidden)
                                   .total;
     if (need > (size_t)LISA_NOALLOC_SCRATCH_BYTES) return LISA_ERR_WORKSPACE;
     void *scratch = nullptr;
@@ -500,7 +509,7 @@ lisa_status run_backward(const void *Q, const void *K, const void *V, const void
     lisa_status st = check_sizes(B, heads, H, W, d_h, d_v, T, dtype);
     if (st != LISA_OK) return st;
     if (!(eps > 0.f) || !std::isfinite(eps)) return LISA_ERR_INVALID_ARG;
-    if (relu_inputs != 0 && relu_inputs != 1) return LISA_ERR_INVALID_ARG;
+    if (relu_inputs < 0 || relu_inputs > 2) return LISA_ERR_INVALID_ARG;
     BwdProblem b{};
     st = resolve_weights(b.fwd, wts, T);
     if (st != LISA_OK) return st;

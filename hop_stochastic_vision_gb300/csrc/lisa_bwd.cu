@@ -61,7 +61,13 @@ __device__ __forceinline__ float ld(const float *p) { return *p; }
 __device__ __forceinline__ float ld(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
 __device__ __forceinline__ void st(float *p, float v) { *p = v; }
 __device__ __forceinline__ void st(__nv_bfloat16 *p, float v) { *p = __float2bfloat16_rn(v); }
-__device__ __forceinline__ float relu_if(float x, int relu) { return (relu && x < 0.f) ? 0.f : x; }
+// The feature map applied on load; `fmap` is the call's relu_inputs:
+// 0 the inputs are the features, 1 ReLU, 2 ELU(x) + 1.
+__device__ __forceinline__ float feature(float x, int fmap) {
+    if (fmap == 1) return x < 0.f ? 0.f : x;
+    if (fmap == 2) return x > 0.f ? x + 1.f : expf(x);
+    return x;
+}
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -186,7 +192,7 @@ __global__ void __launch_bounds__(kThreads) bwd_stats_dub(BwdProblem b) {
             const int j = idx / D, ch = idx % D;
             float qv = 0.f, gv = 0.f;
             if (j < cnt) {
-                qv = relu_if(ld(Q + (size_t)(base + j) * D + ch), p.relu);
+                qv = feature(ld(Q + (size_t)(base + j) * D + ch), p.relu);
                 gv = al * ld(dO + (size_t)(base + j) * D + ch);
             }
             Qs[j][ch] = qv;
@@ -254,7 +260,7 @@ __global__ void __launch_bounds__(kThreads) bwd_stats_duk(BwdProblem b) {
             const int j = idx / D, ch = idx % D;
             float qv = 0.f, gv = 0.f;
             if (j < cnt) {
-                qv = relu_if(ld(Q + (size_t)(base + j) * D + ch), p.relu);
+                qv = feature(ld(Q + (size_t)(base + j) * D + ch), p.relu);
                 gv = al * wt[(size_t)(base + j) * p.T + k] * ld(dO + (size_t)(base + j) * D + ch);
             }
             Qs[j][ch] = qv;
@@ -304,6 +310,14 @@ __device__ __forceinline__ int window(int i, int H, int W, int (&nb)[9]) {
     return cnt;
 }
 
+// dL/dx from dL/dphi(x) through the feature map: ReLU passes x > 0 only,
+// ELU(x) + 1 has slope exp(x) below 0.
+__device__ __forceinline__ float feature_grad(float g, float x, int fmap) {
+    if (fmap == 1) return x > 0.f ? g : 0.f;
+    if (fmap == 2) return x > 0.f ? g : g * expf(x);
+    return g;
+}
+
 // Warp sums of n independent per-lane partials, the butterflies interleaved so
 // their shuffle latencies overlap.
 template <int N>
@@ -320,7 +334,7 @@ __device__ __forceinline__ void load_row(const TIn *row, float (&x)[(D + 31) / 3
 #pragma unroll
     for (int t = 0; t < (D + 31) / 32; ++t) {
         const int ch = lane + 32 * t;
-        x[t] = ch < D ? relu_if(ld(row + ch), relu) : 0.f;
+        x[t] = ch < D ? feature(ld(row + ch), relu) : 0.f;
     }
 }
 template <int D>
@@ -814,9 +828,9 @@ __global__ void __launch_bounds__(kThreads) bwd_token_b(BwdProblem b) {
         float q = 0.f, g = 0.f, k = 0.f, v = 0.f;
         if (j < cnt) {
             const size_t o = (size_t)(j0 + j) * D + ch;
-            q = relu_if(ld(Q + o), p.relu);
+            q = feature(ld(Q + o), p.relu);
             g = ld(dO + o);
-            k = relu_if(ld(K + o), p.relu);
+            k = feature(ld(K + o), p.relu);
             v = ld(V + o);
         }
         Qr[x] = q;
@@ -970,7 +984,7 @@ __global__ void __launch_bounds__(kThreads) bwd_token_b(BwdProblem b) {
             const int ch = lane + 32 * t;
             if (ch < D) {
                 const float xq = ld(Q + (size_t)j * D + ch);
-                st(dQo + (size_t)j * D + ch, (p.relu && !(xq > 0.f)) ? 0.f : dq[t]);
+                st(dQo + (size_t)j * D + ch, feature_grad(dq[t], xq, p.relu));
                 st(dVo + (size_t)j * D + ch, dv[t]);
                 dKp[(size_t)j * D + ch] = dk[t];
             }
@@ -1261,7 +1275,7 @@ __global__ void __launch_bounds__(kThreads) bwd_mlp_params(BwdProblem b) {
         for (int x = tid; x < kTok * 2 * D; x += kThreads) {
             const int j = x / (2 * D), ch = x % (2 * D);
             float v = 0.f;
-            if (j < cnt) v = relu_if(ld((ch < D ? Q : K) + (size_t)(base + j) * D + (ch % D)), p.relu);
+            if (j < cnt) v = feature(ld((ch < D ? Q : K) + (size_t)(base + j) * D + (ch % D)), p.relu);
             Xs[j][ch] = v;
         }
         for (int x = tid; x < kTok * LISA_MAX_HIDDEN; x += kThreads) {
@@ -1358,7 +1372,7 @@ __global__ void __launch_bounds__(kThreads) bwd_finish_k(BwdProblem b) {
         const int ch = (int)(x % D);
         const long long sl = x / ((long long)p.n * D);
         const float v = b.dk_part[x] + b.ds_red[sl * D + ch];
-        st(dKo + x, (p.relu && !(ld(K + x) > 0.f)) ? 0.f : v);
+        st(dKo + x, feature_grad(v, ld(K + x), p.relu));
     }
 }
 
@@ -1393,7 +1407,9 @@ cudaError_t launch_bwd_all(const BwdProblem &b, cudaStream_t st) {
         bwd_token_a<TIn, D><<<grid_tok, kThreads, 0, st>>>(b);
     }
     bwd_recur_back<D><<<p.slices, kThreads, 0, st>>>(b);
-    if constexpr (std::is_same<TIn, __nv_bfloat16>::value && D == 64) {
+    // bf16 at d = 64 takes the tensor-core token pass, except with the ELU map
+    // (its bf16 staging applies ReLU only)
+    if (std::is_same<TIn, __nv_bfloat16>::value && D == 64 && p.relu != 2) {
         bwd_bimg<<<dim3((unsigned)p.slices, 5), kThreads, 0, st>>>(b);
         if ((err = cudaFuncSetAttribute(bwd_token_b_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         kTcSmemBytes)) != cudaSuccess)

@@ -23,7 +23,7 @@ struct Problem {
     int T;             // truncation depth (2 for the untruncated walk: w_0 V + Q~ U-bar)
     int untruncated;   // geometric walk without truncation: U-bar = beta (1-beta) (I - beta M)^-1 U_1
     float beta;        // its continue probability
-    int relu;          // apply ReLU to Q and K on load
+    int relu;          // feature map of Q and K on load: 0 none, 1 ReLU, 2 ELU + 1 (SIMT chains only)
     float eps;
     const float *alpha;  // device [heads]
     int wmode;           // LISA_W_* after GEOMETRIC has been resolved to FIXED

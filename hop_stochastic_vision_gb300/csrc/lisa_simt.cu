@@ -33,7 +33,13 @@ __device__ __forceinline__ float load_elem(const __nv_bfloat16 *p) { return __bf
 __device__ __forceinline__ void store_elem(float *p, float v) { *p = v; }
 __device__ __forceinline__ void store_elem(__nv_bfloat16 *p, float v) { *p = __float2bfloat16_rn(v); }
 
-__device__ __forceinline__ float relu_if(float x, int relu) { return (relu && x < 0.f) ? 0.f : x; }
+// The feature map applied on load; `fmap` is the call's relu_inputs:
+// 0 the inputs are the features, 1 ReLU, 2 ELU(x) + 1.
+__device__ __forceinline__ float feature(float x, int fmap) {
+    if (fmap == 1) return x < 0.f ? 0.f : x;
+    if (fmap == 2) return x > 0.f ? x + 1.f : expf(x);
+    return x;
+}
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -68,7 +74,7 @@ __global__ void __launch_bounds__(kThreads) stats_kv_kernel(Problem p) {
             const int j = idx / D, ch = idx % D;
             float kv = 0.f, vv = 0.f;
             if (j < cnt) {
-                kv = relu_if(load_elem(K + (size_t)(base + j) * D + ch), p.relu);
+                kv = feature(load_elem(K + (size_t)(base + j) * D + ch), p.relu);
                 vv = load_elem(V + (size_t)(base + j) * D + ch);
             }
             Ks[j][ch] = kv;
@@ -133,8 +139,8 @@ __global__ void __launch_bounds__(kThreads) stats_kq_kernel(Problem p) {
             const int j = idx / D, ch = idx % D;
             float kv = 0.f, qv = 0.f;
             if (j < cnt) {
-                kv = relu_if(load_elem(K + (size_t)(base + j) * D + ch), p.relu);
-                qv = relu_if(load_elem(Q + (size_t)(base + j) * D + ch), p.relu);
+                kv = feature(load_elem(K + (size_t)(base + j) * D + ch), p.relu);
+                qv = feature(load_elem(Q + (size_t)(base + j) * D + ch), p.relu);
             }
             Ks[j][ch] = kv;
             Qs[j][ch] = qv;
@@ -277,8 +283,8 @@ __global__ void __launch_bounds__(kThreads) epilogue_kernel(Problem p) {
         const int ch = lane + 32 * t;
         q[t] = k[t] = v[t] = 0.f;
         if (ch < D) {
-            q[t] = relu_if(load_elem(Q + (size_t)i * D + ch), p.relu);
-            k[t] = relu_if(load_elem(K + (size_t)i * D + ch), p.relu);
+            q[t] = feature(load_elem(Q + (size_t)i * D + ch), p.relu);
+            k[t] = feature(load_elem(K + (size_t)i * D + ch), p.relu);
             v[t] = load_elem(V + (size_t)i * D + ch);
         }
     }
@@ -360,7 +366,7 @@ __global__ void __launch_bounds__(kThreads) epilogue_kernel(Problem p) {
 #pragma unroll
         for (int t = 0; t < NC; ++t) {
             const int ch = lane + 32 * t;
-            if (ch < D) acc += q[t] * relu_if(load_elem(K + (size_t)nb[t9] * D + ch), p.relu);
+            if (ch < D) acc += q[t] * feature(load_elem(K + (size_t)nb[t9] * D + ch), p.relu);
         }
         e[t9] = warp_sum(acc) * scale;
         emax = fmaxf(emax, e[t9]);

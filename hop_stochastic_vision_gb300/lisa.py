@@ -193,6 +193,17 @@ def lisa_forward_host(hQ, hK, hV, hO, dQ, dK, dV, dO, B, heads, H, W, d_h, d_v, 
 
 _DTYPES = {torch.float32: LISA_F32, torch.bfloat16: LISA_BF16}
 
+# relu_inputs codes: the feature map applied to Q and K on load
+_FEATURE_MAPS = {False: 0, True: 1, "none": 0, "relu": 1, "elu1": 2}
+
+
+def feature_map_code(relu) -> int:
+    """relu=True (ReLU, the default), False (the inputs are the features) or
+    "elu1" (ELU(x) + 1) as the C ABI's relu_inputs value."""
+    if relu not in _FEATURE_MAPS:
+        raise ValueError("relu must be True, False, 'none', 'relu' or 'elu1'")
+    return _FEATURE_MAPS[relu]
+
 
 def make_weights(T: int, beta=None, w=None, mlp=None):
     """Build the lisa_weights struct.  Returns (struct, keepalive) -- keep the
@@ -252,7 +263,7 @@ def forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, grid, T: int, *, 
         workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
     st = torch.cuda.current_stream(q.device).cuda_stream if stream is None else stream
     status = lisa_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), O.data_ptr(), B, heads, H, W, d,
-                          dv, T, wt, alpha.data_ptr(), float(eps), int(bool(relu)), dt,
+                          dv, T, wt, alpha.data_ptr(), float(eps), feature_map_code(relu), dt,
                           workspace.data_ptr(), workspace.numel(), st)
     del keep
     if status != LISA_OK:
@@ -297,12 +308,12 @@ def backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, dO: torch.Tensor
     if mlp is None:
         status = lisa_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), dO.data_ptr(), dq.data_ptr(),
                                dk.data_ptr(), dvv.data_ptr(), dalpha.data_ptr(), B, heads, H, W, d, dv, T, wt,
-                               alpha.data_ptr(), float(eps), int(bool(relu)), dt, workspace.data_ptr(),
+                               alpha.data_ptr(), float(eps), feature_map_code(relu), dt, workspace.data_ptr(),
                                workspace.numel(), st)
     else:
         status = lisa_backward_mlp(q.data_ptr(), k.data_ptr(), v.data_ptr(), dO.data_ptr(), dq.data_ptr(),
                                    dk.data_ptr(), dvv.data_ptr(), dalpha.data_ptr(), mg, B, heads, H, W, d, dv, T,
-                                   wt, alpha.data_ptr(), float(eps), int(bool(relu)), dt, workspace.data_ptr(),
+                                   wt, alpha.data_ptr(), float(eps), feature_map_code(relu), dt, workspace.data_ptr(),
                                    workspace.numel(), st)
     del keep
     if status != LISA_OK:

@@ -94,8 +94,10 @@ size_t lisa_workspace_bytes(int B, int heads, int H, int W, int d_h, int d_v, in
 /*
  * The LiSA forward layer [note §2.1-2.4] on device buffers.
  *   Q, K        device [B][heads][H*W][d_h], dtype; raw projections Xq, Xk
- *               when relu_inputs = 1 (ReLU applied on load), or already
- *               feature-mapped (non-negative) when relu_inputs = 0.
+ *               when relu_inputs = 1 (ReLU applied on load) or 2 (the
+ *               ELU(x) + 1 feature map applied on load [note §2.1; paper
+ *               Table 8]; served by the SIMT kernels for every dtype), or
+ *               already feature-mapped (non-negative) when relu_inputs = 0.
  *   V           device [B][heads][H*W][d_v], dtype.
  *   O           device [B][heads][H*W][d_v], dtype; written.
  *   T           truncation depth, 1..LISA_MAX_T (1..LISA_MAX_T_MLP for MLP);
@@ -104,7 +106,7 @@ size_t lisa_workspace_bytes(int B, int heads, int H, int W, int d_h, int d_v, in
  *               g = (1-beta) (V + beta Q~ X) with (I - beta M) X = U_1,
  *               M = K^T Q~ (the push-through identity; a d x d solve per
  *               slice).  That system is well posed because the features
- *               are non-negative (relu_inputs = 1, or inputs that already
+ *               are non-negative (relu_inputs = 1 or 2, or inputs that already
  *               are): I - beta M is then a nonsingular M-matrix.  T = 0 with
  *               LISA_W_FIXED or LISA_W_MLP is LISA_ERR_INVALID_ARG.
  *   wts         host struct; see lisa_weights.
@@ -144,7 +146,8 @@ lisa_status lisa_forward_host(const void *hQ, const void *hK, const void *hV, vo
  * width); lisa_num_stages returns 0 for arguments lisa_forward would reject
  * or for an empty problem.  lisa_stage_name returns the kernel's name, or
  * NULL for a bad index.
- * A bad stage index returns LISA_ERR_INVALID_ARG.
+ * A bad stage index, or relu_inputs = 2 (the list describes the chains of
+ * relu_inputs 0 and 1), returns LISA_ERR_INVALID_ARG.
  */
 int lisa_num_stages(int B, int heads, int H, int W, int d_h, int T, int dtype,
                     const lisa_weights *wts);
@@ -197,8 +200,8 @@ lisa_status lisa_forward_noalloc(const void *Q, const void *K, const void *V, vo
  *   Q, K, V     the forward's inputs (device, dtype, [B][heads][H*W][d]).
  *   dO          device [B][heads][H*W][d_v], dtype: upstream gradient.
  *   dQ, dK, dV  device, dtype, same shapes; written: dL/dQ, dL/dK, dL/dV
- *               of the raw inputs (through the ReLU feature map when
- *               relu_inputs = 1: zero where the input is <= 0).
+ *               of the raw inputs (through the feature map: relu_inputs = 1
+ *               zero where the input is <= 0; 2 scaled by exp(x) there).
  *   dalpha      device fp32 [heads]; written (not accumulated): dL/dalpha_h,
  *               summed over the batch.
  * Weights: LISA_W_GEOMETRIC (T >= 1, or T = 0 untruncated) and LISA_W_FIXED;

@@ -105,7 +105,9 @@ def _call(**over):
     (dict(eps=float("inf")), lisa.LISA_ERR_INVALID_ARG),
     (dict(beta=1.0), lisa.LISA_ERR_INVALID_ARG),
     (dict(beta=-0.1), lisa.LISA_ERR_INVALID_ARG),
-    (dict(relu=2), lisa.LISA_ERR_INVALID_ARG),
+    (dict(relu=3), lisa.LISA_ERR_INVALID_ARG),
+    (dict(relu=-1), lisa.LISA_ERR_INVALID_ARG),
+    (dict(relu=2, wbytes=16), lisa.LISA_ERR_WORKSPACE),            # ELU + 1: a valid feature map
     (dict(dtype=5), lisa.LISA_ERR_INVALID_ARG),
     (dict(workspace=0), lisa.LISA_ERR_WORKSPACE),
     (dict(wbytes=16), lisa.LISA_ERR_WORKSPACE),
@@ -284,3 +286,19 @@ def test_backward_workspaces_and_version():
             assert lisa.lisa_backward_mlp_workspace_bytes(B, heads, H, W, d, d, 3, hidden, lisa.LISA_BF16) > plain
         assert lisa.lisa_backward_mlp_workspace_bytes(B, heads, H, W, d, d, 5, 32, lisa.LISA_BF16) > \
             lisa.lisa_backward_mlp_workspace_bytes(B, heads, H, W, d, d, 3, 32, lisa.LISA_BF16)
+
+
+def test_elu_feature_map_host_side():
+    """relu_inputs = 2 (ELU + 1) runs the SIMT chain for every dtype, so the
+    workspace covers that chain too; the per-kernel access refuses it."""
+    B, heads, H, W, d = 32, 1, 56, 56, 64
+    wt, _ = lisa.make_weights(3, beta=0.5)
+    need = lisa.lisa_workspace_bytes(B, heads, H, W, d, d, 3, lisa.LISA_BF16)
+    assert need >= lisa.lisa_workspace_bytes(B, heads, H, W, d, d, 3, lisa.LISA_F32)
+    lib = lisa.load()
+    rc = lib.lisa_forward_stage(0, FAKE, FAKE + 4096, FAKE + 8192, FAKE + 12288, 1, 1, 4, 4, 16, 16, 3,
+                                ctypes.byref(wt), FAKE + 16384, 1e-6, 2, lisa.LISA_F32, FAKE + 32768, 1 << 30, None)
+    assert rc == lisa.LISA_ERR_INVALID_ARG
+    assert lisa.feature_map_code("elu1") == 2 and lisa.feature_map_code(True) == 1
+    with pytest.raises(ValueError):
+        lisa.feature_map_code("elu")
