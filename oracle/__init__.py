@@ -1,4 +1,4 @@
-"""Double-precision CPU oracle of the LiSA forward layer.
+"""Double-precision CPU oracle of the LiSA layer: forward and backward.
 
 TEST INFRASTRUCTURE ONLY: the test suite, the smoke check and the benchmark's
 CPU-baseline leg are the only callers.  The product path (the CUDA library and

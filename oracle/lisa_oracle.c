@@ -1,5 +1,7 @@
 /*
- * lisa_oracle.c -- plain double-precision CPU oracle of the LiSA forward layer.
+ * lisa_oracle.c -- plain double-precision CPU oracle of the LiSA layer: its
+ * forward and its backward (the gradients of the inputs, of alpha and of the
+ * MLP's parameters).
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
  * call this file: only the test suite, the smoke check and the benchmark's
@@ -43,6 +45,13 @@
  *   LOWRANK:  (I - beta Q~ K^T)^(-1) = I + beta Q~ (I - beta M)^(-1) K^T (the
  *             push-through identity, a derivation of ours, not the note's), so
  *             g = (1-beta) (V + beta Q~ Z) with (I - beta M) Z = U_1, d x d.
+ *
+ * Feature maps (the fmap argument, "relu_inputs"): none, ReLU, or ELU(x) + 1,
+ * the reading taken of the note's ELU variant (§2.1; paper Table 8).
+ *
+ * The backward (lisa_oracle_backward) is the chain rule written out by hand
+ * through the forward's steps in reverse; the derivation sits above
+ * backward_slice and mlp_walk_backward.
  *
  * Every array is row-major, double precision, contiguous:
  *   Q, K  [B][heads][n][d_h]      V, O, G, L  [B][heads][n][d_v]
