@@ -57,8 +57,8 @@ def parse_args():
     ap.add_argument("--pass", dest="direction", choices=["forward", "backward"], default="forward",
                     help="forward (the headline) or the backward pass (lisa_backward)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0,
-                    help="wall-time budget of the cpu_baseline sample")
+    ap.add_argument("--cpu-seconds", type=float, default=16.0,
+                    help="wall-time budget of the cpu_baseline sample (half on all cores, half on one)")
     return ap.parse_args()
 
 
@@ -207,7 +207,7 @@ def ncu_traffic(kernel: str, workload: str):
 
 # -- oracle timing (cpu_baseline and the reference arm) --------------------------------------
 
-def oracle_slice_runner(shape, seed=0):
+def oracle_slice_runner(shape, seed=0, threads=None):
     import numpy as np  # noqa: F401
     import oracle
     from lisa_synth import make_inputs, to_f64
@@ -216,7 +216,7 @@ def oracle_slice_runner(shape, seed=0):
     alpha = inp["alpha"].double().numpy()
     kw = {"beta": shape.beta} if shape.weights == "geometric" else \
         {"mlp": tuple(inp[k].double().numpy() for k in ("W1", "b1", "W2", "b2"))}
-    threads = host_cores()
+    threads = host_cores() if threads is None else threads
 
     def run():
         oracle.forward(xq, xk, v, (shape.H, shape.W), shape.T, alpha=alpha, mode=oracle.LOWRANK,
@@ -224,8 +224,8 @@ def oracle_slice_runner(shape, seed=0):
     return run, threads
 
 
-def cpu_baseline(shape, seconds: float):
-    run, threads = oracle_slice_runner(shape)
+def _time_oracle(shape, seconds: float, threads=None):
+    run, threads = oracle_slice_runner(shape, threads=threads)
     run()  # warm
     reps, t0 = 0, time.perf_counter()
     while True:
@@ -234,10 +234,19 @@ def cpu_baseline(shape, seconds: float):
         el = time.perf_counter() - t0
         if el >= seconds:
             break
-    return {"value": reps * shape.n / el, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": "%d repetitions of one (batch, head) slice of the workload (%dx%d grid, n=%d, "
-                      "d=%d, T=%d), double-precision LOWRANK oracle, %.1f s" %
-                      (reps, shape.H, shape.W, shape.n, shape.d, shape.T, el)}
+    sample = ("%d repetitions of one (batch, head) slice of the workload (%dx%d grid, n=%d, d=%d, T=%d), "
+              "double-precision LOWRANK oracle on %d thread%s, %.1f s" %
+              (reps, shape.H, shape.W, shape.n, shape.d, shape.T, threads, "" if threads == 1 else "s", el))
+    return reps * shape.n / el, threads, sample
+
+
+def cpu_baseline(shape, seconds: float):
+    """The oracle on all host cores (the line's value) and on one thread,
+    the budget split evenly between the two."""
+    value, threads, sample = _time_oracle(shape, seconds / 2)
+    one, _, one_sample = _time_oracle(shape, seconds / 2, threads=1)
+    return {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample,
+            "single_thread": {"value": one, "unit": UNIT, "cores": 1, "sample": one_sample}}
 
 
 def reference_arm(args, shape):

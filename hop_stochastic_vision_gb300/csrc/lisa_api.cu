@@ -13,6 +13,7 @@
 #include "lisa_backward_mlp.h"
 #include "lisa_bwd.h"
 #include "lisa_internal.h"
+#include "lisa_testing.h"
 
 namespace lisa {
 namespace {
@@ -78,7 +79,7 @@ Plan make_plan(int slices, int n, int D, int T, int dtype, int wmode, int hidden
     pl.chunk = chunk;
     const size_t S = (size_t)slices, C = (size_t)chunks, d = (size_t)D;
     size_t off = 0;
-    pl.off_err = off;    off = align_up(off + sizeof(int));
+    pl.off_err = off;    off = align_up(off + sizeof(int));   // must stay at 0: lisa_query_status reads it there
     pl.off_s_part = off; off = align_up(off + S * C * d * sizeof(float));
     if (pl.family == kFamilySimt) {
         const size_t nmat = (size_t)(T > 1 ? T - 1 : 1);
@@ -377,19 +378,40 @@ extern "C" const char *lisa_status_string(int status) {
     }
 }
 
-extern "C" int lisa_abi_version(void) { return 102; }
+extern "C" int lisa_abi_version(void) { return 103; }
+
+extern "C" lisa_status lisa_query_status(const void *workspace, void *stream) {
+    if (!workspace || !aligned16(workspace)) return LISA_ERR_INVALID_ARG;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    int word = 0;
+    // the error word is the first int of every forward workspace (Plan::off_err == 0)
+    if (cudaMemcpyAsync(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost, cs) != cudaSuccess ||
+        cudaStreamSynchronize(cs) != cudaSuccess)
+        return LISA_ERR_CUDA;
+    return word == 0 ? LISA_OK : LISA_ERR_TIMEOUT;
+}
+
+extern "C" lisa_status lisa_selftest_wait_timeout(long long cycles, void *workspace, size_t workspace_bytes,
+                                                  void *stream) {
+    if (cycles < 0 || !workspace || !aligned16(workspace) || workspace_bytes < sizeof(int))
+        return LISA_ERR_INVALID_ARG;
+    return launch_wait_selftest(static_cast<int *>(workspace), cycles, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? LISA_OK
+               : LISA_ERR_CUDA;
+}
 
 // ---------------------------------------------------------------------------
 // lisa_forward_noalloc -- the layer for callers that may not allocate device
 // memory.  Some hosts of this code cannot call cudaMalloc when they run it:
-// a stream being captured into a CUDA graph in global capture mode (an
-// allocation there invalidates the capture), an operator plugged into an
-// inference engine or framework that owns all device memory through its own
-// pool and plans it before execution, or a serving loop that cannot afford
-// the device-wide synchronisation cudaFree implies.  This entry point needs
-// no workspace from them: it runs in a scratch array compiled into the
-// library (LISA_NOALLOC_SCRATCH_BYTES on every device that loads the
-// library, held until the process exits).
+// an operator plugged into an inference engine or framework that owns all
+// device memory through its own pool and plans it before execution, or a
+// serving loop that cannot afford the device-wide synchronisation cudaFree
+// implies.  This entry point needs no workspace from them: it runs in a
+// scratch array compiled into the library (LISA_NOALLOC_SCRATCH_BYTES on
+// every device that loads the library, held until the process exits).  The
+// array's device address is looked up once per device, on the first call
+// with that device current, and kept for the life of the process.
 // ---------------------------------------------------------------------------
 namespace {
 

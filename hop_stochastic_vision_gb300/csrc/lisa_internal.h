@@ -53,6 +53,18 @@ struct Problem {
     uint8_t *tc_w1img;     // [2][64][128 B] bf16 MLP first-layer weights
 };
 
+// Bits of the workspace's error word (the first int of every forward
+// workspace): a bounded device wait that gave up.  The first kernel of each
+// forward chain clears the word; lisa_query_status reads it.
+constexpr int kErrTimeoutLoad = 1;   // a wait for a TMA load or a peer's data
+constexpr int kErrTimeoutMma = 2;    // a wait for a tensor-core product or a buffer release
+
+// Test hook: one CTA waits, with a limit of `cycles` SM cycles, on an
+// mbarrier that nothing arrives on, through the same bounded wait the
+// tensor-core kernels use, and records kErrTimeoutLoad in *err when the wait
+// gives up (it clears *err first).
+cudaError_t launch_wait_selftest(int *err, long long cycles, cudaStream_t stream);
+
 constexpr int kFamilySimt = 0;
 constexpr int kFamilyTc = 1;
 

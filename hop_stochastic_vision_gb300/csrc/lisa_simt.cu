@@ -57,6 +57,7 @@ __global__ void __launch_bounds__(kThreads) stats_kv_kernel(Problem p) {
     __shared__ float Ks[kTile][D];
     __shared__ float Vs[kTile][D];
     const int c = blockIdx.x % p.chunks, sl = blockIdx.x / p.chunks, tid = threadIdx.x;
+    if (blockIdx.x == 0 && tid == 0 && p.err) *p.err = 0;   // first kernel of the chain: clear the error word
     const int t0 = c * p.chunk;
     const int t1 = min(p.n, t0 + p.chunk);
     const TIn *K = static_cast<const TIn *>(p.K) + (size_t)sl * p.n * D;

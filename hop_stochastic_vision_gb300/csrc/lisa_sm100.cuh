@@ -44,14 +44,19 @@ __device__ __forceinline__ bool mbar_test_parity(uint32_t bar, uint32_t parity) 
         : "memory");
     return ok != 0;
 }
-// Bounded wait for phase `parity` of the barrier; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Wait for phase `parity` of the barrier for at most `limit` SM cycles;
+// false on timeout.
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, long long limit) {
     if (mbar_test_parity(bar, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_test_parity(bar, parity)) {
-        if (clock64() - t0 > kWaitCycles) return false;
+        if (clock64() - t0 > limit) return false;
     }
     return true;
+}
+// Bounded wait for phase `parity` of the barrier; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    return mbar_wait_for(bar, parity, kWaitCycles);
 }
 
 // The same wait with a 64 ns back-off between polls, for a thread whose spinning

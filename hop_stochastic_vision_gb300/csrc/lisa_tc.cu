@@ -61,9 +61,6 @@ constexpr int kRedStride = 68;                 // fp32 row stride of reduction b
 constexpr int kFusedMaxSub = 7;                // fused stats: resident K chunk <= 448 tokens
 constexpr int kFusedWork = 72 * 1024;          // fused stats: minimum work area
 
-constexpr int kErrTimeoutLoad = 1;
-constexpr int kErrTimeoutMma = 2;
-
 struct TcParams {
     int slices, heads, H, W, n, T, relu, wmode, hidden;
     int untruncated;                 // U-bar = beta (1-beta) (I - beta M)^-1 U_1 instead of the series
@@ -1668,6 +1665,23 @@ cudaError_t launch_tc(const Problem &p, cudaStream_t st, int stage) {
         err = mlp ? launch(tc_epilogue_kernel<true, 1, 1>, 2) : launch(tc_epilogue_kernel<false, 1, 1>, 3);
         if (err != cudaSuccess) return err;
     }
+    return cudaGetLastError();
+}
+
+namespace {
+__global__ void wait_selftest_kernel(int *err, long long cycles) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    *err = 0;
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+    // nothing arrives on the barrier: the wait must give up after `cycles`
+    if (!mbar_wait_for(smem_u32(&bar), 0, cycles)) record_error(err, kErrTimeoutLoad);
+}
+}  // namespace
+
+cudaError_t launch_wait_selftest(int *err, long long cycles, cudaStream_t stream) {
+    wait_selftest_kernel<<<1, 32, 0, stream>>>(err, cycles);
     return cudaGetLastError();
 }
 

@@ -36,7 +36,7 @@ LISA_MAX_HIDDEN = 64
 EXPORTED = ("lisa_workspace_bytes", "lisa_forward", "lisa_forward_host", "lisa_num_stages",
             "lisa_stage_name", "lisa_forward_stage", "lisa_forward_noalloc", "lisa_backward_workspace_bytes",
             "lisa_backward", "lisa_backward_mlp_workspace_bytes", "lisa_backward_mlp", "lisa_status_string",
-            "lisa_abi_version")
+            "lisa_abi_version", "lisa_query_status", "lisa_selftest_wait_timeout")
 
 LISA_NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -109,6 +109,10 @@ def load(path: str = LIB_PATH):
         lib.lisa_status_string.restype = ctypes.c_char_p
         lib.lisa_abi_version.argtypes = []
         lib.lisa_abi_version.restype = i
+        lib.lisa_query_status.argtypes = [vp, vp]
+        lib.lisa_query_status.restype = i
+        lib.lisa_selftest_wait_timeout.argtypes = [ctypes.c_longlong, vp, sz, vp]
+        lib.lisa_selftest_wait_timeout.restype = i
         _lib = lib
         return lib
 
@@ -121,6 +125,14 @@ def lisa_status_string(status: int) -> str:
 
 def lisa_abi_version() -> int:
     return int(load().lisa_abi_version())
+
+
+def lisa_query_status(workspace, stream) -> int:
+    return int(load().lisa_query_status(workspace, stream))
+
+
+def lisa_selftest_wait_timeout(cycles, workspace, workspace_bytes, stream) -> int:
+    return int(load().lisa_selftest_wait_timeout(cycles, workspace, workspace_bytes, stream))
 
 
 def lisa_workspace_bytes(B, heads, H, W, d_h, d_v, T, dtype) -> int:

@@ -28,11 +28,16 @@
  *   - dtype LISA_F32: fp32 in, fp32 out, fp32 arithmetic throughout.
  *     dtype LISA_BF16: bf16 in, bf16 out (round to nearest even), fp32
  *     accumulation; bf16 tensor-core operands where the contraction allows.
- *   - d_h == d_v, each one of 16, 32, 64; other sizes give LISA_ERR_UNSUPPORTED.
+ *   - d_h == d_v, each one of 16, 32, 64; other sizes give LISA_ERR_UNSUPPORTED
+ *     (the layer widths of every configuration here have d_v = d_h; d_v != d_h
+ *     is rejected rather than served).
  *   - Device pointers must be 16-byte aligned.  O must not overlap an input.
- *   - The library allocates nothing and keeps no global state: the caller
- *     owns every buffer, including the workspace.  Calls on different
- *     streams with different workspaces may run concurrently.
+ *   - The library allocates no device memory: the caller owns every buffer,
+ *     including the workspace.  Its host-side state is limited to lookups
+ *     cached once per device (the kernels' shared-memory limits, the tensor
+ *     map encoder, the no-alloc scratch address below), and its one device
+ *     buffer is that scratch array of lisa_forward_noalloc.  Calls on
+ *     different streams with different workspaces may run concurrently.
  *   - Every argument is checked on the host before anything is launched; a
  *     bad argument returns its status and launches nothing.  Launch
  *     failures return LISA_ERR_CUDA.  The call is asynchronous on `stream`
@@ -84,8 +89,11 @@ typedef struct lisa_weights {
  * Bytes of device workspace lisa_forward needs for this problem (a pure
  * host computation; no CUDA call).  Returns 0 for arguments lisa_forward
  * would reject.  The workspace holds the split-K partial sums of sum_j K_j,
- * K^T V and K^T Q~ [note §2.3], the reduced statistics and U_1..U_(T-1);
- * lisa_forward overwrites all of it, so it needs no initialisation.
+ * K^T V and K^T Q~ [note §2.3], the reduced statistics and U_1..U_(T-1).
+ * Its first 4 bytes are the call's error word: the first kernel of every
+ * forward sets it to 0 and a bounded device wait that gives up sets bits in
+ * it (lisa_query_status reads it).  Every other byte is written by the call
+ * before it is read, so the buffer needs no initialisation.
  * T = 0 (the untruncated walk) is accepted and sized like T = 2.
  */
 size_t lisa_workspace_bytes(int B, int heads, int H, int W, int d_h, int d_v, int T,
@@ -161,30 +169,39 @@ lisa_status lisa_forward_stage(int stage, const void *Q, const void *K, const vo
 
 /*
  * lisa_forward without a workspace argument, for callers that cannot
- * allocate device memory when they run the layer: work captured into a CUDA
- * graph in global capture mode (an allocation there breaks the capture), an
- * operator inside an engine or framework that owns all device memory through
- * its own planned pool, or a latency-bound loop that cannot take the
- * device-wide synchronisation of cudaFree.  The paper has no counterpart;
- * this is a property of the library, not of the method.
+ * allocate device memory when they run the layer: an operator inside an
+ * inference engine or framework that owns all device memory through its own
+ * pool, planned before execution, so the operator may not call cudaMalloc;
+ * or a latency-bound serving loop that cannot take the device-wide
+ * synchronisation a cudaFree implies.  The paper has no counterpart; this is
+ * a property of the library, not of the method.
  *
  * Instead of a caller workspace it uses one scratch array compiled into the
  * library: LISA_NOALLOC_SCRATCH_BYTES of device memory on every GPU that
  * loads liblisa.so, held until the process exits.  It calls no cudaMalloc,
  * cudaFree or other allocating routine.
- *   - A problem whose lisa_workspace_bytes(...) exceeds
- *     LISA_NOALLOC_SCRATCH_BYTES is rejected with LISA_ERR_WORKSPACE before
- *     anything is launched; use lisa_forward with your own workspace there.
+ *   - The call's own workspace need (what lisa_forward would use for these
+ *     sizes, weight mode and feature map, at most lisa_workspace_bytes(...))
+ *     must fit in LISA_NOALLOC_SCRATCH_BYTES; a larger problem is rejected
+ *     with LISA_ERR_WORKSPACE before anything is launched.  Use lisa_forward
+ *     with your own workspace there.
  *   - The first call on a device looks up the scratch array's device address
- *     (cudaGetSymbolAddress, with that device current).  Make that first call
- *     before capturing any stream; later calls do no runtime lookups.  Call
- *     with the device of `stream` current.
+ *     (cudaGetSymbolAddress, with that device current) and keeps it for the
+ *     life of the process.  Make that first call before any stream capture
+ *     begins.  Later calls do no runtime lookups.  Call with the device of
+ *     `stream` current.  Calls must not cross a cudaDeviceReset (or any
+ *     other reset of the device's primary context): the kept address would
+ *     be stale afterwards.
  *   - Every call on a device shares the one array, and it keeps whatever the
- *     last call left there.  Nothing in it has to start at zero: each call
- *     writes every scratch entry it reads.  Calls whose kernels overlap on the
- *     GPU (different streams, no ordering between them) race on the array and
- *     give wrong results; order them on one stream, or give each its own
+ *     last call left there.  The only entry that must start at zero, the
+ *     error word, is cleared by each call's first kernel; every other entry
+ *     is written before it is read.  Calls whose kernels overlap on the GPU
+ *     (different streams, no ordering between them) race on the array and
+ *     give wrong results: order them on one stream, or give each its own
  *     workspace through lisa_forward.
+ *   - A timed-out device wait cannot be queried for these calls (the scratch
+ *     array's address is not handed out); lisa_query_status serves
+ *     lisa_forward's caller-owned workspaces.
  * Other arguments, checks and statuses are those of lisa_forward.
  */
 #define LISA_NOALLOC_SCRATCH_BYTES (32u << 20)
@@ -221,6 +238,23 @@ lisa_status lisa_backward(const void *Q, const void *K, const void *V, const voi
                           int d_h, int d_v, int T, const lisa_weights *wts, const float *alpha,
                           float eps, int relu_inputs, int dtype, void *workspace,
                           size_t workspace_bytes, void *stream);
+
+/*
+ * Failure reporting of the device side.  The tensor-core kernels bound every
+ * wait (on a TMA load, a tensor-core product, a buffer release, a peer's
+ * data) to about one second; a wait that gives up sets a bit in the error
+ * word at the start of the call's workspace and the kernel finishes along
+ * its normal path (every CTA still frees its tensor memory and drains its
+ * bulk stores), leaving O undefined.  lisa_forward itself returns before the
+ * kernels run, so it cannot see this.  lisa_query_status reads the word of
+ * `workspace` (the one passed to the last lisa_forward call on it) after the
+ * work queued on `stream` has finished: it synchronises `stream` and
+ * returns LISA_ERR_TIMEOUT if any wait gave up, LISA_OK otherwise, or
+ * LISA_ERR_CUDA if the read itself failed.  A null or misaligned workspace
+ * is LISA_ERR_INVALID_ARG.  The next lisa_forward call on the workspace
+ * clears the word again.
+ */
+lisa_status lisa_query_status(const void *workspace, void *stream);
 
 /* Static, human-readable name of a status code. */
 const char *lisa_status_string(int status);

@@ -302,3 +302,15 @@ def test_elu_feature_map_host_side():
     assert lisa.feature_map_code("elu1") == 2 and lisa.feature_map_code(True) == 1
     with pytest.raises(ValueError):
         lisa.feature_map_code("elu")
+
+
+def test_status_query_and_wait_selftest_reject_before_any_cuda_call():
+    """lisa_query_status and the bounded-wait self-test check their arguments
+    on the host: a null or misaligned workspace, a negative limit or a
+    workspace too small for the error word return LISA_ERR_INVALID_ARG."""
+    assert lisa.lisa_query_status(None, None) == lisa.LISA_ERR_INVALID_ARG
+    assert lisa.lisa_query_status(FAKE + 4, None) == lisa.LISA_ERR_INVALID_ARG
+    assert lisa.lisa_selftest_wait_timeout(-1, FAKE, 256, None) == lisa.LISA_ERR_INVALID_ARG
+    assert lisa.lisa_selftest_wait_timeout(1000, None, 256, None) == lisa.LISA_ERR_INVALID_ARG
+    assert lisa.lisa_selftest_wait_timeout(1000, FAKE + 8, 256, None) == lisa.LISA_ERR_INVALID_ARG
+    assert lisa.lisa_selftest_wait_timeout(1000, FAKE, 2, None) == lisa.LISA_ERR_INVALID_ARG

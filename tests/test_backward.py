@@ -2,14 +2,23 @@
 hand-derived, finite-difference-pinned backward, on the same seeded inputs
 and upstream gradient.
 
-Tolerance: the normwise error of each slice's whole gradient (dXq, dXk,
-dV), max over (batch, head) slices of max_t ||gpu_t - oracle_t||_inf /
-max_t ||oracle_t||_inf, <= 1e-4 (fp32) or 2e-2 (bf16 outputs, fp32
-arithmetic) -- the forward's bounds; dalpha (fp32 in both) within 1e-3
-relative plus 1e-5 of sum_i |dO_i| (|g_i| + |l_i|), its own rounding scale.  The joint norm matters where one gradient is nearly zero by
-cancellation: on a 1 x 1 grid S = Q~K^T = Q.K/(Q.K + eps), so dXq and dXk
-are O(eps) differences of O(1) terms and fp32 rounding is as large as they
-are, while dV is O(1)."""
+Tolerance: each of dXq, dXk and dV separately, max over (batch, head)
+slices of ||gpu - oracle||_inf / ||oracle||_inf of that tensor, <= 1e-4
+(fp32) or 2e-2 (bf16 outputs, fp32 arithmetic) -- the forward's bounds;
+dalpha (fp32 in both) within 1e-3 relative plus 1e-5 of
+sum_i |dO_i| (|g_i| + |l_i|), its own rounding scale.
+
+Only the 1 x 1 grid is measured jointly (each tensor's error against the
+largest of the three): there S = Q~K^T = Q.K/(Q.K + eps), so dXq and dXk are
+O(eps) differences of O(1) terms and fp32 rounding is as large as they are.
+
+With alpha = 1 the output is the walk alone, so dXq and dXk carry only the
+walk's gradient (the reverse recurrence, dM, dU_1 and ds).  On i.i.d. inputs
+that gradient is small and a wrong term in it can stay within the bf16 bar;
+the alpha = 1 cases therefore include structured inputs (near block-diagonal
+S) and deep walks (T = 5, beta = 0.9) on small grids, where a dropped ds or a
+transposed dM moves dXq or dXk by 10% or more of its own norm
+(test_oracle_backward.py pins that on the CPU)."""
 import numpy as np
 import pytest
 import torch
@@ -39,6 +48,19 @@ def joint_rel_err(got, want):
     return float((num / np.where(den > 0, den, 1.0)).max())
 
 
+def assert_per_tensor(got, want, shape):
+    """Each gradient against the oracle on its own norm; the 1 x 1 grid jointly."""
+    tol = TOL[shape.dtype]
+    if shape.n == 1:
+        err = joint_rel_err(got, want)
+        assert err <= tol, "1 x 1 grid: joint gradient err %.3e (%s)" % (err, shape.dtype)
+        return [err] * 3
+    errs = [max_rel_err(g, w) for g, w in zip(got, want)]
+    for name, e in zip(("dXq", "dXk", "dV"), errs):
+        assert e <= tol, "%s err %.3e > %.0e (%s)" % (name, e, tol, shape.dtype)
+    return errs
+
+
 def _upstream(shape, B, heads, seed=7):
     g = torch.Generator("cpu").manual_seed(seed)
     dO = torch.randn(B, heads, shape.n, shape.d, generator=g)
@@ -65,9 +87,7 @@ def _check(shape, *, B=None, heads=None, beta=0.5, w=None, relu=True, seed=0, st
     got = [to_f64(x.cpu()) for x in (dq, dk, dv)]
     for g in got:
         assert np.isfinite(g).all()
-    err = joint_rel_err(got, want[:3])
-    assert err <= TOL[shape.dtype], "gradient normwise err %.3e (%s)" % (err, shape.dtype)
-    errs = [max_rel_err(g, r) for g, r in zip(got, want[:3])]
+    errs = assert_per_tensor(got, want[:3], shape)
     # dalpha = sum_i dO_i . (g_i - l_i): its rounding scales with sum |dO| (|g| + |l|)
     _, G, L = oracle.forward(to_f64(inp["xq"]), to_f64(inp["xk"]), to_f64(inp["v"]), (shape.H, shape.W), shape.T,
                              alpha=inp["alpha"].double().numpy(), relu=relu, branches=True, **okw)
@@ -123,6 +143,29 @@ def test_full_size_pvt_layer():
     _check(shape)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_walk_only_structured(dtype):
+    """alpha = 1: dXq and dXk come from the walk alone.  Structured inputs,
+    T = 3 and the deep walk T = 5, beta = 0.9; the untruncated walk."""
+    _check(_shape(dtype, 64, 24, 20, 3, alpha="0.5"), structured=True, alpha=1.0)
+    _check(_shape(dtype, 64, 24, 20, 5, alpha="0.5"), structured=True, alpha=1.0, beta=0.9)
+    _check(_shape(dtype, 64, 24, 20, 0, alpha="0.5"), structured=True, alpha=1.0, beta=0.9)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d", [32, 64])
+def test_walk_only_deep_small_grid(dtype, d):
+    """alpha = 1 on i.i.d. inputs of a small grid with a deep walk."""
+    _check(_shape(dtype, d, 9, 12, 5, alpha="0.5"), alpha=1.0, beta=0.9)
+    _check(_shape(dtype, d, 7, 9, 3, alpha="0.5"), alpha=1.0)
+
+
+def test_walk_only_full_size_pvt_layer():
+    """alpha = 1 on the PVT stage-1 layer, i.i.d. and structured inputs."""
+    _check(SHAPES["pvt_t_s1_56x56_T3"], alpha=1.0)
+    _check(_shape("bf16", 64, 56, 56, 5, B=4, heads=1, alpha="0.5"), structured=True, alpha=1.0, beta=0.9)
+
+
 def test_deterministic_and_empty():
     from hop_stochastic_vision_gb300 import lisa
     shape = _shape("bf16", 64, 28, 28, 3, B=4, heads=3)
@@ -140,10 +183,13 @@ def test_deterministic_and_empty():
 
 # -- adaptive (MLP) walk weights: lisa_backward_mlp ----------------------------------------
 
-def _check_mlp(dtype, d, H, W, T, *, B=2, heads=2, hidden=32, scale=1.0, seed=0, relu=True):
+def _check_mlp(dtype, d, H, W, T, *, B=2, heads=2, hidden=32, scale=1.0, seed=0, relu=True, alpha=None,
+               structured=False):
     from hop_stochastic_vision_gb300 import lisa
     shape = LayerShape("bwd_mlp", dtype, B, heads, H, W, d, T, "mlp", alpha="uniform(0.3,0.7)", hidden=hidden)
-    inp = make_inputs(shape, seed=seed)
+    inp = make_inputs(shape, seed=seed, structured=structured)
+    if alpha is not None:
+        inp["alpha"] = torch.full_like(inp["alpha"], float(alpha))
     for key in ("W1", "b1", "W2", "b2"):   # the paper's N(0, 0.02) init, optionally scaled up
         inp[key] = inp[key] * scale
     if not relu:
@@ -160,8 +206,7 @@ def _check_mlp(dtype, d, H, W, T, *, B=2, heads=2, hidden=32, scale=1.0, seed=0,
     got = [to_f64(x.cpu()) for x in (dq, dk, dv)]
     for g in got:
         assert np.isfinite(g).all()
-    err = joint_rel_err(got, want[:3])
-    assert err <= TOL[dtype], "gradient normwise err %.3e (%s d=%d T=%d)" % (err, dtype, d, T)
+    err = max(assert_per_tensor(got, want[:3], shape))
     ptol = 1e-3 if dtype == "f32" else 2e-2
     for name, g, ref in zip(("dW1", "db1", "dW2", "db2"), pg, want[4]):
         g = g.cpu().double().numpy()
@@ -192,3 +237,10 @@ def test_mlp_hidden64_paper_init_and_no_feature_map():
 def test_mlp_ragged_grid_and_full_size_deit384():
     _check_mlp("bf16", 64, 57, 55, 3, B=1, heads=2, scale=20.0)
     _check_mlp("bf16", 64, 24, 24, 3, B=64, heads=3, scale=20.0)   # the DeiT-T/384 layer's shape
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_mlp_walk_only(dtype):
+    """alpha = 1 with adaptive weights: the walk's and the MLP's gradients alone."""
+    _check_mlp(dtype, 64, 24, 20, 5, scale=20.0, alpha=1.0, structured=True)
+    _check_mlp(dtype, 64, 9, 12, 5, scale=20.0, alpha=1.0)

@@ -247,3 +247,61 @@ def test_backward_through_elu_feature_map(T, kw):
             dn = float((oracle.forward(xq, xk, v, grid, T, alpha=0.45, relu="elu1", **kw) * dO).sum())
             arr[idx] = keep
             assert abs((up - dn) / (2 * h) - grad[idx]) <= 1e-6 * max(np.abs(grad).max(), 1.0)
+
+
+# -- how much a wrong walk gradient moves the GPU test cases ---------------------------------
+
+def _walk_gradients(xq, xk, v, dO, w, eps=1e-6, plant=None):
+    """The layer at alpha = 1 (the walk alone) restated in the low-rank form
+    of the note (section 2.3: S^k V = Q~ M^(k-1) U_1, M = K^T Q~, U_1 = K^T V)
+    and differentiated by torch autograd.  `plant` puts a known mistake into
+    that backward: "drop_ds" zeroes the gradient reaching s = sum_j K_j,
+    "transpose_dM" transposes the one reaching M."""
+    xq, xk, v = (torch.tensor(a, requires_grad=True) for a in (xq, xk, v))
+    q, k = torch.relu(xq), torch.relu(xk)
+    s = k.sum(0)
+    if plant == "drop_ds":
+        s.register_hook(torch.zeros_like)
+    qt = q / (q @ s + eps)[:, None]
+    M = k.T @ qt
+    if plant == "transpose_dM":
+        M.register_hook(lambda g: g.T.contiguous())
+    u = k.T @ v
+    out = w[0] * v
+    for t in range(1, len(w)):
+        out = out + w[t] * (qt @ u)
+        u = M @ u
+    (out * torch.from_numpy(dO)).sum().backward()
+    return [a.grad.numpy() for a in (xq, xk, v)]
+
+
+def test_walk_only_cases_see_a_wrong_walk_gradient():
+    """The alpha = 1 cases of the GPU backward tests (same seeded inputs and
+    upstream gradient): the restatement above matches the oracle's backward,
+    and planting a dropped ds or a transposed dM into it moves dXk or dXq by
+    more than five times the bf16 bar (2e-2) of the tensor's own norm in at
+    least one case, so a kernel with either mistake fails those tests."""
+    from lisa_synth import LayerShape, make_inputs, to_f64
+    cases = [(LayerShape("bwd", "bf16", 2, 2, 24, 20, 64, 5, "geometric"), True, 0.9),
+             (LayerShape("bwd", "bf16", 2, 2, 9, 12, 64, 5, "geometric"), False, 0.9),
+             (LayerShape("bwd", "bf16", 2, 2, 7, 9, 64, 3, "geometric"), False, 0.5)]
+    worst = {"drop_ds": 0.0, "transpose_dM": 0.0}
+    for shape, structured, beta in cases:
+        inp = make_inputs(shape, structured=structured)
+        g = torch.Generator("cpu").manual_seed(7)
+        dO = to_f64(torch.randn(2, 2, shape.n, shape.d, generator=g).to(torch.bfloat16))
+        xq, xk, v = (to_f64(inp[key]) for key in ("xq", "xk", "v"))
+        w = oracle.geometric_weights(beta, shape.T)
+        ref = oracle.backward(xq, xk, v, dO, (shape.H, shape.W), shape.T, alpha=np.ones(2), beta=beta)
+        for b in range(2):
+            for h in range(2):
+                args = (xq[b, h], xk[b, h], v[b, h], dO[b, h], w)
+                want = [r[b, h] for r in ref[:3]]
+                for got, r in zip(_walk_gradients(*args), want):
+                    assert np.abs(got - r).max() <= 1e-9 * np.abs(r).max()
+                for plant in worst:
+                    got = _walk_gradients(*args, plant=plant)
+                    rel = max(np.abs(x - r).max() / np.abs(r).max() for x, r in zip(got[:2], want[:2]))
+                    worst[plant] = max(worst[plant], rel)
+    for plant, rel in worst.items():
+        assert rel > 5 * 2e-2, (plant, rel)

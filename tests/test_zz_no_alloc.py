@@ -1,8 +1,8 @@
 """lisa_forward_noalloc: the LiSA layer for callers that cannot allocate
-device memory while they run it (work captured into a CUDA graph in global
-capture mode, an operator inside an engine that owns all device memory, a
-loop that cannot take the synchronisation of cudaFree).  It runs in a fixed
-scratch array compiled into the library instead of a caller workspace.
+device memory while they run it (an operator inside an engine that owns all
+device memory through its own planned pool, a serving loop that cannot take
+the synchronisation of cudaFree).  It runs in a fixed scratch array compiled
+into the library instead of a caller workspace.
 
 Each case calls it twice in a row through the C ABI and compares both
 outputs with lisa_forward's (caller-allocated workspace), within the parity
