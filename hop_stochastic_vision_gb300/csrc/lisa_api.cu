@@ -378,7 +378,7 @@ extern "C" const char *lisa_status_string(int status) {
     }
 }
 
-extern "C" int lisa_abi_version(void) { return 103; }
+extern "C" int lisa_abi_version(void) { return 104; }
 
 extern "C" lisa_status lisa_query_status(const void *workspace, void *stream) {
     if (!workspace || !aligned16(workspace)) return LISA_ERR_INVALID_ARG;
@@ -389,6 +389,23 @@ extern "C" lisa_status lisa_query_status(const void *workspace, void *stream) {
         cudaStreamSynchronize(cs) != cudaSuccess)
         return LISA_ERR_CUDA;
     return word == 0 ? LISA_OK : LISA_ERR_TIMEOUT;
+}
+
+extern "C" lisa_status lisa_forward_resident(const void *Q, const void *K, const void *V, void *O,
+                                             int B, int heads, int H, int W, int d_h, int d_v, int T,
+                                             const lisa_weights *wts, const float *alpha, float eps,
+                                             int relu_inputs, int dtype, void *workspace,
+                                             size_t workspace_bytes, void *stream) {
+    Problem p;
+    bool empty;
+    lisa_status st = prepare(p, empty, Q, K, V, O, B, heads, H, W, d_h, d_v, T, wts, alpha, eps,
+                             relu_inputs, dtype, workspace, workspace_bytes);
+    if (st != LISA_OK || empty) return st;
+    if (p.family != kFamilyTc ||
+        !tc_resident_applies(p.slices, H, W, d_h, dtype, p.wmode, p.untruncated, p.relu))
+        return LISA_ERR_UNSUPPORTED;
+    p.resident = 1;
+    return launch(p, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" lisa_status lisa_selftest_wait_timeout(long long cycles, void *workspace, size_t workspace_bytes,

@@ -37,6 +37,7 @@ struct Problem {
     int chunk;           // tokens per chunk (last one may be shorter)
 
     int family;          // kFamilySimt / kFamilyTc
+    int resident;        // 1: the single-kernel tensor-core forward (test entry point only)
 
     // workspace views
     int *err;        // error word (bounded device waits that gave up)
@@ -92,6 +93,13 @@ extern const char *const kSimtStageNames[kSimtStages];
 cudaError_t launch_simt(const Problem &p, cudaStream_t stream, int stage);
 
 cudaError_t launch_tc(const Problem &p, cudaStream_t stream, int stage);
+// The single-kernel tensor-core forward (one thread-block cluster per slice,
+// K resident in shared memory): bf16, d = 64, weights shared by all tokens
+// (truncated or untruncated walk), ReLU or no feature map, grids with an even
+// number of rows and 8 to 64 columns in steps of 8, when its shared-memory
+// plan fits.
+bool tc_resident_applies(int slices, int H, int W, int D, int dtype, int wmode, int untruncated, int relu);
+cudaError_t launch_tc_resident(const Problem &p, cudaStream_t stream);
 // The tensor-core chain is 2 kernels when a slice's chunks fit one cluster
 // (fused statistics), else 4.
 int tc_num_stages(int chunks, int cluster, int chunk);

@@ -44,12 +44,26 @@ __device__ __forceinline__ bool mbar_test_parity(uint32_t bar, uint32_t parity) 
         : "memory");
     return ok != 0;
 }
+// The same test, allowed to suspend the thread until the phase completes or
+// kSuspendNs nanoseconds have passed, so a waiting warp issues no
+// instructions while it waits.
+constexpr uint32_t kSuspendNs = 100000;
+__device__ __forceinline__ bool mbar_test_parity_suspend(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        "selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "n"(kSuspendNs)
+        : "memory");
+    return ok != 0;
+}
 // Wait for phase `parity` of the barrier for at most `limit` SM cycles;
 // false on timeout.
 __device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, long long limit) {
     if (mbar_test_parity(bar, parity)) return true;
     const long long t0 = clock64();
-    while (!mbar_test_parity(bar, parity)) {
+    while (!mbar_test_parity_suspend(bar, parity)) {
         if (clock64() - t0 > limit) return false;
     }
     return true;
@@ -98,6 +112,12 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *map, int x
         " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
         "l"(map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
         : "memory");
+}
+// Tiled prefetch of a box into L2 (no shared-memory destination, no completion).
+__device__ __forceinline__ void tma_prefetch_3d(const void *map, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map), "r"(x), "r"(y),
+                 "r"(z)
+                 : "memory");
 }
 // Tiled store (out-of-range elements are not written); start coordinates >= 0.
 __device__ __forceinline__ void tma_store_4d(const void *map, uint32_t src, int x, int y, int z,

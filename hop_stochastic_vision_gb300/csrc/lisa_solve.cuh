@@ -38,11 +38,15 @@ namespace lisa {
 // again), and slots past the last column hold zeros.
 //
 // scratch: 192 floats of shared memory (pivot column, double-buffered, and
-// the pivots).  D <= 64.  Every thread of the block (kW warps) calls this;
-// it holds __syncthreads.  On return R holds X; A is not written.
-template <int kW, int kC>
+// the pivots).  D <= 64.  Every thread of the kW warps that take part calls
+// this (tid = 0 .. 32 kW - 1); `sync` is their barrier (the whole block by
+// default).  On return R holds X; A is not written.
+struct BlockSync {
+    __device__ __forceinline__ void operator()() const { __syncthreads(); }
+};
+template <int kW, int kC, typename Sync = BlockSync>
 __device__ __forceinline__ void solve_walk_system(const float *A, int sb, float *R, int re, int D, int m,
-                                                  float *scratch, int tid) {
+                                                  float *scratch, int tid, Sync sync = Sync()) {
     const int w = tid >> 5, l = tid & 31;
     const bool h0 = l < D, h1 = l + 32 < D;
     const int NC = D + m;
@@ -60,7 +64,7 @@ __device__ __forceinline__ void solve_walk_system(const float *A, int sb, float 
         if (h1) colbuf[l + 32] = x1[0];
         if (l == 0) pivs[0] = x0[0];
     }
-    __syncthreads();
+    sync();
 #pragma unroll
     for (int ks = 0; ks < (64 + kW - 1) / kW; ++ks) {
         for (int wi = 0; wi < kW; ++wi) {
@@ -90,7 +94,7 @@ __device__ __forceinline__ void solve_walk_system(const float *A, int sb, float 
                 if (h1) cn[l + 32] = l + 32 == pn ? 0.f : y1;
                 if (l == (pn & 31)) pivs[pn] = pn < 32 ? y0 : y1;
             }
-            __syncthreads();
+            sync();
         }
     }
     // X = (transformed R) / pivot, row by row, back into R
@@ -104,7 +108,7 @@ __device__ __forceinline__ void solve_walk_system(const float *A, int sb, float 
             if (h1) col[l + 32] = x1[k] / d1;
         }
     }
-    __syncthreads();
+    sync();
 }
 
 }  // namespace lisa

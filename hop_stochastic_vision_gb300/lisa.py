@@ -36,7 +36,8 @@ LISA_MAX_HIDDEN = 64
 EXPORTED = ("lisa_workspace_bytes", "lisa_forward", "lisa_forward_host", "lisa_num_stages",
             "lisa_stage_name", "lisa_forward_stage", "lisa_forward_noalloc", "lisa_backward_workspace_bytes",
             "lisa_backward", "lisa_backward_mlp_workspace_bytes", "lisa_backward_mlp", "lisa_status_string",
-            "lisa_abi_version", "lisa_query_status", "lisa_selftest_wait_timeout")
+            "lisa_abi_version", "lisa_query_status", "lisa_selftest_wait_timeout",
+            "lisa_forward_resident")
 
 LISA_NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -113,6 +114,8 @@ def load(path: str = LIB_PATH):
         lib.lisa_query_status.restype = i
         lib.lisa_selftest_wait_timeout.argtypes = [ctypes.c_longlong, vp, sz, vp]
         lib.lisa_selftest_wait_timeout.restype = i
+        lib.lisa_forward_resident.argtypes = lib.lisa_forward.argtypes
+        lib.lisa_forward_resident.restype = i
         _lib = lib
         return lib
 
@@ -133,6 +136,15 @@ def lisa_query_status(workspace, stream) -> int:
 
 def lisa_selftest_wait_timeout(cycles, workspace, workspace_bytes, stream) -> int:
     return int(load().lisa_selftest_wait_timeout(cycles, workspace, workspace_bytes, stream))
+
+
+def lisa_forward_resident(Q, K, V, O, B, heads, H, W, d_h, d_v, T, wts, alpha, eps, relu_inputs, dtype,
+                          workspace, workspace_bytes, stream) -> int:
+    """Test hook: lisa_forward's raw call through the single-kernel
+    tensor-core path (LISA_ERR_UNSUPPORTED where it does not apply)."""
+    return int(load().lisa_forward_resident(Q, K, V, O, B, heads, H, W, d_h, d_v, T, ctypes.byref(wts),
+                                            alpha, eps, relu_inputs, dtype, workspace, workspace_bytes,
+                                            stream))
 
 
 def lisa_workspace_bytes(B, heads, H, W, d_h, d_v, T, dtype) -> int:
