@@ -165,11 +165,12 @@ def hbm_peak():
         return 6800.0, "fallback"
 
 
-# The files the tensor-core forward kernels are built from (the kernels whose
-# DRAM traffic profiles/traffic.json records): a change to their code voids
+# The files the forward kernels are built from (the kernels whose DRAM
+# traffic profiles/traffic.json records): a change to their code voids
 # the recorded counters; comments and other kernels' sources do not.
-TRAFFIC_SOURCES = ("hop_stochastic_vision_gb300/csrc/lisa_tc.cu", "hop_stochastic_vision_gb300/csrc/lisa_sm100.cuh",
-                   "hop_stochastic_vision_gb300/csrc/lisa_solve.cuh",
+TRAFFIC_SOURCES = ("hop_stochastic_vision_gb300/csrc/lisa_tc.cu", "hop_stochastic_vision_gb300/csrc/lisa_tc_common.cuh",
+                   "hop_stochastic_vision_gb300/csrc/lisa_sm100.cuh",
+                   "hop_stochastic_vision_gb300/csrc/lisa_solve.cuh", "hop_stochastic_vision_gb300/csrc/lisa_simt.cu",
                    "hop_stochastic_vision_gb300/csrc/lisa_internal.h", "include/lisa.h")
 
 
@@ -436,11 +437,11 @@ def ours_arm(args, shape):
                 for s in range(nstages)]
     dom = max(range(nstages), key=lambda s: stage_us[s])
     peak, peak_src = hbm_peak()
-    dom_bytes = STAGE_BYTES_PER_TOKEN.get(names[dom], 0) * units * (shape.d // 64) * \
-        (1 if shape.dtype == "bf16" else 2)
+    esz = 2 if shape.dtype == "bf16" else 4
+    # the table is per token*head at bf16, d = 64: scale by width and element size
+    dom_bytes = STAGE_BYTES_PER_TOKEN.get(names[dom], 0) * units * shape.d * esz // (64 * 2)
     achieved = dom_bytes / (stage_us[dom] * 1e-6) / 1e9
     traffic = ncu_traffic(names[dom], shape.name)
-    esz = 2 if shape.dtype == "bf16" else 4
     path_bytes = 4 * shape.d * esz * units
     step_s = ms_max / 1e3 / args.steps
 
