@@ -20,6 +20,7 @@ namespace {
 
 constexpr int kTargetCtas = 2 * 152;  // two resident CTAs on each of the 152 SMs
 constexpr int kTcTargetCtas = 228;     // about 1.5 waves of the 152 SMs
+constexpr int kTcOneWaveCtas = 304;    // statistics CTAs resident at once for chunks <= 256 tokens (2 per SM)
 constexpr int kMinChunk = 64;         // smallest split-K chunk, in tokens
 constexpr size_t kAlign = 256;
 
@@ -59,6 +60,11 @@ Plan make_plan(int slices, int n, int D, int T, int dtype, int wmode, int hidden
         if (chunks > max_chunks) chunks = max_chunks;
         if (chunks < 1) chunks = 1;
         if (chunks > 8) chunks = (chunks + 7) / 8 * 8;
+        // short slices: rather one chunk per slice in a single wave than two
+        // half-length chunks in more than one (the per-CTA latency barely
+        // depends on the chunk's length there)
+        if (chunks > 1 && n <= 256 && (long long)slices * chunks > kTcOneWaveCtas)
+            chunks = std::max(1, kTcOneWaveCtas / slices);
         chunk = ((n + chunks - 1) / chunks + 63) / 64 * 64;
         chunks = (n + chunk - 1) / chunk;
         int cl = 1;

@@ -707,10 +707,15 @@ __global__ void __launch_bounds__(256) tc_recur_kernel(TcParams p) {
 // stores it with TMA itself.
 constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = 32 * (kEpiWarps + 1);
+constexpr int kMlpKSteps = LISA_MAX_HIDDEN / 16;   // m16n8k16 steps over the MLP's hidden units
+// Per-lane constants of the MLP head, [2 kMlpKSteps][32 lanes] of 16 bytes:
+// entry kk < kMlpKSteps holds the W2^T B fragments of k-step kk (hi, hi, lo, lo),
+// entry kMlpKSteps + kk the b1 values of the lane's columns in f8 = 2 kk, 2 kk + 1.
+constexpr uint32_t kMlpConstBytes = 2u * kMlpKSteps * 32u * 16u;
 constexpr uint32_t kOutBuf = 16 * kRow;   // one warp's 2 x 8 output block
 
 struct EpiLayout {
-    uint32_t q[2], kh[2], vh[2], kt[2], bepi[2], w1, out, total;
+    uint32_t q[2], kh[2], vh[2], kt[2], bepi[2], w1, mlpc, out, total;
 };
 
 __host__ __device__ inline uint32_t align1k(uint32_t x) { return (x + 1023u) & ~1023u; }
@@ -739,6 +744,7 @@ __host__ __device__ inline EpiLayout epi_layout(int BR, int BC, int epi_rows, in
         }
     }
     L.w1 = off; if (mlp) off += align1k(2u * n_mlp * kRow);
+    L.mlpc = off; if (mlp) off += kMlpConstBytes;
     L.out = off; off += kEpiWarps * 2 * kOutBuf;
     L.total = off;
     return L;
@@ -947,6 +953,44 @@ __global__ void __launch_bounds__(kEpiThreads, kMinBlocks)
             voff[pr] = (uint32_t)((2 * bi + kv2 / 10) * hw + 8 * bj + kv2 % 10);
         }
         const uint32_t qrow = (uint32_t)(16 * blk + (lane & 7) + 8 * ((lane >> 3) & 1));   // A-fragment row
+
+        // Adaptive weights: the logits z = W2 h + b2 of the 16 rows are one
+        // m16n8k16 product per 16 hidden units, h in the C-fragment layout the
+        // TMEM read gives (which is also the A-fragment layout).  W2^T as B
+        // fragments (k = hidden unit, n = walk length t) and b1 at this lane's
+        // hidden columns depend on the lane only: compute warp 0 writes them to
+        // a table once, every compute warp reads its lane's entries per tile.
+        // W2 and h are each split into two bf16 terms (hi + lo), so the
+        // product keeps ~16 significant bits.
+        const uint32_t mlpc = base + L.mlpc + (uint32_t)lane * 16u;
+        float b2r[2];
+        if (mlp) {
+            if (warp == 0) {
+#pragma unroll
+                for (int kk = 0; kk < kMlpKSteps; ++kk) {
+                    uint32_t hi[2], lo[2];
+                    float b1v[4];
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const int m0 = 16 * kk + 8 * hf + 2 * q4;
+                        float x[2];
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
+                            x[c] = (g < p.T && m0 + c < p.hidden) ? p.W2[g * p.hidden + m0 + c] : 0.f;
+                            b1v[2 * hf + c] = m0 + c < p.hidden ? p.b1[m0 + c] : 0.f;
+                        }
+                        hi[hf] = pack_bf16(x[0], x[1]);
+                        lo[hf] = pack_bf16(x[0] - bf16_lo(hi[hf]), x[1] - bf16_hi(hi[hf]));
+                    }
+                    st_shared_v4(mlpc + (uint32_t)kk * 512u, hi[0], hi[1], lo[0], lo[1]);
+                    st_shared_v4(mlpc + (uint32_t)(kMlpKSteps + kk) * 512u, __float_as_uint(b1v[0]),
+                                 __float_as_uint(b1v[1]), __float_as_uint(b1v[2]), __float_as_uint(b1v[3]));
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < 2; ++c) b2r[c] = 2 * q4 + c < p.T ? p.b2[2 * q4 + c] : 0.f;
+            asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");   // the compute warps only
+        }
         const uint32_t out_w = base + L.out + (uint32_t)warp * 2u * kOutBuf;
         const float c2 = 1.4426950408889634f * 0.125f;   // log2(e) / sqrt(64)
 
@@ -1026,59 +1070,57 @@ __global__ void __launch_bounds__(kEpiThreads, kMinBlocks)
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bar.qk_empty[s]));
 
-            float w0[2], wk[2][LISA_MAX_T_MLP];
+            float w0[2], wq[2][2];
             if (mlp) {
                 // adaptive step weights of rows g, g+8 from the MLP hidden layer in TMEM
                 if (!mbar_wait(smem_u32(&bar.mma_full[s]), ph)) record_error(p.err, kErrTimeoutMma);
                 tc_fence_after();
-                uint32_t hr[8][4];
+                // z (C fragment): (row g, t = 2 q4, 2 q4 + 1), (row g + 8, same)
+                float z[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int f8 = 0; f8 < 8; ++f8)
-                    if (8 * f8 < p.n_mlp) tmem_ld_frag_nowait(tl + p.epi_rows + 8 * f8, hr[f8]);
-                tc_wait_ld();
+                for (int kk = 0; kk < kMlpKSteps; ++kk) {
+                    if (16 * kk >= p.n_mlp) break;
+                    uint32_t hr[2][4];   // pre-activations of hidden columns 16 kk .. 16 kk + 15
+                    tmem_ld_frag_nowait(tl + p.epi_rows + 16 * kk, hr[0]);
+                    tmem_ld_frag_nowait(tl + p.epi_rows + 16 * kk + 8, hr[1]);
+                    uint32_t wf[4], bw[4], ahi[4], alo[4];
+                    ld_shared_v4(mlpc + (uint32_t)kk * 512u, wf[0], wf[1], wf[2], wf[3]);
+                    ld_shared_v4(mlpc + (uint32_t)(kMlpKSteps + kk) * 512u, bw[0], bw[1], bw[2], bw[3]);
+                    tc_wait_ld();
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
-#pragma unroll
-                    for (int t2 = 0; t2 < LISA_MAX_T_MLP; ++t2) wk[h][t2] = 0.f;
-#pragma unroll
-                for (int f8 = 0; f8 < 8; ++f8) {
-                    if (8 * f8 >= p.n_mlp) break;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int m = 8 * f8 + 2 * q4 + (e & 1);
-                        if (m < p.hidden) {
-                            const float hv = gelu_erf(__uint_as_float(hr[f8][e]) + p.b1[m]);
-#pragma unroll
-                            for (int t2 = 0; t2 < LISA_MAX_T_MLP; ++t2)
-                                if (t2 < p.T) wk[e >> 1][t2] = fmaf(p.W2[t2 * p.hidden + m], hv, wk[e >> 1][t2]);
-                        }
+                    for (int r = 0; r < 4; ++r) {
+                        // A register r: hidden columns of f8 = 2 kk + (r >> 1), row g (r even) or g + 8
+                        const int hf = r >> 1, e = 2 * (r & 1);
+                        const float h0 = gelu_erf(__uint_as_float(hr[hf][e]) + __uint_as_float(bw[2 * hf]));
+                        const float h1 = gelu_erf(__uint_as_float(hr[hf][e + 1]) + __uint_as_float(bw[2 * hf + 1]));
+                        ahi[r] = pack_bf16(h0, h1);
+                        alo[r] = pack_bf16(h0 - bf16_lo(ahi[r]), h1 - bf16_hi(ahi[r]));
                     }
+                    mma_bf16_16816(z, ahi[0], ahi[1], ahi[2], ahi[3], wf[0], wf[1]);
+                    mma_bf16_16816(z, alo[0], alo[1], alo[2], alo[3], wf[0], wf[1]);
+                    mma_bf16_16816(z, ahi[0], ahi[1], ahi[2], ahi[3], wf[2], wf[3]);
                 }
+                // softmax over t < T across the four lanes of the row's quad
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    float zmax = -INFINITY;
+                    float zz[2];
 #pragma unroll
-                    for (int t2 = 0; t2 < LISA_MAX_T_MLP; ++t2) {
-                        if (t2 >= p.T) break;
-                        float z = wk[h][t2];
-                        z += __shfl_xor_sync(0xffffffffu, z, 1);
-                        z += __shfl_xor_sync(0xffffffffu, z, 2);
-                        z += p.b2[t2];
-                        wk[h][t2] = z;
-                        zmax = fmaxf(zmax, z);
-                    }
-                    float zs = 0.f;
+                    for (int c = 0; c < 2; ++c) zz[c] = 2 * q4 + c < p.T ? z[2 * h + c] + b2r[c] : -INFINITY;
+                    float zmax = fmaxf(zz[0], zz[1]);
+                    zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, 1));
+                    zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, 2));
 #pragma unroll
-                    for (int t2 = 0; t2 < LISA_MAX_T_MLP; ++t2) {
-                        if (t2 >= p.T) break;
-                        wk[h][t2] = expf(wk[h][t2] - zmax);
-                        zs += wk[h][t2];
-                    }
+                    for (int c = 0; c < 2; ++c) wq[h][c] = 2 * q4 + c < p.T ? expf(zz[c] - zmax) : 0.f;
+                    float zs = wq[h][0] + wq[h][1];
+                    zs += __shfl_xor_sync(0xffffffffu, zs, 1);
+                    zs += __shfl_xor_sync(0xffffffffu, zs, 2);
                     const float zi = 1.f / zs;
-#pragma unroll
-                    for (int t2 = 0; t2 < LISA_MAX_T_MLP; ++t2) wk[h][t2] *= zi;
-                    w0[h] = wk[h][0];
+                    wq[h][0] *= zi;
+                    wq[h][1] *= zi;
                 }
+                // weight t of row h sits in lane (quad | t >> 1), element t & 1
+                w0[0] = __shfl_sync(0xffffffffu, wq[0][0], lane & ~3);
+                w0[1] = __shfl_sync(0xffffffffu, wq[1][0], lane & ~3);
             } else {
                 w0[0] = w0[1] = p.w[0];
             }
@@ -1189,14 +1231,22 @@ __global__ void __launch_bounds__(kEpiThreads, kMinBlocks)
                 arq[0] = __fdividef(alpha, d0 + p.eps);
                 arq[1] = __fdividef(alpha, d1 + p.eps);
                 if (mlp) {
+                    // walk length t = u + 1 weighs the product with U_(u+1)
+                    float wu[2];
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) acc[k] = wk[(k >> 1) & 1][1] * __uint_as_float(ru[k]);
-                    for (int u = 1; u < p.n_umat; ++u) {
+                    for (int h = 0; h < 2; ++h) wu[h] = __shfl_sync(0xffffffffu, wq[h][1], lane & ~3);
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) acc[k] = wu[(k >> 1) & 1] * __uint_as_float(ru[k]);
+#pragma unroll
+                    for (int u = 1; u < LISA_MAX_T_MLP - 1; ++u) {
+                        if (u >= p.n_umat) break;
                         tmem_ld_frag8_nowait(tl + u * kD, ru);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+                            wu[h] = __shfl_sync(0xffffffffu, wq[h][(u + 1) & 1], (lane & ~3) | ((u + 1) >> 1));
                         tc_wait_ld();
 #pragma unroll
-                        for (int k = 0; k < 32; ++k)
-                            acc[k] = fmaf(wk[(k >> 1) & 1][u + 1], __uint_as_float(ru[k]), acc[k]);
+                        for (int k = 0; k < 32; ++k) acc[k] = fmaf(wu[(k >> 1) & 1], __uint_as_float(ru[k]), acc[k]);
                     }
                 } else {
 #pragma unroll
