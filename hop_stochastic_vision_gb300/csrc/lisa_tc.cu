@@ -143,15 +143,18 @@ __device__ __forceinline__ void form_qtilde(uint8_t *Qb, const float *s, float e
     }
 }
 
-// TMEM [128 x 64] fp32 -> shared rows of kRedStride floats (thread = row).
-__device__ __forceinline__ void tmem_rows_to_smem(uint32_t tmem, float *red, int warp, int lane) {
-    const int row = 32 * warp + lane;
+// TMEM lanes lane0 .. lane0 + 31 (this warp's quadrant; 64 fp32 columns) ->
+// shared rows `stride` floats apart: thread `lane` writes row 32 w + lane of
+// `dst`.
+__device__ __forceinline__ void tmem_rows_to_smem(uint32_t tmem, float *dst0, int w, int lane, int stride,
+                                                  int lane0) {
+    const int row = 32 * w + lane;
 #pragma unroll
     for (int cb = 0; cb < 64; cb += 16) {
         uint32_t r[16];
-        tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + cb, r);
+        tmem_ld16(tmem + ((uint32_t)lane0 << 16) + cb, r);
         tc_wait_ld();
-        float4 *dst = reinterpret_cast<float4 *>(red + row * kRedStride + cb);
+        float4 *dst = reinterpret_cast<float4 *>(dst0 + row * stride + cb);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
             dst[k] = make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
@@ -370,7 +373,13 @@ __global__ void __launch_bounds__(kStatsThreads) tc_stats_fused_kernel(const __g
     float *Mt = reinterpret_cast<float *>(sm + 36 * 1024);         // [64][kMS], filled by the owners
     float *Ucur = reinterpret_cast<float *>(sm + 54 * 1024);       // [my_u][kUS]
     const int my_u = (64 - (int)rank + CL - 1) / CL;               // own rows e < 64
-    if (warp < 4) tmem_rows_to_smem(tmem, red, warp, lane);
+    if (CL == 1) {
+        // a slice in one CTA: no reduction, the rows go straight to U_1^T and M^T
+        if (warp < 4) tmem_rows_to_smem(tmem, warp < 2 ? Ucur : Mt, warp & 1, lane, warp < 2 ? kUS : kMS, 32 * warp);
+        tc_fence_before();
+        __syncthreads();
+    } else {
+    if (warp < 4) tmem_rows_to_smem(tmem, red, warp, lane, kRedStride, 32 * warp);
     tc_fence_before();
     cluster_sync();                                                // (B)
     {
@@ -392,6 +401,7 @@ __global__ void __launch_bounds__(kStatsThreads) tc_stats_fused_kernel(const __g
         }
     }
     cluster_sync();                                                // (C) M^T complete everywhere
+    }
     if (kUntruncated) {
         // own rows of U_1^T become those of ((I - beta M)^-1 U_1)^T: A = I - beta M
         // in place of M^T (element (a, b) at Mt[b][a]), the own U_1 columns as R
@@ -556,9 +566,7 @@ __global__ void __launch_bounds__(kStatsThreads) tc_stats_split_kernel(const __g
     } else {
         pdl_wait();  // s partials are complete
         if (tid < kD) {
-            float s = 0.f;
-            for (int cc = 0; cc < p.chunks; ++cc) s += p.s_part[((size_t)sl * p.chunks + cc) * kD + tid];
-            s_sh[tid] = s;
+            s_sh[tid] = sum_partials(p.s_part + (size_t)sl * p.chunks * kD, p.chunks, kD, tid);
         }
         named_sync_compute();
         constexpr uint32_t idesc = make_idesc_bf16(128, 64, true, true);
@@ -594,7 +602,7 @@ __global__ void __launch_bounds__(kStatsThreads) tc_stats_split_kernel(const __g
     }
 
     float *red = reinterpret_cast<float *>(sm);
-    if (warp < 4) tmem_rows_to_smem(tmem, red, warp, lane);
+    if (warp < 4) tmem_rows_to_smem(tmem, red, warp, lane, kRedStride, 32 * warp);
     tc_fence_before();
     cluster_sync();
     const uint32_t rank = cluster_rank();
@@ -629,6 +637,7 @@ __global__ void __launch_bounds__(256) tc_recur_kernel(TcParams p) {
         float4 acc[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 2
         for (int q = 0; q < p.parts; ++q) {
             float4 v[4];
 #pragma unroll
@@ -643,6 +652,7 @@ __global__ void __launch_bounds__(256) tc_recur_kernel(TcParams p) {
     }
     {   // own 16 rows of U_1^T: 256 float4, one per thread
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
         for (int q = 0; q < p.parts; ++q) {
             const float4 v = part[((size_t)q * 128 + 16 * rb) * 16 + tid];
             acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
@@ -651,9 +661,7 @@ __global__ void __launch_bounds__(256) tc_recur_kernel(TcParams p) {
         reinterpret_cast<float4 *>(&Fold[0][0])[tid] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     if (tid < kD) {
-        float s = 0.f;
-        for (int cc = 0; cc < p.chunks; ++cc) s += p.s_part[((size_t)sl * p.chunks + cc) * kD + tid];
-        s_sh[tid] = s;
+        s_sh[tid] = sum_partials(p.s_part + (size_t)sl * p.chunks * kD, p.chunks, kD, tid);
     }
     __syncthreads();
     if (p.untruncated) {   // own rows of U_1^T -> those of ((I - beta M)^-1 U_1)^T

@@ -124,12 +124,62 @@ __device__ __forceinline__ void mma_tf32_1688(float (&d)[4], uint32_t a0, uint32
 // (operands rounded to 10-bit mantissas, fp32 accumulation): U and Un with row
 // stride kUS, M^T with row stride kMS.  Warp w of `nwarps` takes the 8-column
 // tiles w, w + nwarps, ...; rows in tiles of 16 (missing rows read as zero and
-// are not stored).  The A fragments of a k-step are loaded once per row tile.
+// are not stored); when there are as many row tiles as warps, warp w takes
+// row tile w whole instead.  The A fragments of a k-step are loaded once per row tile.
 // With `fold`, also fold[i][a] += wk * Un[i][a] (stride kUS; each element is
 // owned by the thread that computes it).
 __device__ __forceinline__ void rows_times_mt_tf32(const float *U, const float *Mt, float *Un, int rows, int warp,
                                                    int lane, int nwarps, float *fold, float wk) {
     const int g = lane >> 2, q4 = lane & 3;
+    if (rows > 16 * (nwarps - 1) && rows <= 16 * nwarps) {
+        // one row tile per warp (a slice held by one CTA): all eight column
+        // tiles of it, four independent accumulator chains at a time
+        const int r0 = 16 * warp + g, r1 = r0 + 8;
+        uint32_t a[8][4];
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            const int b = 8 * ks + q4;
+            a[ks][0] = r0 < rows ? to_tf32(U[r0 * kUS + b]) : 0u;
+            a[ks][1] = r1 < rows ? to_tf32(U[r1 * kUS + b]) : 0u;
+            a[ks][2] = r0 < rows ? to_tf32(U[r0 * kUS + b + 4]) : 0u;
+            a[ks][3] = r1 < rows ? to_tf32(U[r1 * kUS + b + 4]) : 0u;
+        }
+#pragma unroll 1
+        for (int n0 = 0; n0 < 8; n0 += 4) {
+            float d[4][4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const int b = 8 * ks + q4;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    mma_tf32_1688(d[j], a[ks][0], a[ks][1], a[ks][2], a[ks][3],
+                                  to_tf32(Mt[b * kMS + 8 * (n0 + j) + g]), to_tf32(Mt[(b + 4) * kMS + 8 * (n0 + j) + g]));
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int c = 8 * (n0 + j) + 2 * q4;
+                if (r0 < rows) {
+                    Un[r0 * kUS + c] = d[j][0];
+                    Un[r0 * kUS + c + 1] = d[j][1];
+                    if (fold) {
+                        fold[r0 * kUS + c] = fmaf(wk, d[j][0], fold[r0 * kUS + c]);
+                        fold[r0 * kUS + c + 1] = fmaf(wk, d[j][1], fold[r0 * kUS + c + 1]);
+                    }
+                }
+                if (r1 < rows) {
+                    Un[r1 * kUS + c] = d[j][2];
+                    Un[r1 * kUS + c + 1] = d[j][3];
+                    if (fold) {
+                        fold[r1 * kUS + c] = fmaf(wk, d[j][2], fold[r1 * kUS + c]);
+                        fold[r1 * kUS + c + 1] = fmaf(wk, d[j][3], fold[r1 * kUS + c + 1]);
+                    }
+                }
+            }
+        }
+        return;
+    }
     for (int m0 = 0; m0 < rows; m0 += 16) {
         const int r0 = m0 + g, r1 = m0 + g + 8;
         uint32_t a[8][4];
@@ -190,6 +240,25 @@ __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Column `col` of the sum over `count` rows (row stride `stride` floats) of a
+// partial-sum array in global memory: eight loads in flight, eight
+// accumulators, added in a fixed order.
+__device__ __forceinline__ float sum_partials(const float *part, int count, int stride, int col) {
+    float a[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) a[u] = 0.f;
+    int r = 0;
+    for (; r + 8 <= count; r += 8) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = part[(size_t)(r + u) * stride + col];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) a[u] += v[u];
+    }
+    for (; r < count; ++r) a[0] += part[(size_t)r * stride + col];
+    return ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
 }
 
 __device__ __forceinline__ float gelu_erf(float x) {
