@@ -26,8 +26,11 @@ def cuda_lib():
 
 
 def _check(shape: LayerShape, *, seed=0, B=None, heads=None, structured=False, w=None,
-           relu=True, eps=1e-6, alpha=None, explicit=False, tol=None):
+           relu=True, eps=1e-6, alpha=None, explicit=False, tol=None, mlp_scale=None):
     inp = make_inputs(shape, seed=seed, B=B, heads=heads, structured=structured)
+    if mlp_scale is not None:
+        for key in ("W1", "b1", "W2", "b2"):
+            inp[key] = inp[key] * mlp_scale
     if alpha is not None:
         inp["alpha"] = torch.full_like(inp["alpha"], float(alpha))
     if not relu:
@@ -82,6 +85,15 @@ def test_depths_geometric(dtype, T):
 @pytest.mark.parametrize("T", [1, 2, 3, 5, 8])
 def test_adaptive_weights(dtype, d, T):
     _check(_shape(dtype, d, 10, 12, T, weights="mlp"), seed=T)
+
+
+@pytest.mark.parametrize("hidden,T", [(32, 3), (32, 8), (64, 5), (20, 4)])
+def test_adaptive_weights_far_from_uniform(hidden, T):
+    """MLP parameters 25x the N(0, 0.02) init: hidden pre-activations of a
+    few units and logits whose softmax is far from uniform, so the step
+    weights (and the bf16 hi + lo split of W2 and h that forms the logits on
+    the tensor path) matter to the output."""
+    _check(_shape("bf16", 64, 14, 18, T, weights="mlp", hidden=hidden), seed=hidden + T, mlp_scale=25.0)
 
 
 def test_limits_T16_and_hidden64():
