@@ -310,6 +310,14 @@ STAGE_BYTES_PER_TOKEN = {
 }
 
 
+def stage_bytes(name: str, units: int, d: int, dtype: str) -> int:
+    """Algorithmic bytes one launch of kernel `name` moves for `units`
+    token*heads at width d: the table is per token*head at bf16, d = 64, so
+    it scales with the width and the element size."""
+    esz = 2 if dtype == "bf16" else 4
+    return STAGE_BYTES_PER_TOKEN.get(name, 0) * units * d * esz // (64 * 2)
+
+
 def ours_arm(args, shape):
     import torch
     import torch.distributed as dist
@@ -438,8 +446,7 @@ def ours_arm(args, shape):
     dom = max(range(nstages), key=lambda s: stage_us[s])
     peak, peak_src = hbm_peak()
     esz = 2 if shape.dtype == "bf16" else 4
-    # the table is per token*head at bf16, d = 64: scale by width and element size
-    dom_bytes = STAGE_BYTES_PER_TOKEN.get(names[dom], 0) * units * shape.d * esz // (64 * 2)
+    dom_bytes = stage_bytes(names[dom], units, shape.d, shape.dtype)
     achieved = dom_bytes / (stage_us[dom] * 1e-6) / 1e9
     traffic = ncu_traffic(names[dom], shape.name)
     path_bytes = 4 * shape.d * esz * units
@@ -505,7 +512,7 @@ def ours_arm(args, shape):
 
 # -- the backward pass ------------------------------------------------------------------
 
-BWD_METRIC = "LiSA bwd tokens·heads/s (gradients of Xq, Xk, V, alpha%s); % of HBM roofline"
+BWD_METRIC = "LiSA bwd tokens·heads/s (gradients of Xq, Xk, V, alpha%s); %% of HBM roofline"
 # algorithmic bytes per token*head: read Q, K, V, dO, write dQ, dK, dV (d = 64, bf16)
 BWD_BYTES_PER_TOKEN = 7 * 64 * 2
 

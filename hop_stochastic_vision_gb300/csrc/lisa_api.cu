@@ -496,7 +496,7 @@ struct BwdPlan {
     Plan fwd;   // SIMT statistics partials (s, K^T V, K^T Q~) and s
     int nh, nblk;
     size_t off_mred, off_uk, off_ubar, off_ubart, off_dub, off_lstat, off_dalp, off_dsp, off_dm, off_du1,
-        off_dmt, off_du1t, off_dsr, off_dals, off_dkp, off_bimg;
+        off_dmt, off_du1t, off_dsr, off_dals, off_dkp, off_bimg, off_ubimg;
     // adaptive weights only
     size_t off_ukn, off_wtok, off_dz, off_h, off_da, off_dxm, off_dukp, off_pw1, off_pb1, off_pw2, off_pb2;
     size_t total;
@@ -527,6 +527,7 @@ BwdPlan make_bwd_plan(int slices, int n, int D, int T, int hidden) {
     b.off_dals = off;  off = align_up(off + S * sizeof(float));
     b.off_dkp = off;   off = align_up(off + S * N * d * sizeof(float));
     b.off_bimg = off;  off = align_up(off + S * 5 * dd * sizeof(uint16_t));
+    b.off_ubimg = off; off = align_up(off + S * 2 * dd * sizeof(uint16_t));
     if (hidden > 0) {
         const size_t Tz = (size_t)T, Hd = (size_t)hidden, nk = (size_t)b.nh;
         b.off_ukn = off;  off = align_up(off + S * nk * dd * sizeof(float));
@@ -628,6 +629,7 @@ lisa_status run_backward(const void *Q, const void *K, const void *V, const void
     b.dal_slice = f32(pl.off_dals);
     b.dk_part = f32(pl.off_dkp);
     b.bimg = reinterpret_cast<uint16_t *>(ws + pl.off_bimg);
+    b.ubimg = reinterpret_cast<uint16_t *>(ws + pl.off_ubimg);
     if (mlp) {
         b.mlp = 1;
         b.Ukn = f32(pl.off_ukn);

@@ -159,6 +159,11 @@ __global__ void __launch_bounds__(kThreads) bwd_recur(BwdProblem b) {
         const int idx = tid + x * kThreads;
         b.Ubar[(size_t)sl * D * D + idx] = ub[x];
         b.UbarT[(size_t)sl * D * D + (idx % D) * D + idx / D] = ub[x];
+        // the bf16 image of Ubar for the tensor-core token pass: hi, then the rest
+        const __nv_bfloat16 hi = __float2bfloat16_rn(ub[x]);
+        b.ubimg[(size_t)sl * 2 * D * D + idx] = __bfloat16_as_ushort(hi);
+        b.ubimg[(size_t)sl * 2 * D * D + D * D + idx] =
+            __bfloat16_as_ushort(__float2bfloat16_rn(ub[x] - __bfloat162float(hi)));
     }
 }
 
@@ -1034,6 +1039,186 @@ __device__ __forceinline__ uint32_t relu_bf16x2(uint32_t v) {
     return *reinterpret_cast<uint32_t *>(&x);
 }
 
+// ---------------------------------------------------------------------------
+// 3'. bf16, d = 64, fixed weights: step 3 with the global term on the tensor
+// cores and the window in quarter-warps.  The block's Q rows (bf16, exact)
+// times the bf16 image of Ubar (hi + lo terms, so the product keeps ~16
+// significant bits) give Q_i Ubar; g_i = w_0 V_i + (Q_i Ubar) / (Q_i . s + eps).
+// Then eight lanes per token, eight channels per lane: a row is one 16-byte
+// load and a dot product three shuffles, four tokens per warp at a time.
+// ---------------------------------------------------------------------------
+constexpr int kQS = 72;   // row stride (bf16) of the staged Q rows and Ubar image: ldmatrix conflict-free
+
+// Eight bf16 channels at `row` (16-byte aligned) as floats, optionally ReLU'd.
+__device__ __forceinline__ void load8_bf16(const __nv_bfloat16 *row, float (&x)[8], bool relu) {
+    const uint4 w = *reinterpret_cast<const uint4 *>(row);
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        x[2 * k] = sm100::bf16_lo(u[k]);
+        x[2 * k + 1] = sm100::bf16_hi(u[k]);
+    }
+    if (relu)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) x[k] = fmaxf(x[k], 0.f);
+}
+// Sum over the eight lanes of a quarter-warp (lanes 8 q .. 8 q + 7).
+__device__ __forceinline__ float group8_sum(float v) {
+    v += __shfl_xor_sync(0xffffffffu, v, 1);
+    v += __shfl_xor_sync(0xffffffffu, v, 2);
+    v += __shfl_xor_sync(0xffffffffu, v, 4);
+    return v;
+}
+__device__ __forceinline__ float dot8(const float (&x)[8], const float (&y)[8]) {
+    float a = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) a = fmaf(x[k], y[k], a);
+    return a;
+}
+
+__global__ void __launch_bounds__(kThreads) bwd_token_a_tc(BwdProblem b) {
+    constexpr int D = 64;
+    using namespace sm100;
+    __shared__ __align__(16) __nv_bfloat16 Ui[2 * D * kQS];   // Ubar hi rows a (cols e), then lo
+    __shared__ __align__(16) __nv_bfloat16 Qs[kTpb * kQS];    // the block's Q rows (feature-mapped)
+    __shared__ __align__(16) float G[kTpb][D + 4];            // Q_i Ubar
+    __shared__ __align__(16) float s_sh[D];
+    __shared__ float part[kWarps];
+    const Problem &p = b.fwd;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int sl = blockIdx.x / b.nblk, blk = blockIdx.x % b.nblk;
+    const int j0 = blk * kTpb, cnt = min(kTpb, p.n - j0);
+    const size_t sbase = (size_t)sl * p.n * D;
+    const __nv_bfloat16 *Q = static_cast<const __nv_bfloat16 *>(p.Q) + sbase;
+    const __nv_bfloat16 *K = static_cast<const __nv_bfloat16 *>(p.K) + sbase;
+    const __nv_bfloat16 *V = static_cast<const __nv_bfloat16 *>(p.V) + sbase;
+    const __nv_bfloat16 *dO = static_cast<const __nv_bfloat16 *>(b.dO) + sbase;
+    const float al = p.alpha[sl % p.heads], w0 = p.w[0];
+    const float scale = 0.125f;   // 1 / sqrt(64)
+
+    {
+        const uint4 *img = reinterpret_cast<const uint4 *>(b.ubimg + (size_t)sl * 2 * D * D);
+        for (int x = tid; x < 2 * D * 8; x += kThreads)
+            *reinterpret_cast<uint4 *>(Ui + (x >> 3) * kQS + (x & 7) * 8) = img[x];
+        for (int x = tid; x < kTpb * 8; x += kThreads) {
+            const int j = x >> 3, c = x & 7;
+            uint4 q = make_uint4(0u, 0u, 0u, 0u);
+            if (j < cnt) {
+                q = reinterpret_cast<const uint4 *>(Q)[((size_t)(j0 + j) * D) / 8 + c];
+                if (p.relu) q = make_uint4(relu_bf16x2(q.x), relu_bf16x2(q.y), relu_bf16x2(q.z), relu_bf16x2(q.w));
+            }
+            *reinterpret_cast<uint4 *>(Qs + j * kQS + c * 8) = q;
+        }
+        if (tid < D) s_sh[tid] = p.s_red[(size_t)sl * D + tid];
+    }
+    __syncthreads();
+
+    // ---- Q Ubar: warp = 16 tokens (mt) x 16 columns (sb), hi and lo terms
+    {
+        const int mt = warp & 1, sb = warp >> 1;
+        const uint32_t ua = smem_u32(Ui), qa = smem_u32(Qs);
+        const int arow = 16 * mt + (lane & 15), acol = (lane >> 4) * 8;
+        const int mi = lane >> 3, brow = (mi & 1) * 8 + (lane & 7), bcol = 16 * sb + (mi >> 1) * 8;
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(qa + (uint32_t)(arow * kQS + 16 * ks + acol) * 2u, a0, a1, a2, a3);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(ua + (uint32_t)((h * D + 16 * ks + brow) * kQS + bcol) * 2u, b0, b1, b2, b3);
+                mma_bf16_16816(acc[0], a0, a1, a2, a3, b0, b1);
+                mma_bf16_16816(acc[1], a0, a1, a2, a3, b2, b3);
+            }
+        }
+        const int row = 16 * mt + (lane >> 2);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const int col = 16 * sb + 8 * nt + 2 * (lane & 3);
+            G[row][col] = acc[nt][0];
+            G[row][col + 1] = acc[nt][1];
+            G[row + 8][col] = acc[nt][2];
+            G[row + 8][col + 1] = acc[nt][3];
+        }
+    }
+    __syncthreads();
+
+    // ---- quarter-warp per token: window softmax statistics, dl . l, dalpha terms
+    const int qg = lane >> 3, c8 = 8 * (lane & 7);
+    const int u = 4 * warp + qg;              // this quarter's token in the block
+    const bool live = u < cnt;
+    const int i = live ? j0 + u : j0;         // dead quarters repeat a valid token; nothing is kept
+    float q[8], v[8], go[8], g[8], sv[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        q[k] = __bfloat162float(Qs[u * kQS + c8 + k]);
+        sv[k] = s_sh[c8 + k];
+    }
+    load8_bf16(V + (size_t)i * D + c8, v, false);
+    load8_bf16(dO + (size_t)i * D + c8, go, false);
+    const float rq = 1.f / (group8_sum(dot8(q, sv)) + p.eps);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) g[k] = fmaf(rq, G[u][c8 + k], w0 * v[k]);
+    // the 3 x 3 window in row-major order; neighbours off the grid are masked
+    const int r = i / p.W, c = i % p.W;
+    float e[9];
+#pragma unroll
+    for (int t9 = 0; t9 < 9; ++t9) {
+        const int rr = r + t9 / 3 - 1, cc = c + t9 % 3 - 1;
+        const bool in = rr >= 0 && rr < p.H && cc >= 0 && cc < p.W;
+        float kr[8];
+        load8_bf16(K + (size_t)(in ? rr * p.W + cc : i) * D + c8, kr, p.relu);
+        e[t9] = dot8(q, kr);
+    }
+#pragma unroll
+    for (int t9 = 0; t9 < 9; ++t9) e[t9] = group8_sum(e[t9]);
+    float emax = -INFINITY;
+#pragma unroll
+    for (int t9 = 0; t9 < 9; ++t9) {
+        const int rr = r + t9 / 3 - 1, cc = c + t9 % 3 - 1;
+        const bool in = rr >= 0 && rr < p.H && cc >= 0 && cc < p.W;
+        e[t9] = in ? e[t9] * scale : -INFINITY;
+        emax = fmaxf(emax, e[t9]);
+    }
+    float l[8], esum = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) l[k] = 0.f;
+#pragma unroll
+    for (int t9 = 0; t9 < 9; ++t9) {
+        const int rr = r + t9 / 3 - 1, cc = c + t9 % 3 - 1;
+        const bool in = rr >= 0 && rr < p.H && cc >= 0 && cc < p.W;
+        const float a = in ? expf(e[t9] - emax) : 0.f;
+        esum += a;
+        float vr[8];
+        load8_bf16(V + (size_t)(in ? rr * p.W + cc : i) * D + c8, vr, false);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) l[k] = fmaf(a, vr[k], l[k]);
+    }
+    const float inv = 1.f / esum;
+    float dgl = 0.f, dll = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        l[k] *= inv;
+        dgl = fmaf(go[k], g[k] - l[k], dgl);
+        dll = fmaf(go[k], l[k], dll);
+    }
+    dgl = group8_sum(dgl);
+    dll = group8_sum(dll) * (1.f - al);
+    if ((lane & 7) == 0 && live)
+        reinterpret_cast<float4 *>(b.lstat)[(size_t)sl * p.n + j0 + u] = make_float4(emax, esum, dll, 0.f);
+    // dalpha terms of the warp's live tokens, in token order
+    float dal = ((lane & 7) == 0 && live) ? dgl : 0.f;
+    dal = warp_sum(dal);
+    if (lane == 0) part[warp] = dal;
+    __syncthreads();
+    if (tid == 0) {
+        float acc = 0.f;
+        for (int w = 0; w < kWarps; ++w) acc += part[w];
+        b.dal_part[(size_t)sl * b.nblk + blk] = acc;
+    }
+}
+
 __global__ void __launch_bounds__(kThreads) bwd_token_b_tc(BwdProblem b) {
     constexpr int D = 64, NC = 2;
     using namespace sm100;
@@ -1134,107 +1319,229 @@ __global__ void __launch_bounds__(kThreads) bwd_token_b_tc(BwdProblem b) {
     }
     __syncthreads();
 
-    // ---- one warp per token: normaliser, window, stores (as in the SIMT kernel)
-    float ds[NC] = {0.f, 0.f};
-    for (int u = warp; u < cnt; u += kWarps) {
-        const int j = j0 + u;
-        float q[NC], k[NC], v[NC], go[NC], sv[NC], dqt[NC], dv[NC], dk[NC];
+    if (!b.mlp) {
+        // ---- fixed weights: a quarter-warp per token (eight lanes, eight
+        // channels each); normaliser, window, stores
+        const int qg = lane >> 3, c8 = 8 * (lane & 7);
+        const int u = 4 * warp + qg;
+        const bool live = u < cnt;
+        const int j = j0 + (live ? u : 0);
+        float q[8], go[8], k[8], v[8], dqt[8], dv[8], dk[8];
 #pragma unroll
-        for (int t = 0; t < NC; ++t) {
-            const int ch = lane + 32 * t;
-            q[t] = __bfloat162float(Qb[u * D + ch]);
-            go[t] = __bfloat162float(A1[u * kAS + ch]);
-            k[t] = __bfloat162float(A1[u * kAS + 64 + ch]);
-            v[t] = __bfloat162float(A3[u * kAS + ch]);
-            sv[t] = s[ch];
-            dqt[t] = oQ[u * D + ch];
-            dv[t] = fmaf(w0 * al, go[t], oV[u * D + ch]);
-            dk[t] = oK[u * D + ch];
+        for (int e = 0; e < 8; ++e) {
+            q[e] = __bfloat162float(Qb[u * D + c8 + e]);
+            go[e] = __bfloat162float(A1[u * kAS + c8 + e]);
+            k[e] = __bfloat162float(A1[u * kAS + 64 + c8 + e]);
+            v[e] = __bfloat162float(A3[u * kAS + c8 + e]);
+            dqt[e] = oQ[u * D + c8 + e];
+            dv[e] = fmaf(w0 * al, go[e], oV[u * D + c8 + e]);
+            dk[e] = oK[u * D + c8 + e];
         }
-        if (b.mlp) mlp_walk_terms<D>(b, sl, j, lane, al, go, dqt, dv);
         const float rq = rqs[u];
-        const float cj = dot_row<D>(dqt, q) * rq * rq;
-        float dq[NC];
+        const float cj = group8_sum(dot8(dqt, q)) * rq * rq;
+        float dq[8], dsl[8];
 #pragma unroll
-        for (int t = 0; t < NC; ++t) {
-            dq[t] = dqt[t] * rq - cj * sv[t];
-            ds[t] = fmaf(-cj, q[t], ds[t]);
+        for (int e = 0; e < 8; ++e) {
+            dq[e] = dqt[e] * rq - cj * s[c8 + e];
+            dsl[e] = live ? -cj * q[e] : 0.f;
         }
-        if (b.mlp) {   // the MLP's share of dq_j, dk_j
-            const float *xm = b.dxm + ((size_t)sl * p.n + j) * 2 * D;
-#pragma unroll
-            for (int t = 0; t < NC; ++t) {
-                dq[t] += xm[lane + 32 * t];
-                dk[t] += xm[D + lane + 32 * t];
-            }
-        }
-        int nb[9];
-        const int nn = window(j, p.H, p.W, nb);
+        const int r = j / p.W, c = j % p.W;
         const float4 sj = lst[j];
         const float izj = 1.f / sj.y;
+        // j as the query: scores against its window, dl_j . V_i
         {
-            float kr[9][NC], vr[9][NC], d1[18];
+            float d1[18];
 #pragma unroll
             for (int t9 = 0; t9 < 9; ++t9) {
-                const int row = t9 < nn ? nb[t9] : j;
-                load_row<__nv_bfloat16, D>(K + (size_t)row * D, kr[t9], lane, p.relu);
-                load_row<__nv_bfloat16, D>(V + (size_t)row * D, vr[t9], lane, 0);
-                d1[t9] = d1[9 + t9] = 0.f;
-#pragma unroll
-                for (int t = 0; t < NC; ++t) {
-                    d1[t9] = fmaf(q[t], kr[t9][t], d1[t9]);
-                    d1[9 + t9] = fmaf(go[t], vr[t9][t], d1[9 + t9]);
-                }
+                const int rr = r + t9 / 3 - 1, cc = c + t9 % 3 - 1;
+                const bool in = rr >= 0 && rr < p.H && cc >= 0 && cc < p.W;
+                const size_t row = (size_t)(in ? rr * p.W + cc : j) * D + c8;
+                float kr[8], vr[8];
+                load8_bf16(K + row, kr, p.relu);
+                load8_bf16(V + row, vr, false);
+                d1[t9] = dot8(q, kr);
+                d1[9 + t9] = dot8(go, vr);
             }
-            warp_sum_n(d1);
+#pragma unroll
+            for (int t = 0; t < 18; ++t) d1[t] = group8_sum(d1[t]);
 #pragma unroll
             for (int t9 = 0; t9 < 9; ++t9) {
-                if (t9 >= nn) break;
+                const int rr = r + t9 / 3 - 1, cc = c + t9 % 3 - 1;
+                const bool in = rr >= 0 && rr < p.H && cc >= 0 && cc < p.W;
+                if (!in) continue;
                 const float a = expf(d1[t9] * scale - sj.x) * izj;
                 const float de = a * (d1[9 + t9] * (1.f - al) - sj.z) * scale;
+                float kr[8];
+                load8_bf16(K + (size_t)(rr * p.W + cc) * D + c8, kr, p.relu);
 #pragma unroll
-                for (int t = 0; t < NC; ++t) dq[t] = fmaf(de, kr[t9][t], dq[t]);
+                for (int e = 0; e < 8; ++e) dq[e] = fmaf(de, kr[e], dq[e]);
             }
         }
+        // j as a key of each neighbour i's window (the window is symmetric)
         {
-            float qi[9][NC], gi[9][NC], d2[18];
+            float d2[18];
 #pragma unroll
             for (int t9 = 0; t9 < 9; ++t9) {
-                const int row = t9 < nn ? nb[t9] : j;
-                load_row<__nv_bfloat16, D>(Q + (size_t)row * D, qi[t9], lane, p.relu);
-                load_row<__nv_bfloat16, D>(dO + (size_t)row * D, gi[t9], lane, 0);
-                d2[t9] = d2[9 + t9] = 0.f;
-#pragma unroll
-                for (int t = 0; t < NC; ++t) {
-                    d2[t9] = fmaf(qi[t9][t], k[t], d2[t9]);
-                    d2[9 + t9] = fmaf(gi[t9][t], v[t], d2[9 + t9]);
-                }
+                const int rr = r + t9 / 3 - 1, cc = c + t9 % 3 - 1;
+                const bool in = rr >= 0 && rr < p.H && cc >= 0 && cc < p.W;
+                const size_t row = (size_t)(in ? rr * p.W + cc : j) * D + c8;
+                float qi[8], gi[8];
+                load8_bf16(Q + row, qi, p.relu);
+                load8_bf16(dO + row, gi, false);
+                d2[t9] = dot8(qi, k);
+                d2[9 + t9] = dot8(gi, v);
             }
-            warp_sum_n(d2);
+#pragma unroll
+            for (int t = 0; t < 18; ++t) d2[t] = group8_sum(d2[t]);
 #pragma unroll
             for (int t9 = 0; t9 < 9; ++t9) {
-                if (t9 >= nn) break;
-                const float4 si = lst[nb[t9]];
+                const int rr = r + t9 / 3 - 1, cc = c + t9 % 3 - 1;
+                const bool in = rr >= 0 && rr < p.H && cc >= 0 && cc < p.W;
+                if (!in) continue;
+                const int ni = rr * p.W + cc;
+                const float4 si = lst[ni];
                 const float a = expf(d2[t9] * scale - si.x) / si.y;
                 const float de = a * (d2[9 + t9] * (1.f - al) - si.z) * scale;
+                float qi[8], gi[8];
+                load8_bf16(Q + (size_t)ni * D + c8, qi, p.relu);
+                load8_bf16(dO + (size_t)ni * D + c8, gi, false);
 #pragma unroll
-                for (int t = 0; t < NC; ++t) {
-                    dv[t] = fmaf(a * (1.f - al), gi[t9][t], dv[t]);
-                    dk[t] = fmaf(de, qi[t9][t], dk[t]);
+                for (int e = 0; e < 8; ++e) {
+                    dv[e] = fmaf(a * (1.f - al), gi[e], dv[e]);
+                    dk[e] = fmaf(de, qi[e], dk[e]);
                 }
             }
         }
+        if (live) {
+            float xq[8];
+            load8_bf16(Q + (size_t)j * D + c8, xq, false);
+            uint4 oq, ov;
+            uint32_t *pq = &oq.x, *pv = &ov.x;
 #pragma unroll
-        for (int t = 0; t < NC; ++t) {
-            const int ch = lane + 32 * t;
-            const float xq = __bfloat162float(Q[(size_t)j * D + ch]);
-            dQo[(size_t)j * D + ch] = __float2bfloat16_rn((p.relu && !(xq > 0.f)) ? 0.f : dq[t]);
-            dVo[(size_t)j * D + ch] = __float2bfloat16_rn(dv[t]);
-            dKp[(size_t)j * D + ch] = dk[t];
+            for (int e = 0; e < 4; ++e) {
+                const float q0 = (p.relu && !(xq[2 * e] > 0.f)) ? 0.f : dq[2 * e];
+                const float q1 = (p.relu && !(xq[2 * e + 1] > 0.f)) ? 0.f : dq[2 * e + 1];
+                pq[e] = pack_bf16(q0, q1);
+                pv[e] = pack_bf16(dv[2 * e], dv[2 * e + 1]);
+            }
+            *reinterpret_cast<uint4 *>(dQo + (size_t)j * D + c8) = oq;
+            *reinterpret_cast<uint4 *>(dVo + (size_t)j * D + c8) = ov;
+            float4 *kp = reinterpret_cast<float4 *>(dKp + (size_t)j * D + c8);
+            kp[0] = make_float4(dk[0], dk[1], dk[2], dk[3]);
+            kp[1] = make_float4(dk[4], dk[5], dk[6], dk[7]);
         }
-    }
+        // the warp's four tokens' ds terms, summed over the quarters in a fixed order
 #pragma unroll
-    for (int t = 0; t < NC; ++t) dsw[warp][lane + 32 * t] = ds[t];
+        for (int e = 0; e < 8; ++e) {
+            dsl[e] += __shfl_xor_sync(0xffffffffu, dsl[e], 8);
+            dsl[e] += __shfl_xor_sync(0xffffffffu, dsl[e], 16);
+        }
+        if (qg == 0)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) dsw[warp][c8 + e] = dsl[e];
+    } else {
+    // ---- one warp per token: normaliser, window, stores (as in the SIMT kernel)
+        float ds[NC] = {0.f, 0.f};
+        for (int u = warp; u < cnt; u += kWarps) {
+            const int j = j0 + u;
+            float q[NC], k[NC], v[NC], go[NC], sv[NC], dqt[NC], dv[NC], dk[NC];
+#pragma unroll
+            for (int t = 0; t < NC; ++t) {
+                const int ch = lane + 32 * t;
+                q[t] = __bfloat162float(Qb[u * D + ch]);
+                go[t] = __bfloat162float(A1[u * kAS + ch]);
+                k[t] = __bfloat162float(A1[u * kAS + 64 + ch]);
+                v[t] = __bfloat162float(A3[u * kAS + ch]);
+                sv[t] = s[ch];
+                dqt[t] = oQ[u * D + ch];
+                dv[t] = fmaf(w0 * al, go[t], oV[u * D + ch]);
+                dk[t] = oK[u * D + ch];
+            }
+            if (b.mlp) mlp_walk_terms<D>(b, sl, j, lane, al, go, dqt, dv);
+            const float rq = rqs[u];
+            const float cj = dot_row<D>(dqt, q) * rq * rq;
+            float dq[NC];
+#pragma unroll
+            for (int t = 0; t < NC; ++t) {
+                dq[t] = dqt[t] * rq - cj * sv[t];
+                ds[t] = fmaf(-cj, q[t], ds[t]);
+            }
+            if (b.mlp) {   // the MLP's share of dq_j, dk_j
+                const float *xm = b.dxm + ((size_t)sl * p.n + j) * 2 * D;
+#pragma unroll
+                for (int t = 0; t < NC; ++t) {
+                    dq[t] += xm[lane + 32 * t];
+                    dk[t] += xm[D + lane + 32 * t];
+                }
+            }
+            int nb[9];
+            const int nn = window(j, p.H, p.W, nb);
+            const float4 sj = lst[j];
+            const float izj = 1.f / sj.y;
+            {
+                float kr[9][NC], vr[9][NC], d1[18];
+#pragma unroll
+                for (int t9 = 0; t9 < 9; ++t9) {
+                    const int row = t9 < nn ? nb[t9] : j;
+                    load_row<__nv_bfloat16, D>(K + (size_t)row * D, kr[t9], lane, p.relu);
+                    load_row<__nv_bfloat16, D>(V + (size_t)row * D, vr[t9], lane, 0);
+                    d1[t9] = d1[9 + t9] = 0.f;
+#pragma unroll
+                    for (int t = 0; t < NC; ++t) {
+                        d1[t9] = fmaf(q[t], kr[t9][t], d1[t9]);
+                        d1[9 + t9] = fmaf(go[t], vr[t9][t], d1[9 + t9]);
+                    }
+                }
+                warp_sum_n(d1);
+#pragma unroll
+                for (int t9 = 0; t9 < 9; ++t9) {
+                    if (t9 >= nn) break;
+                    const float a = expf(d1[t9] * scale - sj.x) * izj;
+                    const float de = a * (d1[9 + t9] * (1.f - al) - sj.z) * scale;
+#pragma unroll
+                    for (int t = 0; t < NC; ++t) dq[t] = fmaf(de, kr[t9][t], dq[t]);
+                }
+            }
+            {
+                float qi[9][NC], gi[9][NC], d2[18];
+#pragma unroll
+                for (int t9 = 0; t9 < 9; ++t9) {
+                    const int row = t9 < nn ? nb[t9] : j;
+                    load_row<__nv_bfloat16, D>(Q + (size_t)row * D, qi[t9], lane, p.relu);
+                    load_row<__nv_bfloat16, D>(dO + (size_t)row * D, gi[t9], lane, 0);
+                    d2[t9] = d2[9 + t9] = 0.f;
+#pragma unroll
+                    for (int t = 0; t < NC; ++t) {
+                        d2[t9] = fmaf(qi[t9][t], k[t], d2[t9]);
+                        d2[9 + t9] = fmaf(gi[t9][t], v[t], d2[9 + t9]);
+                    }
+                }
+                warp_sum_n(d2);
+#pragma unroll
+                for (int t9 = 0; t9 < 9; ++t9) {
+                    if (t9 >= nn) break;
+                    const float4 si = lst[nb[t9]];
+                    const float a = expf(d2[t9] * scale - si.x) / si.y;
+                    const float de = a * (d2[9 + t9] * (1.f - al) - si.z) * scale;
+#pragma unroll
+                    for (int t = 0; t < NC; ++t) {
+                        dv[t] = fmaf(a * (1.f - al), gi[t9][t], dv[t]);
+                        dk[t] = fmaf(de, qi[t9][t], dk[t]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < NC; ++t) {
+                const int ch = lane + 32 * t;
+                const float xq = __bfloat162float(Q[(size_t)j * D + ch]);
+                dQo[(size_t)j * D + ch] = __float2bfloat16_rn((p.relu && !(xq > 0.f)) ? 0.f : dq[t]);
+                dVo[(size_t)j * D + ch] = __float2bfloat16_rn(dv[t]);
+                dKp[(size_t)j * D + ch] = dk[t];
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < NC; ++t) dsw[warp][lane + 32 * t] = ds[t];
+    }
     __syncthreads();
     for (int ch = tid; ch < D; ch += kThreads) {
         float acc = 0.f;
@@ -1404,7 +1711,10 @@ cudaError_t launch_bwd_all(const BwdProblem &b, cudaStream_t st) {
         if (p.T > 1) bwd_stats_duk<TIn, D><<<dim3(grid_stats, (unsigned)(p.T - 1)), kThreads, 0, st>>>(b);
     } else {
         bwd_stats_dub<TIn, D><<<grid_stats, kThreads, 0, st>>>(b);
-        bwd_token_a<TIn, D><<<grid_tok, kThreads, 0, st>>>(b);
+        if (std::is_same<TIn, __nv_bfloat16>::value && D == 64 && p.relu != 2)
+            bwd_token_a_tc<<<grid_tok, kThreads, 0, st>>>(b);
+        else
+            bwd_token_a<TIn, D><<<grid_tok, kThreads, 0, st>>>(b);
     }
     bwd_recur_back<D><<<p.slices, kThreads, 0, st>>>(b);
     // bf16 at d = 64 takes the tensor-core token pass, except with the ELU map

@@ -29,6 +29,7 @@ struct BwdProblem {
     float *dM, *dU1;     // [S][D][D]
     float *dMT, *dU1T;   // [S][D][D]      the same, transposed
     uint16_t *bimg;      // [S][5 D][D] bf16: [alpha Ubar^T; dM; dU_1^T; dM^T; dU_1] (bf16, d = 64)
+    uint16_t *ubimg;     // [S][2][D][D] bf16: Ubar row-major as hi and lo terms (hi + lo ~ Ubar)
     float *ds_red;       // [S][D]
     float *dal_slice;    // [S]
     float *dk_part;      // [S][n][D]      dK without ds, fp32

@@ -71,3 +71,21 @@ def test_reference_arm_under_torchrun_prints_one_line():
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["steps"] == 2
     assert d["unit"] == bench.UNIT and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_metric_strings_format():
+    """Both metric strings of the JSON line format without error (a literal
+    percent sign in a format string once broke the backward line)."""
+    assert "%" not in bench.METRIC.replace("% of", "")
+    for extra in ("", " and the MLP parameters"):
+        line = bench.BWD_METRIC % extra
+        assert line.endswith("% of HBM roofline") and extra in line
+
+
+def test_roofline_bytes_scale_with_width_and_dtype():
+    """The per-kernel byte table is per token*head at bf16, d = 64; narrower
+    widths and fp32 scale it, never to zero."""
+    assert bench.stage_bytes("epilogue", 196, 16, "f32") == 196 * 4 * 16 * 4      # Q, K, V, O in fp32
+    assert bench.stage_bytes("tc_epilogue", 100352, 64, "bf16") == 100352 * 512
+    assert bench.stage_bytes("tc_stats_fused", 10, 64, "bf16") == 10 * 384
+    assert bench.stage_bytes("tc_recur", 10, 64, "bf16") == 0
