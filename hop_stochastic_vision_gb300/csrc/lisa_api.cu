@@ -494,6 +494,8 @@ constexpr int kBwdTokensPerBlock = 32;   // per-token kernels: 8 warps x 4 token
 
 struct BwdPlan {
     Plan fwd;   // SIMT statistics partials (s, K^T V, K^T Q~) and s
+    Plan tc;    // bf16, d = 64: the tensor-core split statistics' own region (tc.total == 0 otherwise)
+    size_t off_tc;
     int nh, nblk;
     size_t off_mred, off_uk, off_ubar, off_ubart, off_dub, off_lstat, off_dalp, off_dsp, off_dm, off_du1,
         off_dmt, off_du1t, off_dsr, off_dals, off_dkp, off_bimg, off_ubimg;
@@ -504,7 +506,7 @@ struct BwdPlan {
 
 // The backward always runs the SIMT statistics kernels; its own buffers
 // follow the forward plan's.  hidden > 0: the adaptive weights' buffers too.
-BwdPlan make_bwd_plan(int slices, int n, int D, int T, int hidden) {
+BwdPlan make_bwd_plan(int slices, int n, int D, int T, int hidden, int dtype) {
     BwdPlan b{};
     b.fwd = make_plan(slices, n, D, T, LISA_F32, LISA_W_FIXED, 0);   // SIMT family, any dtype
     b.nh = T > 1 ? T - 1 : 1;
@@ -528,6 +530,11 @@ BwdPlan make_bwd_plan(int slices, int n, int D, int T, int hidden) {
     b.off_dkp = off;   off = align_up(off + S * N * d * sizeof(float));
     b.off_bimg = off;  off = align_up(off + S * 5 * dd * sizeof(uint16_t));
     b.off_ubimg = off; off = align_up(off + S * 2 * dd * sizeof(uint16_t));
+    if (dtype == LISA_BF16 && D == 64) {
+        b.tc = make_plan(slices, n, D, T, LISA_BF16, LISA_W_FIXED, 0);
+        b.off_tc = off;
+        off = align_up(off + b.tc.total);
+    }
     if (hidden > 0) {
         const size_t Tz = (size_t)T, Hd = (size_t)hidden, nk = (size_t)b.nh;
         b.off_ukn = off;  off = align_up(off + S * nk * dd * sizeof(float));
@@ -597,7 +604,7 @@ lisa_status run_backward(const void *Q, const void *K, const void *V, const void
     if (overlaps(dalpha, (size_t)heads * sizeof(float), alpha, (size_t)heads * sizeof(float)))
         return LISA_ERR_INVALID_ARG;
 
-    const BwdPlan pl = make_bwd_plan((int)slices, (int)n, d_h, b.fwd.T, mlp ? b.fwd.hidden : 0);
+    const BwdPlan pl = make_bwd_plan((int)slices, (int)n, d_h, b.fwd.T, mlp ? b.fwd.hidden : 0, dtype);
     if (!workspace || workspace_bytes < pl.total) return LISA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return LISA_ERR_INVALID_ARG;
     fill_problem(b.fwd, pl.fwd, Q, K, V, nullptr, (int)slices, heads, H, W, d_h, relu_inputs, eps, alpha, dtype,
@@ -630,6 +637,16 @@ lisa_status run_backward(const void *Q, const void *K, const void *V, const void
     b.dk_part = f32(pl.off_dkp);
     b.bimg = reinterpret_cast<uint16_t *>(ws + pl.off_bimg);
     b.ubimg = reinterpret_cast<uint16_t *>(ws + pl.off_ubimg);
+    if (pl.tc.total > 0 && relu_inputs != 2) {
+        // the statistics on the tensor cores; their kernels report into the
+        // backward's own error word
+        b.tc_stats = 1;
+        b.tcfwd = b.fwd;
+        fill_problem(b.tcfwd, pl.tc, Q, K, V, nullptr, (int)slices, heads, H, W, d_h, relu_inputs, eps, alpha,
+                     dtype, ws + pl.off_tc);
+        b.tcfwd.err = b.fwd.err;
+        b.tcfwd.wmode = LISA_W_FIXED;   // statistics only: the walk weights play no part
+    }
     if (mlp) {
         b.mlp = 1;
         b.Ukn = f32(pl.off_ukn);
@@ -658,7 +675,7 @@ extern "C" size_t lisa_backward_workspace_bytes(int B, int heads, int H, int W, 
     if (check_sizes(B, heads, H, W, d_h, d_v, T, dtype) != LISA_OK) return 0;
     const long long slices = (long long)B * heads, n = (long long)H * W;
     if (slices == 0 || n == 0) return 0;
-    return make_bwd_plan((int)slices, (int)n, d_h, effective_T(T), 0).total;
+    return make_bwd_plan((int)slices, (int)n, d_h, effective_T(T), 0, dtype).total;
 }
 
 extern "C" lisa_status lisa_backward(const void *Q, const void *K, const void *V, const void *dO, void *dQ,
@@ -681,7 +698,7 @@ extern "C" size_t lisa_backward_mlp_workspace_bytes(int B, int heads, int H, int
     if (T < 1 || T > LISA_MAX_T_MLP || hidden < 1 || hidden > LISA_MAX_HIDDEN) return 0;
     const long long slices = (long long)B * heads, n = (long long)H * W;
     if (slices == 0 || n == 0) return 0;
-    return make_bwd_plan((int)slices, (int)n, d_h, T, hidden).total;
+    return make_bwd_plan((int)slices, (int)n, d_h, T, hidden, dtype).total;
 }
 
 extern "C" lisa_status lisa_backward_mlp(const void *Q, const void *K, const void *V, const void *dO, void *dQ,

@@ -87,21 +87,46 @@ __global__ void __launch_bounds__(kThreads) bwd_recur(BwdProblem b) {
     __shared__ float Un[D][D];
     const Problem &p = b.fwd;
     const int sl = blockIdx.x, tid = threadIdx.x;
-    for (int idx = tid; idx < D * D; idx += kThreads) {
-        float m = 0.f, u = 0.f;
-        for (int c = 0; c < p.chunks; ++c) {
-            const size_t pc = ((size_t)sl * p.chunks + c) * D * D + idx;
-            m += p.m_part[pc];
-            u += p.u_part[pc];
+    if (b.tc_stats) {
+        // tensor-core partials: per part a [U_1^T ; M^T] block of 2D rows x D
+        // columns (row e < D: U_1[.][e]; row D + c: M[.][c]), summed in part order
+        const Problem &t = b.tcfwd;
+        const int parts = t.chunks / t.tc_cluster;
+        const float *tp = t.tc_part + (size_t)sl * parts * 2 * D * D;
+        for (int idx = tid; idx < D * D; idx += kThreads) {
+            const int r = idx / D, a = idx % D;   // partial row r (U_1 column r, M column r), column a
+            float m = 0.f, u = 0.f;
+            for (int q = 0; q < parts; ++q) {
+                u += tp[(size_t)q * 2 * D * D + idx];
+                m += tp[(size_t)q * 2 * D * D + D * D + idx];
+            }
+            U[a][r] = u;
+            M[a][r] = m;
         }
-        M[idx / D][idx % D] = m;
-        U[idx / D][idx % D] = u;
-        b.Mred[(size_t)sl * D * D + idx] = m;
-    }
-    if (tid < D) {
-        float acc = 0.f;
-        for (int c = 0; c < p.chunks; ++c) acc += p.s_part[((size_t)sl * p.chunks + c) * D + tid];
-        p.s_red[(size_t)sl * D + tid] = acc;
+        if (tid < D) {
+            float acc = 0.f;
+            for (int c = 0; c < t.chunks; ++c) acc += t.s_part[((size_t)sl * t.chunks + c) * D + tid];
+            p.s_red[(size_t)sl * D + tid] = acc;
+        }
+        __syncthreads();
+        for (int idx = tid; idx < D * D; idx += kThreads) b.Mred[(size_t)sl * D * D + idx] = M[idx / D][idx % D];
+    } else {
+        for (int idx = tid; idx < D * D; idx += kThreads) {
+            float m = 0.f, u = 0.f;
+            for (int c = 0; c < p.chunks; ++c) {
+                const size_t pc = ((size_t)sl * p.chunks + c) * D * D + idx;
+                m += p.m_part[pc];
+                u += p.u_part[pc];
+            }
+            M[idx / D][idx % D] = m;
+            U[idx / D][idx % D] = u;
+            b.Mred[(size_t)sl * D * D + idx] = m;
+        }
+        if (tid < D) {
+            float acc = 0.f;
+            for (int c = 0; c < p.chunks; ++c) acc += p.s_part[((size_t)sl * p.chunks + c) * D + tid];
+            p.s_red[(size_t)sl * D + tid] = acc;
+        }
     }
     __syncthreads();
     float *Uk = b.Uk + (size_t)sl * b.nh * D * D;   // transposed: Uk[c][a] = U_k[a][c]
@@ -1700,9 +1725,13 @@ template <typename TIn, int D>
 cudaError_t launch_bwd_all(const BwdProblem &b, cudaStream_t st) {
     const Problem &p = b.fwd;
     if (b.tpb != kTpb) return cudaErrorInvalidValue;   // the plan's blocks are kTpb tokens
-    cudaError_t err = launch_simt(p, st, 0);   // partial s, K^T V
-    if (err != cudaSuccess) return err;
-    if ((err = launch_simt(p, st, 1)) != cudaSuccess) return err;   // partial K^T Q~
+    cudaError_t err;
+    if (b.tc_stats) {   // key-sum and [U_1^T ; M^T] partials on the tensor cores
+        if ((err = launch_tc_stats_partials(b.tcfwd, st)) != cudaSuccess) return err;
+    } else {
+        if ((err = launch_simt(p, st, 0)) != cudaSuccess) return err;   // partial s, K^T V
+        if ((err = launch_simt(p, st, 1)) != cudaSuccess) return err;   // partial K^T Q~
+    }
     const unsigned grid_stats = (unsigned)p.slices * (unsigned)p.chunks;
     const unsigned grid_tok = (unsigned)p.slices * (unsigned)b.nblk;
     bwd_recur<D><<<p.slices, kThreads, 0, st>>>(b);

@@ -13,6 +13,10 @@ namespace lisa {
 // upstream gradient, the outputs and the backward's workspace views.
 struct BwdProblem {
     Problem fwd;
+    // bf16, d = 64, ReLU or no feature map: the statistics come from the
+    // tensor-core split chain (tcfwd's workspace views) instead of the SIMT one
+    int tc_stats;
+    Problem tcfwd;
     const void *dO;
     void *dQ, *dK, *dV;
     float *dalpha;       // device [heads], overwritten

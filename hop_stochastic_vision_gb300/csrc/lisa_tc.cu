@@ -1344,6 +1344,14 @@ bool tc_fused(int chunks, int cluster, int chunk) {
     return chunks == cluster && (chunk + kSub - 1) / kSub <= kFusedMaxSub;
 }
 
+cudaError_t launch_tc_stats_partials(const Problem &p, cudaStream_t st) {
+    Problem q = p;
+    q.tc_split = 1;
+    q.resident = 0;
+    cudaError_t err = launch_tc(q, st, 0);   // key-sum partials
+    return err == cudaSuccess ? launch_tc(q, st, 1) : err;   // [U_1^T ; M^T] cluster partials
+}
+
 cudaError_t launch_tc(const Problem &p, cudaStream_t st, int stage) {
     if (p.resident)
         return (stage < 0 || stage == 0) ? launch_tc_resident(p, st) : cudaErrorInvalidValue;
@@ -1364,7 +1372,7 @@ cudaError_t launch_tc(const Problem &p, cudaStream_t st, int stage) {
     t.n_mlp = mlp ? (p.hidden + 15) / 16 * 16 : 0;
     t.slot_cols = (t.epi_rows + t.n_mlp + 31) / 32 * 32;
     t.s_part = p.s_part; t.part = p.tc_part; t.bepi = p.tc_bepi; t.w1img = p.tc_w1img; t.err = p.err;
-    const bool fused = tc_fused(p.chunks, p.tc_cluster, p.chunk);
+    const bool fused = !p.tc_split && tc_fused(p.chunks, p.tc_cluster, p.chunk);
     // stage index of each kernel in this chain (-1: not part of it)
     const int s_keysum = fused ? -1 : 0, s_stats = fused ? 0 : 1, s_recur = fused ? -1 : 2,
               s_epi = fused ? 1 : 3;
