@@ -74,6 +74,37 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// 64 x 64 products in shared memory (row stride 64), register-blocked: thread
+// t of 256 owns rows a0 = 4 (t / 16) .. a0 + 3 and columns c0 = 4 (t % 16)
+// .. c0 + 3 of the result.  acc += A B, with A(a, e) = A[e][a] when kTransA.
+template <bool kTransA>
+__device__ __forceinline__ void mm64_acc(const float *A, const float *B, float (&acc)[4][4], int tid) {
+    const int a0 = 4 * (tid >> 4), c0 = 4 * (tid & 15);
+#pragma unroll 4
+    for (int e = 0; e < 64; ++e) {
+        float av[4];
+        if (kTransA) {
+            const float4 t = *reinterpret_cast<const float4 *>(A + e * 64 + a0);
+            av[0] = t.x; av[1] = t.y; av[2] = t.z; av[3] = t.w;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) av[i] = A[(a0 + i) * 64 + e];
+        }
+        const float4 bv = *reinterpret_cast<const float4 *>(B + e * 64 + c0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            acc[i][0] = fmaf(av[i], bv.x, acc[i][0]);
+            acc[i][1] = fmaf(av[i], bv.y, acc[i][1]);
+            acc[i][2] = fmaf(av[i], bv.z, acc[i][2]);
+            acc[i][3] = fmaf(av[i], bv.w, acc[i][3]);
+        }
+    }
+}
+// Row i of a thread's 4 x 4 block to/from shared or global memory (16-byte aligned rows).
+__device__ __forceinline__ void st_row4(float *dst, const float (&v)[4]) {
+    *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+}
+
 // ---------------------------------------------------------------------------
 // 1. reduce the statistics; U_1 .. U_(T-1) and Ubar = sum_k w_k U_k, or for
 // the untruncated walk Z = (I - beta M)^-1 U_1 (kept in U_1's place) and
@@ -158,11 +189,21 @@ __global__ void __launch_bounds__(kThreads) bwd_recur(BwdProblem b) {
             if (b.mlp) b.Ukn[(size_t)sl * b.nh * D * D + idx] = U[idx / D][idx % D];
         }
         for (int k = 2; k < p.T; ++k) {
-            for (int idx = tid; idx < D * D; idx += kThreads) {
-                const int a = idx / D, e = idx % D;
-                float acc = 0.f;
-                for (int c = 0; c < D; ++c) acc = fmaf(M[a][c], U[c][e], acc);
-                Un[a][e] = acc;
+            if constexpr (D == 64) {   // register-blocked product
+                float acc[4][4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+                mm64_acc<false>(&M[0][0], &U[0][0], acc, tid);
+                const int a0 = 4 * (tid >> 4), c0 = 4 * (tid & 15);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) st_row4(&Un[0][0] + (a0 + i) * D + c0, acc[i]);
+            } else {
+                for (int idx = tid; idx < D * D; idx += kThreads) {
+                    const int a = idx / D, e = idx % D;
+                    float acc = 0.f;
+                    for (int c = 0; c < D; ++c) acc = fmaf(M[a][c], U[c][e], acc);
+                    Un[a][e] = acc;
+                }
             }
             __syncthreads();
 #pragma unroll
@@ -666,6 +707,89 @@ __global__ void __launch_bounds__(kThreads) bwd_token_mlp(BwdProblem b) {
 // 4. reduce dUbar; the walk's backward recurrence (or the transposed solve)
 // gives dM and dU_1.
 // ---------------------------------------------------------------------------
+// ---------------------------------------------------------------------------
+// 4 (d = 64, truncated walk). The reverse recurrence of step 4 with every
+// 64 x 64 product register-blocked in shared memory (U_(k-1) staged, not
+// read from global memory in the inner loop).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) bwd_recur_back_64(BwdProblem b) {
+    constexpr int D = 64;
+    __shared__ __align__(16) float M[D * D];
+    __shared__ __align__(16) float G[D * D];
+    __shared__ __align__(16) float X[D * D];
+    const Problem &p = b.fwd;
+    const int sl = blockIdx.x, tid = threadIdx.x;
+    const int a0 = 4 * (tid >> 4), c0 = 4 * (tid & 15);
+    const size_t so = (size_t)sl * D * D;
+    // reduced dUbar at the thread's block (chunk order), M staged
+    float dub[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (!b.mlp)
+            for (int c = 0; c < p.chunks; ++c) {
+                const float4 v = *reinterpret_cast<const float4 *>(
+                    b.dub_part + ((size_t)sl * p.chunks + c) * D * D + (a0 + i) * D + c0);
+                acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+            }
+        dub[i][0] = acc.x; dub[i][1] = acc.y; dub[i][2] = acc.z; dub[i][3] = acc.w;
+    }
+    for (int x = tid; x < D * D / 4; x += kThreads)
+        reinterpret_cast<float4 *>(M)[x] = reinterpret_cast<const float4 *>(b.Mred + so)[x];
+    // the direct term of dL/dU_k on the thread's block: w_k dUbar, or with the
+    // adaptive weights sum_i w_ik Q~_i^T dg_i (its split-K partials, in chunk order)
+    auto level = [&](int k, float (&out)[4][4]) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) out[i][j] = b.mlp ? 0.f : p.w[k] * dub[i][j];
+        if (b.mlp)
+            for (int c = 0; c < p.chunks; ++c)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float4 v = *reinterpret_cast<const float4 *>(
+                        b.dukp + (((size_t)sl * p.chunks + c) * b.nh + (k - 1)) * D * D + (a0 + i) * D + c0);
+                    out[i][0] += v.x; out[i][1] += v.y; out[i][2] += v.z; out[i][3] += v.w;
+                }
+    };
+    const float *Uk = b.Uk + (size_t)sl * b.nh * D * D;   // transposed: Uk[e][c] = U_k[c][e]
+    float dm[4][4], g[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) dm[i][j] = g[i][j] = 0.f;
+    if (p.T > 1) {
+        level(p.T - 1, g);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) st_row4(G + (a0 + i) * D + c0, g[i]);
+        for (int k = p.T - 1; k >= 2; --k) {
+            // dM += G_k U_(k-1)^T: B(e, c) = U_(k-1)[c][e], staged from the transposed copy
+            const float4 *Up = reinterpret_cast<const float4 *>(Uk + (size_t)(k - 2) * D * D);
+            for (int x = tid; x < D * D / 4; x += kThreads) reinterpret_cast<float4 *>(X)[x] = Up[x];
+            __syncthreads();
+            mm64_acc<false>(G, X, dm, tid);
+            // G_(k-1) = (direct term of U_(k-1)) + M^T G_k
+            level(k - 1, g);
+            mm64_acc<true>(M, G, g, tid);
+            __syncthreads();   // every read of G and X done
+#pragma unroll
+            for (int i = 0; i < 4; ++i) st_row4(G + (a0 + i) * D + c0, g[i]);
+        }
+        __syncthreads();
+    }
+    // outputs: dM, dU_1 = G_1 and their transposes
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        st_row4(b.dM + so + (a0 + i) * D + c0, dm[i]);
+        st_row4(b.dU1 + so + (a0 + i) * D + c0, g[i]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            b.dMT[so + (c0 + j) * D + a0 + i] = dm[i][j];
+            b.dU1T[so + (c0 + j) * D + a0 + i] = g[i][j];
+        }
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads) bwd_recur_back(BwdProblem b) {
     constexpr int EPT = D * D / kThreads;
@@ -1699,6 +1823,26 @@ __global__ void __launch_bounds__(kThreads) bwd_finish_k(BwdProblem b) {
     const long long total = (long long)p.slices * p.n * D;
     const TIn *K = static_cast<const TIn *>(p.K);
     TIn *dKo = static_cast<TIn *>(b.dK);
+    if constexpr (std::is_same<TIn, __nv_bfloat16>::value) {
+        // four channels per thread and step: 16-byte dK loads, 8-byte K loads and stores
+        const long long total4 = total / 4;
+        for (long long x4 = (long long)blockIdx.x * kThreads + threadIdx.x; x4 < total4;
+             x4 += (long long)gridDim.x * kThreads) {
+            const long long x = 4 * x4;
+            const int ch = (int)(x % D);
+            const long long sl = x / ((long long)p.n * D);
+            const float4 dk = reinterpret_cast<const float4 *>(b.dk_part)[x4];
+            const float4 ds = *reinterpret_cast<const float4 *>(b.ds_red + sl * D + ch);
+            const uint2 kb = reinterpret_cast<const uint2 *>(K)[x4];
+            const float v[4] = {dk.x + ds.x, dk.y + ds.y, dk.z + ds.z, dk.w + ds.w};
+            const float kx[4] = {sm100::bf16_lo(kb.x), sm100::bf16_hi(kb.x), sm100::bf16_lo(kb.y), sm100::bf16_hi(kb.y)};
+            float o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[e] = feature_grad(v[e], kx[e], p.relu);
+            reinterpret_cast<uint2 *>(dKo)[x4] = make_uint2(sm100::pack_bf16(o[0], o[1]), sm100::pack_bf16(o[2], o[3]));
+        }
+        return;
+    }
     for (long long x = (long long)blockIdx.x * kThreads + threadIdx.x; x < total;
          x += (long long)gridDim.x * kThreads) {
         const int ch = (int)(x % D);
@@ -1745,7 +1889,10 @@ cudaError_t launch_bwd_all(const BwdProblem &b, cudaStream_t st) {
         else
             bwd_token_a<TIn, D><<<grid_tok, kThreads, 0, st>>>(b);
     }
-    bwd_recur_back<D><<<p.slices, kThreads, 0, st>>>(b);
+    if (D == 64 && !p.untruncated)
+        bwd_recur_back_64<<<p.slices, kThreads, 0, st>>>(b);
+    else
+        bwd_recur_back<D><<<p.slices, kThreads, 0, st>>>(b);
     // bf16 at d = 64 takes the tensor-core token pass, except with the ELU map
     // (its bf16 staging applies ReLU only)
     if (std::is_same<TIn, __nv_bfloat16>::value && D == 64 && p.relu != 2) {
