@@ -495,7 +495,7 @@ constexpr int kBwdTokensPerBlock = 32;   // per-token kernels: 8 warps x 4 token
 struct BwdPlan {
     Plan fwd;   // SIMT statistics partials (s, K^T V, K^T Q~) and s
     Plan tc;    // bf16, d = 64: the tensor-core split statistics' own region (tc.total == 0 otherwise)
-    size_t off_tc;
+    size_t off_tc, off_tcdub;
     int nh, nblk;
     size_t off_mred, off_uk, off_ubar, off_ubart, off_dub, off_lstat, off_dalp, off_dsp, off_dm, off_du1,
         off_dmt, off_du1t, off_dsr, off_dals, off_dkp, off_bimg, off_ubimg;
@@ -534,6 +534,8 @@ BwdPlan make_bwd_plan(int slices, int n, int D, int T, int hidden, int dtype) {
         b.tc = make_plan(slices, n, D, T, LISA_BF16, LISA_W_FIXED, 0);
         b.off_tc = off;
         off = align_up(off + b.tc.total);
+        b.off_tcdub = off;   // dUbar's cluster partials, laid out like tc_part
+        off = align_up(off + S * (size_t)(b.tc.chunks / b.tc.cluster) * 128 * 64 * sizeof(float));
     }
     if (hidden > 0) {
         const size_t Tz = (size_t)T, Hd = (size_t)hidden, nk = (size_t)b.nh;
@@ -646,6 +648,8 @@ lisa_status run_backward(const void *Q, const void *K, const void *V, const void
                      dtype, ws + pl.off_tc);
         b.tcfwd.err = b.fwd.err;
         b.tcfwd.wmode = LISA_W_FIXED;   // statistics only: the walk weights play no part
+        b.tcdub = f32(pl.off_tcdub);
+        b.tc_dub = (!mlp && !b.fwd.untruncated) ? 1 : 0;
     }
     if (mlp) {
         b.mlp = 1;

@@ -723,15 +723,25 @@ __global__ void __launch_bounds__(kThreads) bwd_recur_back_64(BwdProblem b) {
     const size_t so = (size_t)sl * D * D;
     // reduced dUbar at the thread's block (chunk order), M staged
     float dub[4][4];
+    const int parts = b.tc_dub ? b.tcfwd.chunks / b.tcfwd.tc_cluster : 0;
+    const float al = p.alpha[sl % p.heads];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (!b.mlp)
+        if (b.tc_dub) {   // alpha (Q~^T dO): rows 64 + a of the tensor-core partials, in part order
+            for (int q = 0; q < parts; ++q) {
+                const float4 v = *reinterpret_cast<const float4 *>(
+                    b.tcdub + ((size_t)sl * parts + q) * 2 * D * D + (D + a0 + i) * D + c0);
+                acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+            }
+            acc.x *= al; acc.y *= al; acc.z *= al; acc.w *= al;
+        } else if (!b.mlp) {
             for (int c = 0; c < p.chunks; ++c) {
                 const float4 v = *reinterpret_cast<const float4 *>(
                     b.dub_part + ((size_t)sl * p.chunks + c) * D * D + (a0 + i) * D + c0);
                 acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
             }
+        }
         dub[i][0] = acc.x; dub[i][1] = acc.y; dub[i][2] = acc.z; dub[i][3] = acc.w;
     }
     for (int x = tid; x < D * D / 4; x += kThreads)
@@ -1883,7 +1893,16 @@ cudaError_t launch_bwd_all(const BwdProblem &b, cudaStream_t st) {
         bwd_token_mlp<TIn, D><<<grid_tok, kThreads, 0, st>>>(b);
         if (p.T > 1) bwd_stats_duk<TIn, D><<<dim3(grid_stats, (unsigned)(p.T - 1)), kThreads, 0, st>>>(b);
     } else {
-        bwd_stats_dub<TIn, D><<<grid_stats, kThreads, 0, st>>>(b);
+        if (b.tc_dub) {   // dUbar / alpha = Q~^T dO: the statistics kernel with dO as its V and K
+            Problem q = b.tcfwd;
+            q.V = b.dO;
+            q.K = b.dO;
+            q.k_raw = 1;
+            q.tc_part = b.tcdub;
+            if ((err = launch_tc_stats_partials(q, st, false)) != cudaSuccess) return err;
+        } else {
+            bwd_stats_dub<TIn, D><<<grid_stats, kThreads, 0, st>>>(b);
+        }
         if (std::is_same<TIn, __nv_bfloat16>::value && D == 64 && p.relu != 2)
             bwd_token_a_tc<<<grid_tok, kThreads, 0, st>>>(b);
         else

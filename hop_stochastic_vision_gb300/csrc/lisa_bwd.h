@@ -17,6 +17,11 @@ struct BwdProblem {
     // tensor-core split chain (tcfwd's workspace views) instead of the SIMT one
     int tc_stats;
     Problem tcfwd;
+    // with tc_stats, fixed truncated walk: dUbar's partials from the same
+    // kernel (dO standing in for V and K): rows 64 + a of each part are
+    // (Q~^T dO)[a][.], [S][parts][128][64]
+    int tc_dub;
+    float *tcdub;
     const void *dO;
     void *dQ, *dK, *dV;
     float *dalpha;       // device [heads], overwritten

@@ -39,6 +39,7 @@ struct Problem {
     int family;          // kFamilySimt / kFamilyTc
     int resident;        // 1: the single-kernel tensor-core forward (test entry point only)
     int tc_split;        // 1: the tensor-core split chain even where the fused one fits
+    int k_raw;           // 1: the statistics' K operand takes no feature map (another tensor stands in for K)
 
     // workspace views
     int *err;        // error word (bounded device waits that gave up)
@@ -97,8 +98,9 @@ cudaError_t launch_tc(const Problem &p, cudaStream_t stream, int stage);
 // The tensor-core split chain's first two kernels only: the key-sum partials
 // (s_part, one per chunk) and the cluster-reduced [U_1^T ; M^T] partials
 // (tc_part, [slices][chunks / cluster][128][64] fp32), for a caller that
-// reduces them itself.
-cudaError_t launch_tc_stats_partials(const Problem &p, cudaStream_t stream);
+// reduces them itself.  Without the key sum, the statistics kernel alone
+// reuses the s_part an earlier call left.
+cudaError_t launch_tc_stats_partials(const Problem &p, cudaStream_t stream, bool with_keysum = true);
 // The single-kernel tensor-core forward (one thread-block cluster per slice,
 // K resident in shared memory): bf16, d = 64, weights shared by all tokens
 // (truncated or untruncated walk), ReLU or no feature map, grids with an even

@@ -62,6 +62,7 @@ constexpr int kFusedWork = 72 * 1024;          // fused stats: minimum work area
 
 struct TcParams {
     int slices, heads, H, W, n, T, relu, wmode, hidden;
+    int k_raw;                       // the K operand of the split statistics takes no feature map
     int untruncated;                 // U-bar = beta (1-beta) (I - beta M)^-1 U_1 instead of the series
     float eps, beta;
     const float *alpha;
@@ -579,7 +580,7 @@ __global__ void __launch_bounds__(kStatsThreads) tc_stats_split_kernel(const __g
             }
             if (!named_sync_and(ok)) break;
             uint8_t *Vb = sm + st * kStage;
-            if (p.relu) relu_smem(Vb + 2 * kSubBytes, kSubBytes, tid, 128);
+            if (p.relu && !p.k_raw) relu_smem(Vb + 2 * kSubBytes, kSubBytes, tid, 128);
             form_qtilde(Vb + kSubBytes, s_sh, p.eps, p.relu, tid);
             fence_proxy_async();
             named_sync_compute();
@@ -1344,12 +1345,12 @@ bool tc_fused(int chunks, int cluster, int chunk) {
     return chunks == cluster && (chunk + kSub - 1) / kSub <= kFusedMaxSub;
 }
 
-cudaError_t launch_tc_stats_partials(const Problem &p, cudaStream_t st) {
+cudaError_t launch_tc_stats_partials(const Problem &p, cudaStream_t st, bool with_keysum) {
     Problem q = p;
     q.tc_split = 1;
     q.resident = 0;
-    cudaError_t err = launch_tc(q, st, 0);   // key-sum partials
-    return err == cudaSuccess ? launch_tc(q, st, 1) : err;   // [U_1^T ; M^T] cluster partials
+    cudaError_t err = with_keysum ? launch_tc(q, st, 0) : cudaSuccess;   // key-sum partials
+    return err == cudaSuccess ? launch_tc(q, st, 1) : err;              // [U_1^T ; M^T] cluster partials
 }
 
 cudaError_t launch_tc(const Problem &p, cudaStream_t st, int stage) {
@@ -1358,6 +1359,7 @@ cudaError_t launch_tc(const Problem &p, cudaStream_t st, int stage) {
     TcParams t{};
     t.slices = p.slices; t.heads = p.heads; t.H = p.H; t.W = p.W; t.n = p.n; t.T = p.T;
     t.relu = p.relu; t.wmode = p.wmode; t.hidden = p.hidden; t.eps = p.eps; t.alpha = p.alpha;
+    t.k_raw = p.k_raw;
     t.untruncated = p.untruncated; t.beta = p.beta;
     for (int k = 0; k < LISA_MAX_T; ++k) t.w[k] = p.w[k];
     t.W1 = p.W1; t.b1 = p.b1; t.W2 = p.W2; t.b2 = p.b2; t.K = p.K;
