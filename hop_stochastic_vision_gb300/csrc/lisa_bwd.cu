@@ -125,11 +125,13 @@ __global__ void __launch_bounds__(kThreads) bwd_recur(BwdProblem b) {
         const int parts = t.chunks / t.tc_cluster;
         const float *tp = t.tc_part + (size_t)sl * parts * 2 * D * D;
         for (int idx = tid; idx < D * D; idx += kThreads) {
-            const int r = idx / D, a = idx % D;   // partial row r (U_1 column r, M column r), column a
+            // element (a, r) of U_1 and M: row r, column a of the partials (strided
+            // global reads, row-contiguous shared-memory writes)
+            const int a = idx / D, r = idx % D;
             float m = 0.f, u = 0.f;
             for (int q = 0; q < parts; ++q) {
-                u += tp[(size_t)q * 2 * D * D + idx];
-                m += tp[(size_t)q * 2 * D * D + D * D + idx];
+                u += tp[(size_t)q * 2 * D * D + r * D + a];
+                m += tp[(size_t)q * 2 * D * D + D * D + r * D + a];
             }
             U[a][r] = u;
             M[a][r] = m;
@@ -184,7 +186,7 @@ __global__ void __launch_bounds__(kThreads) bwd_recur(BwdProblem b) {
 #pragma unroll
         for (int x = 0; x < EPT; ++x) {
             const int idx = tid + x * kThreads;
-            Uk[idx] = U[idx % D][idx / D];
+            Uk[(idx % D) * D + idx / D] = U[idx / D][idx % D];
             ub[x] = p.T > 1 ? p.w[1] * U[idx / D][idx % D] : 0.f;
             if (b.mlp) b.Ukn[(size_t)sl * b.nh * D * D + idx] = U[idx / D][idx % D];
         }
@@ -215,7 +217,7 @@ __global__ void __launch_bounds__(kThreads) bwd_recur(BwdProblem b) {
             }
             __syncthreads();
             for (int idx = tid; idx < D * D; idx += kThreads) {
-                Uk[(size_t)(k - 1) * D * D + idx] = U[idx % D][idx / D];
+                Uk[(size_t)(k - 1) * D * D + (idx % D) * D + idx / D] = U[idx / D][idx % D];
                 if (b.mlp) b.Ukn[((size_t)sl * b.nh + (k - 1)) * D * D + idx] = U[idx / D][idx % D];
             }
         }
