@@ -19,8 +19,11 @@
 //   exactly when j in N(i), so each token gathers its own terms)
 //   feature map: dXq = dQ [Xq > 0], dXk = dK [Xk > 0].
 //
-// Launch chain (after the forward's two SIMT statistics kernels, which leave
-// the split-K partials of s, U_1 = K^T V and M = K^T Q~):
+// Launch chain (after the statistics: the forward's two SIMT kernels, or for
+// bf16 at d = 64 without the ELU map the tensor-core split kernels, which
+// leave the split-K partials of s, U_1 = K^T V and M = K^T Q~; there a second
+// split-statistics launch with dO as its V and K gives dUbar's partials in
+// place of step 2, and steps 3 and 5 take a quarter-warp per token):
 //   1. bwd_recur      per slice: reduce s, U_1, M; U_k, Ubar (or the solve)
 //   2. bwd_stats_dub  per (slice, chunk): partial dUbar = Q~^T (alpha dO)
 //   3. bwd_token_a    warp per token: window softmax max / sum, dl_i . l_i,
