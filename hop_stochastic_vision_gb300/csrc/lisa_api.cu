@@ -494,6 +494,7 @@ constexpr int kBwdTokensPerBlock = 32;   // per-token kernels: 8 warps x 4 token
 
 struct BwdPlan {
     Plan fwd;   // SIMT statistics partials (s, K^T V, K^T Q~) and s
+    int ntile;  // 8 x 8 tiles per slice (the tiled token pass)
     Plan tc;    // bf16, d = 64: the tensor-core split statistics' own region (tc.total == 0 otherwise)
     size_t off_tc, off_tcdub;
     int nh, nblk;
@@ -506,11 +507,14 @@ struct BwdPlan {
 
 // The backward always runs the SIMT statistics kernels; its own buffers
 // follow the forward plan's.  hidden > 0: the adaptive weights' buffers too.
-BwdPlan make_bwd_plan(int slices, int n, int D, int T, int hidden, int dtype) {
+BwdPlan make_bwd_plan(int slices, int H, int W, int D, int T, int hidden, int dtype) {
+    const int n = H * W;
     BwdPlan b{};
     b.fwd = make_plan(slices, n, D, T, LISA_F32, LISA_W_FIXED, 0);   // SIMT family, any dtype
     b.nh = T > 1 ? T - 1 : 1;
     b.nblk = (n + kBwdTokensPerBlock - 1) / kBwdTokensPerBlock;
+    b.ntile = ((H + 7) / 8) * ((W + 7) / 8);
+    const size_t nparts = (size_t)(b.nblk > b.ntile ? b.nblk : b.ntile);   // ds partials of either token pass
     const size_t S = (size_t)slices, C = (size_t)b.fwd.chunks, d = (size_t)D, dd = d * d, N = (size_t)n;
     size_t off = b.fwd.total;
     b.off_mred = off;  off = align_up(off + S * dd * sizeof(float));
@@ -520,7 +524,7 @@ BwdPlan make_bwd_plan(int slices, int n, int D, int T, int hidden, int dtype) {
     b.off_dub = off;   off = align_up(off + S * C * dd * sizeof(float));
     b.off_lstat = off; off = align_up(off + S * N * 4 * sizeof(float));
     b.off_dalp = off;  off = align_up(off + S * b.nblk * sizeof(float));
-    b.off_dsp = off;   off = align_up(off + S * b.nblk * d * sizeof(float));
+    b.off_dsp = off;   off = align_up(off + S * nparts * d * sizeof(float));
     b.off_dm = off;    off = align_up(off + S * dd * sizeof(float));
     b.off_du1 = off;   off = align_up(off + S * dd * sizeof(float));
     b.off_dmt = off;   off = align_up(off + S * dd * sizeof(float));
@@ -606,7 +610,7 @@ lisa_status run_backward(const void *Q, const void *K, const void *V, const void
     if (overlaps(dalpha, (size_t)heads * sizeof(float), alpha, (size_t)heads * sizeof(float)))
         return LISA_ERR_INVALID_ARG;
 
-    const BwdPlan pl = make_bwd_plan((int)slices, (int)n, d_h, b.fwd.T, mlp ? b.fwd.hidden : 0, dtype);
+    const BwdPlan pl = make_bwd_plan((int)slices, H, W, d_h, b.fwd.T, mlp ? b.fwd.hidden : 0, dtype);
     if (!workspace || workspace_bytes < pl.total) return LISA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return LISA_ERR_INVALID_ARG;
     fill_problem(b.fwd, pl.fwd, Q, K, V, nullptr, (int)slices, heads, H, W, d_h, relu_inputs, eps, alpha, dtype,
@@ -650,6 +654,7 @@ lisa_status run_backward(const void *Q, const void *K, const void *V, const void
         b.tcfwd.wmode = LISA_W_FIXED;   // statistics only: the walk weights play no part
         b.tcdub = f32(pl.off_tcdub);
         b.tc_dub = (!mlp && !b.fwd.untruncated) ? 1 : 0;
+        if (!mlp) b.ntile = pl.ntile;   // the tiled token pass
     }
     if (mlp) {
         b.mlp = 1;
@@ -679,7 +684,7 @@ extern "C" size_t lisa_backward_workspace_bytes(int B, int heads, int H, int W, 
     if (check_sizes(B, heads, H, W, d_h, d_v, T, dtype) != LISA_OK) return 0;
     const long long slices = (long long)B * heads, n = (long long)H * W;
     if (slices == 0 || n == 0) return 0;
-    return make_bwd_plan((int)slices, (int)n, d_h, effective_T(T), 0, dtype).total;
+    return make_bwd_plan((int)slices, H, W, d_h, effective_T(T), 0, dtype).total;
 }
 
 extern "C" lisa_status lisa_backward(const void *Q, const void *K, const void *V, const void *dO, void *dQ,
@@ -702,7 +707,7 @@ extern "C" size_t lisa_backward_mlp_workspace_bytes(int B, int heads, int H, int
     if (T < 1 || T > LISA_MAX_T_MLP || hidden < 1 || hidden > LISA_MAX_HIDDEN) return 0;
     const long long slices = (long long)B * heads, n = (long long)H * W;
     if (slices == 0 || n == 0) return 0;
-    return make_bwd_plan((int)slices, (int)n, d_h, T, hidden, dtype).total;
+    return make_bwd_plan((int)slices, H, W, d_h, T, hidden, dtype).total;
 }
 
 extern "C" lisa_status lisa_backward_mlp(const void *Q, const void *K, const void *V, const void *dO, void *dQ,

@@ -26,6 +26,7 @@ struct BwdProblem {
     void *dQ, *dK, *dV;
     float *dalpha;       // device [heads], overwritten
     int tpb, nblk;       // tokens per block of the per-token kernels; blocks per slice
+    int ntile;           // 8 x 8 tiles per slice of the tiled token pass (0: 32-token blocks throughout)
     int nh;              // stored U_k matrices: max(T - 1, 1)
     float *Mred;         // [S][D][D]      M = K^T Q~
     float *Uk;           // [S][nh][D][D]  U_1 .. U_(T-1) (untruncated: Z), transposed
