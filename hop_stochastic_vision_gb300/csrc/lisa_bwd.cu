@@ -1384,20 +1384,21 @@ __global__ void __launch_bounds__(kThreads) bwd_token_a_tc(BwdProblem b) {
 }
 
 // ---------------------------------------------------------------------------
-// 5''. bf16, d = 64, fixed weights: the token pass on 8 x 8 token tiles.  The
-// tile's halo (10 x 10 grid positions) of K, V, Q (feature-mapped) and dO,
-// and the halo tokens' window statistics, go to shared memory once.  The
-// three d x d products gather their A rows from the halo (ldmatrix takes a
-// row address per lane); the quarter-warp phase reads every neighbour row
-// from it.  16 warps, one CTA per SM.
+// 5''. bf16, d = 64, fixed weights: the token pass on 8 x 8 token tiles.  A
+// persistent CTA of 16 warps walks a contiguous run of tiles.  Each tile's
+// halo (10 x 10 grid positions) of K, V, Q (feature-mapped) and dO, and the
+// halo tokens' window statistics, arrive in shared memory by cp.async while
+// the previous tile computes (two halo buffers); the three d x d products
+// gather their A rows from the halo (ldmatrix takes a row address per lane);
+// the quarter-warp phase reads every neighbour row from it.
 // ---------------------------------------------------------------------------
 constexpr int kHaloSide = 10;                 // an 8 x 8 tile and its one-token border
 constexpr int kHaloRows = kHaloSide * kHaloSide;
 constexpr int kTileTok = 64;
 constexpr int kTileWarps = 16;
 constexpr int kTileThreads = 32 * kTileWarps;
-constexpr int kTileSmemBytes = kImgRows * kBS * 2 + 4 * kHaloRows * kQS * 2 + kTileTok * kQS * 2 +
-                               3 * kTileTok * 64 * 4 + kHaloRows * 16;
+constexpr int kHaloBytes = 4 * kHaloRows * kQS * 2 + kHaloRows * 16;   // K, V, Q, dO rows; statistics
+constexpr int kTileSmemBytes = kImgRows * kBS * 2 + 2 * kHaloBytes + kTileTok * kQS * 2 + 3 * kTileTok * 64 * 4;
 
 // Halo row of the grid position (dy, dx) away from the tile's token u.
 __device__ __forceinline__ int halo_row(int u, int dy, int dx) {
@@ -1413,237 +1414,273 @@ __device__ __forceinline__ void lds8_bf16(const __nv_bfloat16 *row, float (&x)[8
         x[2 * k + 1] = sm100::bf16_hi(u[k]);
     }
 }
+// 16-byte asynchronous copy global -> shared; zero-filled when !valid (src
+// is then not read).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 __global__ void __launch_bounds__(kTileThreads, 1) bwd_token_b_tile(BwdProblem b) {
     constexpr int D = 64;
     using namespace sm100;
     extern __shared__ float4 smem_tile[];
     __nv_bfloat16 *Bs = reinterpret_cast<__nv_bfloat16 *>(smem_tile);
-    __nv_bfloat16 *Kh = Bs + kImgRows * kBS;   // halo rows (stride kQS): K, V, Q, dO
-    __nv_bfloat16 *Vh = Kh + kHaloRows * kQS;
-    __nv_bfloat16 *Qh = Vh + kHaloRows * kQS;
-    __nv_bfloat16 *Gh = Qh + kHaloRows * kQS;
-    __nv_bfloat16 *Qt = Gh + kHaloRows * kQS;  // Q~ of the tile's tokens
+    uint8_t *halo0 = reinterpret_cast<uint8_t *>(Bs + kImgRows * kBS);   // two halo buffers
+    __nv_bfloat16 *Qt = reinterpret_cast<__nv_bfloat16 *>(halo0 + 2 * kHaloBytes);   // Q~ of the tile's tokens
     float *oQ = reinterpret_cast<float *>(Qt + kTileTok * kQS), *oV = oQ + kTileTok * D, *oK = oV + kTileTok * D;
-    float4 *lsh = reinterpret_cast<float4 *>(oK + kTileTok * D);   // halo tokens' window statistics
     __shared__ float rqs[kTileTok];
     __shared__ float dsw[kTileWarps][D];
     const Problem &p = b.fwd;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int sl = blockIdx.x / b.ntile, tile = blockIdx.x % b.ntile;
     const int tiles_c = (p.W + 7) / 8;
-    const int r0 = (tile / tiles_c) * 8, c0 = (tile % tiles_c) * 8;
-    const size_t sbase = (size_t)sl * p.n * D;
-    const __nv_bfloat16 *Q = static_cast<const __nv_bfloat16 *>(p.Q) + sbase;
-    const __nv_bfloat16 *K = static_cast<const __nv_bfloat16 *>(p.K) + sbase;
-    const __nv_bfloat16 *V = static_cast<const __nv_bfloat16 *>(p.V) + sbase;
-    const __nv_bfloat16 *dO = static_cast<const __nv_bfloat16 *>(b.dO) + sbase;
-    __nv_bfloat16 *dQo = static_cast<__nv_bfloat16 *>(b.dQ) + sbase;
-    __nv_bfloat16 *dVo = static_cast<__nv_bfloat16 *>(b.dV) + sbase;
-    float *dKp = b.dk_part + sbase;
-    const float4 *lst = reinterpret_cast<const float4 *>(b.lstat) + (size_t)sl * p.n;
-    const float *s = p.s_red + (size_t)sl * D;
-    const float al = p.alpha[sl % p.heads], w0 = p.w[0];
+    const long long ntiles = (long long)p.slices * b.ntile;
+    const int t_begin = (int)(blockIdx.x * ntiles / gridDim.x), t_end = (int)((blockIdx.x + 1) * ntiles / gridDim.x);
     const float scale = 0.125f;   // 1 / sqrt(64)
-
-    // ---- stage the B image, the halo rows and the halo's window statistics
-    {
-        const uint4 *img = reinterpret_cast<const uint4 *>(b.bimg + (size_t)sl * kImgRows * D);
-        for (int x = tid; x < kImgRows * 8; x += kTileThreads)
-            *reinterpret_cast<uint4 *>(Bs + (x >> 3) * kBS + (x & 7) * 8) = img[x];
-    }
-    for (int x = tid; x < 4 * kHaloRows * 8; x += kTileThreads) {
-        const int t = x / (kHaloRows * 8), h = (x >> 3) % kHaloRows, c = x & 7;
-        const int gr = r0 - 1 + h / kHaloSide, gc = c0 - 1 + h % kHaloSide;
-        const __nv_bfloat16 *src = t == 0 ? K : (t == 1 ? V : (t == 2 ? Q : dO));
-        __nv_bfloat16 *dst = t == 0 ? Kh : (t == 1 ? Vh : (t == 2 ? Qh : Gh));
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (gr >= 0 && gr < p.H && gc >= 0 && gc < p.W) {
-            v = reinterpret_cast<const uint4 *>(src)[((size_t)(gr * p.W + gc) * D) / 8 + c];
-            if (p.relu && (t == 0 || t == 2))
-                v = make_uint4(relu_bf16x2(v.x), relu_bf16x2(v.y), relu_bf16x2(v.z), relu_bf16x2(v.w));
-        }
-        *reinterpret_cast<uint4 *>(dst + h * kQS + c * 8) = v;
-    }
-    for (int h = tid; h < kHaloRows; h += kTileThreads) {
-        const int gr = r0 - 1 + h / kHaloSide, gc = c0 - 1 + h % kHaloSide;
-        lsh[h] = (gr >= 0 && gr < p.H && gc >= 0 && gc < p.W) ? lst[gr * p.W + gc] : make_float4(0.f, 1.f, 0.f, 0.f);
-    }
-    __syncthreads();
     const int qg = lane >> 3, c8 = 8 * (lane & 7);
-    const int u = 4 * warp + qg;   // this quarter's token of the tile
-    {   // 1 / (Q_u . s + eps) and Q~_u (bf16) for the second product
-        float q[8], sv[8];
-        lds8_bf16(Qh + halo_row(u, 0, 0) * kQS + c8, q);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) sv[e] = s[c8 + e];
-        const float rq = 1.f / (group8_sum(dot8(q, sv)) + p.eps);
-        if ((lane & 7) == 0) rqs[u] = rq;
-        *reinterpret_cast<uint4 *>(Qt + u * kQS + c8) =
-            make_uint4(pack_bf16(q[0] * rq, q[1] * rq), pack_bf16(q[2] * rq, q[3] * rq),
-                       pack_bf16(q[4] * rq, q[5] * rq), pack_bf16(q[6] * rq, q[7] * rq));
-    }
-    __syncthreads();
+    const int u = 4 * warp + qg;   // this quarter's token of a tile
 
-    // ---- the three products: warp = 16 tokens (mt) x 16 columns (sb) of each
-    //   dQ~ = [dO | K] [alpha Ubar^T ; dM],  dK = [V | Q~] [dU_1^T ; dM^T],  dV = K dU_1
-    {
-        const int mt = warp & 3, sb = warp >> 2;
-        const int ua = 16 * mt + (lane & 15), acol = (lane >> 4) * 8;
-        const uint32_t hrow = (uint32_t)halo_row(ua, 0, 0) * kQS, trow = (uint32_t)ua * kQS;
-        const uint32_t bs = smem_u32(Bs);
-        const int mi = lane >> 3, brow = (mi & 1) * 8 + (lane & 7), bcol = 16 * sb + (mi >> 1) * 8;
-#pragma unroll
-        for (int pr = 0; pr < 3; ++pr) {
-            const int brow0 = pr == 0 ? 0 : (pr == 1 ? 128 : 256);
-            const int ksteps = pr == 2 ? 4 : 8;
-            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                if (ks >= ksteps) break;
-                // A operand of this k-step: which halo (or Q~) row, which 16 channels
-                const __nv_bfloat16 *abuf = pr == 0 ? (ks < 4 ? Gh : Kh) : (pr == 1 ? (ks < 4 ? Vh : Qt) : Kh);
-                const uint32_t arow = (pr == 1 && ks >= 4) ? trow : hrow;
-                uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-                ldsm_x4(smem_u32(abuf) + (arow + 16 * (ks & 3) + acol) * 2u, a0, a1, a2, a3);
-                ldsm_x4_t(bs + (uint32_t)((brow0 + 16 * ks + brow) * kBS + bcol) * 2u, b0, b1, b2, b3);
-                mma_bf16_16816(acc[0], a0, a1, a2, a3, b0, b1);
-                mma_bf16_16816(acc[1], a0, a1, a2, a3, b2, b3);
-            }
-            float *out = pr == 0 ? oQ : (pr == 1 ? oK : oV);
-            const int row = 16 * mt + (lane >> 2);
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int col = 16 * sb + 8 * nt + 2 * (lane & 3);
-                out[row * D + col] = acc[nt][0];
-                out[row * D + col + 1] = acc[nt][1];
-                out[(row + 8) * D + col] = acc[nt][2];
-                out[(row + 8) * D + col + 1] = acc[nt][3];
-            }
+    // K, V, Q, dO rows and statistics of tile t's halo into buffer `buf`, asynchronously
+    auto stage_halo = [&](int t, int buf) {
+        const int sl = t / b.ntile, tile = t % b.ntile;
+        const int r0 = (tile / tiles_c) * 8, c0 = (tile % tiles_c) * 8;
+        const size_t sbase = (size_t)sl * p.n * D;
+        const uint32_t hb = smem_u32(halo0 + buf * kHaloBytes);
+        for (int x = tid; x < 4 * kHaloRows * 8; x += kTileThreads) {
+            const int tn = x / (kHaloRows * 8), h = (x >> 3) % kHaloRows, c = x & 7;
+            const int gr = r0 - 1 + h / kHaloSide, gc = c0 - 1 + h % kHaloSide;
+            const bool in = gr >= 0 && gr < p.H && gc >= 0 && gc < p.W;
+            const void *src = tn == 0 ? p.K : (tn == 1 ? p.V : (tn == 2 ? p.Q : b.dO));
+            const __nv_bfloat16 *row = static_cast<const __nv_bfloat16 *>(src) + sbase +
+                                       (size_t)(in ? gr * p.W + gc : 0) * D + c * 8;
+            cp_async16(hb + (uint32_t)((tn * kHaloRows + h) * kQS + c * 8) * 2u, row, in);
         }
-    }
-    __syncthreads();
+        const float4 *lst = reinterpret_cast<const float4 *>(b.lstat) + (size_t)sl * p.n;
+        for (int h = tid; h < kHaloRows; h += kTileThreads) {
+            const int gr = r0 - 1 + h / kHaloSide, gc = c0 - 1 + h % kHaloSide;
+            const bool in = gr >= 0 && gr < p.H && gc >= 0 && gc < p.W;
+            cp_async16(hb + (uint32_t)(4 * kHaloRows * kQS * 2 + h * 16), lst + (in ? gr * p.W + gc : 0), in);
+        }
+        cp_async_commit();
+    };
 
-    // ---- a quarter-warp per token: normaliser, window, stores
-    const int y = u / 8, xx = u % 8, r = r0 + y, c = c0 + xx;
-    const bool live = r < p.H && c < p.W;
-    const int j = r * p.W + c;
-    const int hc = halo_row(u, 0, 0);
-    float q[8], go[8], k[8], v[8], dqt[8], dv[8], dk[8];
-    lds8_bf16(Qh + hc * kQS + c8, q);
-    lds8_bf16(Gh + hc * kQS + c8, go);
-    lds8_bf16(Kh + hc * kQS + c8, k);
-    lds8_bf16(Vh + hc * kQS + c8, v);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        dqt[e] = oQ[u * D + c8 + e];
-        dv[e] = fmaf(w0 * al, go[e], oV[u * D + c8 + e]);
-        dk[e] = oK[u * D + c8 + e];
-    }
-    const float rq = rqs[u];
-    const float cj = group8_sum(dot8(dqt, q)) * rq * rq;
-    float dq[8], dsl[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        dq[e] = dqt[e] * rq - cj * s[c8 + e];
-        dsl[e] = live ? -cj * q[e] : 0.f;
-    }
-    const float4 sj = lsh[hc];
-    const float izj = 1.f / sj.y;
-    // the window three neighbours (one halo row band) at a time, to keep the
-    // dot products in few registers
-#pragma unroll 1
-    for (int dyi = 0; dyi < 3; ++dyi) {
-        const int dy = dyi - 1, rr = r + dy;
-        const bool row_in = rr >= 0 && rr < p.H;
-        {   // u as the query: scores against its window, dl_u . V_i
-            float d1[6];
-#pragma unroll
-            for (int t3 = 0; t3 < 3; ++t3) {
-                const int hr = halo_row(u, dy, t3 - 1);
-                float kr[8], vr[8];
-                lds8_bf16(Kh + hr * kQS + c8, kr);
-                lds8_bf16(Vh + hr * kQS + c8, vr);
-                d1[t3] = dot8(q, kr);
-                d1[3 + t3] = dot8(go, vr);
-            }
-#pragma unroll
-            for (int t = 0; t < 6; ++t) d1[t] = group8_sum(d1[t]);
-#pragma unroll
-            for (int t3 = 0; t3 < 3; ++t3) {
-                const int cc = c + t3 - 1;
-                if (!row_in || cc < 0 || cc >= p.W) continue;
-                const float a = expf(d1[t3] * scale - sj.x) * izj;
-                const float de = a * (d1[3 + t3] * (1.f - al) - sj.z) * scale;
-                float kr[8];
-                lds8_bf16(Kh + halo_row(u, dy, t3 - 1) * kQS + c8, kr);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) dq[e] = fmaf(de, kr[e], dq[e]);
-            }
+    int img_sl = -1;
+    if (t_begin < t_end) stage_halo(t_begin, 0);
+    for (int t = t_begin, it = 0; t < t_end; ++t, ++it) {
+        const int cur = it & 1;
+        // the next tile's halo streams in while this one computes; its buffer
+        // was last read by the tile before this one, which ended on a barrier
+        if (t + 1 < t_end) {
+            stage_halo(t + 1, cur ^ 1);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
         }
-        {   // u as a key of each neighbour i's window (the window is symmetric)
-            float d2[6];
-#pragma unroll
-            for (int t3 = 0; t3 < 3; ++t3) {
-                const int hr = halo_row(u, dy, t3 - 1);
-                float qi[8], gi[8];
-                lds8_bf16(Qh + hr * kQS + c8, qi);
-                lds8_bf16(Gh + hr * kQS + c8, gi);
-                d2[t3] = dot8(qi, k);
-                d2[3 + t3] = dot8(gi, v);
+        const int sl = t / b.ntile, tile = t % b.ntile;
+        const int r0 = (tile / tiles_c) * 8, c0 = (tile % tiles_c) * 8;
+        if (sl != img_sl) {   // the slice's B image (tiles of one slice are consecutive)
+            const uint4 *img = reinterpret_cast<const uint4 *>(b.bimg + (size_t)sl * kImgRows * D);
+            for (int x = tid; x < kImgRows * 8; x += kTileThreads)
+                *reinterpret_cast<uint4 *>(Bs + (x >> 3) * kBS + (x & 7) * 8) = img[x];
+            img_sl = sl;
+        }
+        __syncthreads();   // this tile's halo (every thread's copies) and the B image are in place
+        __nv_bfloat16 *Kc = reinterpret_cast<__nv_bfloat16 *>(halo0 + cur * kHaloBytes);
+        __nv_bfloat16 *Vc = Kc + kHaloRows * kQS, *Qc = Vc + kHaloRows * kQS, *Gc = Qc + kHaloRows * kQS;
+        const float4 *Lc = reinterpret_cast<const float4 *>(Gc + kHaloRows * kQS);
+        if (p.relu) {   // the feature map of K and Q, in place
+            for (int x = tid; x < 2 * kHaloRows * 8; x += kTileThreads) {
+                __nv_bfloat16 *base = x < kHaloRows * 8 ? Kc : Qc;
+                const int y = x % (kHaloRows * 8);
+                uint4 *pv = reinterpret_cast<uint4 *>(base + (y >> 3) * kQS + (y & 7) * 8);
+                const uint4 v = *pv;
+                *pv = make_uint4(relu_bf16x2(v.x), relu_bf16x2(v.y), relu_bf16x2(v.z), relu_bf16x2(v.w));
             }
+            __syncthreads();
+        }
+        const size_t sbase = (size_t)sl * p.n * D;
+        __nv_bfloat16 *dQo = static_cast<__nv_bfloat16 *>(b.dQ) + sbase;
+        __nv_bfloat16 *dVo = static_cast<__nv_bfloat16 *>(b.dV) + sbase;
+        float *dKp = b.dk_part + sbase;
+        const float *s = p.s_red + (size_t)sl * D;
+        const float al = p.alpha[sl % p.heads], w0 = p.w[0];
+        {   // 1 / (Q_u . s + eps) and Q~_u (bf16) for the second product
+            float q[8], sv[8];
+            lds8_bf16(Qc + halo_row(u, 0, 0) * kQS + c8, q);
 #pragma unroll
-            for (int t = 0; t < 6; ++t) d2[t] = group8_sum(d2[t]);
+            for (int e = 0; e < 8; ++e) sv[e] = s[c8 + e];
+            const float rq = 1.f / (group8_sum(dot8(q, sv)) + p.eps);
+            if ((lane & 7) == 0) rqs[u] = rq;
+            *reinterpret_cast<uint4 *>(Qt + u * kQS + c8) =
+                make_uint4(pack_bf16(q[0] * rq, q[1] * rq), pack_bf16(q[2] * rq, q[3] * rq),
+                           pack_bf16(q[4] * rq, q[5] * rq), pack_bf16(q[6] * rq, q[7] * rq));
+        }
+        __syncthreads();
+
+        // ---- the three products: warp = 16 tokens (mt) x 16 columns (sb) of each
+        //   dQ~ = [dO | K] [alpha Ubar^T ; dM],  dK = [V | Q~] [dU_1^T ; dM^T],  dV = K dU_1
+        {
+            const int mt = warp & 3, sb = warp >> 2;
+            const int ua = 16 * mt + (lane & 15), acol = (lane >> 4) * 8;
+            const uint32_t hrow = (uint32_t)halo_row(ua, 0, 0) * kQS, trow = (uint32_t)ua * kQS;
+            const uint32_t bs = smem_u32(Bs);
+            const int mi = lane >> 3, brow = (mi & 1) * 8 + (lane & 7), bcol = 16 * sb + (mi >> 1) * 8;
 #pragma unroll
-            for (int t3 = 0; t3 < 3; ++t3) {
-                const int cc = c + t3 - 1;
-                if (!row_in || cc < 0 || cc >= p.W) continue;
-                const int hr = halo_row(u, dy, t3 - 1);
-                const float4 si = lsh[hr];
-                const float a = expf(d2[t3] * scale - si.x) / si.y;
-                const float de = a * (d2[3 + t3] * (1.f - al) - si.z) * scale;
-                float qi[8], gi[8];
-                lds8_bf16(Qh + hr * kQS + c8, qi);
-                lds8_bf16(Gh + hr * kQS + c8, gi);
+            for (int pr = 0; pr < 3; ++pr) {
+                const int brow0 = pr == 0 ? 0 : (pr == 1 ? 128 : 256);
+                const int ksteps = pr == 2 ? 4 : 8;
+                float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    dv[e] = fmaf(a * (1.f - al), gi[e], dv[e]);
-                    dk[e] = fmaf(de, qi[e], dk[e]);
+                for (int ks = 0; ks < 8; ++ks) {
+                    if (ks >= ksteps) break;
+                    // A operand of this k-step: which halo (or Q~) row, which 16 channels
+                    const __nv_bfloat16 *abuf = pr == 0 ? (ks < 4 ? Gc : Kc) : (pr == 1 ? (ks < 4 ? Vc : Qt) : Kc);
+                    const uint32_t arow = (pr == 1 && ks >= 4) ? trow : hrow;
+                    uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+                    ldsm_x4(smem_u32(abuf) + (arow + 16 * (ks & 3) + acol) * 2u, a0, a1, a2, a3);
+                    ldsm_x4_t(bs + (uint32_t)((brow0 + 16 * ks + brow) * kBS + bcol) * 2u, b0, b1, b2, b3);
+                    mma_bf16_16816(acc[0], a0, a1, a2, a3, b0, b1);
+                    mma_bf16_16816(acc[1], a0, a1, a2, a3, b2, b3);
+                }
+                float *out = pr == 0 ? oQ : (pr == 1 ? oK : oV);
+                const int row = 16 * mt + (lane >> 2);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int col = 16 * sb + 8 * nt + 2 * (lane & 3);
+                    out[row * D + col] = acc[nt][0];
+                    out[row * D + col + 1] = acc[nt][1];
+                    out[(row + 8) * D + col] = acc[nt][2];
+                    out[(row + 8) * D + col + 1] = acc[nt][3];
                 }
             }
         }
-    }
-    if (live) {
-        // dXq through the feature map: the staged Q is ReLU'd, and ReLU(x) > 0 exactly when x > 0
-        uint4 oq, ov;
-        uint32_t *pq = &oq.x, *pv = &ov.x;
+        __syncthreads();
+
+        // ---- a quarter-warp per token: normaliser, window, stores
+        const int y = u / 8, xx = u % 8, r = r0 + y, c = c0 + xx;
+        const bool live = r < p.H && c < p.W;
+        const int j = r * p.W + c;
+        const int hc = halo_row(u, 0, 0);
+        float q[8], go[8], k[8], v[8], dqt[8], dv[8], dk[8];
+        lds8_bf16(Qc + hc * kQS + c8, q);
+        lds8_bf16(Gc + hc * kQS + c8, go);
+        lds8_bf16(Kc + hc * kQS + c8, k);
+        lds8_bf16(Vc + hc * kQS + c8, v);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float q0 = (p.relu && !(q[2 * e] > 0.f)) ? 0.f : dq[2 * e];
-            const float q1 = (p.relu && !(q[2 * e + 1] > 0.f)) ? 0.f : dq[2 * e + 1];
-            pq[e] = pack_bf16(q0, q1);
-            pv[e] = pack_bf16(dv[2 * e], dv[2 * e + 1]);
+        for (int e = 0; e < 8; ++e) {
+            dqt[e] = oQ[u * D + c8 + e];
+            dv[e] = fmaf(w0 * al, go[e], oV[u * D + c8 + e]);
+            dk[e] = oK[u * D + c8 + e];
         }
-        *reinterpret_cast<uint4 *>(dQo + (size_t)j * D + c8) = oq;
-        *reinterpret_cast<uint4 *>(dVo + (size_t)j * D + c8) = ov;
-        float4 *kp = reinterpret_cast<float4 *>(dKp + (size_t)j * D + c8);
-        kp[0] = make_float4(dk[0], dk[1], dk[2], dk[3]);
-        kp[1] = make_float4(dk[4], dk[5], dk[6], dk[7]);
-    }
-    // the warp's four tokens' ds terms, summed over the quarters in a fixed order
+        const float rq = rqs[u];
+        const float cj = group8_sum(dot8(dqt, q)) * rq * rq;
+        float dq[8], dsl[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        dsl[e] += __shfl_xor_sync(0xffffffffu, dsl[e], 8);
-        dsl[e] += __shfl_xor_sync(0xffffffffu, dsl[e], 16);
-    }
-    if (qg == 0)
+        for (int e = 0; e < 8; ++e) {
+            dq[e] = dqt[e] * rq - cj * s[c8 + e];
+            dsl[e] = live ? -cj * q[e] : 0.f;
+        }
+        const float4 sj = live ? Lc[hc] : make_float4(0.f, 1.f, 0.f, 0.f);
+        const float izj = 1.f / sj.y;
+        // the window three neighbours (one halo row band) at a time, to keep the
+        // dot products in few registers
+#pragma unroll 1
+        for (int dyi = 0; dyi < 3; ++dyi) {
+            const int dy = dyi - 1, rr = r + dy;
+            const bool row_in = rr >= 0 && rr < p.H;
+            {   // u as the query: scores against its window, dl_u . V_i
+                float d1[6];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) dsw[warp][c8 + e] = dsl[e];
-    __syncthreads();
-    for (int ch = tid; ch < D; ch += kTileThreads) {
-        float acc = 0.f;
-        for (int w = 0; w < kTileWarps; ++w) acc += dsw[w][ch];
-        b.ds_part[((size_t)sl * b.ntile + tile) * D + ch] = acc;
+                for (int t3 = 0; t3 < 3; ++t3) {
+                    const int hr = halo_row(u, dy, t3 - 1);
+                    float kr[8], vr[8];
+                    lds8_bf16(Kc + hr * kQS + c8, kr);
+                    lds8_bf16(Vc + hr * kQS + c8, vr);
+                    d1[t3] = dot8(q, kr);
+                    d1[3 + t3] = dot8(go, vr);
+                }
+#pragma unroll
+                for (int t = 0; t < 6; ++t) d1[t] = group8_sum(d1[t]);
+#pragma unroll
+                for (int t3 = 0; t3 < 3; ++t3) {
+                    const int cc = c + t3 - 1;
+                    if (!row_in || cc < 0 || cc >= p.W) continue;
+                    const float a = expf(d1[t3] * scale - sj.x) * izj;
+                    const float de = a * (d1[3 + t3] * (1.f - al) - sj.z) * scale;
+                    float kr[8];
+                    lds8_bf16(Kc + halo_row(u, dy, t3 - 1) * kQS + c8, kr);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) dq[e] = fmaf(de, kr[e], dq[e]);
+                }
+            }
+            {   // u as a key of each neighbour i's window (the window is symmetric)
+                float d2[6];
+#pragma unroll
+                for (int t3 = 0; t3 < 3; ++t3) {
+                    const int hr = halo_row(u, dy, t3 - 1);
+                    float qi[8], gi[8];
+                    lds8_bf16(Qc + hr * kQS + c8, qi);
+                    lds8_bf16(Gc + hr * kQS + c8, gi);
+                    d2[t3] = dot8(qi, k);
+                    d2[3 + t3] = dot8(gi, v);
+                }
+#pragma unroll
+                for (int t = 0; t < 6; ++t) d2[t] = group8_sum(d2[t]);
+#pragma unroll
+                for (int t3 = 0; t3 < 3; ++t3) {
+                    const int cc = c + t3 - 1;
+                    if (!row_in || cc < 0 || cc >= p.W) continue;
+                    const int hr = halo_row(u, dy, t3 - 1);
+                    const float4 si = Lc[hr];
+                    const float a = expf(d2[t3] * scale - si.x) / si.y;
+                    const float de = a * (d2[3 + t3] * (1.f - al) - si.z) * scale;
+                    float qi[8], gi[8];
+                    lds8_bf16(Qc + hr * kQS + c8, qi);
+                    lds8_bf16(Gc + hr * kQS + c8, gi);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        dv[e] = fmaf(a * (1.f - al), gi[e], dv[e]);
+                        dk[e] = fmaf(de, qi[e], dk[e]);
+                    }
+                }
+            }
+        }
+        if (live) {
+            // dXq through the feature map: the staged Q is ReLU'd, and ReLU(x) > 0 exactly when x > 0
+            uint4 oq, ov;
+            uint32_t *pq = &oq.x, *pv = &ov.x;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float q0 = (p.relu && !(q[2 * e] > 0.f)) ? 0.f : dq[2 * e];
+                const float q1 = (p.relu && !(q[2 * e + 1] > 0.f)) ? 0.f : dq[2 * e + 1];
+                pq[e] = pack_bf16(q0, q1);
+                pv[e] = pack_bf16(dv[2 * e], dv[2 * e + 1]);
+            }
+            *reinterpret_cast<uint4 *>(dQo + (size_t)j * D + c8) = oq;
+            *reinterpret_cast<uint4 *>(dVo + (size_t)j * D + c8) = ov;
+            float4 *kp = reinterpret_cast<float4 *>(dKp + (size_t)j * D + c8);
+            kp[0] = make_float4(dk[0], dk[1], dk[2], dk[3]);
+            kp[1] = make_float4(dk[4], dk[5], dk[6], dk[7]);
+        }
+        // the warp's four tokens' ds terms, summed over the quarters in a fixed order
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            dsl[e] += __shfl_xor_sync(0xffffffffu, dsl[e], 8);
+            dsl[e] += __shfl_xor_sync(0xffffffffu, dsl[e], 16);
+        }
+        if (qg == 0)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) dsw[warp][c8 + e] = dsl[e];
+        __syncthreads();
+        for (int ch = tid; ch < D; ch += kTileThreads) {
+            float acc = 0.f;
+            for (int w = 0; w < kTileWarps; ++w) acc += dsw[w][ch];
+            b.ds_part[((size_t)sl * b.ntile + tile) * D + ch] = acc;
+        }
+        __syncthreads();   // every read of this tile's buffers, Qt, the outputs and dsw is done
     }
 }
 
@@ -2189,7 +2226,9 @@ cudaError_t launch_bwd_all(const BwdProblem &b, cudaStream_t st) {
         if ((err = cudaFuncSetAttribute(bwd_token_b_tile, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         kTileSmemBytes)) != cudaSuccess)
             return err;
-        bwd_token_b_tile<<<(unsigned)p.slices * (unsigned)b.ntile, kTileThreads, kTileSmemBytes, st>>>(b);
+        const long long ntiles = (long long)p.slices * b.ntile;
+        const unsigned grid = (unsigned)(ntiles < 152 ? ntiles : 152);   // persistent: one CTA per SM
+        bwd_token_b_tile<<<grid, kTileThreads, kTileSmemBytes, st>>>(b);
     } else if (std::is_same<TIn, __nv_bfloat16>::value && D == 64 && p.relu != 2) {
         bwd_bimg<<<dim3((unsigned)p.slices, 5), kThreads, 0, st>>>(b);
         if ((err = cudaFuncSetAttribute(bwd_token_b_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
