@@ -1592,14 +1592,14 @@ __global__ void __launch_bounds__(kTileThreads, 1) bwd_token_b_tile(BwdProblem b
             const int dy = dyi - 1, rr = r + dy;
             const bool row_in = rr >= 0 && rr < p.H;
             {   // u as the query: scores against its window, dl_u . V_i
-                float d1[6];
+                float kr[3][8], d1[6];
 #pragma unroll
                 for (int t3 = 0; t3 < 3; ++t3) {
                     const int hr = halo_row(u, dy, t3 - 1);
-                    float kr[8], vr[8];
-                    lds8_bf16(Kc + hr * kQS + c8, kr);
+                    float vr[8];
+                    lds8_bf16(Kc + hr * kQS + c8, kr[t3]);
                     lds8_bf16(Vc + hr * kQS + c8, vr);
-                    d1[t3] = dot8(q, kr);
+                    d1[t3] = dot8(q, kr[t3]);
                     d1[3 + t3] = dot8(go, vr);
                 }
 #pragma unroll
@@ -1610,22 +1610,19 @@ __global__ void __launch_bounds__(kTileThreads, 1) bwd_token_b_tile(BwdProblem b
                     if (!row_in || cc < 0 || cc >= p.W) continue;
                     const float a = expf(d1[t3] * scale - sj.x) * izj;
                     const float de = a * (d1[3 + t3] * (1.f - al) - sj.z) * scale;
-                    float kr[8];
-                    lds8_bf16(Kc + halo_row(u, dy, t3 - 1) * kQS + c8, kr);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) dq[e] = fmaf(de, kr[e], dq[e]);
+                    for (int e = 0; e < 8; ++e) dq[e] = fmaf(de, kr[t3][e], dq[e]);
                 }
             }
             {   // u as a key of each neighbour i's window (the window is symmetric)
-                float d2[6];
+                float qi[3][8], gi[3][8], d2[6];
 #pragma unroll
                 for (int t3 = 0; t3 < 3; ++t3) {
                     const int hr = halo_row(u, dy, t3 - 1);
-                    float qi[8], gi[8];
-                    lds8_bf16(Qc + hr * kQS + c8, qi);
-                    lds8_bf16(Gc + hr * kQS + c8, gi);
-                    d2[t3] = dot8(qi, k);
-                    d2[3 + t3] = dot8(gi, v);
+                    lds8_bf16(Qc + hr * kQS + c8, qi[t3]);
+                    lds8_bf16(Gc + hr * kQS + c8, gi[t3]);
+                    d2[t3] = dot8(qi[t3], k);
+                    d2[3 + t3] = dot8(gi[t3], v);
                 }
 #pragma unroll
                 for (int t = 0; t < 6; ++t) d2[t] = group8_sum(d2[t]);
@@ -1633,17 +1630,13 @@ __global__ void __launch_bounds__(kTileThreads, 1) bwd_token_b_tile(BwdProblem b
                 for (int t3 = 0; t3 < 3; ++t3) {
                     const int cc = c + t3 - 1;
                     if (!row_in || cc < 0 || cc >= p.W) continue;
-                    const int hr = halo_row(u, dy, t3 - 1);
-                    const float4 si = Lc[hr];
+                    const float4 si = Lc[halo_row(u, dy, t3 - 1)];
                     const float a = expf(d2[t3] * scale - si.x) / si.y;
                     const float de = a * (d2[3 + t3] * (1.f - al) - si.z) * scale;
-                    float qi[8], gi[8];
-                    lds8_bf16(Qc + hr * kQS + c8, qi);
-                    lds8_bf16(Gc + hr * kQS + c8, gi);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        dv[e] = fmaf(a * (1.f - al), gi[e], dv[e]);
-                        dk[e] = fmaf(de, qi[e], dk[e]);
+                        dv[e] = fmaf(a * (1.f - al), gi[t3][e], dv[e]);
+                        dk[e] = fmaf(de, qi[t3][e], dk[e]);
                     }
                 }
             }
