@@ -1392,13 +1392,15 @@ __global__ void __launch_bounds__(kThreads) bwd_token_a_tc(BwdProblem b) {
 // gather their A rows from the halo (ldmatrix takes a row address per lane);
 // the quarter-warp phase reads every neighbour row from it.
 // ---------------------------------------------------------------------------
+constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kHaloSide = 10;                 // an 8 x 8 tile and its one-token border
 constexpr int kHaloRows = kHaloSide * kHaloSide;
 constexpr int kTileTok = 64;
 constexpr int kTileWarps = 16;
 constexpr int kTileThreads = 32 * kTileWarps;
 constexpr int kHaloBytes = 4 * kHaloRows * kQS * 2 + kHaloRows * 16;   // K, V, Q, dO rows; statistics
-constexpr int kTileSmemBytes = kImgRows * kBS * 2 + 2 * kHaloBytes + kTileTok * kQS * 2 + 3 * kTileTok * 64 * 4;
+constexpr int kOS = 68;                      // row stride (floats) of the products' outputs: conflict-free column reads
+constexpr int kTileSmemBytes = kImgRows * kBS * 2 + 2 * kHaloBytes + kTileTok * kQS * 2 + 3 * kTileTok * kOS * 4;
 
 // Halo row of the grid position (dy, dx) away from the tile's token u.
 __device__ __forceinline__ int halo_row(int u, int dy, int dx) {
@@ -1414,6 +1416,13 @@ __device__ __forceinline__ void lds8_bf16(const __nv_bfloat16 *row, float (&x)[8
         x[2 * k + 1] = sm100::bf16_hi(u[k]);
     }
 }
+// 2^x on the special-function unit (approximate, as the forward's local softmax).
+__device__ __forceinline__ float ex2_fast(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // 16-byte asynchronous copy global -> shared; zero-filled when !valid (src
 // is then not read).
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
@@ -1431,8 +1440,9 @@ __global__ void __launch_bounds__(kTileThreads, 1) bwd_token_b_tile(BwdProblem b
     __nv_bfloat16 *Bs = reinterpret_cast<__nv_bfloat16 *>(smem_tile);
     uint8_t *halo0 = reinterpret_cast<uint8_t *>(Bs + kImgRows * kBS);   // two halo buffers
     __nv_bfloat16 *Qt = reinterpret_cast<__nv_bfloat16 *>(halo0 + 2 * kHaloBytes);   // Q~ of the tile's tokens
-    float *oQ = reinterpret_cast<float *>(Qt + kTileTok * kQS), *oV = oQ + kTileTok * D, *oK = oV + kTileTok * D;
+    float *oQ = reinterpret_cast<float *>(Qt + kTileTok * kQS), *oV = oQ + kTileTok * kOS, *oK = oV + kTileTok * kOS;
     __shared__ float rqs[kTileTok];
+    __shared__ float cjs[kTileTok];
     __shared__ float dsw[kTileWarps][D];
     const Problem &p = b.fwd;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1550,123 +1560,192 @@ __global__ void __launch_bounds__(kTileThreads, 1) bwd_token_b_tile(BwdProblem b
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
                     const int col = 16 * sb + 8 * nt + 2 * (lane & 3);
-                    out[row * D + col] = acc[nt][0];
-                    out[row * D + col + 1] = acc[nt][1];
-                    out[(row + 8) * D + col] = acc[nt][2];
-                    out[(row + 8) * D + col + 1] = acc[nt][3];
+                    out[row * kOS + col] = acc[nt][0];
+                    out[row * kOS + col + 1] = acc[nt][1];
+                    out[(row + 8) * kOS + col] = acc[nt][2];
+                    out[(row + 8) * kOS + col + 1] = acc[nt][3];
                 }
             }
         }
         __syncthreads();
 
-        // ---- a quarter-warp per token: normaliser, window, stores
-        const int y = u / 8, xx = u % 8, r = r0 + y, c = c0 + xx;
-        const bool live = r < p.H && c < p.W;
-        const int j = r * p.W + c;
-        const int hc = halo_row(u, 0, 0);
-        float q[8], go[8], k[8], v[8], dqt[8], dv[8], dk[8];
-        lds8_bf16(Qc + hc * kQS + c8, q);
-        lds8_bf16(Gc + hc * kQS + c8, go);
-        lds8_bf16(Kc + hc * kQS + c8, k);
-        lds8_bf16(Vc + hc * kQS + c8, v);
+        // ---- per token (quarter-warp): the normaliser's cj = (dQ~_u . Q_u) rq^2 and the ds terms
+        {
+            float dsl[8];
+            const int y = u / 8, xx = u % 8;
+            const bool live = r0 + y < p.H && c0 + xx < p.W;
+            float q[8], dqt[8];
+            lds8_bf16(Qc + halo_row(u, 0, 0) * kQS + c8, q);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            dqt[e] = oQ[u * D + c8 + e];
-            dv[e] = fmaf(w0 * al, go[e], oV[u * D + c8 + e]);
-            dk[e] = oK[u * D + c8 + e];
-        }
-        const float rq = rqs[u];
-        const float cj = group8_sum(dot8(dqt, q)) * rq * rq;
-        float dq[8], dsl[8];
+            for (int e = 0; e < 8; ++e) dqt[e] = oQ[u * kOS + c8 + e];
+            const float rq = rqs[u];
+            const float cj = group8_sum(dot8(dqt, q)) * rq * rq;
+            if ((lane & 7) == 0) cjs[u] = cj;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            dq[e] = dqt[e] * rq - cj * s[c8 + e];
-            dsl[e] = live ? -cj * q[e] : 0.f;
-        }
-        const float4 sj = live ? Lc[hc] : make_float4(0.f, 1.f, 0.f, 0.f);
-        const float izj = 1.f / sj.y;
-        // the window three neighbours (one halo row band) at a time, to keep the
-        // dot products in few registers
-#pragma unroll 1
-        for (int dyi = 0; dyi < 3; ++dyi) {
-            const int dy = dyi - 1, rr = r + dy;
-            const bool row_in = rr >= 0 && rr < p.H;
-            {   // u as the query: scores against its window, dl_u . V_i
-                float kr[3][8], d1[6];
+            for (int e = 0; e < 8; ++e) dsl[e] = live ? -cj * q[e] : 0.f;
+            // the warp's four tokens' ds terms, summed over the quarters in a fixed order
 #pragma unroll
-                for (int t3 = 0; t3 < 3; ++t3) {
-                    const int hr = halo_row(u, dy, t3 - 1);
-                    float vr[8];
-                    lds8_bf16(Kc + hr * kQS + c8, kr[t3]);
-                    lds8_bf16(Vc + hr * kQS + c8, vr);
-                    d1[t3] = dot8(q, kr[t3]);
-                    d1[3 + t3] = dot8(go, vr);
-                }
-#pragma unroll
-                for (int t = 0; t < 6; ++t) d1[t] = group8_sum(d1[t]);
-#pragma unroll
-                for (int t3 = 0; t3 < 3; ++t3) {
-                    const int cc = c + t3 - 1;
-                    if (!row_in || cc < 0 || cc >= p.W) continue;
-                    const float a = expf(d1[t3] * scale - sj.x) * izj;
-                    const float de = a * (d1[3 + t3] * (1.f - al) - sj.z) * scale;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) dq[e] = fmaf(de, kr[t3][e], dq[e]);
-                }
+            for (int e = 0; e < 8; ++e) {
+                dsl[e] += __shfl_xor_sync(0xffffffffu, dsl[e], 8);
+                dsl[e] += __shfl_xor_sync(0xffffffffu, dsl[e], 16);
             }
-            {   // u as a key of each neighbour i's window (the window is symmetric)
-                float qi[3][8], gi[3][8], d2[6];
+            if (qg == 0)
 #pragma unroll
-                for (int t3 = 0; t3 < 3; ++t3) {
-                    const int hr = halo_row(u, dy, t3 - 1);
-                    lds8_bf16(Qc + hr * kQS + c8, qi[t3]);
-                    lds8_bf16(Gc + hr * kQS + c8, gi[t3]);
-                    d2[t3] = dot8(qi[t3], k);
-                    d2[3 + t3] = dot8(gi[t3], v);
+                for (int e = 0; e < 8; ++e) dsw[warp][c8 + e] = dsl[e];
+        }
+        __syncthreads();
+
+        // ---- the window on the tensor cores: warp = block beta (tile rows 2 beta,
+        // 2 beta + 1) x role (0: the block's tokens as queries -> dQ; 1: as keys
+        // -> dK; 2: as keys -> dV).  Scores of the 16 tokens against the 4 x 10
+        // window of the block; only the 3 x 3 window of each token counts.
+        const int beta = warp & 3, role = warp >> 2;
+        if (role < 3) {
+            const int g = lane >> 2, q4 = lane & 3;
+            // halo row of the block's fragment row m, and of window position kappa
+            auto hrow_b = [&](int m) { return (2 * beta + 1 + (m >> 3)) * kHaloSide + (m & 7) + 1; };
+            auto hrow_w = [&](int kappa) { return (2 * beta + kappa / 10) * kHaloSide + kappa % 10; };
+            // bit j*4+e: window position 8j + 2 q4 + (e & 1) is inside the 3 x 3 window of
+            // fragment row g + 8 (e >> 1) and inside the grid
+            uint32_t wmask = 0;
+#pragma unroll
+            for (int j = 0; j < 5; ++j)
+#pragma unroll
+                for (int bb = 0; bb < 2; ++bb) {
+                    const int kappa = 8 * j + 2 * q4 + bb, ka = kappa / 10, kb = kappa % 10;
+                    const int gr = r0 - 1 + 2 * beta + ka, gc = c0 - 1 + kb;
+                    if (gr < 0 || gr >= p.H || gc < 0 || gc >= p.W) continue;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int du = ka - h, dv = kb - g;
+                        if (du >= 0 && du <= 2 && dv >= 0 && dv <= 2) wmask |= 1u << (j * 4 + 2 * h + bb);
+                    }
                 }
+            const uint32_t arow_m = (uint32_t)((lane & 7) + 8 * ((lane >> 3) & 1));   // A-fragment row of this lane
+            // scores [16 x 40] = rows(Ab) . rows(Bw)^T over the 64 channels
+            auto scores = [&](const __nv_bfloat16 *Ab, const __nv_bfloat16 *Bw, float (&sc)[5][4]) {
 #pragma unroll
-                for (int t = 0; t < 6; ++t) d2[t] = group8_sum(d2[t]);
+                for (int j = 0; j < 5; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+                const uint32_t abase = smem_u32(Ab) + (uint32_t)hrow_b(arow_m) * kQS * 2u;
 #pragma unroll
-                for (int t3 = 0; t3 < 3; ++t3) {
-                    const int cc = c + t3 - 1;
-                    if (!row_in || cc < 0 || cc >= p.W) continue;
-                    const float4 si = Lc[halo_row(u, dy, t3 - 1)];
-                    const float a = expf(d2[t3] * scale - si.x) / si.y;
-                    const float de = a * (d2[3 + t3] * (1.f - al) - si.z) * scale;
+                for (int ks = 0; ks < 4; ++ks) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(abase + (uint32_t)((2 * ks + (lane >> 4)) * 8) * 2u, a0, a1, a2, a3);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        dv[e] = fmaf(a * (1.f - al), gi[t3][e], dv[e]);
-                        dk[e] = fmaf(de, qi[t3][e], dk[e]);
+                    for (int pr = 0; pr < 3; ++pr) {
+                        const int kk = 8 * (2 * pr + (lane >> 4)) + (lane & 7);
+                        const int kk2 = kk < 40 ? kk : 0;
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4(smem_u32(Bw) + (uint32_t)(hrow_w(kk2) * kQS + (2 * ks + ((lane >> 3) & 1)) * 8) * 2u,
+                                b0, b1, b2, b3);
+                        mma_bf16_16816(sc[2 * pr], a0, a1, a2, a3, b0, b1);
+                        if (pr < 2) mma_bf16_16816(sc[2 * pr + 1], a0, a1, a2, a3, b2, b3);
+                    }
+                }
+            };
+            // acc [16 x 64] = w [16 x 40] . rows(Xw) (w in C-fragment layout, rounded to bf16)
+            auto times_window = [&](const float (&w)[5][4], const __nv_bfloat16 *Xw, float (&acc)[8][4]) {
+#pragma unroll
+                for (int nt = 0; nt < 8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+#pragma unroll
+                for (int ks = 0; ks < 3; ++ks) {
+                    const int j0 = 2 * ks, j1 = 2 * ks + 1;
+                    const uint32_t pa0 = pack_bf16(w[j0][0], w[j0][1]), pa1 = pack_bf16(w[j0][2], w[j0][3]);
+                    const uint32_t pa2 = j1 < 5 ? pack_bf16(w[j1][0], w[j1][1]) : 0u;
+                    const uint32_t pa3 = j1 < 5 ? pack_bf16(w[j1][2], w[j1][3]) : 0u;
+                    const int kv = 16 * ks + (lane & 7) + 8 * ((lane >> 3) & 1);
+                    const uint32_t vrow = smem_u32(Xw) + (uint32_t)hrow_w(kv < 40 ? kv : 0) * kQS * 2u;
+#pragma unroll
+                    for (int np = 0; np < 4; ++np) {
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4_t(vrow + (uint32_t)((2 * np + (lane >> 4)) * 8) * 2u, b0, b1, b2, b3);
+                        mma_bf16_16816(acc[2 * np], pa0, pa1, pa2, pa3, b0, b1);
+                        mma_bf16_16816(acc[2 * np + 1], pa0, pa1, pa2, pa3, b2, b3);
+                    }
+                }
+            };
+            float sc[5][4], acc[8][4];
+            if (role == 0) {
+                // the block's tokens as queries: P = softmax weights (their own statistics),
+                // dP = dl_i . V_j, de = P (dP - dl_i . l_i) / sqrt(d); dQ window term = de K
+                scores(Qc, Kc, sc);
+                float emx[2], ies[2], dll[2];   // row statistics, the max in log2 units
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float4 sh = Lc[hrow_b(g + 8 * h)];
+                    emx[h] = sh.x * kLog2e;
+                    ies[h] = 1.f / sh.y;
+                    dll[h] = sh.z;
+                }
+                float dp[5][4];
+                scores(Gc, Vc, dp);
+#pragma unroll
+                for (int j = 0; j < 5; ++j)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int h = e >> 1;
+                        const float a = ((wmask >> (j * 4 + e)) & 1u)
+                                            ? ex2_fast(fmaf(sc[j][e], scale * kLog2e, -emx[h])) * ies[h] : 0.f;
+                        sc[j][e] = a * (dp[j][e] * (1.f - al) - dll[h]) * scale;
+                    }
+                times_window(sc, Kc, acc);
+            } else {
+                // the block's tokens as keys of the window's queries: P' with each query's
+                // statistics; role 1: de' = P' (dP' - dl_i . l_i) / sqrt(d), dK term = de' Q;
+                // role 2: dV term = (1 - alpha) P' dO
+                scores(Kc, Qc, sc);
+                float dp[5][4];
+                if (role == 1) scores(Vc, Gc, dp);
+#pragma unroll
+                for (int j = 0; j < 5; ++j)
+#pragma unroll
+                    for (int bb = 0; bb < 2; ++bb) {
+                        const int kappa = 8 * j + 2 * q4 + bb;
+                        const float4 sk = Lc[hrow_w(kappa < 40 ? kappa : 0)];
+                        const float emx = sk.x * kLog2e, ies = ((wmask >> (j * 4 + bb)) & 0x5u) ? 1.f / sk.y : 0.f;
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int e = 2 * h + bb;
+                            const float a = ((wmask >> (j * 4 + e)) & 1u)
+                                                ? ex2_fast(fmaf(sc[j][e], scale * kLog2e, -emx)) * ies : 0.f;
+                            sc[j][e] = role == 1 ? a * (dp[j][e] * (1.f - al) - sk.z) * scale : a * (1.f - al);
+                        }
+                    }
+                times_window(sc, role == 1 ? Qc : Gc, acc);
+            }
+            // ---- combine with the products' terms and store (C-fragment layout)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int m = g + 8 * h, ut = (2 * beta + h) * 8 + g;   // tile token of fragment row m
+                const int rr = r0 + 2 * beta + h, cc = c0 + g;
+                if (rr >= p.H || cc >= p.W) continue;
+                const size_t jt = (size_t)(rr * p.W + cc) * D;
+                const float rq = rqs[ut], cj = cjs[ut];
+#pragma unroll
+                for (int nt = 0; nt < 8; ++nt) {
+                    const int col = 8 * nt + 2 * q4;
+                    const float x0 = acc[nt][2 * h], x1 = acc[nt][2 * h + 1];
+                    if (role == 0) {
+                        float d0 = oQ[ut * kOS + col] * rq - cj * s[col] + x0;
+                        float d1 = oQ[ut * kOS + col + 1] * rq - cj * s[col + 1] + x1;
+                        if (p.relu) {   // dXq through the feature map (the staged Q is ReLU'd)
+                            const uint32_t qp = *reinterpret_cast<const uint32_t *>(Qc + hrow_b(m) * kQS + col);
+                            if (!(bf16_lo(qp) > 0.f)) d0 = 0.f;
+                            if (!(bf16_hi(qp) > 0.f)) d1 = 0.f;
+                        }
+                        *reinterpret_cast<uint32_t *>(dQo + jt + col) = pack_bf16(d0, d1);
+                    } else if (role == 1) {
+                        *reinterpret_cast<float2 *>(dKp + jt + col) =
+                            make_float2(oK[ut * kOS + col] + x0, oK[ut * kOS + col + 1] + x1);
+                    } else {
+                        const uint32_t gp = *reinterpret_cast<const uint32_t *>(Gc + hrow_b(m) * kQS + col);
+                        const float d0 = fmaf(w0 * al, bf16_lo(gp), oV[ut * kOS + col]) + x0;
+                        const float d1 = fmaf(w0 * al, bf16_hi(gp), oV[ut * kOS + col + 1]) + x1;
+                        *reinterpret_cast<uint32_t *>(dVo + jt + col) = pack_bf16(d0, d1);
                     }
                 }
             }
         }
-        if (live) {
-            // dXq through the feature map: the staged Q is ReLU'd, and ReLU(x) > 0 exactly when x > 0
-            uint4 oq, ov;
-            uint32_t *pq = &oq.x, *pv = &ov.x;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float q0 = (p.relu && !(q[2 * e] > 0.f)) ? 0.f : dq[2 * e];
-                const float q1 = (p.relu && !(q[2 * e + 1] > 0.f)) ? 0.f : dq[2 * e + 1];
-                pq[e] = pack_bf16(q0, q1);
-                pv[e] = pack_bf16(dv[2 * e], dv[2 * e + 1]);
-            }
-            *reinterpret_cast<uint4 *>(dQo + (size_t)j * D + c8) = oq;
-            *reinterpret_cast<uint4 *>(dVo + (size_t)j * D + c8) = ov;
-            float4 *kp = reinterpret_cast<float4 *>(dKp + (size_t)j * D + c8);
-            kp[0] = make_float4(dk[0], dk[1], dk[2], dk[3]);
-            kp[1] = make_float4(dk[4], dk[5], dk[6], dk[7]);
-        }
-        // the warp's four tokens' ds terms, summed over the quarters in a fixed order
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            dsl[e] += __shfl_xor_sync(0xffffffffu, dsl[e], 8);
-            dsl[e] += __shfl_xor_sync(0xffffffffu, dsl[e], 16);
-        }
-        if (qg == 0)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) dsw[warp][c8 + e] = dsl[e];
         __syncthreads();
         for (int ch = tid; ch < D; ch += kTileThreads) {
             float acc = 0.f;
