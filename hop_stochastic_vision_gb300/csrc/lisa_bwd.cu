@@ -52,6 +52,7 @@
 #include "lisa_internal.h"
 #include "lisa_sm100.cuh"
 #include "lisa_solve.cuh"
+#include "lisa_tc_common.cuh"
 
 namespace lisa {
 namespace {
@@ -1387,10 +1388,10 @@ __global__ void __launch_bounds__(kThreads) bwd_token_a_tc(BwdProblem b) {
 // 5''. bf16, d = 64, fixed weights: the token pass on 8 x 8 token tiles.  A
 // persistent CTA of 16 warps walks a contiguous run of tiles.  Each tile's
 // halo (10 x 10 grid positions) of K, V, Q (feature-mapped) and dO, and the
-// halo tokens' window statistics, arrive in shared memory by cp.async while
-// the previous tile computes (two halo buffers); the three d x d products
-// gather their A rows from the halo (ldmatrix takes a row address per lane);
-// the quarter-warp phase reads every neighbour row from it.
+// halo tokens' window statistics, arrive in shared memory by TMA (tiled 4-D
+// boxes, zero-filled off the grid; 128-byte swizzled rows) while the
+// previous tile computes (two halo buffers); the three d x d products gather
+// their A rows from the halo (ldmatrix takes a row address per lane).
 // ---------------------------------------------------------------------------
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kHaloSide = 10;                 // an 8 x 8 tile and its one-token border
@@ -1398,17 +1399,27 @@ constexpr int kHaloRows = kHaloSide * kHaloSide;
 constexpr int kTileTok = 64;
 constexpr int kTileWarps = 16;
 constexpr int kTileThreads = 32 * kTileWarps;
-constexpr int kHaloBytes = 4 * kHaloRows * kQS * 2 + kHaloRows * 16;   // K, V, Q, dO rows; statistics
+// one halo buffer: K, V, Q, dO as 100 rows of 128 B each (a 1024-byte
+// multiple apart, as the 128-byte swizzle wants), then the 100 statistics
+constexpr int kHaloTensor = (kHaloRows * 128 + 1023) / 1024 * 1024;
+constexpr int kHaloStats = 4 * kHaloTensor;
+constexpr int kHaloBytes = (kHaloStats + kHaloRows * 16 + 1023) / 1024 * 1024;
+constexpr uint32_t kHaloTx = 4u * kHaloRows * 128u + kHaloRows * 16u;     // bytes one tile's TMA delivers
 constexpr int kOS = 68;                      // row stride (floats) of the products' outputs: conflict-free column reads
-constexpr int kTileSmemBytes = kImgRows * kBS * 2 + 2 * kHaloBytes + kTileTok * kQS * 2 + 3 * kTileTok * kOS * 4;
+constexpr int kTileSmemBytes =
+    1024 + 2 * kHaloBytes + kImgRows * kBS * 2 + kTileTok * kQS * 2 + 3 * kTileTok * kOS * 4;
 
 // Halo row of the grid position (dy, dx) away from the tile's token u.
 __device__ __forceinline__ int halo_row(int u, int dy, int dx) {
     return (u / 8 + 1 + dy) * kHaloSide + (u % 8 + 1 + dx);
 }
-// Eight bf16 channels of a shared-memory row (16-byte aligned) as floats.
-__device__ __forceinline__ void lds8_bf16(const __nv_bfloat16 *row, float (&x)[8]) {
-    const uint4 w = *reinterpret_cast<const uint4 *>(row);
+// Byte offset of 16-byte chunk `chunk` of halo row `row` (128-byte swizzle).
+__device__ __forceinline__ uint32_t hoff(int row, int chunk) {
+    return (uint32_t)row * 128u + ((uint32_t)(chunk ^ (row & 7)) << 4);
+}
+// Eight bf16 channels (chunk `chunk`) of halo row `row` as floats.
+__device__ __forceinline__ void lds8_sw(const uint8_t *region, int row, int chunk, float (&x)[8]) {
+    const uint4 w = *reinterpret_cast<const uint4 *>(region + hoff(row, chunk));
     const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -1423,23 +1434,17 @@ __device__ __forceinline__ float ex2_fast(float x) {
     return y;
 }
 
-// 16-byte asynchronous copy global -> shared; zero-filled when !valid (src
-// is then not read).
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-__global__ void __launch_bounds__(kTileThreads, 1) bwd_token_b_tile(BwdProblem b) {
+__global__ void __launch_bounds__(kTileThreads, 1)
+    bwd_token_b_tile(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
+                     const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mG,
+                     const __grid_constant__ CUtensorMap mL, BwdProblem b) {
     constexpr int D = 64;
     using namespace sm100;
-    extern __shared__ float4 smem_tile[];
-    __nv_bfloat16 *Bs = reinterpret_cast<__nv_bfloat16 *>(smem_tile);
-    uint8_t *halo0 = reinterpret_cast<uint8_t *>(Bs + kImgRows * kBS);   // two halo buffers
-    __nv_bfloat16 *Qt = reinterpret_cast<__nv_bfloat16 *>(halo0 + 2 * kHaloBytes);   // Q~ of the tile's tokens
+    extern __shared__ uint8_t smem_tile_raw[];
+    uint8_t *halo0 = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_tile_raw) + 1023) & ~uintptr_t(1023));
+    __nv_bfloat16 *Bs = reinterpret_cast<__nv_bfloat16 *>(halo0 + 2 * kHaloBytes);
+    __nv_bfloat16 *Qt = Bs + kImgRows * kBS;   // Q~ of the tile's tokens
+    __shared__ __align__(8) uint64_t hbar[2];   // a halo buffer's TMA landed
     float *oQ = reinterpret_cast<float *>(Qt + kTileTok * kQS), *oV = oQ + kTileTok * kOS, *oK = oV + kTileTok * kOS;
     __shared__ float rqs[kTileTok];
     __shared__ float cjs[kTileTok];
@@ -1453,42 +1458,34 @@ __global__ void __launch_bounds__(kTileThreads, 1) bwd_token_b_tile(BwdProblem b
     const int qg = lane >> 3, c8 = 8 * (lane & 7);
     const int u = 4 * warp + qg;   // this quarter's token of a tile
 
-    // K, V, Q, dO rows and statistics of tile t's halo into buffer `buf`, asynchronously
+    if (tid == 0) {
+        mbar_init(smem_u32(&hbar[0]), 1);
+        mbar_init(smem_u32(&hbar[1]), 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    // the halo of tile t (K, V, Q, dO rows, statistics) into buffer `buf`; one thread
     auto stage_halo = [&](int t, int buf) {
         const int sl = t / b.ntile, tile = t % b.ntile;
         const int r0 = (tile / tiles_c) * 8, c0 = (tile % tiles_c) * 8;
-        const size_t sbase = (size_t)sl * p.n * D;
-        const uint32_t hb = smem_u32(halo0 + buf * kHaloBytes);
-        for (int x = tid; x < 4 * kHaloRows * 8; x += kTileThreads) {
-            const int tn = x / (kHaloRows * 8), h = (x >> 3) % kHaloRows, c = x & 7;
-            const int gr = r0 - 1 + h / kHaloSide, gc = c0 - 1 + h % kHaloSide;
-            const bool in = gr >= 0 && gr < p.H && gc >= 0 && gc < p.W;
-            const void *src = tn == 0 ? p.K : (tn == 1 ? p.V : (tn == 2 ? p.Q : b.dO));
-            const __nv_bfloat16 *row = static_cast<const __nv_bfloat16 *>(src) + sbase +
-                                       (size_t)(in ? gr * p.W + gc : 0) * D + c * 8;
-            cp_async16(hb + (uint32_t)((tn * kHaloRows + h) * kQS + c * 8) * 2u, row, in);
-        }
-        const float4 *lst = reinterpret_cast<const float4 *>(b.lstat) + (size_t)sl * p.n;
-        for (int h = tid; h < kHaloRows; h += kTileThreads) {
-            const int gr = r0 - 1 + h / kHaloSide, gc = c0 - 1 + h % kHaloSide;
-            const bool in = gr >= 0 && gr < p.H && gc >= 0 && gc < p.W;
-            cp_async16(hb + (uint32_t)(4 * kHaloRows * kQS * 2 + h * 16), lst + (in ? gr * p.W + gc : 0), in);
-        }
-        cp_async_commit();
+        const uint32_t hb = smem_u32(halo0 + buf * kHaloBytes), bar = smem_u32(&hbar[buf]);
+        fence_proxy_async();   // this buffer's earlier generic writes (the ReLU pass) before the async ones
+        mbar_arrive_expect_tx(bar, kHaloTx);
+        tma_load_4d(hb, &mK, 0, c0 - 1, r0 - 1, sl, bar);
+        tma_load_4d(hb + kHaloTensor, &mV, 0, c0 - 1, r0 - 1, sl, bar);
+        tma_load_4d(hb + 2 * kHaloTensor, &mQ, 0, c0 - 1, r0 - 1, sl, bar);
+        tma_load_4d(hb + 3 * kHaloTensor, &mG, 0, c0 - 1, r0 - 1, sl, bar);
+        tma_load_4d(hb + kHaloStats, &mL, 0, c0 - 1, r0 - 1, sl, bar);
     };
 
     int img_sl = -1;
-    if (t_begin < t_end) stage_halo(t_begin, 0);
+    if (t_begin < t_end && tid == 0) stage_halo(t_begin, 0);
     for (int t = t_begin, it = 0; t < t_end; ++t, ++it) {
         const int cur = it & 1;
         // the next tile's halo streams in while this one computes; its buffer
         // was last read by the tile before this one, which ended on a barrier
-        if (t + 1 < t_end) {
-            stage_halo(t + 1, cur ^ 1);
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
-        }
+        if (t + 1 < t_end && tid == 0) stage_halo(t + 1, cur ^ 1);
+        if (!mbar_wait(smem_u32(&hbar[cur]), (uint32_t)(it >> 1) & 1u)) record_error(p.err, kErrTimeoutLoad);
         const int sl = t / b.ntile, tile = t % b.ntile;
         const int r0 = (tile / tiles_c) * 8, c0 = (tile % tiles_c) * 8;
         if (sl != img_sl) {   // the slice's B image (tiles of one slice are consecutive)
@@ -1497,15 +1494,15 @@ __global__ void __launch_bounds__(kTileThreads, 1) bwd_token_b_tile(BwdProblem b
                 *reinterpret_cast<uint4 *>(Bs + (x >> 3) * kBS + (x & 7) * 8) = img[x];
             img_sl = sl;
         }
-        __syncthreads();   // this tile's halo (every thread's copies) and the B image are in place
-        __nv_bfloat16 *Kc = reinterpret_cast<__nv_bfloat16 *>(halo0 + cur * kHaloBytes);
-        __nv_bfloat16 *Vc = Kc + kHaloRows * kQS, *Qc = Vc + kHaloRows * kQS, *Gc = Qc + kHaloRows * kQS;
-        const float4 *Lc = reinterpret_cast<const float4 *>(Gc + kHaloRows * kQS);
-        if (p.relu) {   // the feature map of K and Q, in place
+        __syncthreads();   // the B image is in place
+        uint8_t *Kc = halo0 + cur * kHaloBytes;
+        uint8_t *Vc = Kc + kHaloTensor, *Qc = Kc + 2 * kHaloTensor, *Gc = Kc + 3 * kHaloTensor;
+        const float4 *Lc = reinterpret_cast<const float4 *>(Kc + kHaloStats);
+        if (p.relu) {   // the feature map of K and Q, in place (layout-blind: every 16-byte chunk)
             for (int x = tid; x < 2 * kHaloRows * 8; x += kTileThreads) {
-                __nv_bfloat16 *base = x < kHaloRows * 8 ? Kc : Qc;
+                uint8_t *base = x < kHaloRows * 8 ? Kc : Qc;
                 const int y = x % (kHaloRows * 8);
-                uint4 *pv = reinterpret_cast<uint4 *>(base + (y >> 3) * kQS + (y & 7) * 8);
+                uint4 *pv = reinterpret_cast<uint4 *>(base + y * 16);
                 const uint4 v = *pv;
                 *pv = make_uint4(relu_bf16x2(v.x), relu_bf16x2(v.y), relu_bf16x2(v.z), relu_bf16x2(v.w));
             }
@@ -1519,7 +1516,7 @@ __global__ void __launch_bounds__(kTileThreads, 1) bwd_token_b_tile(BwdProblem b
         const float al = p.alpha[sl % p.heads], w0 = p.w[0];
         {   // 1 / (Q_u . s + eps) and Q~_u (bf16) for the second product
             float q[8], sv[8];
-            lds8_bf16(Qc + halo_row(u, 0, 0) * kQS + c8, q);
+            lds8_sw(Qc, halo_row(u, 0, 0), c8 >> 3, q);
 #pragma unroll
             for (int e = 0; e < 8; ++e) sv[e] = s[c8 + e];
             const float rq = 1.f / (group8_sum(dot8(q, sv)) + p.eps);
@@ -1535,7 +1532,8 @@ __global__ void __launch_bounds__(kTileThreads, 1) bwd_token_b_tile(BwdProblem b
         {
             const int mt = warp & 3, sb = warp >> 2;
             const int ua = 16 * mt + (lane & 15), acol = (lane >> 4) * 8;
-            const uint32_t hrow = (uint32_t)halo_row(ua, 0, 0) * kQS, trow = (uint32_t)ua * kQS;
+            const int hrow = halo_row(ua, 0, 0);
+            const uint32_t trow = (uint32_t)ua * kQS;
             const uint32_t bs = smem_u32(Bs);
             const int mi = lane >> 3, brow = (mi & 1) * 8 + (lane & 7), bcol = 16 * sb + (mi >> 1) * 8;
 #pragma unroll
@@ -1546,11 +1544,13 @@ __global__ void __launch_bounds__(kTileThreads, 1) bwd_token_b_tile(BwdProblem b
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     if (ks >= ksteps) break;
-                    // A operand of this k-step: which halo (or Q~) row, which 16 channels
-                    const __nv_bfloat16 *abuf = pr == 0 ? (ks < 4 ? Gc : Kc) : (pr == 1 ? (ks < 4 ? Vc : Qt) : Kc);
-                    const uint32_t arow = (pr == 1 && ks >= 4) ? trow : hrow;
+                    // A operand of this k-step: which halo row (or Q~ row), which 16 channels
+                    const uint8_t *abuf = pr == 0 ? (ks < 4 ? Gc : Kc) : (pr == 1 ? Vc : Kc);
+                    const uint32_t aaddr = (pr == 1 && ks >= 4)
+                                               ? smem_u32(Qt) + (trow + 16 * (ks & 3) + acol) * 2u
+                                               : smem_u32(abuf) + hoff(hrow, 2 * (ks & 3) + (lane >> 4));
                     uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-                    ldsm_x4(smem_u32(abuf) + (arow + 16 * (ks & 3) + acol) * 2u, a0, a1, a2, a3);
+                    ldsm_x4(aaddr, a0, a1, a2, a3);
                     ldsm_x4_t(bs + (uint32_t)((brow0 + 16 * ks + brow) * kBS + bcol) * 2u, b0, b1, b2, b3);
                     mma_bf16_16816(acc[0], a0, a1, a2, a3, b0, b1);
                     mma_bf16_16816(acc[1], a0, a1, a2, a3, b2, b3);
@@ -1575,7 +1575,7 @@ __global__ void __launch_bounds__(kTileThreads, 1) bwd_token_b_tile(BwdProblem b
             const int y = u / 8, xx = u % 8;
             const bool live = r0 + y < p.H && c0 + xx < p.W;
             float q[8], dqt[8];
-            lds8_bf16(Qc + halo_row(u, 0, 0) * kQS + c8, q);
+            lds8_sw(Qc, halo_row(u, 0, 0), c8 >> 3, q);
 #pragma unroll
             for (int e = 0; e < 8; ++e) dqt[e] = oQ[u * kOS + c8 + e];
             const float rq = rqs[u];
@@ -1623,28 +1623,27 @@ __global__ void __launch_bounds__(kTileThreads, 1) bwd_token_b_tile(BwdProblem b
                 }
             const uint32_t arow_m = (uint32_t)((lane & 7) + 8 * ((lane >> 3) & 1));   // A-fragment row of this lane
             // scores [16 x 40] = rows(Ab) . rows(Bw)^T over the 64 channels
-            auto scores = [&](const __nv_bfloat16 *Ab, const __nv_bfloat16 *Bw, float (&sc)[5][4]) {
+            auto scores = [&](const uint8_t *Ab, const uint8_t *Bw, float (&sc)[5][4]) {
 #pragma unroll
                 for (int j = 0; j < 5; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
-                const uint32_t abase = smem_u32(Ab) + (uint32_t)hrow_b(arow_m) * kQS * 2u;
+                const int ar = hrow_b(arow_m);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
                     uint32_t a0, a1, a2, a3;
-                    ldsm_x4(abase + (uint32_t)((2 * ks + (lane >> 4)) * 8) * 2u, a0, a1, a2, a3);
+                    ldsm_x4(smem_u32(Ab) + hoff(ar, 2 * ks + (lane >> 4)), a0, a1, a2, a3);
 #pragma unroll
                     for (int pr = 0; pr < 3; ++pr) {
                         const int kk = 8 * (2 * pr + (lane >> 4)) + (lane & 7);
                         const int kk2 = kk < 40 ? kk : 0;
                         uint32_t b0, b1, b2, b3;
-                        ldsm_x4(smem_u32(Bw) + (uint32_t)(hrow_w(kk2) * kQS + (2 * ks + ((lane >> 3) & 1)) * 8) * 2u,
-                                b0, b1, b2, b3);
+                        ldsm_x4(smem_u32(Bw) + hoff(hrow_w(kk2), 2 * ks + ((lane >> 3) & 1)), b0, b1, b2, b3);
                         mma_bf16_16816(sc[2 * pr], a0, a1, a2, a3, b0, b1);
                         if (pr < 2) mma_bf16_16816(sc[2 * pr + 1], a0, a1, a2, a3, b2, b3);
                     }
                 }
             };
             // acc [16 x 64] = w [16 x 40] . rows(Xw) (w in C-fragment layout, rounded to bf16)
-            auto times_window = [&](const float (&w)[5][4], const __nv_bfloat16 *Xw, float (&acc)[8][4]) {
+            auto times_window = [&](const float (&w)[5][4], const uint8_t *Xw, float (&acc)[8][4]) {
 #pragma unroll
                 for (int nt = 0; nt < 8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
 #pragma unroll
@@ -1654,11 +1653,11 @@ __global__ void __launch_bounds__(kTileThreads, 1) bwd_token_b_tile(BwdProblem b
                     const uint32_t pa2 = j1 < 5 ? pack_bf16(w[j1][0], w[j1][1]) : 0u;
                     const uint32_t pa3 = j1 < 5 ? pack_bf16(w[j1][2], w[j1][3]) : 0u;
                     const int kv = 16 * ks + (lane & 7) + 8 * ((lane >> 3) & 1);
-                    const uint32_t vrow = smem_u32(Xw) + (uint32_t)hrow_w(kv < 40 ? kv : 0) * kQS * 2u;
+                    const int vr = hrow_w(kv < 40 ? kv : 0);
 #pragma unroll
                     for (int np = 0; np < 4; ++np) {
                         uint32_t b0, b1, b2, b3;
-                        ldsm_x4_t(vrow + (uint32_t)((2 * np + (lane >> 4)) * 8) * 2u, b0, b1, b2, b3);
+                        ldsm_x4_t(smem_u32(Xw) + hoff(vr, 2 * np + (lane >> 4)), b0, b1, b2, b3);
                         mma_bf16_16816(acc[2 * np], pa0, pa1, pa2, pa3, b0, b1);
                         mma_bf16_16816(acc[2 * np + 1], pa0, pa1, pa2, pa3, b2, b3);
                     }
@@ -1729,7 +1728,8 @@ __global__ void __launch_bounds__(kTileThreads, 1) bwd_token_b_tile(BwdProblem b
                         float d0 = oQ[ut * kOS + col] * rq - cj * s[col] + x0;
                         float d1 = oQ[ut * kOS + col + 1] * rq - cj * s[col + 1] + x1;
                         if (p.relu) {   // dXq through the feature map (the staged Q is ReLU'd)
-                            const uint32_t qp = *reinterpret_cast<const uint32_t *>(Qc + hrow_b(m) * kQS + col);
+                            const uint32_t qp =
+                                *reinterpret_cast<const uint32_t *>(Qc + hoff(hrow_b(m), col >> 3) + (col & 7) * 2);
                             if (!(bf16_lo(qp) > 0.f)) d0 = 0.f;
                             if (!(bf16_hi(qp) > 0.f)) d1 = 0.f;
                         }
@@ -1738,7 +1738,8 @@ __global__ void __launch_bounds__(kTileThreads, 1) bwd_token_b_tile(BwdProblem b
                         *reinterpret_cast<float2 *>(dKp + jt + col) =
                             make_float2(oK[ut * kOS + col] + x0, oK[ut * kOS + col + 1] + x1);
                     } else {
-                        const uint32_t gp = *reinterpret_cast<const uint32_t *>(Gc + hrow_b(m) * kQS + col);
+                        const uint32_t gp =
+                            *reinterpret_cast<const uint32_t *>(Gc + hoff(hrow_b(m), col >> 3) + (col & 7) * 2);
                         const float d0 = fmaf(w0 * al, bf16_lo(gp), oV[ut * kOS + col]) + x0;
                         const float d1 = fmaf(w0 * al, bf16_hi(gp), oV[ut * kOS + col + 1]) + x1;
                         *reinterpret_cast<uint32_t *>(dVo + jt + col) = pack_bf16(d0, d1);
@@ -2254,6 +2255,18 @@ __global__ void __launch_bounds__(kThreads) bwd_dalpha(BwdProblem b) {
     }
 }
 
+// 4-D map over the window statistics [S][H][W][4] fp32, box {4, 10, 10, 1}.
+bool make_map_stats(CUtensorMap *m, const float *lstat, const Problem &p) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[4] = {4, (cuuint64_t)p.W, (cuuint64_t)p.H, (cuuint64_t)p.slices};
+    cuuint64_t strides[3] = {16, (cuuint64_t)p.W * 16, (cuuint64_t)p.H * p.W * 16};
+    cuuint32_t box[4] = {4, (cuuint32_t)kHaloSide, (cuuint32_t)kHaloSide, 1}, es[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float *>(lstat), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <typename TIn, int D>
 cudaError_t launch_bwd_all(const BwdProblem &b, cudaStream_t st) {
     const Problem &p = b.fwd;
@@ -2298,9 +2311,18 @@ cudaError_t launch_bwd_all(const BwdProblem &b, cudaStream_t st) {
         if ((err = cudaFuncSetAttribute(bwd_token_b_tile, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         kTileSmemBytes)) != cudaSuccess)
             return err;
+        // tiled 4-D maps: 10 x 10 halo boxes of the inputs (128-byte swizzle) and of
+        // the window statistics ([S][H][W][4] fp32)
+        CUtensorMap mK, mV, mQ, mG, mL;
+        if (!make_map_grid(&mK, p.K, p.slices, p.H, p.W, kHaloSide, kHaloSide) ||
+            !make_map_grid(&mV, p.V, p.slices, p.H, p.W, kHaloSide, kHaloSide) ||
+            !make_map_grid(&mQ, p.Q, p.slices, p.H, p.W, kHaloSide, kHaloSide) ||
+            !make_map_grid(&mG, b.dO, p.slices, p.H, p.W, kHaloSide, kHaloSide) || !make_map_stats(&mL, b.lstat, p))
+            return cudaErrorInvalidValue;
         const long long ntiles = (long long)p.slices * b.ntile;
-        const unsigned grid = (unsigned)(ntiles < 152 ? ntiles : 152);   // persistent: one CTA per SM
-        bwd_token_b_tile<<<grid, kTileThreads, kTileSmemBytes, st>>>(b);
+        const int nsm = sm_count();
+        const unsigned grid = (unsigned)(ntiles < nsm ? ntiles : nsm);   // persistent: one CTA per SM
+        bwd_token_b_tile<<<grid, kTileThreads, kTileSmemBytes, st>>>(mK, mV, mQ, mG, mL, b);
     } else if (std::is_same<TIn, __nv_bfloat16>::value && D == 64 && p.relu != 2) {
         bwd_bimg<<<dim3((unsigned)p.slices, 5), kThreads, 0, st>>>(b);
         if ((err = cudaFuncSetAttribute(bwd_token_b_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
