@@ -1,7 +1,8 @@
 // lisa_bwd.cu -- backward pass of the LiSA layer (fixed walk weights, incl.
 // geometric and the untruncated walk): dL/dXq, dL/dXk, dL/dV, dL/dalpha for
-// an upstream gradient dO, fp32 arithmetic on CUDA cores, every dtype and
-// head width the forward serves.
+// an upstream gradient dO, every dtype and head width the forward serves:
+// fp32 on CUDA cores, and for bf16 at d = 64 the contractions on the tensor
+// cores (bf16 operands, fp32 accumulation).
 //
 // The chain rule through the forward's steps ("LiSA: Linear Stochastic
 // Attention for Long-Range Visual Modeling", reading note §2.1-2.4; paper
