@@ -241,6 +241,91 @@ __global__ void __launch_bounds__(kThreads) bwd_recur(BwdProblem b) {
 }
 
 // ---------------------------------------------------------------------------
+// 1' (d = 64, truncated walk, statistics from the tensor-core partials). Step
+// 1 split over four CTAs per slice: U_k^T = U_(k-1)^T M^T, so rows e0 .. e0 +
+// 15 of every U_k^T (columns of U_k) depend only on the same rows of U_1^T,
+// and each CTA carries its 16 rows through the whole recurrence (M^T reduced
+// by each).  CTA 0 of a slice also writes s and M.
+// ---------------------------------------------------------------------------
+constexpr int kRecurSplit = 4;
+
+__global__ void __launch_bounds__(kThreads) bwd_recur_rows(BwdProblem b) {
+    constexpr int D = 64, R = D / kRecurSplit;
+    __shared__ __align__(16) float Mt[D][D];   // M^T: Mt[c][a] = M[a][c]
+    __shared__ __align__(16) float Ut[R][D];   // this CTA's rows of U_k^T
+    __shared__ __align__(16) float Un[R][D];
+    const Problem &p = b.fwd;
+    const Problem &t = b.tcfwd;
+    const int sl = blockIdx.x / kRecurSplit, cb = blockIdx.x % kRecurSplit, e0 = R * cb, tid = threadIdx.x;
+    const int parts = t.chunks / t.tc_cluster;
+    const float *tp = t.tc_part + (size_t)sl * parts * 2 * D * D;
+    // partials: row e < 64 holds U_1[.][e] (a row of U_1^T), row 64 + c holds M[.][c] (a row of M^T)
+    for (int idx = tid; idx < D * D; idx += kThreads) {
+        float m = 0.f;
+        for (int q = 0; q < parts; ++q) m += tp[(size_t)q * 2 * D * D + D * D + idx];
+        Mt[idx / D][idx % D] = m;
+    }
+    for (int idx = tid; idx < R * D; idx += kThreads) {
+        float u = 0.f;
+        for (int q = 0; q < parts; ++q) u += tp[(size_t)q * 2 * D * D + e0 * D + idx];
+        Ut[idx / D][idx % D] = u;
+    }
+    if (cb == 0 && tid < D)
+        p.s_red[(size_t)sl * D + tid] = sum_partials(t.s_part + (size_t)sl * t.chunks * D, t.chunks, D, tid);
+    __syncthreads();
+    const size_t so = (size_t)sl * D * D;
+    if (cb == 0)
+        for (int idx = tid; idx < D * D; idx += kThreads)   // M row-major: strided global writes
+            b.Mred[so + (idx % D) * D + idx / D] = Mt[idx / D][idx % D];
+    // thread: row i of the block, columns a0 .. a0 + 3
+    const int i = tid >> 4, a0 = 4 * (tid & 15), e = e0 + i;
+    float ub[4];
+    float *Uk = b.Uk + (size_t)sl * b.nh * D * D;   // transposed: Uk[e][a] = U_k[a][e]
+    auto emit = [&](int k) {   // U_k's rows of this thread into the stored copies
+        const float4 u = *reinterpret_cast<const float4 *>(&Ut[i][a0]);
+        *reinterpret_cast<float4 *>(Uk + (size_t)(k - 1) * D * D + e * D + a0) = u;
+        if (b.mlp) {
+            float *Ukn = b.Ukn + ((size_t)sl * b.nh + (k - 1)) * D * D;
+            Ukn[(a0 + 0) * D + e] = u.x; Ukn[(a0 + 1) * D + e] = u.y;
+            Ukn[(a0 + 2) * D + e] = u.z; Ukn[(a0 + 3) * D + e] = u.w;
+        }
+        return u;
+    };
+    {
+        const float4 u = emit(1);
+        const float w1 = p.T > 1 ? p.w[1] : 0.f;
+        ub[0] = w1 * u.x; ub[1] = w1 * u.y; ub[2] = w1 * u.z; ub[3] = w1 * u.w;
+    }
+    for (int k = 2; k < p.T; ++k) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+        for (int c = 0; c < D; ++c) {
+            const float x = Ut[i][c];
+            const float4 m = *reinterpret_cast<const float4 *>(&Mt[c][a0]);
+            acc[0] = fmaf(x, m.x, acc[0]); acc[1] = fmaf(x, m.y, acc[1]);
+            acc[2] = fmaf(x, m.z, acc[2]); acc[3] = fmaf(x, m.w, acc[3]);
+        }
+        *reinterpret_cast<float4 *>(&Un[i][a0]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        __syncthreads();
+        *reinterpret_cast<float4 *>(&Ut[i][a0]) = *reinterpret_cast<const float4 *>(&Un[i][a0]);
+        __syncthreads();
+        const float4 u = emit(k);
+        ub[0] = fmaf(p.w[k], u.x, ub[0]); ub[1] = fmaf(p.w[k], u.y, ub[1]);
+        ub[2] = fmaf(p.w[k], u.z, ub[2]); ub[3] = fmaf(p.w[k], u.w, ub[3]);
+    }
+    // Ubar (row-major and transposed) and its bf16 hi + lo image
+    *reinterpret_cast<float4 *>(b.UbarT + so + e * D + a0) = make_float4(ub[0], ub[1], ub[2], ub[3]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int a = a0 + j;
+        b.Ubar[so + a * D + e] = ub[j];
+        const __nv_bfloat16 hi = __float2bfloat16_rn(ub[j]);
+        b.ubimg[so * 2 + a * D + e] = __bfloat16_as_ushort(hi);
+        b.ubimg[so * 2 + D * D + a * D + e] = __bfloat16_as_ushort(__float2bfloat16_rn(ub[j] - __bfloat162float(hi)));
+    }
+}
+
+// ---------------------------------------------------------------------------
 // 2. partial dUbar = sum_j Q~_j (alpha dO_j)^T over one chunk.
 // ---------------------------------------------------------------------------
 template <typename TIn, int D>
@@ -2281,7 +2366,10 @@ cudaError_t launch_bwd_all(const BwdProblem &b, cudaStream_t st) {
     }
     const unsigned grid_stats = (unsigned)p.slices * (unsigned)p.chunks;
     const unsigned grid_tok = (unsigned)p.slices * (unsigned)b.nblk;
-    bwd_recur<D><<<p.slices, kThreads, 0, st>>>(b);
+    if (D == 64 && b.tc_stats && !p.untruncated)
+        bwd_recur_rows<<<(unsigned)p.slices * kRecurSplit, kThreads, 0, st>>>(b);
+    else
+        bwd_recur<D><<<p.slices, kThreads, 0, st>>>(b);
     if (b.mlp) {   // per-token weights: the MLP's backward, then one dU_k per walk length
         bwd_token_mlp<TIn, D><<<grid_tok, kThreads, 0, st>>>(b);
         if (p.T > 1) bwd_stats_duk<TIn, D><<<dim3(grid_stats, (unsigned)(p.T - 1)), kThreads, 0, st>>>(b);
