@@ -224,8 +224,11 @@ lisa_status lisa_forward_noalloc(const void *Q, const void *K, const void *V, vo
  * Weights: LISA_W_GEOMETRIC (T >= 1, or T = 0 untruncated) and LISA_W_FIXED;
  * LISA_W_MLP returns LISA_ERR_UNSUPPORTED.  Outputs may not overlap each
  * other or any input.  Arithmetic is fp32 (bf16 inputs widened, bf16
- * outputs rounded to nearest even); every sum runs in a fixed order, so the
- * result is the same on every run.  The workspace (>= the bytes
+ * outputs rounded to nearest even), except that for bf16 at d = 64 with
+ * ReLU or no feature map the contractions run on the tensor cores with bf16
+ * operands (Q~, the window weights, the d x d matrices) and fp32
+ * accumulation; every sum runs in a fixed order, so the result is the same
+ * on every run.  The workspace (>= the bytes
  * lisa_backward_workspace_bytes returns, 16-byte aligned) needs no
  * initialisation.  Checks, statuses and stream behaviour as for
  * lisa_forward.  An empty problem (B * heads * H * W == 0) only zeroes
@@ -245,14 +248,16 @@ lisa_status lisa_backward(const void *Q, const void *K, const void *V, const voi
  * data) to about one second; a wait that gives up sets a bit in the error
  * word at the start of the call's workspace and the kernel finishes along
  * its normal path (every CTA still frees its tensor memory and drains its
- * bulk stores), leaving O undefined.  lisa_forward itself returns before the
- * kernels run, so it cannot see this.  lisa_query_status reads the word of
- * `workspace` (the one passed to the last lisa_forward call on it) after the
- * work queued on `stream` has finished: it synchronises `stream` and
- * returns LISA_ERR_TIMEOUT if any wait gave up, LISA_OK otherwise, or
- * LISA_ERR_CUDA if the read itself failed.  A null or misaligned workspace
- * is LISA_ERR_INVALID_ARG.  The next lisa_forward call on the workspace
- * clears the word again.
+ * bulk stores), leaving the outputs undefined.  The backward's tensor-core
+ * kernels do the same in the backward workspace.  lisa_forward and
+ * lisa_backward return before the kernels run, so they cannot see this.
+ * lisa_query_status reads the word of `workspace` (the one passed to the
+ * last lisa_forward or lisa_backward call on it) after the work queued on
+ * `stream` has finished: it synchronises `stream` and returns
+ * LISA_ERR_TIMEOUT if any wait gave up, LISA_OK otherwise, or LISA_ERR_CUDA
+ * if the read itself failed.  A null or misaligned workspace is
+ * LISA_ERR_INVALID_ARG.  The next call on the workspace clears the word
+ * again.
  */
 lisa_status lisa_query_status(const void *workspace, void *stream);
 
