@@ -1100,8 +1100,8 @@ __global__ void __launch_bounds__(kEpiThreads, kMinBlocks)
                     for (int r = 0; r < 4; ++r) {
                         // A register r: hidden columns of f8 = 2 kk + (r >> 1), row g (r even) or g + 8
                         const int hf = r >> 1, e = 2 * (r & 1);
-                        const float h0 = gelu_erf(__uint_as_float(hr[hf][e]) + __uint_as_float(bw[2 * hf]));
-                        const float h1 = gelu_erf(__uint_as_float(hr[hf][e + 1]) + __uint_as_float(bw[2 * hf + 1]));
+                        const float h0 = gelu_as7126(__uint_as_float(hr[hf][e]) + __uint_as_float(bw[2 * hf]));
+                        const float h1 = gelu_as7126(__uint_as_float(hr[hf][e + 1]) + __uint_as_float(bw[2 * hf + 1]));
                         ahi[r] = pack_bf16(h0, h1);
                         alo[r] = pack_bf16(h0 - bf16_lo(ahi[r]), h1 - bf16_hi(ahi[r]));
                     }

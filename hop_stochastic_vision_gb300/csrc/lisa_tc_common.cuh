@@ -265,6 +265,21 @@ __device__ __forceinline__ float gelu_erf(float x) {
     return 0.5f * x * (1.f + erff(x * 0.70710678118654752f));
 }
 
+// GELU(x) = x (1 + erf(x / sqrt 2)) / 2 with erf from Abramowitz & Stegun,
+// Handbook of Mathematical Functions, formula 7.1.26 (the formula's absolute
+// error is at most 1.5e-7; the approximate reciprocal and 2^x below add a few
+// fp32 ulps): for z >= 0, erf(z) = 1 - t (a1 + t (a2 + t (a3 + t (a4 + t a5))))
+// exp(-z^2), t = 1 / (1 + p z); erf is odd.  Used by the adaptive-weight
+// epilogue, where it replaces erff's longer evaluation on the per-token path.
+__device__ __forceinline__ float gelu_as7126(float x) {
+    const float z = fabsf(x) * 0.70710678118654752f;
+    const float t = __fdividef(1.f, fmaf(0.3275911f, z, 1.f));
+    const float poly =
+        t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, 1.061405429f, -1.453152027f), 1.421413741f), -0.284496736f), 0.254829592f);
+    const float erf_abs = fmaf(-poly, ex2_approx(-z * z * 1.4426950408889634f), 1.f);
+    return 0.5f * x * (1.f + copysignf(erf_abs, x));
+}
+
 // 16 TMEM lanes x 8 consecutive fp32 columns per repetition, in mma.sync
 // C-fragment layout: regs 4r+0,1 = (row g, cols 8r+2q, +1), 4r+2,3 = (row g+8, same).
 __device__ __forceinline__ void tmem_ld_frag8_nowait(uint32_t taddr, uint32_t (&r)[32]) {
