@@ -1843,6 +1843,373 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     }
 }
 
+// ---------------------------------------------------------------------------
+// 3a'. bf16, d = 64, adaptive weights: step 3a with its three products on the
+// tensor cores, per block of 32 tokens (mma.sync, bf16 operands, fp32
+// accumulation; W1, U_k and da enter as bf16 hi + lo terms, Q and K are exact
+// in bf16): the hidden pre-activations [Q | K] W1^T, the walk terms
+// Y_k = Q U_k (k = 1 .. T-1, one U_k image at a time, folded into g and the
+// dw partials as they come out), and the MLP's share of [dq; dk] = da W1.
+// The softmax, the window and the MLP's elementwise backward stay per token.
+// ---------------------------------------------------------------------------
+constexpr int kMA = 136;                 // [Q | K] and W1 image row stride (bf16): 128 channels + pad
+constexpr int kMH = LISA_MAX_HIDDEN;     // hidden units held (a multiple of 16)
+constexpr int kMlpTcSmemBytes = kTpb * kMA * 2              // [Q | K] rows
+                                + 2 * kMH * kMA * 2         // W1 hi, lo
+                                + 2 * 64 * kQS * 2          // U_k hi, lo
+                                + 2 * kTpb * kQS * 2        // da hi, lo
+                                + 3 * kTpb * 68 * 4         // pre-activations (then da), g, V and dO rows (fp32)
+                                + kTpb * 68 * 4;
+
+__global__ void __launch_bounds__(kThreads) bwd_token_mlp_tc(BwdProblem b) {
+    constexpr int D = 64, TM = LISA_MAX_T_MLP;
+    using namespace sm100;
+    extern __shared__ float4 smem_mlp[];
+    __nv_bfloat16 *Qk = reinterpret_cast<__nv_bfloat16 *>(smem_mlp);   // [kTpb][kMA]: Q | K
+    __nv_bfloat16 *W1i = Qk + kTpb * kMA;                              // [2][kMH][kMA]
+    __nv_bfloat16 *Ui = W1i + 2 * kMH * kMA;                           // [2][64][kQS]
+    __nv_bfloat16 *Di = Ui + 2 * 64 * kQS;                             // [2][kTpb][kQS]: da hi, lo
+    float *pre = reinterpret_cast<float *>(Di + 2 * kTpb * kQS);      // [kTpb][68]
+    float *G = pre + kTpb * 68;                                        // [kTpb][68]: g without w_0 V
+    float *Vs = G + kTpb * 68;                                         // [kTpb][68]: V rows
+    float *Gs = Vs + kTpb * 68;                                        // [kTpb][68]: dO rows
+    __shared__ float rqs[kTpb];
+    __shared__ float wts[kTpb][TM];
+    __shared__ float dwp[TM][kTpb][4];    // dw_k partials per row and 16-column group
+    __shared__ float part[kWarps];
+    const Problem &p = b.fwd;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int sl = blockIdx.x / b.nblk, blk = blockIdx.x % b.nblk;
+    const int j0 = blk * kTpb, cnt = min(kTpb, p.n - j0);
+    const int T = p.T, hid = p.hidden, nmh = (hid + 15) / 16 * 16;
+    const size_t sbase = (size_t)sl * p.n * D;
+    const __nv_bfloat16 *Q = static_cast<const __nv_bfloat16 *>(p.Q) + sbase;
+    const __nv_bfloat16 *K = static_cast<const __nv_bfloat16 *>(p.K) + sbase;
+    const __nv_bfloat16 *V = static_cast<const __nv_bfloat16 *>(p.V) + sbase;
+    const __nv_bfloat16 *dO = static_cast<const __nv_bfloat16 *>(b.dO) + sbase;
+    const float *s = p.s_red + (size_t)sl * D;
+    const float al = p.alpha[sl % p.heads];
+
+    // ---- stage [Q | K] (feature-mapped), V and dO rows (fp32), W1 as bf16 hi + lo
+    for (int x = tid; x < kTpb * 8; x += kThreads) {
+        const int j = x >> 3, c = x & 7;
+        uint4 q = make_uint4(0u, 0u, 0u, 0u), k = q, v = q, g = q;
+        if (j < cnt) {
+            const size_t o = ((size_t)(j0 + j) * D) / 8 + c;
+            q = reinterpret_cast<const uint4 *>(Q)[o];
+            k = reinterpret_cast<const uint4 *>(K)[o];
+            v = reinterpret_cast<const uint4 *>(V)[o];
+            g = reinterpret_cast<const uint4 *>(dO)[o];
+            if (p.relu) {
+                q = make_uint4(relu_bf16x2(q.x), relu_bf16x2(q.y), relu_bf16x2(q.z), relu_bf16x2(q.w));
+                k = make_uint4(relu_bf16x2(k.x), relu_bf16x2(k.y), relu_bf16x2(k.z), relu_bf16x2(k.w));
+            }
+        }
+        *reinterpret_cast<uint4 *>(Qk + j * kMA + c * 8) = q;
+        *reinterpret_cast<uint4 *>(Qk + j * kMA + 64 + c * 8) = k;
+        const uint32_t vv[4] = {v.x, v.y, v.z, v.w}, gg[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            Vs[j * 68 + c * 8 + 2 * e] = bf16_lo(vv[e]);
+            Vs[j * 68 + c * 8 + 2 * e + 1] = bf16_hi(vv[e]);
+            Gs[j * 68 + c * 8 + 2 * e] = bf16_lo(gg[e]);
+            Gs[j * 68 + c * 8 + 2 * e + 1] = bf16_hi(gg[e]);
+        }
+    }
+    for (int x = tid; x < nmh * 2 * D; x += kThreads) {
+        const int m = x / (2 * D), c = x % (2 * D);
+        const float w = m < hid ? p.W1[(size_t)m * 2 * D + c] : 0.f;
+        const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+        W1i[m * kMA + c] = hi;
+        W1i[kMH * kMA + m * kMA + c] = __float2bfloat16_rn(w - __bfloat162float(hi));
+    }
+    for (int x = tid; x < TM * kTpb * 4; x += kThreads) (&dwp[0][0][0])[x] = 0.f;
+    __syncthreads();
+    for (int j = warp; j < kTpb; j += kWarps) {   // 1 / (Q_j . s + eps)
+        float d = 0.f;
+        for (int ch = lane; ch < D; ch += 32) d += __bfloat162float(Qk[j * kMA + ch]) * s[ch];
+        d = warp_sum(d);
+        if (lane == 0) rqs[j] = 1.f / (d + p.eps);
+    }
+
+    // ---- hidden pre-activations [Q | K] W1^T + b1: warp = 16 tokens x 16 hidden units
+    {
+        const int mt = warp & 1, pr = warp >> 1;   // n-tiles 2 pr, 2 pr + 1
+        if (16 * pr < nmh) {
+            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            const uint32_t qa = smem_u32(Qk) + (uint32_t)((16 * mt + (lane & 15)) * kMA + (lane >> 4) * 8) * 2u;
+            const int wrow = 16 * pr + (lane & 7) + 8 * (lane >> 4);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(qa + (uint32_t)(16 * ks) * 2u, a0, a1, a2, a3);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(smem_u32(W1i) + (uint32_t)(h * kMH * kMA + wrow * kMA + 16 * ks + ((lane >> 3) & 1) * 8) * 2u,
+                            b0, b1, b2, b3);
+                    mma_bf16_16816(acc[0], a0, a1, a2, a3, b0, b1);
+                    mma_bf16_16816(acc[1], a0, a1, a2, a3, b2, b3);
+                }
+            }
+            const int row = 16 * mt + (lane >> 2);
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int m = 16 * pr + 8 * nt + 2 * (lane & 3);
+                const float b10 = m < hid ? p.b1[m] : 0.f, b11 = m + 1 < hid ? p.b1[m + 1] : 0.f;
+                pre[row * 68 + m] = acc[nt][0] + b10;
+                pre[row * 68 + m + 1] = acc[nt][1] + b11;
+                pre[(row + 8) * 68 + m] = acc[nt][2] + b10;
+                pre[(row + 8) * 68 + m + 1] = acc[nt][3] + b11;
+            }
+        }
+    }
+    __syncthreads();
+    // ---- per token: h = GELU(a), z = W2 h + b2, w = softmax(z) (warp per token)
+    for (int u = warp; u < kTpb; u += kWarps) {
+        float zt[TM];
+#pragma unroll
+        for (int t = 0; t < TM; ++t) zt[t] = 0.f;
+        for (int m = lane; m < hid; m += 32) {
+            const float h = gelu_exact(pre[u * 68 + m]);
+#pragma unroll
+            for (int t = 0; t < TM; ++t)
+                if (t < T) zt[t] = fmaf(p.W2[(size_t)t * hid + m], h, zt[t]);
+            if (u < cnt) b.hbuf[((size_t)sl * p.n + j0 + u) * hid + m] = h;
+        }
+        warp_sum_n(zt);
+        float zmax = -INFINITY, zs = 0.f;
+#pragma unroll
+        for (int t = 0; t < TM; ++t)
+            if (t < T) {
+                zt[t] += p.b2[t];
+                zmax = fmaxf(zmax, zt[t]);
+            }
+#pragma unroll
+        for (int t = 0; t < TM; ++t)
+            if (t < T) {
+                zt[t] = expf(zt[t] - zmax);
+                zs += zt[t];
+            }
+        if (lane < T) {
+            float wl = 0.f;
+#pragma unroll
+            for (int t = 0; t < TM; ++t)
+                if (t == lane) wl = zt[t] / zs;
+            wts[u][lane] = wl;
+        }
+    }
+    __syncthreads();
+
+    // ---- walk terms Y_k = Q U_k on the tensor cores; g = sum_k w_k Y_k rq, and
+    // dw_k partials alpha dO . Y_k rq per row and 16-column group
+    {
+        const int mt = warp & 1, sb = warp >> 1;
+        const uint32_t qa = smem_u32(Qk) + (uint32_t)((16 * mt + (lane & 15)) * kMA + (lane >> 4) * 8) * 2u;
+        const int mi = lane >> 3, brow = (mi & 1) * 8 + (lane & 7), bcol = 16 * sb + (mi >> 1) * 8;
+        const int r0 = 16 * mt + (lane >> 2);
+        float gacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        for (int kk = 1; kk < T; ++kk) {
+            // U_k (fp32, row-major) as bf16 hi + lo
+            const float *Un = b.Ukn + ((size_t)sl * b.nh + (kk - 1)) * D * D;
+            for (int x = tid; x < D * D; x += kThreads) {
+                const float uv = Un[x];
+                const __nv_bfloat16 hi = __float2bfloat16_rn(uv);
+                Ui[(x >> 6) * kQS + (x & 63)] = hi;
+                Ui[64 * kQS + (x >> 6) * kQS + (x & 63)] = __float2bfloat16_rn(uv - __bfloat162float(hi));
+            }
+            __syncthreads();
+            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(qa + (uint32_t)(16 * ks) * 2u, a0, a1, a2, a3);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(smem_u32(Ui) + (uint32_t)((h * 64 + 16 * ks + brow) * kQS + bcol) * 2u, b0, b1, b2, b3);
+                    mma_bf16_16816(acc[0], a0, a1, a2, a3, b0, b1);
+                    mma_bf16_16816(acc[1], a0, a1, a2, a3, b2, b3);
+                }
+            }
+            float dwr[2] = {0.f, 0.f};   // rows r0, r0 + 8
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int row = r0 + 8 * h;
+                const float rq = rqs[row], wk = wts[row][kk];
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int col = 16 * sb + 8 * nt + 2 * (lane & 3);
+                    const float y0 = acc[nt][2 * h] * rq, y1 = acc[nt][2 * h + 1] * rq;
+                    gacc[nt][2 * h] = fmaf(wk, y0, gacc[nt][2 * h]);
+                    gacc[nt][2 * h + 1] = fmaf(wk, y1, gacc[nt][2 * h + 1]);
+                    dwr[h] = fmaf(Gs[row * 68 + col], y0, fmaf(Gs[row * 68 + col + 1], y1, dwr[h]));
+                }
+                dwr[h] += __shfl_xor_sync(0xffffffffu, dwr[h], 1);
+                dwr[h] += __shfl_xor_sync(0xffffffffu, dwr[h], 2);
+            }
+            if ((lane & 3) == 0) {
+                dwp[kk][r0][sb] = al * dwr[0];
+                dwp[kk][r0 + 8][sb] = al * dwr[1];
+            }
+            __syncthreads();   // every read of this U_k image is done
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int col = 16 * sb + 8 * nt + 2 * (lane & 3);
+                G[(r0 + 8 * h) * 68 + col] = gacc[nt][2 * h];
+                G[(r0 + 8 * h) * 68 + col + 1] = gacc[nt][2 * h + 1];
+            }
+    }
+    __syncthreads();
+
+    // ---- per token (warp): the window (as bwd_token_a), dalpha terms, the
+    // softmax's and the MLP's elementwise backward; da into pre's place
+    float dal = 0.f;
+    for (int u = warp; u < cnt; u += kWarps) {
+        const int i = j0 + u;
+        float q[2], v[2], go[2], g[2];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const int ch = lane + 32 * t;
+            q[t] = __bfloat162float(Qk[u * kMA + ch]);
+            v[t] = Vs[u * 68 + ch];
+            go[t] = Gs[u * 68 + ch];
+            g[t] = fmaf(wts[u][0], v[t], G[u * 68 + ch]);
+        }
+        int nb[9];
+        const int nn = window(i, p.H, p.W, nb);
+        float kr[9][2], vr[9][2], e[9];
+#pragma unroll
+        for (int t9 = 0; t9 < 9; ++t9) {
+            const int row = t9 < nn ? nb[t9] : i;
+            load_row<__nv_bfloat16, D>(K + (size_t)row * D, kr[t9], lane, p.relu);
+            load_row<__nv_bfloat16, D>(V + (size_t)row * D, vr[t9], lane, 0);
+            e[t9] = fmaf(q[0], kr[t9][0], q[1] * kr[t9][1]);
+        }
+        warp_sum_n(e);
+        float emax = -INFINITY;
+#pragma unroll
+        for (int t9 = 0; t9 < 9; ++t9)
+            if (t9 < nn) emax = fmaxf(emax, e[t9] * 0.125f);
+        float l[2] = {0.f, 0.f}, esum = 0.f;
+#pragma unroll
+        for (int t9 = 0; t9 < 9; ++t9) {
+            if (t9 >= nn) break;
+            const float a = expf(e[t9] * 0.125f - emax);
+            esum += a;
+            l[0] = fmaf(a, vr[t9][0], l[0]);
+            l[1] = fmaf(a, vr[t9][1], l[1]);
+        }
+        const float inv = 1.f / esum;
+        float red[3] = {0.f, 0.f, 0.f};
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            l[t] *= inv;
+            red[0] = fmaf(go[t], g[t] - l[t], red[0]);
+            red[1] = fmaf(go[t], l[t], red[1]);
+            red[2] = fmaf(go[t], v[t], red[2]);   // dw_0 / alpha
+        }
+        warp_sum_n(red);
+        dal += red[0];
+        const size_t ti = (size_t)sl * p.n + i;
+        if (lane == 0) reinterpret_cast<float4 *>(b.lstat)[ti] = make_float4(emax, esum, red[1] * (1.f - al), 0.f);
+        // dz = w (dw - w . dw), dw_0 = alpha dO . V, dw_k from the partials
+        float w[TM], dw[TM], wdw = 0.f;
+#pragma unroll
+        for (int t = 0; t < TM; ++t) {
+            w[t] = t < T ? wts[u][t] : 0.f;
+            dw[t] = t == 0 ? al * red[2]
+                           : (t < T ? ((dwp[t][u][0] + dwp[t][u][1]) + (dwp[t][u][2] + dwp[t][u][3])) : 0.f);
+            wdw = fmaf(w[t], dw[t], wdw);
+        }
+        float dz[TM];
+#pragma unroll
+        for (int t = 0; t < TM; ++t) dz[t] = w[t] * (dw[t] - wdw);
+        if (lane < T) {
+            float wl = 0.f, dzl = 0.f;
+#pragma unroll
+            for (int t = 0; t < TM; ++t)
+                if (t == lane) {
+                    wl = w[t];
+                    dzl = dz[t];
+                }
+            b.wtok[ti * T + lane] = wl;
+            b.dzbuf[ti * T + lane] = dzl;
+        }
+        for (int m = lane; m < nmh; m += 32) {
+            float da = 0.f;
+            if (m < hid) {
+                float dh = 0.f;
+#pragma unroll
+                for (int t = 0; t < TM; ++t)
+                    if (t < T) dh = fmaf(p.W2[(size_t)t * hid + m], dz[t], dh);
+                da = dh * gelu_exact_grad(pre[u * 68 + m]);
+                b.dabuf[ti * hid + m] = da;
+            }
+            const __nv_bfloat16 hi = __float2bfloat16_rn(da);
+            Di[u * kQS + m] = hi;
+            Di[kTpb * kQS + u * kQS + m] = __float2bfloat16_rn(da - __bfloat162float(hi));
+        }
+    }
+    for (int u = cnt + warp; u < kTpb; u += kWarps)   // rows past the slice's end: no da
+        for (int m = lane; m < nmh; m += 32) {
+            Di[u * kQS + m] = __float2bfloat16_rn(0.f);
+            Di[kTpb * kQS + u * kQS + m] = __float2bfloat16_rn(0.f);
+        }
+    if (lane == 0) part[warp] = dal;
+    __syncthreads();
+    if (tid == 0) {
+        float acc = 0.f;
+        for (int w2 = 0; w2 < kWarps; ++w2) acc += part[w2];
+        b.dal_part[(size_t)sl * b.nblk + blk] = acc;
+    }
+
+    // ---- the MLP's share of [dq | dk] = da W1: warp = 16 tokens x 32 channels
+    {
+        const int mt = warp & 1, cg = warp >> 1;   // channels 32 cg .. 32 cg + 31
+        const uint32_t da0 = smem_u32(Di) + (uint32_t)((16 * mt + (lane & 15)) * kQS + (lane >> 4) * 8) * 2u;
+        const int mi = lane >> 3, brow = (mi & 1) * 8 + (lane & 7);
+        float acc[4][4];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+        for (int ks = 0; 16 * ks < nmh; ++ks) {
+#pragma unroll
+            for (int ah = 0; ah < 2; ++ah) {   // da hi, lo
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(da0 + (uint32_t)(ah * kTpb * kQS + 16 * ks) * 2u, a0, a1, a2, a3);
+#pragma unroll
+                for (int wh = 0; wh < 2; ++wh) {   // W1 hi, lo (lo x lo left out)
+                    if (ah == 1 && wh == 1) continue;
+#pragma unroll
+                    for (int np = 0; np < 2; ++np) {
+                        const int bcol = 32 * cg + 16 * np + (mi >> 1) * 8;
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4_t(smem_u32(W1i) + (uint32_t)(wh * kMH * kMA + (16 * ks + brow) * kMA + bcol) * 2u,
+                                  b0, b1, b2, b3);
+                        mma_bf16_16816(acc[2 * np], a0, a1, a2, a3, b0, b1);
+                        mma_bf16_16816(acc[2 * np + 1], a0, a1, a2, a3, b2, b3);
+                    }
+                }
+            }
+        }
+        const int row = 16 * mt + (lane >> 2);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int u = row + 8 * h;
+            if (u >= cnt) continue;
+            float *xm = b.dxm + ((size_t)sl * p.n + j0 + u) * 2 * D;
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                const int c = 32 * cg + 8 * nt + 2 * (lane & 3);
+                *reinterpret_cast<float2 *>(xm + c) = make_float2(acc[nt][2 * h], acc[nt][2 * h + 1]);
+            }
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kThreads) bwd_token_b_tc(BwdProblem b) {
     constexpr int D = 64, NC = 2;
     using namespace sm100;
@@ -2250,7 +2617,14 @@ cudaError_t launch_bwd_all(const BwdProblem &b, cudaStream_t st) {
     else
         bwd_recur<D><<<p.slices, kThreads, 0, st>>>(b);
     if (b.mlp) {   // per-token weights: the MLP's backward, then one dU_k per walk length
-        bwd_token_mlp<TIn, D><<<grid_tok, kThreads, 0, st>>>(b);
+        if (std::is_same<TIn, __nv_bfloat16>::value && D == 64 && p.relu != 2) {
+            if ((err = cudaFuncSetAttribute(bwd_token_mlp_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            kMlpTcSmemBytes)) != cudaSuccess)
+                return err;
+            bwd_token_mlp_tc<<<grid_tok, kThreads, kMlpTcSmemBytes, st>>>(b);
+        } else {
+            bwd_token_mlp<TIn, D><<<grid_tok, kThreads, 0, st>>>(b);
+        }
         if (p.T > 1) bwd_stats_duk<TIn, D><<<dim3(grid_stats, (unsigned)(p.T - 1)), kThreads, 0, st>>>(b);
     } else {
         if (b.tc_dub) {   // dUbar / alpha = Q~^T dO: the statistics kernel with dO as its V and K
