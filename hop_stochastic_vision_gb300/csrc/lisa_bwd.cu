@@ -2310,6 +2310,66 @@ __global__ void __launch_bounds__(kThreads) bwd_token_b_tc(BwdProblem b) {
     }
     __syncthreads();
 
+    // ---- adaptive weights: the token's own walk terms, which the block's shared
+    // products leave out: dV_j += w_j0 alpha dO_j and dQ~_j += alpha sum_{k>=1}
+    // w_jk dO_j U_k^T, the latter as (alpha dO) U_k^T on mma.sync per k (U_k^T
+    // as bf16 hi + lo, staged where the B image was), each token's row scaled
+    // by its own w_jk
+    if (b.mlp) {
+        __shared__ float wts_s[kTpb][LISA_MAX_T_MLP];
+        const int T = p.T;
+        for (int x = tid; x < kTpb * T; x += kThreads) {
+            const int j = x / T, t = x % T;
+            wts_s[j][t] = j < cnt ? b.wtok[((size_t)sl * p.n + j0 + j) * T + t] : 0.f;
+        }
+        __syncthreads();
+        for (int x = tid; x < kTpb * D; x += kThreads) {
+            const int j = x / D, ch = x % D;
+            oV[j * D + ch] = fmaf(wts_s[j][0] * al, __bfloat162float(A1[j * kAS + ch]), oV[j * D + ch]);
+        }
+        __nv_bfloat16 *Ui = Bs;   // the B image is no longer read
+        const int mt = warp & 1, sb = warp >> 1;
+        const uint32_t ga = smem_u32(A1) + (uint32_t)((16 * mt + (lane & 15)) * kAS + (lane >> 4) * 8) * 2u;
+        const int mi = lane >> 3, brow = (mi & 1) * 8 + (lane & 7), bcol = 16 * sb + (mi >> 1) * 8;
+        const int r0 = 16 * mt + (lane >> 2);
+        for (int kk = 1; kk < T; ++kk) {
+            const float *UT = b.Uk + ((size_t)sl * b.nh + (kk - 1)) * D * D;   // UT[c][a] = U_k[a][c]
+            __syncthreads();   // the products (or the previous k) no longer read this region
+            for (int x = tid; x < D * D; x += kThreads) {
+                const float uv = UT[x];
+                const __nv_bfloat16 hi = __float2bfloat16_rn(uv);
+                Ui[(x >> 6) * kQS + (x & 63)] = hi;
+                Ui[64 * kQS + (x >> 6) * kQS + (x & 63)] = __float2bfloat16_rn(uv - __bfloat162float(hi));
+            }
+            __syncthreads();
+            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(ga + (uint32_t)(16 * ks) * 2u, a0, a1, a2, a3);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(smem_u32(Ui) + (uint32_t)((h * 64 + 16 * ks + brow) * kQS + bcol) * 2u, b0, b1, b2, b3);
+                    mma_bf16_16816(acc[0], a0, a1, a2, a3, b0, b1);
+                    mma_bf16_16816(acc[1], a0, a1, a2, a3, b2, b3);
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int row = r0 + 8 * h;
+                const float wk = al * wts_s[row][kk];
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int col = 16 * sb + 8 * nt + 2 * (lane & 3);
+                    oQ[row * D + col] = fmaf(wk, acc[nt][2 * h], oQ[row * D + col]);
+                    oQ[row * D + col + 1] = fmaf(wk, acc[nt][2 * h + 1], oQ[row * D + col + 1]);
+                }
+            }
+        }
+        __syncthreads();
+    }
+
     // ---- one warp per token: normaliser, window, stores (as in the SIMT kernel);
     // the adaptive weights come here, fixed weights take the tiled pass
     float ds[NC] = {0.f, 0.f};
@@ -2328,7 +2388,6 @@ __global__ void __launch_bounds__(kThreads) bwd_token_b_tc(BwdProblem b) {
             dv[t] = fmaf(w0 * al, go[t], oV[u * D + ch]);
             dk[t] = oK[u * D + ch];
         }
-        if (b.mlp) mlp_walk_terms<D>(b, sl, j, lane, al, go, dqt, dv);
         const float rq = rqs[u];
         const float cj = dot_row<D>(dqt, q) * rq * rq;
         float dq[NC];
