@@ -2370,107 +2370,136 @@ __global__ void __launch_bounds__(kThreads) bwd_token_b_tc(BwdProblem b) {
         __syncthreads();
     }
 
-    // ---- one warp per token: normaliser, window, stores (as in the SIMT kernel);
-    // the adaptive weights come here, fixed weights take the tiled pass
-    float ds[NC] = {0.f, 0.f};
-    for (int u = warp; u < cnt; u += kWarps) {
-        const int j = j0 + u;
-        float q[NC], k[NC], v[NC], go[NC], sv[NC], dqt[NC], dv[NC], dk[NC];
+    // ---- a quarter-warp per token (eight lanes, eight channels each):
+    // normaliser, the MLP's share, window, stores
+    const int qg = lane >> 3, c8 = 8 * (lane & 7);
+    const int u = 4 * warp + qg;
+    const bool live = u < cnt;
+    const int j = j0 + (live ? u : 0);
+    float q[8], go[8], k[8], v[8], dqt[8], dv[8], dk[8];
 #pragma unroll
-        for (int t = 0; t < NC; ++t) {
-            const int ch = lane + 32 * t;
-            q[t] = __bfloat162float(Qb[u * D + ch]);
-            go[t] = __bfloat162float(A1[u * kAS + ch]);
-            k[t] = __bfloat162float(A1[u * kAS + 64 + ch]);
-            v[t] = __bfloat162float(A3[u * kAS + ch]);
-            sv[t] = s[ch];
-            dqt[t] = oQ[u * D + ch];
-            dv[t] = fmaf(w0 * al, go[t], oV[u * D + ch]);
-            dk[t] = oK[u * D + ch];
-        }
-        const float rq = rqs[u];
-        const float cj = dot_row<D>(dqt, q) * rq * rq;
-        float dq[NC];
+    for (int e = 0; e < 8; ++e) {
+        q[e] = __bfloat162float(Qb[u * D + c8 + e]);
+        go[e] = __bfloat162float(A1[u * kAS + c8 + e]);
+        k[e] = __bfloat162float(A1[u * kAS + 64 + c8 + e]);
+        v[e] = __bfloat162float(A3[u * kAS + c8 + e]);
+        dqt[e] = oQ[u * D + c8 + e];
+        dv[e] = fmaf(w0 * al, go[e], oV[u * D + c8 + e]);
+        dk[e] = oK[u * D + c8 + e];
+    }
+    const float rq = rqs[u];
+    const float cj = group8_sum(dot8(dqt, q)) * rq * rq;
+    float dq[8], dsl[8];
 #pragma unroll
-        for (int t = 0; t < NC; ++t) {
-            dq[t] = dqt[t] * rq - cj * sv[t];
-            ds[t] = fmaf(-cj, q[t], ds[t]);
-        }
-        if (b.mlp) {   // the MLP's share of dq_j, dk_j
-            const float *xm = b.dxm + ((size_t)sl * p.n + j) * 2 * D;
+    for (int e = 0; e < 8; ++e) {
+        dq[e] = dqt[e] * rq - cj * s[c8 + e];
+        dsl[e] = live ? -cj * q[e] : 0.f;
+    }
+    {   // the MLP's share of dq_j, dk_j
+        const float4 *xm = reinterpret_cast<const float4 *>(b.dxm + ((size_t)sl * p.n + j) * 2 * D + c8);
+        const float4 x0 = xm[0], x1 = xm[1], x2 = xm[16], x3 = xm[17];
+        const float xq[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        const float xk[8] = {x2.x, x2.y, x2.z, x2.w, x3.x, x3.y, x3.z, x3.w};
 #pragma unroll
-            for (int t = 0; t < NC; ++t) {
-                dq[t] += xm[lane + 32 * t];
-                dk[t] += xm[D + lane + 32 * t];
-            }
-        }
-        int nb[9];
-        const int nn = window(j, p.H, p.W, nb);
-        const float4 sj = lst[j];
-        const float izj = 1.f / sj.y;
-        {
-            float kr[9][NC], vr[9][NC], d1[18];
-#pragma unroll
-            for (int t9 = 0; t9 < 9; ++t9) {
-                const int row = t9 < nn ? nb[t9] : j;
-                load_row<__nv_bfloat16, D>(K + (size_t)row * D, kr[t9], lane, p.relu);
-                load_row<__nv_bfloat16, D>(V + (size_t)row * D, vr[t9], lane, 0);
-                d1[t9] = d1[9 + t9] = 0.f;
-#pragma unroll
-                for (int t = 0; t < NC; ++t) {
-                    d1[t9] = fmaf(q[t], kr[t9][t], d1[t9]);
-                    d1[9 + t9] = fmaf(go[t], vr[t9][t], d1[9 + t9]);
-                }
-            }
-            warp_sum_n(d1);
-#pragma unroll
-            for (int t9 = 0; t9 < 9; ++t9) {
-                if (t9 >= nn) break;
-                const float a = expf(d1[t9] * scale - sj.x) * izj;
-                const float de = a * (d1[9 + t9] * (1.f - al) - sj.z) * scale;
-#pragma unroll
-                for (int t = 0; t < NC; ++t) dq[t] = fmaf(de, kr[t9][t], dq[t]);
-            }
-        }
-        {
-            float qi[9][NC], gi[9][NC], d2[18];
-#pragma unroll
-            for (int t9 = 0; t9 < 9; ++t9) {
-                const int row = t9 < nn ? nb[t9] : j;
-                load_row<__nv_bfloat16, D>(Q + (size_t)row * D, qi[t9], lane, p.relu);
-                load_row<__nv_bfloat16, D>(dO + (size_t)row * D, gi[t9], lane, 0);
-                d2[t9] = d2[9 + t9] = 0.f;
-#pragma unroll
-                for (int t = 0; t < NC; ++t) {
-                    d2[t9] = fmaf(qi[t9][t], k[t], d2[t9]);
-                    d2[9 + t9] = fmaf(gi[t9][t], v[t], d2[9 + t9]);
-                }
-            }
-            warp_sum_n(d2);
-#pragma unroll
-            for (int t9 = 0; t9 < 9; ++t9) {
-                if (t9 >= nn) break;
-                const float4 si = lst[nb[t9]];
-                const float a = expf(d2[t9] * scale - si.x) / si.y;
-                const float de = a * (d2[9 + t9] * (1.f - al) - si.z) * scale;
-#pragma unroll
-                for (int t = 0; t < NC; ++t) {
-                    dv[t] = fmaf(a * (1.f - al), gi[t9][t], dv[t]);
-                    dk[t] = fmaf(de, qi[t9][t], dk[t]);
-                }
-            }
-        }
-#pragma unroll
-        for (int t = 0; t < NC; ++t) {
-            const int ch = lane + 32 * t;
-            const float xq = __bfloat162float(Q[(size_t)j * D + ch]);
-            dQo[(size_t)j * D + ch] = __float2bfloat16_rn((p.relu && !(xq > 0.f)) ? 0.f : dq[t]);
-            dVo[(size_t)j * D + ch] = __float2bfloat16_rn(dv[t]);
-            dKp[(size_t)j * D + ch] = dk[t];
+        for (int e = 0; e < 8; ++e) {
+            dq[e] += xq[e];
+            dk[e] += xk[e];
         }
     }
+    const int r = j / p.W, c = j % p.W;
+    const float4 sj = lst[j];
+    const float izj = 1.f / sj.y;
+    // j as the query: scores against its window, dl_j . V_i
+    {
+        float d1[18];
 #pragma unroll
-    for (int t = 0; t < NC; ++t) dsw[warp][lane + 32 * t] = ds[t];
+        for (int t9 = 0; t9 < 9; ++t9) {
+            const int rr = r + t9 / 3 - 1, cc = c + t9 % 3 - 1;
+            const bool in = rr >= 0 && rr < p.H && cc >= 0 && cc < p.W;
+            const size_t row = (size_t)(in ? rr * p.W + cc : j) * D + c8;
+            float kr[8], vr[8];
+            load8_bf16(K + row, kr, p.relu);
+            load8_bf16(V + row, vr, false);
+            d1[t9] = dot8(q, kr);
+            d1[9 + t9] = dot8(go, vr);
+        }
+#pragma unroll
+        for (int t = 0; t < 18; ++t) d1[t] = group8_sum(d1[t]);
+#pragma unroll
+        for (int t9 = 0; t9 < 9; ++t9) {
+            const int rr = r + t9 / 3 - 1, cc = c + t9 % 3 - 1;
+            const bool in = rr >= 0 && rr < p.H && cc >= 0 && cc < p.W;
+            if (!in) continue;
+            const float a = expf(d1[t9] * scale - sj.x) * izj;
+            const float de = a * (d1[9 + t9] * (1.f - al) - sj.z) * scale;
+            float kr[8];
+            load8_bf16(K + (size_t)(rr * p.W + cc) * D + c8, kr, p.relu);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) dq[e] = fmaf(de, kr[e], dq[e]);
+        }
+    }
+    // j as a key of each neighbour i's window (the window is symmetric)
+    {
+        float d2[18];
+#pragma unroll
+        for (int t9 = 0; t9 < 9; ++t9) {
+            const int rr = r + t9 / 3 - 1, cc = c + t9 % 3 - 1;
+            const bool in = rr >= 0 && rr < p.H && cc >= 0 && cc < p.W;
+            const size_t row = (size_t)(in ? rr * p.W + cc : j) * D + c8;
+            float qi[8], gi[8];
+            load8_bf16(Q + row, qi, p.relu);
+            load8_bf16(dO + row, gi, false);
+            d2[t9] = dot8(qi, k);
+            d2[9 + t9] = dot8(gi, v);
+        }
+#pragma unroll
+        for (int t = 0; t < 18; ++t) d2[t] = group8_sum(d2[t]);
+#pragma unroll
+        for (int t9 = 0; t9 < 9; ++t9) {
+            const int rr = r + t9 / 3 - 1, cc = c + t9 % 3 - 1;
+            const bool in = rr >= 0 && rr < p.H && cc >= 0 && cc < p.W;
+            if (!in) continue;
+            const int ni = rr * p.W + cc;
+            const float4 si = lst[ni];
+            const float a = expf(d2[t9] * scale - si.x) / si.y;
+            const float de = a * (d2[9 + t9] * (1.f - al) - si.z) * scale;
+            float qi[8], gi[8];
+            load8_bf16(Q + (size_t)ni * D + c8, qi, p.relu);
+            load8_bf16(dO + (size_t)ni * D + c8, gi, false);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                dv[e] = fmaf(a * (1.f - al), gi[e], dv[e]);
+                dk[e] = fmaf(de, qi[e], dk[e]);
+            }
+        }
+    }
+    if (live) {
+        float xq[8];
+        load8_bf16(Q + (size_t)j * D + c8, xq, false);
+        uint4 oq, ov;
+        uint32_t *pq = &oq.x, *pv = &ov.x;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float q0 = (p.relu && !(xq[2 * e] > 0.f)) ? 0.f : dq[2 * e];
+            const float q1 = (p.relu && !(xq[2 * e + 1] > 0.f)) ? 0.f : dq[2 * e + 1];
+            pq[e] = pack_bf16(q0, q1);
+            pv[e] = pack_bf16(dv[2 * e], dv[2 * e + 1]);
+        }
+        *reinterpret_cast<uint4 *>(dQo + (size_t)j * D + c8) = oq;
+        *reinterpret_cast<uint4 *>(dVo + (size_t)j * D + c8) = ov;
+        float4 *kp = reinterpret_cast<float4 *>(dKp + (size_t)j * D + c8);
+        kp[0] = make_float4(dk[0], dk[1], dk[2], dk[3]);
+        kp[1] = make_float4(dk[4], dk[5], dk[6], dk[7]);
+    }
+    // the warp's four tokens' ds terms, summed over the quarters in a fixed order
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        dsl[e] += __shfl_xor_sync(0xffffffffu, dsl[e], 8);
+        dsl[e] += __shfl_xor_sync(0xffffffffu, dsl[e], 16);
+    }
+    if (qg == 0)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) dsw[warp][c8 + e] = dsl[e];
     __syncthreads();
     for (int ch = tid; ch < D; ch += kThreads) {
         float acc = 0.f;
