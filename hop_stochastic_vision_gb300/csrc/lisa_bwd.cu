@@ -1965,24 +1965,26 @@ __global__ void __launch_bounds__(kThreads) bwd_token_mlp_tc(BwdProblem b) {
         }
     }
     __syncthreads();
-    // ---- per token: h = GELU(a), z = W2 h + b2, w = softmax(z) (warp per token)
-    for (int u = warp; u < kTpb; u += kWarps) {
+    // ---- per token (a quarter-warp, lanes over hidden units): h = GELU(a),
+    // z = W2 h + b2, w = softmax(z)
+    const int qg = lane >> 3, l8 = lane & 7;
+    const int uq = 4 * warp + qg;   // this quarter's token of the block
+    {
         float zt[TM];
 #pragma unroll
         for (int t = 0; t < TM; ++t) zt[t] = 0.f;
-        for (int m = lane; m < hid; m += 32) {
-            const float h = gelu_exact(pre[u * 68 + m]);
+        for (int m = l8; m < hid; m += 8) {
+            const float h = gelu_exact(pre[uq * 68 + m]);
 #pragma unroll
             for (int t = 0; t < TM; ++t)
                 if (t < T) zt[t] = fmaf(p.W2[(size_t)t * hid + m], h, zt[t]);
-            if (u < cnt) b.hbuf[((size_t)sl * p.n + j0 + u) * hid + m] = h;
+            if (uq < cnt) b.hbuf[((size_t)sl * p.n + j0 + uq) * hid + m] = h;
         }
-        warp_sum_n(zt);
         float zmax = -INFINITY, zs = 0.f;
 #pragma unroll
         for (int t = 0; t < TM; ++t)
             if (t < T) {
-                zt[t] += p.b2[t];
+                zt[t] = group8_sum(zt[t]) + p.b2[t];
                 zmax = fmaxf(zmax, zt[t]);
             }
 #pragma unroll
@@ -1991,13 +1993,9 @@ __global__ void __launch_bounds__(kThreads) bwd_token_mlp_tc(BwdProblem b) {
                 zt[t] = expf(zt[t] - zmax);
                 zs += zt[t];
             }
-        if (lane < T) {
-            float wl = 0.f;
 #pragma unroll
-            for (int t = 0; t < TM; ++t)
-                if (t == lane) wl = zt[t] / zs;
-            wts[u][lane] = wl;
-        }
+        for (int t = 0; t < TM; ++t)
+            if (t < T && t == l8) wts[uq][t] = zt[t] / zs;
     }
     __syncthreads();
 
@@ -2065,101 +2063,108 @@ __global__ void __launch_bounds__(kThreads) bwd_token_mlp_tc(BwdProblem b) {
     }
     __syncthreads();
 
-    // ---- per token (warp): the window (as bwd_token_a), dalpha terms, the
-    // softmax's and the MLP's elementwise backward; da into pre's place
-    float dal = 0.f;
-    for (int u = warp; u < cnt; u += kWarps) {
-        const int i = j0 + u;
-        float q[2], v[2], go[2], g[2];
+    // ---- per token (a quarter-warp): the window (as bwd_token_a), dalpha terms,
+    // the softmax's and the MLP's elementwise backward; da as bf16 hi + lo
+    {
+        const int c8 = 8 * l8;
+        const bool live = uq < cnt;
+        const int i = j0 + (live ? uq : 0);
+        const int r = i / p.W, c = i % p.W;
+        float q[8], v[8], go[8], g[8];
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-            const int ch = lane + 32 * t;
-            q[t] = __bfloat162float(Qk[u * kMA + ch]);
-            v[t] = Vs[u * 68 + ch];
-            go[t] = Gs[u * 68 + ch];
-            g[t] = fmaf(wts[u][0], v[t], G[u * 68 + ch]);
+        for (int e = 0; e < 8; ++e) {
+            q[e] = __bfloat162float(Qk[uq * kMA + c8 + e]);
+            v[e] = Vs[uq * 68 + c8 + e];
+            go[e] = Gs[uq * 68 + c8 + e];
+            g[e] = fmaf(wts[uq][0], v[e], G[uq * 68 + c8 + e]);
         }
-        int nb[9];
-        const int nn = window(i, p.H, p.W, nb);
-        float kr[9][2], vr[9][2], e[9];
+        float ev[9];
 #pragma unroll
         for (int t9 = 0; t9 < 9; ++t9) {
-            const int row = t9 < nn ? nb[t9] : i;
-            load_row<__nv_bfloat16, D>(K + (size_t)row * D, kr[t9], lane, p.relu);
-            load_row<__nv_bfloat16, D>(V + (size_t)row * D, vr[t9], lane, 0);
-            e[t9] = fmaf(q[0], kr[t9][0], q[1] * kr[t9][1]);
+            const int rr = r + t9 / 3 - 1, cc = c + t9 % 3 - 1;
+            const bool in = rr >= 0 && rr < p.H && cc >= 0 && cc < p.W;
+            float kr[8];
+            load8_bf16(K + (size_t)(in ? rr * p.W + cc : i) * D + c8, kr, p.relu);
+            ev[t9] = dot8(q, kr);
         }
-        warp_sum_n(e);
+        // the group sums run on every lane (each shuffle needs all 32); the mask after
+#pragma unroll
+        for (int t9 = 0; t9 < 9; ++t9) ev[t9] = group8_sum(ev[t9]);
         float emax = -INFINITY;
 #pragma unroll
-        for (int t9 = 0; t9 < 9; ++t9)
-            if (t9 < nn) emax = fmaxf(emax, e[t9] * 0.125f);
-        float l[2] = {0.f, 0.f}, esum = 0.f;
+        for (int t9 = 0; t9 < 9; ++t9) {
+            const int rr = r + t9 / 3 - 1, cc = c + t9 % 3 - 1;
+            const bool in = rr >= 0 && rr < p.H && cc >= 0 && cc < p.W;
+            ev[t9] = in ? ev[t9] * 0.125f : -INFINITY;
+            emax = fmaxf(emax, ev[t9]);
+        }
+        float l[8], esum = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) l[e] = 0.f;
 #pragma unroll
         for (int t9 = 0; t9 < 9; ++t9) {
-            if (t9 >= nn) break;
-            const float a = expf(e[t9] * 0.125f - emax);
+            const int rr = r + t9 / 3 - 1, cc = c + t9 % 3 - 1;
+            const bool in = rr >= 0 && rr < p.H && cc >= 0 && cc < p.W;
+            const float a = in ? expf(ev[t9] - emax) : 0.f;
             esum += a;
-            l[0] = fmaf(a, vr[t9][0], l[0]);
-            l[1] = fmaf(a, vr[t9][1], l[1]);
+            float vr[8];
+            load8_bf16(V + (size_t)(in ? rr * p.W + cc : i) * D + c8, vr, false);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) l[e] = fmaf(a, vr[e], l[e]);
         }
         const float inv = 1.f / esum;
-        float red[3] = {0.f, 0.f, 0.f};
+        float dgl = 0.f, dll = 0.f, dgv = 0.f;
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-            l[t] *= inv;
-            red[0] = fmaf(go[t], g[t] - l[t], red[0]);
-            red[1] = fmaf(go[t], l[t], red[1]);
-            red[2] = fmaf(go[t], v[t], red[2]);   // dw_0 / alpha
+        for (int e = 0; e < 8; ++e) {
+            l[e] *= inv;
+            dgl = fmaf(go[e], g[e] - l[e], dgl);
+            dll = fmaf(go[e], l[e], dll);
+            dgv = fmaf(go[e], v[e], dgv);   // dw_0 / alpha
         }
-        warp_sum_n(red);
-        dal += red[0];
+        dgl = group8_sum(dgl);
+        dll = group8_sum(dll);
+        dgv = group8_sum(dgv);
         const size_t ti = (size_t)sl * p.n + i;
-        if (lane == 0) reinterpret_cast<float4 *>(b.lstat)[ti] = make_float4(emax, esum, red[1] * (1.f - al), 0.f);
+        if (l8 == 0 && live) reinterpret_cast<float4 *>(b.lstat)[ti] = make_float4(emax, esum, dll * (1.f - al), 0.f);
         // dz = w (dw - w . dw), dw_0 = alpha dO . V, dw_k from the partials
         float w[TM], dw[TM], wdw = 0.f;
 #pragma unroll
         for (int t = 0; t < TM; ++t) {
-            w[t] = t < T ? wts[u][t] : 0.f;
-            dw[t] = t == 0 ? al * red[2]
-                           : (t < T ? ((dwp[t][u][0] + dwp[t][u][1]) + (dwp[t][u][2] + dwp[t][u][3])) : 0.f);
+            w[t] = t < T ? wts[uq][t] : 0.f;
+            dw[t] = t == 0 ? al * dgv
+                           : (t < T ? ((dwp[t][uq][0] + dwp[t][uq][1]) + (dwp[t][uq][2] + dwp[t][uq][3])) : 0.f);
             wdw = fmaf(w[t], dw[t], wdw);
         }
         float dz[TM];
 #pragma unroll
         for (int t = 0; t < TM; ++t) dz[t] = w[t] * (dw[t] - wdw);
-        if (lane < T) {
-            float wl = 0.f, dzl = 0.f;
+        if (live) {
 #pragma unroll
             for (int t = 0; t < TM; ++t)
-                if (t == lane) {
-                    wl = w[t];
-                    dzl = dz[t];
+                if (t < T && t == l8) {
+                    b.wtok[ti * T + t] = w[t];
+                    b.dzbuf[ti * T + t] = dz[t];
                 }
-            b.wtok[ti * T + lane] = wl;
-            b.dzbuf[ti * T + lane] = dzl;
         }
-        for (int m = lane; m < nmh; m += 32) {
+        for (int m = l8; m < nmh; m += 8) {
             float da = 0.f;
-            if (m < hid) {
+            if (m < hid && live) {
                 float dh = 0.f;
 #pragma unroll
                 for (int t = 0; t < TM; ++t)
                     if (t < T) dh = fmaf(p.W2[(size_t)t * hid + m], dz[t], dh);
-                da = dh * gelu_exact_grad(pre[u * 68 + m]);
+                da = dh * gelu_exact_grad(pre[uq * 68 + m]);
                 b.dabuf[ti * hid + m] = da;
             }
             const __nv_bfloat16 hi = __float2bfloat16_rn(da);
-            Di[u * kQS + m] = hi;
-            Di[kTpb * kQS + u * kQS + m] = __float2bfloat16_rn(da - __bfloat162float(hi));
+            Di[uq * kQS + m] = hi;
+            Di[kTpb * kQS + uq * kQS + m] = __float2bfloat16_rn(da - __bfloat162float(hi));
         }
+        // dalpha terms of the warp's live tokens, in token order
+        float dal = (l8 == 0 && live) ? dgl : 0.f;
+        dal = warp_sum(dal);
+        if (lane == 0) part[warp] = dal;
     }
-    for (int u = cnt + warp; u < kTpb; u += kWarps)   // rows past the slice's end: no da
-        for (int m = lane; m < nmh; m += 32) {
-            Di[u * kQS + m] = __float2bfloat16_rn(0.f);
-            Di[kTpb * kQS + u * kQS + m] = __float2bfloat16_rn(0.f);
-        }
-    if (lane == 0) part[warp] = dal;
     __syncthreads();
     if (tid == 0) {
         float acc = 0.f;
