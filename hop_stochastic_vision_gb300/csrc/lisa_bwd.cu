@@ -2215,6 +2215,123 @@ __global__ void __launch_bounds__(kThreads) bwd_token_mlp_tc(BwdProblem b) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// The MLP parameters' partial gradients per (slice, chunk), bf16 at d = 64:
+// dW1 = sum_i da_i [q_i; k_i]^T on mma.sync over 32-token tiles (da as bf16
+// hi + lo, its A fragments read from the token-major tile by ldmatrix.trans;
+// [Q | K] exact in bf16), the small dW2 = sum_i dz_i h_i^T and the exact fp32
+// sums db1, db2 on CUDA cores as in bwd_mlp_params.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) bwd_mlp_params_tc(BwdProblem b) {
+    constexpr int D = 64;
+    using namespace sm100;
+    __shared__ __align__(16) __nv_bfloat16 Xs[kTpb][kMA];        // [Q | K] rows
+    __shared__ __align__(16) __nv_bfloat16 Das[2][kTpb][kQS];    // da hi, lo (token-major)
+    __shared__ float As[kTpb][LISA_MAX_HIDDEN];
+    __shared__ float Hs[kTpb][LISA_MAX_HIDDEN];
+    __shared__ float Zs[kTpb][LISA_MAX_T_MLP];
+    const Problem &p = b.fwd;
+    const int c = blockIdx.x % p.chunks, sl = blockIdx.x / p.chunks, tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int T = p.T, hid = p.hidden, nmh = (hid + 15) / 16 * 16;
+    const int t0 = c * p.chunk, t1 = min(p.n, t0 + p.chunk);
+    const size_t sbase = (size_t)sl * p.n * D, tb = (size_t)sl * p.n;
+    const __nv_bfloat16 *Q = static_cast<const __nv_bfloat16 *>(p.Q) + sbase;
+    const __nv_bfloat16 *K = static_cast<const __nv_bfloat16 *>(p.K) + sbase;
+    // warp: hidden rows 16 mt .. 16 mt + 15 x channels 64 ng .. 64 ng + 63
+    const int mt = warp & 3, ng = warp >> 2;
+    const bool mma_warp = 16 * mt < nmh;
+    float acc[8][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    float w2[2] = {0.f, 0.f}, bb = 0.f;
+    for (int base = t0; base < t1; base += kTpb) {
+        const int cnt = min(kTpb, t1 - base);
+        for (int x = tid; x < kTpb * 8; x += kThreads) {
+            const int j = x >> 3, ch = x & 7;
+            uint4 q = make_uint4(0u, 0u, 0u, 0u), k = q;
+            if (j < cnt) {
+                const size_t o = ((size_t)(base + j) * D) / 8 + ch;
+                q = reinterpret_cast<const uint4 *>(Q)[o];
+                k = reinterpret_cast<const uint4 *>(K)[o];
+                if (p.relu) {
+                    q = make_uint4(relu_bf16x2(q.x), relu_bf16x2(q.y), relu_bf16x2(q.z), relu_bf16x2(q.w));
+                    k = make_uint4(relu_bf16x2(k.x), relu_bf16x2(k.y), relu_bf16x2(k.z), relu_bf16x2(k.w));
+                }
+            }
+            *reinterpret_cast<uint4 *>(&Xs[j][ch * 8]) = q;
+            *reinterpret_cast<uint4 *>(&Xs[j][64 + ch * 8]) = k;
+        }
+        for (int x = tid; x < kTpb * LISA_MAX_HIDDEN; x += kThreads) {
+            const int j = x / LISA_MAX_HIDDEN, m = x % LISA_MAX_HIDDEN;
+            const bool in = j < cnt && m < hid;
+            const float da = in ? b.dabuf[(tb + base + j) * hid + m] : 0.f;
+            As[j][m] = da;
+            Hs[j][m] = in ? b.hbuf[(tb + base + j) * hid + m] : 0.f;
+            const __nv_bfloat16 hi = __float2bfloat16_rn(da);
+            Das[0][j][m] = hi;
+            Das[1][j][m] = __float2bfloat16_rn(da - __bfloat162float(hi));
+        }
+        for (int x = tid; x < kTpb * LISA_MAX_T_MLP; x += kThreads) {
+            const int j = x / LISA_MAX_T_MLP, t = x % LISA_MAX_T_MLP;
+            Zs[j][t] = (j < cnt && t < T) ? b.dzbuf[(tb + base + j) * T + t] : 0.f;
+        }
+        __syncthreads();
+        if (mma_warp) {
+            const int arow = (lane & 7) + 8 * (lane >> 4), acol = 16 * mt + 8 * ((lane >> 3) & 1);
+            const int mi = lane >> 3, brow = (mi & 1) * 8 + (lane & 7);
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {   // tokens 16 ks .. 16 ks + 15
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {   // da hi, lo
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4_t(smem_u32(&Das[h][16 * ks + arow][acol]), a0, a1, a2, a3);
+#pragma unroll
+                    for (int np = 0; np < 4; ++np) {
+                        const int bcol = 64 * ng + 16 * np + (mi >> 1) * 8;
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4_t(smem_u32(&Xs[16 * ks + brow][bcol]), b0, b1, b2, b3);
+                        mma_bf16_16816(acc[2 * np], a0, a1, a2, a3, b0, b1);
+                        mma_bf16_16816(acc[2 * np + 1], a0, a1, a2, a3, b2, b3);
+                    }
+                }
+            }
+        }
+        for (int j = 0; j < cnt; ++j) {
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int e = tid + r * kThreads, t = e / LISA_MAX_HIDDEN, m = e % LISA_MAX_HIDDEN;
+                if (t < LISA_MAX_T_MLP) w2[r] = fmaf(Zs[j][t], Hs[j][m], w2[r]);
+            }
+            if (tid < LISA_MAX_HIDDEN) bb += As[j][tid];
+            else if (tid - LISA_MAX_HIDDEN < LISA_MAX_T_MLP) bb += Zs[j][tid - LISA_MAX_HIDDEN];
+        }
+        __syncthreads();
+    }
+    const size_t pc = (size_t)sl * p.chunks + c;
+    if (mma_warp) {
+        const int g = lane >> 2, q4 = lane & 3;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int m = 16 * mt + g + 8 * h;
+            if (m >= hid) continue;
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) {
+                const int ch = 64 * ng + 8 * nt + 2 * q4;
+                *reinterpret_cast<float2 *>(b.pw1 + pc * hid * 2 * D + (size_t)m * 2 * D + ch) =
+                    make_float2(acc[nt][2 * h], acc[nt][2 * h + 1]);
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const int e = tid + r * kThreads, t = e / LISA_MAX_HIDDEN, m = e % LISA_MAX_HIDDEN;
+        if (t < T && m < hid) b.pw2[(pc * T + t) * hid + m] = w2[r];
+    }
+    if (tid < hid) b.pb1[pc * hid + tid] = bb;
+    else if (tid >= LISA_MAX_HIDDEN && tid - LISA_MAX_HIDDEN < T) b.pb2[pc * T + tid - LISA_MAX_HIDDEN] = bb;
+}
+
 __global__ void __launch_bounds__(kThreads) bwd_token_b_tc(BwdProblem b) {
     constexpr int D = 64, NC = 2;
     using namespace sm100;
@@ -2604,9 +2721,7 @@ __global__ void __launch_bounds__(kThreads) bwd_mlp_reduce(BwdProblem b, int D) 
         else if (e < n1 + hid) { src = b.pb1; dst = b.db1; stride = hid; off = e - n1; }
         else if (e < n1 + hid + n2) { src = b.pw2; dst = b.dW2; stride = n2; off = e - n1 - hid; }
         else { src = b.pb2; dst = b.db2; stride = T; off = e - n1 - hid - n2; }
-        float acc = 0.f;
-        for (size_t q = 0; q < parts; ++q) acc += src[q * stride + off];
-        dst[off] = acc;
+        dst[off] = sum_partials(src, (int)parts, stride, off);   // eight loads in flight, fixed order
     }
 }
 
@@ -2778,7 +2893,10 @@ cudaError_t launch_bwd_all(const BwdProblem &b, cudaStream_t st) {
     bwd_finish_k<TIn, D><<<(unsigned)blocks, kThreads, 0, st>>>(b);
     bwd_dalpha<<<(p.heads + kThreads - 1) / kThreads, kThreads, 0, st>>>(b);
     if (b.mlp) {
-        bwd_mlp_params<TIn, D><<<grid_stats, kThreads, 0, st>>>(b);
+        if (std::is_same<TIn, __nv_bfloat16>::value && D == 64 && p.relu != 2)
+            bwd_mlp_params_tc<<<grid_stats, kThreads, 0, st>>>(b);
+        else
+            bwd_mlp_params<TIn, D><<<grid_stats, kThreads, 0, st>>>(b);
         const int total = p.hidden * 2 * D + p.hidden + p.T * p.hidden + p.T;
         bwd_mlp_reduce<<<(total + kThreads - 1) / kThreads, kThreads, 0, st>>>(b, D);
     }
