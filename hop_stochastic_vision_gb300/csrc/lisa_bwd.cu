@@ -2216,6 +2216,89 @@ __global__ void __launch_bounds__(kThreads) bwd_token_mlp_tc(BwdProblem b) {
 }
 
 // ---------------------------------------------------------------------------
+// 2'. adaptive weights on the tensor path (bf16, d = 64): the chunk's partial
+// dU_k = sum_j Q_j (c_jk dO_j)^T with c_jk = alpha w_jk / (Q_j . s + eps), the
+// same sum as bwd_stats_duk with the token's scalars moved onto dO.  Q^T is
+// exact in bf16 (A operand, ldmatrix.trans from the token-major tile), c_jk dO_j
+// goes in as bf16 hi + lo; one quarter-warp stages each token.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) bwd_stats_duk_tc(BwdProblem b) {
+    constexpr int D = 64;
+    static_assert(kTpb * 8 == kThreads, "one quarter-warp per staged token");
+    using namespace sm100;
+    __shared__ __align__(16) __nv_bfloat16 Qs[kTpb][kQS];
+    __shared__ __align__(16) __nv_bfloat16 Gs[2][kTpb][kQS];   // c dO hi, lo
+    const Problem &p = b.fwd;
+    const int c = blockIdx.x % p.chunks, sl = blockIdx.x / p.chunks, k = 1 + blockIdx.y, tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int t0 = c * p.chunk, t1 = min(p.n, t0 + p.chunk);
+    const __nv_bfloat16 *Q = static_cast<const __nv_bfloat16 *>(p.Q) + (size_t)sl * p.n * D;
+    const __nv_bfloat16 *dO = static_cast<const __nv_bfloat16 *>(b.dO) + (size_t)sl * p.n * D;
+    const float *wt = b.wtok + (size_t)sl * p.n * p.T;
+    const float al = p.alpha[sl % p.heads];
+    const int j8 = tid >> 3, c8 = tid & 7;   // staging: token j8, channels 8 c8 .. 8 c8 + 7
+    float sv[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) sv[u] = p.s_red[(size_t)sl * D + 8 * c8 + u];
+    // warp: Q channels 16 mt .. 16 mt + 15 x dO channels 32 ng .. 32 ng + 31
+    const int mt = warp & 3, ng = warp >> 2;
+    const int arow = (lane & 7) + 8 * (lane >> 4), acol = 16 * mt + 8 * ((lane >> 3) & 1);
+    const int mi = lane >> 3, brow = (mi & 1) * 8 + (lane & 7);
+    float acc[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    for (int base = t0; base < t1; base += kTpb) {
+        const bool in = j8 < t1 - base;
+        float q[8], g[8];
+        if (in) {
+            load8_bf16(Q + (size_t)(base + j8) * D + 8 * c8, q, p.relu != 0);
+            load8_bf16(dO + (size_t)(base + j8) * D + 8 * c8, g, false);
+        } else {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) q[u] = g[u] = 0.f;
+        }
+        const float den = group8_sum(dot8(q, sv)) + p.eps;   // every lane: the shuffles need all 32
+        const float cj = in ? al * wt[(size_t)(base + j8) * p.T + k] / den : 0.f;
+        uint32_t qw[4], hw[4], lw[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            qw[u] = pack_bf16(q[2 * u], q[2 * u + 1]);
+            const float x0 = cj * g[2 * u], x1 = cj * g[2 * u + 1];
+            const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
+            hw[u] = pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
+            lw[u] = pack_bf16(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
+        }
+        *reinterpret_cast<uint4 *>(&Qs[j8][8 * c8]) = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+        *reinterpret_cast<uint4 *>(&Gs[0][j8][8 * c8]) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4 *>(&Gs[1][j8][8 * c8]) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        __syncthreads();
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {   // tokens 16 ks .. 16 ks + 15
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_t(smem_u32(&Qs[16 * ks + arow][acol]), a0, a1, a2, a3);
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int np = 0; np < 2; ++np) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(smem_u32(&Gs[h][16 * ks + brow][32 * ng + 16 * np + (mi >> 1) * 8]), b0, b1, b2, b3);
+                    mma_bf16_16816(acc[2 * np], a0, a1, a2, a3, b0, b1);
+                    mma_bf16_16816(acc[2 * np + 1], a0, a1, a2, a3, b2, b3);
+                }
+        }
+        __syncthreads();
+    }
+    float *out = b.dukp + (((size_t)sl * p.chunks + c) * b.nh + (k - 1)) * D * D;
+    const int g4 = lane >> 2, q4 = lane & 3;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+            *reinterpret_cast<float2 *>(out + (size_t)(16 * mt + g4 + 8 * h) * D + 32 * ng + 8 * nt + 2 * q4) =
+                make_float2(acc[nt][2 * h], acc[nt][2 * h + 1]);
+}
+
+// ---------------------------------------------------------------------------
 // The MLP parameters' partial gradients per (slice, chunk), bf16 at d = 64:
 // dW1 = sum_i da_i [q_i; k_i]^T on mma.sync over 32-token tiles (da as bf16
 // hi + lo, its A fragments read from the token-major tile by ldmatrix.trans;
@@ -2333,7 +2416,7 @@ __global__ void __launch_bounds__(kThreads) bwd_mlp_params_tc(BwdProblem b) {
 }
 
 __global__ void __launch_bounds__(kThreads) bwd_token_b_tc(BwdProblem b) {
-    constexpr int D = 64, NC = 2;
+    constexpr int D = 64;
     using namespace sm100;
     extern __shared__ float4 smem_tc[];
     __nv_bfloat16 *Bs = reinterpret_cast<__nv_bfloat16 *>(smem_tc);
@@ -2707,21 +2790,46 @@ __global__ void __launch_bounds__(kThreads) bwd_mlp_params(BwdProblem b) {
     else if (tid >= LISA_MAX_HIDDEN && tid - LISA_MAX_HIDDEN < T) b.pb2[pc * T + tid - LISA_MAX_HIDDEN] = bb;
 }
 
+// 32 consecutive parameter entries per block: warp g sums the partials
+// g, g + 8, g + 16, ... of its lane's entry (coalesced 128-byte rows, four
+// loads in flight), then lane 0..31 of warp 0 adds the eight warp sums in a
+// fixed order.
 __global__ void __launch_bounds__(kThreads) bwd_mlp_reduce(BwdProblem b, int D) {
+    constexpr int kGroups = kThreads / 32;
+    __shared__ float red[kGroups][32];
     const Problem &p = b.fwd;
     const int T = p.T, hid = p.hidden;
     const int n1 = hid * 2 * D, n2 = T * hid;
     const int total = n1 + hid + n2 + T;
-    const size_t parts = (size_t)p.slices * p.chunks;
-    for (int e = blockIdx.x * kThreads + threadIdx.x; e < total; e += gridDim.x * kThreads) {
-        const float *src;
-        float *dst;
-        int stride, off;
-        if (e < n1) { src = b.pw1; dst = b.dW1; stride = n1; off = e; }
-        else if (e < n1 + hid) { src = b.pb1; dst = b.db1; stride = hid; off = e - n1; }
-        else if (e < n1 + hid + n2) { src = b.pw2; dst = b.dW2; stride = n2; off = e - n1 - hid; }
-        else { src = b.pb2; dst = b.db2; stride = T; off = e - n1 - hid - n2; }
-        dst[off] = sum_partials(src, (int)parts, stride, off);   // eight loads in flight, fixed order
+    const int parts = p.slices * p.chunks;
+    const int lane = threadIdx.x & 31, g = threadIdx.x >> 5;
+    const int e = blockIdx.x * 32 + lane;
+    const float *src = nullptr;
+    float *dst = nullptr;
+    int stride = 0, off = 0;
+    if (e < n1) { src = b.pw1; dst = b.dW1; stride = n1; off = e; }
+    else if (e < n1 + hid) { src = b.pb1; dst = b.db1; stride = hid; off = e - n1; }
+    else if (e < n1 + hid + n2) { src = b.pw2; dst = b.dW2; stride = n2; off = e - n1 - hid; }
+    else if (e < total) { src = b.pb2; dst = b.db2; stride = T; off = e - n1 - hid - n2; }
+    float a[4] = {0.f, 0.f, 0.f, 0.f};
+    if (src) {
+        int r = g;
+        for (; r + 3 * kGroups < parts; r += 4 * kGroups) {
+            float v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v[u] = src[(size_t)(r + u * kGroups) * stride + off];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) a[u] += v[u];
+        }
+        for (; r < parts; r += kGroups) a[0] += src[(size_t)r * stride + off];
+    }
+    red[g][lane] = (a[0] + a[1]) + (a[2] + a[3]);
+    __syncthreads();
+    if (g == 0 && dst) {
+        float t = 0.f;
+#pragma unroll
+        for (int k = 0; k < kGroups; ++k) t += red[k][lane];
+        dst[off] = t;
     }
 }
 
@@ -2833,7 +2941,12 @@ cudaError_t launch_bwd_all(const BwdProblem &b, cudaStream_t st) {
         } else {
             bwd_token_mlp<TIn, D><<<grid_tok, kThreads, 0, st>>>(b);
         }
-        if (p.T > 1) bwd_stats_duk<TIn, D><<<dim3(grid_stats, (unsigned)(p.T - 1)), kThreads, 0, st>>>(b);
+        if (p.T > 1) {
+            if (std::is_same<TIn, __nv_bfloat16>::value && D == 64 && p.relu != 2)
+                bwd_stats_duk_tc<<<dim3(grid_stats, (unsigned)(p.T - 1)), kThreads, 0, st>>>(b);
+            else
+                bwd_stats_duk<TIn, D><<<dim3(grid_stats, (unsigned)(p.T - 1)), kThreads, 0, st>>>(b);
+        }
     } else {
         if (b.tc_dub) {   // dUbar / alpha = Q~^T dO: the statistics kernel with dO as its V and K
             Problem q = b.tcfwd;
@@ -2898,7 +3011,7 @@ cudaError_t launch_bwd_all(const BwdProblem &b, cudaStream_t st) {
         else
             bwd_mlp_params<TIn, D><<<grid_stats, kThreads, 0, st>>>(b);
         const int total = p.hidden * 2 * D + p.hidden + p.T * p.hidden + p.T;
-        bwd_mlp_reduce<<<(total + kThreads - 1) / kThreads, kThreads, 0, st>>>(b, D);
+        bwd_mlp_reduce<<<(total + 31) / 32, kThreads, 0, st>>>(b, D);
     }
     return cudaGetLastError();
 }
