@@ -1327,7 +1327,7 @@ __device__ __forceinline__ float dot8(const float (&x)[8], const float (&y)[8]) 
     return a;
 }
 
-__global__ void __launch_bounds__(kThreads) bwd_token_a_tc(BwdProblem b) {
+__global__ void __launch_bounds__(kThreads, 4) bwd_token_a_tc(BwdProblem b) {
     constexpr int D = 64;
     using namespace sm100;
     __shared__ __align__(16) __nv_bfloat16 Ui[2 * D * kQS];   // Ubar hi rows a (cols e), then lo
@@ -2305,7 +2305,7 @@ __global__ void __launch_bounds__(kThreads) bwd_stats_duk_tc(BwdProblem b) {
 // [Q | K] exact in bf16), the small dW2 = sum_i dz_i h_i^T and the exact fp32
 // sums db1, db2 on CUDA cores as in bwd_mlp_params.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) bwd_mlp_params_tc(BwdProblem b) {
+__global__ void __launch_bounds__(kThreads, 3) bwd_mlp_params_tc(BwdProblem b) {
     constexpr int D = 64;
     using namespace sm100;
     __shared__ __align__(16) __nv_bfloat16 Xs[kTpb][kMA];        // [Q | K] rows
