@@ -121,8 +121,11 @@ def test_fixed_weights_and_untruncated(dtype):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("grid", [(1, 1), (1, 7), (9, 1), (57, 55)])
+@pytest.mark.parametrize("grid", [(1, 1), (1, 7), (9, 1), (57, 55), (4, 64), (5, 65), (3, 130)])
 def test_grids(dtype, grid):
+    """Ragged and narrow grids; rows of 64 tokens and wider (the window-row
+    staging of the bf16 statistics pass holds grids up to 64 wide, wider ones
+    read their window rows from global memory)."""
     _check(_shape(dtype, 64, grid[0], grid[1], 3))
 
 
