@@ -501,7 +501,8 @@ struct BwdPlan {
     size_t off_mred, off_uk, off_ubar, off_ubart, off_dub, off_lstat, off_dalp, off_dsp, off_dm, off_du1,
         off_dmt, off_du1t, off_dsr, off_dals, off_dkp, off_bimg, off_ubimg;
     // adaptive weights only
-    size_t off_ukn, off_wtok, off_dz, off_h, off_da, off_dxm, off_dukp, off_pw1, off_pb1, off_pw2, off_pb2;
+    size_t off_ukn, off_wtok, off_dz, off_h, off_da, off_dxm, off_dukp, off_pw1, off_pb1, off_pw2, off_pb2,
+        off_ukimg, off_w1img;
     size_t total;
 };
 
@@ -554,6 +555,8 @@ BwdPlan make_bwd_plan(int slices, int H, int W, int D, int T, int hidden, int dt
         b.off_pb1 = off;  off = align_up(off + S * C * Hd * sizeof(float));
         b.off_pw2 = off;  off = align_up(off + S * C * Tz * Hd * sizeof(float));
         b.off_pb2 = off;  off = align_up(off + S * C * Tz * sizeof(float));
+        b.off_ukimg = off; off = align_up(off + S * nk * 2 * 64 * 72 * sizeof(uint16_t));
+        b.off_w1img = off; off = align_up(off + 2 * LISA_MAX_HIDDEN * 136 * sizeof(uint16_t));
     }
     b.total = off;
     return b;
@@ -669,6 +672,8 @@ lisa_status run_backward(const void *Q, const void *K, const void *V, const void
         b.pb1 = f32(pl.off_pb1);
         b.pw2 = f32(pl.off_pw2);
         b.pb2 = f32(pl.off_pb2);
+        b.ukimg = reinterpret_cast<uint16_t *>(ws + pl.off_ukimg);
+        b.w1img = reinterpret_cast<uint16_t *>(ws + pl.off_w1img);
         b.dW1 = mg->dW1;
         b.db1 = mg->db1;
         b.dW2 = mg->dW2;

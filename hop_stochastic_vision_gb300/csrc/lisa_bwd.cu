@@ -1861,6 +1861,34 @@ constexpr int kMlpTcSmemBytes = kTpb * kMA * 2              // [Q | K] rows
                                 + 3 * kTpb * 68 * 4         // pre-activations (then da), g, V and dO rows (fp32)
                                 + kTpb * 68 * 4;
 
+// The tensor-core MLP pass's bf16 operand images, once per backward: block
+// (slice, k) writes U_k (row-major) as hi and lo rows of kQS columns, the last
+// block W1 as hi and lo rows of kMA columns (rows hidden .. kMH - 1 zero).
+__global__ void __launch_bounds__(kThreads) bwd_mlp_images(BwdProblem b) {
+    constexpr int D = 64;
+    const Problem &p = b.fwd;
+    const int tid = threadIdx.x;
+    if (blockIdx.x < (unsigned)(p.slices * b.nh)) {
+        const float *Un = b.Ukn + (size_t)blockIdx.x * D * D;
+        uint16_t *img = b.ukimg + (size_t)blockIdx.x * 2 * 64 * kQS;
+        for (int x = tid; x < D * D; x += kThreads) {
+            const float uv = Un[x];
+            const __nv_bfloat16 hi = __float2bfloat16_rn(uv);
+            img[(x >> 6) * kQS + (x & 63)] = __bfloat16_as_ushort(hi);
+            const float lo = uv - __bfloat162float(hi);
+            img[64 * kQS + (x >> 6) * kQS + (x & 63)] = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+        }
+    } else {
+        for (int x = tid; x < kMH * 2 * D; x += kThreads) {
+            const int m = x / (2 * D), c = x % (2 * D);
+            const float w = m < p.hidden ? p.W1[(size_t)m * 2 * D + c] : 0.f;
+            const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+            b.w1img[m * kMA + c] = __bfloat16_as_ushort(hi);
+            b.w1img[kMH * kMA + m * kMA + c] = __bfloat16_as_ushort(__float2bfloat16_rn(w - __bfloat162float(hi)));
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kThreads) bwd_token_mlp_tc(BwdProblem b) {
     constexpr int D = 64, TM = LISA_MAX_T_MLP;
     using namespace sm100;
@@ -1916,12 +1944,13 @@ __global__ void __launch_bounds__(kThreads) bwd_token_mlp_tc(BwdProblem b) {
             Gs[j * 68 + c * 8 + 2 * e + 1] = bf16_hi(gg[e]);
         }
     }
-    for (int x = tid; x < nmh * 2 * D; x += kThreads) {
-        const int m = x / (2 * D), c = x % (2 * D);
-        const float w = m < hid ? p.W1[(size_t)m * 2 * D + c] : 0.f;
-        const __nv_bfloat16 hi = __float2bfloat16_rn(w);
-        W1i[m * kMA + c] = hi;
-        W1i[kMH * kMA + m * kMA + c] = __float2bfloat16_rn(w - __bfloat162float(hi));
+    {   // W1 hi and lo rows from the precomputed image (the rows below nmh of each)
+        constexpr int kRowV = kMA / 8;   // 16-byte pieces per row
+        const uint4 *img = reinterpret_cast<const uint4 *>(b.w1img);
+        for (int x = tid; x < 2 * nmh * kRowV; x += kThreads) {
+            const int h = x / (nmh * kRowV), y = x % (nmh * kRowV);
+            reinterpret_cast<uint4 *>(W1i + h * kMH * kMA)[y] = img[h * kMH * kRowV + y];
+        }
     }
     for (int x = tid; x < TM * kTpb * 4; x += kThreads) (&dwp[0][0][0])[x] = 0.f;
     __syncthreads();
@@ -2008,13 +2037,10 @@ __global__ void __launch_bounds__(kThreads) bwd_token_mlp_tc(BwdProblem b) {
         const int r0 = 16 * mt + (lane >> 2);
         float gacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         for (int kk = 1; kk < T; ++kk) {
-            // U_k (fp32, row-major) as bf16 hi + lo
-            const float *Un = b.Ukn + ((size_t)sl * b.nh + (kk - 1)) * D * D;
-            for (int x = tid; x < D * D; x += kThreads) {
-                const float uv = Un[x];
-                const __nv_bfloat16 hi = __float2bfloat16_rn(uv);
-                Ui[(x >> 6) * kQS + (x & 63)] = hi;
-                Ui[64 * kQS + (x >> 6) * kQS + (x & 63)] = __float2bfloat16_rn(uv - __bfloat162float(hi));
+            {   // U_k's bf16 hi and lo rows from the precomputed image
+                const uint4 *img =
+                    reinterpret_cast<const uint4 *>(b.ukimg + ((size_t)sl * b.nh + (kk - 1)) * 2 * 64 * kQS);
+                for (int x = tid; x < 2 * 64 * kQS / 8; x += kThreads) reinterpret_cast<uint4 *>(Ui)[x] = img[x];
             }
             __syncthreads();
             float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -2937,6 +2963,7 @@ cudaError_t launch_bwd_all(const BwdProblem &b, cudaStream_t st) {
             if ((err = cudaFuncSetAttribute(bwd_token_mlp_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             kMlpTcSmemBytes)) != cudaSuccess)
                 return err;
+            bwd_mlp_images<<<(unsigned)(p.slices * b.nh + 1), kThreads, 0, st>>>(b);
             bwd_token_mlp_tc<<<grid_tok, kThreads, kMlpTcSmemBytes, st>>>(b);
         } else {
             bwd_token_mlp<TIn, D><<<grid_tok, kThreads, 0, st>>>(b);
