@@ -657,7 +657,7 @@ lisa_status run_backward(const void *Q, const void *K, const void *V, const void
         b.tcfwd.wmode = LISA_W_FIXED;   // statistics only: the walk weights play no part
         b.tcdub = f32(pl.off_tcdub);
         b.tc_dub = (!mlp && !b.fwd.untruncated) ? 1 : 0;
-        if (!mlp) b.ntile = pl.ntile;   // the tiled token pass
+        b.ntile = pl.ntile;   // the tiled token pass
     }
     if (mlp) {
         b.mlp = 1;

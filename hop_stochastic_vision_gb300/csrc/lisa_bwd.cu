@@ -1520,6 +1520,7 @@ __device__ __forceinline__ float ex2_fast(float x) {
     return y;
 }
 
+template <bool kMlp>
 __global__ void __launch_bounds__(kTileThreads, 1)
     bwd_token_b_tile(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
                      const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mG,
@@ -1535,6 +1536,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     __shared__ float rqs[kTileTok];
     __shared__ float cjs[kTileTok];
     __shared__ float dsw[kTileWarps][D];
+    __shared__ float wts_t[kMlp ? kTileTok : 1][kMlp ? LISA_MAX_T_MLP : 1];   // adaptive weights of the tile's tokens
     const Problem &p = b.fwd;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int tiles_c = (p.W + 7) / 8;
@@ -1652,6 +1654,55 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                     out[(row + 8) * kOS + col + 1] = acc[nt][3];
                 }
             }
+        }
+        if (kMlp) {
+            // ---- adaptive weights: each token's own walk terms, which the shared
+            // products leave out: dQ~_u += alpha sum_{k>=1} w_uk dO_u U_k^T, as
+            // dO U_k^T on mma.sync per k (U_k's bf16 hi + lo rows staged where the
+            // B image was, read as the B operand without transposition), each
+            // row scaled by its token's alpha w_uk
+            for (int x = tid; x < kTileTok * p.T; x += kTileThreads) {
+                const int uu = x / p.T, t = x % p.T;
+                const int rr = r0 + uu / 8, cc = c0 + uu % 8;
+                wts_t[uu][t] =
+                    (rr < p.H && cc < p.W) ? b.wtok[((size_t)sl * p.n + rr * p.W + cc) * p.T + t] : 0.f;
+            }
+            const int mt = warp & 3, sb = warp >> 2;
+            const int hrow = halo_row(16 * mt + (lane & 15), 0, 0);
+            const int nrow = 16 * sb + (lane & 7) + 8 * (lane >> 4), kofs = ((lane >> 3) & 1) * 8;
+            const int row = 16 * mt + (lane >> 2);
+            for (int kk = 1; kk < p.T; ++kk) {
+                __syncthreads();   // nothing reads the B region any more; the weights are in place
+                const uint4 *img =
+                    reinterpret_cast<const uint4 *>(b.ukimg + ((size_t)sl * b.nh + (kk - 1)) * 2 * 64 * kQS);
+                for (int x = tid; x < 2 * 64 * kQS / 8; x += kTileThreads) reinterpret_cast<uint4 *>(Bs)[x] = img[x];
+                __syncthreads();
+                float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(smem_u32(Gc) + hoff(hrow, 2 * ks + (lane >> 4)), a0, a1, a2, a3);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4(smem_u32(Bs) + (uint32_t)((h * 64 + nrow) * kQS + 16 * ks + kofs) * 2u, b0, b1, b2, b3);
+                        mma_bf16_16816(acc[0], a0, a1, a2, a3, b0, b1);
+                        mma_bf16_16816(acc[1], a0, a1, a2, a3, b2, b3);
+                    }
+                }
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float wk = al * wts_t[row + 8 * h][kk];
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const int col = 16 * sb + 8 * nt + 2 * (lane & 3);
+                        float *o = oQ + (row + 8 * h) * kOS + col;
+                        o[0] = fmaf(wk, acc[nt][2 * h], o[0]);
+                        o[1] = fmaf(wk, acc[nt][2 * h + 1], o[1]);
+                    }
+                }
+            }
+            img_sl = -1;   // the B region holds U_k now: the next tile stages its B image again
         }
         __syncthreads();
 
@@ -1806,6 +1857,9 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                 if (rr >= p.H || cc >= p.W) continue;
                 const size_t jt = (size_t)(rr * p.W + cc) * D;
                 const float rq = rqs[ut], cj = cjs[ut];
+                // adaptive weights: the MLP's share of [dq | dk] and the token's own w_0
+                const float *xm = kMlp ? b.dxm + ((size_t)sl * p.n + rr * p.W + cc) * 2 * D : nullptr;
+                const float wv0 = kMlp ? wts_t[ut][0] : w0;
 #pragma unroll
                 for (int nt = 0; nt < 8; ++nt) {
                     const int col = 8 * nt + 2 * q4;
@@ -1813,6 +1867,11 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                     if (role == 0) {
                         float d0 = oQ[ut * kOS + col] * rq - cj * s[col] + x0;
                         float d1 = oQ[ut * kOS + col + 1] * rq - cj * s[col + 1] + x1;
+                        if (kMlp) {
+                            const float2 xq = *reinterpret_cast<const float2 *>(xm + col);
+                            d0 += xq.x;
+                            d1 += xq.y;
+                        }
                         if (p.relu) {   // dXq through the feature map (the staged Q is ReLU'd)
                             const uint32_t qp =
                                 *reinterpret_cast<const uint32_t *>(Qc + hoff(hrow_b(m), col >> 3) + (col & 7) * 2);
@@ -1821,13 +1880,18 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                         }
                         *reinterpret_cast<uint32_t *>(dQo + jt + col) = pack_bf16(d0, d1);
                     } else if (role == 1) {
-                        *reinterpret_cast<float2 *>(dKp + jt + col) =
-                            make_float2(oK[ut * kOS + col] + x0, oK[ut * kOS + col + 1] + x1);
+                        float k0 = oK[ut * kOS + col] + x0, k1 = oK[ut * kOS + col + 1] + x1;
+                        if (kMlp) {
+                            const float2 xk = *reinterpret_cast<const float2 *>(xm + D + col);
+                            k0 += xk.x;
+                            k1 += xk.y;
+                        }
+                        *reinterpret_cast<float2 *>(dKp + jt + col) = make_float2(k0, k1);
                     } else {
                         const uint32_t gp =
                             *reinterpret_cast<const uint32_t *>(Gc + hoff(hrow_b(m), col >> 3) + (col & 7) * 2);
-                        const float d0 = fmaf(w0 * al, bf16_lo(gp), oV[ut * kOS + col]) + x0;
-                        const float d1 = fmaf(w0 * al, bf16_hi(gp), oV[ut * kOS + col + 1]) + x1;
+                        const float d0 = fmaf(wv0 * al, bf16_lo(gp), oV[ut * kOS + col]) + x0;
+                        const float d1 = fmaf(wv0 * al, bf16_hi(gp), oV[ut * kOS + col + 1]) + x1;
                         *reinterpret_cast<uint32_t *>(dVo + jt + col) = pack_bf16(d0, d1);
                     }
                 }
@@ -2998,8 +3062,9 @@ cudaError_t launch_bwd_all(const BwdProblem &b, cudaStream_t st) {
     // (its bf16 staging applies ReLU only)
     if (b.ntile) {   // bf16, d = 64, fixed weights: 8 x 8 tiles with their halo in shared memory
         bwd_bimg<<<dim3((unsigned)p.slices, 5), kThreads, 0, st>>>(b);
-        if ((err = cudaFuncSetAttribute(bwd_token_b_tile, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        kTileSmemBytes)) != cudaSuccess)
+        auto tile_kern = b.mlp ? bwd_token_b_tile<true> : bwd_token_b_tile<false>;
+        if ((err = cudaFuncSetAttribute(tile_kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTileSmemBytes)) !=
+            cudaSuccess)
             return err;
         // tiled 4-D maps: 10 x 10 halo boxes of the inputs (128-byte swizzle) and of
         // the window statistics ([S][H][W][4] fp32)
@@ -3012,7 +3077,7 @@ cudaError_t launch_bwd_all(const BwdProblem &b, cudaStream_t st) {
         const long long ntiles = (long long)p.slices * b.ntile;
         const int nsm = sm_count();
         const unsigned grid = (unsigned)(ntiles < nsm ? ntiles : nsm);   // persistent: one CTA per SM
-        bwd_token_b_tile<<<grid, kTileThreads, kTileSmemBytes, st>>>(mK, mV, mQ, mG, mL, b);
+        tile_kern<<<grid, kTileThreads, kTileSmemBytes, st>>>(mK, mV, mQ, mG, mL, b);
     } else if (std::is_same<TIn, __nv_bfloat16>::value && D == 64 && p.relu != 2) {
         bwd_bimg<<<dim3((unsigned)p.slices, 5), kThreads, 0, st>>>(b);
         if ((err = cudaFuncSetAttribute(bwd_token_b_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
