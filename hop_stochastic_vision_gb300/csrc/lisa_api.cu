@@ -502,7 +502,7 @@ struct BwdPlan {
         off_dmt, off_du1t, off_dsr, off_dals, off_dkp, off_bimg, off_ubimg;
     // adaptive weights only
     size_t off_ukn, off_wtok, off_dz, off_h, off_da, off_dxm, off_dukp, off_pw1, off_pb1, off_pw2, off_pb2,
-        off_ukimg, off_w1img;
+        off_ukimg, off_w1img, off_ukimgt;
     size_t total;
 };
 
@@ -557,6 +557,7 @@ BwdPlan make_bwd_plan(int slices, int H, int W, int D, int T, int hidden, int dt
         b.off_pb2 = off;  off = align_up(off + S * C * Tz * sizeof(float));
         b.off_ukimg = off; off = align_up(off + S * nk * 2 * 64 * 72 * sizeof(uint16_t));
         b.off_w1img = off; off = align_up(off + 2 * LISA_MAX_HIDDEN * 136 * sizeof(uint16_t));
+        b.off_ukimgt = off; off = align_up(off + S * nk * 64 * 72 * sizeof(uint16_t));
     }
     b.total = off;
     return b;
@@ -674,6 +675,7 @@ lisa_status run_backward(const void *Q, const void *K, const void *V, const void
         b.pb2 = f32(pl.off_pb2);
         b.ukimg = reinterpret_cast<uint16_t *>(ws + pl.off_ukimg);
         b.w1img = reinterpret_cast<uint16_t *>(ws + pl.off_w1img);
+        b.ukimgT = reinterpret_cast<uint16_t *>(ws + pl.off_ukimgt);
         b.dW1 = mg->dW1;
         b.db1 = mg->db1;
         b.dW2 = mg->dW2;

@@ -1274,8 +1274,11 @@ constexpr int kTcSmemBytes = kImgRows * kBS * 2 + 2 * kTpb * kAS * 2 + kTpb * 64
 __global__ void __launch_bounds__(kThreads) bwd_bimg(BwdProblem b) {
     const int sl = blockIdx.x, m = blockIdx.y;
     const size_t mo = (size_t)sl * 64 * 64;
-    const float *srcs[5] = {b.UbarT, b.dM, b.dU1T, b.dMT, b.dU1};
-    const float4 *src = reinterpret_cast<const float4 *>(srcs[m] + mo);
+    // adaptive weights: alpha U_1^T stands where alpha Ubar^T does (the tiled pass
+    // scales that half of its first product by each token's w_1)
+    const float *srcs[5] = {b.mlp ? b.Uk + (size_t)sl * b.nh * 64 * 64 : b.UbarT + mo, b.dM + mo, b.dU1T + mo,
+                            b.dMT + mo, b.dU1 + mo};
+    const float4 *src = reinterpret_cast<const float4 *>(srcs[m]);
     const float f = m == 0 ? b.fwd.alpha[sl % b.fwd.heads] : 1.f;
     uint2 *img = reinterpret_cast<uint2 *>(b.bimg + ((size_t)sl * kImgRows + (size_t)m * 64) * 64);
     for (int x = threadIdx.x; x < 64 * 64 / 4; x += kThreads) {
@@ -1613,10 +1616,19 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                 make_uint4(pack_bf16(q[0] * rq, q[1] * rq), pack_bf16(q[2] * rq, q[3] * rq),
                            pack_bf16(q[4] * rq, q[5] * rq), pack_bf16(q[6] * rq, q[7] * rq));
         }
+        if (kMlp)   // the adaptive weights of the tile's tokens (0 off the grid)
+            for (int x = tid; x < kTileTok * p.T; x += kTileThreads) {
+                const int uu = x / p.T, t = x % p.T;
+                const int rr = r0 + uu / 8, cc = c0 + uu % 8;
+                wts_t[uu][t] =
+                    (rr < p.H && cc < p.W) ? b.wtok[((size_t)sl * p.n + rr * p.W + cc) * p.T + t] : 0.f;
+            }
         __syncthreads();
 
         // ---- the three products: warp = 16 tokens (mt) x 16 columns (sb) of each
         //   dQ~ = [dO | K] [alpha Ubar^T ; dM],  dK = [V | Q~] [dU_1^T ; dM^T],  dV = K dU_1
+        // (adaptive weights: the image holds alpha U_1^T where alpha Ubar^T stands, and
+        // the dO half of dQ~'s sum is scaled by each token's own w_1)
         {
             const int mt = warp & 3, sb = warp >> 2;
             const int ua = 16 * mt + (lane & 15), acol = (lane >> 4) * 8;
@@ -1629,6 +1641,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                 const int brow0 = pr == 0 ? 0 : (pr == 1 ? 128 : 256);
                 const int ksteps = pr == 2 ? 4 : 8;
                 float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                float accw[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};   // kMlp: dO U_1^T alpha
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     if (ks >= ksteps) break;
@@ -1640,11 +1653,26 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                     uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
                     ldsm_x4(aaddr, a0, a1, a2, a3);
                     ldsm_x4_t(bs + (uint32_t)((brow0 + 16 * ks + brow) * kBS + bcol) * 2u, b0, b1, b2, b3);
-                    mma_bf16_16816(acc[0], a0, a1, a2, a3, b0, b1);
-                    mma_bf16_16816(acc[1], a0, a1, a2, a3, b2, b3);
+                    if (kMlp && pr == 0 && ks < 4) {
+                        mma_bf16_16816(accw[0], a0, a1, a2, a3, b0, b1);
+                        mma_bf16_16816(accw[1], a0, a1, a2, a3, b2, b3);
+                    } else {
+                        mma_bf16_16816(acc[0], a0, a1, a2, a3, b0, b1);
+                        mma_bf16_16816(acc[1], a0, a1, a2, a3, b2, b3);
+                    }
                 }
                 float *out = pr == 0 ? oQ : (pr == 1 ? oK : oV);
                 const int row = 16 * mt + (lane >> 2);
+                if (kMlp && pr == 0) {
+                    const float w1a = p.T > 1 ? wts_t[row][1] : 0.f, w1b = p.T > 1 ? wts_t[row + 8][1] : 0.f;
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        acc[nt][0] = fmaf(w1a, accw[nt][0], acc[nt][0]);
+                        acc[nt][1] = fmaf(w1a, accw[nt][1], acc[nt][1]);
+                        acc[nt][2] = fmaf(w1b, accw[nt][2], acc[nt][2]);
+                        acc[nt][3] = fmaf(w1b, accw[nt][3], acc[nt][3]);
+                    }
+                }
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
                     const int col = 16 * sb + 8 * nt + 2 * (lane & 3);
@@ -1655,44 +1683,32 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                 }
             }
         }
-        if (kMlp) {
-            // ---- adaptive weights: each token's own walk terms, which the shared
-            // products leave out: dQ~_u += alpha sum_{k>=1} w_uk dO_u U_k^T, as
-            // dO U_k^T on mma.sync per k (U_k's bf16 hi + lo rows staged where the
-            // B image was, read as the B operand without transposition), each
-            // row scaled by its token's alpha w_uk
-            for (int x = tid; x < kTileTok * p.T; x += kTileThreads) {
-                const int uu = x / p.T, t = x % p.T;
-                const int rr = r0 + uu / 8, cc = c0 + uu % 8;
-                wts_t[uu][t] =
-                    (rr < p.H && cc < p.W) ? b.wtok[((size_t)sl * p.n + rr * p.W + cc) * p.T + t] : 0.f;
-            }
+        if (kMlp && p.T > 2) {
+            // ---- adaptive weights: the walk terms of k >= 2, dQ~_u += alpha w_uk dO_u U_k^T,
+            // as dO U_k^T on mma.sync per k (alpha U_k^T's bf16 image staged where Q~ was,
+            // which the products no longer read), each row scaled by its token's w_uk
             const int mt = warp & 3, sb = warp >> 2;
             const int hrow = halo_row(16 * mt + (lane & 15), 0, 0);
-            const int nrow = 16 * sb + (lane & 7) + 8 * (lane >> 4), kofs = ((lane >> 3) & 1) * 8;
+            const int mi = lane >> 3, brow = (mi & 1) * 8 + (lane & 7), bcol = 16 * sb + (mi >> 1) * 8;
             const int row = 16 * mt + (lane >> 2);
-            for (int kk = 1; kk < p.T; ++kk) {
-                __syncthreads();   // nothing reads the B region any more; the weights are in place
+            for (int kk = 2; kk < p.T; ++kk) {
+                __syncthreads();   // the products (or the previous k) no longer read the Q~ region
                 const uint4 *img =
-                    reinterpret_cast<const uint4 *>(b.ukimg + ((size_t)sl * b.nh + (kk - 1)) * 2 * 64 * kQS);
-                for (int x = tid; x < 2 * 64 * kQS / 8; x += kTileThreads) reinterpret_cast<uint4 *>(Bs)[x] = img[x];
+                    reinterpret_cast<const uint4 *>(b.ukimgT + ((size_t)sl * b.nh + (kk - 1)) * 64 * kQS);
+                for (int x = tid; x < 64 * kQS / 8; x += kTileThreads) reinterpret_cast<uint4 *>(Qt)[x] = img[x];
                 __syncthreads();
                 float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
-                    uint32_t a0, a1, a2, a3;
+                    uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
                     ldsm_x4(smem_u32(Gc) + hoff(hrow, 2 * ks + (lane >> 4)), a0, a1, a2, a3);
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint32_t b0, b1, b2, b3;
-                        ldsm_x4(smem_u32(Bs) + (uint32_t)((h * 64 + nrow) * kQS + 16 * ks + kofs) * 2u, b0, b1, b2, b3);
-                        mma_bf16_16816(acc[0], a0, a1, a2, a3, b0, b1);
-                        mma_bf16_16816(acc[1], a0, a1, a2, a3, b2, b3);
-                    }
+                    ldsm_x4_t(smem_u32(Qt) + (uint32_t)((16 * ks + brow) * kQS + bcol) * 2u, b0, b1, b2, b3);
+                    mma_bf16_16816(acc[0], a0, a1, a2, a3, b0, b1);
+                    mma_bf16_16816(acc[1], a0, a1, a2, a3, b2, b3);
                 }
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const float wk = al * wts_t[row + 8 * h][kk];
+                    const float wk = wts_t[row + 8 * h][kk];
 #pragma unroll
                     for (int nt = 0; nt < 2; ++nt) {
                         const int col = 16 * sb + 8 * nt + 2 * (lane & 3);
@@ -1702,7 +1718,6 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                     }
                 }
             }
-            img_sl = -1;   // the B region holds U_k now: the next tile stages its B image again
         }
         __syncthreads();
 
@@ -1925,9 +1940,10 @@ constexpr int kMlpTcSmemBytes = kTpb * kMA * 2              // [Q | K] rows
                                 + 3 * kTpb * 68 * 4         // pre-activations (then da), g, V and dO rows (fp32)
                                 + kTpb * 68 * 4;
 
-// The tensor-core MLP pass's bf16 operand images, once per backward: block
-// (slice, k) writes U_k (row-major) as hi and lo rows of kQS columns, the last
-// block W1 as hi and lo rows of kMA columns (rows hidden .. kMH - 1 zero).
+// The tensor-core MLP passes' bf16 operand images, once per backward: block
+// (slice, k) writes U_k (row-major) as hi and lo rows of kQS columns and
+// alpha U_k^T (row c, column a) rounded to bf16, the last block W1 as hi and lo
+// rows of kMA columns (rows hidden .. kMH - 1 zero).
 __global__ void __launch_bounds__(kThreads) bwd_mlp_images(BwdProblem b) {
     constexpr int D = 64;
     const Problem &p = b.fwd;
@@ -1935,9 +1951,12 @@ __global__ void __launch_bounds__(kThreads) bwd_mlp_images(BwdProblem b) {
     if (blockIdx.x < (unsigned)(p.slices * b.nh)) {
         const float *Un = b.Ukn + (size_t)blockIdx.x * D * D;
         uint16_t *img = b.ukimg + (size_t)blockIdx.x * 2 * 64 * kQS;
+        uint16_t *imgT = b.ukimgT + (size_t)blockIdx.x * 64 * kQS;
+        const float al = p.alpha[(blockIdx.x / b.nh) % p.heads];
         for (int x = tid; x < D * D; x += kThreads) {
             const float uv = Un[x];
             const __nv_bfloat16 hi = __float2bfloat16_rn(uv);
+            imgT[(x & 63) * kQS + (x >> 6)] = __bfloat16_as_ushort(__float2bfloat16_rn(al * uv));
             img[(x >> 6) * kQS + (x & 63)] = __bfloat16_as_ushort(hi);
             const float lo = uv - __bfloat162float(hi);
             img[64 * kQS + (x >> 6) * kQS + (x & 63)] = __bfloat16_as_ushort(__float2bfloat16_rn(lo));

@@ -47,6 +47,7 @@ struct BwdProblem {
     float *Ukn;          // [S][nh][D][D]  U_1 .. U_(T-1), row-major
     uint16_t *ukimg;     // [S][nh][2][64][72] bf16: U_k rows as hi, lo terms (72-wide rows; bf16, d = 64)
     uint16_t *w1img;     // [2][64][136] bf16: W1 rows as hi, lo terms (136-wide rows; bf16, d = 64)
+    uint16_t *ukimgT;    // [S][nh][64][72] bf16: alpha U_k^T, row c, column a (72-wide rows; bf16, d = 64)
     float *wtok;         // [S][n][T]      per-token walk weights w_i
     float *dzbuf;        // [S][n][T]      dL/dz_i (softmax logits)
     float *hbuf;         // [S][n][hid]    h_i = GELU(W1 x_i + b1)
