@@ -1576,6 +1576,12 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         // the next tile's halo streams in while this one computes; its buffer
         // was last read by the tile before this one, which ended on a barrier
         if (t + 1 < t_end && tid == 0) stage_halo(t + 1, cur ^ 1);
+        float wpre = 0.f;   // adaptive weights: this thread's w of the tile, in flight during the halo wait
+        if (kMlp && tid < kTileTok * p.T) {
+            const int tsl = t / b.ntile, ttile = t % b.ntile, uu = tid / p.T;
+            const int rr = (ttile / tiles_c) * 8 + uu / 8, cc = (ttile % tiles_c) * 8 + uu % 8;
+            if (rr < p.H && cc < p.W) wpre = b.wtok[((size_t)tsl * p.n + rr * p.W + cc) * p.T + tid % p.T];
+        }
         if (!mbar_wait(smem_u32(&hbar[cur]), (uint32_t)(it >> 1) & 1u)) record_error(p.err, kErrTimeoutLoad);
         const int sl = t / b.ntile, tile = t % b.ntile;
         const int r0 = (tile / tiles_c) * 8, c0 = (tile % tiles_c) * 8;
@@ -1616,13 +1622,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                 make_uint4(pack_bf16(q[0] * rq, q[1] * rq), pack_bf16(q[2] * rq, q[3] * rq),
                            pack_bf16(q[4] * rq, q[5] * rq), pack_bf16(q[6] * rq, q[7] * rq));
         }
-        if (kMlp)   // the adaptive weights of the tile's tokens (0 off the grid)
-            for (int x = tid; x < kTileTok * p.T; x += kTileThreads) {
-                const int uu = x / p.T, t = x % p.T;
-                const int rr = r0 + uu / 8, cc = c0 + uu % 8;
-                wts_t[uu][t] =
-                    (rr < p.H && cc < p.W) ? b.wtok[((size_t)sl * p.n + rr * p.W + cc) * p.T + t] : 0.f;
-            }
+        if (kMlp && tid < kTileTok * p.T) wts_t[tid / p.T][tid % p.T] = wpre;   // 0 off the grid
         __syncthreads();
 
         // ---- the three products: warp = 16 tokens (mt) x 16 columns (sb) of each
@@ -1726,6 +1726,12 @@ __global__ void __launch_bounds__(kTileThreads, 1)
             float dsl[8];
             const int y = u / 8, xx = u % 8;
             const bool live = r0 + y < p.H && c0 + xx < p.W;
+            float4 xm[4];   // adaptive weights: the MLP's share of [dq | dk] for these channels
+            if (kMlp && live) {
+                const float4 *src = reinterpret_cast<const float4 *>(
+                    b.dxm + ((size_t)sl * p.n + (r0 + y) * p.W + c0 + xx) * 2 * D + c8);
+                xm[0] = src[0], xm[1] = src[1], xm[2] = src[16], xm[3] = src[17];
+            }
             float q[8], dqt[8];
             lds8_sw(Qc, halo_row(u, 0, 0), c8 >> 3, q);
 #pragma unroll
@@ -1733,6 +1739,15 @@ __global__ void __launch_bounds__(kTileThreads, 1)
             const float rq = rqs[u];
             const float cj = group8_sum(dot8(dqt, q)) * rq * rq;
             if ((lane & 7) == 0) cjs[u] = cj;
+            if (kMlp && live) {   // oQ becomes dq before the window term (dQ~ rq - cj s + the MLP's dq), oK gains dk
+                const float xq[8] = {xm[0].x, xm[0].y, xm[0].z, xm[0].w, xm[1].x, xm[1].y, xm[1].z, xm[1].w};
+                const float xk[8] = {xm[2].x, xm[2].y, xm[2].z, xm[2].w, xm[3].x, xm[3].y, xm[3].z, xm[3].w};
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    oQ[u * kOS + c8 + e] = dqt[e] * rq - cj * s[c8 + e] + xq[e];
+                    oK[u * kOS + c8 + e] += xk[e];
+                }
+            }
 #pragma unroll
             for (int e = 0; e < 8; ++e) dsl[e] = live ? -cj * q[e] : 0.f;
             // the warp's four tokens' ds terms, summed over the quarters in a fixed order
@@ -1872,21 +1887,16 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                 if (rr >= p.H || cc >= p.W) continue;
                 const size_t jt = (size_t)(rr * p.W + cc) * D;
                 const float rq = rqs[ut], cj = cjs[ut];
-                // adaptive weights: the MLP's share of [dq | dk] and the token's own w_0
-                const float *xm = kMlp ? b.dxm + ((size_t)sl * p.n + rr * p.W + cc) * 2 * D : nullptr;
-                const float wv0 = kMlp ? wts_t[ut][0] : w0;
+                const float wv0 = kMlp ? wts_t[ut][0] : w0;   // adaptive weights: the token's own w_0
 #pragma unroll
                 for (int nt = 0; nt < 8; ++nt) {
                     const int col = 8 * nt + 2 * q4;
                     const float x0 = acc[nt][2 * h], x1 = acc[nt][2 * h + 1];
                     if (role == 0) {
-                        float d0 = oQ[ut * kOS + col] * rq - cj * s[col] + x0;
-                        float d1 = oQ[ut * kOS + col + 1] * rq - cj * s[col + 1] + x1;
-                        if (kMlp) {
-                            const float2 xq = *reinterpret_cast<const float2 *>(xm + col);
-                            d0 += xq.x;
-                            d1 += xq.y;
-                        }
+                        // (adaptive weights: oQ already holds dq before the window term)
+                        float d0 = kMlp ? oQ[ut * kOS + col] + x0 : oQ[ut * kOS + col] * rq - cj * s[col] + x0;
+                        float d1 = kMlp ? oQ[ut * kOS + col + 1] + x1
+                                        : oQ[ut * kOS + col + 1] * rq - cj * s[col + 1] + x1;
                         if (p.relu) {   // dXq through the feature map (the staged Q is ReLU'd)
                             const uint32_t qp =
                                 *reinterpret_cast<const uint32_t *>(Qc + hoff(hrow_b(m), col >> 3) + (col & 7) * 2);
@@ -1895,13 +1905,8 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                         }
                         *reinterpret_cast<uint32_t *>(dQo + jt + col) = pack_bf16(d0, d1);
                     } else if (role == 1) {
-                        float k0 = oK[ut * kOS + col] + x0, k1 = oK[ut * kOS + col + 1] + x1;
-                        if (kMlp) {
-                            const float2 xk = *reinterpret_cast<const float2 *>(xm + D + col);
-                            k0 += xk.x;
-                            k1 += xk.y;
-                        }
-                        *reinterpret_cast<float2 *>(dKp + jt + col) = make_float2(k0, k1);
+                        *reinterpret_cast<float2 *>(dKp + jt + col) =
+                            make_float2(oK[ut * kOS + col] + x0, oK[ut * kOS + col + 1] + x1);
                     } else {
                         const uint32_t gp =
                             *reinterpret_cast<const uint32_t *>(Gc + hoff(hrow_b(m), col >> 3) + (col & 7) * 2);
