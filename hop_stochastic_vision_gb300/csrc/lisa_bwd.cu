@@ -1995,44 +1995,8 @@ __global__ void __launch_bounds__(kThreads) bwd_token_mlp_tc(BwdProblem b) {
     __shared__ float part[kWarps];
     const Problem &p = b.fwd;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int sl = blockIdx.x / b.nblk, blk = blockIdx.x % b.nblk;
-    const int j0 = blk * kTpb, cnt = min(kTpb, p.n - j0);
     const int T = p.T, hid = p.hidden, nmh = (hid + 15) / 16 * 16;
-    const size_t sbase = (size_t)sl * p.n * D;
-    const __nv_bfloat16 *Q = static_cast<const __nv_bfloat16 *>(p.Q) + sbase;
-    const __nv_bfloat16 *K = static_cast<const __nv_bfloat16 *>(p.K) + sbase;
-    const __nv_bfloat16 *V = static_cast<const __nv_bfloat16 *>(p.V) + sbase;
-    const __nv_bfloat16 *dO = static_cast<const __nv_bfloat16 *>(b.dO) + sbase;
-    const float *s = p.s_red + (size_t)sl * D;
-    const float al = p.alpha[sl % p.heads];
-
-    // ---- stage [Q | K] (feature-mapped), V and dO rows (fp32), W1 as bf16 hi + lo
-    for (int x = tid; x < kTpb * 8; x += kThreads) {
-        const int j = x >> 3, c = x & 7;
-        uint4 q = make_uint4(0u, 0u, 0u, 0u), k = q, v = q, g = q;
-        if (j < cnt) {
-            const size_t o = ((size_t)(j0 + j) * D) / 8 + c;
-            q = reinterpret_cast<const uint4 *>(Q)[o];
-            k = reinterpret_cast<const uint4 *>(K)[o];
-            v = reinterpret_cast<const uint4 *>(V)[o];
-            g = reinterpret_cast<const uint4 *>(dO)[o];
-            if (p.relu) {
-                q = make_uint4(relu_bf16x2(q.x), relu_bf16x2(q.y), relu_bf16x2(q.z), relu_bf16x2(q.w));
-                k = make_uint4(relu_bf16x2(k.x), relu_bf16x2(k.y), relu_bf16x2(k.z), relu_bf16x2(k.w));
-            }
-        }
-        *reinterpret_cast<uint4 *>(Qk + j * kMA + c * 8) = q;
-        *reinterpret_cast<uint4 *>(Qk + j * kMA + 64 + c * 8) = k;
-        const uint32_t vv[4] = {v.x, v.y, v.z, v.w}, gg[4] = {g.x, g.y, g.z, g.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            Vs[j * 68 + c * 8 + 2 * e] = bf16_lo(vv[e]);
-            Vs[j * 68 + c * 8 + 2 * e + 1] = bf16_hi(vv[e]);
-            Gs[j * 68 + c * 8 + 2 * e] = bf16_lo(gg[e]);
-            Gs[j * 68 + c * 8 + 2 * e + 1] = bf16_hi(gg[e]);
-        }
-    }
-    {   // W1 hi and lo rows from the precomputed image (the rows below nmh of each)
+    {   // W1 hi and lo rows from the precomputed image (the rows below nmh of each), once per CTA
         constexpr int kRowV = kMA / 8;   // 16-byte pieces per row
         const uint4 *img = reinterpret_cast<const uint4 *>(b.w1img);
         for (int x = tid; x < 2 * nmh * kRowV; x += kThreads) {
@@ -2040,292 +2004,335 @@ __global__ void __launch_bounds__(kThreads) bwd_token_mlp_tc(BwdProblem b) {
             reinterpret_cast<uint4 *>(W1i + h * kMH * kMA)[y] = img[h * kMH * kRowV + y];
         }
     }
-    for (int x = tid; x < TM * kTpb * 4; x += kThreads) (&dwp[0][0][0])[x] = 0.f;
-    __syncthreads();
-    for (int j = warp; j < kTpb; j += kWarps) {   // 1 / (Q_j . s + eps)
-        float d = 0.f;
-        for (int ch = lane; ch < D; ch += 32) d += __bfloat162float(Qk[j * kMA + ch]) * s[ch];
-        d = warp_sum(d);
-        if (lane == 0) rqs[j] = 1.f / (d + p.eps);
-    }
+    // persistent: the CTA walks blocks of kTpb tokens; W1 stays staged
+    const int nbt = p.slices * b.nblk;
+    for (int bi = blockIdx.x; bi < nbt; bi += gridDim.x) {
+        const int sl = bi / b.nblk, blk = bi % b.nblk;
+        const int j0 = blk * kTpb, cnt = min(kTpb, p.n - j0);
+        const size_t sbase = (size_t)sl * p.n * D;
+        const __nv_bfloat16 *Q = static_cast<const __nv_bfloat16 *>(p.Q) + sbase;
+        const __nv_bfloat16 *K = static_cast<const __nv_bfloat16 *>(p.K) + sbase;
+        const __nv_bfloat16 *V = static_cast<const __nv_bfloat16 *>(p.V) + sbase;
+        const __nv_bfloat16 *dO = static_cast<const __nv_bfloat16 *>(b.dO) + sbase;
+        const float *s = p.s_red + (size_t)sl * D;
+        const float al = p.alpha[sl % p.heads];
 
-    // ---- hidden pre-activations [Q | K] W1^T + b1: warp = 16 tokens x 16 hidden units
-    {
-        const int mt = warp & 1, pr = warp >> 1;   // n-tiles 2 pr, 2 pr + 1
-        if (16 * pr < nmh) {
-            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            const uint32_t qa = smem_u32(Qk) + (uint32_t)((16 * mt + (lane & 15)) * kMA + (lane >> 4) * 8) * 2u;
-            const int wrow = 16 * pr + (lane & 7) + 8 * (lane >> 4);
+        // ---- stage [Q | K] (feature-mapped), V and dO rows (fp32), W1 as bf16 hi + lo
+        for (int x = tid; x < kTpb * 8; x += kThreads) {
+            const int j = x >> 3, c = x & 7;
+            uint4 q = make_uint4(0u, 0u, 0u, 0u), k = q, v = q, g = q;
+            if (j < cnt) {
+                const size_t o = ((size_t)(j0 + j) * D) / 8 + c;
+                q = reinterpret_cast<const uint4 *>(Q)[o];
+                k = reinterpret_cast<const uint4 *>(K)[o];
+                v = reinterpret_cast<const uint4 *>(V)[o];
+                g = reinterpret_cast<const uint4 *>(dO)[o];
+                if (p.relu) {
+                    q = make_uint4(relu_bf16x2(q.x), relu_bf16x2(q.y), relu_bf16x2(q.z), relu_bf16x2(q.w));
+                    k = make_uint4(relu_bf16x2(k.x), relu_bf16x2(k.y), relu_bf16x2(k.z), relu_bf16x2(k.w));
+                }
+            }
+            *reinterpret_cast<uint4 *>(Qk + j * kMA + c * 8) = q;
+            *reinterpret_cast<uint4 *>(Qk + j * kMA + 64 + c * 8) = k;
+            const uint32_t vv[4] = {v.x, v.y, v.z, v.w}, gg[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4(qa + (uint32_t)(16 * ks) * 2u, a0, a1, a2, a3);
+            for (int e = 0; e < 4; ++e) {
+                Vs[j * 68 + c * 8 + 2 * e] = bf16_lo(vv[e]);
+                Vs[j * 68 + c * 8 + 2 * e + 1] = bf16_hi(vv[e]);
+                Gs[j * 68 + c * 8 + 2 * e] = bf16_lo(gg[e]);
+                Gs[j * 68 + c * 8 + 2 * e + 1] = bf16_hi(gg[e]);
+            }
+        }
+        for (int x = tid; x < TM * kTpb * 4; x += kThreads) (&dwp[0][0][0])[x] = 0.f;
+        __syncthreads();
+        for (int j = warp; j < kTpb; j += kWarps) {   // 1 / (Q_j . s + eps)
+            float d = 0.f;
+            for (int ch = lane; ch < D; ch += 32) d += __bfloat162float(Qk[j * kMA + ch]) * s[ch];
+            d = warp_sum(d);
+            if (lane == 0) rqs[j] = 1.f / (d + p.eps);
+        }
+
+        // ---- hidden pre-activations [Q | K] W1^T + b1: warp = 16 tokens x 16 hidden units
+        {
+            const int mt = warp & 1, pr = warp >> 1;   // n-tiles 2 pr, 2 pr + 1
+            if (16 * pr < nmh) {
+                float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                const uint32_t qa = smem_u32(Qk) + (uint32_t)((16 * mt + (lane & 15)) * kMA + (lane >> 4) * 8) * 2u;
+                const int wrow = 16 * pr + (lane & 7) + 8 * (lane >> 4);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(qa + (uint32_t)(16 * ks) * 2u, a0, a1, a2, a3);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t b0, b1, b2, b3;
+                        const uint32_t wofs = (uint32_t)(h * kMH * kMA + wrow * kMA + 16 * ks + ((lane >> 3) & 1) * 8);
+                        ldsm_x4(smem_u32(W1i) + wofs * 2u, b0, b1, b2, b3);
+                        mma_bf16_16816(acc[0], a0, a1, a2, a3, b0, b1);
+                        mma_bf16_16816(acc[1], a0, a1, a2, a3, b2, b3);
+                    }
+                }
+                const int row = 16 * mt + (lane >> 2);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int m = 16 * pr + 8 * nt + 2 * (lane & 3);
+                    const float b10 = m < hid ? p.b1[m] : 0.f, b11 = m + 1 < hid ? p.b1[m + 1] : 0.f;
+                    pre[row * 68 + m] = acc[nt][0] + b10;
+                    pre[row * 68 + m + 1] = acc[nt][1] + b11;
+                    pre[(row + 8) * 68 + m] = acc[nt][2] + b10;
+                    pre[(row + 8) * 68 + m + 1] = acc[nt][3] + b11;
+                }
+            }
+        }
+        __syncthreads();
+        // ---- per token (a quarter-warp, lanes over hidden units): h = GELU(a),
+        // z = W2 h + b2, w = softmax(z)
+        const int qg = lane >> 3, l8 = lane & 7;
+        const int uq = 4 * warp + qg;   // this quarter's token of the block
+        {
+            float zt[TM];
+#pragma unroll
+            for (int t = 0; t < TM; ++t) zt[t] = 0.f;
+            for (int m = l8; m < hid; m += 8) {
+                const float h = gelu_exact(pre[uq * 68 + m]);
+#pragma unroll
+                for (int t = 0; t < TM; ++t)
+                    if (t < T) zt[t] = fmaf(p.W2[(size_t)t * hid + m], h, zt[t]);
+                if (uq < cnt) b.hbuf[((size_t)sl * p.n + j0 + uq) * hid + m] = h;
+            }
+            float zmax = -INFINITY, zs = 0.f;
+#pragma unroll
+            for (int t = 0; t < TM; ++t)
+                if (t < T) {
+                    zt[t] = group8_sum(zt[t]) + p.b2[t];
+                    zmax = fmaxf(zmax, zt[t]);
+                }
+#pragma unroll
+            for (int t = 0; t < TM; ++t)
+                if (t < T) {
+                    zt[t] = expf(zt[t] - zmax);
+                    zs += zt[t];
+                }
+#pragma unroll
+            for (int t = 0; t < TM; ++t)
+                if (t < T && t == l8) wts[uq][t] = zt[t] / zs;
+        }
+        __syncthreads();
+
+        // ---- walk terms Y_k = Q U_k on the tensor cores; g = sum_k w_k Y_k rq, and
+        // dw_k partials alpha dO . Y_k rq per row and 16-column group
+        {
+            const int mt = warp & 1, sb = warp >> 1;
+            const uint32_t qa = smem_u32(Qk) + (uint32_t)((16 * mt + (lane & 15)) * kMA + (lane >> 4) * 8) * 2u;
+            const int mi = lane >> 3, brow = (mi & 1) * 8 + (lane & 7), bcol = 16 * sb + (mi >> 1) * 8;
+            const int r0 = 16 * mt + (lane >> 2);
+            float gacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            for (int kk = 1; kk < T; ++kk) {
+                {   // U_k's bf16 hi and lo rows from the precomputed image
+                    const uint4 *img =
+                        reinterpret_cast<const uint4 *>(b.ukimg + ((size_t)sl * b.nh + (kk - 1)) * 2 * 64 * kQS);
+                    for (int x = tid; x < 2 * 64 * kQS / 8; x += kThreads) reinterpret_cast<uint4 *>(Ui)[x] = img[x];
+                }
+                __syncthreads();
+                float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(qa + (uint32_t)(16 * ks) * 2u, a0, a1, a2, a3);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4_t(smem_u32(Ui) + (uint32_t)((h * 64 + 16 * ks + brow) * kQS + bcol) * 2u, b0, b1, b2,
+                                  b3);
+                        mma_bf16_16816(acc[0], a0, a1, a2, a3, b0, b1);
+                        mma_bf16_16816(acc[1], a0, a1, a2, a3, b2, b3);
+                    }
+                }
+                float dwr[2] = {0.f, 0.f};   // rows r0, r0 + 8
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(smem_u32(W1i) + (uint32_t)(h * kMH * kMA + wrow * kMA + 16 * ks + ((lane >> 3) & 1) * 8) * 2u,
-                            b0, b1, b2, b3);
-                    mma_bf16_16816(acc[0], a0, a1, a2, a3, b0, b1);
-                    mma_bf16_16816(acc[1], a0, a1, a2, a3, b2, b3);
+                    const int row = r0 + 8 * h;
+                    const float rq = rqs[row], wk = wts[row][kk];
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const int col = 16 * sb + 8 * nt + 2 * (lane & 3);
+                        const float y0 = acc[nt][2 * h] * rq, y1 = acc[nt][2 * h + 1] * rq;
+                        gacc[nt][2 * h] = fmaf(wk, y0, gacc[nt][2 * h]);
+                        gacc[nt][2 * h + 1] = fmaf(wk, y1, gacc[nt][2 * h + 1]);
+                        dwr[h] = fmaf(Gs[row * 68 + col], y0, fmaf(Gs[row * 68 + col + 1], y1, dwr[h]));
+                    }
+                    dwr[h] += __shfl_xor_sync(0xffffffffu, dwr[h], 1);
+                    dwr[h] += __shfl_xor_sync(0xffffffffu, dwr[h], 2);
+                }
+                if ((lane & 3) == 0) {
+                    dwp[kk][r0][sb] = al * dwr[0];
+                    dwp[kk][r0 + 8][sb] = al * dwr[1];
+                }
+                __syncthreads();   // every read of this U_k image is done
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int col = 16 * sb + 8 * nt + 2 * (lane & 3);
+                    G[(r0 + 8 * h) * 68 + col] = gacc[nt][2 * h];
+                    G[(r0 + 8 * h) * 68 + col + 1] = gacc[nt][2 * h + 1];
+                }
+        }
+        __syncthreads();
+
+        // ---- per token (a quarter-warp): the window (as bwd_token_a), dalpha terms,
+        // the softmax's and the MLP's elementwise backward; da as bf16 hi + lo
+        {
+            const int c8 = 8 * l8;
+            const bool live = uq < cnt;
+            const int i = j0 + (live ? uq : 0);
+            const int r = i / p.W, c = i % p.W;
+            float q[8], v[8], go[8], g[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                q[e] = __bfloat162float(Qk[uq * kMA + c8 + e]);
+                v[e] = Vs[uq * 68 + c8 + e];
+                go[e] = Gs[uq * 68 + c8 + e];
+                g[e] = fmaf(wts[uq][0], v[e], G[uq * 68 + c8 + e]);
+            }
+            float ev[9];
+#pragma unroll
+            for (int t9 = 0; t9 < 9; ++t9) {
+                const int rr = r + t9 / 3 - 1, cc = c + t9 % 3 - 1;
+                const bool in = rr >= 0 && rr < p.H && cc >= 0 && cc < p.W;
+                float kr[8];
+                load8_bf16(K + (size_t)(in ? rr * p.W + cc : i) * D + c8, kr, p.relu);
+                ev[t9] = dot8(q, kr);
+            }
+            // the group sums run on every lane (each shuffle needs all 32); the mask after
+#pragma unroll
+            for (int t9 = 0; t9 < 9; ++t9) ev[t9] = group8_sum(ev[t9]);
+            float emax = -INFINITY;
+#pragma unroll
+            for (int t9 = 0; t9 < 9; ++t9) {
+                const int rr = r + t9 / 3 - 1, cc = c + t9 % 3 - 1;
+                const bool in = rr >= 0 && rr < p.H && cc >= 0 && cc < p.W;
+                ev[t9] = in ? ev[t9] * 0.125f : -INFINITY;
+                emax = fmaxf(emax, ev[t9]);
+            }
+            float l[8], esum = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) l[e] = 0.f;
+#pragma unroll
+            for (int t9 = 0; t9 < 9; ++t9) {
+                const int rr = r + t9 / 3 - 1, cc = c + t9 % 3 - 1;
+                const bool in = rr >= 0 && rr < p.H && cc >= 0 && cc < p.W;
+                const float a = in ? expf(ev[t9] - emax) : 0.f;
+                esum += a;
+                float vr[8];
+                load8_bf16(V + (size_t)(in ? rr * p.W + cc : i) * D + c8, vr, false);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) l[e] = fmaf(a, vr[e], l[e]);
+            }
+            const float inv = 1.f / esum;
+            float dgl = 0.f, dll = 0.f, dgv = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                l[e] *= inv;
+                dgl = fmaf(go[e], g[e] - l[e], dgl);
+                dll = fmaf(go[e], l[e], dll);
+                dgv = fmaf(go[e], v[e], dgv);   // dw_0 / alpha
+            }
+            dgl = group8_sum(dgl);
+            dll = group8_sum(dll);
+            dgv = group8_sum(dgv);
+            const size_t ti = (size_t)sl * p.n + i;
+            if (l8 == 0 && live)
+                reinterpret_cast<float4 *>(b.lstat)[ti] = make_float4(emax, esum, dll * (1.f - al), 0.f);
+            // dz = w (dw - w . dw), dw_0 = alpha dO . V, dw_k from the partials
+            float w[TM], dw[TM], wdw = 0.f;
+#pragma unroll
+            for (int t = 0; t < TM; ++t) {
+                w[t] = t < T ? wts[uq][t] : 0.f;
+                dw[t] = t == 0 ? al * dgv
+                               : (t < T ? ((dwp[t][uq][0] + dwp[t][uq][1]) + (dwp[t][uq][2] + dwp[t][uq][3])) : 0.f);
+                wdw = fmaf(w[t], dw[t], wdw);
+            }
+            float dz[TM];
+#pragma unroll
+            for (int t = 0; t < TM; ++t) dz[t] = w[t] * (dw[t] - wdw);
+            if (live) {
+#pragma unroll
+                for (int t = 0; t < TM; ++t)
+                    if (t < T && t == l8) {
+                        b.wtok[ti * T + t] = w[t];
+                        b.dzbuf[ti * T + t] = dz[t];
+                    }
+            }
+            for (int m = l8; m < nmh; m += 8) {
+                float da = 0.f;
+                if (m < hid && live) {
+                    float dh = 0.f;
+#pragma unroll
+                    for (int t = 0; t < TM; ++t)
+                        if (t < T) dh = fmaf(p.W2[(size_t)t * hid + m], dz[t], dh);
+                    da = dh * gelu_exact_grad(pre[uq * 68 + m]);
+                    b.dabuf[ti * hid + m] = da;
+                }
+                const __nv_bfloat16 hi = __float2bfloat16_rn(da);
+                Di[uq * kQS + m] = hi;
+                Di[kTpb * kQS + uq * kQS + m] = __float2bfloat16_rn(da - __bfloat162float(hi));
+            }
+            // dalpha terms of the warp's live tokens, in token order
+            float dal = (l8 == 0 && live) ? dgl : 0.f;
+            dal = warp_sum(dal);
+            if (lane == 0) part[warp] = dal;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            float acc = 0.f;
+            for (int w2 = 0; w2 < kWarps; ++w2) acc += part[w2];
+            b.dal_part[(size_t)sl * b.nblk + blk] = acc;
+        }
+
+        // ---- the MLP's share of [dq | dk] = da W1: warp = 16 tokens x 32 channels
+        {
+            const int mt = warp & 1, cg = warp >> 1;   // channels 32 cg .. 32 cg + 31
+            const uint32_t da0 = smem_u32(Di) + (uint32_t)((16 * mt + (lane & 15)) * kQS + (lane >> 4) * 8) * 2u;
+            const int mi = lane >> 3, brow = (mi & 1) * 8 + (lane & 7);
+            float acc[4][4];
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+            for (int ks = 0; 16 * ks < nmh; ++ks) {
+#pragma unroll
+                for (int ah = 0; ah < 2; ++ah) {   // da hi, lo
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(da0 + (uint32_t)(ah * kTpb * kQS + 16 * ks) * 2u, a0, a1, a2, a3);
+#pragma unroll
+                    for (int wh = 0; wh < 2; ++wh) {   // W1 hi, lo (lo x lo left out)
+                        if (ah == 1 && wh == 1) continue;
+#pragma unroll
+                        for (int np = 0; np < 2; ++np) {
+                            const int bcol = 32 * cg + 16 * np + (mi >> 1) * 8;
+                            uint32_t b0, b1, b2, b3;
+                            ldsm_x4_t(smem_u32(W1i) + (uint32_t)(wh * kMH * kMA + (16 * ks + brow) * kMA + bcol) * 2u,
+                                      b0, b1, b2, b3);
+                            mma_bf16_16816(acc[2 * np], a0, a1, a2, a3, b0, b1);
+                            mma_bf16_16816(acc[2 * np + 1], a0, a1, a2, a3, b2, b3);
+                        }
+                    }
                 }
             }
             const int row = 16 * mt + (lane >> 2);
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int m = 16 * pr + 8 * nt + 2 * (lane & 3);
-                const float b10 = m < hid ? p.b1[m] : 0.f, b11 = m + 1 < hid ? p.b1[m + 1] : 0.f;
-                pre[row * 68 + m] = acc[nt][0] + b10;
-                pre[row * 68 + m + 1] = acc[nt][1] + b11;
-                pre[(row + 8) * 68 + m] = acc[nt][2] + b10;
-                pre[(row + 8) * 68 + m + 1] = acc[nt][3] + b11;
-            }
-        }
-    }
-    __syncthreads();
-    // ---- per token (a quarter-warp, lanes over hidden units): h = GELU(a),
-    // z = W2 h + b2, w = softmax(z)
-    const int qg = lane >> 3, l8 = lane & 7;
-    const int uq = 4 * warp + qg;   // this quarter's token of the block
-    {
-        float zt[TM];
-#pragma unroll
-        for (int t = 0; t < TM; ++t) zt[t] = 0.f;
-        for (int m = l8; m < hid; m += 8) {
-            const float h = gelu_exact(pre[uq * 68 + m]);
-#pragma unroll
-            for (int t = 0; t < TM; ++t)
-                if (t < T) zt[t] = fmaf(p.W2[(size_t)t * hid + m], h, zt[t]);
-            if (uq < cnt) b.hbuf[((size_t)sl * p.n + j0 + uq) * hid + m] = h;
-        }
-        float zmax = -INFINITY, zs = 0.f;
-#pragma unroll
-        for (int t = 0; t < TM; ++t)
-            if (t < T) {
-                zt[t] = group8_sum(zt[t]) + p.b2[t];
-                zmax = fmaxf(zmax, zt[t]);
-            }
-#pragma unroll
-        for (int t = 0; t < TM; ++t)
-            if (t < T) {
-                zt[t] = expf(zt[t] - zmax);
-                zs += zt[t];
-            }
-#pragma unroll
-        for (int t = 0; t < TM; ++t)
-            if (t < T && t == l8) wts[uq][t] = zt[t] / zs;
-    }
-    __syncthreads();
-
-    // ---- walk terms Y_k = Q U_k on the tensor cores; g = sum_k w_k Y_k rq, and
-    // dw_k partials alpha dO . Y_k rq per row and 16-column group
-    {
-        const int mt = warp & 1, sb = warp >> 1;
-        const uint32_t qa = smem_u32(Qk) + (uint32_t)((16 * mt + (lane & 15)) * kMA + (lane >> 4) * 8) * 2u;
-        const int mi = lane >> 3, brow = (mi & 1) * 8 + (lane & 7), bcol = 16 * sb + (mi >> 1) * 8;
-        const int r0 = 16 * mt + (lane >> 2);
-        float gacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        for (int kk = 1; kk < T; ++kk) {
-            {   // U_k's bf16 hi and lo rows from the precomputed image
-                const uint4 *img =
-                    reinterpret_cast<const uint4 *>(b.ukimg + ((size_t)sl * b.nh + (kk - 1)) * 2 * 64 * kQS);
-                for (int x = tid; x < 2 * 64 * kQS / 8; x += kThreads) reinterpret_cast<uint4 *>(Ui)[x] = img[x];
-            }
-            __syncthreads();
-            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4(qa + (uint32_t)(16 * ks) * 2u, a0, a1, a2, a3);
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(smem_u32(Ui) + (uint32_t)((h * 64 + 16 * ks + brow) * kQS + bcol) * 2u, b0, b1, b2, b3);
-                    mma_bf16_16816(acc[0], a0, a1, a2, a3, b0, b1);
-                    mma_bf16_16816(acc[1], a0, a1, a2, a3, b2, b3);
-                }
-            }
-            float dwr[2] = {0.f, 0.f};   // rows r0, r0 + 8
-#pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const int row = r0 + 8 * h;
-                const float rq = rqs[row], wk = wts[row][kk];
+                const int u = row + 8 * h;
+                if (u >= cnt) continue;
+                float *xm = b.dxm + ((size_t)sl * p.n + j0 + u) * 2 * D;
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const int col = 16 * sb + 8 * nt + 2 * (lane & 3);
-                    const float y0 = acc[nt][2 * h] * rq, y1 = acc[nt][2 * h + 1] * rq;
-                    gacc[nt][2 * h] = fmaf(wk, y0, gacc[nt][2 * h]);
-                    gacc[nt][2 * h + 1] = fmaf(wk, y1, gacc[nt][2 * h + 1]);
-                    dwr[h] = fmaf(Gs[row * 68 + col], y0, fmaf(Gs[row * 68 + col + 1], y1, dwr[h]));
-                }
-                dwr[h] += __shfl_xor_sync(0xffffffffu, dwr[h], 1);
-                dwr[h] += __shfl_xor_sync(0xffffffffu, dwr[h], 2);
-            }
-            if ((lane & 3) == 0) {
-                dwp[kk][r0][sb] = al * dwr[0];
-                dwp[kk][r0 + 8][sb] = al * dwr[1];
-            }
-            __syncthreads();   // every read of this U_k image is done
-        }
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int col = 16 * sb + 8 * nt + 2 * (lane & 3);
-                G[(r0 + 8 * h) * 68 + col] = gacc[nt][2 * h];
-                G[(r0 + 8 * h) * 68 + col + 1] = gacc[nt][2 * h + 1];
-            }
-    }
-    __syncthreads();
-
-    // ---- per token (a quarter-warp): the window (as bwd_token_a), dalpha terms,
-    // the softmax's and the MLP's elementwise backward; da as bf16 hi + lo
-    {
-        const int c8 = 8 * l8;
-        const bool live = uq < cnt;
-        const int i = j0 + (live ? uq : 0);
-        const int r = i / p.W, c = i % p.W;
-        float q[8], v[8], go[8], g[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            q[e] = __bfloat162float(Qk[uq * kMA + c8 + e]);
-            v[e] = Vs[uq * 68 + c8 + e];
-            go[e] = Gs[uq * 68 + c8 + e];
-            g[e] = fmaf(wts[uq][0], v[e], G[uq * 68 + c8 + e]);
-        }
-        float ev[9];
-#pragma unroll
-        for (int t9 = 0; t9 < 9; ++t9) {
-            const int rr = r + t9 / 3 - 1, cc = c + t9 % 3 - 1;
-            const bool in = rr >= 0 && rr < p.H && cc >= 0 && cc < p.W;
-            float kr[8];
-            load8_bf16(K + (size_t)(in ? rr * p.W + cc : i) * D + c8, kr, p.relu);
-            ev[t9] = dot8(q, kr);
-        }
-        // the group sums run on every lane (each shuffle needs all 32); the mask after
-#pragma unroll
-        for (int t9 = 0; t9 < 9; ++t9) ev[t9] = group8_sum(ev[t9]);
-        float emax = -INFINITY;
-#pragma unroll
-        for (int t9 = 0; t9 < 9; ++t9) {
-            const int rr = r + t9 / 3 - 1, cc = c + t9 % 3 - 1;
-            const bool in = rr >= 0 && rr < p.H && cc >= 0 && cc < p.W;
-            ev[t9] = in ? ev[t9] * 0.125f : -INFINITY;
-            emax = fmaxf(emax, ev[t9]);
-        }
-        float l[8], esum = 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) l[e] = 0.f;
-#pragma unroll
-        for (int t9 = 0; t9 < 9; ++t9) {
-            const int rr = r + t9 / 3 - 1, cc = c + t9 % 3 - 1;
-            const bool in = rr >= 0 && rr < p.H && cc >= 0 && cc < p.W;
-            const float a = in ? expf(ev[t9] - emax) : 0.f;
-            esum += a;
-            float vr[8];
-            load8_bf16(V + (size_t)(in ? rr * p.W + cc : i) * D + c8, vr, false);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) l[e] = fmaf(a, vr[e], l[e]);
-        }
-        const float inv = 1.f / esum;
-        float dgl = 0.f, dll = 0.f, dgv = 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            l[e] *= inv;
-            dgl = fmaf(go[e], g[e] - l[e], dgl);
-            dll = fmaf(go[e], l[e], dll);
-            dgv = fmaf(go[e], v[e], dgv);   // dw_0 / alpha
-        }
-        dgl = group8_sum(dgl);
-        dll = group8_sum(dll);
-        dgv = group8_sum(dgv);
-        const size_t ti = (size_t)sl * p.n + i;
-        if (l8 == 0 && live) reinterpret_cast<float4 *>(b.lstat)[ti] = make_float4(emax, esum, dll * (1.f - al), 0.f);
-        // dz = w (dw - w . dw), dw_0 = alpha dO . V, dw_k from the partials
-        float w[TM], dw[TM], wdw = 0.f;
-#pragma unroll
-        for (int t = 0; t < TM; ++t) {
-            w[t] = t < T ? wts[uq][t] : 0.f;
-            dw[t] = t == 0 ? al * dgv
-                           : (t < T ? ((dwp[t][uq][0] + dwp[t][uq][1]) + (dwp[t][uq][2] + dwp[t][uq][3])) : 0.f);
-            wdw = fmaf(w[t], dw[t], wdw);
-        }
-        float dz[TM];
-#pragma unroll
-        for (int t = 0; t < TM; ++t) dz[t] = w[t] * (dw[t] - wdw);
-        if (live) {
-#pragma unroll
-            for (int t = 0; t < TM; ++t)
-                if (t < T && t == l8) {
-                    b.wtok[ti * T + t] = w[t];
-                    b.dzbuf[ti * T + t] = dz[t];
-                }
-        }
-        for (int m = l8; m < nmh; m += 8) {
-            float da = 0.f;
-            if (m < hid && live) {
-                float dh = 0.f;
-#pragma unroll
-                for (int t = 0; t < TM; ++t)
-                    if (t < T) dh = fmaf(p.W2[(size_t)t * hid + m], dz[t], dh);
-                da = dh * gelu_exact_grad(pre[uq * 68 + m]);
-                b.dabuf[ti * hid + m] = da;
-            }
-            const __nv_bfloat16 hi = __float2bfloat16_rn(da);
-            Di[uq * kQS + m] = hi;
-            Di[kTpb * kQS + uq * kQS + m] = __float2bfloat16_rn(da - __bfloat162float(hi));
-        }
-        // dalpha terms of the warp's live tokens, in token order
-        float dal = (l8 == 0 && live) ? dgl : 0.f;
-        dal = warp_sum(dal);
-        if (lane == 0) part[warp] = dal;
-    }
-    __syncthreads();
-    if (tid == 0) {
-        float acc = 0.f;
-        for (int w2 = 0; w2 < kWarps; ++w2) acc += part[w2];
-        b.dal_part[(size_t)sl * b.nblk + blk] = acc;
-    }
-
-    // ---- the MLP's share of [dq | dk] = da W1: warp = 16 tokens x 32 channels
-    {
-        const int mt = warp & 1, cg = warp >> 1;   // channels 32 cg .. 32 cg + 31
-        const uint32_t da0 = smem_u32(Di) + (uint32_t)((16 * mt + (lane & 15)) * kQS + (lane >> 4) * 8) * 2u;
-        const int mi = lane >> 3, brow = (mi & 1) * 8 + (lane & 7);
-        float acc[4][4];
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-        for (int ks = 0; 16 * ks < nmh; ++ks) {
-#pragma unroll
-            for (int ah = 0; ah < 2; ++ah) {   // da hi, lo
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4(da0 + (uint32_t)(ah * kTpb * kQS + 16 * ks) * 2u, a0, a1, a2, a3);
-#pragma unroll
-                for (int wh = 0; wh < 2; ++wh) {   // W1 hi, lo (lo x lo left out)
-                    if (ah == 1 && wh == 1) continue;
-#pragma unroll
-                    for (int np = 0; np < 2; ++np) {
-                        const int bcol = 32 * cg + 16 * np + (mi >> 1) * 8;
-                        uint32_t b0, b1, b2, b3;
-                        ldsm_x4_t(smem_u32(W1i) + (uint32_t)(wh * kMH * kMA + (16 * ks + brow) * kMA + bcol) * 2u,
-                                  b0, b1, b2, b3);
-                        mma_bf16_16816(acc[2 * np], a0, a1, a2, a3, b0, b1);
-                        mma_bf16_16816(acc[2 * np + 1], a0, a1, a2, a3, b2, b3);
-                    }
+                for (int nt = 0; nt < 4; ++nt) {
+                    const int c = 32 * cg + 8 * nt + 2 * (lane & 3);
+                    *reinterpret_cast<float2 *>(xm + c) = make_float2(acc[nt][2 * h], acc[nt][2 * h + 1]);
                 }
             }
         }
-        const int row = 16 * mt + (lane >> 2);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int u = row + 8 * h;
-            if (u >= cnt) continue;
-            float *xm = b.dxm + ((size_t)sl * p.n + j0 + u) * 2 * D;
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt) {
-                const int c = 32 * cg + 8 * nt + 2 * (lane & 3);
-                *reinterpret_cast<float2 *>(xm + c) = make_float2(acc[nt][2 * h], acc[nt][2 * h + 1]);
-            }
-        }
+        __syncthreads();   // the next block restages the shared rows
     }
 }
 
@@ -3052,7 +3059,9 @@ cudaError_t launch_bwd_all(const BwdProblem &b, cudaStream_t st) {
                                             kMlpTcSmemBytes)) != cudaSuccess)
                 return err;
             bwd_mlp_images<<<(unsigned)(p.slices * b.nh + 1), kThreads, 0, st>>>(b);
-            bwd_token_mlp_tc<<<grid_tok, kThreads, kMlpTcSmemBytes, st>>>(b);
+            // persistent: two CTAs per SM (its shared memory allows two)
+            const unsigned grid_mlp = std::min(grid_tok, 2u * (unsigned)sm_count());
+            bwd_token_mlp_tc<<<grid_mlp, kThreads, kMlpTcSmemBytes, st>>>(b);
         } else {
             bwd_token_mlp<TIn, D><<<grid_tok, kThreads, 0, st>>>(b);
         }
