@@ -31,17 +31,20 @@
 //                     dalpha terms (per-block partial sums)
 //   4. bwd_recur_back per slice: reduce dUbar; G_k; dM, dU_1 (or the solve)
 //   5. bwd_token_b    per block of 32 tokens: the d x d products from shared
-//                     memory (bf16, d = 64: on the tensor cores, from a bf16
-//                     operand image built by bwd_bimg), then a warp per token:
-//                     dXq, dV, the ds terms (per-block sums), dK without ds
+//                     memory, then a warp per token: dXq, dV, the ds terms
+//                     (per-block sums), dK without ds.  bf16, d = 64:
+//                     bwd_token_b_tile on 8 x 8 token tiles with their halo in
+//                     shared memory, the products and the window on the tensor
+//                     cores (B operands from a bf16 image built by bwd_bimg)
 //   6. bwd_reduce     per slice: ds and the slice's dalpha
 //   7. bwd_finish_k   one thread per element: dXk = (dK + ds) [Xk > 0]
 //   8. bwd_dalpha     dalpha per head = sum over the batch
 // With the adaptive (MLP) weights, steps 2-3 become bwd_token_mlp (the
-// window statistics, the MLP's forward and backward per token) and
-// bwd_stats_duk (one split-K dU_k = sum_i w_ik Q~_i^T dg_i per walk length);
-// step 5 adds each token's own walk terms; bwd_mlp_params and
-// bwd_mlp_reduce produce dW1, db1, dW2, db2.
+// window statistics, the MLP's forward and backward per token; bf16, d = 64:
+// bwd_token_mlp_tc after bwd_mlp_images has built the bf16 U_k and W1 operand
+// images) and bwd_stats_duk (one split-K dU_k = sum_i w_ik Q~_i^T dg_i per walk
+// length); step 5 adds each token's own walk terms and the MLP's share of
+// dq, dk; bwd_mlp_params and bwd_mlp_reduce produce dW1, db1, dW2, db2.
 // Every reduction runs in a fixed order: the result does not depend on
 // scheduling.
 #include <cuda_bf16.h>
@@ -284,11 +287,6 @@ __global__ void __launch_bounds__(kThreads) bwd_recur_rows(BwdProblem b) {
     auto emit = [&](int k) {   // U_k's rows of this thread into the stored copies
         const float4 u = *reinterpret_cast<const float4 *>(&Ut[i][a0]);
         *reinterpret_cast<float4 *>(Uk + (size_t)(k - 1) * D * D + e * D + a0) = u;
-        if (b.mlp) {
-            float *Ukn = b.Ukn + ((size_t)sl * b.nh + (k - 1)) * D * D;
-            Ukn[(a0 + 0) * D + e] = u.x; Ukn[(a0 + 1) * D + e] = u.y;
-            Ukn[(a0 + 2) * D + e] = u.z; Ukn[(a0 + 3) * D + e] = u.w;
-        }
         return u;
     };
     {
@@ -1258,17 +1256,14 @@ __global__ void __launch_bounds__(kThreads) bwd_token_b(BwdProblem b) {
 }
 
 // ---------------------------------------------------------------------------
-// 5'. bf16, d = 64: the same per-token gradients with the three d x d
-// products on the tensor cores (mma.sync m16n8k16, bf16 operands, fp32
-// accumulation):
+// 5'. bf16, d = 64: the B operands of the tiled token pass's three d x d
+// products (mma.sync m16n8k16, bf16 operands, fp32 accumulation)
 //   dQ~ = [dO | K] [alpha Ubar^T ; dM],  dK = [V | Q~] [dU_1^T ; dM^T],  dV = K dU_1
-// The B operands come from a bf16 image built once per slice (bwd_bimg); Q~
-// is rounded to bf16 as an operand, the inputs are bf16 already.
+// as one bf16 image per slice, built once per backward (bwd_bimg); Q~ is
+// rounded to bf16 as an operand, the inputs are bf16 already.
 // ---------------------------------------------------------------------------
 constexpr int kImgRows = 5 * 64;   // [alpha Ubar^T; dM; dU_1^T; dM^T; dU_1], 64 columns each
 constexpr int kBS = 72;            // B-image row stride in shared memory, bf16 (144 B: ldmatrix conflict-free)
-constexpr int kAS = 136;           // A row stride, bf16 (272 B)
-constexpr int kTcSmemBytes = kImgRows * kBS * 2 + 2 * kTpb * kAS * 2 + kTpb * 64 * 2 + 3 * kTpb * 64 * 4;
 
 // grid (slices, 5): block (sl, m) converts matrix m of slice sl, four floats per thread and step
 __global__ void __launch_bounds__(kThreads) bwd_bimg(BwdProblem b) {
@@ -1954,17 +1949,18 @@ __global__ void __launch_bounds__(kThreads) bwd_mlp_images(BwdProblem b) {
     const Problem &p = b.fwd;
     const int tid = threadIdx.x;
     if (blockIdx.x < (unsigned)(p.slices * b.nh)) {
-        const float *Un = b.Ukn + (size_t)blockIdx.x * D * D;
+        const float *Ut = b.Uk + (size_t)blockIdx.x * D * D;   // transposed: Ut[e * D + a] = U_k[a][e]
         uint16_t *img = b.ukimg + (size_t)blockIdx.x * 2 * 64 * kQS;
         uint16_t *imgT = b.ukimgT + (size_t)blockIdx.x * 64 * kQS;
         const float al = p.alpha[(blockIdx.x / b.nh) % p.heads];
         for (int x = tid; x < D * D; x += kThreads) {
-            const float uv = Un[x];
+            const int e = x >> 6, a = x & 63;
+            const float uv = Ut[x];
             const __nv_bfloat16 hi = __float2bfloat16_rn(uv);
-            imgT[(x & 63) * kQS + (x >> 6)] = __bfloat16_as_ushort(__float2bfloat16_rn(al * uv));
-            img[(x >> 6) * kQS + (x & 63)] = __bfloat16_as_ushort(hi);
+            imgT[e * kQS + a] = __bfloat16_as_ushort(__float2bfloat16_rn(al * uv));
+            img[a * kQS + e] = __bfloat16_as_ushort(hi);
             const float lo = uv - __bfloat162float(hi);
-            img[64 * kQS + (x >> 6) * kQS + (x & 63)] = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+            img[64 * kQS + a * kQS + e] = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
         }
     } else {
         for (int x = tid; x < kMH * 2 * D; x += kThreads) {
@@ -2536,304 +2532,6 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_mlp_params_tc(BwdProblem b) {
     else if (tid >= LISA_MAX_HIDDEN && tid - LISA_MAX_HIDDEN < T) b.pb2[pc * T + tid - LISA_MAX_HIDDEN] = bb;
 }
 
-__global__ void __launch_bounds__(kThreads) bwd_token_b_tc(BwdProblem b) {
-    constexpr int D = 64;
-    using namespace sm100;
-    extern __shared__ float4 smem_tc[];
-    __nv_bfloat16 *Bs = reinterpret_cast<__nv_bfloat16 *>(smem_tc);
-    __nv_bfloat16 *A1 = Bs + kImgRows * kBS;   // [dO | K] rows
-    __nv_bfloat16 *A3 = A1 + kTpb * kAS;       // [V | Q~] rows
-    __nv_bfloat16 *Qb = A3 + kTpb * kAS;       // Q rows (feature-mapped)
-    float *oQ = reinterpret_cast<float *>(Qb + kTpb * D), *oV = oQ + kTpb * D, *oK = oV + kTpb * D;
-    __shared__ float rqs[kTpb];
-    __shared__ float dsw[kWarps][D];
-    const Problem &p = b.fwd;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int sl = blockIdx.x / b.nblk, blk = blockIdx.x % b.nblk;
-    const int j0 = blk * kTpb, cnt = min(kTpb, p.n - j0);
-    const size_t sbase = (size_t)sl * p.n * D;
-    const __nv_bfloat16 *Q = static_cast<const __nv_bfloat16 *>(p.Q) + sbase;
-    const __nv_bfloat16 *K = static_cast<const __nv_bfloat16 *>(p.K) + sbase;
-    const __nv_bfloat16 *V = static_cast<const __nv_bfloat16 *>(p.V) + sbase;
-    const __nv_bfloat16 *dO = static_cast<const __nv_bfloat16 *>(b.dO) + sbase;
-    __nv_bfloat16 *dQo = static_cast<__nv_bfloat16 *>(b.dQ) + sbase;
-    __nv_bfloat16 *dVo = static_cast<__nv_bfloat16 *>(b.dV) + sbase;
-    float *dKp = b.dk_part + sbase;
-    const float4 *lst = reinterpret_cast<const float4 *>(b.lstat) + (size_t)sl * p.n;
-    const float *s = p.s_red + (size_t)sl * D;
-    const float al = p.alpha[sl % p.heads], w0 = p.w[0];
-    const float scale = rsqrtf((float)D);
-
-    // ---- stage the B image and the block's rows (16-byte pieces)
-    {
-        const uint4 *img = reinterpret_cast<const uint4 *>(b.bimg + (size_t)sl * kImgRows * D);
-        for (int x = tid; x < kImgRows * 8; x += kThreads)
-            *reinterpret_cast<uint4 *>(Bs + (x >> 3) * kBS + (x & 7) * 8) = img[x];
-    }
-    for (int x = tid; x < kTpb * 8; x += kThreads) {
-        const int j = x >> 3, c = x & 7;
-        uint4 g = make_uint4(0, 0, 0, 0), k = g, v = g, q = g;
-        if (j < cnt) {
-            const size_t o = ((size_t)(j0 + j) * D) / 8 + c;
-            g = reinterpret_cast<const uint4 *>(dO)[o];
-            k = reinterpret_cast<const uint4 *>(K)[o];
-            v = reinterpret_cast<const uint4 *>(V)[o];
-            q = reinterpret_cast<const uint4 *>(Q)[o];
-            if (p.relu) {
-                k = make_uint4(relu_bf16x2(k.x), relu_bf16x2(k.y), relu_bf16x2(k.z), relu_bf16x2(k.w));
-                q = make_uint4(relu_bf16x2(q.x), relu_bf16x2(q.y), relu_bf16x2(q.z), relu_bf16x2(q.w));
-            }
-        }
-        *reinterpret_cast<uint4 *>(A1 + j * kAS + c * 8) = g;
-        *reinterpret_cast<uint4 *>(A1 + j * kAS + 64 + c * 8) = k;
-        *reinterpret_cast<uint4 *>(A3 + j * kAS + c * 8) = v;
-        *reinterpret_cast<uint4 *>(Qb + j * D + c * 8) = q;
-    }
-    __syncthreads();
-    for (int j = warp; j < kTpb; j += kWarps) {   // 1 / (Q_j . s + eps)
-        float d = 0.f;
-        for (int ch = lane; ch < D; ch += 32) d += __bfloat162float(Qb[j * D + ch]) * s[ch];
-        d = warp_sum(d);
-        if (lane == 0) rqs[j] = 1.f / (d + p.eps);
-    }
-    __syncthreads();
-    for (int x = tid; x < kTpb * D; x += kThreads) {   // Q~ half of A3, rounded to bf16
-        const int j = x / D, ch = x % D;
-        A3[j * kAS + 64 + ch] = __float2bfloat16_rn(__bfloat162float(Qb[j * D + ch]) * rqs[j]);
-    }
-    __syncthreads();
-
-    // ---- the three products: warp = 16 tokens (mt) x 16 columns (sb) of each
-    {
-        const int mt = warp & 1, sb = warp >> 1;
-        const uint32_t bs = smem_u32(Bs), a1 = smem_u32(A1), a3 = smem_u32(A3);
-        const int arow = 16 * mt + (lane & 15), acol = (lane >> 4) * 8;
-        const int mi = lane >> 3, brow = (mi & 1) * 8 + (lane & 7), bcol = 16 * sb + (mi >> 1) * 8;
-#pragma unroll
-        for (int pr = 0; pr < 3; ++pr) {
-            const uint32_t abase = (pr == 1 ? a3 : a1) + (uint32_t)(arow * kAS + (pr == 2 ? 64 : 0) + acol) * 2u;
-            const int brow0 = pr == 0 ? 0 : (pr == 1 ? 128 : 256);
-            const int ksteps = pr == 2 ? 4 : 8;
-            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            for (int ks = 0; ks < ksteps; ++ks) {
-                uint32_t a0, a1r, a2, a3r, b0, b1, b2, b3;
-                ldsm_x4(abase + (uint32_t)(16 * ks) * 2u, a0, a1r, a2, a3r);
-                ldsm_x4_t(bs + (uint32_t)((brow0 + 16 * ks + brow) * kBS + bcol) * 2u, b0, b1, b2, b3);
-                mma_bf16_16816(acc[0], a0, a1r, a2, a3r, b0, b1);
-                mma_bf16_16816(acc[1], a0, a1r, a2, a3r, b2, b3);
-            }
-            float *out = pr == 0 ? oQ : (pr == 1 ? oK : oV);
-            const int row = 16 * mt + (lane >> 2);
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int col = 16 * sb + 8 * nt + 2 * (lane & 3);
-                out[row * D + col] = acc[nt][0];
-                out[row * D + col + 1] = acc[nt][1];
-                out[(row + 8) * D + col] = acc[nt][2];
-                out[(row + 8) * D + col + 1] = acc[nt][3];
-            }
-        }
-    }
-    __syncthreads();
-
-    // ---- adaptive weights: the token's own walk terms, which the block's shared
-    // products leave out: dV_j += w_j0 alpha dO_j and dQ~_j += alpha sum_{k>=1}
-    // w_jk dO_j U_k^T, the latter as (alpha dO) U_k^T on mma.sync per k (U_k^T
-    // as bf16 hi + lo, staged where the B image was), each token's row scaled
-    // by its own w_jk
-    if (b.mlp) {
-        __shared__ float wts_s[kTpb][LISA_MAX_T_MLP];
-        const int T = p.T;
-        for (int x = tid; x < kTpb * T; x += kThreads) {
-            const int j = x / T, t = x % T;
-            wts_s[j][t] = j < cnt ? b.wtok[((size_t)sl * p.n + j0 + j) * T + t] : 0.f;
-        }
-        __syncthreads();
-        for (int x = tid; x < kTpb * D; x += kThreads) {
-            const int j = x / D, ch = x % D;
-            oV[j * D + ch] = fmaf(wts_s[j][0] * al, __bfloat162float(A1[j * kAS + ch]), oV[j * D + ch]);
-        }
-        __nv_bfloat16 *Ui = Bs;   // the B image is no longer read
-        const int mt = warp & 1, sb = warp >> 1;
-        const uint32_t ga = smem_u32(A1) + (uint32_t)((16 * mt + (lane & 15)) * kAS + (lane >> 4) * 8) * 2u;
-        const int mi = lane >> 3, brow = (mi & 1) * 8 + (lane & 7), bcol = 16 * sb + (mi >> 1) * 8;
-        const int r0 = 16 * mt + (lane >> 2);
-        for (int kk = 1; kk < T; ++kk) {
-            const float *UT = b.Uk + ((size_t)sl * b.nh + (kk - 1)) * D * D;   // UT[c][a] = U_k[a][c]
-            __syncthreads();   // the products (or the previous k) no longer read this region
-            for (int x = tid; x < D * D; x += kThreads) {
-                const float uv = UT[x];
-                const __nv_bfloat16 hi = __float2bfloat16_rn(uv);
-                Ui[(x >> 6) * kQS + (x & 63)] = hi;
-                Ui[64 * kQS + (x >> 6) * kQS + (x & 63)] = __float2bfloat16_rn(uv - __bfloat162float(hi));
-            }
-            __syncthreads();
-            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4(ga + (uint32_t)(16 * ks) * 2u, a0, a1, a2, a3);
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(smem_u32(Ui) + (uint32_t)((h * 64 + 16 * ks + brow) * kQS + bcol) * 2u, b0, b1, b2, b3);
-                    mma_bf16_16816(acc[0], a0, a1, a2, a3, b0, b1);
-                    mma_bf16_16816(acc[1], a0, a1, a2, a3, b2, b3);
-                }
-            }
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int row = r0 + 8 * h;
-                const float wk = al * wts_s[row][kk];
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const int col = 16 * sb + 8 * nt + 2 * (lane & 3);
-                    oQ[row * D + col] = fmaf(wk, acc[nt][2 * h], oQ[row * D + col]);
-                    oQ[row * D + col + 1] = fmaf(wk, acc[nt][2 * h + 1], oQ[row * D + col + 1]);
-                }
-            }
-        }
-        __syncthreads();
-    }
-
-    // ---- a quarter-warp per token (eight lanes, eight channels each):
-    // normaliser, the MLP's share, window, stores
-    const int qg = lane >> 3, c8 = 8 * (lane & 7);
-    const int u = 4 * warp + qg;
-    const bool live = u < cnt;
-    const int j = j0 + (live ? u : 0);
-    float q[8], go[8], k[8], v[8], dqt[8], dv[8], dk[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        q[e] = __bfloat162float(Qb[u * D + c8 + e]);
-        go[e] = __bfloat162float(A1[u * kAS + c8 + e]);
-        k[e] = __bfloat162float(A1[u * kAS + 64 + c8 + e]);
-        v[e] = __bfloat162float(A3[u * kAS + c8 + e]);
-        dqt[e] = oQ[u * D + c8 + e];
-        dv[e] = fmaf(w0 * al, go[e], oV[u * D + c8 + e]);
-        dk[e] = oK[u * D + c8 + e];
-    }
-    const float rq = rqs[u];
-    const float cj = group8_sum(dot8(dqt, q)) * rq * rq;
-    float dq[8], dsl[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        dq[e] = dqt[e] * rq - cj * s[c8 + e];
-        dsl[e] = live ? -cj * q[e] : 0.f;
-    }
-    {   // the MLP's share of dq_j, dk_j
-        const float4 *xm = reinterpret_cast<const float4 *>(b.dxm + ((size_t)sl * p.n + j) * 2 * D + c8);
-        const float4 x0 = xm[0], x1 = xm[1], x2 = xm[16], x3 = xm[17];
-        const float xq[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-        const float xk[8] = {x2.x, x2.y, x2.z, x2.w, x3.x, x3.y, x3.z, x3.w};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            dq[e] += xq[e];
-            dk[e] += xk[e];
-        }
-    }
-    const int r = j / p.W, c = j % p.W;
-    const float4 sj = lst[j];
-    const float izj = 1.f / sj.y;
-    // j as the query: scores against its window, dl_j . V_i
-    {
-        float d1[18];
-#pragma unroll
-        for (int t9 = 0; t9 < 9; ++t9) {
-            const int rr = r + t9 / 3 - 1, cc = c + t9 % 3 - 1;
-            const bool in = rr >= 0 && rr < p.H && cc >= 0 && cc < p.W;
-            const size_t row = (size_t)(in ? rr * p.W + cc : j) * D + c8;
-            float kr[8], vr[8];
-            load8_bf16(K + row, kr, p.relu);
-            load8_bf16(V + row, vr, false);
-            d1[t9] = dot8(q, kr);
-            d1[9 + t9] = dot8(go, vr);
-        }
-#pragma unroll
-        for (int t = 0; t < 18; ++t) d1[t] = group8_sum(d1[t]);
-#pragma unroll
-        for (int t9 = 0; t9 < 9; ++t9) {
-            const int rr = r + t9 / 3 - 1, cc = c + t9 % 3 - 1;
-            const bool in = rr >= 0 && rr < p.H && cc >= 0 && cc < p.W;
-            if (!in) continue;
-            const float a = expf(d1[t9] * scale - sj.x) * izj;
-            const float de = a * (d1[9 + t9] * (1.f - al) - sj.z) * scale;
-            float kr[8];
-            load8_bf16(K + (size_t)(rr * p.W + cc) * D + c8, kr, p.relu);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) dq[e] = fmaf(de, kr[e], dq[e]);
-        }
-    }
-    // j as a key of each neighbour i's window (the window is symmetric)
-    {
-        float d2[18];
-#pragma unroll
-        for (int t9 = 0; t9 < 9; ++t9) {
-            const int rr = r + t9 / 3 - 1, cc = c + t9 % 3 - 1;
-            const bool in = rr >= 0 && rr < p.H && cc >= 0 && cc < p.W;
-            const size_t row = (size_t)(in ? rr * p.W + cc : j) * D + c8;
-            float qi[8], gi[8];
-            load8_bf16(Q + row, qi, p.relu);
-            load8_bf16(dO + row, gi, false);
-            d2[t9] = dot8(qi, k);
-            d2[9 + t9] = dot8(gi, v);
-        }
-#pragma unroll
-        for (int t = 0; t < 18; ++t) d2[t] = group8_sum(d2[t]);
-#pragma unroll
-        for (int t9 = 0; t9 < 9; ++t9) {
-            const int rr = r + t9 / 3 - 1, cc = c + t9 % 3 - 1;
-            const bool in = rr >= 0 && rr < p.H && cc >= 0 && cc < p.W;
-            if (!in) continue;
-            const int ni = rr * p.W + cc;
-            const float4 si = lst[ni];
-            const float a = expf(d2[t9] * scale - si.x) / si.y;
-            const float de = a * (d2[9 + t9] * (1.f - al) - si.z) * scale;
-            float qi[8], gi[8];
-            load8_bf16(Q + (size_t)ni * D + c8, qi, p.relu);
-            load8_bf16(dO + (size_t)ni * D + c8, gi, false);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                dv[e] = fmaf(a * (1.f - al), gi[e], dv[e]);
-                dk[e] = fmaf(de, qi[e], dk[e]);
-            }
-        }
-    }
-    if (live) {
-        float xq[8];
-        load8_bf16(Q + (size_t)j * D + c8, xq, false);
-        uint4 oq, ov;
-        uint32_t *pq = &oq.x, *pv = &ov.x;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float q0 = (p.relu && !(xq[2 * e] > 0.f)) ? 0.f : dq[2 * e];
-            const float q1 = (p.relu && !(xq[2 * e + 1] > 0.f)) ? 0.f : dq[2 * e + 1];
-            pq[e] = pack_bf16(q0, q1);
-            pv[e] = pack_bf16(dv[2 * e], dv[2 * e + 1]);
-        }
-        *reinterpret_cast<uint4 *>(dQo + (size_t)j * D + c8) = oq;
-        *reinterpret_cast<uint4 *>(dVo + (size_t)j * D + c8) = ov;
-        float4 *kp = reinterpret_cast<float4 *>(dKp + (size_t)j * D + c8);
-        kp[0] = make_float4(dk[0], dk[1], dk[2], dk[3]);
-        kp[1] = make_float4(dk[4], dk[5], dk[6], dk[7]);
-    }
-    // the warp's four tokens' ds terms, summed over the quarters in a fixed order
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        dsl[e] += __shfl_xor_sync(0xffffffffu, dsl[e], 8);
-        dsl[e] += __shfl_xor_sync(0xffffffffu, dsl[e], 16);
-    }
-    if (qg == 0)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) dsw[warp][c8 + e] = dsl[e];
-    __syncthreads();
-    for (int ch = tid; ch < D; ch += kThreads) {
-        float acc = 0.f;
-        for (int w = 0; w < kWarps; ++w) acc += dsw[w][ch];
-        b.ds_part[((size_t)sl * b.nblk + blk) * D + ch] = acc;
-    }
-}
-
 // ---------------------------------------------------------------------------
 // adaptive weights: the MLP parameters' gradients.  Per (slice, chunk):
 //   dW1 += sum_i da_i x_i^T (x_i = [q_i; k_i]), db1 += sum_i da_i,
@@ -3111,12 +2809,6 @@ cudaError_t launch_bwd_all(const BwdProblem &b, cudaStream_t st) {
         const int nsm = sm_count();
         const unsigned grid = (unsigned)(ntiles < nsm ? ntiles : nsm);   // persistent: one CTA per SM
         tile_kern<<<grid, kTileThreads, kTileSmemBytes, st>>>(mK, mV, mQ, mG, mL, b);
-    } else if (std::is_same<TIn, __nv_bfloat16>::value && D == 64 && p.relu != 2) {
-        bwd_bimg<<<dim3((unsigned)p.slices, 5), kThreads, 0, st>>>(b);
-        if ((err = cudaFuncSetAttribute(bwd_token_b_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        kTcSmemBytes)) != cudaSuccess)
-            return err;
-        bwd_token_b_tc<<<grid_tok, kThreads, kTcSmemBytes, st>>>(b);
     } else {
         constexpr int smem_b = token_b_smem_floats<D>() * (int)sizeof(float);
         if ((err = cudaFuncSetAttribute(bwd_token_b<TIn, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -44,7 +44,7 @@ struct BwdProblem {
     float *dal_slice;    // [S]
     float *dk_part;      // [S][n][D]      dK without ds, fp32
     // adaptive (MLP) walk weights only (null otherwise)
-    float *Ukn;          // [S][nh][D][D]  U_1 .. U_(T-1), row-major
+    float *Ukn;          // [S][nh][D][D]  U_1 .. U_(T-1), row-major (the SIMT adaptive-weight pass)
     uint16_t *ukimg;     // [S][nh][2][64][72] bf16: U_k rows as hi, lo terms (72-wide rows; bf16, d = 64)
     uint16_t *w1img;     // [2][64][136] bf16: W1 rows as hi, lo terms (136-wide rows; bf16, d = 64)
     uint16_t *ukimgT;    // [S][nh][64][72] bf16: alpha U_k^T, row c, column a (72-wide rows; bf16, d = 64)
