@@ -1989,6 +1989,7 @@ __global__ void __launch_bounds__(kThreads) bwd_token_mlp_tc(BwdProblem b) {
     __shared__ float wts[kTpb][TM];
     __shared__ float dwp[TM][kTpb][4];    // dw_k partials per row and 16-column group
     __shared__ float part[kWarps];
+    __shared__ float W2s[TM * kMH], b2s[TM];   // the MLP's second layer, staged once per CTA
     const Problem &p = b.fwd;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int T = p.T, hid = p.hidden, nmh = (hid + 15) / 16 * 16;
@@ -2000,33 +2001,44 @@ __global__ void __launch_bounds__(kThreads) bwd_token_mlp_tc(BwdProblem b) {
             reinterpret_cast<uint4 *>(W1i + h * kMH * kMA)[y] = img[h * kMH * kRowV + y];
         }
     }
+    for (int x = tid; x < T * hid; x += kThreads) W2s[x] = p.W2[x];
+    if (tid < T) b2s[tid] = p.b2[tid];
+    // this thread's 16-byte piece of a block's Q, K, V and dO rows (token tid / 8,
+    // channels 8 (tid % 8) ..), loaded one block ahead so the loads overlap the
+    // previous block's work
+    static_assert(kTpb * 8 == kThreads, "one 16-byte piece of each row per thread");
+    uint4 rq_q, rq_k, rq_v, rq_g;
+    auto load_rows = [&](int bj) {
+        const int slj = bj / b.nblk, j0j = (bj % b.nblk) * kTpb, jj = tid >> 3;
+        rq_q = rq_k = rq_v = rq_g = make_uint4(0u, 0u, 0u, 0u);
+        if (j0j + jj < p.n) {
+            const size_t o = ((size_t)slj * p.n * D + (size_t)(j0j + jj) * D) / 8 + (tid & 7);
+            rq_q = reinterpret_cast<const uint4 *>(p.Q)[o];
+            rq_k = reinterpret_cast<const uint4 *>(p.K)[o];
+            rq_v = reinterpret_cast<const uint4 *>(p.V)[o];
+            rq_g = reinterpret_cast<const uint4 *>(b.dO)[o];
+        }
+    };
+    if (blockIdx.x < (unsigned)(p.slices * b.nblk)) load_rows(blockIdx.x);
     // persistent: the CTA walks blocks of kTpb tokens; W1 stays staged
     const int nbt = p.slices * b.nblk;
     for (int bi = blockIdx.x; bi < nbt; bi += gridDim.x) {
         const int sl = bi / b.nblk, blk = bi % b.nblk;
         const int j0 = blk * kTpb, cnt = min(kTpb, p.n - j0);
         const size_t sbase = (size_t)sl * p.n * D;
-        const __nv_bfloat16 *Q = static_cast<const __nv_bfloat16 *>(p.Q) + sbase;
-        const __nv_bfloat16 *K = static_cast<const __nv_bfloat16 *>(p.K) + sbase;
+        const __nv_bfloat16 *K = static_cast<const __nv_bfloat16 *>(p.K) + sbase;   // the window's rows
         const __nv_bfloat16 *V = static_cast<const __nv_bfloat16 *>(p.V) + sbase;
-        const __nv_bfloat16 *dO = static_cast<const __nv_bfloat16 *>(b.dO) + sbase;
         const float *s = p.s_red + (size_t)sl * D;
         const float al = p.alpha[sl % p.heads];
 
-        // ---- stage [Q | K] (feature-mapped), V and dO rows (fp32), W1 as bf16 hi + lo
-        for (int x = tid; x < kTpb * 8; x += kThreads) {
-            const int j = x >> 3, c = x & 7;
-            uint4 q = make_uint4(0u, 0u, 0u, 0u), k = q, v = q, g = q;
-            if (j < cnt) {
-                const size_t o = ((size_t)(j0 + j) * D) / 8 + c;
-                q = reinterpret_cast<const uint4 *>(Q)[o];
-                k = reinterpret_cast<const uint4 *>(K)[o];
-                v = reinterpret_cast<const uint4 *>(V)[o];
-                g = reinterpret_cast<const uint4 *>(dO)[o];
-                if (p.relu) {
-                    q = make_uint4(relu_bf16x2(q.x), relu_bf16x2(q.y), relu_bf16x2(q.z), relu_bf16x2(q.w));
-                    k = make_uint4(relu_bf16x2(k.x), relu_bf16x2(k.y), relu_bf16x2(k.z), relu_bf16x2(k.w));
-                }
+        // ---- stage [Q | K] (feature-mapped), V and dO rows (fp32) from the prefetched pieces
+        {
+            const int j = tid >> 3, c = tid & 7;
+            uint4 q = rq_q, k = rq_k;
+            const uint4 v = rq_v, g = rq_g;
+            if (p.relu) {
+                q = make_uint4(relu_bf16x2(q.x), relu_bf16x2(q.y), relu_bf16x2(q.z), relu_bf16x2(q.w));
+                k = make_uint4(relu_bf16x2(k.x), relu_bf16x2(k.y), relu_bf16x2(k.z), relu_bf16x2(k.w));
             }
             *reinterpret_cast<uint4 *>(Qk + j * kMA + c * 8) = q;
             *reinterpret_cast<uint4 *>(Qk + j * kMA + 64 + c * 8) = k;
@@ -2039,6 +2051,7 @@ __global__ void __launch_bounds__(kThreads) bwd_token_mlp_tc(BwdProblem b) {
                 Gs[j * 68 + c * 8 + 2 * e + 1] = bf16_hi(gg[e]);
             }
         }
+        if (bi + (int)gridDim.x < nbt) load_rows(bi + (int)gridDim.x);   // the next block's rows, in flight
         for (int x = tid; x < TM * kTpb * 4; x += kThreads) (&dwp[0][0][0])[x] = 0.f;
         __syncthreads();
         for (int j = warp; j < kTpb; j += kWarps) {   // 1 / (Q_j . s + eps)
@@ -2090,17 +2103,17 @@ __global__ void __launch_bounds__(kThreads) bwd_token_mlp_tc(BwdProblem b) {
 #pragma unroll
             for (int t = 0; t < TM; ++t) zt[t] = 0.f;
             for (int m = l8; m < hid; m += 8) {
-                const float h = gelu_exact(pre[uq * 68 + m]);
+                const float h = gelu_as7126(pre[uq * 68 + m]);
 #pragma unroll
                 for (int t = 0; t < TM; ++t)
-                    if (t < T) zt[t] = fmaf(p.W2[(size_t)t * hid + m], h, zt[t]);
+                    if (t < T) zt[t] = fmaf(W2s[t * hid + m], h, zt[t]);
                 if (uq < cnt) b.hbuf[((size_t)sl * p.n + j0 + uq) * hid + m] = h;
             }
             float zmax = -INFINITY, zs = 0.f;
 #pragma unroll
             for (int t = 0; t < TM; ++t)
                 if (t < T) {
-                    zt[t] = group8_sum(zt[t]) + p.b2[t];
+                    zt[t] = group8_sum(zt[t]) + b2s[t];
                     zmax = fmaxf(zmax, zt[t]);
                 }
 #pragma unroll
@@ -2267,8 +2280,8 @@ __global__ void __launch_bounds__(kThreads) bwd_token_mlp_tc(BwdProblem b) {
                     float dh = 0.f;
 #pragma unroll
                     for (int t = 0; t < TM; ++t)
-                        if (t < T) dh = fmaf(p.W2[(size_t)t * hid + m], dz[t], dh);
-                    da = dh * gelu_exact_grad(pre[uq * 68 + m]);
+                        if (t < T) dh = fmaf(W2s[t * hid + m], dz[t], dh);
+                    da = dh * gelu_grad_as7126(pre[uq * 68 + m]);
                     b.dabuf[ti * hid + m] = da;
                 }
                 const __nv_bfloat16 hi = __float2bfloat16_rn(da);

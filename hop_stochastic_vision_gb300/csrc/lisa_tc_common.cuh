@@ -280,6 +280,19 @@ __device__ __forceinline__ float gelu_as7126(float x) {
     return 0.5f * x * (1.f + copysignf(erf_abs, x));
 }
 
+// GELU'(x) = Phi(x) + x phi(x): Phi(x) = (1 + erf(x / sqrt 2)) / 2 from the same
+// formula 7.1.26, whose exp(-z^2) = exp(-x^2 / 2) also gives the normal density
+// phi(x) = exp(-x^2 / 2) / sqrt(2 pi).  Used by the adaptive-weight backward.
+__device__ __forceinline__ float gelu_grad_as7126(float x) {
+    const float z = fabsf(x) * 0.70710678118654752f;
+    const float t = __fdividef(1.f, fmaf(0.3275911f, z, 1.f));
+    const float poly =
+        t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, 1.061405429f, -1.453152027f), 1.421413741f), -0.284496736f), 0.254829592f);
+    const float e = ex2_approx(-z * z * 1.4426950408889634f);
+    const float erf_abs = fmaf(-poly, e, 1.f);
+    return fmaf(x * 0.39894228040143268f, e, 0.5f * (1.f + copysignf(erf_abs, x)));
+}
+
 // 16 TMEM lanes x 8 consecutive fp32 columns per repetition, in mma.sync
 // C-fragment layout: regs 4r+0,1 = (row g, cols 8r+2q, +1), 4r+2,3 = (row g+8, same).
 __device__ __forceinline__ void tmem_ld_frag8_nowait(uint32_t taddr, uint32_t (&r)[32]) {
