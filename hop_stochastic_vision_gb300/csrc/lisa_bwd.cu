@@ -311,7 +311,9 @@ __global__ void __launch_bounds__(kThreads) bwd_recur_rows(BwdProblem b) {
         ub[0] = fmaf(p.w[k], u.x, ub[0]); ub[1] = fmaf(p.w[k], u.y, ub[1]);
         ub[2] = fmaf(p.w[k], u.z, ub[2]); ub[3] = fmaf(p.w[k], u.w, ub[3]);
     }
-    // Ubar (row-major and transposed) and its bf16 hi + lo image
+    // Ubar (row-major and transposed) and its bf16 hi + lo image; the adaptive
+    // weights' passes on this path read none of them (their walk terms are per token)
+    if (b.mlp) return;
     *reinterpret_cast<float4 *>(b.UbarT + so + e * D + a0) = make_float4(ub[0], ub[1], ub[2], ub[3]);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -1953,14 +1955,16 @@ __global__ void __launch_bounds__(kThreads) bwd_mlp_images(BwdProblem b) {
         uint16_t *img = b.ukimg + (size_t)blockIdx.x * 2 * 64 * kQS;
         uint16_t *imgT = b.ukimgT + (size_t)blockIdx.x * 64 * kQS;
         const float al = p.alpha[(blockIdx.x / b.nh) % p.heads];
+        __shared__ float tile[D][D + 1];   // tile[e][a] = U_k[a][e]; both images written row by row
+        for (int x = tid; x < D * D; x += kThreads) tile[x >> 6][x & 63] = Ut[x];
+        __syncthreads();
         for (int x = tid; x < D * D; x += kThreads) {
-            const int e = x >> 6, a = x & 63;
-            const float uv = Ut[x];
+            const int r = x >> 6, c = x & 63;
+            imgT[r * kQS + c] = __bfloat16_as_ushort(__float2bfloat16_rn(al * tile[r][c]));
+            const float uv = tile[c][r];   // U_k[r][c]
             const __nv_bfloat16 hi = __float2bfloat16_rn(uv);
-            imgT[e * kQS + a] = __bfloat16_as_ushort(__float2bfloat16_rn(al * uv));
-            img[a * kQS + e] = __bfloat16_as_ushort(hi);
-            const float lo = uv - __bfloat162float(hi);
-            img[64 * kQS + a * kQS + e] = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+            img[r * kQS + c] = __bfloat16_as_ushort(hi);
+            img[64 * kQS + r * kQS + c] = __bfloat16_as_ushort(__float2bfloat16_rn(uv - __bfloat162float(hi)));
         }
     } else {
         for (int x = tid; x < kMH * 2 * D; x += kThreads) {
