@@ -254,9 +254,9 @@ constexpr int kRecurSplit = 4;
 
 __global__ void __launch_bounds__(kThreads) bwd_recur_rows(BwdProblem b) {
     constexpr int D = 64, R = D / kRecurSplit;
-    __shared__ __align__(16) float Mt[D][D];   // M^T: Mt[c][a] = M[a][c]
+    __shared__ __align__(16) float Mt[D][D + 4];   // M^T: Mt[c][a] = M[a][c] (padded for the column reads)
     __shared__ __align__(16) float Ut[R][D];   // this CTA's rows of U_k^T
-    __shared__ __align__(16) float Un[R][D];
+    __shared__ __align__(16) float Un[R][D + 4];   // padded: the last step reads it by columns
     const Problem &p = b.fwd;
     const Problem &t = b.tcfwd;
     const int sl = blockIdx.x / kRecurSplit, cb = blockIdx.x % kRecurSplit, e0 = R * cb, tid = threadIdx.x;
@@ -278,8 +278,8 @@ __global__ void __launch_bounds__(kThreads) bwd_recur_rows(BwdProblem b) {
     __syncthreads();
     const size_t so = (size_t)sl * D * D;
     if (cb == 0)
-        for (int idx = tid; idx < D * D; idx += kThreads)   // M row-major: strided global writes
-            b.Mred[so + (idx % D) * D + idx / D] = Mt[idx / D][idx % D];
+        for (int idx = tid; idx < D * D; idx += kThreads)   // M row-major, rows written whole
+            b.Mred[so + idx] = Mt[idx % D][idx / D];
     // thread: row i of the block, columns a0 .. a0 + 3
     const int i = tid >> 4, a0 = 4 * (tid & 15), e = e0 + i;
     float ub[4];
@@ -311,17 +311,21 @@ __global__ void __launch_bounds__(kThreads) bwd_recur_rows(BwdProblem b) {
         ub[0] = fmaf(p.w[k], u.x, ub[0]); ub[1] = fmaf(p.w[k], u.y, ub[1]);
         ub[2] = fmaf(p.w[k], u.z, ub[2]); ub[3] = fmaf(p.w[k], u.w, ub[3]);
     }
-    // Ubar (row-major and transposed) and its bf16 hi + lo image; the adaptive
-    // weights' passes on this path read none of them (their walk terms are per token)
+    // Ubar transposed and its bf16 hi + lo image (the tensor-core passes on this
+    // path read no row-major fp32 copy); the adaptive weights' passes read none
+    // of them (their walk terms are per token)
     if (b.mlp) return;
     *reinterpret_cast<float4 *>(b.UbarT + so + e * D + a0) = make_float4(ub[0], ub[1], ub[2], ub[3]);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int a = a0 + j;
-        b.Ubar[so + a * D + e] = ub[j];
-        const __nv_bfloat16 hi = __float2bfloat16_rn(ub[j]);
-        b.ubimg[so * 2 + a * D + e] = __bfloat16_as_ushort(hi);
-        b.ubimg[so * 2 + D * D + a * D + e] = __bfloat16_as_ushort(__float2bfloat16_rn(ub[j] - __bfloat162float(hi)));
+    // the image is row-major (Ubar[a][e]): through shared memory, so that each row's
+    // R entries of this CTA go out together
+    *reinterpret_cast<float4 *>(&Un[i][a0]) = make_float4(ub[0], ub[1], ub[2], ub[3]);
+    __syncthreads();
+    for (int x = tid; x < D * R; x += kThreads) {
+        const int a = x / R, ii = x % R;
+        const float v = Un[ii][a];
+        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+        b.ubimg[so * 2 + a * D + e0 + ii] = __bfloat16_as_ushort(hi);
+        b.ubimg[so * 2 + D * D + a * D + e0 + ii] = __bfloat16_as_ushort(__float2bfloat16_rn(v - __bfloat162float(hi)));
     }
 }
 
