@@ -2358,16 +2358,18 @@ __global__ void __launch_bounds__(kThreads) bwd_token_mlp_tc(BwdProblem b) {
 // dU_k = sum_j Q_j (c_jk dO_j)^T with c_jk = alpha w_jk / (Q_j . s + eps), the
 // same sum as bwd_stats_duk with the token's scalars moved onto dO.  Q^T is
 // exact in bf16 (A operand, ldmatrix.trans from the token-major tile), c_jk dO_j
-// goes in as bf16 hi + lo; one quarter-warp stages each token.
+// goes in as bf16 hi + lo; one quarter-warp stages each token; a block takes
+// kDukPerBlock walk lengths.
 // ---------------------------------------------------------------------------
+constexpr int kDukPerBlock = 2;   // walk lengths per block: Q and dO are staged once for both
 __global__ void __launch_bounds__(kThreads) bwd_stats_duk_tc(BwdProblem b) {
-    constexpr int D = 64;
+    constexpr int D = 64, KP = kDukPerBlock;
     static_assert(kTpb * 8 == kThreads, "one quarter-warp per staged token");
     using namespace sm100;
     __shared__ __align__(16) __nv_bfloat16 Qs[kTpb][kQS];
-    __shared__ __align__(16) __nv_bfloat16 Gs[2][kTpb][kQS];   // c dO hi, lo
+    __shared__ __align__(16) __nv_bfloat16 Gs[KP][2][kTpb][kQS];   // per walk length: c dO hi, lo
     const Problem &p = b.fwd;
-    const int c = blockIdx.x % p.chunks, sl = blockIdx.x / p.chunks, k = 1 + blockIdx.y, tid = threadIdx.x;
+    const int c = blockIdx.x % p.chunks, sl = blockIdx.x / p.chunks, k0 = 1 + KP * blockIdx.y, tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
     const int t0 = c * p.chunk, t1 = min(p.n, t0 + p.chunk);
     const __nv_bfloat16 *Q = static_cast<const __nv_bfloat16 *>(p.Q) + (size_t)sl * p.n * D;
@@ -2382,9 +2384,11 @@ __global__ void __launch_bounds__(kThreads) bwd_stats_duk_tc(BwdProblem b) {
     const int mt = warp & 3, ng = warp >> 2;
     const int arow = (lane & 7) + 8 * (lane >> 4), acol = 16 * mt + 8 * ((lane >> 3) & 1);
     const int mi = lane >> 3, brow = (mi & 1) * 8 + (lane & 7);
-    float acc[4][4];
+    float acc[KP][4][4];
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    for (int kp = 0; kp < KP; ++kp)
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) acc[kp][nt][0] = acc[kp][nt][1] = acc[kp][nt][2] = acc[kp][nt][3] = 0.f;
     for (int base = t0; base < t1; base += kTpb) {
         const bool in = j8 < t1 - base;
         float q[8], g[8];
@@ -2396,44 +2400,58 @@ __global__ void __launch_bounds__(kThreads) bwd_stats_duk_tc(BwdProblem b) {
             for (int u = 0; u < 8; ++u) q[u] = g[u] = 0.f;
         }
         const float den = group8_sum(dot8(q, sv)) + p.eps;   // every lane: the shuffles need all 32
-        const float cj = in ? al * wt[(size_t)(base + j8) * p.T + k] / den : 0.f;
-        uint32_t qw[4], hw[4], lw[4];
+        uint32_t qw[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            qw[u] = pack_bf16(q[2 * u], q[2 * u + 1]);
-            const float x0 = cj * g[2 * u], x1 = cj * g[2 * u + 1];
-            const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
-            hw[u] = pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
-            lw[u] = pack_bf16(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
-        }
+        for (int u = 0; u < 4; ++u) qw[u] = pack_bf16(q[2 * u], q[2 * u + 1]);
         *reinterpret_cast<uint4 *>(&Qs[j8][8 * c8]) = make_uint4(qw[0], qw[1], qw[2], qw[3]);
-        *reinterpret_cast<uint4 *>(&Gs[0][j8][8 * c8]) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-        *reinterpret_cast<uint4 *>(&Gs[1][j8][8 * c8]) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+#pragma unroll
+        for (int kp = 0; kp < KP; ++kp) {
+            const int k = k0 + kp;
+            const float cj = (in && k < p.T) ? al * wt[(size_t)(base + j8) * p.T + k] / den : 0.f;
+            uint32_t hw[4], lw[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float x0 = cj * g[2 * u], x1 = cj * g[2 * u + 1];
+                const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
+                hw[u] = pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
+                lw[u] = pack_bf16(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
+            }
+            *reinterpret_cast<uint4 *>(&Gs[kp][0][j8][8 * c8]) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4 *>(&Gs[kp][1][j8][8 * c8]) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
         __syncthreads();
 #pragma unroll
         for (int ks = 0; ks < 2; ++ks) {   // tokens 16 ks .. 16 ks + 15
             uint32_t a0, a1, a2, a3;
             ldsm_x4_t(smem_u32(&Qs[16 * ks + arow][acol]), a0, a1, a2, a3);
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
+            for (int kp = 0; kp < KP; ++kp)
 #pragma unroll
-                for (int np = 0; np < 2; ++np) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(smem_u32(&Gs[h][16 * ks + brow][32 * ng + 16 * np + (mi >> 1) * 8]), b0, b1, b2, b3);
-                    mma_bf16_16816(acc[2 * np], a0, a1, a2, a3, b0, b1);
-                    mma_bf16_16816(acc[2 * np + 1], a0, a1, a2, a3, b2, b3);
-                }
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int np = 0; np < 2; ++np) {
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4_t(smem_u32(&Gs[kp][h][16 * ks + brow][32 * ng + 16 * np + (mi >> 1) * 8]), b0, b1,
+                                  b2, b3);
+                        mma_bf16_16816(acc[kp][2 * np], a0, a1, a2, a3, b0, b1);
+                        mma_bf16_16816(acc[kp][2 * np + 1], a0, a1, a2, a3, b2, b3);
+                    }
         }
         __syncthreads();
     }
-    float *out = b.dukp + (((size_t)sl * p.chunks + c) * b.nh + (k - 1)) * D * D;
     const int g4 = lane >> 2, q4 = lane & 3;
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
+    for (int kp = 0; kp < KP; ++kp) {
+        const int k = k0 + kp;
+        if (k >= p.T) break;
+        float *out = b.dukp + (((size_t)sl * p.chunks + c) * b.nh + (k - 1)) * D * D;
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-            *reinterpret_cast<float2 *>(out + (size_t)(16 * mt + g4 + 8 * h) * D + 32 * ng + 8 * nt + 2 * q4) =
-                make_float2(acc[nt][2 * h], acc[nt][2 * h + 1]);
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+                *reinterpret_cast<float2 *>(out + (size_t)(16 * mt + g4 + 8 * h) * D + 32 * ng + 8 * nt + 2 * q4) =
+                    make_float2(acc[kp][nt][2 * h], acc[kp][nt][2 * h + 1]);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -2786,7 +2804,8 @@ cudaError_t launch_bwd_all(const BwdProblem &b, cudaStream_t st) {
         }
         if (p.T > 1) {
             if (std::is_same<TIn, __nv_bfloat16>::value && D == 64 && p.relu != 2)
-                bwd_stats_duk_tc<<<dim3(grid_stats, (unsigned)(p.T - 1)), kThreads, 0, st>>>(b);
+                bwd_stats_duk_tc<<<dim3(grid_stats, (unsigned)((p.T - 1 + kDukPerBlock - 1) / kDukPerBlock)),
+                                   kThreads, 0, st>>>(b);
             else
                 bwd_stats_duk<TIn, D><<<dim3(grid_stats, (unsigned)(p.T - 1)), kThreads, 0, st>>>(b);
         }
