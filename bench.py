@@ -625,9 +625,12 @@ def backward_arm(args, shape):
     clocks = sampler.stop()
     ms = start.elapsed_time(end)
     value = units * args.steps / (ms / 1e3)
-    # kernels per backward: 2 statistics + 8, plus the bf16 operand image at d = 64;
-    # adaptive weights: the MLP pass replaces two, one dU_k pass if T > 1, two for the parameters
-    nk = 10 + (1 if (shape.dtype == "bf16" and D == 64) else 0) + ((1 if T > 1 else 0) + 1 if mlp else 0)
+    # kernels per backward: 2 statistics + 7 (recurrence, dUbar, window statistics, reverse
+    # recurrence, token pass, per-slice reduction, dK finish with dalpha), plus the bf16 operand
+    # image at d = 64; adaptive weights: the MLP pass replaces two, one dU_k pass if T > 1, two
+    # for the parameters, and at bf16, d = 64 the MLP operand images
+    tc = 1 if (shape.dtype == "bf16" and D == 64) else 0
+    nk = 9 + tc + ((1 + (1 if T > 1 else 0) + tc) if mlp else 0)
     peak, peak_src = hbm_peak()
     esz = 2 if shape.dtype == "bf16" else 4
     bytes_step = 7 * D * esz * units

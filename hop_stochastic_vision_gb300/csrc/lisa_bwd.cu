@@ -37,8 +37,8 @@
 //                     shared memory, the products and the window on the tensor
 //                     cores (B operands from a bf16 image built by bwd_bimg)
 //   6. bwd_reduce     per slice: ds and the slice's dalpha
-//   7. bwd_finish_k   one thread per element: dXk = (dK + ds) [Xk > 0]
-//   8. bwd_dalpha     dalpha per head = sum over the batch
+//   7. bwd_finish_k   one thread per element: dXk = (dK + ds) [Xk > 0];
+//                     its block 0 also sums dalpha per head over the batch
 // With the adaptive (MLP) weights, steps 2-3 become bwd_token_mlp (the
 // window statistics, the MLP's forward and backward per token; bf16, d = 64:
 // bwd_token_mlp_tc after bwd_mlp_images has built the bf16 U_k and W1 operand
@@ -2697,25 +2697,27 @@ __global__ void __launch_bounds__(kThreads) bwd_mlp_reduce(BwdProblem b, int D) 
 template <int D>
 __global__ void __launch_bounds__(kThreads) bwd_reduce(BwdProblem b) {
     const int sl = blockIdx.x, tid = threadIdx.x;
-    if (tid < D) {
-        float acc = 0.f;
+    if (tid < D) {   // eight partials in flight per thread, in a fixed order
         const int nds = b.ntile ? b.ntile : b.nblk;   // blocks of the token pass
-        for (int k = 0; k < nds; ++k) acc += b.ds_part[((size_t)sl * nds + k) * D + tid];
-        b.ds_red[(size_t)sl * D + tid] = acc;
+        b.ds_red[(size_t)sl * D + tid] = sum_partials(b.ds_part + (size_t)sl * nds * D, nds, D, tid);
     }
-    if (tid == kThreads - 1) {
-        float acc = 0.f;
-        for (int k = 0; k < b.nblk; ++k) acc += b.dal_part[(size_t)sl * b.nblk + k];
-        b.dal_slice[sl] = acc;
-    }
+    if (tid == kThreads - 1) b.dal_slice[sl] = sum_partials(b.dal_part + (size_t)sl * b.nblk, b.nblk, 1, 0);
 }
 
 // ---------------------------------------------------------------------------
-// 7. dXk = (dK + ds) [Xk > 0], one thread per element.
+// 7. dXk = (dK + ds) [Xk > 0], one thread per element; block 0 also writes
+// dalpha per head, the sum over the batch in batch order (8.).
 // ---------------------------------------------------------------------------
 template <typename TIn, int D>
 __global__ void __launch_bounds__(kThreads) bwd_finish_k(BwdProblem b) {
     const Problem &p = b.fwd;
+    if (blockIdx.x == 0)
+        for (int h = threadIdx.x; h < p.heads; h += kThreads) {
+            const int B = p.slices / p.heads;
+            float acc = 0.f;
+            for (int bb = 0; bb < B; ++bb) acc += b.dal_slice[(size_t)bb * p.heads + h];
+            b.dalpha[h] = acc;
+        }
     const long long total = (long long)p.slices * p.n * D;
     const TIn *K = static_cast<const TIn *>(p.K);
     TIn *dKo = static_cast<TIn *>(b.dK);
@@ -2745,19 +2747,6 @@ __global__ void __launch_bounds__(kThreads) bwd_finish_k(BwdProblem b) {
         const long long sl = x / ((long long)p.n * D);
         const float v = b.dk_part[x] + b.ds_red[sl * D + ch];
         st(dKo + x, feature_grad(v, ld(K + x), p.relu));
-    }
-}
-
-// ---------------------------------------------------------------------------
-// 8. dalpha per head: the sum over the batch, in batch order.
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) bwd_dalpha(BwdProblem b) {
-    const Problem &p = b.fwd;
-    const int B = p.slices / p.heads;
-    for (int h = blockIdx.x * kThreads + threadIdx.x; h < p.heads; h += gridDim.x * kThreads) {
-        float acc = 0.f;
-        for (int bb = 0; bb < B; ++bb) acc += b.dal_slice[(size_t)bb * p.heads + h];
-        b.dalpha[h] = acc;
     }
 }
 
@@ -2861,7 +2850,6 @@ cudaError_t launch_bwd_all(const BwdProblem &b, cudaStream_t st) {
     long long blocks = (total + kThreads - 1) / kThreads;
     if (blocks > 152 * 16) blocks = 152 * 16;
     bwd_finish_k<TIn, D><<<(unsigned)blocks, kThreads, 0, st>>>(b);
-    bwd_dalpha<<<(p.heads + kThreads - 1) / kThreads, kThreads, 0, st>>>(b);
     if (b.mlp) {
         if (std::is_same<TIn, __nv_bfloat16>::value && D == 64 && p.relu != 2)
             bwd_mlp_params_tc<<<grid_stats, kThreads, 0, st>>>(b);
