@@ -896,6 +896,68 @@ __global__ void __launch_bounds__(kThreads) bwd_recur_back_64(BwdProblem b) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// 4'' (d = 64, truncated walk, T <= 3, fixed weights, dUbar from the
+// tensor-core partials): the reverse recurrence split over kRecurSplit CTAs
+// per slice.  With T <= 3 there is at most one step: G_2 = w_2 dUbar,
+// dM = G_2 U_1^T and dU_1 = G_1 = w_1 dUbar + M^T G_2, so rows e0 .. e0 + 15
+// of dM and dU_1 need only the whole dUbar, M and U_1.  Each CTA reduces the
+// whole dUbar (in the same order as bwd_recur_back_64, so the bits agree) and
+// computes its own rows.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) bwd_recur_back_rows(BwdProblem b) {
+    constexpr int D = 64, R = D / kRecurSplit;
+    __shared__ __align__(16) float M[D * D];   // M row-major: M[e * D + a] = M[e][a]
+    __shared__ __align__(16) float G[D * D];   // dUbar, row-major
+    __shared__ __align__(16) float X[D * D];   // U_1 transposed: X[e * D + c] = U_1[c][e]
+    const Problem &p = b.fwd;
+    const int sl = blockIdx.x / kRecurSplit, e0 = R * (blockIdx.x % kRecurSplit), tid = threadIdx.x;
+    const size_t so = (size_t)sl * D * D;
+    const int parts = b.tcfwd.chunks / b.tcfwd.tc_cluster;
+    const float al = p.alpha[sl % p.heads];
+    for (int x = tid; x < D * D / 4; x += kThreads) {   // alpha (Q~^T dO): rows 64 + a of the partials
+        const int a = x / 16, c4 = (x % 16) * 4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q = 0; q < parts; ++q) {
+            const float4 v =
+                *reinterpret_cast<const float4 *>(b.tcdub + ((size_t)sl * parts + q) * 2 * D * D + (D + a) * D + c4);
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+        acc.x *= al; acc.y *= al; acc.z *= al; acc.w *= al;
+        *reinterpret_cast<float4 *>(G + a * D + c4) = acc;
+        reinterpret_cast<float4 *>(M)[x] = reinterpret_cast<const float4 *>(b.Mred + so)[x];
+        if (p.T > 2)   // U_1 (k = 1 of the transposed copies)
+            reinterpret_cast<float4 *>(X)[x] = reinterpret_cast<const float4 *>(b.Uk + (size_t)sl * b.nh * D * D)[x];
+    }
+    __syncthreads();
+    // thread: row a = e0 + tid / 16, columns c0 .. c0 + 3
+    const int a = e0 + (tid >> 4), c0 = 4 * (tid & 15);
+    const float w1 = p.T > 1 ? p.w[1] : 0.f, w2 = p.T > 2 ? p.w[2] : 0.f;
+    float g[4], dm[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) g[j] = w1 * G[a * D + c0 + j];
+    if (p.T > 2) {
+#pragma unroll 4
+        for (int e = 0; e < D; ++e) {
+            const float ga = w2 * G[a * D + e];   // G_2[a][e]
+            const float me = M[e * D + a];        // M[e][a]
+            const float4 xv = *reinterpret_cast<const float4 *>(X + e * D + c0);
+            const float4 gv = *reinterpret_cast<const float4 *>(G + e * D + c0);
+            dm[0] = fmaf(ga, xv.x, dm[0]); dm[1] = fmaf(ga, xv.y, dm[1]);
+            dm[2] = fmaf(ga, xv.z, dm[2]); dm[3] = fmaf(ga, xv.w, dm[3]);
+            g[0] = fmaf(me, w2 * gv.x, g[0]); g[1] = fmaf(me, w2 * gv.y, g[1]);
+            g[2] = fmaf(me, w2 * gv.z, g[2]); g[3] = fmaf(me, w2 * gv.w, g[3]);
+        }
+    }
+    st_row4(b.dM + so + a * D + c0, dm);
+    st_row4(b.dU1 + so + a * D + c0, g);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        b.dMT[so + (c0 + j) * D + a] = dm[j];
+        b.dU1T[so + (c0 + j) * D + a] = g[j];
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads) bwd_recur_back(BwdProblem b) {
     constexpr int EPT = D * D / kThreads;
@@ -2814,7 +2876,9 @@ cudaError_t launch_bwd_all(const BwdProblem &b, cudaStream_t st) {
         else
             bwd_token_a<TIn, D><<<grid_tok, kThreads, 0, st>>>(b);
     }
-    if (D == 64 && !p.untruncated)
+    if (D == 64 && !p.untruncated && b.tc_dub && p.T <= 3)
+        bwd_recur_back_rows<<<(unsigned)p.slices * kRecurSplit, kThreads, 0, st>>>(b);
+    else if (D == 64 && !p.untruncated)
         bwd_recur_back_64<<<p.slices, kThreads, 0, st>>>(b);
     else
         bwd_recur_back<D><<<p.slices, kThreads, 0, st>>>(b);
