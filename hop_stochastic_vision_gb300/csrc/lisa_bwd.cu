@@ -1366,18 +1366,17 @@ __device__ __forceinline__ uint32_t relu_bf16x2(uint32_t v) {
 // ---------------------------------------------------------------------------
 constexpr int kQS = 72;   // row stride (bf16) of the staged Q rows and Ubar image: ldmatrix conflict-free
 
-// Eight bf16 channels at `row` (16-byte aligned) as floats, optionally ReLU'd.
+// Eight bf16 channels at `row` (16-byte aligned) as floats, optionally ReLU'd
+// (on the packed pairs: max(x, 0) is exact in bf16).
 __device__ __forceinline__ void load8_bf16(const __nv_bfloat16 *row, float (&x)[8], bool relu) {
-    const uint4 w = *reinterpret_cast<const uint4 *>(row);
+    uint4 w = *reinterpret_cast<const uint4 *>(row);
+    if (relu) w = make_uint4(relu_bf16x2(w.x), relu_bf16x2(w.y), relu_bf16x2(w.z), relu_bf16x2(w.w));
     const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         x[2 * k] = sm100::bf16_lo(u[k]);
         x[2 * k + 1] = sm100::bf16_hi(u[k]);
     }
-    if (relu)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) x[k] = fmaxf(x[k], 0.f);
 }
 // Sum over the eight lanes of a quarter-warp (lanes 8 q .. 8 q + 7).
 __device__ __forceinline__ float group8_sum(float v) {
@@ -1505,7 +1504,7 @@ __global__ void __launch_bounds__(kThreads, 4) bwd_token_a_tc(BwdProblem b) {
     for (int t9 = 0; t9 < 9; ++t9) {
         const int rr = r + t9 / 3 - 1, cc = c + t9 % 3 - 1;
         const bool in = rr >= 0 && rr < p.H && cc >= 0 && cc < p.W;
-        const float a = in ? expf(e[t9] - emax) : 0.f;
+        const float a = in ? ex2_approx((e[t9] - emax) * 1.4426950408889634f) : 0.f;   // as the tiled pass
         esum += a;
         float vr[8];
         load8_bf16(V + (size_t)(in ? rr * p.W + cc : i) * D + c8, vr, false);
@@ -2302,7 +2301,7 @@ __global__ void __launch_bounds__(kThreads) bwd_token_mlp_tc(BwdProblem b) {
             for (int t9 = 0; t9 < 9; ++t9) {
                 const int rr = r + t9 / 3 - 1, cc = c + t9 % 3 - 1;
                 const bool in = rr >= 0 && rr < p.H && cc >= 0 && cc < p.W;
-                const float a = in ? expf(ev[t9] - emax) : 0.f;
+                const float a = in ? ex2_approx((ev[t9] - emax) * 1.4426950408889634f) : 0.f;
                 esum += a;
                 float vr[8];
                 load8_bf16(V + (size_t)(in ? rr * p.W + cc : i) * D + c8, vr, false);
