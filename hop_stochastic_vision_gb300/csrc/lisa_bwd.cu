@@ -29,7 +29,8 @@
 //   2. bwd_stats_dub  per (slice, chunk): partial dUbar = Q~^T (alpha dO)
 //   3. bwd_token_a    warp per token: window softmax max / sum, dl_i . l_i,
 //                     dalpha terms (per-block partial sums)
-//   4. bwd_recur_back per slice: reduce dUbar; G_k; dM, dU_1 (or the solve)
+//   4. bwd_recur_back per slice: reduce dUbar; G_k; dM, dU_1 (or the solve);
+//                     bf16, d = 64, T <= 3: bwd_recur_back_rows, four CTAs per slice
 //   5. bwd_token_b    per block of 32 tokens: the d x d products from shared
 //                     memory, then a warp per token: dXq, dV, the ds terms
 //                     (per-block sums), dK without ds.  bf16, d = 64:
