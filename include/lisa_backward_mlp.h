@@ -11,7 +11,12 @@
  * parameters, which every head and batch element shares.
  *
  * Conventions, checks, statuses and stream behaviour are those of
- * lisa_backward in include/lisa.h.
+ * lisa_backward in include/lisa.h.  Arithmetic as there; for bf16 at d = 64
+ * with ReLU or no feature map the MLP's contractions run on the tensor cores
+ * too (W1, U_k and the hidden-layer gradients enter as bf16 hi + lo terms,
+ * fp32 accumulation), and GELU and its derivative take erf from
+ * Abramowitz & Stegun 7.1.26 (absolute error <= 1.5e-7), as the forward's
+ * adaptive-weight path does.
  */
 #ifndef LISA_BACKWARD_MLP_H_
 #define LISA_BACKWARD_MLP_H_
