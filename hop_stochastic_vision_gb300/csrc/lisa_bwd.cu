@@ -51,6 +51,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
 #include <type_traits>
 
 #include "lisa_bwd.h"
@@ -2824,13 +2825,79 @@ bool make_map_stats(CUtensorMap *m, const float *lstat, const Problem &p) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The backward's second stream, one per device: dUbar's statistics launch
+// (fixed weights, tensor-core path) runs there, forked from the caller's
+// stream after the key sum and joined back before the reverse recurrence, so
+// it overlaps the forward recurrence and the window-statistics pass (they
+// share no data).  Created on first use outside stream capture and kept for
+// the life of the process; a call made while its stream is being captured
+// before that first use runs the launch in line instead.  The mutex also
+// keeps concurrent callers' fork ... join sections (which reuse the two
+// events) apart.
+struct SideStream {
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_side_mu;
+SideStream g_side[64];
+
+SideStream *side_stream(cudaStream_t st) {   // g_side_mu held
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    SideStream &ss = g_side[dev];
+    if (ss.s) return &ss;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    cudaStream_t s2 = nullptr;
+    cudaEvent_t e1 = nullptr, e2 = nullptr;
+    if (cudaStreamCreateWithFlags(&s2, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&e1, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&e2, cudaEventDisableTiming) != cudaSuccess) {
+        if (e1) cudaEventDestroy(e1);
+        if (s2) cudaStreamDestroy(s2);
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    ss.s = s2;
+    ss.fork = e1;
+    ss.join = e2;
+    return &ss;
+}
+
 template <typename TIn, int D>
 cudaError_t launch_bwd_all(const BwdProblem &b, cudaStream_t st) {
     const Problem &p = b.fwd;
     if (b.tpb != kTpb) return cudaErrorInvalidValue;   // the plan's blocks are kTpb tokens
     cudaError_t err;
+    std::unique_lock<std::mutex> side_lock(g_side_mu, std::defer_lock);
+    SideStream *side = nullptr;
+    if (!b.mlp && b.tc_dub) {
+        side_lock.lock();
+        side = side_stream(st);
+        if (!side) side_lock.unlock();
+    }
+    // dUbar / alpha = Q~^T dO: the statistics kernel with dO as its V and K (and the
+    // key-sum partials of the first launch)
+    auto launch_dub = [&](cudaStream_t s2) {
+        Problem q = b.tcfwd;
+        q.V = b.dO;
+        q.K = b.dO;
+        q.k_raw = 1;
+        q.tc_part = b.tcdub;
+        return launch_tc_stats_partials(q, s2, false);
+    };
     if (b.tc_stats) {   // key-sum and [U_1^T ; M^T] partials on the tensor cores
         if ((err = launch_tc_stats_partials(b.tcfwd, st)) != cudaSuccess) return err;
+        if (side) {
+            if ((err = cudaEventRecord(side->fork, st)) != cudaSuccess ||
+                (err = cudaStreamWaitEvent(side->s, side->fork, 0)) != cudaSuccess ||
+                (err = launch_dub(side->s)) != cudaSuccess ||
+                (err = cudaEventRecord(side->join, side->s)) != cudaSuccess)
+                return err;
+        }
     } else {
         if ((err = launch_simt(p, st, 0)) != cudaSuccess) return err;   // partial s, K^T V
         if ((err = launch_simt(p, st, 1)) != cudaSuccess) return err;   // partial K^T Q~
@@ -2861,13 +2928,8 @@ cudaError_t launch_bwd_all(const BwdProblem &b, cudaStream_t st) {
                 bwd_stats_duk<TIn, D><<<dim3(grid_stats, (unsigned)(p.T - 1)), kThreads, 0, st>>>(b);
         }
     } else {
-        if (b.tc_dub) {   // dUbar / alpha = Q~^T dO: the statistics kernel with dO as its V and K
-            Problem q = b.tcfwd;
-            q.V = b.dO;
-            q.K = b.dO;
-            q.k_raw = 1;
-            q.tc_part = b.tcdub;
-            if ((err = launch_tc_stats_partials(q, st, false)) != cudaSuccess) return err;
+        if (b.tc_dub) {
+            if (!side && (err = launch_dub(st)) != cudaSuccess) return err;   // else on the side stream
         } else {
             bwd_stats_dub<TIn, D><<<grid_stats, kThreads, 0, st>>>(b);
         }
@@ -2875,6 +2937,10 @@ cudaError_t launch_bwd_all(const BwdProblem &b, cudaStream_t st) {
             bwd_token_a_tc<<<grid_tok, kThreads, 0, st>>>(b);
         else
             bwd_token_a<TIn, D><<<grid_tok, kThreads, 0, st>>>(b);
+    }
+    if (side) {   // join: the reverse recurrence reads dUbar's partials
+        if ((err = cudaStreamWaitEvent(st, side->join, 0)) != cudaSuccess) return err;
+        side_lock.unlock();
     }
     if (D == 64 && !p.untruncated && b.tc_dub && p.T <= 3)
         bwd_recur_back_rows<<<(unsigned)p.slices * kRecurSplit, kThreads, 0, st>>>(b);
