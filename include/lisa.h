@@ -231,8 +231,14 @@ lisa_status lisa_forward_noalloc(const void *Q, const void *K, const void *V, vo
  * on every run.  The workspace (>= the bytes
  * lisa_backward_workspace_bytes returns, 16-byte aligned) needs no
  * initialisation.  Checks, statuses and stream behaviour as for
- * lisa_forward.  An empty problem (B * heads * H * W == 0) only zeroes
- * dalpha.
+ * lisa_forward, with one addition: on the tensor-core path the call forks
+ * one statistics launch onto a library-owned stream of the current device
+ * and joins it back into `stream` before its last kernel, so all of its work
+ * stays ordered after earlier work on `stream` and before later work (and a
+ * CUDA graph captured from `stream` holds the fork and the join).  That
+ * stream is created by the first such call that is not made during stream
+ * capture; until then the launch runs on `stream` itself.  An empty problem
+ * (B * heads * H * W == 0) only zeroes dalpha.
  */
 size_t lisa_backward_workspace_bytes(int B, int heads, int H, int W, int d_h, int d_v, int T,
                                      int dtype);
