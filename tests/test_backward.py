@@ -184,6 +184,41 @@ def test_deterministic_and_empty():
     assert dq.shape == q.shape and torch.equal(da.cpu(), torch.zeros(3))
 
 
+def test_captured_in_a_cuda_graph():
+    """For bf16 at d = 64 the backward forks its dUbar launch onto a
+    library-owned stream and joins it back into the caller's.  Captured in a
+    CUDA graph (the fork and the join inside the capture) and replayed, it
+    gives the eager call's bits; replayed on new inputs copied into the
+    captured buffers, that input's eager bits."""
+    from hop_stochastic_vision_gb300 import lisa
+    shape = _shape("bf16", 64, 28, 28, 3, B=4, heads=3)
+    sets = [(to_device(make_inputs(shape, seed=s)), _upstream(shape, 4, 3, seed=s + 1).cuda()) for s in (0, 1)]
+
+    def run(inp, dO):
+        return lisa.backward(inp["xq"], inp["xk"], inp["v"], dO, (28, 28), 3, alpha=inp["alpha"], beta=0.5)
+
+    eager = [run(*x) for x in sets]   # the first eager call also creates the second stream
+    torch.cuda.synchronize()
+    inp = {k: v.clone() for k, v in sets[0][0].items()}
+    dO = sets[0][1].clone()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):   # warm-up on the capture stream
+        run(inp, dO)
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        outs = run(inp, dO)
+    for j, (x, y) in enumerate(sets):
+        for key in ("xq", "xk", "v", "alpha"):
+            inp[key].copy_(x[key])
+        dO.copy_(y)
+        graph.replay()
+        torch.cuda.synchronize()
+        for got, want in zip(outs, eager[j]):
+            assert torch.equal(got, want), j
+
+
 # -- adaptive (MLP) walk weights: lisa_backward_mlp ----------------------------------------
 
 def _check_mlp(dtype, d, H, W, T, *, B=2, heads=2, hidden=32, scale=1.0, seed=0, relu=True, alpha=None,
