@@ -1580,12 +1580,6 @@ __device__ __forceinline__ void lds8_sw(const uint8_t *region, int row, int chun
         x[2 * k + 1] = sm100::bf16_hi(u[k]);
     }
 }
-// 2^x on the special-function unit (approximate, as the forward's local softmax).
-__device__ __forceinline__ float ex2_fast(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
 
 template <bool kMlp>
 __global__ void __launch_bounds__(kTileThreads, 1)
@@ -1915,7 +1909,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                     for (int e = 0; e < 4; ++e) {
                         const int h = e >> 1;
                         const float a = ((wmask >> (j * 4 + e)) & 1u)
-                                            ? ex2_fast(fmaf(sc[j][e], scale * kLog2e, -emx[h])) * ies[h] : 0.f;
+                                            ? ex2_approx(fmaf(sc[j][e], scale * kLog2e, -emx[h])) * ies[h] : 0.f;
                         sc[j][e] = a * (dp[j][e] * (1.f - al) - dll[h]) * scale;
                     }
                 times_window(sc, Kc, acc);
@@ -1937,7 +1931,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                         for (int h = 0; h < 2; ++h) {
                             const int e = 2 * h + bb;
                             const float a = ((wmask >> (j * 4 + e)) & 1u)
-                                                ? ex2_fast(fmaf(sc[j][e], scale * kLog2e, -emx)) * ies : 0.f;
+                                                ? ex2_approx(fmaf(sc[j][e], scale * kLog2e, -emx)) * ies : 0.f;
                             sc[j][e] = role == 1 ? a * (dp[j][e] * (1.f - al) - sk.z) * scale : a * (1.f - al);
                         }
                     }
