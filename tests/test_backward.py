@@ -113,6 +113,13 @@ def test_depths(dtype, T):
     _check(_shape(dtype, 32, 11, 10, T))
 
 
+@pytest.mark.parametrize("T", [1, 2])
+def test_short_walks_tensor_path(T):
+    """bf16 at d = 64 with T = 1 (no hop term) and T = 2 (no recurrence step):
+    the split recurrences' degenerate cases."""
+    _check(_shape("bf16", 64, 11, 10, T))
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_fixed_weights_and_untruncated(dtype):
     _check(_shape(dtype, 64, 9, 12, 4), w=(0.2, -0.5, 1.3, 0.7))
