@@ -250,6 +250,15 @@ def test_backward_mlp_workspace_bytes():
     assert ws(1, 1, 4, 4, 64, 64, 0, 32, lisa.LISA_BF16) == 0        # no untruncated adaptive walk
     assert ws(1, 1, 4, 4, 64, 64, 3, 65, lisa.LISA_BF16) == 0        # hidden too wide
     assert ws(1, 1, 4, 4, 64, 64, 3, 0, lisa.LISA_BF16) == 0
+    # the adaptive weights' own buffers include the bf16 operand images of the
+    # tensor path: per slice and walk length U_k as hi + lo rows and alpha U_k^T
+    # (72-wide rows), and W1 as hi + lo rows (136 wide)
+    S, T, hidden, n = 8 * 3, 3, 32, 24 * 24
+    images = S * (T - 1) * (2 * 64 * 72 + 64 * 72) * 2 + 2 * 64 * 136 * 2
+    per_token = S * n * 4 * (2 * T + 2 * hidden + 2 * 64)   # w, dz, h, da and the MLP's share of dq, dk
+    extra = ws(8, 3, 24, 24, 64, 64, T, hidden, lisa.LISA_BF16) - lisa.lisa_backward_workspace_bytes(
+        8, 3, 24, 24, 64, 64, T, lisa.LISA_BF16)
+    assert extra >= images + per_token
 
 
 def test_backward_mlp_rejects_before_launch():
